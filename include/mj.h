@@ -1,0 +1,196 @@
+/*
+ * mj.h — C ABI of the paged fp8-KV split-KV decode attention library
+ * (libmj.so, sm_103a / GB300).
+ *
+ * The operation (source: the "mjolnir/t5_decode.py" page — module docstring
+ * on vLLM-shaped inputs and the causal tail; `plan_split_kv` for the plan;
+ * the `decode` kernel's softmax/epilogue and the `reduction` kernel for the
+ * split merge; `pack_q` / `unpack_o` for the query packing):
+ *
+ *   For each sequence b, kv head g and packed query row n (query token
+ *   qi = n / h_r of query head h = g*h_r + n % h_r), with L = seq_lens[b]
+ *   counting the q_len new tokens:
+ *     visible keys   j <= L - q_len + qi (causal) or j <= L - 1 (non-causal)
+ *     key/value j    K/V[block_table[b][j / page_size], j % page_size, g, :]
+ *     z_j            = softmax_scale * qd[b,g] * kd[b,g] * <q_n, k_j>
+ *     O[n]           = scale_o * vd[b,g] * sum_j softmax(z)_j * v_j   (bf16)
+ *     LSE[n]         = log(sum_j exp(z_j))                  (natural log)
+ *   A row with no visible key gets O = 0 and LSE = -inf.
+ *
+ * K and V are e4m3 (E4M3FN) codes; Q is bf16 or e4m3.  Scores, softmax and
+ * accumulation are fp32.  The KV range of a sequence may be cut into
+ * contiguous chunks (split-KV); split sequences are merged by a second
+ * kernel that touches only them.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are caller-owned.  The library allocates nothing and keeps
+ *     no state between calls.
+ *   - "device" pointers must be valid on the current CUDA device; "host"
+ *     pointers are ordinary CPU memory.
+ *   - Strides are in ELEMENTS of the tensor they index (K/V elements are
+ *     bytes).  The head dimension is always contiguous.
+ *   - Every function validates its arguments first and returns an error
+ *     code without launching anything when they are bad.
+ *   - Launch entry points enqueue on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronise the host, so they can be
+ *     captured in a CUDA graph.
+ */
+#ifndef MJ_H_
+#define MJ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without requiring the CUDA headers. */
+typedef struct CUstream_st* mj_stream_t;
+
+typedef enum {
+  MJ_OK = 0,
+  MJ_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad stride, bad shape */
+  MJ_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels cover */
+  MJ_ERR_CAPACITY = 3,    /* an output buffer or the workspace is too small */
+  MJ_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  MJ_ERR_TIMEOUT = 5      /* written by a kernel into the status word */
+} mj_status;
+
+typedef enum { MJ_BF16 = 0, MJ_E4M3 = 1 } mj_dtype;
+
+/* Problem shape and fixed choices.
+ *   num_seqs    b >= 1
+ *   q_len       query tokens per sequence (>= 1; > 1 for speculative verify)
+ *   h_k, h_r    kv heads, query heads per kv head (n_q = q_len * h_r rows)
+ *   head_dim    d; must be 128
+ *   page_size   rows per KV page: 16, 32, 64 or 128
+ *   max_blocks  row length of block_table
+ *   num_pages   pages in the KV pool
+ *   causal      1: causal tail; 0: every query token sees all L keys
+ *   q_dtype     mj_dtype of Q (K/V are always e4m3)
+ *   max_splits  partial slots per sequence, 1..256 (1 = never split) */
+typedef struct {
+  int32_t num_seqs, q_len, h_k, h_r, head_dim, page_size;
+  int32_t max_blocks, num_pages, causal, q_dtype, max_splits;
+} mj_decode_params;
+
+/* Plan knobs (source: `plan_split_kv`).  A field left 0 takes the
+ * library's value for the kernel mj_decode_attn will launch for these
+ * params, and is filled in on return, so a caller can reproduce the plan:
+ *   sm_count         SMs of the target GPU (0 -> 152, a GB300)
+ *   ctas_per_sm      co-resident decode CTAs per SM of the chosen kernel
+ *   n_q_tiles        CTAs per (work item, kv head) along the packed rows
+ *   force_splits     > 0: cut every sequence into this many chunks
+ *   min_chunk_tiles  lower bound of the chunk size in 128-row tiles (0 -> 1)
+ *   pad_to           > 0: pad the work list with empty items to this length */
+typedef struct {
+  int32_t sm_count, ctas_per_sm, n_q_tiles, force_splits, min_chunk_tiles, pad_to;
+} mj_plan_opts;
+
+/* Occupancy-pinned split-KV plan (host only; no CUDA call; deterministic).
+ *
+ * Every sequence has T_b = max(1, ceil(L_b / 128)) tiles of 128 KV rows.
+ * One wave holds slots = max(1, sm_count*ctas_per_sm / (h_k*n_q_tiles))
+ * work items.  The chunk size is the smallest number of tiles, at least
+ * max(min_chunk_tiles, ceil(T_max / max_splits)), whose chunk count over
+ * all sequences fits one wave (force_splits > 0 takes
+ * max(that floor, ceil(T_max / force_splits)); a batch that already fills
+ * the wave, or max_splits == 1, is not split).  Items are ordered longest
+ * first, ties in (b, slot) order.
+ *
+ *   seq_lens_host  host int32[num_seqs]; 0 <= L_b <= max_blocks*page_size
+ *   work_out       host int32[work_cap][4]: (seq, tile_begin, tile_end,
+ *                  split_slot); padding items are (0, 0, 0, 0)
+ *   num_work       host out: items written
+ *   n_splits_out   host int32[num_seqs]: chunks per sequence
+ *   chunk_tiles    host out (may be NULL)
+ * Errors: MJ_ERR_INVALID_ARG (nulls, bad params, a length out of range,
+ * pad_to below the item count), MJ_ERR_CAPACITY (work_cap too small). */
+mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts* opts,
+                         const int32_t* seq_lens_host, int32_t* work_out, int32_t work_cap,
+                         int32_t* num_work, int32_t* n_splits_out, int32_t* chunk_tiles);
+
+/* Bytes of workspace mj_decode_attn needs: fp32 partial O, max and sum for
+ * max_splits slots of every (seq, kv head, row); 0 when max_splits == 1.
+ * Layout (private): o[b][g][slot][n][d], then m and l [b][g][slot][n]. */
+size_t mj_decode_workspace_bytes(const mj_decode_params* params);
+
+/* Device-side arguments of mj_decode_attn.
+ *   q            device, packed (b, h_k, n_q, d) rows of q_dtype; row n of
+ *                kv head g of sequence b at q + b*q_seq_stride + (g*n_q+n)*d
+ *                (for q_len == 1 vLLM's (b, h_q, d) is already packed)
+ *   k, v         device e4m3 pools; element (page, r, g, i) at
+ *                page*x_page + r*x_row + g*x_head + i; every stride a
+ *                multiple of 16 bytes (K and V may share one buffer)
+ *   block_table  device int32 (b, max_blocks); entries past ceil(L/PS) are
+ *                never read; entries before must be in [0, num_pages)
+ *   seq_lens     device int32[b], the same values the plan saw
+ *   work, n_splits, num_work   device copies of the plan's outputs
+ *   *_descale    device fp32, (b, g) at b*x_seq + g*x_head (strides 0 =
+ *                per tensor); finite and > 0
+ *   o            device bf16, packed like q with o_seq_stride
+ *   lse          device fp32 (b, h_k, n_q), contiguous
+ *   workspace    device, >= mj_decode_workspace_bytes; need not be
+ *                initialised; may be NULL when max_splits == 1
+ *   status       optional device int32, caller-zeroed; kernels that give up
+ *                a bounded wait write MJ_ERR_TIMEOUT there; NULL = off
+ *   timing_events optional: NULL, or 3 cudaEvent_t recorded on `stream`
+ *                before the decode kernel, between decode and merge, and
+ *                after the merge (instrumentation only) */
+typedef struct {
+  const void* q;
+  int64_t q_seq_stride;
+  const uint8_t* k;
+  const uint8_t* v;
+  int64_t k_page, k_row, k_head, v_page, v_row, v_head;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* work;
+  const int32_t* n_splits;
+  int32_t num_work;
+  const float* q_descale;
+  const float* k_descale;
+  const float* v_descale;
+  int64_t qd_seq, qd_head, kd_seq, kd_head, vd_seq, vd_head;
+  float softmax_scale, scale_o;
+  void* o;
+  int64_t o_seq_stride;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* status;
+  void* const* timing_events;
+} mj_decode_args;
+
+/* Decode attention for one step: the decode kernel over every work item,
+ * then, if any sequence was split (max_splits > 1), the merge kernel over
+ * the split sequences.  Writes O and LSE of every (b, g, n).  Deterministic:
+ * repeated calls give identical bytes.
+ * Errors: MJ_ERR_INVALID_ARG, MJ_ERR_UNSUPPORTED (head_dim != 128, bad
+ * page size, q_dtype), MJ_ERR_CAPACITY (workspace), MJ_ERR_CUDA. */
+mj_status mj_decode_attn(const mj_decode_params* params, const mj_decode_args* args,
+                         mj_stream_t stream);
+
+/* vLLM query layout (num_seqs*q_len, h_k*h_r, d) -> packed (num_seqs, h_k,
+ * q_len*h_r, d), row n = qi*h_r + hr (source: `pack_q`).  Both device,
+ * contiguous, must not overlap; elem_bytes is 2 (bf16) or 1 (e4m3). */
+mj_status mj_pack_q(const void* q_vllm, void* q_packed, int32_t elem_bytes, int32_t num_seqs,
+                    int32_t q_len, int32_t h_k, int32_t h_r, int32_t head_dim, mj_stream_t stream);
+
+/* Inverse permutation for the bf16 output (source: `unpack_o`). */
+mj_status mj_unpack_o(const void* o_packed, void* o_vllm, int32_t num_seqs, int32_t q_len,
+                      int32_t h_k, int32_t h_r, int32_t head_dim, mj_stream_t stream);
+
+/* Static text for a status code. */
+const char* mj_status_string(mj_status status);
+
+/* Which kernel mj_decode_attn runs for these params: writes a short name
+ * (e.g. "cc_n4_bf16") into buf (NUL-terminated, truncated to len). */
+mj_status mj_kernel_name(const mj_decode_params* params, char* buf, int32_t len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MJ_H_ */

@@ -1,0 +1,339 @@
+"""Paged fp8-KV split-KV decode attention for GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI of ``libmj.so`` (declared in
+``include/mj.h``): argument marshalling only.  Every step of the decode path
+runs in the library's CUDA kernels; there is no Python or CPU fallback, and
+loading fails loudly when the library has not been built
+(``python -m paged_fp8_kv_gb300.build``).
+
+PyTorch is used only for device memory, streams and events.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmj.so")
+
+MJ_OK = 0
+MJ_ERR_INVALID_ARG = 1
+MJ_ERR_UNSUPPORTED = 2
+MJ_ERR_CAPACITY = 3
+MJ_ERR_CUDA = 4
+MJ_ERR_TIMEOUT = 5
+
+MJ_BF16 = 0
+MJ_E4M3 = 1
+
+
+class MjError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class DecodeParams(ctypes.Structure):
+    _fields_ = [
+        (name, ctypes.c_int32)
+        for name in (
+            "num_seqs",
+            "q_len",
+            "h_k",
+            "h_r",
+            "head_dim",
+            "page_size",
+            "max_blocks",
+            "num_pages",
+            "causal",
+            "q_dtype",
+            "max_splits",
+        )
+    ]
+
+
+class PlanOpts(ctypes.Structure):
+    _fields_ = [
+        (name, ctypes.c_int32)
+        for name in ("sm_count", "ctas_per_sm", "n_q_tiles", "force_splits", "min_chunk_tiles", "pad_to")
+    ]
+
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", _vp),
+        ("q_seq_stride", _i64),
+        ("k", _vp),
+        ("v", _vp),
+        ("k_page", _i64),
+        ("k_row", _i64),
+        ("k_head", _i64),
+        ("v_page", _i64),
+        ("v_row", _i64),
+        ("v_head", _i64),
+        ("block_table", _vp),
+        ("seq_lens", _vp),
+        ("work", _vp),
+        ("n_splits", _vp),
+        ("num_work", ctypes.c_int32),
+        ("q_descale", _vp),
+        ("k_descale", _vp),
+        ("v_descale", _vp),
+        ("qd_seq", _i64),
+        ("qd_head", _i64),
+        ("kd_seq", _i64),
+        ("kd_head", _i64),
+        ("vd_seq", _i64),
+        ("vd_head", _i64),
+        ("softmax_scale", ctypes.c_float),
+        ("scale_o", ctypes.c_float),
+        ("o", _vp),
+        ("o_seq_stride", _i64),
+        ("lse", _vp),
+        ("workspace", _vp),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("status", _vp),
+        ("timing_events", _vp),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmj.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m paged_fp8_kv_gb300.build` "
+                "(there is no fallback implementation)"
+            )
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER
+        L.mj_decode_plan.restype = ctypes.c_int
+        L.mj_decode_plan.argtypes = [P(DecodeParams), P(PlanOpts), _vp, _vp, ctypes.c_int32, _vp, _vp, _vp]
+        L.mj_decode_workspace_bytes.restype = ctypes.c_size_t
+        L.mj_decode_workspace_bytes.argtypes = [P(DecodeParams)]
+        L.mj_decode_attn.restype = ctypes.c_int
+        L.mj_decode_attn.argtypes = [P(DecodeParams), P(DecodeArgs), _vp]
+        L.mj_pack_q.restype = ctypes.c_int
+        L.mj_pack_q.argtypes = [_vp, _vp] + [ctypes.c_int32] * 6 + [_vp]
+        L.mj_unpack_o.restype = ctypes.c_int
+        L.mj_unpack_o.argtypes = [_vp, _vp] + [ctypes.c_int32] * 5 + [_vp]
+        L.mj_status_string.restype = ctypes.c_char_p
+        L.mj_status_string.argtypes = [ctypes.c_int]
+        L.mj_kernel_name.restype = ctypes.c_int
+        L.mj_kernel_name.argtypes = [P(DecodeParams), ctypes.c_char_p, ctypes.c_int32]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mj_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != MJ_OK:
+        raise MjError(status, what)
+
+
+def make_params(
+    num_seqs: int,
+    q_len: int,
+    h_k: int,
+    h_r: int,
+    page_size: int,
+    max_blocks: int,
+    num_pages: int,
+    causal: bool = True,
+    q_dtype: int = MJ_BF16,
+    max_splits: int = 16,
+    head_dim: int = 128,
+) -> DecodeParams:
+    return DecodeParams(
+        num_seqs, q_len, h_k, h_r, head_dim, page_size, max_blocks, num_pages, int(causal), q_dtype, max_splits
+    )
+
+
+@dataclass
+class Plan:
+    work: np.ndarray  # int32 (num_work, 4)
+    n_splits: np.ndarray  # int32 (num_seqs,)
+    chunk_tiles: int
+    opts: PlanOpts
+
+    @property
+    def num_work(self) -> int:
+        return int(self.work.shape[0])
+
+    @property
+    def max_n_splits(self) -> int:
+        return int(self.n_splits.max())
+
+
+def decode_plan(
+    params: DecodeParams,
+    seq_lens: Sequence[int],
+    sm_count: int = 0,
+    ctas_per_sm: int = 0,
+    n_q_tiles: int = 0,
+    force_splits: int = 0,
+    min_chunk_tiles: int = 0,
+    pad_to: int = 0,
+) -> Plan:
+    """mj_decode_plan on host seq_lens."""
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    opts = PlanOpts(sm_count, ctas_per_sm, n_q_tiles, force_splits, min_chunk_tiles, pad_to)
+    cap = max(pad_to, int(params.num_seqs) * int(params.max_splits), 1)
+    work = np.zeros((cap, 4), dtype=np.int32)
+    n_splits = np.zeros(int(params.num_seqs), dtype=np.int32)
+    num_work = ctypes.c_int32(0)
+    chunk = ctypes.c_int32(0)
+    st = lib().mj_decode_plan(
+        ctypes.byref(params),
+        ctypes.byref(opts),
+        sl.ctypes.data,
+        work.ctypes.data,
+        cap,
+        ctypes.addressof(num_work),
+        n_splits.ctypes.data,
+        ctypes.addressof(chunk),
+    )
+    _check(st, "mj_decode_plan")
+    return Plan(work[: num_work.value].copy(), n_splits, chunk.value, opts)
+
+
+def workspace_bytes(params: DecodeParams) -> int:
+    return int(lib().mj_decode_workspace_bytes(ctypes.byref(params)))
+
+
+def kernel_name(params: DecodeParams) -> str:
+    buf = ctypes.create_string_buffer(64)
+    _check(lib().mj_kernel_name(ctypes.byref(params), buf, 64), "mj_kernel_name")
+    return buf.value.decode()
+
+
+# ------------------------------------------------------------ torch glue
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def descale_strides(t, num_seqs: int, h_k: int) -> Tuple[int, int]:
+    """(seq, head) element strides of a descale tensor: one element is a
+    per-tensor scale, (h_k,) per head, (b, h_k) per sequence and head."""
+    if t.numel() == 1:
+        return (0, 0)
+    if t.dim() == 1:
+        if t.shape[0] != h_k:
+            raise ValueError(f"descale shape {tuple(t.shape)}")
+        return (0, int(t.stride(0)))
+    if t.dim() != 2 or t.shape[1] != h_k or t.shape[0] != num_seqs:
+        raise ValueError(f"descale shape {tuple(t.shape)}")
+    return (int(t.stride(0)), int(t.stride(1)))
+
+
+def kv_strides(t) -> Tuple[int, int, int]:
+    """(page, row, head) strides of a (num_pages, PS, h_k, d) byte view."""
+    if t.element_size() != 1 or t.stride(3) != 1:
+        raise ValueError("KV cache must be a 1-byte view with d contiguous")
+    return (int(t.stride(0)), int(t.stride(1)), int(t.stride(2)))
+
+
+def decode_attn(
+    params: DecodeParams,
+    *,
+    q,
+    k_cache,
+    v_cache,
+    block_table,
+    seq_lens,
+    work,
+    n_splits,
+    q_descale,
+    k_descale,
+    v_descale,
+    o,
+    lse,
+    workspace=None,
+    softmax_scale: float,
+    scale_o: float = 1.0,
+    status=None,
+    timing_events=None,
+    stream=None,
+) -> None:
+    """mj_decode_attn on device tensors.
+
+    q / o are packed (b, h_k, n_q, d) views (rows contiguous, sequence stride
+    free); k_cache / v_cache are (num_pages, PS, h_k, d) 1-byte views of any
+    physical layout with d contiguous."""
+    a = DecodeArgs()
+    a.q = _ptr(q)
+    a.q_seq_stride = int(q.stride(0))
+    a.k, a.v = _ptr(k_cache), _ptr(v_cache)
+    a.k_page, a.k_row, a.k_head = kv_strides(k_cache)
+    a.v_page, a.v_row, a.v_head = kv_strides(v_cache)
+    a.block_table, a.seq_lens = _ptr(block_table), _ptr(seq_lens)
+    a.work, a.n_splits = _ptr(work), _ptr(n_splits)
+    a.num_work = int(work.shape[0])
+    nb, hk = int(params.num_seqs), int(params.h_k)
+    a.q_descale, a.k_descale, a.v_descale = _ptr(q_descale), _ptr(k_descale), _ptr(v_descale)
+    a.qd_seq, a.qd_head = descale_strides(q_descale, nb, hk)
+    a.kd_seq, a.kd_head = descale_strides(k_descale, nb, hk)
+    a.vd_seq, a.vd_head = descale_strides(v_descale, nb, hk)
+    a.softmax_scale, a.scale_o = float(softmax_scale), float(scale_o)
+    a.o = _ptr(o)
+    a.o_seq_stride = int(o.stride(0))
+    a.lse = _ptr(lse)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = 0 if workspace is None else int(workspace.numel() * workspace.element_size())
+    a.status = _ptr(status)
+    ev_arr = None
+    if timing_events is not None:
+        ev_arr = (ctypes.c_void_p * 3)(*[int(e.cuda_event) for e in timing_events])
+        a.timing_events = ctypes.cast(ev_arr, ctypes.c_void_p)
+    st = lib().mj_decode_attn(ctypes.byref(params), ctypes.byref(a), _stream_handle(stream))
+    _check(st, "mj_decode_attn")
+
+
+def pack_q(q_vllm, q_packed, num_seqs: int, q_len: int, h_k: int, h_r: int, stream=None) -> None:
+    """mj_pack_q: (b*q_len, h_k*h_r, d) -> (b, h_k, q_len*h_r, d)."""
+    st = lib().mj_pack_q(
+        _ptr(q_vllm),
+        _ptr(q_packed),
+        int(q_vllm.element_size()),
+        num_seqs,
+        q_len,
+        h_k,
+        h_r,
+        int(q_vllm.shape[-1]),
+        _stream_handle(stream),
+    )
+    _check(st, "mj_pack_q")
+
+
+def unpack_o(o_packed, o_vllm, num_seqs: int, q_len: int, h_k: int, h_r: int, stream=None) -> None:
+    """mj_unpack_o: (b, h_k, q_len*h_r, d) -> (b*q_len, h_k*h_r, d), bf16."""
+    st = lib().mj_unpack_o(
+        _ptr(o_packed), _ptr(o_vllm), num_seqs, q_len, h_k, h_r, int(o_packed.shape[-1]), _stream_handle(stream)
+    )
+    _check(st, "mj_unpack_o")

@@ -1,0 +1,212 @@
+// C ABI entry points: argument validation, kernel choice and launches.
+
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+
+#include "mj.h"
+#include "mj_internal.h"
+#include "mj_kernels.h"
+
+namespace mj {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct WorkspaceLayout {
+  size_t o_off, m_off, l_off, total;
+};
+
+WorkspaceLayout workspace_layout(const mj_decode_params& p) {
+  WorkspaceLayout w{0, 0, 0, 0};
+  if (p.max_splits <= 1) return w;
+  const size_t rows = static_cast<size_t>(p.num_seqs) * p.h_k * p.max_splits * p.q_len * p.h_r;
+  w.o_off = 0;
+  w.m_off = round_up(rows * kHeadDim * sizeof(float));
+  w.l_off = w.m_off + round_up(rows * sizeof(float));
+  w.total = w.l_off + round_up(rows * sizeof(float));
+  return w;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kSmemPerSm = 233472;  // 228 KiB usable shared memory per SM
+constexpr int kSmemReservedPerCta = 1024;
+
+}  // namespace
+
+KernelChoice choose_kernel(const mj_decode_params& p) {
+  const int n_q = p.q_len * p.h_r;
+  KernelChoice k{};
+  k.kind = KernelKind::kCudaCore;
+  k.rows_per_cta = n_q <= 4 ? 4 : (n_q <= 8 ? 8 : 16);
+  k.n_q_tiles = (n_q + k.rows_per_cta - 1) / k.rows_per_cta;
+  const int smem = cc_smem_bytes(k.rows_per_cta) + kSmemReservedPerCta;
+  int per_sm = kSmemPerSm / smem;
+  if (per_sm > 16) per_sm = 16;
+  k.ctas_per_sm = per_sm < 1 ? 1 : per_sm;
+  const bool e4m3 = p.q_dtype == MJ_E4M3;
+  static const char* names[2][3] = {{"cc_n4_bf16", "cc_n8_bf16", "cc_n16_bf16"},
+                                    {"cc_n4_e4m3", "cc_n8_e4m3", "cc_n16_e4m3"}};
+  k.name = names[e4m3][k.rows_per_cta == 4 ? 0 : (k.rows_per_cta == 8 ? 1 : 2)];
+  return k;
+}
+
+}  // namespace mj
+
+using namespace mj;
+
+extern "C" const char* mj_status_string(mj_status s) {
+  switch (s) {
+    case MJ_OK: return "ok";
+    case MJ_ERR_INVALID_ARG: return "invalid argument";
+    case MJ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MJ_ERR_CAPACITY: return "buffer or workspace too small";
+    case MJ_ERR_CUDA: return "CUDA error";
+    case MJ_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+extern "C" size_t mj_decode_workspace_bytes(const mj_decode_params* params) {
+  if (check_params(params) != MJ_OK) return 0;
+  return workspace_layout(*params).total;
+}
+
+extern "C" mj_status mj_kernel_name(const mj_decode_params* params, char* buf, int32_t len) {
+  const mj_status st = check_params(params);
+  if (st != MJ_OK) return st;
+  if (!buf || len < 1) return MJ_ERR_INVALID_ARG;
+  std::snprintf(buf, static_cast<size_t>(len), "%s", choose_kernel(*params).name);
+  return MJ_OK;
+}
+
+extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_decode_args* args,
+                                    mj_stream_t stream_) {
+  mj_status st = check_params(params);
+  if (st != MJ_OK) return st;
+  if (!args) return MJ_ERR_INVALID_ARG;
+  const mj_decode_params& p = *params;
+  const mj_decode_args& a = *args;
+  if (!a.q || !a.k || !a.v || !a.block_table || !a.seq_lens || !a.work || !a.n_splits || !a.q_descale ||
+      !a.k_descale || !a.v_descale || !a.o || !a.lse)
+    return MJ_ERR_INVALID_ARG;
+  if (a.num_work < 1) return MJ_ERR_INVALID_ARG;
+  // 16-byte page gathers: base pointers and every KV stride 16-byte aligned
+  if (!aligned16(a.k) || !aligned16(a.v)) return MJ_ERR_INVALID_ARG;
+  const int64_t kv_strides[6] = {a.k_page, a.k_row, a.k_head, a.v_page, a.v_row, a.v_head};
+  for (int64_t s : kv_strides)
+    if (s < 0 || (s & 15) != 0) return MJ_ERR_INVALID_ARG;
+  const int q_bytes = p.q_dtype == MJ_E4M3 ? 1 : 2;
+  if (!aligned16(a.q) || !aligned16(a.o)) return MJ_ERR_INVALID_ARG;
+  if (a.q_seq_stride < 0 || ((a.q_seq_stride * q_bytes) & 15) != 0) return MJ_ERR_INVALID_ARG;
+  if (a.o_seq_stride < 0 || ((a.o_seq_stride * 2) & 15) != 0) return MJ_ERR_INVALID_ARG;
+  const int64_t d_strides[6] = {a.qd_seq, a.qd_head, a.kd_seq, a.kd_head, a.vd_seq, a.vd_head};
+  for (int64_t s : d_strides)
+    if (s < 0) return MJ_ERR_INVALID_ARG;
+  if (!(a.softmax_scale > 0.f) || !(a.scale_o == a.scale_o)) return MJ_ERR_INVALID_ARG;
+  const WorkspaceLayout ws = workspace_layout(p);
+  if (ws.total > 0) {
+    if (!a.workspace) return MJ_ERR_INVALID_ARG;
+    if (a.workspace_bytes < ws.total) return MJ_ERR_CAPACITY;
+    if ((reinterpret_cast<uintptr_t>(a.workspace) & (kAlign - 1)) != 0) return MJ_ERR_INVALID_ARG;
+  }
+
+  DecodeDev d{};
+  d.q = a.q;
+  d.q_seq = a.q_seq_stride;
+  d.k = a.k;
+  d.v = a.v;
+  d.k_page = a.k_page;
+  d.k_row = a.k_row;
+  d.k_head = a.k_head;
+  d.v_page = a.v_page;
+  d.v_row = a.v_row;
+  d.v_head = a.v_head;
+  d.block_table = a.block_table;
+  d.seq_lens = a.seq_lens;
+  d.work = a.work;
+  d.n_splits = a.n_splits;
+  d.qd = a.q_descale;
+  d.kd = a.k_descale;
+  d.vd = a.v_descale;
+  d.qd_seq = a.qd_seq;
+  d.qd_head = a.qd_head;
+  d.kd_seq = a.kd_seq;
+  d.kd_head = a.kd_head;
+  d.vd_seq = a.vd_seq;
+  d.vd_head = a.vd_head;
+  d.softmax_scale = a.softmax_scale;
+  d.scale_o = a.scale_o;
+  d.o = static_cast<__nv_bfloat16*>(a.o);
+  d.o_seq = a.o_seq_stride;
+  d.lse = a.lse;
+  if (ws.total > 0) {
+    char* base = static_cast<char*>(a.workspace);
+    d.o_part = reinterpret_cast<float*>(base + ws.o_off);
+    d.m_part = reinterpret_cast<float*>(base + ws.m_off);
+    d.l_part = reinterpret_cast<float*>(base + ws.l_off);
+  }
+  d.status = a.status;
+  d.num_seqs = p.num_seqs;
+  d.h_k = p.h_k;
+  d.n_q = p.q_len * p.h_r;
+  d.q_len = p.q_len;
+  d.h_r = p.h_r;
+  d.page_size = p.page_size;
+  d.max_blocks = p.max_blocks;
+  d.causal = p.causal;
+  d.max_splits = p.max_splits;
+  d.num_work = a.num_work;
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  if (a.timing_events)
+    for (int i = 0; i < 3; ++i) ev[i] = static_cast<cudaEvent_t>(a.timing_events[i]);
+
+  const KernelChoice kc = choose_kernel(p);
+  cudaError_t e = cudaSuccess;
+  if (ev[0] && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return MJ_ERR_CUDA;
+  e = launch_decode_cc(d, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
+  if (e != cudaSuccess) return MJ_ERR_CUDA;
+  if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return MJ_ERR_CUDA;
+  if (p.max_splits > 1) {
+    e = launch_merge(d, stream);
+    if (e != cudaSuccess) return MJ_ERR_CUDA;
+  }
+  if (ev[2] && cudaEventRecord(ev[2], stream) != cudaSuccess) return MJ_ERR_CUDA;
+  return MJ_OK;
+}
+
+namespace {
+
+mj_status permute(const void* src, void* dst, int32_t elem_bytes, int32_t num_seqs, int32_t q_len,
+                  int32_t h_k, int32_t h_r, int32_t head_dim, bool to_packed, mj_stream_t stream) {
+  if (!src || !dst || !aligned16(src) || !aligned16(dst)) return MJ_ERR_INVALID_ARG;
+  if (elem_bytes != 1 && elem_bytes != 2) return MJ_ERR_INVALID_ARG;
+  if (num_seqs < 1 || q_len < 1 || h_k < 1 || h_r < 1 || head_dim < 1) return MJ_ERR_INVALID_ARG;
+  if ((head_dim * elem_bytes) % 16 != 0) return MJ_ERR_UNSUPPORTED;
+  const char* s = static_cast<const char*>(src);
+  const char* d = static_cast<const char*>(dst);
+  const size_t bytes = static_cast<size_t>(num_seqs) * q_len * h_k * h_r * head_dim * elem_bytes;
+  if (s < d + bytes && d < s + bytes) return MJ_ERR_INVALID_ARG;  // overlap
+  const cudaError_t e = launch_permute_rows(src, dst, elem_bytes, num_seqs, q_len, h_k, h_r, head_dim,
+                                            to_packed, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MJ_OK : MJ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" mj_status mj_pack_q(const void* q_vllm, void* q_packed, int32_t elem_bytes, int32_t num_seqs,
+                               int32_t q_len, int32_t h_k, int32_t h_r, int32_t head_dim,
+                               mj_stream_t stream) {
+  return permute(q_vllm, q_packed, elem_bytes, num_seqs, q_len, h_k, h_r, head_dim, true, stream);
+}
+
+extern "C" mj_status mj_unpack_o(const void* o_packed, void* o_vllm, int32_t num_seqs, int32_t q_len,
+                                 int32_t h_k, int32_t h_r, int32_t head_dim, mj_stream_t stream) {
+  return permute(o_packed, o_vllm, 2, num_seqs, q_len, h_k, h_r, head_dim, false, stream);
+}

@@ -1,0 +1,33 @@
+// Host-side internals shared by the plan, the validation and the launchers.
+#pragma once
+
+#include <cstdint>
+
+#include "mj.h"
+
+namespace mj {
+
+constexpr int kTileRows = 128;  // plan unit: KV rows per tile
+constexpr int kHeadDim = 128;
+constexpr int kMaxSplits = 256;
+constexpr int kDefaultSmCount = 152;  // GB300
+
+enum class KernelKind { kCudaCore = 0, kTensorCore = 1 };
+
+// The decode kernel mj_decode_attn launches for a problem, and the
+// occupancy facts the plan needs about it.
+struct KernelChoice {
+  KernelKind kind;
+  int rows_per_cta;  // packed query rows one CTA covers
+  int n_q_tiles;     // CTAs along the packed rows
+  int ctas_per_sm;   // co-resident CTAs per SM
+  const char* name;
+};
+
+// Validates the shape fields every entry point shares.
+mj_status check_params(const mj_decode_params* p);
+
+// Kernel choice for valid params.
+KernelChoice choose_kernel(const mj_decode_params& p);
+
+}  // namespace mj

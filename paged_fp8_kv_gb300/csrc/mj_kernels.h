@@ -1,0 +1,25 @@
+// Launchers of the device kernels (host-callable, defined in the .cu files).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "mj_device.cuh"
+
+namespace mj {
+
+constexpr int kHeadDimDev = 128;
+constexpr int kTileRowsDev = 128;
+
+// CUDA-core decode (rows_per_cta in {4, 8, 16}).
+cudaError_t launch_decode_cc(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
+                             cudaStream_t stream);
+int cc_smem_bytes(int rows_per_cta);
+
+// Merge of split sequences' partials into O / LSE.
+cudaError_t launch_merge(const DecodeDev& a, cudaStream_t stream);
+
+// Layout permutations (vLLM <-> packed rows).
+cudaError_t launch_permute_rows(const void* src, void* dst, int elem_bytes, int num_seqs, int q_len,
+                                int h_k, int h_r, int head_dim, bool to_packed, cudaStream_t stream);
+
+}  // namespace mj

@@ -1,0 +1,135 @@
+// Host plan: occupancy-pinned split-KV work list.
+//
+// Source: the "mjolnir/t5_decode.py" page, `plan_split_kv` and `SplitPlan`
+// (host helpers section).  The plan is pure integer code; it makes no CUDA
+// call, so it can run on any host thread while the GPU works.
+
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "mj_internal.h"
+
+namespace mj {
+
+mj_status check_params(const mj_decode_params* p) {
+  if (!p) return MJ_ERR_INVALID_ARG;
+  if (p->num_seqs < 1 || p->q_len < 1 || p->h_k < 1 || p->h_r < 1) return MJ_ERR_INVALID_ARG;
+  if (p->max_blocks < 1 || p->num_pages < 1) return MJ_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return MJ_ERR_INVALID_ARG;
+  if (p->max_splits < 1 || p->max_splits > kMaxSplits) return MJ_ERR_INVALID_ARG;
+  if (p->head_dim != kHeadDim) return MJ_ERR_UNSUPPORTED;
+  if (p->page_size != 16 && p->page_size != 32 && p->page_size != 64 && p->page_size != 128)
+    return MJ_ERR_UNSUPPORTED;
+  if (p->q_dtype != MJ_BF16 && p->q_dtype != MJ_E4M3) return MJ_ERR_UNSUPPORTED;
+  // int32 index ranges used by the kernels
+  const int64_t n_q = static_cast<int64_t>(p->q_len) * p->h_r;
+  if (n_q > 4096 || static_cast<int64_t>(p->num_seqs) * p->h_k * n_q > (int64_t{1} << 30))
+    return MJ_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(p->max_blocks) * p->page_size > (int64_t{1} << 30)) return MJ_ERR_UNSUPPORTED;
+  return MJ_OK;
+}
+
+namespace {
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Item {
+  int32_t seq, begin, end, slot;
+};
+
+}  // namespace
+
+}  // namespace mj
+
+extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts* opts,
+                                    const int32_t* seq_lens_host, int32_t* work_out,
+                                    int32_t work_cap, int32_t* num_work, int32_t* n_splits_out,
+                                    int32_t* chunk_tiles) {
+  using namespace mj;
+  mj_status st = check_params(params);
+  if (st != MJ_OK) return st;
+  if (!opts || !seq_lens_host || !work_out || !num_work || !n_splits_out || work_cap < 1)
+    return MJ_ERR_INVALID_ARG;
+  if (opts->sm_count < 0 || opts->ctas_per_sm < 0 || opts->n_q_tiles < 0 || opts->force_splits < 0 ||
+      opts->min_chunk_tiles < 0 || opts->pad_to < 0)
+    return MJ_ERR_INVALID_ARG;
+
+  const KernelChoice kc = choose_kernel(*params);
+  if (opts->sm_count == 0) opts->sm_count = kDefaultSmCount;
+  if (opts->ctas_per_sm == 0) opts->ctas_per_sm = kc.ctas_per_sm;
+  if (opts->n_q_tiles == 0) opts->n_q_tiles = kc.n_q_tiles;
+  if (opts->min_chunk_tiles == 0) opts->min_chunk_tiles = 1;
+
+  const int b = params->num_seqs;
+  const int64_t max_len = static_cast<int64_t>(params->max_blocks) * params->page_size;
+  std::vector<int64_t> tiles(b);
+  int64_t longest = 0;
+  for (int i = 0; i < b; ++i) {
+    const int64_t L = seq_lens_host[i];
+    if (L < 0 || L > max_len) return MJ_ERR_INVALID_ARG;
+    tiles[i] = std::max<int64_t>(1, ceil_div(L, kTileRows));
+    longest = std::max(longest, tiles[i]);
+  }
+
+  const int64_t per_wave = static_cast<int64_t>(opts->sm_count) * opts->ctas_per_sm;
+  const int64_t slots =
+      std::max<int64_t>(1, per_wave / (static_cast<int64_t>(params->h_k) * opts->n_q_tiles));
+  const int64_t floor_chunk =
+      std::max<int64_t>(opts->min_chunk_tiles, ceil_div(longest, params->max_splits));
+
+  auto total_chunks = [&](int64_t chunk) {
+    int64_t s = 0;
+    for (int64_t t : tiles) s += ceil_div(t, chunk);
+    return s;
+  };
+
+  int64_t chunk;
+  if (opts->force_splits > 0) {
+    chunk = std::max(floor_chunk, ceil_div(longest, opts->force_splits));
+  } else if (b >= slots || params->max_splits == 1) {
+    chunk = longest;
+  } else {
+    // Smallest chunk in [floor_chunk, longest] whose chunks fit one wave;
+    // total_chunks() is non-increasing in chunk.
+    int64_t lo = floor_chunk, hi = std::max(floor_chunk, longest);
+    while (lo < hi) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (total_chunks(mid) <= slots)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    chunk = lo;
+  }
+
+  std::vector<Item> items;
+  items.reserve(static_cast<size_t>(total_chunks(chunk)));
+  for (int i = 0; i < b; ++i) {
+    const int64_t k = ceil_div(tiles[i], chunk);
+    if (k > params->max_splits) return MJ_ERR_INVALID_ARG;  // force_splits beyond max_splits
+    n_splits_out[i] = static_cast<int32_t>(k);
+    for (int64_t s = 0; s < k; ++s) {
+      const int64_t beg = s * chunk;
+      const int64_t end = std::min(tiles[i], beg + chunk);
+      items.push_back({i, static_cast<int32_t>(beg), static_cast<int32_t>(end), static_cast<int32_t>(s)});
+    }
+  }
+  std::stable_sort(items.begin(), items.end(), [](const Item& x, const Item& y) {
+    return (x.end - x.begin) > (y.end - y.begin);
+  });
+  const int64_t n_items = static_cast<int64_t>(items.size());
+  if (opts->pad_to > 0 && opts->pad_to < n_items) return MJ_ERR_INVALID_ARG;
+  const int64_t n_out = opts->pad_to > 0 ? opts->pad_to : n_items;
+  if (n_out > work_cap) return MJ_ERR_CAPACITY;
+  for (int64_t i = 0; i < n_out; ++i) {
+    const Item it = i < n_items ? items[i] : Item{0, 0, 0, 0};
+    work_out[4 * i + 0] = it.seq;
+    work_out[4 * i + 1] = it.begin;
+    work_out[4 * i + 2] = it.end;
+    work_out[4 * i + 3] = it.slot;
+  }
+  *num_work = static_cast<int32_t>(n_out);
+  if (chunk_tiles) *chunk_tiles = static_cast<int32_t>(chunk);
+  return MJ_OK;
+}

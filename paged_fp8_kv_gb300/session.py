@@ -1,0 +1,169 @@
+"""Device-resident decode step for one batch: the buffers a caller keeps
+between steps, and the calls of one step (plan, pack, decode + merge,
+unpack), all through the C ABI.  Marshalling only.
+"""
+
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import (
+    MJ_BF16,
+    MJ_E4M3,
+    decode_attn,
+    decode_plan,
+    kernel_name,
+    make_params,
+    pack_q,
+    unpack_o,
+    workspace_bytes,
+)
+
+
+class DecodeSession:
+    """Holds a workload's cache, tables and outputs on the GPU.
+
+    ``w`` is any object with the fields of
+    :class:`paged_fp8_kv_gb300.synthetic.Workload` (host numpy arrays)."""
+
+    def __init__(
+        self,
+        w,
+        device: str = "cuda",
+        max_splits: Optional[int] = None,
+        sm_count: Optional[int] = None,
+        force_splits: int = 0,
+        pad_to: int = 0,
+        kv_layout: str = "nhd",
+    ):
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        self.num_seqs, self.q_len, self.h_k, self.h_r = w.num_seqs, w.q_len, w.h_k, w.h_r
+        self.n_q = w.q_len * w.h_r
+        self.d = w.head_dim
+        self.q_dtype = MJ_E4M3 if w.q_is_e4m3 else MJ_BF16
+        self.max_splits = int(max_splits if max_splits is not None else w.max_splits)
+        self.params = make_params(
+            w.num_seqs,
+            w.q_len,
+            w.h_k,
+            w.h_r,
+            w.page_size,
+            w.max_blocks,
+            w.num_pages,
+            bool(w.causal),
+            self.q_dtype,
+            self.max_splits,
+            w.head_dim,
+        )
+        self.kernel = kernel_name(self.params)
+        if sm_count is None:
+            sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.sm_count = int(sm_count)
+
+        # KV cache in the requested physical layout, exposed as logical
+        # (num_pages, PS, h_k, d) byte views.
+        k = torch.from_numpy(w.k_cache)
+        v = torch.from_numpy(w.v_cache)
+        if kv_layout == "nhd":
+            self.k_cache = k.to(dev)
+            self.v_cache = v.to(dev)
+        elif kv_layout == "hnd":  # (pages, 2, h_k, PS, d)
+            buf = torch.stack([k.permute(0, 2, 1, 3), v.permute(0, 2, 1, 3)], dim=1).contiguous().to(dev)
+            self.k_cache = buf[:, 0].transpose(1, 2)
+            self.v_cache = buf[:, 1].transpose(1, 2)
+            self._kv_buf = buf
+        elif kv_layout == "interleaved":  # (pages, h_k, PS, 2d)
+            buf = torch.cat([k.permute(0, 2, 1, 3), v.permute(0, 2, 1, 3)], dim=-1).contiguous().to(dev)
+            kv = buf.transpose(1, 2)
+            self.k_cache = kv[..., : self.d]
+            self.v_cache = kv[..., self.d :]
+            self._kv_buf = buf
+        elif kv_layout == "flashinfer":  # (pages, 2, PS, h_k, d)
+            buf = torch.stack([k, v], dim=1).contiguous().to(dev)
+            self.k_cache = buf[:, 0]
+            self.v_cache = buf[:, 1]
+            self._kv_buf = buf
+        else:
+            raise ValueError(kv_layout)
+
+        self.block_table = torch.from_numpy(w.block_table).to(dev)
+        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+        self.q_descale = torch.from_numpy(np.ascontiguousarray(w.q_descale)).to(dev)
+        self.k_descale = torch.from_numpy(np.ascontiguousarray(w.k_descale)).to(dev)
+        self.v_descale = torch.from_numpy(np.ascontiguousarray(w.v_descale)).to(dev)
+
+        q_host = torch.from_numpy(w.q.view(np.int16) if w.q.dtype == np.uint16 else w.q)
+        self.q_vllm = q_host.to(dev)  # (b*q_len, h_q, d), int16 (bf16 bits) or uint8
+        self.q_packed = (
+            self.q_vllm.view(self.num_seqs, self.h_k, self.n_q, self.d)
+            if self.q_len == 1
+            else torch.empty(self.num_seqs, self.h_k, self.n_q, self.d, dtype=self.q_vllm.dtype, device=dev)
+        )
+        self.o_packed = torch.empty(self.num_seqs, self.h_k, self.n_q, self.d, dtype=torch.bfloat16, device=dev)
+        self.o_vllm = (
+            self.o_packed.view(self.num_seqs * self.q_len, self.h_k * self.h_r, self.d)
+            if self.q_len == 1
+            else torch.empty(self.num_seqs * self.q_len, self.h_k * self.h_r, self.d, dtype=torch.bfloat16, device=dev)
+        )
+        self.lse = torch.empty(self.num_seqs, self.h_k, self.n_q, dtype=torch.float32, device=dev)
+        ws = workspace_bytes(self.params)
+        self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev) if ws else None
+        self.replan(w.seq_lens, force_splits=force_splits, pad_to=pad_to)
+
+    def replan(self, seq_lens_host, force_splits: int = 0, pad_to: int = 0) -> None:
+        self.plan = decode_plan(
+            self.params, seq_lens_host, sm_count=self.sm_count, force_splits=force_splits, pad_to=pad_to
+        )
+        self.work = torch.from_numpy(self.plan.work).to(self.device)
+        self.n_splits = torch.from_numpy(self.plan.n_splits).to(self.device)
+
+    def fill_workspace(self, value: float) -> None:
+        if self.workspace is not None:
+            self.workspace.view(torch.float32)[: self.workspace.numel() // 4].fill_(value)
+
+    def decode(self, stream=None, status=None, timing_events=None) -> None:
+        decode_attn(
+            self.params,
+            q=self.q_packed,
+            k_cache=self.k_cache,
+            v_cache=self.v_cache,
+            block_table=self.block_table,
+            seq_lens=self.seq_lens,
+            work=self.work,
+            n_splits=self.n_splits,
+            q_descale=self.q_descale,
+            k_descale=self.k_descale,
+            v_descale=self.v_descale,
+            o=self.o_packed,
+            lse=self.lse,
+            workspace=self.workspace,
+            softmax_scale=self.w.softmax_scale,
+            scale_o=self.w.scale_o,
+            status=status,
+            timing_events=timing_events,
+            stream=stream,
+        )
+
+    def step(self, stream=None, status=None, timing_events=None) -> None:
+        """pack (q_len > 1) -> decode + merge -> unpack (q_len > 1)."""
+        if self.q_len > 1:
+            pack_q(self.q_vllm, self.q_packed, self.num_seqs, self.q_len, self.h_k, self.h_r, stream=stream)
+        self.decode(stream=stream, status=status, timing_events=timing_events)
+        if self.q_len > 1:
+            unpack_o(self.o_packed, self.o_vllm, self.num_seqs, self.q_len, self.h_k, self.h_r, stream=stream)
+
+    def launches_per_step(self) -> int:
+        n = 1 + (1 if self.max_splits > 1 else 0)
+        return n + (2 if self.q_len > 1 else 0)
+
+    # host copies of the outputs, packed (b, h_k, n_q, d) / (b, h_k, n_q)
+    def o_host(self) -> np.ndarray:
+        return self.o_packed.float().cpu().numpy()
+
+    def lse_host(self) -> np.ndarray:
+        return self.lse.cpu().numpy()

@@ -1,0 +1,189 @@
+"""The C ABI without a GPU: the library loads and exports every symbol the
+header declares; the host plan matches the plan oracle bit for bit; argument
+validation rejects bad calls before anything is launched."""
+
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_fp8_kv_gb300 as mj
+from oracle.plan_ref import plan_ref
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mj.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_fp8_kv_gb300.build import build
+
+    build()
+
+
+def test_every_declared_symbol_is_exported():
+    text = open(HEADER).read()
+    names = sorted(set(re.findall(r"\b(mj_[a-z_0-9]+)\s*\(", text)))
+    assert len(names) >= 7
+    L = mj.lib()
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in mj.h but not exported"
+
+
+def _params(b, h_k=1, q_len=1, h_r=4, ps=16, max_blocks=1 << 16, max_splits=16, q_dtype=0):
+    return mj.make_params(b, q_len, h_k, h_r, ps, max_blocks, 100000, True, q_dtype, max_splits)
+
+
+@pytest.mark.parametrize("case", json.load(open(os.path.join(ROOT, "tests", "golden", "plan_examples.json")))["cases"])
+def test_plan_golden(case):
+    a = case["args"]
+    p = _params(len(a["seq_lens"]), h_k=a["h_k"], max_splits=a["max_splits"])
+    plan = mj.decode_plan(
+        p,
+        a["seq_lens"],
+        sm_count=a["sm_count"],
+        ctas_per_sm=a["ctas_per_sm"],
+        n_q_tiles=a["n_q_tiles"],
+        force_splits=a.get("force_splits", 0),
+        pad_to=a.get("pad_to", 0),
+    )
+    assert plan.chunk_tiles == case["chunk_tiles"]
+    assert plan.n_splits.tolist() == case["n_splits"]
+    if "work" in case:
+        assert plan.work.tolist() == case["work"]
+    else:
+        assert plan.num_work == case["work_len"]
+
+
+def test_plan_matches_oracle_bit_exact():
+    rng = np.random.default_rng(41)
+    for _ in range(500):
+        b = int(rng.integers(1, 64))
+        seq_lens = rng.integers(0, 40000, size=b)
+        if rng.random() < 0.3:
+            seq_lens[0] = int(rng.integers(100000, 300000))
+        h_k = int(rng.choice([1, 2, 4, 8]))
+        sm = int(rng.choice([20, 132, 148, 152]))
+        cps = int(rng.integers(1, 9))
+        ntiles = int(rng.choice([1, 2, 3]))
+        max_splits = int(rng.choice([1, 2, 16, 64, 256]))
+        force = int(rng.choice([0, 0, 0, 2, 7]))
+        min_chunk = int(rng.choice([1, 1, 3]))
+        ref = plan_ref(seq_lens.tolist(), h_k, ntiles, sm, cps, max_splits, force, min_chunk, 0)
+        pad = 0 if rng.random() < 0.5 else len(ref.work) + int(rng.integers(0, 9))
+        if pad:
+            ref = plan_ref(seq_lens.tolist(), h_k, ntiles, sm, cps, max_splits, force, min_chunk, pad)
+        p = _params(b, h_k=h_k, max_splits=max_splits, max_blocks=300000 // 16 + 1)
+        got = mj.decode_plan(p, seq_lens, sm, cps, ntiles, force, min_chunk, pad)
+        assert got.work.tolist() == [list(w) for w in ref.work]
+        assert got.n_splits.tolist() == ref.n_splits
+        assert got.chunk_tiles == ref.chunk_tiles
+
+
+def test_plan_reports_library_defaults():
+    p = _params(4, h_k=8, h_r=4)
+    plan = mj.decode_plan(p, [1000, 2000, 3000, 4000])
+    assert plan.opts.sm_count == 152 and plan.opts.ctas_per_sm >= 1 and plan.opts.n_q_tiles >= 1
+    ref = plan_ref([1000, 2000, 3000, 4000], 8, plan.opts.n_q_tiles, 152, plan.opts.ctas_per_sm, 16)
+    assert plan.work.tolist() == [list(w) for w in ref.work]
+
+
+def _plan_status(params, seq_lens, cap=None, **opts):
+    L = mj.lib()
+    o = mj.PlanOpts(opts.get("sm", 0), 0, 0, 0, 0, opts.get("pad_to", 0))
+    sl = np.asarray(seq_lens, dtype=np.int32)
+    cap = cap if cap is not None else 4096
+    work = np.zeros((max(cap, 1), 4), dtype=np.int32)
+    ns = np.zeros(max(params.num_seqs, 1), dtype=np.int32)
+    nw = ctypes.c_int32()
+    return L.mj_decode_plan(
+        ctypes.byref(params), ctypes.byref(o), sl.ctypes.data, work.ctypes.data, cap, ctypes.addressof(nw), ns.ctypes.data, None
+    )
+
+
+def test_plan_rejects_bad_input():
+    p = _params(2, max_blocks=4, ps=16)  # at most 64 rows
+    assert _plan_status(p, [64, 10]) == mj.MJ_OK
+    assert _plan_status(p, [65, 10]) == mj.MJ_ERR_INVALID_ARG
+    assert _plan_status(p, [-1, 10]) == mj.MJ_ERR_INVALID_ARG
+    assert _plan_status(p, [64, 10], cap=1) == mj.MJ_ERR_CAPACITY
+    assert _plan_status(p, [64, 10], pad_to=1) == mj.MJ_ERR_INVALID_ARG
+    bad = _params(2)
+    bad.head_dim = 64
+    assert _plan_status(bad, [10, 10]) == mj.MJ_ERR_UNSUPPORTED
+    bad = _params(2)
+    bad.page_size = 8
+    assert _plan_status(bad, [10, 10]) == mj.MJ_ERR_UNSUPPORTED
+    bad = _params(2, max_splits=257)
+    assert _plan_status(bad, [10, 10]) == mj.MJ_ERR_INVALID_ARG
+
+
+def test_workspace_bytes():
+    p = _params(3, h_k=2, q_len=2, h_r=4, max_splits=16)
+    rows = 3 * 2 * 16 * 8
+    ru = lambda x: (x + 255) // 256 * 256
+    assert mj.workspace_bytes(p) == ru(rows * 128 * 4) + 2 * ru(rows * 4)
+    assert mj.workspace_bytes(_params(3, max_splits=1)) == 0
+
+
+def _good_args():
+    a = mj.DecodeArgs()
+    fake = 1 << 20  # aligned, never dereferenced: validation fails first
+    for f in ("q", "k", "v", "block_table", "seq_lens", "work", "n_splits", "q_descale", "k_descale", "v_descale", "o", "lse"):
+        setattr(a, f, fake)
+    a.q_seq_stride = 4 * 128
+    a.k_page, a.k_row, a.k_head = 16 * 128, 128, 128
+    a.v_page, a.v_row, a.v_head = 16 * 128, 128, 128
+    a.num_work = 1
+    a.softmax_scale = 0.088
+    a.scale_o = 1.0
+    a.o_seq_stride = 4 * 128
+    return a
+
+
+def _attn_status(params, args):
+    return mj.lib().mj_decode_attn(ctypes.byref(params), ctypes.byref(args), None)
+
+
+def test_decode_attn_validation_rejects_before_launch():
+    p = _params(1, h_r=4, max_splits=16)
+    for field, val, want in [
+        ("q", None, mj.MJ_ERR_INVALID_ARG),
+        ("k", (1 << 20) + 8, mj.MJ_ERR_INVALID_ARG),  # misaligned
+        ("k_row", 100, mj.MJ_ERR_INVALID_ARG),  # not a 16-byte multiple
+        ("v_head", -16, mj.MJ_ERR_INVALID_ARG),
+        ("num_work", 0, mj.MJ_ERR_INVALID_ARG),
+        ("q_seq_stride", 3, mj.MJ_ERR_INVALID_ARG),
+        ("softmax_scale", 0.0, mj.MJ_ERR_INVALID_ARG),
+        ("workspace", None, mj.MJ_ERR_INVALID_ARG),  # max_splits > 1 needs one
+    ]:
+        a = _good_args()
+        a.workspace = 1 << 20
+        a.workspace_bytes = mj.workspace_bytes(p)
+        setattr(a, field, val)
+        assert _attn_status(p, a) == want, field
+    a = _good_args()
+    a.workspace = 1 << 20
+    a.workspace_bytes = mj.workspace_bytes(p) - 1
+    assert _attn_status(p, a) == mj.MJ_ERR_CAPACITY
+    bad = _params(1, h_r=4)
+    bad.head_dim = 256
+    assert _attn_status(bad, _good_args()) == mj.MJ_ERR_UNSUPPORTED
+
+
+def test_pack_validation():
+    L = mj.lib()
+    fake = 1 << 20
+    assert L.mj_pack_q(fake, fake + (1 << 24), 3, 1, 1, 1, 1, 128, None) == mj.MJ_ERR_INVALID_ARG
+    assert L.mj_pack_q(fake, fake + 8, 2, 1, 2, 1, 2, 128, None) == mj.MJ_ERR_INVALID_ARG  # misaligned dst
+    assert L.mj_pack_q(fake, fake, 2, 1, 2, 1, 2, 128, None) == mj.MJ_ERR_INVALID_ARG  # overlap
+    assert L.mj_unpack_o(None, fake, 1, 2, 1, 2, 128, None) == mj.MJ_ERR_INVALID_ARG
+
+
+def test_status_strings_and_kernel_name():
+    assert mj.status_string(mj.MJ_OK) == "ok"
+    assert "timed out" in mj.status_string(mj.MJ_ERR_TIMEOUT)
+    assert mj.kernel_name(_params(2, h_r=4)).startswith(("cc_", "tc_"))

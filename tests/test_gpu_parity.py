@@ -1,0 +1,236 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, on
+the same seeded inputs, element by element.
+
+Small cases (several KV tiles and a ragged tail, every row checked) cover
+each config; full-size cases (the benchmark's sizes and launch
+configuration) are checked on sampled (sequence, kv head) units.  Edge
+cases: empty and shorter-than-q_len sequences, padded work lists, an
+uninitialised (NaN) workspace, poisoned unused pages and garbage block-table
+padding, forced splits, every KV layout the strides allow, descale
+broadcasts, determinism and CUDA-graph replay.
+"""
+
+import copy
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.layout_ref import pack_q_ref, unpack_o_ref
+from paged_fp8_kv_gb300 import synthetic as syn
+from paged_fp8_kv_gb300.session import DecodeSession
+from tests.gpu_helpers import compare, sample_units
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_fp8_kv_gb300.build import build
+
+    build()
+
+
+def run(w, nan_workspace=True, **kw):
+    s = DecodeSession(w, **kw)
+    if nan_workspace:
+        s.fill_workspace(float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s.step(status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return s
+
+
+def check(w, units=None, **kw):
+    s = run(w, **kw)
+    return s, compare(w, s.o_host(), s.lse_host(), units=units)
+
+
+# ------------------------------------------------------------------ configs
+
+
+def test_config1_tiny_full():
+    w = syn.config(1)
+    s, errs = check(w)
+    assert s.plan.max_n_splits == 1
+
+
+@pytest.mark.parametrize("force", [0, 3])
+def test_config2_small(force):
+    w = syn.config(2, num_seqs=6, len_range=(300, 1500))
+    check(w, force_splits=force)
+
+
+def test_config2_full_sampled():
+    w = syn.config(2)
+    s = run(w)
+    units = sample_units(w, 24, seed=2, include=[(int(np.argmax(w.seq_lens)), 0)])
+    compare(w, s.o_host(), s.lse_host(), units=units)
+
+
+def test_config3_small_split_and_merge():
+    w = syn.config(3, num_seqs=4, len_range=(6000, 500))
+    s, _ = check(w)
+    assert s.plan.n_splits[0] > 1  # the long sequence is split and merged
+
+
+def test_config3_full_sampled():
+    w = syn.config(3)
+    s = run(w)
+    assert s.plan.n_splits[0] > 1
+    compare(w, s.o_host(), s.lse_host(), units=[(0, 0), (3, 0), (7, 0)])
+
+
+@pytest.mark.parametrize("variant", [None, "noncausal"])
+def test_config4_small(variant):
+    w = syn.config(4, variant=variant, num_seqs=5, len_range=(200, 1300))
+    check(w)
+
+
+def test_config4_full_sampled():
+    w = syn.config(4)
+    s = run(w)
+    units = sample_units(w, 12, seed=4, include=[(int(np.argmax(w.seq_lens)), 7)])
+    compare(w, s.o_host(), s.lse_host(), units=units)
+
+
+@pytest.mark.parametrize("h_r,q_len", syn.SWEEP_POINTS)
+def test_config5_small(h_r, q_len):
+    w = syn.config(5, h_r=h_r, q_len=q_len, num_seqs=3, len_range=(0, 700))
+    check(w)
+
+
+@pytest.mark.parametrize("h_r,q_len", [(16, 1), (32, 16)])
+def test_config5_full_sampled(h_r, q_len):
+    w = syn.config(5, h_r=h_r, q_len=q_len)
+    s = run(w)
+    compare(w, s.o_host(), s.lse_host(), units=[(0, 0), (77, 0), (127, 0)])
+
+
+# --------------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("q_len,causal", [(1, True), (4, True), (3, False)])
+def test_empty_short_and_aligned_lengths(q_len, causal):
+    lens = [0, 1, 2, 3, 16, 127, 128, 129, 256, 300]
+    w = syn.make_workload("edge", lens, q_len, 2, 4, 16, seed=51, causal=causal, max_splits=4)
+    s, _ = check(w, force_splits=2)
+    lse = s.lse_host()
+    assert np.all(np.isneginf(lse[0]))  # L = 0
+    assert np.all(s.o_host()[0] == 0.0)
+
+
+def test_padded_work_list_changes_nothing():
+    w = syn.config(2, num_seqs=5, len_range=(200, 900))
+    a = run(w)
+    b = run(w, pad_to=a.plan.num_work + 37)
+    assert b.plan.num_work == a.plan.num_work + 37
+    assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
+
+
+def test_workspace_contents_do_not_matter():
+    w = syn.config(3, num_seqs=3, len_range=(3000, 400))
+    a = run(w, nan_workspace=True)
+    b = run(w, nan_workspace=False)
+    b.fill_workspace(1e30)
+    b.step()
+    torch.cuda.synchronize()
+    assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
+
+
+def test_unused_pages_and_table_padding_are_never_read():
+    w = syn.config(4, num_seqs=3, len_range=(100, 700))
+    a = run(w)
+    w2 = copy.deepcopy(w)
+    owned = set()
+    for bi, L in enumerate(w.seq_lens):
+        owned |= set(w.block_table[bi, : -(-int(L) // w.page_size)].tolist())
+    free = [p for p in range(w.num_pages) if p not in owned]
+    w2.k_cache[free] = 0x3F
+    w2.v_cache[free] = 0x40
+    b = run(w2)
+    assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
+
+
+def test_page_permutation_gives_identical_bytes():
+    w = syn.config(2, num_seqs=4, len_range=(300, 800))
+    a = run(w)
+    w2 = copy.deepcopy(w)
+    perm = np.random.default_rng(9).permutation(w.num_pages)
+    inv = np.argsort(perm)
+    w2.k_cache = np.ascontiguousarray(w.k_cache[perm])
+    w2.v_cache = np.ascontiguousarray(w.v_cache[perm])
+    for bi, L in enumerate(w.seq_lens):
+        n = -(-int(L) // w.page_size)
+        w2.block_table[bi, :n] = inv[w.block_table[bi, :n]]
+    b = run(w2)
+    assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
+
+
+def test_determinism_and_graph_replay():
+    w = syn.config(4, num_seqs=4, len_range=(500, 2000))
+    s = run(w)
+    o0, l0 = s.o_vllm.clone(), s.lse.clone()
+    for _ in range(3):
+        s.step()
+    torch.cuda.synchronize()
+    assert torch.equal(o0, s.o_vllm) and torch.equal(l0, s.lse)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    s.o_vllm.zero_()
+    with torch.cuda.graph(g, stream=stream):
+        s.step(stream=stream)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o0, s.o_vllm) and torch.equal(l0, s.lse)
+
+
+@pytest.mark.parametrize("layout", ["hnd", "interleaved", "flashinfer"])
+def test_kv_layouts_match_nhd(layout):
+    w = syn.config(4, num_seqs=3, len_range=(200, 900))
+    a = run(w)
+    b = run(w, kv_layout=layout)
+    assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
+
+
+@pytest.mark.parametrize("kind", ["per_tensor", "per_head"])
+def test_descale_broadcasts(kind):
+    w = syn.config(2, num_seqs=3, len_range=(200, 700))
+    if kind == "per_tensor":
+        w.k_descale = np.array([1.375], dtype=np.float32)
+        w.v_descale = np.array([0.625], dtype=np.float32)
+    else:
+        w.k_descale = np.linspace(0.5, 2.0, w.h_k).astype(np.float32)
+        w.v_descale = np.linspace(2.0, 0.5, w.h_k).astype(np.float32)
+    check(w)
+
+
+@pytest.mark.parametrize("q_is_e4m3", [False, True])
+def test_pack_unpack_bit_exact(q_is_e4m3):
+    w = syn.make_workload("pack", [50, 60, 70], 5, 3, 4, 16, seed=61, q_is_e4m3=q_is_e4m3)
+    s = DecodeSession(w)
+    from paged_fp8_kv_gb300 import pack_q, unpack_o
+
+    pack_q(s.q_vllm, s.q_packed, 3, 5, 3, 4)
+    torch.cuda.synchronize()
+    ref = pack_q_ref(w.q.view(np.int16) if w.q.dtype == np.uint16 else w.q, 3, 5, 3, 4)
+    np.testing.assert_array_equal(s.q_packed.cpu().numpy(), ref)
+    src = torch.randn(3, 3, 20, 128, device="cuda").to(torch.bfloat16)
+    dst = torch.empty(15, 12, 128, dtype=torch.bfloat16, device="cuda")
+    unpack_o(src, dst, 3, 5, 3, 4)
+    torch.cuda.synchronize()
+    ref_o = unpack_o_ref(src.view(torch.int16).cpu().numpy(), 3, 5, 3, 4)
+    np.testing.assert_array_equal(dst.view(torch.int16).cpu().numpy(), ref_o)
+
+
+def test_unpacked_output_matches_oracle_layout():
+    w = syn.config(4, num_seqs=2, len_range=(300, 600))
+    s = run(w)
+    ref_o, _ = oracle.attention(w)
+    got = s.o_vllm.float().cpu().numpy()
+    ref_v = unpack_o_ref(ref_o, w.num_seqs, w.q_len, w.h_k, w.h_r)
+    assert np.all(np.abs(got - ref_v) <= 2e-2 + 2e-2 * np.abs(ref_v))
