@@ -1,0 +1,470 @@
+"""Benchmark: paged fp8-KV split-KV decode attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mj|reference]
+                    [--config 2] [--variant ...] [--h_r ..] [--q_len ..]
+
+One step = one pass of the decode hot path over one batch: pack Q (q_len >
+1), the decode kernel over every work item, the merge of split sequences,
+unpack O (q_len > 1).  The plan is host work done once per batch shape and
+reported separately (`plan_us`).  Inputs are synthetic (seeded, see
+paged_fp8_kv_gb300/synthetic.py) and already resident in HBM.
+
+`value` is algorithmic bytes per step (KV rows < L, Q, O, LSE, block table,
+work list, descales, split partials written and read) / device time, in
+GB/s, summed over ranks.  L2 is flushed (a 512 MiB write) before every timed
+step, outside the step's CUDA events.
+
+`--impl reference` times the fp64 CPU oracle, the only reference this
+method has, on a bounded sample of the same workload.
+
+With N > 1 (torchrun) every rank runs an independent replica: there is no
+data-path collective; barriers only bracket the timed region.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step and KV GB/s vs GB300 HBM roofline, at 1 GPU"
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mj", choices=["mj", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--variant", default=None)
+    ap.add_argument("--h_r", type=int, default=None)
+    ap.add_argument("--q_len", type=int, default=None)
+    ap.add_argument("--max_splits", type=int, default=None)
+    ap.add_argument("--num_seqs", type=int, default=None, help="smaller batch of the same config (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------- workload
+
+
+def workload(args):
+    from paged_fp8_kv_gb300 import synthetic as syn
+
+    return syn.config(
+        args.config,
+        variant=args.variant,
+        h_r=args.h_r,
+        q_len=args.q_len,
+        max_splits=args.max_splits,
+        num_seqs=args.num_seqs,
+    )
+
+
+def describe(w) -> str:
+    lens = w.seq_lens
+    return (
+        f"{w.name}: b={w.num_seqs}, q_len={w.q_len}, h_k={w.h_k}, h_r={w.h_r}, d={w.head_dim}, "
+        f"PS={w.page_size}, L in [{int(lens.min())},{int(lens.max())}] (sum {int(lens.sum())}), "
+        f"{'causal' if w.causal else 'non-causal'}, Q {'e4m3' if w.q_is_e4m3 else 'bf16'}, KV e4m3"
+    )
+
+
+def algorithmic_bytes(w, plan):
+    """(decode kernel bytes, merge kernel bytes, step bytes): what the method
+    must move, not what a kernel happens to touch."""
+    b, h_k, n_q, d = w.num_seqs, w.h_k, w.n_q, w.head_dim
+    lens = w.seq_lens.astype(np.int64)
+    qb = 1 if w.q_is_e4m3 else 2
+    kv = int(lens.sum()) * h_k * d * 2
+    q = b * h_k * n_q * d * qb
+    o = b * h_k * n_q * d * 2
+    lse = b * h_k * n_q * 4
+    bt = int(np.sum(-(-lens // w.page_size))) * 4
+    meta = plan.num_work * 16 + b * 8 + 3 * b * h_k * 4
+    split = plan.n_splits > 1
+    part_rows = int(plan.n_splits[split].sum()) * h_k * n_q
+    part = part_rows * (4 * d + 8)
+    split_out = int(split.sum()) * h_k * n_q * (2 * d + 4)
+    decode = kv + q + (o + lse - split_out) + bt + meta + part
+    merge = part + split_out + b * 4 if split.any() else 0
+    step = kv + q + o + lse + bt + meta + 2 * part
+    if w.q_len > 1:  # pack reads + writes Q, unpack reads + writes O
+        step += 2 * q + 2 * o
+    return decode, merge, step
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = (
+        "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+        "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+    )
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mj_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f,
+                stderr=subprocess.DEVNULL,
+            )
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record(kernel: str, workload_name: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(PROFILES, "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    entry = rec.get(kernel, {}).get(workload_name)
+    if not entry:
+        return None
+    src = os.path.join(ROOT, "paged_fp8_kv_gb300", "csrc", entry["source"])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return entry["dram_bytes_per_launch"] if sha == entry["source_sha"] else None
+
+
+# --------------------------------------------------------------- GPU arm
+
+
+def run_mj(args, rank, world, local_rank):
+    import torch
+
+    from paged_fp8_kv_gb300.build import build
+    from paged_fp8_kv_gb300.session import DecodeSession
+    from paged_fp8_kv_gb300 import decode_plan
+
+    if rank == 0:
+        build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workload(args)
+    s = DecodeSession(w, device=str(dev))
+    d_bytes, m_bytes, step_bytes = algorithmic_bytes(w, s.plan)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # host plan cost (the plan runs once per batch shape, on the host)
+    t = time.perf_counter()
+    for _ in range(20):
+        decode_plan(s.params, w.seq_lens, sm_count=s.sm_count)
+    plan_us = (time.perf_counter() - t) / 20 * 1e6
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        s.step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for e in [x for row in evs for x in row]:
+        e.record()  # torch creates the CUDA event lazily, at its first record
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)  # L2 flush, outside the step's events
+            sev[i][0].record()
+            s.step(timing_events=evs[i])
+            sev[i][1].record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    decode_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    merge_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in sev]))
+    t_dec = float(np.mean(decode_ms))
+
+    if world > 1:
+        tt = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(tt.item())
+
+    launches = s.launches_per_step() * args.steps
+    e2e = None if args.no_e2e else e2e_measure(args, s, w, step_bytes, dev)
+    clocks = clk.summary()
+    return dict(
+        w=w,
+        s=s,
+        step_ms=step_ms,
+        decode_ms=t_dec,
+        merge_ms=float(np.mean(merge_ms)),
+        d_bytes=d_bytes,
+        m_bytes=m_bytes,
+        step_bytes=step_bytes,
+        plan_us=plan_us,
+        launches=launches,
+        e2e=e2e,
+        clocks=clocks,
+    )
+
+
+def e2e_measure(args, s, w, step_bytes, dev):
+    """Same step through the public API from HOST buffers: host plan, H2D of
+    the step's inputs (Q, seq_lens, block table, work list, n_splits), the
+    step, D2H of O and LSE; host wall clock per step."""
+    import torch
+
+    from paged_fp8_kv_gb300 import decode_plan
+
+    pin = lambda t: t.cpu().pin_memory()
+    q_h = pin(s.q_vllm)
+    sl_h = pin(s.seq_lens)
+    bt_h = pin(s.block_table)
+    o_h = torch.empty(s.o_vllm.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(s.lse.shape, dtype=torch.float32).pin_memory()
+    seq_host = w.seq_lens
+    h2d = q_h.numel() * q_h.element_size() + sl_h.numel() * 4 + bt_h.numel() * 4
+    d2h = o_h.numel() * 2 + lse_h.numel() * 4
+    times = []
+    for i in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        plan = decode_plan(s.params, seq_host, sm_count=s.sm_count)
+        work_h = torch.from_numpy(plan.work).pin_memory()
+        ns_h = torch.from_numpy(plan.n_splits).pin_memory()
+        s.q_vllm.copy_(q_h, non_blocking=True)
+        s.seq_lens.copy_(sl_h, non_blocking=True)
+        s.block_table.copy_(bt_h, non_blocking=True)
+        if s.work.shape == work_h.shape:
+            s.work.copy_(work_h, non_blocking=True)
+        else:
+            s.work = work_h.to(dev, non_blocking=True)
+        s.n_splits.copy_(ns_h, non_blocking=True)
+        s.step()
+        o_h.copy_(s.o_vllm, non_blocking=True)
+        lse_h.copy_(s.lse, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+        h2d_step = h2d + work_h.numel() * 4 + ns_h.numel() * 4
+    t = float(np.mean(times))
+    return {
+        "value": round(step_bytes / t / 1e9, 2),
+        "unit": "GB/s",
+        "us_per_step": round(t * 1e6, 2),
+        "h2d_bytes_per_step": int(h2d_step),
+        "d2h_bytes_per_step": int(d2h),
+    }
+
+
+# ------------------------------------------------------------ CPU oracle
+
+
+def oracle_sample(w, budget_s: float, threads: int = 0, seed: int = 0):
+    """Time the fp64 oracle on random (seq, kv head) units until about
+    budget_s of work; returns (GB/s of algorithmic KV bytes, units, threads)."""
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    order = [(int(b), int(g)) for b in rng.permutation(w.num_seqs) for g in range(w.h_k)]
+    nthreads = threads or (os.cpu_count() or 1)
+    done_bytes, done_t, units_done = 0, 0.0, 0
+    batch = max(1, nthreads)
+    i = 0
+    while i < len(order) and done_t < budget_s:
+        units = order[i : i + batch]
+        i += batch
+        t = time.perf_counter()
+        oracle.attention(w, units=units, threads=nthreads)
+        done_t += time.perf_counter() - t
+        done_bytes += sum(int(w.seq_lens[b]) for b, _ in units) * w.head_dim * 2
+        units_done += len(units)
+        batch = min(batch * 2, 4096)
+    return done_bytes / done_t / 1e9, units_done, nthreads, done_t
+
+
+# ------------------------------------------------------------------ main
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = workload(args)
+        vals, units, nthreads = [], 0, os.cpu_count() or 1
+        for i in range(args.warmup + args.steps):
+            gbs, u, nthreads, _ = oracle_sample(w, budget_s=2.0, seed=i)
+            if i >= args.warmup:
+                vals.append(gbs)
+                units = u
+        v = float(np.mean(vals))
+        line = {
+            "impl": "reference",
+            "metric": METRIC,
+            "value": round(v, 4),
+            "unit": "GB/s",
+            "n_gpus": args.gpus,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": describe(w)},
+            "cpu_baseline": {
+                "value": round(v, 4),
+                "unit": "GB/s",
+                "cores": nthreads,
+                "kind": "oracle",
+                "sample": f"{units} random (seq, kv-head) units per step, ~2 s of fp64 oracle work; GB/s of KV rows read",
+            },
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    r = run_mj(args, rank, world, local_rank)
+    w, s = r["w"], r["s"]
+    peak, peak_src = measured_peaks()
+    achieved = r["d_bytes"] / (r["decode_ms"] * 1e-3) / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        gbs, units, nthreads, secs = oracle_sample(w, budget_s=15.0)
+        cpu = {
+            "value": round(gbs, 4),
+            "unit": "GB/s",
+            "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{units} random (seq, kv-head) units of the same workload, {secs:.1f} s of fp64 oracle work; GB/s of KV rows read",
+        }
+    value = world * r["step_bytes"] / (r["step_ms"] * 1e-3) / 1e9
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(r["step_ms"], 5),
+            "us_per_step": round(r["step_ms"] * 1e3, 2),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": describe(w),
+                "kernel": s.kernel,
+                "max_splits": s.max_splits,
+                "plan": {
+                    "work_items": s.plan.num_work,
+                    "chunk_tiles": s.plan.chunk_tiles,
+                    "max_n_splits": s.plan.max_n_splits,
+                    "ctas_per_sm": s.plan.opts.ctas_per_sm,
+                    "sm_count": s.plan.opts.sm_count,
+                },
+                "l2": "flushed before every step (512 MiB write outside the step events); KV also exceeds L2",
+                "parallelism": f"replicas x{world}",
+                "bytes_per_step": r["step_bytes"],
+                "plan_us": round(r["plan_us"], 2),
+            },
+            "frac_of_8000_gbs": round(value / world / 8000.0, 4),
+            "roofline": {
+                "bound": "hbm",
+                "kernel": s.kernel,
+                "achieved": round(achieved, 2),
+                "peak": peak,
+                "peak_source": peak_src,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": traffic_record(s.kernel, w.name),
+                "algorithmic_bytes_per_launch": r["d_bytes"],
+                "decode_us": round(r["decode_ms"] * 1e3, 2),
+                "merge_us": round(r["merge_ms"] * 1e3, 2),
+            },
+            "cpu_baseline": cpu,
+            "e2e": r["e2e"],
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -309,7 +309,10 @@ def decode_attn(
     a.status = _ptr(status)
     ev_arr = None
     if timing_events is not None:
-        ev_arr = (ctypes.c_void_p * 3)(*[int(e.cuda_event) for e in timing_events])
+        handles = [int(e.cuda_event) for e in timing_events]
+        if len(handles) != 3 or not all(handles):
+            raise ValueError("timing_events: three created CUDA events (record each once first)")
+        ev_arr = (ctypes.c_void_p * 3)(*handles)
         a.timing_events = ctypes.cast(ev_arr, ctypes.c_void_p)
     st = lib().mj_decode_attn(ctypes.byref(params), ctypes.byref(a), _stream_handle(stream))
     _check(st, "mj_decode_attn")
