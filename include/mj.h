@@ -69,11 +69,22 @@ typedef enum { MJ_BF16 = 0, MJ_E4M3 = 1 } mj_dtype;
  *   num_pages   pages in the KV pool
  *   causal      1: causal tail; 0: every query token sees all L keys
  *   q_dtype     mj_dtype of Q (K/V are always e4m3)
- *   max_splits  partial slots per sequence, 1..256 (1 = never split) */
+ *   max_splits  partial slots per sequence, 1..256 (1 = never split)
+ *   kernel      mj_kernel_pref: which decode kernel to run (0 = library's
+ *               choice) */
 typedef struct {
   int32_t num_seqs, q_len, h_k, h_r, head_dim, page_size;
-  int32_t max_blocks, num_pages, causal, q_dtype, max_splits;
+  int32_t max_blocks, num_pages, causal, q_dtype, max_splits, kernel;
 } mj_decode_params;
+
+/* Decode kernel families.  Both compute the same function; the choice only
+ * changes speed (and last-bit rounding).
+ *   MJ_KERNEL_AUTO         the library's choice for the shape
+ *   MJ_KERNEL_CUDA_CORE    fp32 CUDA-core kernel, exact e4m3 dequant in
+ *                          registers, fp32 P
+ *   MJ_KERNEL_TENSOR_CORE  tcgen05 swap-AB kernel: e4m3 K/V tiles straight
+ *                          from TMA into the MMA, Q and P as hi+lo e4m3 */
+typedef enum { MJ_KERNEL_AUTO = 0, MJ_KERNEL_CUDA_CORE = 1, MJ_KERNEL_TENSOR_CORE = 2 } mj_kernel_pref;
 
 /* Plan knobs (source: `plan_split_kv`).  A field left 0 takes the
  * library's value for the kernel mj_decode_attn will launch for these

@@ -31,6 +31,10 @@ MJ_ERR_TIMEOUT = 5
 MJ_BF16 = 0
 MJ_E4M3 = 1
 
+MJ_KERNEL_AUTO = 0
+MJ_KERNEL_CUDA_CORE = 1
+MJ_KERNEL_TENSOR_CORE = 2
+
 
 class MjError(RuntimeError):
     def __init__(self, status: int, what: str):
@@ -53,6 +57,7 @@ class DecodeParams(ctypes.Structure):
             "causal",
             "q_dtype",
             "max_splits",
+            "kernel",
         )
     ]
 
@@ -159,9 +164,10 @@ def make_params(
     q_dtype: int = MJ_BF16,
     max_splits: int = 16,
     head_dim: int = 128,
+    kernel: int = MJ_KERNEL_AUTO,
 ) -> DecodeParams:
     return DecodeParams(
-        num_seqs, q_len, h_k, h_r, head_dim, page_size, max_blocks, num_pages, int(causal), q_dtype, max_splits
+        num_seqs, q_len, h_k, h_r, head_dim, page_size, max_blocks, num_pages, int(causal), q_dtype, max_splits, kernel
     )
 
 

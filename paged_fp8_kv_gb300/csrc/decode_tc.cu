@@ -1,0 +1,741 @@
+// Split-KV paged decode attention on the 5th-generation tensor cores
+// (tcgen05, kind::f8f6f4), swap-AB orientation: the 128 KV rows of a tile
+// are the MMA's M, the NT packed query rows of the CTA are its N.
+//
+// Sources: the "mjolnir/t5_decode.py" page — `decode` kernel (warp roles,
+// paged TMA gather with out-of-range pages read as zeros, masking by select,
+// online softmax with descales folded into the exponent and the -inf guard,
+// lazy O rescale, deferred column sums, final-vs-partial epilogue, P stored
+// as e4m3(p * 448)); the vLLM pull request page on the swap-AB decode kernel
+// (KV slots on M, live heads on N).
+//
+// What this kernel does differently from those designs (GB300-first):
+//  * K and V are never dequantised: the e4m3 tiles the TMA lands in shared
+//    memory are the MMA operands directly (K as a K-major A, V as an
+//    MN-major A for O^T = V^T P).
+//  * A bf16 Q is split once per CTA into two e4m3 parts, x = q * 2^s =
+//    hi + lo with hi = e4m3(x), lo = e4m3(x - hi), and both parts are
+//    multiplied into the same accumulator.  The power-of-two s puts the
+//    tile's largest |q| in [128, 256); hi + lo carries bf16's 8 significant
+//    bits exactly for every |x| >= 2^-2 (smaller values keep an error below
+//    2^-10 in x units).
+//  * P is split the same way, x = 448 p = hi + lo, so the PV product sees
+//    about 8 significant bits of p (bf16-like) instead of e4m3's 4.
+//
+// Roles (192 threads):
+//   warp 0      TMA producer: K and V tiles, one box per KV page.
+//   warp 1      TMEM allocator; lane 0 issues every MMA and commit.
+//   warps 2..5  softmax / correction / epilogue; warp w reads TMEM lanes
+//               32*(w%4).. (TMEM lane = KV row for S, = head-dim row for O).
+//
+// Every mbarrier wait is bounded (wall clock); a role that gives up sets a
+// shared abort flag and writes MJ_ERR_TIMEOUT to the optional status word,
+// the others stop at their next wait, in-flight copies and MMAs are drained
+// (bounded again) and TMEM is freed before the CTA exits.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "mj_device.cuh"
+#include "mj_kernels.h"
+#include "sm100_ptx.cuh"
+
+namespace mj {
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kTileKV = 128;                 // KV rows per tile (MMA M)
+constexpr int kKVTileBytes = kTileKV * 128;  // one K or V tile: 16 KB
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legal wait
+constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
+
+template <int NT>
+struct TcCfg {
+  static constexpr int kStages = NT <= 16 ? 3 : 2;
+  static constexpr int kQBytes = NT * 128;           // one Q part, SW128 K-major
+  static constexpr int kPBytes = NT * kTileKV;       // one P part, MN-major, no swizzle
+  static constexpr int kTmemCols = NT <= 16 ? 64 : (NT <= 32 ? 128 : 256);
+  // shared memory layout (offsets from a 1024-aligned base)
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kStages * kKVTileBytes;
+  static constexpr int kOffQ = 2 * kStages * kKVTileBytes;  // [part][NT][128]
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;          // [buf][part][NT/16][128][16]
+  static constexpr int kOffRed = kOffP + 4 * kPBytes;        // [2][4][NT] floats
+  static constexpr int kOffM = kOffRed + 2 * 4 * NT * 4;     // [2][NT] floats
+  static constexpr int kOffBar = kOffM + 2 * NT * 4;
+  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 64 + 1024;  // + alignment slack
+};
+
+// Thin state shared by the roles.
+struct Bars {
+  uint32_t kfull, vfull, kvempty;  // + stage * 8
+  uint32_t sfull, sfree;           // + buf * 8
+  uint32_t pfull, pfree;           // + buf * 8
+  uint32_t odone, qready, drain;
+};
+
+__device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) {
+  *abort = 1;
+  if (status) atomicExch(status, kStatusTimeout);
+}
+
+// Max over the 32 lanes of NT per-lane values, scattered: on return lane l
+// holds the warp maximum of column l % NT in v[0] (NT in {16, 32}) or of
+// columns l and l + 32 in v[0], v[1] (NT = 64).  Reduce-scatter by halving.
+template <int NT, bool kMax>
+__device__ __forceinline__ void warp_reduce_scatter(float* v, int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  if constexpr (NT == 64) {
+    // fold the upper 32 columns onto lanes' second slot later: reduce the two
+    // halves independently with the 32-column scheme
+    warp_reduce_scatter<32, kMax>(v, lane);
+    warp_reduce_scatter<32, kMax>(v + 32, lane);
+    v[1] = v[32];
+  } else {
+    // width = number of live values; each step halves it
+    int width = NT;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      if (width > 1) {
+        const bool upper = (lane & off) != 0;
+        const int half = width >> 1;
+#pragma unroll
+        for (int i = 0; i < NT / 2; ++i) {
+          if (i < half) {
+            // keep my half, send the other
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            const float got = __shfl_xor_sync(0xffffffffu, send, off);
+            v[i] = op(keep, got);
+          }
+        }
+        width = half;
+      } else {
+        v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
+      }
+    }
+  }
+}
+
+// Column index a lane holds after warp_reduce_scatter<NT> (first slot).
+template <int NT>
+__device__ __forceinline__ int scatter_col(int lane) {
+  // After the halving steps with offsets 16, 8, ..., the lane bits that
+  // chose the upper halves, read most significant first, give the column.
+  if constexpr (NT == 64 || NT == 32) {
+    return ((lane >> 4) & 1) * 16 + ((lane >> 3) & 1) * 8 + ((lane >> 2) & 1) * 4 + ((lane >> 1) & 1) * 2 +
+           (lane & 1);
+  } else {  // NT == 16: four halving steps (16, 8, 4, 2), then a full sum over bit 0
+    return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+  }
+}
+
+template <int NT, bool kQe4m3>
+__global__ void __launch_bounds__(kTcThreads, 2)
+decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
+                 const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
+  using C = TcCfg<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(sm);
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);  // [2][4][NT]
+  float* m_run = reinterpret_cast<float*>(sm + C::kOffM);  // [2][NT]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
+  int* q_shift = reinterpret_cast<int*>(sm + C::kOffMisc + 8);
+  float* amax_red = reinterpret_cast<float*>(sm + C::kOffMisc + 16);  // [4]
+
+  Bars bar;
+  {
+    uint32_t p = sbase + C::kOffBar;
+    bar.kfull = p;
+    p += 8 * C::kStages;
+    bar.vfull = p;
+    p += 8 * C::kStages;
+    bar.kvempty = p;
+    p += 8 * C::kStages;
+    bar.sfull = p;
+    p += 16;
+    bar.sfree = p;
+    p += 16;
+    bar.pfull = p;
+    p += 16;
+    bar.pfree = p;
+    p += 16;
+    bar.odone = p;
+    p += 8;
+    bar.qready = p;
+    p += 8;
+    bar.drain = p;
+  }
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int w_idx = blockIdx.x / n_q_tiles;
+  const int qt = blockIdx.x % n_q_tiles;
+  const int g = blockIdx.y;
+  const int n0 = qt * NT;
+
+  const int4 item = reinterpret_cast<const int4*>(a.work)[w_idx];
+  const int b = item.x, t_begin = item.y, t_end = item.z, slot = item.w;
+  if (t_end <= t_begin) return;  // padding item: uniform exit before any setup
+  const int T = t_end - t_begin;
+  const int L = a.seq_lens[b];
+
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(bar.kfull + 8 * s, 1);
+      ptx::mbar_init(bar.vfull + 8 * s, 1);
+      ptx::mbar_init(bar.kvempty + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(bar.sfull + 8 * s, 1);
+      ptx::mbar_init(bar.sfree + 8 * s, 4);
+      ptx::mbar_init(bar.pfull + 8 * s, 4);
+      ptx::mbar_init(bar.pfree + 8 * s, 1);
+    }
+    ptx::mbar_init(bar.odone, 1);
+    ptx::mbar_init(bar.qready, 1);
+    ptx::mbar_init(bar.drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sbase + C::kOffMisc, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_s = tmem;              // S buffers: columns [0, 2 NT)
+  const uint32_t tmem_o = tmem + 2 * NT;     // O: columns [2 NT, 3 NT)
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Lane j handles page j of each tile: the block-table lookups of a tile
+    // run in parallel, and the next tile's lookups are in flight while this
+    // tile's copies are issued.
+    const int PS = a.page_size;
+    const int ppt = kTileKV / PS;  // pages per tile: 1, 2, 4 or 8
+    const int64_t bt_row = static_cast<int64_t>(b) * a.max_blocks;
+    int valid_pages = (L + PS - 1) / PS;
+    valid_pages = valid_pages < a.max_blocks ? valid_pages : a.max_blocks;
+    auto lookup = [&](int tile) -> int {
+      const int blk = tile * ppt + lane;
+      // pages past the sequence end are read out of range: zeros
+      return (lane < ppt && blk < valid_pages) ? a.block_table[bt_row + blk] : a.num_pages;
+    };
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmap_k);
+      ptx::prefetch_tmap(&tmap_v);
+    }
+    int next_page = lookup(t_begin);
+    int issued = 0;
+    for (int i = 0; i < T; ++i) {
+      const int st = i % C::kStages;
+      if (i >= C::kStages) {
+        const bool got =
+            ptx::mbar_wait_bounded(bar.kvempty + 8 * st, ((i / C::kStages) - 1) & 1, abort_flag, kWaitNs);
+        if (__any_sync(0xffffffffu, !got)) {  // leave the loop together
+          if (lane == 0) set_abort(abort_flag, a.status);
+          break;
+        }
+      }
+      const int page = next_page;
+      if (i + 1 < T) next_page = lookup(t_begin + i + 1);
+      const uint32_t dk = sbase + C::kOffK + st * kKVTileBytes;
+      const uint32_t dv = sbase + C::kOffV + st * kKVTileBytes;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar.kfull + 8 * st, kKVTileBytes);
+        ptx::mbar_arrive_expect_tx(bar.vfull + 8 * st, kKVTileBytes);
+      }
+      __syncwarp();
+      if (lane < ppt) {
+        ptx::tma_load_4d(dk + lane * PS * 128, &tmap_k, bar.kfull + 8 * st, 0, 0, g, page);
+        ptx::tma_load_4d(dv + lane * PS * 128, &tmap_v, bar.vfull + 8 * st, 0, 0, g, page);
+      }
+      issued = i + 1;
+    }
+    if (*abort_flag && lane == 0) {
+      // drain: wait (bounded) for every tile this warp issued to land
+      for (int i = (issued > C::kStages ? issued - C::kStages : 0); i < issued; ++i) {
+        const int st = i % C::kStages;
+        const uint32_t par = (i / C::kStages) & 1;
+        volatile int never = 0;
+        ptx::mbar_wait_bounded(bar.kfull + 8 * st, par, &never, kWaitNs / 4);
+        ptx::mbar_wait_bounded(bar.vfull + 8 * st, par, &never, kWaitNs / 4);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idesc_s = ptx::idesc_e4m3(kTileKV, NT, false, false);  // S = K Q^T
+      const uint32_t idesc_o = ptx::idesc_e4m3(kTileKV, NT, true, true);    // O = V^T P
+      constexpr int kQParts = kQe4m3 ? 1 : 2;
+      bool ok = ptx::mbar_wait_bounded(bar.qready, 0, abort_flag, kWaitNs);
+      auto gemm2 = [&](int j) -> bool {
+        const int st = j % C::kStages;
+        const int pb = j & 1;
+        if (!ptx::mbar_wait_bounded(bar.vfull + 8 * st, (j / C::kStages) & 1, abort_flag, kWaitNs)) return false;
+        if (!ptx::mbar_wait_bounded(bar.pfull + 8 * pb, (j >> 1) & 1, abort_flag, kWaitNs)) return false;
+        ptx::tc_fence_after();
+        const uint32_t v_base = sbase + C::kOffV + st * kKVTileBytes;
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t p_base = sbase + C::kOffP + (pb * 2 + part) * C::kPBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTileKV / 32; ++kk) {
+            // A = V^T: MN-major, 128-byte swizzle, 8-row groups 1024 B apart;
+            // one K step = 32 KV rows = 4 groups.
+            const uint64_t ad = ptx::smem_desc(v_base + kk * 4096, 0, 1024, ptx::kSwizzle128B);
+            // B = P: MN-major, no swizzle, 8-row core matrices 128 B apart
+            // along K, 16-column groups 2048 B apart along N.
+            const uint64_t bd = ptx::smem_desc(p_base + kk * 512, 128, 2048, ptx::kSwizzleNone);
+            ptx::mma_e4m3(tmem_o, ad, bd, idesc_o, (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        ptx::mma_commit(bar.odone);
+        ptx::mma_commit(bar.pfree + 8 * pb);
+        ptx::mma_commit(bar.kvempty + 8 * st);
+        return true;
+      };
+      for (int i = 0; ok && i < T; ++i) {
+        const int st = i % C::kStages;
+        const int sb = i & 1;
+        if (!ptx::mbar_wait_bounded(bar.kfull + 8 * st, (i / C::kStages) & 1, abort_flag, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        if (i >= 2 && !ptx::mbar_wait_bounded(bar.sfree + 8 * sb, ((i >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t k_base = sbase + C::kOffK + st * kKVTileBytes;
+#pragma unroll
+        for (int part = 0; part < kQParts; ++part) {
+          const uint32_t q_base = sbase + C::kOffQ + part * C::kQBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // A = K (K-major, 128-byte swizzle, 8-row groups 1024 B apart);
+            // B = Q part (same layout); one K step = 32 bytes of d.
+            const uint64_t ad = ptx::smem_desc(k_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
+            const uint64_t bd = ptx::smem_desc(q_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
+            ptx::mma_e4m3(tmem_s + sb * NT, ad, bd, idesc_s, (part > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        ptx::mma_commit(bar.sfull + 8 * sb);
+        if (i >= 1 && !gemm2(i - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok) ok = gemm2(T - 1);
+      if (!ok) set_abort(abort_flag, a.status);
+      // every MMA this thread issued has completed once `drain` fires
+      ptx::mma_commit(bar.drain);
+      volatile int never = 0;
+      ptx::mbar_wait_bounded(bar.drain, 0, &never, kWaitNs);
+    }
+  } else {
+    // ------------------------------------------------- softmax warpgroup
+    const int sw = warp - 2;          // 0..3 within the softmax group
+    const int quarter = warp & 3;     // TMEM lane quarter this warp may access
+    const int st_tid = sw * 32 + lane;
+    const int row = quarter * 32 + lane;  // TMEM lane: KV row (S) / d (O)
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    constexpr int kBarSm = 1;         // named barrier id of the softmax group
+
+    const float qd = a.qd[b * a.qd_seq + g * a.qd_head];
+    const float kd = a.kd[b * a.kd_seq + g * a.kd_head];
+    const float vd = a.vd[b * a.vd_seq + g * a.vd_head];
+
+    // ---- Q tile -> shared (e4m3 parts, 128-byte swizzled K-major rows)
+    {
+      // thread -> (row n, 16-byte chunk cc) pairs; NT*8 chunks over 128 threads
+      float amax = 0.f;
+      constexpr int kChunks = NT * 8 / 128;
+      float xv[kChunks][16];
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k) {
+        const int id = k * 128 + st_tid;
+        const int n = id >> 3, cc = id & 7;
+        const int qrow = n0 + n;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) xv[k][e] = 0.f;
+        if (qrow < a.n_q) {
+          const int64_t off = b * a.q_seq + (static_cast<int64_t>(g) * a.n_q + qrow) * kHeadDimDev + cc * 16;
+          if (kQe4m3) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + off);
+            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) e4m3x4_to_f32(w4[wi], &xv[k][wi * 4]);
+          } else {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + off);
+            const uint4 r0 = src[0], r1 = src[1];
+            const uint32_t w8[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) {
+              xv[k][2 * wi] = __uint_as_float(w8[wi] << 16);
+              xv[k][2 * wi + 1] = __uint_as_float(w8[wi] & 0xFFFF0000u);
+            }
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(xv[k][e]));
+      }
+      int shift = 0;
+      if (!kQe4m3) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (lane == 0) amax_red[sw] = amax;
+        ptx::named_bar_sync(kBarSm, 128);
+        amax = fmaxf(fmaxf(amax_red[0], amax_red[1]), fmaxf(amax_red[2], amax_red[3]));
+        if (amax > 0.f) {
+          const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;  // floor(log2) for normals
+          shift = 7 - e;
+          shift = shift > 126 ? 126 : (shift < -126 ? -126 : shift);
+        }
+      }
+      const float qscale = kQe4m3 ? 1.f : ldexpf(1.f, shift);
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k) {
+        const int id = k * 128 + st_tid;
+        const int n = id >> 3, cc = id & 7;
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          uint16_t h01, h23, l01, l23;
+          if (kQe4m3) {
+            h01 = ptx::f32x2_to_e4m3x2(xv[k][4 * wi], xv[k][4 * wi + 1]);
+            h23 = ptx::f32x2_to_e4m3x2(xv[k][4 * wi + 2], xv[k][4 * wi + 3]);
+            l01 = l23 = 0;
+          } else {
+            float x[4], r[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = xv[k][4 * wi + e] * qscale;
+            h01 = ptx::f32x2_to_e4m3x2(x[0], x[1]);
+            h23 = ptx::f32x2_to_e4m3x2(x[2], x[3]);
+            float hf[4];
+            e4m3x4_to_f32(static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16), hf);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) r[e] = x[e] - hf[e];
+            l01 = ptx::f32x2_to_e4m3x2(r[0], r[1]);
+            l23 = ptx::f32x2_to_e4m3x2(r[2], r[3]);
+          }
+          hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
+          lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+        }
+        const int pos = n * 128 + ((cc ^ (n & 7)) << 4);  // 128-byte swizzle
+        *reinterpret_cast<uint4*>(sm + C::kOffQ + pos) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (!kQe4m3)
+          *reinterpret_cast<uint4*>(sm + C::kOffQ + C::kQBytes + pos) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      if (st_tid == 0) *q_shift = shift;
+      // running max starts at -inf
+      if (st_tid < NT) m_run[st_tid] = -INFINITY;
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(kBarSm, 128);
+      if (st_tid == 0) ptx::mbar_arrive(bar.qready);
+    }
+    const int shift = *q_shift;
+    // raw (computed) score -> logit and -> log2 units; 2^-shift undoes the Q scaling
+    const float cta_scale = a.softmax_scale * qd * kd * ldexpf(1.f, -shift);
+    const float c2 = cta_scale * kLog2e;
+
+    float l_thr[NT];
+#pragma unroll
+    for (int c = 0; c < NT; ++c) l_thr[c] = 0.f;
+
+    bool ok = true;
+    const int vis_all = a.causal ? L - a.q_len : L - 1;  // keys every row sees
+    for (int i = 0; i < T; ++i) {
+      const int sb = i & 1;
+      const int j = (t_begin + i) * kTileKV + row;  // this thread's key
+      if (!ptx::mbar_wait_bounded(bar.sfull + 8 * sb, (i >> 1) & 1, abort_flag, kWaitNs)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      float sc[NT];
+#pragma unroll
+      for (int c0 = 0; c0 < NT; c0 += 16) {
+        uint32_t r[16];
+        MJ_TMEM_LD16(tmem_s + lane_off + sb * NT + c0, r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sc[c0 + e] = __uint_as_float(r[e]);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar.sfree + 8 * sb);
+
+      // mask by select (garbage or poison rows never leak)
+      if (j > vis_all) {
+#pragma unroll
+        for (int c = 0; c < NT; ++c) {
+          const int n = n0 + c;
+          int lim = a.causal ? L - a.q_len + n / a.h_r : L - 1;
+          lim = lim < L - 1 ? lim : L - 1;
+          if (j > lim) sc[c] = -INFINITY;
+        }
+      }
+
+      // column max over the 128 rows: reduce-scatter in the warp, then the
+      // four warps through shared memory
+      float* redb = red + sb * 4 * NT;
+      {
+        float v[NT];
+#pragma unroll
+        for (int c = 0; c < NT; ++c) v[c] = sc[c];
+        warp_reduce_scatter<NT, true>(v, lane);
+        const int col = scatter_col<NT>(lane);
+        if (NT == 16) {
+          if ((lane & 1) == 0) redb[sw * NT + col] = v[0];
+        } else {
+          redb[sw * NT + col] = v[0];
+          if (NT == 64) redb[sw * NT + 32 + col] = v[1];
+        }
+      }
+      ptx::named_bar_sync(kBarSm, 128);
+      const float* m_prev = m_run + (i & 1) * NT;
+      float* m_next = m_run + ((i + 1) & 1) * NT;
+      bool moved = false;
+      float m_use[NT], corr[NT];
+#pragma unroll
+      for (int c = 0; c < NT; ++c) {
+        const float t = fmaxf(fmaxf(redb[c], redb[NT + c]), fmaxf(redb[2 * NT + c], redb[3 * NT + c]));
+        const float mp = m_prev[c];
+        const float mn = fmaxf(mp, t);
+        moved |= (mn != mp);
+        m_use[c] = (mn == -INFINITY) ? 0.f : mn;
+      }
+      if (st_tid < NT) {
+        const float t = fmaxf(fmaxf(redb[st_tid], redb[NT + st_tid]), fmaxf(redb[2 * NT + st_tid], redb[3 * NT + st_tid]));
+        m_next[st_tid] = fmaxf(m_prev[st_tid], t);
+      }
+      // probabilities and the deferred row sums
+#pragma unroll
+      for (int c = 0; c < NT; ++c) {
+        const float mp = m_prev[c];
+        const float cf = moved ? fast_exp2((mp - m_use[c]) * c2) : 1.f;
+        const float p = fast_exp2((sc[c] - m_use[c]) * c2);
+        l_thr[c] = fmaf(l_thr[c], cf, p);
+        corr[c] = cf;
+        sc[c] = p;
+      }
+
+      // P buffer i&1 is free once GEMM2(i-2) finished
+      const int pb = i & 1;
+      if (i >= 2 && !ptx::mbar_wait_bounded(bar.pfree + 8 * pb, ((i >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+        ok = false;
+        break;
+      }
+      // split 448 p = hi + lo (e4m3) and store this row's bytes:
+      // part buffer [NT/16 groups][128 rows][16 bytes]
+      uint8_t* p_hi = sm + C::kOffP + (pb * 2 + 0) * C::kPBytes;
+      uint8_t* p_lo = sm + C::kOffP + (pb * 2 + 1) * C::kPBytes;
+#pragma unroll
+      for (int gq = 0; gq < NT / 16; ++gq) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          float x[4], hf[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = sc[gq * 16 + wi * 4 + e] * 448.f;
+          const uint16_t h01 = ptx::f32x2_to_e4m3x2(x[0], x[1]);
+          const uint16_t h23 = ptx::f32x2_to_e4m3x2(x[2], x[3]);
+          hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
+          e4m3x4_to_f32(hw[wi], hf);
+          const uint16_t l01 = ptx::f32x2_to_e4m3x2(x[0] - hf[0], x[1] - hf[1]);
+          const uint16_t l23 = ptx::f32x2_to_e4m3x2(x[2] - hf[2], x[3] - hf[3]);
+          lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+        }
+        const int off = gq * (kTileKV * 16) + row * 16;
+        *reinterpret_cast<uint4*>(p_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(p_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      // rows past the sequence end: zero their V row so 0 * poison cannot
+      // reach O (the TMA landed the whole last page)
+      if (j >= L) {
+        const int st = i % C::kStages;
+        if (!ptx::mbar_wait_bounded(bar.vfull + 8 * st, (i / C::kStages) & 1, abort_flag, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        uint4* vrow = reinterpret_cast<uint4*>(sm + C::kOffV + st * kKVTileBytes + row * 128);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      // lazy O correction: only when some column max moved, after GEMM2(i-1)
+      if (moved && i > 0) {
+        if (!ptx::mbar_wait_bounded(bar.odone, (i - 1) & 1, abort_flag, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+          uint32_t r[16];
+          MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr[c0 + e]);
+          MJ_TMEM_ST16(tmem_o + lane_off + c0, r);
+        }
+        ptx::tmem_st_wait();
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar.pfull + 8 * pb);
+    }
+
+    // ---- epilogue
+    if (ok && !ptx::mbar_wait_bounded(bar.odone, (T - 1) & 1, abort_flag, kWaitNs)) ok = false;
+    if (!ok) {
+      set_abort(abort_flag, a.status);
+    } else {
+      ptx::tc_fence_after();
+      // row sums: reduce over the 128 KV rows
+      float* redl = red;  // reuse buffer 0 after the loop
+      ptx::named_bar_sync(kBarSm, 128);  // everyone is done reading red / m_run
+      {
+        warp_reduce_scatter<NT, false>(l_thr, lane);
+        const int col = scatter_col<NT>(lane);
+        if (NT == 16) {
+          if ((lane & 1) == 0) redl[sw * NT + col] = l_thr[0];
+        } else {
+          redl[sw * NT + col] = l_thr[0];
+          if (NT == 64) redl[sw * NT + 32 + col] = l_thr[1];
+        }
+      }
+      ptx::named_bar_sync(kBarSm, 128);
+      const float* m_fin = m_run + (T & 1) * NT;
+      const int nsp = a.n_splits[b];
+      const bool final_out = nsp <= 1;
+      const float out_scale = vd * (1.f / 448.f);
+      const int d = row;  // TMEM lane of O = head-dim index
+#pragma unroll
+      for (int c0 = 0; c0 < NT; c0 += 16) {
+        uint32_t r[16];
+        MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = c0 + e;
+          const int n = n0 + c;
+          if (n >= a.n_q) break;
+          const float l = redl[c] + redl[NT + c] + redl[2 * NT + c] + redl[3 * NT + c];
+          const float o = __uint_as_float(r[e]) * out_scale;
+          if (final_out) {
+            const int64_t orow = b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + n) * kHeadDimDev;
+            a.o[orow + d] = __float2bfloat16_rn(o * (a.scale_o / (l + 1e-30f)));
+          } else {
+            const int64_t pr = part_row(a, b, g, slot, n);
+            a.o_part[pr * kHeadDimDev + d] = o;
+          }
+        }
+      }
+      if (st_tid < NT && n0 + st_tid < a.n_q) {
+        const int c = st_tid, n = n0 + c;
+        const float l = redl[c] + redl[NT + c] + redl[2 * NT + c] + redl[3 * NT + c];
+        const float m_logit = m_fin[c] * cta_scale;
+        if (final_out) {
+          a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + n] = m_logit + logf(l);
+        } else {
+          const int64_t pr = part_row(a, b, g, slot, n);
+          a.m_part[pr] = m_logit;
+          a.l_part[pr] = l;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// -------------------------------------------------------- host: tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// (d bytes, rows in page, kv heads, pages) view of a paged e4m3 pool; one box
+// is one page of one head: 128 bytes x page_size rows, 128-byte swizzle.
+bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, int num_pages, int64_t s_row,
+                 int64_t s_head, int64_t s_page) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(h_k),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_row), static_cast<cuuint64_t>(s_head),
+                                 static_cast<cuuint64_t>(s_page)};
+  const cuuint32_t box[4] = {128, static_cast<cuuint32_t>(page_size), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int NT, bool kQe4m3>
+cudaError_t launch_tc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page) ||
+      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page))
+    return cudaErrorInvalidValue;
+  const int smem = TcCfg<NT>::kBytes;
+  auto kern = decode_tc_kernel<NT, kQe4m3>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles, a.h_k, 1);
+  kern<<<grid, kTcThreads, smem, stream>>>(a, mk, mv, n_q_tiles);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
+                             cudaStream_t stream) {
+  switch (rows_per_cta) {
+    case 16:
+      return q_e4m3 ? launch_tc<16, true>(a, n_q_tiles, stream) : launch_tc<16, false>(a, n_q_tiles, stream);
+    case 32:
+      return q_e4m3 ? launch_tc<32, true>(a, n_q_tiles, stream) : launch_tc<32, false>(a, n_q_tiles, stream);
+    case 64:
+      return q_e4m3 ? launch_tc<64, true>(a, n_q_tiles, stream) : launch_tc<64, false>(a, n_q_tiles, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+int tc_smem_bytes(int rows_per_cta) {
+  switch (rows_per_cta) {
+    case 16: return TcCfg<16>::kBytes;
+    case 32: return TcCfg<32>::kBytes;
+    case 64: return TcCfg<64>::kBytes;
+    default: return 0;
+  }
+}
+
+}  // namespace mj

@@ -40,18 +40,29 @@ constexpr int kSmemReservedPerCta = 1024;
 
 KernelChoice choose_kernel(const mj_decode_params& p) {
   const int n_q = p.q_len * p.h_r;
-  KernelChoice k{};
-  k.kind = KernelKind::kCudaCore;
-  k.rows_per_cta = n_q <= 4 ? 4 : (n_q <= 8 ? 8 : 16);
-  k.n_q_tiles = (n_q + k.rows_per_cta - 1) / k.rows_per_cta;
-  const int smem = cc_smem_bytes(k.rows_per_cta) + kSmemReservedPerCta;
-  int per_sm = kSmemPerSm / smem;
-  if (per_sm > 16) per_sm = 16;
-  k.ctas_per_sm = per_sm < 1 ? 1 : per_sm;
   const bool e4m3 = p.q_dtype == MJ_E4M3;
-  static const char* names[2][3] = {{"cc_n4_bf16", "cc_n8_bf16", "cc_n16_bf16"},
-                                    {"cc_n4_e4m3", "cc_n8_e4m3", "cc_n16_e4m3"}};
-  k.name = names[e4m3][k.rows_per_cta == 4 ? 0 : (k.rows_per_cta == 8 ? 1 : 2)];
+  KernelChoice k{};
+  int smem;
+  if (p.kernel == MJ_KERNEL_CUDA_CORE) {
+    k.kind = KernelKind::kCudaCore;
+    k.rows_per_cta = n_q <= 4 ? 4 : (n_q <= 8 ? 8 : 16);
+    smem = cc_smem_bytes(k.rows_per_cta);
+    static const char* names[2][3] = {{"cc_n4_bf16", "cc_n8_bf16", "cc_n16_bf16"},
+                                      {"cc_n4_e4m3", "cc_n8_e4m3", "cc_n16_e4m3"}};
+    k.name = names[e4m3][k.rows_per_cta == 4 ? 0 : (k.rows_per_cta == 8 ? 1 : 2)];
+  } else {
+    k.kind = KernelKind::kTensorCore;
+    k.rows_per_cta = n_q <= 16 ? 16 : (n_q <= 32 ? 32 : 64);
+    smem = tc_smem_bytes(k.rows_per_cta);
+    static const char* names[2][3] = {{"tc_n16_bf16", "tc_n32_bf16", "tc_n64_bf16"},
+                                      {"tc_n16_e4m3", "tc_n32_e4m3", "tc_n64_e4m3"}};
+    k.name = names[e4m3][k.rows_per_cta == 16 ? 0 : (k.rows_per_cta == 32 ? 1 : 2)];
+  }
+  k.n_q_tiles = (n_q + k.rows_per_cta - 1) / k.rows_per_cta;
+  int per_sm = kSmemPerSm / (smem + kSmemReservedPerCta);
+  const int cap = k.kind == KernelKind::kTensorCore ? 2 : 16;  // TC: launch bounds / TMEM
+  if (per_sm > cap) per_sm = cap;
+  k.ctas_per_sm = per_sm < 1 ? 1 : per_sm;
   return k;
 }
 
@@ -99,7 +110,7 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   if (!aligned16(a.k) || !aligned16(a.v)) return MJ_ERR_INVALID_ARG;
   const int64_t kv_strides[6] = {a.k_page, a.k_row, a.k_head, a.v_page, a.v_row, a.v_head};
   for (int64_t s : kv_strides)
-    if (s < 0 || (s & 15) != 0) return MJ_ERR_INVALID_ARG;
+    if (s <= 0 || (s & 15) != 0 || s >= (int64_t{1} << 40)) return MJ_ERR_INVALID_ARG;
   const int q_bytes = p.q_dtype == MJ_E4M3 ? 1 : 2;
   if (!aligned16(a.q) || !aligned16(a.o)) return MJ_ERR_INVALID_ARG;
   if (a.q_seq_stride < 0 || ((a.q_seq_stride * q_bytes) & 15) != 0) return MJ_ERR_INVALID_ARG;
@@ -161,6 +172,7 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   d.causal = p.causal;
   d.max_splits = p.max_splits;
   d.num_work = a.num_work;
+  d.num_pages = p.num_pages;
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
@@ -170,7 +182,10 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   const KernelChoice kc = choose_kernel(p);
   cudaError_t e = cudaSuccess;
   if (ev[0] && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return MJ_ERR_CUDA;
-  e = launch_decode_cc(d, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
+  if (kc.kind == KernelKind::kTensorCore)
+    e = launch_decode_tc(d, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
+  else
+    e = launch_decode_cc(d, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
   if (e != cudaSuccess) return MJ_ERR_CUDA;
   if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return MJ_ERR_CUDA;
   if (p.max_splits > 1) {

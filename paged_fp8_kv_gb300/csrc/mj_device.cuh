@@ -32,6 +32,7 @@ struct DecodeDev {
   float* l_part;
   int32_t* status;
   int32_t num_seqs, h_k, n_q, q_len, h_r, page_size, max_blocks, causal, max_splits, num_work;
+  int32_t num_pages;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;

@@ -38,6 +38,7 @@ class DecodeSession:
         force_splits: int = 0,
         pad_to: int = 0,
         kv_layout: str = "nhd",
+        kernel: int = 0,
     ):
         self.w = w
         self.device = torch.device(device)
@@ -59,6 +60,7 @@ class DecodeSession:
             self.q_dtype,
             self.max_splits,
             w.head_dim,
+            kernel,
         )
         self.kernel = kernel_name(self.params)
         if sm_count is None:

@@ -24,6 +24,9 @@ from tests.gpu_helpers import compare, sample_units
 
 pytestmark = pytest.mark.gpu
 
+CC, TC = 1, 2  # MJ_KERNEL_CUDA_CORE, MJ_KERNEL_TENSOR_CORE
+KERNELS = pytest.mark.parametrize("kernel", [CC, TC], ids=["cuda_core", "tensor_core"])
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
@@ -53,98 +56,111 @@ def check(w, units=None, **kw):
 # ------------------------------------------------------------------ configs
 
 
-def test_config1_tiny_full():
+@KERNELS
+def test_config1_tiny_full(kernel):
     w = syn.config(1)
-    s, errs = check(w)
+    s, errs = check(w, kernel=kernel)
     assert s.plan.max_n_splits == 1
 
 
+@KERNELS
 @pytest.mark.parametrize("force", [0, 3])
-def test_config2_small(force):
+def test_config2_small(force, kernel):
     w = syn.config(2, num_seqs=6, len_range=(300, 1500))
-    check(w, force_splits=force)
+    check(w, force_splits=force, kernel=kernel)
 
 
-def test_config2_full_sampled():
+@KERNELS
+def test_config2_full_sampled(kernel):
     w = syn.config(2)
-    s = run(w)
+    s = run(w, kernel=kernel)
     units = sample_units(w, 24, seed=2, include=[(int(np.argmax(w.seq_lens)), 0)])
     compare(w, s.o_host(), s.lse_host(), units=units)
 
 
-def test_config3_small_split_and_merge():
+@KERNELS
+def test_config3_small_split_and_merge(kernel):
     w = syn.config(3, num_seqs=4, len_range=(6000, 500))
-    s, _ = check(w)
+    s, _ = check(w, kernel=kernel)
     assert s.plan.n_splits[0] > 1  # the long sequence is split and merged
 
 
-def test_config3_full_sampled():
+@KERNELS
+def test_config3_full_sampled(kernel):
     w = syn.config(3)
-    s = run(w)
+    s = run(w, kernel=kernel)
     assert s.plan.n_splits[0] > 1
     compare(w, s.o_host(), s.lse_host(), units=[(0, 0), (3, 0), (7, 0)])
 
 
+@KERNELS
 @pytest.mark.parametrize("variant", [None, "noncausal"])
-def test_config4_small(variant):
+def test_config4_small(variant, kernel):
     w = syn.config(4, variant=variant, num_seqs=5, len_range=(200, 1300))
-    check(w)
+    check(w, kernel=kernel)
 
 
-def test_config4_full_sampled():
+@KERNELS
+def test_config4_full_sampled(kernel):
     w = syn.config(4)
-    s = run(w)
+    s = run(w, kernel=kernel)
     units = sample_units(w, 12, seed=4, include=[(int(np.argmax(w.seq_lens)), 7)])
     compare(w, s.o_host(), s.lse_host(), units=units)
 
 
+@KERNELS
 @pytest.mark.parametrize("h_r,q_len", syn.SWEEP_POINTS)
-def test_config5_small(h_r, q_len):
+def test_config5_small(h_r, q_len, kernel):
     w = syn.config(5, h_r=h_r, q_len=q_len, num_seqs=3, len_range=(0, 700))
-    check(w)
+    check(w, kernel=kernel)
 
 
+@KERNELS
 @pytest.mark.parametrize("h_r,q_len", [(16, 1), (32, 16)])
-def test_config5_full_sampled(h_r, q_len):
+def test_config5_full_sampled(h_r, q_len, kernel):
     w = syn.config(5, h_r=h_r, q_len=q_len)
-    s = run(w)
+    s = run(w, kernel=kernel)
     compare(w, s.o_host(), s.lse_host(), units=[(0, 0), (77, 0), (127, 0)])
 
 
 # --------------------------------------------------------------- edge cases
 
 
+@KERNELS
 @pytest.mark.parametrize("q_len,causal", [(1, True), (4, True), (3, False)])
-def test_empty_short_and_aligned_lengths(q_len, causal):
+def test_empty_short_and_aligned_lengths(q_len, causal, kernel):
     lens = [0, 1, 2, 3, 16, 127, 128, 129, 256, 300]
     w = syn.make_workload("edge", lens, q_len, 2, 4, 16, seed=51, causal=causal, max_splits=4)
-    s, _ = check(w, force_splits=2)
+    s, _ = check(w, force_splits=2, kernel=kernel)
     lse = s.lse_host()
     assert np.all(np.isneginf(lse[0]))  # L = 0
     assert np.all(s.o_host()[0] == 0.0)
 
 
-def test_padded_work_list_changes_nothing():
+@KERNELS
+def test_padded_work_list_changes_nothing(kernel):
     w = syn.config(2, num_seqs=5, len_range=(200, 900))
-    a = run(w)
-    b = run(w, pad_to=a.plan.num_work + 37)
+    a = run(w, kernel=kernel)
+    b = run(w, pad_to=a.plan.num_work + 37, kernel=kernel)
     assert b.plan.num_work == a.plan.num_work + 37
     assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
 
 
-def test_workspace_contents_do_not_matter():
+@KERNELS
+def test_workspace_contents_do_not_matter(kernel):
     w = syn.config(3, num_seqs=3, len_range=(3000, 400))
-    a = run(w, nan_workspace=True)
-    b = run(w, nan_workspace=False)
+    a = run(w, nan_workspace=True, kernel=kernel)
+    b = run(w, nan_workspace=False, kernel=kernel)
     b.fill_workspace(1e30)
     b.step()
     torch.cuda.synchronize()
     assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
 
 
-def test_unused_pages_and_table_padding_are_never_read():
+@KERNELS
+def test_unused_pages_and_table_padding_are_never_read(kernel):
     w = syn.config(4, num_seqs=3, len_range=(100, 700))
-    a = run(w)
+    a = run(w, kernel=kernel)
     w2 = copy.deepcopy(w)
     owned = set()
     for bi, L in enumerate(w.seq_lens):
@@ -152,13 +168,14 @@ def test_unused_pages_and_table_padding_are_never_read():
     free = [p for p in range(w.num_pages) if p not in owned]
     w2.k_cache[free] = 0x3F
     w2.v_cache[free] = 0x40
-    b = run(w2)
+    b = run(w2, kernel=kernel)
     assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
 
 
-def test_page_permutation_gives_identical_bytes():
+@KERNELS
+def test_page_permutation_gives_identical_bytes(kernel):
     w = syn.config(2, num_seqs=4, len_range=(300, 800))
-    a = run(w)
+    a = run(w, kernel=kernel)
     w2 = copy.deepcopy(w)
     perm = np.random.default_rng(9).permutation(w.num_pages)
     inv = np.argsort(perm)
@@ -167,13 +184,14 @@ def test_page_permutation_gives_identical_bytes():
     for bi, L in enumerate(w.seq_lens):
         n = -(-int(L) // w.page_size)
         w2.block_table[bi, :n] = inv[w.block_table[bi, :n]]
-    b = run(w2)
+    b = run(w2, kernel=kernel)
     assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
 
 
-def test_determinism_and_graph_replay():
+@KERNELS
+def test_determinism_and_graph_replay(kernel):
     w = syn.config(4, num_seqs=4, len_range=(500, 2000))
-    s = run(w)
+    s = run(w, kernel=kernel)
     o0, l0 = s.o_vllm.clone(), s.lse.clone()
     for _ in range(3):
         s.step()
@@ -189,16 +207,18 @@ def test_determinism_and_graph_replay():
     assert torch.equal(o0, s.o_vllm) and torch.equal(l0, s.lse)
 
 
+@KERNELS
 @pytest.mark.parametrize("layout", ["hnd", "interleaved", "flashinfer"])
-def test_kv_layouts_match_nhd(layout):
+def test_kv_layouts_match_nhd(layout, kernel):
     w = syn.config(4, num_seqs=3, len_range=(200, 900))
-    a = run(w)
-    b = run(w, kv_layout=layout)
+    a = run(w, kernel=kernel)
+    b = run(w, kv_layout=layout, kernel=kernel)
     assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
 
 
+@KERNELS
 @pytest.mark.parametrize("kind", ["per_tensor", "per_head"])
-def test_descale_broadcasts(kind):
+def test_descale_broadcasts(kind, kernel):
     w = syn.config(2, num_seqs=3, len_range=(200, 700))
     if kind == "per_tensor":
         w.k_descale = np.array([1.375], dtype=np.float32)
@@ -206,7 +226,7 @@ def test_descale_broadcasts(kind):
     else:
         w.k_descale = np.linspace(0.5, 2.0, w.h_k).astype(np.float32)
         w.v_descale = np.linspace(2.0, 0.5, w.h_k).astype(np.float32)
-    check(w)
+    check(w, kernel=kernel)
 
 
 @pytest.mark.parametrize("q_is_e4m3", [False, True])
