@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--q_len", type=int, default=None)
     ap.add_argument("--max_splits", type=int, default=None)
     ap.add_argument("--num_seqs", type=int, default=None, help="smaller batch of the same config (profiling)")
+    ap.add_argument("--kv_layout", default="nhd", choices=["nhd", "hnd", "interleaved", "flashinfer"])
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--l2_prefetch", type=int, default=0, help="0 default, -1 off, 1..8 tiles ahead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -210,7 +213,7 @@ def run_mj(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = workload(args)
-    s = DecodeSession(w, device=str(dev))
+    s = DecodeSession(w, device=str(dev), kv_layout=args.kv_layout, kernel=args.kernel, l2_prefetch=args.l2_prefetch)
     d_bytes, m_bytes, step_bytes = algorithmic_bytes(w, s.plan)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -429,6 +432,8 @@ def main():
             "config": {
                 "workload": describe(w),
                 "kernel": s.kernel,
+                "kv_layout": args.kv_layout,
+                "l2_prefetch": args.l2_prefetch,
                 "max_splits": s.max_splits,
                 "plan": {
                     "work_items": s.plan.num_work,

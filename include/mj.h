@@ -71,10 +71,15 @@ typedef enum { MJ_BF16 = 0, MJ_E4M3 = 1 } mj_dtype;
  *   q_dtype     mj_dtype of Q (K/V are always e4m3)
  *   max_splits  partial slots per sequence, 1..256 (1 = never split)
  *   kernel      mj_kernel_pref: which decode kernel to run (0 = library's
- *               choice) */
+ *               choice)
+ *   l2_prefetch tensor-core kernel: KV tiles its producer pulls into L2
+ *               ahead of the shared-memory loads (source: the kernel's
+ *               `l2_prefetch` option on the "mjolnir/t5_decode.py" page);
+ *               0 = library default, -1 = off, 1..8 = distance in tiles */
 typedef struct {
   int32_t num_seqs, q_len, h_k, h_r, head_dim, page_size;
   int32_t max_blocks, num_pages, causal, q_dtype, max_splits, kernel;
+  int32_t l2_prefetch;
 } mj_decode_params;
 
 /* Decode kernel families.  Both compute the same function; the choice only
@@ -146,6 +151,10 @@ size_t mj_decode_workspace_bytes(const mj_decode_params* params);
  *                initialised; may be NULL when max_splits == 1
  *   status       optional device int32, caller-zeroed; kernels that give up
  *                a bounded wait write MJ_ERR_TIMEOUT there; NULL = off
+ *   max_n_splits host hint: the plan's largest n_splits (1 = nothing was
+ *                split: the merge kernel is not launched; it also sizes the
+ *                merge); 0 = unknown (the merge runs, sized for max_splits).
+ *                A value below the true maximum gives wrong results.
  *   timing_events optional: NULL, or 3 cudaEvent_t recorded on `stream`
  *                before the decode kernel, between decode and merge, and
  *                after the merge (instrumentation only) */
@@ -171,6 +180,7 @@ typedef struct {
   void* workspace;
   size_t workspace_bytes;
   int32_t* status;
+  int32_t max_n_splits;
   void* const* timing_events;
 } mj_decode_args;
 

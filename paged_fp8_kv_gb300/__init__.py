@@ -58,6 +58,7 @@ class DecodeParams(ctypes.Structure):
             "q_dtype",
             "max_splits",
             "kernel",
+            "l2_prefetch",
         )
     ]
 
@@ -107,6 +108,7 @@ class DecodeArgs(ctypes.Structure):
         ("workspace", _vp),
         ("workspace_bytes", ctypes.c_size_t),
         ("status", _vp),
+        ("max_n_splits", ctypes.c_int32),
         ("timing_events", _vp),
     ]
 
@@ -165,9 +167,22 @@ def make_params(
     max_splits: int = 16,
     head_dim: int = 128,
     kernel: int = MJ_KERNEL_AUTO,
+    l2_prefetch: int = 0,
 ) -> DecodeParams:
     return DecodeParams(
-        num_seqs, q_len, h_k, h_r, head_dim, page_size, max_blocks, num_pages, int(causal), q_dtype, max_splits, kernel
+        num_seqs,
+        q_len,
+        h_k,
+        h_r,
+        head_dim,
+        page_size,
+        max_blocks,
+        num_pages,
+        int(causal),
+        q_dtype,
+        max_splits,
+        kernel,
+        l2_prefetch,
     )
 
 
@@ -284,6 +299,7 @@ def decode_attn(
     softmax_scale: float,
     scale_o: float = 1.0,
     status=None,
+    max_n_splits: int = 0,
     timing_events=None,
     stream=None,
 ) -> None:
@@ -313,6 +329,7 @@ def decode_attn(
     a.workspace = _ptr(workspace)
     a.workspace_bytes = 0 if workspace is None else int(workspace.numel() * workspace.element_size())
     a.status = _ptr(status)
+    a.max_n_splits = int(max_n_splits)
     ev_arr = None
     if timing_events is not None:
         handles = [int(e.cuda_event) for e in timing_events]

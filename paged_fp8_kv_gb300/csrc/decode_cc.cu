@@ -41,16 +41,18 @@ struct CcSmem {
 
 template <int NT, bool kQe4m3>
 __global__ void __launch_bounds__(kThreads)
-decode_cc_kernel(const DecodeDev a) {
+decode_cc_kernel(const DecodeDev a, int n_q_tiles) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   CcSmem<NT>& sm = *reinterpret_cast<CcSmem<NT>*>(smem_raw);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int w_idx = blockIdx.x;
-  const int n0 = blockIdx.y * NT;
-  const int g = blockIdx.z;
+  // Linear grid, work item outermost (see the tensor-core kernel).
+  const int g = blockIdx.x % a.h_k;
+  const int rest = blockIdx.x / a.h_k;
+  const int n0 = (rest % n_q_tiles) * NT;
+  const int w_idx = rest / n_q_tiles;
 
   const int4 item = reinterpret_cast<const int4*>(a.work)[w_idx];
   const int b = item.x, t_begin = item.y, t_end = item.z, slot = item.w;
@@ -291,8 +293,8 @@ cudaError_t launch_cc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   auto kern = decode_cc_kernel<NT, kQe4m3>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_work, n_q_tiles, a.h_k);
-  kern<<<grid, kThreads, smem, stream>>>(a);
+  dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
+  kern<<<grid, kThreads, smem, stream>>>(a, n_q_tiles);
   return cudaGetLastError();
 }
 

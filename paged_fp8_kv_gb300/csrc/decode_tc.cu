@@ -51,7 +51,11 @@ constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
 
 template <int NT>
 struct TcCfg {
-  static constexpr int kStages = NT <= 16 ? 3 : 2;
+  // ring depth, P buffers and co-resident CTAs, sized so that kMinBlocks
+  // CTAs fit one SM's shared memory (228 KB) and register file
+  static constexpr int kStages = NT <= 16 ? 2 : (NT <= 32 ? 2 : 4);
+  static constexpr int kPBufs = NT <= 16 ? 1 : (NT <= 32 ? 2 : 1);
+  static constexpr int kMinBlocks = NT <= 16 ? 3 : (NT <= 32 ? 2 : 1);
   static constexpr int kQBytes = NT * 128;           // one Q part, SW128 K-major
   static constexpr int kPBytes = NT * kTileKV;       // one P part, MN-major, no swizzle
   static constexpr int kTmemCols = NT <= 16 ? 64 : (NT <= 32 ? 128 : 256);
@@ -60,12 +64,14 @@ struct TcCfg {
   static constexpr int kOffV = kStages * kKVTileBytes;
   static constexpr int kOffQ = 2 * kStages * kKVTileBytes;  // [part][NT][128]
   static constexpr int kOffP = kOffQ + 2 * kQBytes;          // [buf][part][NT/16][128][16]
-  static constexpr int kOffRed = kOffP + 4 * kPBytes;        // [2][4][NT] floats
-  static constexpr int kOffM = kOffRed + 2 * 4 * NT * 4;     // [2][NT] floats
-  static constexpr int kOffBar = kOffM + 2 * NT * 4;
+  static constexpr int kOffRed = kOffP + 2 * kPBufs * kPBytes;  // [4][NT] floats
+  static constexpr int kOffM = kOffRed + 4 * NT * 4;            // [2][NT] running max
+  static constexpr int kOffCorr = kOffM + 2 * NT * 4;           // [NT] correction
+  static constexpr int kOffBar = kOffCorr + NT * 4;
   static constexpr int kNumBars = 3 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  static_assert(kMinBlocks * (kBytes + 1024) <= 233472, "shared memory for kMinBlocks CTAs");
 };
 
 // Thin state shared by the roles.
@@ -133,15 +139,16 @@ __device__ __forceinline__ int scatter_col(int lane) {
 }
 
 template <int NT, bool kQe4m3>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, TcCfg<NT>::kMinBlocks)
 decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
   using C = TcCfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(sm);
-  float* red = reinterpret_cast<float*>(sm + C::kOffRed);  // [2][4][NT]
-  float* m_run = reinterpret_cast<float*>(sm + C::kOffM);  // [2][NT]
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);  // [4][NT]
+  float* m_s = reinterpret_cast<float*>(sm + C::kOffM);      // [2][NT]
+  float* corr_s = reinterpret_cast<float*>(sm + C::kOffCorr);  // [NT]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
   int* q_shift = reinterpret_cast<int*>(sm + C::kOffMisc + 8);
@@ -174,9 +181,13 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int w_idx = blockIdx.x / n_q_tiles;
-  const int qt = blockIdx.x % n_q_tiles;
-  const int g = blockIdx.y;
+  // Linear grid, work item outermost: the plan's longest-first order holds
+  // for the whole launch, and the heads / query tiles of one work item (which
+  // read the same KV pages) run side by side.
+  const int g = blockIdx.x % a.h_k;
+  const int rest = blockIdx.x / a.h_k;
+  const int qt = rest % n_q_tiles;
+  const int w_idx = rest / n_q_tiles;
   const int n0 = qt * NT;
 
   const int4 item = reinterpret_cast<const int4*>(a.work)[w_idx];
@@ -247,6 +258,18 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       }
       const int page = next_page;
       if (i + 1 < T) next_page = lookup(t_begin + i + 1);
+      // L2 prefetch of a tile further ahead: its HBM latency overlaps the
+      // wait for a free stage, and its TMA load later hits L2.
+      const int ahead = i + a.l2_prefetch;
+      if (a.l2_prefetch > 0 && ahead < T && ahead >= (i == 0 ? 1 : 0)) {
+        for (int pf = (i == 0 ? 1 : ahead); pf <= ahead; ++pf) {
+          const int pp = lookup(t_begin + pf);
+          if (lane < ppt && pp < a.num_pages) {
+            ptx::tma_prefetch_l2_4d(&tmap_k, 0, 0, g, pp);
+            ptx::tma_prefetch_l2_4d(&tmap_v, 0, 0, g, pp);
+          }
+        }
+      }
       const uint32_t dk = sbase + C::kOffK + st * kKVTileBytes;
       const uint32_t dv = sbase + C::kOffV + st * kKVTileBytes;
       if (lane == 0) {
@@ -277,63 +300,73 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const uint32_t idesc_o = ptx::idesc_e4m3(kTileKV, NT, true, true);    // O = V^T P
       constexpr int kQParts = kQe4m3 ? 1 : 2;
       bool ok = ptx::mbar_wait_bounded(bar.qready, 0, abort_flag, kWaitNs);
-      auto gemm2 = [&](int j) -> bool {
-        const int st = j % C::kStages;
-        const int pb = j & 1;
-        if (!ptx::mbar_wait_bounded(bar.vfull + 8 * st, (j / C::kStages) & 1, abort_flag, kWaitNs)) return false;
-        if (!ptx::mbar_wait_bounded(bar.pfull + 8 * pb, (j >> 1) & 1, abort_flag, kWaitNs)) return false;
-        ptx::tc_fence_after();
-        const uint32_t v_base = sbase + C::kOffV + st * kKVTileBytes;
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t p_base = sbase + C::kOffP + (pb * 2 + part) * C::kPBytes;
+      // Issue GEMM1 and GEMM2 as their inputs become ready, whichever comes
+      // first: GEMM2(j) must not wait behind the arrival of a later K tile,
+      // or the ring's stages would be released one TMA latency late.
+      int g1 = 0, g2 = 0;
+      uint64_t stall_since = 0;
+      while (ok && g2 < T) {
+        bool progressed = false;
+        if (g1 < T) {
+          const int st = g1 % C::kStages;
+          const int sb = g1 & 1;
+          if (ptx::mbar_test_wait(bar.kfull + 8 * st, (g1 / C::kStages) & 1) &&
+              (g1 < 2 || ptx::mbar_test_wait(bar.sfree + 8 * sb, ((g1 >> 1) - 1) & 1))) {
+            ptx::tc_fence_after();
+            const uint32_t k_base = sbase + C::kOffK + st * kKVTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < kTileKV / 32; ++kk) {
-            // A = V^T: MN-major, 128-byte swizzle, 8-row groups 1024 B apart;
-            // one K step = 32 KV rows = 4 groups.
-            const uint64_t ad = ptx::smem_desc(v_base + kk * 4096, 0, 1024, ptx::kSwizzle128B);
-            // B = P: MN-major, no swizzle, 8-row core matrices 128 B apart
-            // along K, 16-column groups 2048 B apart along N.
-            const uint64_t bd = ptx::smem_desc(p_base + kk * 512, 128, 2048, ptx::kSwizzleNone);
-            ptx::mma_e4m3(tmem_o, ad, bd, idesc_o, (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+            for (int part = 0; part < kQParts; ++part) {
+              const uint32_t q_base = sbase + C::kOffQ + part * C::kQBytes;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                // A = K (K-major, 128-byte swizzle, 8-row groups 1024 B
+                // apart); B = Q part (same layout); one K step = 32 bytes of d.
+                const uint64_t ad = ptx::smem_desc(k_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
+                const uint64_t bd = ptx::smem_desc(q_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
+                ptx::mma_e4m3(tmem_s + sb * NT, ad, bd, idesc_s, (part > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            ptx::mma_commit(bar.sfull + 8 * sb);
+            ++g1;
+            progressed = true;
           }
         }
-        ptx::mma_commit(bar.odone);
-        ptx::mma_commit(bar.pfree + 8 * pb);
-        ptx::mma_commit(bar.kvempty + 8 * st);
-        return true;
-      };
-      for (int i = 0; ok && i < T; ++i) {
-        const int st = i % C::kStages;
-        const int sb = i & 1;
-        if (!ptx::mbar_wait_bounded(bar.kfull + 8 * st, (i / C::kStages) & 1, abort_flag, kWaitNs)) {
-          ok = false;
-          break;
-        }
-        if (i >= 2 && !ptx::mbar_wait_bounded(bar.sfree + 8 * sb, ((i >> 1) - 1) & 1, abort_flag, kWaitNs)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t k_base = sbase + C::kOffK + st * kKVTileBytes;
+        if (g2 < g1) {
+          const int st = g2 % C::kStages;
+          const int pb = g2 % C::kPBufs;
+          if (ptx::mbar_test_wait(bar.pfull + 8 * pb, (g2 / C::kPBufs) & 1) &&
+              ptx::mbar_test_wait(bar.vfull + 8 * st, (g2 / C::kStages) & 1)) {
+            ptx::tc_fence_after();
+            const uint32_t v_base = sbase + C::kOffV + st * kKVTileBytes;
 #pragma unroll
-        for (int part = 0; part < kQParts; ++part) {
-          const uint32_t q_base = sbase + C::kOffQ + part * C::kQBytes;
+            for (int part = 0; part < 2; ++part) {
+              const uint32_t p_base = sbase + C::kOffP + (pb * 2 + part) * C::kPBytes;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // A = K (K-major, 128-byte swizzle, 8-row groups 1024 B apart);
-            // B = Q part (same layout); one K step = 32 bytes of d.
-            const uint64_t ad = ptx::smem_desc(k_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
-            const uint64_t bd = ptx::smem_desc(q_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
-            ptx::mma_e4m3(tmem_s + sb * NT, ad, bd, idesc_s, (part > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kTileKV / 32; ++kk) {
+                // A = V^T: MN-major, 128-byte swizzle, 8-row groups 1024 B
+                // apart; one K step = 32 KV rows = 4 groups.  B = P: MN-major,
+                // no swizzle, 8-row core matrices 128 B apart along K,
+                // 16-column groups 2048 B apart along N.
+                const uint64_t ad = ptx::smem_desc(v_base + kk * 4096, 0, 1024, ptx::kSwizzle128B);
+                const uint64_t bd = ptx::smem_desc(p_base + kk * 512, 128, 2048, ptx::kSwizzleNone);
+                ptx::mma_e4m3(tmem_o, ad, bd, idesc_o, (g2 > 0 || part > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            ptx::mma_commit(bar.odone);
+            ptx::mma_commit(bar.pfree + 8 * pb);
+            ptx::mma_commit(bar.kvempty + 8 * st);
+            ++g2;
+            progressed = true;
           }
         }
-        ptx::mma_commit(bar.sfull + 8 * sb);
-        if (i >= 1 && !gemm2(i - 1)) {
-          ok = false;
-          break;
+        if (progressed) {
+          stall_since = 0;
+        } else {
+          const uint64_t now = ptx::globaltimer_ns();
+          if (stall_since == 0) stall_since = now;
+          if (*abort_flag || now - stall_since > kWaitNs) ok = false;
         }
       }
-      if (ok) ok = gemm2(T - 1);
       if (!ok) set_abort(abort_flag, a.status);
       // every MMA this thread issued has completed once `drain` fires
       ptx::mma_commit(bar.drain);
@@ -435,8 +468,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           *reinterpret_cast<uint4*>(sm + C::kOffQ + C::kQBytes + pos) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
       if (st_tid == 0) *q_shift = shift;
-      // running max starts at -inf
-      if (st_tid < NT) m_run[st_tid] = -INFINITY;
+      if (st_tid < NT) m_s[st_tid] = -INFINITY;  // running max starts at -inf
       ptx::fence_proxy_async_smem();
       ptx::named_bar_sync(kBarSm, 128);
       if (st_tid == 0) ptx::mbar_arrive(bar.qready);
@@ -446,9 +478,10 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     const float cta_scale = a.softmax_scale * qd * kd * ldexpf(1.f, -shift);
     const float c2 = cta_scale * kLog2e;
 
-    float l_thr[NT];
+    float l_thr[NT];  // deferred row sums
 #pragma unroll
     for (int c = 0; c < NT; ++c) l_thr[c] = 0.f;
+    int mb = 0;  // which half of m_s holds the running column max (raw units)
 
     bool ok = true;
     const int vis_all = a.causal ? L - a.q_len : L - 1;  // keys every row sees
@@ -461,76 +494,122 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       }
       ptx::tc_fence_after();
       float sc[NT];
+      // S row of this thread's key, masked by select (garbage or poison
+      // rows never leak)
+      auto load_s = [&]() {
 #pragma unroll
-      for (int c0 = 0; c0 < NT; c0 += 16) {
-        uint32_t r[16];
-        MJ_TMEM_LD16(tmem_s + lane_off + sb * NT + c0, r);
-        ptx::tmem_ld_wait();
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+          uint32_t r[16];
+          MJ_TMEM_LD16(tmem_s + lane_off + sb * NT + c0, r);
+          ptx::tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sc[c0 + e] = __uint_as_float(r[e]);
+          for (int e = 0; e < 16; ++e) sc[c0 + e] = __uint_as_float(r[e]);
+        }
+        if (j > vis_all) {
+#pragma unroll
+          for (int c = 0; c < NT; ++c) {
+            const int n = n0 + c;
+            int lim = a.causal ? L - a.q_len + n / a.h_r : L - 1;
+            lim = lim < L - 1 ? lim : L - 1;
+            if (j > lim) sc[c] = -INFINITY;
+          }
+        }
+      };
+      load_s();
+
+      // Running maximum (shared, identical for every thread): only when some
+      // row sees a score above it (one barrier-reduction answers that for
+      // the group) are the column maxima reduced: reduce-scatter in the
+      // warp, the four warps through shared memory, then thread c updates
+      // column c.  Otherwise the stage needs no exchange at all.
+      const float* m_now = m_s + mb * NT;
+      bool exceed = false;
+#pragma unroll
+      for (int c4 = 0; c4 < NT; c4 += 4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(m_now + c4);
+        exceed |= (sc[c4] > m4.x) | (sc[c4 + 1] > m4.y) | (sc[c4 + 2] > m4.z) | (sc[c4 + 3] > m4.w);
+      }
+      bool moved = false;
+      if (ptx::named_bar_red_or(kBarSm, 128, exceed)) {
+        warp_reduce_scatter<NT, true>(sc, lane);  // in place; S is read again below
+        const int col = scatter_col<NT>(lane);
+        if (NT == 16) {
+          if ((lane & 1) == 0) red[sw * NT + col] = sc[0];
+        } else {
+          red[sw * NT + col] = sc[0];
+          if (NT == 64) red[sw * NT + 32 + col] = sc[1];
+        }
+        ptx::named_bar_sync(kBarSm, 128);
+        bool moved_c = false;
+        if (st_tid < NT) {
+          const int c = st_tid;
+          const float t = fmaxf(fmaxf(red[c], red[NT + c]), fmaxf(red[2 * NT + c], red[3 * NT + c]));
+          const float mo = m_now[c];
+          const float mn = fmaxf(mo, t);
+          moved_c = mn != mo;
+          // corr = 2^((m_old - m_use) c2); the -inf guard makes it 0 for a
+          // column that had seen no key
+          const float mu = (mn == -INFINITY) ? 0.f : mn;
+          corr_s[c] = fast_exp2((mo - mu) * c2);
+          m_s[(mb ^ 1) * NT + c] = mn;
+        }
+        moved = ptx::named_bar_red_or(kBarSm, 128, moved_c);
+        mb ^= 1;
+        if (moved) {
+#pragma unroll
+          for (int c4 = 0; c4 < NT; c4 += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(corr_s + c4);
+            l_thr[c4] *= f.x;
+            l_thr[c4 + 1] *= f.y;
+            l_thr[c4 + 2] *= f.z;
+            l_thr[c4 + 3] *= f.w;
+          }
+        }
+        load_s();
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar.sfree + 8 * sb);
-
-      // mask by select (garbage or poison rows never leak)
-      if (j > vis_all) {
-#pragma unroll
-        for (int c = 0; c < NT; ++c) {
-          const int n = n0 + c;
-          int lim = a.causal ? L - a.q_len + n / a.h_r : L - 1;
-          lim = lim < L - 1 ? lim : L - 1;
-          if (j > lim) sc[c] = -INFINITY;
+      // lazy O correction: only when some column max moved, after GEMM2(i-1)
+      if (moved && i > 0) {
+        if (!ptx::mbar_wait_bounded(bar.odone, (i - 1) & 1, abort_flag, kWaitNs)) {
+          ok = false;
+          break;
         }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+          uint32_t r[16];
+          MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr_s[c0 + e]);
+          MJ_TMEM_ST16(tmem_o + lane_off + c0, r);
+        }
+        ptx::tmem_st_wait();
       }
-
-      // column max over the 128 rows: reduce-scatter in the warp, then the
-      // four warps through shared memory
-      float* redb = red + sb * 4 * NT;
+      // probabilities and the deferred row sums; the -inf guard uses 0 as
+      // the reference of a column that has seen no key yet
       {
-        float v[NT];
+        const float* m_new = m_s + mb * NT;
 #pragma unroll
-        for (int c = 0; c < NT; ++c) v[c] = sc[c];
-        warp_reduce_scatter<NT, true>(v, lane);
-        const int col = scatter_col<NT>(lane);
-        if (NT == 16) {
-          if ((lane & 1) == 0) redb[sw * NT + col] = v[0];
-        } else {
-          redb[sw * NT + col] = v[0];
-          if (NT == 64) redb[sw * NT + 32 + col] = v[1];
+        for (int c4 = 0; c4 < NT; c4 += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(m_new + c4);
+          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float m_use = (mm[e] == -INFINITY) ? 0.f : mm[e];
+            const float p = fast_exp2(fmaf(sc[c4 + e], c2, -m_use * c2));
+            l_thr[c4 + e] += p;
+            sc[c4 + e] = p;
+          }
         }
       }
-      ptx::named_bar_sync(kBarSm, 128);
-      const float* m_prev = m_run + (i & 1) * NT;
-      float* m_next = m_run + ((i + 1) & 1) * NT;
-      bool moved = false;
-      float m_use[NT], corr[NT];
-#pragma unroll
-      for (int c = 0; c < NT; ++c) {
-        const float t = fmaxf(fmaxf(redb[c], redb[NT + c]), fmaxf(redb[2 * NT + c], redb[3 * NT + c]));
-        const float mp = m_prev[c];
-        const float mn = fmaxf(mp, t);
-        moved |= (mn != mp);
-        m_use[c] = (mn == -INFINITY) ? 0.f : mn;
-      }
-      if (st_tid < NT) {
-        const float t = fmaxf(fmaxf(redb[st_tid], redb[NT + st_tid]), fmaxf(redb[2 * NT + st_tid], redb[3 * NT + st_tid]));
-        m_next[st_tid] = fmaxf(m_prev[st_tid], t);
-      }
-      // probabilities and the deferred row sums
-#pragma unroll
-      for (int c = 0; c < NT; ++c) {
-        const float mp = m_prev[c];
-        const float cf = moved ? fast_exp2((mp - m_use[c]) * c2) : 1.f;
-        const float p = fast_exp2((sc[c] - m_use[c]) * c2);
-        l_thr[c] = fmaf(l_thr[c], cf, p);
-        corr[c] = cf;
-        sc[c] = p;
-      }
 
-      // P buffer i&1 is free once GEMM2(i-2) finished
-      const int pb = i & 1;
-      if (i >= 2 && !ptx::mbar_wait_bounded(bar.pfree + 8 * pb, ((i >> 1) - 1) & 1, abort_flag, kWaitNs)) {
+      // the P buffer is free once GEMM2 of the tile that last used it finished
+      const int pb = i % C::kPBufs;
+      if (i >= C::kPBufs &&
+          !ptx::mbar_wait_bounded(bar.pfree + 8 * pb, ((i / C::kPBufs) - 1) & 1, abort_flag, kWaitNs)) {
         ok = false;
         break;
       }
@@ -570,24 +649,6 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
         for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
       }
-      // lazy O correction: only when some column max moved, after GEMM2(i-1)
-      if (moved && i > 0) {
-        if (!ptx::mbar_wait_bounded(bar.odone, (i - 1) & 1, abort_flag, kWaitNs)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < NT; c0 += 16) {
-          uint32_t r[16];
-          MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr[c0 + e]);
-          MJ_TMEM_ST16(tmem_o + lane_off + c0, r);
-        }
-        ptx::tmem_st_wait();
-      }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
@@ -613,8 +674,8 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           if (NT == 64) redl[sw * NT + 32 + col] = l_thr[1];
         }
       }
+      const float* m_fin = m_s + mb * NT;
       ptx::named_bar_sync(kBarSm, 128);
-      const float* m_fin = m_run + (T & 1) * NT;
       const int nsp = a.n_splits[b];
       const bool final_out = nsp <= 1;
       const float out_scale = vd * (1.f / 448.f);
@@ -708,7 +769,7 @@ cudaError_t launch_tc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   auto kern = decode_tc_kernel<NT, kQe4m3>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles, a.h_k, 1);
+  dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
   kern<<<grid, kTcThreads, smem, stream>>>(a, mk, mv, n_q_tiles);
   return cudaGetLastError();
 }
@@ -726,6 +787,15 @@ cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles
       return q_e4m3 ? launch_tc<64, true>(a, n_q_tiles, stream) : launch_tc<64, false>(a, n_q_tiles, stream);
     default:
       return cudaErrorInvalidValue;
+  }
+}
+
+int tc_min_blocks(int rows_per_cta) {
+  switch (rows_per_cta) {
+    case 16: return TcCfg<16>::kMinBlocks;
+    case 32: return TcCfg<32>::kMinBlocks;
+    case 64: return TcCfg<64>::kMinBlocks;
+    default: return 1;
   }
 }
 

@@ -33,6 +33,7 @@ WorkspaceLayout workspace_layout(const mj_decode_params& p) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kDefaultL2Prefetch = 0;  // tiles; measured choice
 constexpr int kSmemPerSm = 233472;  // 228 KiB usable shared memory per SM
 constexpr int kSmemReservedPerCta = 1024;
 
@@ -60,7 +61,7 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
   }
   k.n_q_tiles = (n_q + k.rows_per_cta - 1) / k.rows_per_cta;
   int per_sm = kSmemPerSm / (smem + kSmemReservedPerCta);
-  const int cap = k.kind == KernelKind::kTensorCore ? 2 : 16;  // TC: launch bounds / TMEM
+  const int cap = k.kind == KernelKind::kTensorCore ? tc_min_blocks(k.rows_per_cta) : 16;
   if (per_sm > cap) per_sm = cap;
   k.ctas_per_sm = per_sm < 1 ? 1 : per_sm;
   return k;
@@ -119,6 +120,7 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   for (int64_t s : d_strides)
     if (s < 0) return MJ_ERR_INVALID_ARG;
   if (!(a.softmax_scale > 0.f) || !(a.scale_o == a.scale_o)) return MJ_ERR_INVALID_ARG;
+  if (a.max_n_splits < 0 || a.max_n_splits > p.max_splits) return MJ_ERR_INVALID_ARG;
   const WorkspaceLayout ws = workspace_layout(p);
   if (ws.total > 0) {
     if (!a.workspace) return MJ_ERR_INVALID_ARG;
@@ -173,6 +175,7 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   d.max_splits = p.max_splits;
   d.num_work = a.num_work;
   d.num_pages = p.num_pages;
+  d.l2_prefetch = p.l2_prefetch == 0 ? kDefaultL2Prefetch : (p.l2_prefetch < 0 ? 0 : p.l2_prefetch);
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
@@ -188,8 +191,9 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
     e = launch_decode_cc(d, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
   if (e != cudaSuccess) return MJ_ERR_CUDA;
   if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return MJ_ERR_CUDA;
-  if (p.max_splits > 1) {
-    e = launch_merge(d, stream);
+  const int merge_splits = a.max_n_splits == 0 ? p.max_splits : a.max_n_splits;
+  if (p.max_splits > 1 && merge_splits > 1) {
+    e = launch_merge(d, merge_splits, stream);
     if (e != cudaSuccess) return MJ_ERR_CUDA;
   }
   if (ev[2] && cudaEventRecord(ev[2], stream) != cudaSuccess) return MJ_ERR_CUDA;

@@ -19,9 +19,11 @@ int cc_smem_bytes(int rows_per_cta);
 cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
                              cudaStream_t stream);
 int tc_smem_bytes(int rows_per_cta);
+int tc_min_blocks(int rows_per_cta);  // co-resident CTAs per SM the kernel is built for
 
-// Merge of split sequences' partials into O / LSE.
-cudaError_t launch_merge(const DecodeDev& a, cudaStream_t stream);
+// Merge of split sequences' partials into O / LSE; max_n_splits (> 1) sizes
+// the number of warps that share one row.
+cudaError_t launch_merge(const DecodeDev& a, int max_n_splits, cudaStream_t stream);
 
 // Layout permutations (vLLM <-> packed rows).
 cudaError_t launch_permute_rows(const void* src, void* dst, int elem_bytes, int num_seqs, int q_len,

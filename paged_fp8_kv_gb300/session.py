@@ -39,6 +39,7 @@ class DecodeSession:
         pad_to: int = 0,
         kv_layout: str = "nhd",
         kernel: int = 0,
+        l2_prefetch: int = 0,
     ):
         self.w = w
         self.device = torch.device(device)
@@ -61,6 +62,7 @@ class DecodeSession:
             self.max_splits,
             w.head_dim,
             kernel,
+            l2_prefetch,
         )
         self.kernel = kernel_name(self.params)
         if sm_count is None:
@@ -147,6 +149,7 @@ class DecodeSession:
             softmax_scale=self.w.softmax_scale,
             scale_o=self.w.scale_o,
             status=status,
+            max_n_splits=self.plan.max_n_splits,
             timing_events=timing_events,
             stream=stream,
         )
@@ -160,7 +163,7 @@ class DecodeSession:
             unpack_o(self.o_packed, self.o_vllm, self.num_seqs, self.q_len, self.h_k, self.h_r, stream=stream)
 
     def launches_per_step(self) -> int:
-        n = 1 + (1 if self.max_splits > 1 else 0)
+        n = 1 + (1 if self.plan.max_n_splits > 1 else 0)
         return n + (2 if self.q_len > 1 else 0)
 
     # host copies of the outputs, packed (b, h_k, n_q, d) / (b, h_k, n_q)

@@ -146,6 +146,27 @@ def test_padded_work_list_changes_nothing(kernel):
     assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
 
 
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_merge_hint_unknown_gives_same_bytes(cfg):
+    w = syn.config(cfg, num_seqs=3, len_range=(3000, 400) if cfg == 3 else (0, 3000))
+    a = run(w)
+    assert a.plan.max_n_splits > 1
+    b = DecodeSession(w)
+    from paged_fp8_kv_gb300 import decode_attn
+
+    decode_attn(
+        b.params, q=b.q_packed, k_cache=b.k_cache, v_cache=b.v_cache, block_table=b.block_table,
+        seq_lens=b.seq_lens, work=b.work, n_splits=b.n_splits, q_descale=b.q_descale, k_descale=b.k_descale,
+        v_descale=b.v_descale, o=b.o_packed, lse=b.lse, workspace=b.workspace, softmax_scale=w.softmax_scale,
+        scale_o=w.scale_o, max_n_splits=0,
+    )
+    torch.cuda.synchronize()
+    # the hint sizes the merge (warps per row), which may change the
+    # summation order of merged rows: equal up to fp32 rounding
+    torch.testing.assert_close(a.o_packed.float(), b.o_packed.float(), rtol=1e-2, atol=1e-6)
+    torch.testing.assert_close(a.lse, b.lse, rtol=1e-6, atol=1e-6)
+
+
 @KERNELS
 def test_workspace_contents_do_not_matter(kernel):
     w = syn.config(3, num_seqs=3, len_range=(3000, 400))
