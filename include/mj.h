@@ -193,6 +193,30 @@ typedef struct {
 mj_status mj_decode_attn(const mj_decode_params* params, const mj_decode_args* args,
                          mj_stream_t stream);
 
+/* Size of the fixed device scratch behind mj_decode_attn_static_ws. */
+#define MJ_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
+
+/* Same as mj_decode_attn, but without a caller workspace: the split partials
+ * go to a fixed MJ_STATIC_WORKSPACE_BYTES device array inside the library,
+ * so the call allocates nothing.  (The source pages have no counterpart;
+ * this serves callers that may not allocate device memory at call time, such
+ * as runtimes that give the whole device to their own arena or plugins in a
+ * framework that owns the allocator.)
+ *   - args->workspace / workspace_bytes are ignored; everything else is as
+ *     for mj_decode_attn.
+ *   - Problems whose mj_decode_workspace_bytes exceeds the array return
+ *     MJ_ERR_CAPACITY before anything is launched.
+ *   - The array is looked up once per device, on the first call made with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array and nothing in it needs to
+ *     start at zero (every partial is written before it is read); calls whose
+ *     kernels overlap on the GPU (different streams without ordering) race on
+ *     it and must be serialised by the caller.
+ *   - Each GPU that loads the library keeps the array until the process
+ *     exits. */
+mj_status mj_decode_attn_static_ws(const mj_decode_params* params, const mj_decode_args* args,
+                                   mj_stream_t stream);
+
 /* vLLM query layout (num_seqs*q_len, h_k*h_r, d) -> packed (num_seqs, h_k,
  * q_len*h_r, d), row n = qi*h_r + hr (source: `pack_q`).  Both device,
  * contiguous, must not overlap; elem_bytes is 2 (bf16) or 1 (e4m3). */
