@@ -1,6 +1,7 @@
 // Split-KV paged decode attention on the 5th-generation tensor cores
 // (tcgen05, kind::f8f6f4), swap-AB orientation: the 128 KV rows of a tile
-// are the MMA's M, the NT packed query rows of the CTA are its N.
+// are the MMA's M, the R packed query rows of the CTA (twice, as hi and lo
+// parts) are its N.
 //
 // Sources: the "mjolnir/t5_decode.py" page — `decode` kernel (warp roles,
 // paged TMA gather with out-of-range pages read as zeros, masking by select,
@@ -21,6 +22,9 @@
 //    2^-10 in x units).
 //  * P is split the same way, x = 448 p = hi + lo, so the PV product sees
 //    about 8 significant bits of p (bf16-like) instead of e4m3's 4.
+//  * The hi and lo parts are stacked along the MMA's N (Q: 2R rows of B;
+//    P: 2R columns of B) so each K step is one MMA; their products land in
+//    accumulator columns c and R + c, which the softmax / epilogue add.
 //
 // Roles (192 threads):
 //   warp 0      TMA producer: K and V tiles, one box per KV page.
@@ -49,37 +53,48 @@ constexpr int kKVTileBytes = kTileKV * 128;  // one K or V tile: 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legal wait
 constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
 
-template <int NT>
+constexpr int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// Shape constants of one instance: R packed query rows per CTA.
+//   GEMM1 B operand (Q): kN1 rows = [hi rows | lo rows] for bf16 Q (2R), the
+//     e4m3 codes for e4m3 Q (R, at least 16 as the MMA requires).
+//   GEMM2 B operand (P): kN2 = 2R columns = [hi columns | lo columns].
+// The hi and lo parts share one MMA per K step; their products land in
+// separate accumulator columns (c and R + c) that the softmax adds.
+template <int R, bool kQe4m3>
 struct TcCfg {
-  // ring depth, P buffers and co-resident CTAs, sized so that kMinBlocks
-  // CTAs fit one SM's shared memory (228 KB) and register file
-  static constexpr int kStages = NT <= 16 ? 2 : (NT <= 32 ? 2 : 4);
-  static constexpr int kPBufs = NT <= 16 ? 1 : (NT <= 32 ? 2 : 1);
-  static constexpr int kMinBlocks = NT <= 16 ? 3 : (NT <= 32 ? 2 : 1);
-  static constexpr int kQBytes = NT * 128;           // one Q part, SW128 K-major
-  static constexpr int kPBytes = NT * kTileKV;       // one P part, MN-major, no swizzle
-  static constexpr int kTmemCols = NT <= 16 ? 64 : (NT <= 32 ? 128 : 256);
+  static constexpr int kN1 = kQe4m3 ? (R < 16 ? 16 : R) : 2 * R;
+  static constexpr int kN2 = 2 * R;
+  static constexpr int kStages = R <= 32 ? 2 : 5;
+  static constexpr int kMinBlocks = R <= 16 ? 3 : (R <= 32 ? 2 : 1);
+  static constexpr int kQBytes = kN1 * 128;    // SW128 K-major rows
+  static constexpr int kPBytes = kN2 * kTileKV;  // MN-major, no swizzle
+  static constexpr int kTmemCols = pow2_at_least(2 * kN1 + kN2);
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kStages * kKVTileBytes;
-  static constexpr int kOffQ = 2 * kStages * kKVTileBytes;  // [part][NT][128]
-  static constexpr int kOffP = kOffQ + 2 * kQBytes;          // [buf][part][NT/16][128][16]
-  static constexpr int kOffRed = kOffP + 2 * kPBufs * kPBytes;  // [4][NT] floats
-  static constexpr int kOffM = kOffRed + 4 * NT * 4;            // [2][NT] running max
-  static constexpr int kOffCorr = kOffM + 2 * NT * 4;           // [NT] correction
-  static constexpr int kOffBar = kOffCorr + NT * 4;
-  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+  static constexpr int kOffQ = 2 * kStages * kKVTileBytes;
+  static constexpr int kOffP = kOffQ + kQBytes;       // [kN2/16 groups][128 rows][16 B]
+  static constexpr int kOffRed = kOffP + kPBytes;      // [4][R] floats
+  static constexpr int kOffM = kOffRed + 4 * R * 4;    // [2][R] running max
+  static constexpr int kOffCorr = kOffM + 2 * R * 4;   // [R] correction
+  static constexpr int kOffBar = kOffCorr + R * 4;
+  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 1 + 1 + 1 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  static_assert(kN1 % 16 == 0 && kN1 <= 256 && kN2 % 16 == 0 && kN2 <= 256, "MMA N");
+  static_assert(kMinBlocks * kTmemCols <= 512, "TMEM for kMinBlocks CTAs");
   static_assert(kMinBlocks * (kBytes + 1024) <= 233472, "shared memory for kMinBlocks CTAs");
 };
 
-// Thin state shared by the roles.
 struct Bars {
   uint32_t kfull, vfull, kvempty;  // + stage * 8
   uint32_t sfull, sfree;           // + buf * 8
-  uint32_t pfull, pfree;           // + buf * 8
-  uint32_t odone, qready, drain;
+  uint32_t pfull, pfree, odone, qready, drain;
 };
 
 __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) {
@@ -87,34 +102,30 @@ __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) 
   if (status) atomicExch(status, kStatusTimeout);
 }
 
-// Max over the 32 lanes of NT per-lane values, scattered: on return lane l
-// holds the warp maximum of column l % NT in v[0] (NT in {16, 32}) or of
-// columns l and l + 32 in v[0], v[1] (NT = 64).  Reduce-scatter by halving.
-template <int NT, bool kMax>
+// Reduces R per-lane values over the 32 lanes (max or sum), scattered by
+// recursive halving: each step keeps half of the live values and adds the
+// partner lane's copy of them.  On return v[0] holds the warp total of
+// column warp_col<R>(lane) (and, for R = 64, v[1] that of column + 32).
+template <int R, bool kMax>
 __device__ __forceinline__ void warp_reduce_scatter(float* v, int lane) {
-  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-  if constexpr (NT == 64) {
-    // fold the upper 32 columns onto lanes' second slot later: reduce the two
-    // halves independently with the 32-column scheme
+  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
+  if constexpr (R == 64) {
     warp_reduce_scatter<32, kMax>(v, lane);
     warp_reduce_scatter<32, kMax>(v + 32, lane);
     v[1] = v[32];
   } else {
-    // width = number of live values; each step halves it
-    int width = NT;
+    int width = R;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
       if (width > 1) {
         const bool upper = (lane & off) != 0;
         const int half = width >> 1;
 #pragma unroll
-        for (int i = 0; i < NT / 2; ++i) {
+        for (int i = 0; i < R / 2; ++i) {
           if (i < half) {
-            // keep my half, send the other
             const float send = upper ? v[i] : v[i + half];
             const float keep = upper ? v[i + half] : v[i];
-            const float got = __shfl_xor_sync(0xffffffffu, send, off);
-            v[i] = op(keep, got);
+            v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
           }
         }
         width = half;
@@ -125,30 +136,31 @@ __device__ __forceinline__ void warp_reduce_scatter(float* v, int lane) {
   }
 }
 
-// Column index a lane holds after warp_reduce_scatter<NT> (first slot).
-template <int NT>
-__device__ __forceinline__ int scatter_col(int lane) {
-  // After the halving steps with offsets 16, 8, ..., the lane bits that
-  // chose the upper halves, read most significant first, give the column.
-  if constexpr (NT == 64 || NT == 32) {
-    return ((lane >> 4) & 1) * 16 + ((lane >> 3) & 1) * 8 + ((lane >> 2) & 1) * 4 + ((lane >> 1) & 1) * 2 +
-           (lane & 1);
-  } else {  // NT == 16: four halving steps (16, 8, 4, 2), then a full sum over bit 0
-    return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-  }
+// Column held by a lane after warp_reduce_scatter<R>: the lane bits that
+// chose upper halves, most significant first; lanes that agree on them hold
+// the same total (only the lowest of them stores it).
+template <int R>
+__device__ __forceinline__ int warp_col(int lane) {
+  constexpr int kShift = R >= 32 ? 0 : (R == 16 ? 1 : 2);
+  return lane >> kShift;
+}
+template <int R>
+__device__ __forceinline__ bool warp_col_writer(int lane) {
+  constexpr int kMask = R >= 32 ? 0 : (R == 16 ? 1 : 3);
+  return (lane & kMask) == 0;
 }
 
-template <int NT, bool kQe4m3>
-__global__ void __launch_bounds__(kTcThreads, TcCfg<NT>::kMinBlocks)
+template <int R, bool kQe4m3>
+__global__ void __launch_bounds__(kTcThreads, (TcCfg<R, kQe4m3>::kMinBlocks))
 decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
-  using C = TcCfg<NT>;
+  using C = TcCfg<R, kQe4m3>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(sm);
-  float* red = reinterpret_cast<float*>(sm + C::kOffRed);  // [4][NT]
-  float* m_s = reinterpret_cast<float*>(sm + C::kOffM);      // [2][NT]
-  float* corr_s = reinterpret_cast<float*>(sm + C::kOffCorr);  // [NT]
+  float* red = reinterpret_cast<float*>(sm + C::kOffRed);      // [4][R]
+  float* m_s = reinterpret_cast<float*>(sm + C::kOffM);        // [2][R]
+  float* corr_s = reinterpret_cast<float*>(sm + C::kOffCorr);  // [R]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
   int* q_shift = reinterpret_cast<int*>(sm + C::kOffMisc + 8);
@@ -168,9 +180,9 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     bar.sfree = p;
     p += 16;
     bar.pfull = p;
-    p += 16;
+    p += 8;
     bar.pfree = p;
-    p += 16;
+    p += 8;
     bar.odone = p;
     p += 8;
     bar.qready = p;
@@ -188,7 +200,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   const int rest = blockIdx.x / a.h_k;
   const int qt = rest % n_q_tiles;
   const int w_idx = rest / n_q_tiles;
-  const int n0 = qt * NT;
+  const int n0 = qt * R;
 
   const int4 item = reinterpret_cast<const int4*>(a.work)[w_idx];
   const int b = item.x, t_begin = item.y, t_end = item.z, slot = item.w;
@@ -205,9 +217,9 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar.sfull + 8 * s, 1);
       ptx::mbar_init(bar.sfree + 8 * s, 4);
-      ptx::mbar_init(bar.pfull + 8 * s, 4);
-      ptx::mbar_init(bar.pfree + 8 * s, 1);
     }
+    ptx::mbar_init(bar.pfull, 4);
+    ptx::mbar_init(bar.pfree, 1);
     ptx::mbar_init(bar.odone, 1);
     ptx::mbar_init(bar.qready, 1);
     ptx::mbar_init(bar.drain, 1);
@@ -222,8 +234,8 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem;              // S buffers: columns [0, 2 NT)
-  const uint32_t tmem_o = tmem + 2 * NT;     // O: columns [2 NT, 3 NT)
+  const uint32_t tmem_s = tmem;                // S buffers: columns [0, 2 kN1)
+  const uint32_t tmem_o = tmem + 2 * C::kN1;   // O: columns [2 kN1, 2 kN1 + kN2)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -261,7 +273,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       // L2 prefetch of a tile further ahead: its HBM latency overlaps the
       // wait for a free stage, and its TMA load later hits L2.
       const int ahead = i + a.l2_prefetch;
-      if (a.l2_prefetch > 0 && ahead < T && ahead >= (i == 0 ? 1 : 0)) {
+      if (a.l2_prefetch > 0 && ahead < T) {
         for (int pf = (i == 0 ? 1 : ahead); pf <= ahead; ++pf) {
           const int pp = lookup(t_begin + pf);
           if (lane < ppt && pp < a.num_pages) {
@@ -296,9 +308,10 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t idesc_s = ptx::idesc_e4m3(kTileKV, NT, false, false);  // S = K Q^T
-      const uint32_t idesc_o = ptx::idesc_e4m3(kTileKV, NT, true, true);    // O = V^T P
-      constexpr int kQParts = kQe4m3 ? 1 : 2;
+      const uint32_t idesc_s = ptx::idesc_e4m3(kTileKV, C::kN1, false, false);  // S = K Q^T
+      const uint32_t idesc_o = ptx::idesc_e4m3(kTileKV, C::kN2, true, true);    // O = V^T P
+      const uint32_t q_base = sbase + C::kOffQ;
+      const uint32_t p_base = sbase + C::kOffP;
       bool ok = ptx::mbar_wait_bounded(bar.qready, 0, abort_flag, kWaitNs);
       // Issue GEMM1 and GEMM2 as their inputs become ready, whichever comes
       // first: GEMM2(j) must not wait behind the arrival of a later K tile,
@@ -315,16 +328,12 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
             ptx::tc_fence_after();
             const uint32_t k_base = sbase + C::kOffK + st * kKVTileBytes;
 #pragma unroll
-            for (int part = 0; part < kQParts; ++part) {
-              const uint32_t q_base = sbase + C::kOffQ + part * C::kQBytes;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                // A = K (K-major, 128-byte swizzle, 8-row groups 1024 B
-                // apart); B = Q part (same layout); one K step = 32 bytes of d.
-                const uint64_t ad = ptx::smem_desc(k_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
-                const uint64_t bd = ptx::smem_desc(q_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
-                ptx::mma_e4m3(tmem_s + sb * NT, ad, bd, idesc_s, (part > 0 || kk > 0) ? 1u : 0u);
-              }
+            for (int kk = 0; kk < 4; ++kk) {
+              // A = K (K-major, 128-byte swizzle, 8-row groups 1024 B apart);
+              // B = Q hi|lo rows (same layout); one K step = 32 bytes of d.
+              const uint64_t ad = ptx::smem_desc(k_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
+              const uint64_t bd = ptx::smem_desc(q_base + kk * 32, 16, 1024, ptx::kSwizzle128B);
+              ptx::mma_e4m3(tmem_s + sb * C::kN1, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
             }
             ptx::mma_commit(bar.sfull + 8 * sb);
             ++g1;
@@ -333,27 +342,21 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         }
         if (g2 < g1) {
           const int st = g2 % C::kStages;
-          const int pb = g2 % C::kPBufs;
-          if (ptx::mbar_test_wait(bar.pfull + 8 * pb, (g2 / C::kPBufs) & 1) &&
-              ptx::mbar_test_wait(bar.vfull + 8 * st, (g2 / C::kStages) & 1)) {
+          if (ptx::mbar_test_wait(bar.pfull, g2 & 1) && ptx::mbar_test_wait(bar.vfull + 8 * st, (g2 / C::kStages) & 1)) {
             ptx::tc_fence_after();
             const uint32_t v_base = sbase + C::kOffV + st * kKVTileBytes;
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const uint32_t p_base = sbase + C::kOffP + (pb * 2 + part) * C::kPBytes;
-#pragma unroll
-              for (int kk = 0; kk < kTileKV / 32; ++kk) {
-                // A = V^T: MN-major, 128-byte swizzle, 8-row groups 1024 B
-                // apart; one K step = 32 KV rows = 4 groups.  B = P: MN-major,
-                // no swizzle, 8-row core matrices 128 B apart along K,
-                // 16-column groups 2048 B apart along N.
-                const uint64_t ad = ptx::smem_desc(v_base + kk * 4096, 0, 1024, ptx::kSwizzle128B);
-                const uint64_t bd = ptx::smem_desc(p_base + kk * 512, 128, 2048, ptx::kSwizzleNone);
-                ptx::mma_e4m3(tmem_o, ad, bd, idesc_o, (g2 > 0 || part > 0 || kk > 0) ? 1u : 0u);
-              }
+            for (int kk = 0; kk < kTileKV / 32; ++kk) {
+              // A = V^T: MN-major, 128-byte swizzle, 8-row groups 1024 B
+              // apart; one K step = 32 KV rows = 4 groups.  B = P hi|lo:
+              // MN-major, no swizzle, 8-row core matrices 128 B apart along
+              // K, 16-column groups 2048 B apart along N.
+              const uint64_t ad = ptx::smem_desc(v_base + kk * 4096, 0, 1024, ptx::kSwizzle128B);
+              const uint64_t bd = ptx::smem_desc(p_base + kk * 512, 128, 2048, ptx::kSwizzleNone);
+              ptx::mma_e4m3(tmem_o, ad, bd, idesc_o, (g2 > 0 || kk > 0) ? 1u : 0u);
             }
             ptx::mma_commit(bar.odone);
-            ptx::mma_commit(bar.pfree + 8 * pb);
+            ptx::mma_commit(bar.pfree);
             ptx::mma_commit(bar.kvempty + 8 * st);
             ++g2;
             progressed = true;
@@ -386,11 +389,11 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     const float kd = a.kd[b * a.kd_seq + g * a.kd_head];
     const float vd = a.vd[b * a.vd_seq + g * a.vd_head];
 
-    // ---- Q tile -> shared (e4m3 parts, 128-byte swizzled K-major rows)
+    // ---- Q tile -> shared: e4m3 rows in the 128-byte swizzled K-major
+    // layout, [hi rows 0..R) [lo rows R..2R) for bf16 Q
     {
-      // thread -> (row n, 16-byte chunk cc) pairs; NT*8 chunks over 128 threads
+      constexpr int kChunks = (R * 8 + 127) / 128;  // (row, 16-byte chunk) pairs per thread
       float amax = 0.f;
-      constexpr int kChunks = NT * 8 / 128;
       float xv[kChunks][16];
 #pragma unroll
       for (int k = 0; k < kChunks; ++k) {
@@ -399,7 +402,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         const int qrow = n0 + n;
 #pragma unroll
         for (int e = 0; e < 16; ++e) xv[k][e] = 0.f;
-        if (qrow < a.n_q) {
+        if (n < R && qrow < a.n_q) {
           const int64_t off = b * a.q_seq + (static_cast<int64_t>(g) * a.n_q + qrow) * kHeadDimDev + cc * 16;
           if (kQe4m3) {
             const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + off);
@@ -434,41 +437,48 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         }
       }
       const float qscale = kQe4m3 ? 1.f : ldexpf(1.f, shift);
+      // rows of the Q buffer no thread fills (e4m3 Q with R < 16) are zero
+      if (kQe4m3 && R < C::kN1) {
+        for (int id = st_tid; id < (C::kN1 - R) * 8; id += 128)
+          *reinterpret_cast<uint4*>(sm + C::kOffQ + R * 128 + id * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
       for (int k = 0; k < kChunks; ++k) {
         const int id = k * 128 + st_tid;
         const int n = id >> 3, cc = id & 7;
-        uint32_t hw[4], lw[4];
+        if (n < R) {
+          uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          uint16_t h01, h23, l01, l23;
-          if (kQe4m3) {
-            h01 = ptx::f32x2_to_e4m3x2(xv[k][4 * wi], xv[k][4 * wi + 1]);
-            h23 = ptx::f32x2_to_e4m3x2(xv[k][4 * wi + 2], xv[k][4 * wi + 3]);
-            l01 = l23 = 0;
-          } else {
-            float x[4], r[4];
+          for (int wi = 0; wi < 4; ++wi) {
+            uint16_t h01, h23, l01 = 0, l23 = 0;
+            if (kQe4m3) {
+              h01 = ptx::f32x2_to_e4m3x2(xv[k][4 * wi], xv[k][4 * wi + 1]);
+              h23 = ptx::f32x2_to_e4m3x2(xv[k][4 * wi + 2], xv[k][4 * wi + 3]);
+            } else {
+              float x[4], hf[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = xv[k][4 * wi + e] * qscale;
-            h01 = ptx::f32x2_to_e4m3x2(x[0], x[1]);
-            h23 = ptx::f32x2_to_e4m3x2(x[2], x[3]);
-            float hf[4];
-            e4m3x4_to_f32(static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16), hf);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) r[e] = x[e] - hf[e];
-            l01 = ptx::f32x2_to_e4m3x2(r[0], r[1]);
-            l23 = ptx::f32x2_to_e4m3x2(r[2], r[3]);
+              for (int e = 0; e < 4; ++e) x[e] = xv[k][4 * wi + e] * qscale;
+              h01 = ptx::f32x2_to_e4m3x2(x[0], x[1]);
+              h23 = ptx::f32x2_to_e4m3x2(x[2], x[3]);
+              e4m3x4_to_f32(static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16), hf);
+              l01 = ptx::f32x2_to_e4m3x2(x[0] - hf[0], x[1] - hf[1]);
+              l23 = ptx::f32x2_to_e4m3x2(x[2] - hf[2], x[3] - hf[3]);
+            }
+            hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
+            lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
           }
-          hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
-          lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+          // 128-byte swizzle: chunk cc of row n at chunk position cc ^ (n % 8)
+          *reinterpret_cast<uint4*>(sm + C::kOffQ + n * 128 + ((cc ^ (n & 7)) << 4)) =
+              make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          if (!kQe4m3) {
+            const int nl = R + n;
+            *reinterpret_cast<uint4*>(sm + C::kOffQ + nl * 128 + ((cc ^ (nl & 7)) << 4)) =
+                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
         }
-        const int pos = n * 128 + ((cc ^ (n & 7)) << 4);  // 128-byte swizzle
-        *reinterpret_cast<uint4*>(sm + C::kOffQ + pos) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        if (!kQe4m3)
-          *reinterpret_cast<uint4*>(sm + C::kOffQ + C::kQBytes + pos) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
       if (st_tid == 0) *q_shift = shift;
-      if (st_tid < NT) m_s[st_tid] = -INFINITY;  // running max starts at -inf
+      if (st_tid < R) m_s[st_tid] = -INFINITY;  // running max starts at -inf
       ptx::fence_proxy_async_smem();
       ptx::named_bar_sync(kBarSm, 128);
       if (st_tid == 0) ptx::mbar_arrive(bar.qready);
@@ -478,9 +488,9 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     const float cta_scale = a.softmax_scale * qd * kd * ldexpf(1.f, -shift);
     const float c2 = cta_scale * kLog2e;
 
-    float l_thr[NT];  // deferred row sums
+    float l_thr[R];  // deferred row sums of unrounded p
 #pragma unroll
-    for (int c = 0; c < NT; ++c) l_thr[c] = 0.f;
+    for (int c = 0; c < R; ++c) l_thr[c] = 0.f;
     int mb = 0;  // which half of m_s holds the running column max (raw units)
 
     bool ok = true;
@@ -493,21 +503,30 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         break;
       }
       ptx::tc_fence_after();
-      float sc[NT];
-      // S row of this thread's key, masked by select (garbage or poison
-      // rows never leak)
+      float sc[R];
+      // S row of this thread's key (hi + lo partial products), masked by
+      // select: garbage or poison rows never leak
       auto load_s = [&]() {
 #pragma unroll
-        for (int c0 = 0; c0 < NT; c0 += 16) {
+        for (int c0 = 0; c0 < C::kN1; c0 += 16) {
           uint32_t r[16];
-          MJ_TMEM_LD16(tmem_s + lane_off + sb * NT + c0, r);
+          MJ_TMEM_LD16(tmem_s + lane_off + sb * C::kN1 + c0, r);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) sc[c0 + e] = __uint_as_float(r[e]);
+          for (int e = 0; e < 16; ++e) {
+            const int c = c0 + e;
+            if (kQe4m3) {
+              if (c < R) sc[c] = __uint_as_float(r[e]);
+            } else if (c < R) {
+              sc[c] = __uint_as_float(r[e]);
+            } else {
+              sc[c - R] += __uint_as_float(r[e]);
+            }
+          }
         }
         if (j > vis_all) {
 #pragma unroll
-          for (int c = 0; c < NT; ++c) {
+          for (int c = 0; c < R; ++c) {
             const int n = n0 + c;
             int lim = a.causal ? L - a.q_len + n / a.h_r : L - 1;
             lim = lim < L - 1 ? lim : L - 1;
@@ -521,29 +540,27 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       // row sees a score above it (one barrier-reduction answers that for
       // the group) are the column maxima reduced: reduce-scatter in the
       // warp, the four warps through shared memory, then thread c updates
-      // column c.  Otherwise the stage needs no exchange at all.
-      const float* m_now = m_s + mb * NT;
+      // column c.  Otherwise the tile needs no exchange at all.
+      const float* m_now = m_s + mb * R;
       bool exceed = false;
 #pragma unroll
-      for (int c4 = 0; c4 < NT; c4 += 4) {
+      for (int c4 = 0; c4 < R; c4 += 4) {
         const float4 m4 = *reinterpret_cast<const float4*>(m_now + c4);
         exceed |= (sc[c4] > m4.x) | (sc[c4 + 1] > m4.y) | (sc[c4 + 2] > m4.z) | (sc[c4 + 3] > m4.w);
       }
       bool moved = false;
       if (ptx::named_bar_red_or(kBarSm, 128, exceed)) {
-        warp_reduce_scatter<NT, true>(sc, lane);  // in place; S is read again below
-        const int col = scatter_col<NT>(lane);
-        if (NT == 16) {
-          if ((lane & 1) == 0) red[sw * NT + col] = sc[0];
-        } else {
-          red[sw * NT + col] = sc[0];
-          if (NT == 64) red[sw * NT + 32 + col] = sc[1];
+        warp_reduce_scatter<R, true>(sc, lane);  // in place; S is read again below
+        if (warp_col_writer<R>(lane)) {
+          const int col = warp_col<R>(lane);
+          red[sw * R + col] = sc[0];
+          if (R == 64) red[sw * R + 32 + col] = sc[1];
         }
         ptx::named_bar_sync(kBarSm, 128);
         bool moved_c = false;
-        if (st_tid < NT) {
+        if (st_tid < R) {
           const int c = st_tid;
-          const float t = fmaxf(fmaxf(red[c], red[NT + c]), fmaxf(red[2 * NT + c], red[3 * NT + c]));
+          const float t = fmaxf(fmaxf(red[c], red[R + c]), fmaxf(red[2 * R + c], red[3 * R + c]));
           const float mo = m_now[c];
           const float mn = fmaxf(mo, t);
           moved_c = mn != mo;
@@ -551,13 +568,13 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           // column that had seen no key
           const float mu = (mn == -INFINITY) ? 0.f : mn;
           corr_s[c] = fast_exp2((mo - mu) * c2);
-          m_s[(mb ^ 1) * NT + c] = mn;
+          m_s[(mb ^ 1) * R + c] = mn;
         }
         moved = ptx::named_bar_red_or(kBarSm, 128, moved_c);
         mb ^= 1;
         if (moved) {
 #pragma unroll
-          for (int c4 = 0; c4 < NT; c4 += 4) {
+          for (int c4 = 0; c4 < R; c4 += 4) {
             const float4 f = *reinterpret_cast<const float4*>(corr_s + c4);
             l_thr[c4] *= f.x;
             l_thr[c4 + 1] *= f.y;
@@ -570,7 +587,8 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar.sfree + 8 * sb);
-      // lazy O correction: only when some column max moved, after GEMM2(i-1)
+      // lazy O correction (both the hi and the lo columns of a row): only
+      // when some column max moved, after GEMM2(i-1)
       if (moved && i > 0) {
         if (!ptx::mbar_wait_bounded(bar.odone, (i - 1) & 1, abort_flag, kWaitNs)) {
           ok = false;
@@ -578,12 +596,13 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         }
         ptx::tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < NT; c0 += 16) {
+        for (int c0 = 0; c0 < C::kN2; c0 += 16) {
           uint32_t r[16];
           MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr_s[c0 + e]);
+          for (int e = 0; e < 16; ++e)
+            r[e] = __float_as_uint(__uint_as_float(r[e]) * corr_s[(c0 + e) % R]);
           MJ_TMEM_ST16(tmem_o + lane_off + c0, r);
         }
         ptx::tmem_st_wait();
@@ -591,9 +610,9 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       // probabilities and the deferred row sums; the -inf guard uses 0 as
       // the reference of a column that has seen no key yet
       {
-        const float* m_new = m_s + mb * NT;
+        const float* m_new = m_s + mb * R;
 #pragma unroll
-        for (int c4 = 0; c4 < NT; c4 += 4) {
+        for (int c4 = 0; c4 < R; c4 += 4) {
           const float4 m4 = *reinterpret_cast<const float4*>(m_new + c4);
           const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
@@ -605,26 +624,20 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           }
         }
       }
-
-      // the P buffer is free once GEMM2 of the tile that last used it finished
-      const int pb = i % C::kPBufs;
-      if (i >= C::kPBufs &&
-          !ptx::mbar_wait_bounded(bar.pfree + 8 * pb, ((i / C::kPBufs) - 1) & 1, abort_flag, kWaitNs)) {
+      // the P buffer is free once GEMM2(i-1) finished reading it
+      if (i >= 1 && !ptx::mbar_wait_bounded(bar.pfree, (i - 1) & 1, abort_flag, kWaitNs)) {
         ok = false;
         break;
       }
-      // split 448 p = hi + lo (e4m3) and store this row's bytes:
-      // part buffer [NT/16 groups][128 rows][16 bytes]
-      uint8_t* p_hi = sm + C::kOffP + (pb * 2 + 0) * C::kPBytes;
-      uint8_t* p_lo = sm + C::kOffP + (pb * 2 + 1) * C::kPBytes;
+      // split 448 p = hi + lo (e4m3); hi -> column c, lo -> column R + c of
+      // the P buffer [kN2/16 groups][128 rows][16 bytes]
+      {
+        uint32_t hw[R / 4], lw[R / 4];
 #pragma unroll
-      for (int gq = 0; gq < NT / 16; ++gq) {
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
+        for (int wi = 0; wi < R / 4; ++wi) {
           float x[4], hf[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = sc[gq * 16 + wi * 4 + e] * 448.f;
+          for (int e = 0; e < 4; ++e) x[e] = sc[wi * 4 + e] * 448.f;
           const uint16_t h01 = ptx::f32x2_to_e4m3x2(x[0], x[1]);
           const uint16_t h23 = ptx::f32x2_to_e4m3x2(x[2], x[3]);
           hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
@@ -633,9 +646,18 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           const uint16_t l23 = ptx::f32x2_to_e4m3x2(x[2] - hf[2], x[3] - hf[3]);
           lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
         }
-        const int off = gq * (kTileKV * 16) + row * 16;
-        *reinterpret_cast<uint4*>(p_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(p_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        uint8_t* pbuf = sm + C::kOffP + row * 16;
+        if (R == 8) {
+          *reinterpret_cast<uint4*>(pbuf) = make_uint4(hw[0], hw[1], lw[0], lw[1]);
+        } else {
+#pragma unroll
+          for (int gq = 0; gq < R / 16; ++gq) {
+            *reinterpret_cast<uint4*>(pbuf + gq * (kTileKV * 16)) =
+                make_uint4(hw[4 * gq], hw[4 * gq + 1], hw[4 * gq + 2], hw[4 * gq + 3]);
+            *reinterpret_cast<uint4*>(pbuf + (R / 16 + gq) * (kTileKV * 16)) =
+                make_uint4(lw[4 * gq], lw[4 * gq + 1], lw[4 * gq + 2], lw[4 * gq + 3]);
+          }
+        }
       }
       // rows past the sequence end: zero their V row so 0 * poison cannot
       // reach O (the TMA landed the whole last page)
@@ -652,7 +674,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar.pfull + 8 * pb);
+      if (lane == 0) ptx::mbar_arrive(bar.pfull);
     }
 
     // ---- epilogue
@@ -662,48 +684,51 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     } else {
       ptx::tc_fence_after();
       // row sums: reduce over the 128 KV rows
-      float* redl = red;  // reuse buffer 0 after the loop
-      ptx::named_bar_sync(kBarSm, 128);  // everyone is done reading red / m_run
-      {
-        warp_reduce_scatter<NT, false>(l_thr, lane);
-        const int col = scatter_col<NT>(lane);
-        if (NT == 16) {
-          if ((lane & 1) == 0) redl[sw * NT + col] = l_thr[0];
-        } else {
-          redl[sw * NT + col] = l_thr[0];
-          if (NT == 64) redl[sw * NT + 32 + col] = l_thr[1];
-        }
+      ptx::named_bar_sync(kBarSm, 128);  // everyone is done reading red
+      warp_reduce_scatter<R, false>(l_thr, lane);
+      if (warp_col_writer<R>(lane)) {
+        const int col = warp_col<R>(lane);
+        red[sw * R + col] = l_thr[0];
+        if (R == 64) red[sw * R + 32 + col] = l_thr[1];
       }
-      const float* m_fin = m_s + mb * NT;
+      const float* m_fin = m_s + mb * R;
       ptx::named_bar_sync(kBarSm, 128);
       const int nsp = a.n_splits[b];
       const bool final_out = nsp <= 1;
       const float out_scale = vd * (1.f / 448.f);
       const int d = row;  // TMEM lane of O = head-dim index
+      float o_row[R];     // O[d][c] = hi column c + lo column R + c
 #pragma unroll
-      for (int c0 = 0; c0 < NT; c0 += 16) {
+      for (int c0 = 0; c0 < C::kN2; c0 += 16) {
         uint32_t r[16];
         MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = c0 + e;
-          const int n = n0 + c;
-          if (n >= a.n_q) break;
-          const float l = redl[c] + redl[NT + c] + redl[2 * NT + c] + redl[3 * NT + c];
-          const float o = __uint_as_float(r[e]) * out_scale;
-          if (final_out) {
-            const int64_t orow = b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + n) * kHeadDimDev;
-            a.o[orow + d] = __float2bfloat16_rn(o * (a.scale_o / (l + 1e-30f)));
-          } else {
-            const int64_t pr = part_row(a, b, g, slot, n);
-            a.o_part[pr * kHeadDimDev + d] = o;
-          }
+          if (c < R)
+            o_row[c] = __uint_as_float(r[e]);
+          else
+            o_row[c - R] += __uint_as_float(r[e]);
         }
       }
-      if (st_tid < NT && n0 + st_tid < a.n_q) {
+#pragma unroll
+      for (int c = 0; c < R; ++c) {
+        const int n = n0 + c;
+        if (n >= a.n_q) break;
+        const float l = red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c];
+        const float o = o_row[c] * out_scale;
+        if (final_out) {
+          const int64_t orow = b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + n) * kHeadDimDev;
+          a.o[orow + d] = __float2bfloat16_rn(o * (a.scale_o / (l + 1e-30f)));
+        } else {
+          const int64_t pr = part_row(a, b, g, slot, n);
+          a.o_part[pr * kHeadDimDev + d] = o;
+        }
+      }
+      if (st_tid < R && n0 + st_tid < a.n_q) {
         const int c = st_tid, n = n0 + c;
-        const float l = redl[c] + redl[NT + c] + redl[2 * NT + c] + redl[3 * NT + c];
+        const float l = red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c];
         const float m_logit = m_fin[c] * cta_scale;
         if (final_out) {
           a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + n] = m_logit + logf(l);
@@ -759,14 +784,14 @@ bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, in
   return r == CUDA_SUCCESS;
 }
 
-template <int NT, bool kQe4m3>
+template <int R, bool kQe4m3>
 cudaError_t launch_tc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   CUtensorMap mk, mv;
   if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page) ||
       !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page))
     return cudaErrorInvalidValue;
-  const int smem = TcCfg<NT>::kBytes;
-  auto kern = decode_tc_kernel<NT, kQe4m3>;
+  const int smem = TcCfg<R, kQe4m3>::kBytes;
+  auto kern = decode_tc_kernel<R, kQe4m3>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
@@ -774,36 +799,40 @@ cudaError_t launch_tc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int R>
+cudaError_t launch_tc_q(const DecodeDev& a, int n_q_tiles, bool q_e4m3, cudaStream_t stream) {
+  return q_e4m3 ? launch_tc<R, true>(a, n_q_tiles, stream) : launch_tc<R, false>(a, n_q_tiles, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
                              cudaStream_t stream) {
   switch (rows_per_cta) {
-    case 16:
-      return q_e4m3 ? launch_tc<16, true>(a, n_q_tiles, stream) : launch_tc<16, false>(a, n_q_tiles, stream);
-    case 32:
-      return q_e4m3 ? launch_tc<32, true>(a, n_q_tiles, stream) : launch_tc<32, false>(a, n_q_tiles, stream);
-    case 64:
-      return q_e4m3 ? launch_tc<64, true>(a, n_q_tiles, stream) : launch_tc<64, false>(a, n_q_tiles, stream);
-    default:
-      return cudaErrorInvalidValue;
+    case 8: return launch_tc_q<8>(a, n_q_tiles, q_e4m3, stream);
+    case 16: return launch_tc_q<16>(a, n_q_tiles, q_e4m3, stream);
+    case 32: return launch_tc_q<32>(a, n_q_tiles, q_e4m3, stream);
+    case 64: return launch_tc_q<64>(a, n_q_tiles, q_e4m3, stream);
+    default: return cudaErrorInvalidValue;
   }
 }
 
-int tc_min_blocks(int rows_per_cta) {
+int tc_min_blocks(int rows_per_cta, bool q_e4m3) {
   switch (rows_per_cta) {
-    case 16: return TcCfg<16>::kMinBlocks;
-    case 32: return TcCfg<32>::kMinBlocks;
-    case 64: return TcCfg<64>::kMinBlocks;
+    case 8: return q_e4m3 ? TcCfg<8, true>::kMinBlocks : TcCfg<8, false>::kMinBlocks;
+    case 16: return q_e4m3 ? TcCfg<16, true>::kMinBlocks : TcCfg<16, false>::kMinBlocks;
+    case 32: return q_e4m3 ? TcCfg<32, true>::kMinBlocks : TcCfg<32, false>::kMinBlocks;
+    case 64: return q_e4m3 ? TcCfg<64, true>::kMinBlocks : TcCfg<64, false>::kMinBlocks;
     default: return 1;
   }
 }
 
-int tc_smem_bytes(int rows_per_cta) {
+int tc_smem_bytes(int rows_per_cta, bool q_e4m3) {
   switch (rows_per_cta) {
-    case 16: return TcCfg<16>::kBytes;
-    case 32: return TcCfg<32>::kBytes;
-    case 64: return TcCfg<64>::kBytes;
+    case 8: return q_e4m3 ? TcCfg<8, true>::kBytes : TcCfg<8, false>::kBytes;
+    case 16: return q_e4m3 ? TcCfg<16, true>::kBytes : TcCfg<16, false>::kBytes;
+    case 32: return q_e4m3 ? TcCfg<32, true>::kBytes : TcCfg<32, false>::kBytes;
+    case 64: return q_e4m3 ? TcCfg<64, true>::kBytes : TcCfg<64, false>::kBytes;
     default: return 0;
   }
 }

@@ -15,11 +15,11 @@ cudaError_t launch_decode_cc(const DecodeDev& a, int rows_per_cta, int n_q_tiles
                              cudaStream_t stream);
 int cc_smem_bytes(int rows_per_cta);
 
-// Tensor-core (tcgen05) decode (rows_per_cta in {16, 32, 64}).
+// Tensor-core (tcgen05) decode (rows_per_cta in {8, 16, 32, 64}).
 cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
                              cudaStream_t stream);
-int tc_smem_bytes(int rows_per_cta);
-int tc_min_blocks(int rows_per_cta);  // co-resident CTAs per SM the kernel is built for
+int tc_smem_bytes(int rows_per_cta, bool q_e4m3);
+int tc_min_blocks(int rows_per_cta, bool q_e4m3);  // co-resident CTAs per SM the kernel is built for
 
 // Merge of split sequences' partials into O / LSE; max_n_splits (> 1) sizes
 // the number of warps that share one row.
