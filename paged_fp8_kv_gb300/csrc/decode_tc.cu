@@ -26,11 +26,13 @@
 //    P: 2R columns of B) so each K step is one MMA; their products land in
 //    accumulator columns c and R + c, which the softmax / epilogue add.
 //
-// Roles (192 threads):
+// Roles (64 + 128 or 64 + 256 threads):
 //   warp 0      TMA producer: K and V tiles, one box per KV page.
 //   warp 1      TMEM allocator; lane 0 issues every MMA and commit.
-//   warps 2..5  softmax / correction / epilogue; warp w reads TMEM lanes
-//               32*(w%4).. (TMEM lane = KV row for S, = head-dim row for O).
+//   warps 2..   softmax / correction / epilogue; warp w reads TMEM lanes
+//               32*(w%4).. (TMEM lane = KV row for S, = head-dim row for O);
+//               with 8 softmax warps two share a lane quarter, each taking
+//               half of the columns.
 //
 // Every mbarrier wait is bounded (wall clock); a role that gives up sets a
 // shared abort flag and writes MJ_ERR_TIMEOUT to the optional status word,
@@ -47,11 +49,11 @@
 namespace mj {
 namespace {
 
-constexpr int kTcThreads = 192;
 constexpr int kTileKV = 128;                 // KV rows per tile (MMA M)
 constexpr int kKVTileBytes = kTileKV * 128;  // one K or V tile: 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legal wait
 constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
+constexpr float kLog2P448 = 8.807354922057604f;  // log2(448): P is produced as 448 p
 
 constexpr int pow2_at_least(int x) {
   int p = 32;
@@ -71,6 +73,16 @@ struct TcCfg {
   static constexpr int kN2 = 2 * R;
   static constexpr int kStages = R <= 32 ? 2 : 5;
   static constexpr int kMinBlocks = R <= 16 ? 3 : (R <= 32 ? 2 : 1);
+  // two P buffers let the softmax of tile i write while GEMM2(i-1) still
+  // reads; R = 16 at 3 CTAs/SM has no room for the second one
+  static constexpr int kPBufs = R == 16 ? 1 : 2;
+  // softmax warps: four cover the 128 TMEM lanes; with R = 32 a second four
+  // take the other half of the columns (two warps per lane quarter)
+  static constexpr int kSmWarps = R >= 32 ? 8 : 4;
+  static constexpr int kSmThreads = 32 * kSmWarps;
+  static constexpr int kThreads = 64 + kSmThreads;
+  static constexpr int kHalves = kSmWarps / 4;
+  static constexpr int kCols = R / kHalves;  // columns per softmax thread
   static constexpr int kQBytes = kN1 * 128;    // SW128 K-major rows
   static constexpr int kPBytes = kN2 * kTileKV;  // MN-major, no swizzle
   static constexpr int kTmemCols = pow2_at_least(2 * kN1 + kN2);
@@ -78,12 +90,12 @@ struct TcCfg {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kStages * kKVTileBytes;
   static constexpr int kOffQ = 2 * kStages * kKVTileBytes;
-  static constexpr int kOffP = kOffQ + kQBytes;       // [kN2/16 groups][128 rows][16 B]
-  static constexpr int kOffRed = kOffP + kPBytes;      // [4][R] floats
+  static constexpr int kOffP = kOffQ + kQBytes;       // [buf][kN2/16 groups][128 rows][16 B]
+  static constexpr int kOffRed = kOffP + kPBufs * kPBytes;  // [4][R] floats
   static constexpr int kOffM = kOffRed + 4 * R * 4;    // [2][R] running max
   static constexpr int kOffCorr = kOffM + 2 * R * 4;   // [R] correction
   static constexpr int kOffBar = kOffCorr + R * 4;
-  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 1 + 1 + 1 + 1 + 1;
+  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64 + 1024;  // + alignment slack
   static_assert(kN1 % 16 == 0 && kN1 <= 256 && kN2 % 16 == 0 && kN2 <= 256, "MMA N");
@@ -94,7 +106,8 @@ struct TcCfg {
 struct Bars {
   uint32_t kfull, vfull, kvempty;  // + stage * 8
   uint32_t sfull, sfree;           // + buf * 8
-  uint32_t pfull, pfree, odone, qready, drain;
+  uint32_t pfull, pfree;  // + buf * 8
+  uint32_t odone, qready, drain;
 };
 
 __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) {
@@ -150,8 +163,17 @@ __device__ __forceinline__ bool warp_col_writer(int lane) {
   return (lane & kMask) == 0;
 }
 
+// x rounded to 4 significant bits, ties to even: the value e4m3 gives a
+// non-negative x in its normal range [2^-6, 448] (below 2^-6 the e4m3 grid is
+// coarser; the caller's residual then carries an error below 2^-10).
+__device__ __forceinline__ float round_4_sig_bits(float x) {
+  uint32_t u = __float_as_uint(x);
+  u = (u + 0x7FFFFu + ((u >> 20) & 1u)) & 0xFFF00000u;
+  return __uint_as_float(u);
+}
+
 template <int R, bool kQe4m3>
-__global__ void __launch_bounds__(kTcThreads, (TcCfg<R, kQe4m3>::kMinBlocks))
+__global__ void __launch_bounds__((TcCfg<R, kQe4m3>::kThreads), (TcCfg<R, kQe4m3>::kMinBlocks))
 decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
   using C = TcCfg<R, kQe4m3>;
@@ -164,7 +186,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
   int* q_shift = reinterpret_cast<int*>(sm + C::kOffMisc + 8);
-  float* amax_red = reinterpret_cast<float*>(sm + C::kOffMisc + 16);  // [4]
+  float* amax_red = reinterpret_cast<float*>(sm + C::kOffMisc + 16);  // [8]
 
   Bars bar;
   {
@@ -180,9 +202,9 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     bar.sfree = p;
     p += 16;
     bar.pfull = p;
-    p += 8;
+    p += 16;
     bar.pfree = p;
-    p += 8;
+    p += 16;
     bar.odone = p;
     p += 8;
     bar.qready = p;
@@ -216,10 +238,12 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar.sfull + 8 * s, 1);
-      ptx::mbar_init(bar.sfree + 8 * s, 4);
+      ptx::mbar_init(bar.sfree + 8 * s, C::kSmWarps);
     }
-    ptx::mbar_init(bar.pfull, 4);
-    ptx::mbar_init(bar.pfree, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(bar.pfull + 8 * s, C::kSmWarps);
+      ptx::mbar_init(bar.pfree + 8 * s, 1);
+    }
     ptx::mbar_init(bar.odone, 1);
     ptx::mbar_init(bar.qready, 1);
     ptx::mbar_init(bar.drain, 1);
@@ -311,7 +335,6 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const uint32_t idesc_s = ptx::idesc_e4m3(kTileKV, C::kN1, false, false);  // S = K Q^T
       const uint32_t idesc_o = ptx::idesc_e4m3(kTileKV, C::kN2, true, true);    // O = V^T P
       const uint32_t q_base = sbase + C::kOffQ;
-      const uint32_t p_base = sbase + C::kOffP;
       bool ok = ptx::mbar_wait_bounded(bar.qready, 0, abort_flag, kWaitNs);
       // Issue GEMM1 and GEMM2 as their inputs become ready, whichever comes
       // first: GEMM2(j) must not wait behind the arrival of a later K tile,
@@ -342,9 +365,12 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         }
         if (g2 < g1) {
           const int st = g2 % C::kStages;
-          if (ptx::mbar_test_wait(bar.pfull, g2 & 1) && ptx::mbar_test_wait(bar.vfull + 8 * st, (g2 / C::kStages) & 1)) {
+          const int pb = g2 % C::kPBufs;
+          if (ptx::mbar_test_wait(bar.pfull + 8 * pb, (g2 / C::kPBufs) & 1) &&
+              ptx::mbar_test_wait(bar.vfull + 8 * st, (g2 / C::kStages) & 1)) {
             ptx::tc_fence_after();
             const uint32_t v_base = sbase + C::kOffV + st * kKVTileBytes;
+            const uint32_t p_base = sbase + C::kOffP + pb * C::kPBytes;
 #pragma unroll
             for (int kk = 0; kk < kTileKV / 32; ++kk) {
               // A = V^T: MN-major, 128-byte swizzle, 8-row groups 1024 B
@@ -356,7 +382,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
               ptx::mma_e4m3(tmem_o, ad, bd, idesc_o, (g2 > 0 || kk > 0) ? 1u : 0u);
             }
             ptx::mma_commit(bar.odone);
-            ptx::mma_commit(bar.pfree);
+            ptx::mma_commit(bar.pfree + 8 * pb);
             ptx::mma_commit(bar.kvempty + 8 * st);
             ++g2;
             progressed = true;
@@ -365,6 +391,13 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         if (progressed) {
           stall_since = 0;
         } else {
+          // Nothing ready: sleep on the event the pipeline needs next (P of
+          // the oldest tile, else K of the next one) instead of spinning on
+          // the issue slots the softmax warps share with this warp.
+          if (g2 < g1)
+            ptx::mbar_try_wait_hint(bar.pfull + 8 * (g2 % C::kPBufs), (g2 / C::kPBufs) & 1, 200);
+          else if (g1 < T)
+            ptx::mbar_try_wait_hint(bar.kfull + 8 * (g1 % C::kStages), (g1 / C::kStages) & 1, 200);
           const uint64_t now = ptx::globaltimer_ns();
           if (stall_since == 0) stall_since = now;
           if (*abort_flag || now - stall_since > kWaitNs) ok = false;
@@ -378,8 +411,11 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     }
   } else {
     // ------------------------------------------------- softmax warpgroup
-    const int sw = warp - 2;          // 0..3 within the softmax group
+    constexpr int kCols = C::kCols;
+    constexpr int kSmT = C::kSmThreads;
+    const int sw = warp - 2;          // 0 .. kSmWarps-1 within the softmax group
     const int quarter = warp & 3;     // TMEM lane quarter this warp may access
+    const int col0 = (sw / 4) * kCols;  // first column of this thread's half
     const int st_tid = sw * 32 + lane;
     const int row = quarter * 32 + lane;  // TMEM lane: KV row (S) / d (O)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -392,12 +428,12 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     // ---- Q tile -> shared: e4m3 rows in the 128-byte swizzled K-major
     // layout, [hi rows 0..R) [lo rows R..2R) for bf16 Q
     {
-      constexpr int kChunks = (R * 8 + 127) / 128;  // (row, 16-byte chunk) pairs per thread
+      constexpr int kChunks = (R * 8 + kSmT - 1) / kSmT;  // (row, 16-byte chunk) pairs per thread
       float amax = 0.f;
       float xv[kChunks][16];
 #pragma unroll
       for (int k = 0; k < kChunks; ++k) {
-        const int id = k * 128 + st_tid;
+        const int id = k * kSmT + st_tid;
         const int n = id >> 3, cc = id & 7;
         const int qrow = n0 + n;
 #pragma unroll
@@ -428,8 +464,8 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         if (lane == 0) amax_red[sw] = amax;
-        ptx::named_bar_sync(kBarSm, 128);
-        amax = fmaxf(fmaxf(amax_red[0], amax_red[1]), fmaxf(amax_red[2], amax_red[3]));
+        ptx::named_bar_sync(kBarSm, kSmT);
+        for (int w = 0; w < C::kSmWarps; ++w) amax = fmaxf(amax, amax_red[w]);
         if (amax > 0.f) {
           const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;  // floor(log2) for normals
           shift = 7 - e;
@@ -439,12 +475,12 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const float qscale = kQe4m3 ? 1.f : ldexpf(1.f, shift);
       // rows of the Q buffer no thread fills (e4m3 Q with R < 16) are zero
       if (kQe4m3 && R < C::kN1) {
-        for (int id = st_tid; id < (C::kN1 - R) * 8; id += 128)
+        for (int id = st_tid; id < (C::kN1 - R) * 8; id += kSmT)
           *reinterpret_cast<uint4*>(sm + C::kOffQ + R * 128 + id * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int k = 0; k < kChunks; ++k) {
-        const int id = k * 128 + st_tid;
+        const int id = k * kSmT + st_tid;
         const int n = id >> 3, cc = id & 7;
         if (n < R) {
           uint32_t hw[4], lw[4];
@@ -480,7 +516,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       if (st_tid == 0) *q_shift = shift;
       if (st_tid < R) m_s[st_tid] = -INFINITY;  // running max starts at -inf
       ptx::fence_proxy_async_smem();
-      ptx::named_bar_sync(kBarSm, 128);
+      ptx::named_bar_sync(kBarSm, kSmT);
       if (st_tid == 0) ptx::mbar_arrive(bar.qready);
     }
     const int shift = *q_shift;
@@ -488,9 +524,9 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     const float cta_scale = a.softmax_scale * qd * kd * ldexpf(1.f, -shift);
     const float c2 = cta_scale * kLog2e;
 
-    float l_thr[R];  // deferred row sums of unrounded p
+    float l_thr[kCols];  // deferred row sums (of 448 p) for this thread's columns
 #pragma unroll
-    for (int c = 0; c < R; ++c) l_thr[c] = 0.f;
+    for (int c = 0; c < kCols; ++c) l_thr[c] = 0.f;
     int mb = 0;  // which half of m_s holds the running column max (raw units)
 
     bool ok = true;
@@ -503,31 +539,39 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         break;
       }
       ptx::tc_fence_after();
-      float sc[R];
-      // S row of this thread's key (hi + lo partial products), masked by
-      // select: garbage or poison rows never leak
+      float sc[kCols];
+      // S row of this thread's key for its columns (hi + lo partial
+      // products), masked by select: garbage or poison rows never leak
       auto load_s = [&]() {
+        const uint32_t s_base = tmem_s + lane_off + sb * C::kN1;
+        if constexpr (C::kHalves == 1) {
+          uint32_t r[C::kN1];  // every chunk in flight, one wait
 #pragma unroll
-        for (int c0 = 0; c0 < C::kN1; c0 += 16) {
-          uint32_t r[16];
-          MJ_TMEM_LD16(tmem_s + lane_off + sb * C::kN1 + c0, r);
+          for (int c0 = 0; c0 < C::kN1; c0 += 16) MJ_TMEM_LD16(s_base + c0, (r + c0));
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = c0 + e;
-            if (kQe4m3) {
-              if (c < R) sc[c] = __uint_as_float(r[e]);
-            } else if (c < R) {
-              sc[c] = __uint_as_float(r[e]);
-            } else {
-              sc[c - R] += __uint_as_float(r[e]);
-            }
+          for (int c = 0; c < R; ++c) {
+            sc[c] = __uint_as_float(r[c]);
+            if (!kQe4m3) sc[c] += __uint_as_float(r[R + c]);
+          }
+        } else {
+          uint32_t r[2 * kCols];
+#pragma unroll
+          for (int c0 = 0; c0 < kCols; c0 += 16) {
+            MJ_TMEM_LD16(s_base + col0 + c0, (r + c0));
+            if (!kQe4m3) MJ_TMEM_LD16(s_base + R + col0 + c0, (r + kCols + c0));
+          }
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) {
+            sc[c] = __uint_as_float(r[c]);
+            if (!kQe4m3) sc[c] += __uint_as_float(r[kCols + c]);
           }
         }
         if (j > vis_all) {
 #pragma unroll
-          for (int c = 0; c < R; ++c) {
-            const int n = n0 + c;
+          for (int c = 0; c < kCols; ++c) {
+            const int n = n0 + col0 + c;
             int lim = a.causal ? L - a.q_len + n / a.h_r : L - 1;
             lim = lim < L - 1 ? lim : L - 1;
             if (j > lim) sc[c] = -INFINITY;
@@ -541,27 +585,27 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       // the group) are the column maxima reduced: reduce-scatter in the
       // warp, the four warps through shared memory, then thread c updates
       // column c.  Otherwise the tile needs no exchange at all.
-      const float* m_now = m_s + mb * R;
+      const float* m_now = m_s + mb * R + col0;
       bool exceed = false;
 #pragma unroll
-      for (int c4 = 0; c4 < R; c4 += 4) {
+      for (int c4 = 0; c4 < kCols; c4 += 4) {
         const float4 m4 = *reinterpret_cast<const float4*>(m_now + c4);
         exceed |= (sc[c4] > m4.x) | (sc[c4 + 1] > m4.y) | (sc[c4 + 2] > m4.z) | (sc[c4 + 3] > m4.w);
       }
       bool moved = false;
-      if (ptx::named_bar_red_or(kBarSm, 128, exceed)) {
-        warp_reduce_scatter<R, true>(sc, lane);  // in place; S is read again below
-        if (warp_col_writer<R>(lane)) {
-          const int col = warp_col<R>(lane);
-          red[sw * R + col] = sc[0];
-          if (R == 64) red[sw * R + 32 + col] = sc[1];
+      if (ptx::named_bar_red_or(kBarSm, kSmT, exceed)) {
+        warp_reduce_scatter<kCols, true>(sc, lane);  // in place; S is read again below
+        if (warp_col_writer<kCols>(lane)) {
+          const int col = col0 + warp_col<kCols>(lane);
+          red[quarter * R + col] = sc[0];
+          if (kCols == 64) red[quarter * R + 32 + col] = sc[1];
         }
-        ptx::named_bar_sync(kBarSm, 128);
+        ptx::named_bar_sync(kBarSm, kSmT);
         bool moved_c = false;
         if (st_tid < R) {
           const int c = st_tid;
           const float t = fmaxf(fmaxf(red[c], red[R + c]), fmaxf(red[2 * R + c], red[3 * R + c]));
-          const float mo = m_now[c];
+          const float mo = m_s[mb * R + c];
           const float mn = fmaxf(mo, t);
           moved_c = mn != mo;
           // corr = 2^((m_old - m_use) c2); the -inf guard makes it 0 for a
@@ -570,12 +614,12 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           corr_s[c] = fast_exp2((mo - mu) * c2);
           m_s[(mb ^ 1) * R + c] = mn;
         }
-        moved = ptx::named_bar_red_or(kBarSm, 128, moved_c);
+        moved = ptx::named_bar_red_or(kBarSm, kSmT, moved_c);
         mb ^= 1;
         if (moved) {
 #pragma unroll
-          for (int c4 = 0; c4 < R; c4 += 4) {
-            const float4 f = *reinterpret_cast<const float4*>(corr_s + c4);
+          for (int c4 = 0; c4 < kCols; c4 += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(corr_s + col0 + c4);
             l_thr[c4] *= f.x;
             l_thr[c4 + 1] *= f.y;
             l_thr[c4 + 2] *= f.z;
@@ -595,73 +639,84 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           break;
         }
         ptx::tc_fence_after();
+        // this thread's columns of O: hi [col0, col0 + kCols), lo R + those
 #pragma unroll
-        for (int c0 = 0; c0 < C::kN2; c0 += 16) {
-          uint32_t r[16];
-          MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
-          ptx::tmem_ld_wait();
+        for (int part = 0; part < 2; ++part) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            r[e] = __float_as_uint(__uint_as_float(r[e]) * corr_s[(c0 + e) % R]);
-          MJ_TMEM_ST16(tmem_o + lane_off + c0, r);
+          for (int c0 = 0; c0 < kCols; c0 += 16) {
+            const int oc = (C::kHalves == 1) ? (part * 16 + c0) : (part * R + col0 + c0);
+            if (C::kHalves == 1 && oc >= C::kN2) break;
+            uint32_t r[16];
+            MJ_TMEM_LD16(tmem_o + lane_off + oc, r);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              r[e] = __float_as_uint(__uint_as_float(r[e]) * corr_s[(oc + e) % R]);
+            MJ_TMEM_ST16(tmem_o + lane_off + oc, r);
+          }
         }
         ptx::tmem_st_wait();
       }
-      // probabilities and the deferred row sums; the -inf guard uses 0 as
-      // the reference of a column that has seen no key yet
+      // 448 p = 2^((s - m) c2 + log2 448), directly in e4m3's range; the row
+      // sums keep the same factor 448.  The -inf guard uses 0 as the
+      // reference of a column that has seen no key yet.
       {
-        const float* m_new = m_s + mb * R;
+        const float* m_new = m_s + mb * R + col0;
 #pragma unroll
-        for (int c4 = 0; c4 < R; c4 += 4) {
+        for (int c4 = 0; c4 < kCols; c4 += 4) {
           const float4 m4 = *reinterpret_cast<const float4*>(m_new + c4);
           const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float m_use = (mm[e] == -INFINITY) ? 0.f : mm[e];
-            const float p = fast_exp2(fmaf(sc[c4 + e], c2, -m_use * c2));
+            const float p = fast_exp2(fmaf(sc[c4 + e], c2, fmaf(-m_use, c2, kLog2P448)));
             l_thr[c4 + e] += p;
             sc[c4 + e] = p;
           }
         }
       }
-      // the P buffer is free once GEMM2(i-1) finished reading it
-      if (i >= 1 && !ptx::mbar_wait_bounded(bar.pfree, (i - 1) & 1, abort_flag, kWaitNs)) {
+      // P buffer i % kPBufs is free once GEMM2(i - kPBufs) finished reading it
+      const int pb = i % C::kPBufs;
+      if (i >= C::kPBufs &&
+          !ptx::mbar_wait_bounded(bar.pfree + 8 * pb, ((i / C::kPBufs) - 1) & 1, abort_flag, kWaitNs)) {
         ok = false;
         break;
       }
-      // split 448 p = hi + lo (e4m3); hi -> column c, lo -> column R + c of
-      // the P buffer [kN2/16 groups][128 rows][16 bytes]
+      // split x = 448 p = hi + lo (e4m3); hi -> column c, lo -> column R + c
+      // of the P buffer [kN2/16 groups][128 rows][16 bytes]
       {
-        uint32_t hw[R / 4], lw[R / 4];
+        uint32_t hw[kCols / 4], lw[kCols / 4];
 #pragma unroll
-        for (int wi = 0; wi < R / 4; ++wi) {
+        for (int wi = 0; wi < kCols / 4; ++wi) {
           float x[4], hf[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = sc[wi * 4 + e] * 448.f;
-          const uint16_t h01 = ptx::f32x2_to_e4m3x2(x[0], x[1]);
-          const uint16_t h23 = ptx::f32x2_to_e4m3x2(x[2], x[3]);
+          for (int e = 0; e < 4; ++e) {
+            x[e] = sc[wi * 4 + e];
+            hf[e] = round_4_sig_bits(x[e]);
+          }
+          const uint16_t h01 = ptx::f32x2_to_e4m3x2(hf[0], hf[1]);
+          const uint16_t h23 = ptx::f32x2_to_e4m3x2(hf[2], hf[3]);
           hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
-          e4m3x4_to_f32(hw[wi], hf);
           const uint16_t l01 = ptx::f32x2_to_e4m3x2(x[0] - hf[0], x[1] - hf[1]);
           const uint16_t l23 = ptx::f32x2_to_e4m3x2(x[2] - hf[2], x[3] - hf[3]);
           lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
         }
-        uint8_t* pbuf = sm + C::kOffP + row * 16;
+        uint8_t* pbuf = sm + C::kOffP + pb * C::kPBytes + row * 16;
         if (R == 8) {
           *reinterpret_cast<uint4*>(pbuf) = make_uint4(hw[0], hw[1], lw[0], lw[1]);
         } else {
 #pragma unroll
-          for (int gq = 0; gq < R / 16; ++gq) {
-            *reinterpret_cast<uint4*>(pbuf + gq * (kTileKV * 16)) =
+          for (int gq = 0; gq < kCols / 16; ++gq) {
+            *reinterpret_cast<uint4*>(pbuf + (col0 / 16 + gq) * (kTileKV * 16)) =
                 make_uint4(hw[4 * gq], hw[4 * gq + 1], hw[4 * gq + 2], hw[4 * gq + 3]);
-            *reinterpret_cast<uint4*>(pbuf + (R / 16 + gq) * (kTileKV * 16)) =
+            *reinterpret_cast<uint4*>(pbuf + ((R + col0) / 16 + gq) * (kTileKV * 16)) =
                 make_uint4(lw[4 * gq], lw[4 * gq + 1], lw[4 * gq + 2], lw[4 * gq + 3]);
           }
         }
       }
       // rows past the sequence end: zero their V row so 0 * poison cannot
       // reach O (the TMA landed the whole last page)
-      if (j >= L) {
+      if (j >= L && col0 == 0) {
         const int st = i % C::kStages;
         if (!ptx::mbar_wait_bounded(bar.vfull + 8 * st, (i / C::kStages) & 1, abort_flag, kWaitNs)) {
           ok = false;
@@ -674,7 +729,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar.pfull);
+      if (lane == 0) ptx::mbar_arrive(bar.pfull + 8 * pb);
     }
 
     // ---- epilogue
@@ -684,40 +739,53 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     } else {
       ptx::tc_fence_after();
       // row sums: reduce over the 128 KV rows
-      ptx::named_bar_sync(kBarSm, 128);  // everyone is done reading red
-      warp_reduce_scatter<R, false>(l_thr, lane);
-      if (warp_col_writer<R>(lane)) {
-        const int col = warp_col<R>(lane);
-        red[sw * R + col] = l_thr[0];
-        if (R == 64) red[sw * R + 32 + col] = l_thr[1];
+      ptx::named_bar_sync(kBarSm, kSmT);  // everyone is done reading red
+      warp_reduce_scatter<kCols, false>(l_thr, lane);
+      if (warp_col_writer<kCols>(lane)) {
+        const int col = col0 + warp_col<kCols>(lane);
+        red[quarter * R + col] = l_thr[0];
+        if (kCols == 64) red[quarter * R + 32 + col] = l_thr[1];
       }
       const float* m_fin = m_s + mb * R;
-      ptx::named_bar_sync(kBarSm, 128);
+      ptx::named_bar_sync(kBarSm, kSmT);
       const int nsp = a.n_splits[b];
       const bool final_out = nsp <= 1;
-      const float out_scale = vd * (1.f / 448.f);
+      const float out_scale = vd * (1.f / 448.f);  // O and the row sums both carry 448
       const int d = row;  // TMEM lane of O = head-dim index
-      float o_row[R];     // O[d][c] = hi column c + lo column R + c
+      float o_row[kCols];  // O[d][c] = hi column c + lo column R + c
+      if constexpr (C::kHalves == 1) {
 #pragma unroll
-      for (int c0 = 0; c0 < C::kN2; c0 += 16) {
-        uint32_t r[16];
-        MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
-        ptx::tmem_ld_wait();
+        for (int c0 = 0; c0 < C::kN2; c0 += 16) {
+          uint32_t r[16];
+          MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
+          ptx::tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = c0 + e;
-          if (c < R)
-            o_row[c] = __uint_as_float(r[e]);
-          else
-            o_row[c - R] += __uint_as_float(r[e]);
+          for (int e = 0; e < 16; ++e) {
+            const int c = c0 + e;
+            if (c < R)
+              o_row[c] = __uint_as_float(r[e]);
+            else
+              o_row[c - R] += __uint_as_float(r[e]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < kCols; c0 += 16) {
+          uint32_t rh[16], rl[16];
+          MJ_TMEM_LD16(tmem_o + lane_off + col0 + c0, rh);
+          MJ_TMEM_LD16(tmem_o + lane_off + R + col0 + c0, rl);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o_row[c0 + e] = __uint_as_float(rh[e]) + __uint_as_float(rl[e]);
         }
       }
 #pragma unroll
-      for (int c = 0; c < R; ++c) {
+      for (int cl = 0; cl < kCols; ++cl) {
+        const int c = col0 + cl;
         const int n = n0 + c;
         if (n >= a.n_q) break;
-        const float l = red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c];
-        const float o = o_row[c] * out_scale;
+        const float l = (red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c]) * (1.f / 448.f);
+        const float o = o_row[cl] * out_scale;
         if (final_out) {
           const int64_t orow = b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + n) * kHeadDimDev;
           a.o[orow + d] = __float2bfloat16_rn(o * (a.scale_o / (l + 1e-30f)));
@@ -728,7 +796,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       }
       if (st_tid < R && n0 + st_tid < a.n_q) {
         const int c = st_tid, n = n0 + c;
-        const float l = red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c];
+        const float l = (red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c]) * (1.f / 448.f);
         const float m_logit = m_fin[c] * cta_scale;
         if (final_out) {
           a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + n] = m_logit + logf(l);
@@ -795,7 +863,7 @@ cudaError_t launch_tc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
-  kern<<<grid, kTcThreads, smem, stream>>>(a, mk, mv, n_q_tiles);
+  kern<<<grid, TcCfg<R, kQe4m3>::kThreads, smem, stream>>>(a, mk, mv, n_q_tiles);
   return cudaGetLastError();
 }
 
@@ -812,7 +880,6 @@ cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles
     case 8: return launch_tc_q<8>(a, n_q_tiles, q_e4m3, stream);
     case 16: return launch_tc_q<16>(a, n_q_tiles, q_e4m3, stream);
     case 32: return launch_tc_q<32>(a, n_q_tiles, q_e4m3, stream);
-    case 64: return launch_tc_q<64>(a, n_q_tiles, q_e4m3, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -822,7 +889,6 @@ int tc_min_blocks(int rows_per_cta, bool q_e4m3) {
     case 8: return q_e4m3 ? TcCfg<8, true>::kMinBlocks : TcCfg<8, false>::kMinBlocks;
     case 16: return q_e4m3 ? TcCfg<16, true>::kMinBlocks : TcCfg<16, false>::kMinBlocks;
     case 32: return q_e4m3 ? TcCfg<32, true>::kMinBlocks : TcCfg<32, false>::kMinBlocks;
-    case 64: return q_e4m3 ? TcCfg<64, true>::kMinBlocks : TcCfg<64, false>::kMinBlocks;
     default: return 1;
   }
 }
@@ -832,7 +898,6 @@ int tc_smem_bytes(int rows_per_cta, bool q_e4m3) {
     case 8: return q_e4m3 ? TcCfg<8, true>::kBytes : TcCfg<8, false>::kBytes;
     case 16: return q_e4m3 ? TcCfg<16, true>::kBytes : TcCfg<16, false>::kBytes;
     case 32: return q_e4m3 ? TcCfg<32, true>::kBytes : TcCfg<32, false>::kBytes;
-    case 64: return q_e4m3 ? TcCfg<64, true>::kBytes : TcCfg<64, false>::kBytes;
     default: return 0;
   }
 }

@@ -15,7 +15,7 @@ cudaError_t launch_decode_cc(const DecodeDev& a, int rows_per_cta, int n_q_tiles
                              cudaStream_t stream);
 int cc_smem_bytes(int rows_per_cta);
 
-// Tensor-core (tcgen05) decode (rows_per_cta in {8, 16, 32, 64}).
+// Tensor-core (tcgen05) decode (rows_per_cta in {8, 16, 32}).
 cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
                              cudaStream_t stream);
 int tc_smem_bytes(int rows_per_cta, bool q_e4m3);

@@ -74,6 +74,20 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Like mbar_try_wait, but the thread may be suspended for up to about
+// `hint_ns` while the phase is incomplete (it does not spin on issue slots).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // `timeout_ns` of wall time, or at once when *abort becomes non-zero (another
 // role of the CTA already gave up).  Returns false when it gave up.
@@ -146,6 +160,12 @@ __device__ __forceinline__ void tc_fence_after() {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),     \
         "=r"(r[14]), "=r"(r[15])                                                                     \
       : "r"(taddr))
+
+#define MJ_TMEM_LD8(taddr, r)                                                                      \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"                \
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),  \
+                 "=r"(r[7])                                                                          \
+               : "r"(taddr))
 
 #define MJ_TMEM_ST16(taddr, r)                                                                        \
   asm volatile(                                                                                       \
