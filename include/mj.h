@@ -88,14 +88,27 @@ typedef struct {
  *   MJ_KERNEL_CUDA_CORE    fp32 CUDA-core kernel, exact e4m3 dequant in
  *                          registers, fp32 P
  *   MJ_KERNEL_TENSOR_CORE  tcgen05 swap-AB kernel: e4m3 K/V tiles straight
- *                          from TMA into the MMA, Q and P as hi+lo e4m3 */
-typedef enum { MJ_KERNEL_AUTO = 0, MJ_KERNEL_CUDA_CORE = 1, MJ_KERNEL_TENSOR_CORE = 2 } mj_kernel_pref;
+ *                          from TMA into the MMA, Q and P as hi+lo e4m3;
+ *                          one CTA per kv head
+ *   MJ_KERNEL_TENSOR_CORE_GROUPED
+ *                          the same arithmetic with one CTA per group of 4
+ *                          or 8 kv heads, whose rows of each page it reads
+ *                          together; needs h_k a multiple of 4 and
+ *                          q_len*h_r <= 8 (MJ_ERR_UNSUPPORTED otherwise) */
+typedef enum {
+  MJ_KERNEL_AUTO = 0,
+  MJ_KERNEL_CUDA_CORE = 1,
+  MJ_KERNEL_TENSOR_CORE = 2,
+  MJ_KERNEL_TENSOR_CORE_GROUPED = 3
+} mj_kernel_pref;
 
 /* Plan knobs (source: `plan_split_kv`).  A field left 0 takes the
  * library's value for the kernel mj_decode_attn will launch for these
  * params, and is filled in on return, so a caller can reproduce the plan:
  *   sm_count         SMs of the target GPU (0 -> 152, a GB300)
- *   ctas_per_sm      co-resident decode CTAs per SM of the chosen kernel
+ *   ctas_per_sm      co-resident (decode CTA, kv head) pairs per SM of the
+ *                    chosen kernel: CTAs per SM, times the kv heads one
+ *                    CTA serves
  *   n_q_tiles        CTAs per (work item, kv head) along the packed rows
  *   force_splits     > 0: cut every sequence into this many chunks
  *   min_chunk_tiles  lower bound of the chunk size in 128-row tiles (0 -> 1)

@@ -34,6 +34,7 @@ MJ_E4M3 = 1
 MJ_KERNEL_AUTO = 0
 MJ_KERNEL_CUDA_CORE = 1
 MJ_KERNEL_TENSOR_CORE = 2
+MJ_KERNEL_TENSOR_CORE_GROUPED = 3
 
 
 class MjError(RuntimeError):

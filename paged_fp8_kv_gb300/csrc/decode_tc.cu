@@ -47,6 +47,48 @@
 #include "sm100_ptx.cuh"
 
 namespace mj {
+// -------------------------------------------------------- host: tensor maps
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// (d bytes, rows in page, kv heads, pages) view of a paged e4m3 pool; one box
+// is box_rows rows of box_heads heads: 128 bytes x box_rows x box_heads,
+// head-major in shared memory, 128-byte swizzle.
+bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, int num_pages, int64_t s_row,
+                 int64_t s_head, int64_t s_page, int box_rows, int box_heads) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(h_k),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_row), static_cast<cuuint64_t>(s_head),
+                                 static_cast<cuuint64_t>(s_page)};
+  const cuuint32_t box[4] = {128, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_heads), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 constexpr int kTileKV = 128;                 // KV rows per tile (MMA M)
@@ -715,16 +757,20 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         }
       }
       // rows past the sequence end: zero their V row so 0 * poison cannot
-      // reach O (the TMA landed the whole last page)
-      if (j >= L && col0 == 0) {
+      // reach O (the TMA landed the whole last page).  Every thread of a
+      // tile that reaches the end waits, so that a wait that gives up does
+      // so in all warps alike.
+      if ((t_begin + i + 1) * kTileKV > L) {
         const int st = i % C::kStages;
         if (!ptx::mbar_wait_bounded(bar.vfull + 8 * st, (i / C::kStages) & 1, abort_flag, kWaitNs)) {
           ok = false;
           break;
         }
-        uint4* vrow = reinterpret_cast<uint4*>(sm + C::kOffV + st * kKVTileBytes + row * 128);
+        if (j >= L && col0 == 0) {
+          uint4* vrow = reinterpret_cast<uint4*>(sm + C::kOffV + st * kKVTileBytes + row * 128);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
+          for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
@@ -733,7 +779,11 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     }
 
     // ---- epilogue
-    if (ok && !ptx::mbar_wait_bounded(bar.odone, (T - 1) & 1, abort_flag, kWaitNs)) ok = false;
+    // `drain` fires once every MMA the CTA issued is done (a parity wait on
+    // `odone` could not tell GEMM2(T - 1) from GEMM2(T - 3) when two P
+    // buffers let two GEMM2s be in flight)
+    if (ok && !ptx::mbar_wait_bounded(bar.drain, 0, abort_flag, kWaitNs)) ok = false;
+    if (*abort_flag) ok = false;
     if (!ok) {
       set_abort(abort_flag, a.status);
     } else {
@@ -815,48 +865,11 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   if (warp == 1) ptx::tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// -------------------------------------------------------- host: tensor maps
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// (d bytes, rows in page, kv heads, pages) view of a paged e4m3 pool; one box
-// is one page of one head: 128 bytes x page_size rows, 128-byte swizzle.
-bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, int num_pages, int64_t s_row,
-                 int64_t s_head, int64_t s_page) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(h_k),
-                              static_cast<cuuint64_t>(num_pages)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_row), static_cast<cuuint64_t>(s_head),
-                                 static_cast<cuuint64_t>(s_page)};
-  const cuuint32_t box[4] = {128, static_cast<cuuint32_t>(page_size), 1, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int R, bool kQe4m3>
 cudaError_t launch_tc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page) ||
-      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page))
+  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, a.page_size, 1) ||
+      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, a.page_size, 1))
     return cudaErrorInvalidValue;
   const int smem = TcCfg<R, kQe4m3>::kBytes;
   auto kern = decode_tc_kernel<R, kQe4m3>;

@@ -1,0 +1,967 @@
+// Head-grouped split-KV paged decode attention on the tensor cores (tcgen05,
+// kind::f8f6f4) for GQA caches with several kv heads: a persistent kernel,
+// one CTA per SM.
+//
+// Sources: as for the per-head kernel in decode_tc.cu — the
+// "mjolnir/t5_decode.py" page (`decode`: paged TMA gather, select masking,
+// online softmax with folded descales and the -inf guard, lazy O rescale,
+// final-vs-partial epilogue, 448-scaled e4m3 P) and the swap-AB decode pull
+// request page (KV slots on M, live heads on N).  What a work unit computes
+// is the page's; which CTA computes it is not part of the result.
+//
+// Why a second kernel: one CTA per kv head reads each KV row of its head as
+// a separate 128-byte piece, h_k*128 bytes apart; on GB300 that pattern
+// streams at about 4.9 TB/s however deep the pipeline.  Here a CTA serves G
+// kv heads of a work item and fetches each page's rows of all G heads as one
+// TMA box.  Under load a TMA round trip takes 2-3 us, so the SM needs about
+// 150 KB outstanding: the CTA owns the SM, keeps a six-stage ring of 32 KB
+// tiles, and never drains it between work units — it takes units from a
+// shared counter (greedy, longest first, as the plan orders them) and its
+// producer streams the next unit's tiles while the softmax finishes the
+// last one.
+//
+// Roles (416 threads): warps 0 and 12 issue the K and the V TMA tiles;
+// warp 1 (one thread)
+// issues the S = K Q^T MMAs and warp 11 (one thread) the O += V^T P MMAs —
+// one thread issues a tcgen05.mma only every 70-100 cycles, slower than the
+// tensor pipe runs them, and a 32 KB tile takes eight; warps 2-9 are two
+// softmax warpgroups taking alternate tiles, each with its own S, O and
+// running max (merged per unit); warp 10 fetches the next unit, its
+// descriptor and scales, and converts its Q tile to e4m3, one unit ahead.
+//
+// One MMA tile is 128 rows = G heads x KR = 128/G keys (head-major: row
+// h*KR + k).  Its N side holds the GR = G*RH query rows of all G heads
+// (column h*RH + n), twice for bf16 Q (hi | lo e4m3 parts):
+//   S[row, col]  = K[row] . Q[col]       -- only the head-diagonal blocks
+//                                           (head(row) == head(col)) are used
+//   O[d, col]   += V[row, d] P[row, col] -- P is zero off the diagonal, so
+//                                           each column sums its own head
+// The MMA costs the same ~70 cycles for any N up to 128, so computing the
+// off-diagonal blocks is free; the zeros of P are written once.
+//
+// A head's KR rows live in one warp (G = 8: half a warp; G = 4: a warp), so
+// the column maxima and row sums are warp-local shuffles; one barrier per
+// tile tells a warpgroup whether any head's maximum moved (then its O, whose
+// TMEM lanes are the head dimension and span all heads, is corrected).
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "mj_device.cuh"
+#include "mj_kernels.h"
+#include "sm100_ptx.cuh"
+
+namespace mj {
+namespace {
+
+constexpr int kRows = 128;                   // MMA M: rows of one tile
+constexpr int kTileBytes = kRows * 128;      // one K or V tile: 16 KB
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legal wait
+constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
+constexpr float kLog2P448 = 8.807354922057604f;  // log2(448): P is produced as 448 p
+constexpr int kWG = 2;                       // softmax warpgroups
+constexpr int kThreads = 64 + 128 * kWG + 96;
+constexpr int kSchedWarp = 2 + 4 * kWG;      // warp index of the scheduler
+constexpr int kMma2Warp = kSchedWarp + 1;    // warp index of the GEMM2 issuer
+constexpr int kVLoadWarp = kSchedWarp + 2;   // warp index of the V-tile producer
+constexpr int kItemBytes = 128;              // one unit descriptor in shared memory
+
+constexpr int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+template <int G, int RH, bool kQe4m3>
+struct GCfg {
+  static constexpr int KR = kRows / G;     // keys per head per tile
+  static constexpr int GR = G * RH;        // query columns of the CTA
+  static constexpr int HPW = 32 / KR;      // heads per warp
+  static constexpr int W = HPW * RH;       // S columns a warp reads
+  static constexpr int kN1 = kQe4m3 ? (GR < 16 ? 16 : GR) : 2 * GR;
+  static constexpr int kN2 = 2 * GR;
+  // K and V rings: a K stage is free once its GEMM1 ran, a V stage only
+  // after the tile's softmax and GEMM2, so V gets more stages
+  static constexpr int kStagesK = 5;
+  static constexpr int kStagesV = 7;
+  static constexpr int kQBytes = kN1 * 128;
+  static constexpr int kPBytes = kN2 * kRows;  // [kN2/16 groups][128 rows][16 B]
+  static constexpr int kWgCols = pow2_at_least(2 * kN1 + kN2);  // TMEM per warpgroup: S x2, O
+  static constexpr int kTmemCols = kWG * kWgCols;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kStagesK * kTileBytes;
+  static constexpr int kOffQ = (kStagesK + kStagesV) * kTileBytes;  // [2 unit slots]
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;          // [kWG] P buffers
+  static constexpr int kOffCorr = kOffP + kWG * kPBytes;     // [kWG][2][GR]
+  static constexpr int kOffStat0 = kOffCorr + kWG * 2 * GR * 4;  // group 0: [GR] max, [GR] sum
+  static constexpr int kOffStat1 = kOffStat0 + 2 * GR * 4;       // group 1: [2 slots][GR] max, sum
+  static constexpr int kOffItem = kOffStat1 + 2 * 2 * GR * 4;    // [2 slots] descriptors
+  static constexpr int kOffBar = kOffItem + 2 * kItemBytes;
+  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 6 * kWG + 2 + 2 + 1 + 1 + 2;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 32 + 1024;
+  static_assert(KR >= 16 && KR <= 32, "a head's rows must sit within one warp");
+  static_assert(W == 8 || W == 16, "TMEM load width");
+  static_assert(kN1 % 16 == 0 && kN2 % 16 == 0 && kN1 <= 256 && kN2 <= 256, "MMA N");
+  static_assert(kTmemCols <= 512, "TMEM");
+  static_assert(kBytes <= 232448, "shared memory");
+  static_assert(40 + 8 * G <= kItemBytes, "unit descriptor");
+  static_assert(kOffBar % 8 == 0, "mbarrier alignment");
+  static_assert(16 * 128 * 4 <= kPBytes && GR % 16 == 0, "epilogue stage: 16 columns in a P buffer");
+};
+
+// Unit descriptor, written by the scheduler warp, read by every role.
+template <int G>
+struct Item {
+  int valid, b, t_begin, TS, L, g0, n0, slot, nsp, shift;
+  float vd[G], cs[G];  // v descale, logit scale (softmax_scale * qd * kd) per head
+};
+
+__device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) {
+  *abort = 1;
+  if (status) atomicExch(status, kStatusTimeout);
+}
+
+__device__ __forceinline__ float round_4_sig_bits(float x) {
+  uint32_t u = __float_as_uint(x);
+  u = (u + 0x7FFFFu + ((u >> 20) & 1u)) & 0xFFF00000u;
+  return __uint_as_float(u);
+}
+
+// `N` e4m3 codes (N in {4, 8}) of the hi and lo parts of x = 448 p.
+template <int N>
+__device__ __forceinline__ void split_p(const float* x, uint32_t* hi, uint32_t* lo) {
+#pragma unroll
+  for (int w = 0; w < N / 4; ++w) {
+    float h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = round_4_sig_bits(x[4 * w + e]);
+    const uint16_t h01 = ptx::f32x2_to_e4m3x2(h[0], h[1]);
+    const uint16_t h23 = ptx::f32x2_to_e4m3x2(h[2], h[3]);
+    const uint16_t l01 = ptx::f32x2_to_e4m3x2(x[4 * w] - h[0], x[4 * w + 1] - h[1]);
+    const uint16_t l23 = ptx::f32x2_to_e4m3x2(x[4 * w + 2] - h[2], x[4 * w + 3] - h[3]);
+    hi[w] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
+    lo[w] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+  }
+}
+
+// Named barriers: 1 + wg within a softmax warpgroup, kBarAll across both.
+constexpr int kBarAll = 3;
+
+template <int G, int RH, bool kQe4m3>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles, int num_units, int* sched) {
+  using C = GCfg<G, RH, kQe4m3>;
+  using It = Item<G>;
+  constexpr int KR = C::KR, GR = C::GR, SK = C::kStagesK, SV = C::kStagesV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(sm);
+  float* corr_all = reinterpret_cast<float*>(sm + C::kOffCorr);
+  float* stat0 = reinterpret_cast<float*>(sm + C::kOffStat0);  // [GR] m, [GR] l
+  float* stat1 = reinterpret_cast<float*>(sm + C::kOffStat1);  // [2][GR] m, [2][GR] l
+  auto item = [&](int slot) -> It& { return *reinterpret_cast<It*>(sm + C::kOffItem + slot * kItemBytes); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
+
+  // mbarriers: the K ring (full, empty), the V ring (full, empty); per
+  // warpgroup S full x2, S free x2, P full, P free; unit slot full x2 /
+  // empty x2; O free; MMA drain; unit descriptor full x2.
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto kfull = [&](int s) { return bar0 + 8u * s; };
+  auto kempty = [&](int s) { return bar0 + 8u * (SK + s); };
+  auto vfull = [&](int s) { return bar0 + 8u * (2 * SK + s); };
+  auto vempty = [&](int s) { return bar0 + 8u * (2 * SK + SV + s); };
+  constexpr int kB = 2 * (SK + SV);
+  // k: 0, 1 S full; 2, 3 S free; 4 P full; 5 P free
+  auto wgbar = [&](int wg, int k) { return bar0 + 8u * (kB + 6 * wg + k); };
+  auto ifull = [&](int slot) { return bar0 + 8u * (kB + 6 * kWG + slot); };
+  auto iempty = [&](int slot) { return bar0 + 8u * (kB + 6 * kWG + 2 + slot); };
+  const uint32_t ofree = bar0 + 8u * (kB + 6 * kWG + 4);
+  const uint32_t drain = ofree + 8u;
+  // the descriptor alone (the producer needs no Q): before the Q conversion
+  auto dfull = [&](int slot) { return drain + 8u * (1 + slot); };
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int groups = a.h_k / G;
+
+  if (tid == 0) {
+    for (int s = 0; s < SK; ++s) {
+      ptx::mbar_init(kfull(s), 1);
+      ptx::mbar_init(kempty(s), 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      ptx::mbar_init(vfull(s), 1);
+      ptx::mbar_init(vempty(s), 1);
+    }
+    for (int wg = 0; wg < kWG; ++wg) {
+      ptx::mbar_init(wgbar(wg, 0), 1);
+      ptx::mbar_init(wgbar(wg, 1), 1);
+      ptx::mbar_init(wgbar(wg, 2), 4);
+      ptx::mbar_init(wgbar(wg, 3), 4);
+      ptx::mbar_init(wgbar(wg, 4), 4);
+      ptx::mbar_init(wgbar(wg, 5), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(ifull(s), 1);
+      ptx::mbar_init(dfull(s), 1);
+      ptx::mbar_init(iempty(s), 2 + 4 * kWG);  // both MMA issuers, every softmax warp
+    }
+    ptx::mbar_init(ofree, 4);
+    ptx::mbar_init(drain, 2);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  // P: every byte off the head diagonal stays zero for the whole kernel
+  // (published to the tensor core by the fence before each P-full arrival)
+  if (warp >= 2 && warp < kSchedWarp) {
+    uint4* p = reinterpret_cast<uint4*>(sm + C::kOffP);
+    for (int id = tid - 64; id < kWG * C::kPBytes / 16; id += 128 * kWG) p[id] = make_uint4(0u, 0u, 0u, 0u);
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sbase + C::kOffMisc, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kSchedWarp) {
+    // ----------------------------------------------------------- scheduler
+    // Takes units from the shared counter (unit = work item x q tile x head
+    // group, work item outermost, so the plan's longest-first order is the
+    // order units are handed out), and fills a unit slot: descriptor, per-
+    // head scales, and the Q tile as e4m3 (hi | lo rows for bf16 Q) in the
+    // 128-byte swizzled K-major layout.
+    for (int it = 0;; ++it) {
+      const int slot = it & 1;
+      if (it >= 2) {
+        const bool got = ptx::mbar_wait_bounded(iempty(slot), ((it >> 1) - 1) & 1, abort_flag, kWaitNs);
+        if (__any_sync(0xffffffffu, !got)) {
+          if (lane == 0) set_abort(abort_flag, a.status);
+          break;
+        }
+      }
+      int u = 0, b = 0, t_begin = 0, t_end = 0, wslot = 0, qt = 0, grp = 0;
+      bool valid = false;
+      for (;;) {  // the next unit that is not padding
+        if (lane == 0) u = atomicAdd(sched, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (u >= num_units) break;
+        grp = u % groups;
+        const int rest = u / groups;
+        qt = rest % n_q_tiles;
+        const int4 wk = reinterpret_cast<const int4*>(a.work)[rest / n_q_tiles];
+        b = wk.x;
+        t_begin = wk.y;
+        t_end = wk.z;
+        wslot = wk.w;
+        if (t_end > t_begin) {
+          valid = true;
+          break;
+        }
+      }
+      It& I = item(slot);
+      int L = 0;
+      if (valid) {
+        L = a.seq_lens[b];
+        int key_stop = t_end * 128;
+        key_stop = key_stop < L ? key_stop : L;
+        const int TS = (key_stop - t_begin * 128 + KR - 1) / KR;
+        if (lane == 0) {
+          I.b = b;
+          I.t_begin = t_begin;
+          I.TS = TS < 1 ? 1 : TS;
+          I.L = L;
+          I.g0 = grp * G;
+          I.n0 = qt * RH;
+          I.slot = wslot;
+          I.nsp = a.n_splits[b];
+        }
+      }
+      if (lane == 0) I.valid = valid ? 1 : 0;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(dfull(slot));  // the producer may start on the unit's tiles
+      if (valid) {
+        const int g0 = grp * G, n0 = qt * RH;
+        if (lane < G) {
+          const int g = g0 + lane;
+          I.vd[lane] = a.vd[b * a.vd_seq + g * a.vd_head];
+          I.cs[lane] = a.softmax_scale * a.qd[b * a.qd_seq + g * a.qd_head] * a.kd[b * a.kd_seq + g * a.kd_head];
+        }
+        // Q rows: column c = hq * RH + n (head g0 + hq, packed row n0 + n);
+        // chunk id = c * 8 + 16-element chunk, lane l owning ids l + 32 kc.
+        // The loads of a half are all issued before any is used (one memory
+        // latency per half); the conversion pass reads them again from L1.
+        constexpr int kChunks = GR * 8 / 32;
+        constexpr int kHalf = kChunks >= 2 ? kChunks / 2 : 1;
+        constexpr int kWords = kQe4m3 ? 1 : 2;  // 16-byte words per chunk
+        auto q_src = [&](int kc, bool& live) -> const uint4* {
+          const int id = kc * 32 + lane;
+          const int c = id >> 3, cc = id & 7;
+          const int hq = c / RH, qrow = n0 + c % RH;
+          live = qrow < a.n_q;
+          const int64_t off =
+              b * a.q_seq + (static_cast<int64_t>(g0 + hq) * a.n_q + (live ? qrow : 0)) * kHeadDimDev + cc * 16;
+          return kQe4m3 ? reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + off)
+                        : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + off);
+        };
+        int shift = 0;
+        if (!kQe4m3) {
+          // bf16 |q| max: integer max of the magnitude bits
+          uint32_t mbits = 0;
+#pragma unroll
+          for (int k0 = 0; k0 < kChunks; k0 += kHalf) {
+            uint4 raw[kHalf][2];
+#pragma unroll
+            for (int u = 0; u < kHalf; ++u) {
+              bool live;
+              const uint4* src = q_src(k0 + u, live);
+              raw[u][0] = live ? src[0] : make_uint4(0u, 0u, 0u, 0u);
+              raw[u][1] = live ? src[1] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < kHalf; ++u) {
+              const uint32_t w8[8] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
+                                      raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
+#pragma unroll
+              for (int wi = 0; wi < 8; ++wi) {
+                mbits = max(mbits, w8[wi] & 0x7FFFu);
+                mbits = max(mbits, (w8[wi] >> 16) & 0x7FFFu);
+              }
+            }
+          }
+          float amax = __uint_as_float(mbits << 16);
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+          if (amax > 0.f) {
+            const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+            shift = 7 - e;  // max |q| 2^shift in [128, 256)
+            shift = shift > 126 ? 126 : (shift < -126 ? -126 : shift);
+          }
+        }
+        const float qscale = kQe4m3 ? 1.f : ldexpf(1.f, shift);
+        uint8_t* qbuf = sm + C::kOffQ + slot * C::kQBytes;
+        if (kQe4m3 && GR < C::kN1) {
+          for (int id = lane; id < (C::kN1 - GR) * 8; id += 32)
+            *reinterpret_cast<uint4*>(qbuf + GR * 128 + id * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll 2
+        for (int kc = 0; kc < kChunks; ++kc) {
+          const int id = kc * 32 + lane;
+          const int c = id >> 3, cc = id & 7;
+          bool live;
+          const uint4* src = q_src(kc, live);
+          uint4 raw[kWords];
+#pragma unroll
+          for (int wd = 0; wd < kWords; ++wd) raw[wd] = live ? src[wd] : make_uint4(0u, 0u, 0u, 0u);
+          float x[16];
+          if (kQe4m3) {
+            const uint32_t w4[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) e4m3x4_to_f32(w4[wi], x + wi * 4);
+          } else {
+            const uint32_t w8[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w,
+                                    raw[kWords - 1].x, raw[kWords - 1].y, raw[kWords - 1].z, raw[kWords - 1].w};
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) {
+              x[2 * wi] = __uint_as_float(w8[wi] << 16);
+              x[2 * wi + 1] = __uint_as_float(w8[wi] & 0xFFFF0000u);
+            }
+          }
+          uint32_t hwd[4], lwd[4];
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            uint16_t h01, h23, l01 = 0, l23 = 0;
+            if (kQe4m3) {
+              h01 = ptx::f32x2_to_e4m3x2(x[4 * wi], x[4 * wi + 1]);
+              h23 = ptx::f32x2_to_e4m3x2(x[4 * wi + 2], x[4 * wi + 3]);
+            } else {
+              float xs[4], hf[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) xs[e] = x[4 * wi + e] * qscale;
+              h01 = ptx::f32x2_to_e4m3x2(xs[0], xs[1]);
+              h23 = ptx::f32x2_to_e4m3x2(xs[2], xs[3]);
+              e4m3x4_to_f32(static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16), hf);
+              l01 = ptx::f32x2_to_e4m3x2(xs[0] - hf[0], xs[1] - hf[1]);
+              l23 = ptx::f32x2_to_e4m3x2(xs[2] - hf[2], xs[3] - hf[3]);
+            }
+            hwd[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
+            lwd[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+          }
+          // 128-byte swizzle: chunk cc of row c at chunk position cc ^ (c % 8)
+          *reinterpret_cast<uint4*>(qbuf + c * 128 + ((cc ^ (c & 7)) << 4)) = make_uint4(hwd[0], hwd[1], hwd[2], hwd[3]);
+          if (!kQe4m3) {
+            const int cl = GR + c;
+            *reinterpret_cast<uint4*>(qbuf + cl * 128 + ((cc ^ (cl & 7)) << 4)) =
+                make_uint4(lwd[0], lwd[1], lwd[2], lwd[3]);
+          }
+        }
+        if (lane == 0) I.shift = shift;
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ifull(slot));
+      if (!valid) break;
+    }
+  } else if (warp == 0 || warp == kVLoadWarp) {
+    // ----------------------------------------------------------- producers
+    // Warp 0 loads the K tiles, warp 12 the V tiles, each as its ring's
+    // stages free up (a K stage after its GEMM1, a V stage after its GEMM2):
+    // two short loops, so that issuing never waits on the other tensor's
+    // ring or on a busy issue slot shared with the softmax warps.
+    //
+    // Per tile: the rows of keys [k0, k0 + KR) of the G heads.  When a page
+    // holds whole tiles (PS >= KR) that is one TMA box, all G heads of one
+    // page (the per-SM rate of TMA operations, not bytes, bounds small
+    // boxes); else box jb of head h on lane h * bph + jb.  Block-table
+    // entries come from a register window (lane l holds block wbase + l)
+    // refilled 32 blocks ahead.
+    const bool is_k = warp == 0;
+    const int NS = is_k ? SK : SV;
+    const uint32_t ring = sbase + (is_k ? C::kOffK : C::kOffV);
+    const CUtensorMap* tmap = is_k ? &tmap_k : &tmap_v;
+    auto full = [&](int st) { return is_k ? kfull(st) : vfull(st); };
+    auto empty = [&](int st) { return is_k ? kempty(st) : vempty(st); };
+    const int PS = a.page_size;
+    const int box_rows = KR < PS ? KR : PS;
+    const int bph = KR / box_rows;  // boxes per head per tile
+    const int h = lane / bph, jb = lane % bph;
+    const bool active = lane < G * bph;
+    const bool one_box = bph == 1 && box_rows == KR;
+    if (lane == 0) ptx::prefetch_tmap(tmap);
+    uint32_t n = 0;  // tiles issued, over all units
+    bool alive = true;
+    for (int it = 0; alive; ++it) {
+      const int slot = it & 1;
+      const bool got = ptx::mbar_wait_bounded(dfull(slot), (it >> 1) & 1, abort_flag, kWaitNs);
+      if (__any_sync(0xffffffffu, !got)) {
+        if (lane == 0) set_abort(abort_flag, a.status);
+        break;
+      }
+      const It& I = item(slot);
+      if (!I.valid) break;
+      const int L = I.L, TS = I.TS, g0 = I.g0;
+      const int key_begin = I.t_begin * 128;
+      const int64_t bt_row = static_cast<int64_t>(I.b) * a.max_blocks;
+      int valid_pages = (L + PS - 1) / PS;
+      valid_pages = valid_pages < a.max_blocks ? valid_pages : a.max_blocks;
+      auto load_win = [&](int base) -> int {
+        const int blk = base + lane;
+        return blk < valid_pages ? a.block_table[bt_row + blk] : a.num_pages;
+      };
+      // A tile spans at most two blocks and starts on a block boundary when
+      // it spans two (KR a multiple of PS); the window starts at the unit's
+      // first block, so a tile never straddles two windows.
+      int wbase = key_begin / PS;
+      int win = load_win(wbase);
+      int win_next = load_win(wbase + 32);
+      for (int i = 0; i < TS; ++i, ++n) {
+        const int st = n % NS;
+        if (n >= static_cast<uint32_t>(NS)) {
+          const bool freed = ptx::mbar_wait_bounded(empty(st), ((n / NS) - 1) & 1, abort_flag, kWaitNs);
+          if (__any_sync(0xffffffffu, !freed)) {
+            if (lane == 0) set_abort(abort_flag, a.status);
+            alive = false;
+            break;
+          }
+        }
+        const int key0 = key_begin + i * KR;
+        if (key0 / PS >= wbase + 32) {  // uniform over the warp
+          wbase += 32;
+          win = win_next;
+          win_next = load_win(wbase + 32);
+        }
+        const int key = key0 + jb * box_rows;
+        const int pg = __shfl_sync(0xffffffffu, win, (key / PS - wbase) & 31);
+        const int page = (active && key < L) ? pg : a.num_pages;
+        const int row_off = key % PS;
+        const uint32_t dst = ring + st * kTileBytes;
+        if (one_box) {
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(full(st), kTileBytes);
+            ptx::tma_load_4d(dst, tmap, full(st), 0, row_off, g0, page);
+          }
+        } else {
+          if (lane == 0) ptx::mbar_arrive_expect_tx(full(st), kTileBytes);
+          __syncwarp();
+          if (active) ptx::tma_load_4d(dst + (h * KR + jb * box_rows) * 128, tmap, full(st), 0, row_off, g0 + h, page);
+        }
+      }
+    }
+    if (*abort_flag && lane == 0) {
+      // drain: wait (bounded) for every tile still in flight to land
+      volatile int never = 0;
+      for (uint32_t i = (n > static_cast<uint32_t>(NS) ? n - NS : 0); i < n; ++i)
+        ptx::mbar_wait_bounded(full(i % NS), (i / NS) & 1, &never, kWaitNs / 4);
+    }
+  } else if (warp == 1 || warp == kMma2Warp) {
+    // ----------------------------------------------------------------- MMA
+    // Tile number n counts tiles over all units; tile n goes to warpgroup
+    // n & 1 as its local tile t = n >> 1: GEMM1 (warp 1) into that group's
+    // S buffer t & 1, GEMM2 (warp 11) into its O.  Each issuer walks the
+    // units in order with blocking waits; GEMM1 runs ahead as far as the S
+    // buffers allow.  Shared-memory descriptors are a base plus the
+    // operand's offset >> 4 (every offset stays inside the 14-bit field).
+    if (lane == 0) {
+      const bool gemm1 = warp == 1;
+      bool ok = true;
+      uint32_t n = 0;  // this issuer's tiles so far
+      for (int it = 0; ok; ++it) {
+        const int slot = it & 1;
+        if (!ptx::mbar_wait_bounded(ifull(slot), (it >> 1) & 1, abort_flag, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        const It& I = item(slot);
+        if (!I.valid) break;
+        const int TS = I.TS;
+        if (gemm1) {
+          const uint32_t idesc_s = ptx::idesc_e4m3(kRows, C::kN1, false, false);
+          const uint64_t kdesc0 = ptx::smem_desc(sbase + C::kOffK, 16, 1024, ptx::kSwizzle128B);
+          const uint64_t qdesc = ptx::smem_desc(sbase + C::kOffQ + slot * C::kQBytes, 16, 1024, ptx::kSwizzle128B);
+          for (int i = 0; i < TS; ++i, ++n) {
+            const int st = n % SK;
+            const int wg = n & 1, t = n >> 1, sb = t & 1;
+            if (!ptx::mbar_wait_bounded(kfull(st), (n / SK) & 1, abort_flag, kWaitNs) ||
+                (t >= 2 && !ptx::mbar_wait_bounded(wgbar(wg, 2 + sb), ((t >> 1) - 1) & 1, abort_flag, kWaitNs))) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t kdesc = kdesc0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+            const uint32_t d_s = tmem + wg * C::kWgCols + sb * C::kN1;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // one K step = 32 bytes of d
+              ptx::mma_e4m3(d_s, kdesc + 2 * kk, qdesc + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+            ptx::mma_commit(wgbar(wg, sb));
+            ptx::mma_commit(kempty(st));
+          }
+        } else {
+          const uint32_t idesc_o = ptx::idesc_e4m3(kRows, C::kN2, true, true);
+          const uint64_t vdesc0 = ptx::smem_desc(sbase + C::kOffV, 0, 1024, ptx::kSwizzle128B);
+          const uint64_t pdesc0 = ptx::smem_desc(sbase + C::kOffP, 128, 2048, ptx::kSwizzleNone);
+          for (int i = 0; i < TS; ++i, ++n) {
+            const int st = n % SV;
+            const int wg = n & 1, t = n >> 1;
+            const bool first = i < 2;  // this group's first tile of the unit: O starts over
+            if (!ptx::mbar_wait_bounded(wgbar(wg, 4), t & 1, abort_flag, kWaitNs) ||
+                !ptx::mbar_wait_bounded(vfull(st), (n / SV) & 1, abort_flag, kWaitNs) ||
+                (first && it > 0 && !ptx::mbar_wait_bounded(ofree, (it - 1) & 1, abort_flag, kWaitNs))) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t vdesc = vdesc0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+            const uint64_t pdesc = pdesc0 + static_cast<uint64_t>((wg * C::kPBytes) >> 4);
+            const uint32_t d_o = tmem + wg * C::kWgCols + 2 * C::kN1;
+#pragma unroll
+            for (int kk = 0; kk < kRows / 32; ++kk)  // one K step = 32 KV rows
+              ptx::mma_e4m3(d_o, vdesc + 256 * kk, pdesc + 32 * kk, idesc_o, (!first || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(wgbar(wg, 5));
+            ptx::mma_commit(vempty(st));
+          }
+        }
+        if (ok) ptx::mma_commit(iempty(slot));  // this unit's Q and slot are no longer read
+      }
+      if (!ok) set_abort(abort_flag, a.status);
+      // every MMA of both issuers has completed once `drain` fires
+      ptx::mma_commit(drain);
+      volatile int never = 0;
+      ptx::mbar_wait_bounded(drain, 0, &never, kWaitNs);
+    }
+  } else {
+    // ------------------------------------------------ softmax warpgroups
+    // A wait that gives up sets the abort flag and the work runs on (every
+    // later wait returns at once), so that every warp meets the same named
+    // barriers; nothing is written out after an abort.
+    const int wg = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int st_tid = ((warp - 2) & 3) * 32 + lane;
+    const int row = quarter * 32 + lane;  // TMEM lane: tile row (S) / d (O)
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int h = row / KR;               // this row's head within the group
+    const int k = row % KR;               // ... and key within the tile
+    const int h_first = (quarter * 32) / KR;  // first head of this warp
+    const int hw = h - h_first;           // 0 .. HPW-1
+    const int bar_wg = 1 + wg;
+    const uint32_t tmem_s = tmem + wg * C::kWgCols;
+    const uint32_t tmem_o = tmem_s + 2 * C::kN1;
+    uint8_t* const pbuf_wg = sm + C::kOffP + wg * C::kPBytes;
+    float* const corr_wg = corr_all + wg * 2 * GR;
+
+    uint32_t n_base = 0;  // tiles of all earlier units
+    for (int it = 0;; ++it) {
+      const int slot = it & 1;
+      const bool got = ptx::mbar_wait_bounded(ifull(slot), (it >> 1) & 1, abort_flag, kWaitNs);
+      // one decision for both groups: both take the same path through the
+      // barriers below
+      if (ptx::named_bar_red_or(kBarAll, 128 * kWG, !got)) {
+        if (st_tid == 0) set_abort(abort_flag, a.status);
+        break;
+      }
+      const It& I = item(slot);
+      if (!I.valid) break;
+      const int b = I.b, L = I.L, TS = I.TS, n0 = I.n0;
+      const int key_begin = I.t_begin * 128;
+      const float two_m_shift = ldexpf(1.f, -I.shift);
+      const float c2 = I.cs[h] * two_m_shift * kLog2e;  // raw score -> log2 units, this row's head
+
+      float l_thr[RH], m_cur[RH];  // deferred row sums (of 448 p); running column max (raw)
+      int lim[RH];                 // last visible key of column n of this row's head (-1: none)
+#pragma unroll
+      for (int nn = 0; nn < RH; ++nn) {
+        l_thr[nn] = 0.f;
+        m_cur[nn] = -INFINITY;
+        const int qrow = n0 + nn;
+        int l = a.causal ? L - a.q_len + qrow / a.h_r : L - 1;
+        l = l < L - 1 ? l : L - 1;
+        lim[nn] = qrow < a.n_q ? l : -1;
+      }
+
+      bool ok = true;
+      int t_last = -1;  // this group's last local tile of the unit
+      for (int i = static_cast<int>((static_cast<uint32_t>(wg) - n_base) & 1u); i < TS; i += 2) {
+        const uint32_t n = n_base + i;
+        const int t = static_cast<int>(n >> 1);
+        const int sb = t & 1;
+        const bool first = i < 2;
+        const int j = key_begin + i * KR + k;  // this row's key
+        t_last = t;
+        if (!ptx::mbar_wait_bounded(wgbar(wg, sb), (t >> 1) & 1, abort_flag, kWaitNs)) ok = false;
+        ptx::tc_fence_after();
+        float sc[RH];
+        {
+          // this warp's heads' columns (hi and lo parts), then this row's head
+          uint32_t rh[C::W], rl[C::W];
+          const uint32_t s_base = tmem_s + lane_off + sb * C::kN1 + h_first * RH;
+          if constexpr (C::W == 8) {
+            MJ_TMEM_LD8(s_base, rh);
+            if (!kQe4m3) MJ_TMEM_LD8(s_base + GR, rl);
+          } else {
+            MJ_TMEM_LD16(s_base, rh);
+            if (!kQe4m3) MJ_TMEM_LD16(s_base + GR, rl);
+          }
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int nn = 0; nn < RH; ++nn) {
+            float v = __uint_as_float(rh[nn]);
+            if (!kQe4m3) v += __uint_as_float(rl[nn]);
+            if (C::HPW == 2) {
+              float v1 = __uint_as_float(rh[RH + nn]);
+              if (!kQe4m3) v1 += __uint_as_float(rl[RH + nn]);
+              v = hw ? v1 : v;
+            }
+            sc[nn] = (j <= lim[nn]) ? v : -INFINITY;  // select: garbage rows never leak
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(wgbar(wg, 2 + sb));
+
+        // column maxima of this head: shuffles within the head's KR lanes
+        bool moved = false;
+        float corr[RH];
+#pragma unroll
+        for (int nn = 0; nn < RH; ++nn) {
+          float v = sc[nn];
+#pragma unroll
+          for (int off = KR / 2; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+          const float mn = fmaxf(m_cur[nn], v);
+          moved |= (mn != m_cur[nn]);
+          const float mu = (mn == -INFINITY) ? 0.f : mn;
+          corr[nn] = fast_exp2((m_cur[nn] - mu) * c2);  // the -inf guard: 0 for a fresh column
+          m_cur[nn] = mn;
+        }
+        float* corr_b = corr_wg + sb * GR;
+        if (k == 0) {
+#pragma unroll
+          for (int nn = 0; nn < RH; ++nn) corr_b[h * RH + nn] = moved ? corr[nn] : 1.f;
+        }
+        const bool any_moved = ptx::named_bar_red_or(bar_wg, 128, moved);
+        if (moved) {
+#pragma unroll
+          for (int nn = 0; nn < RH; ++nn) l_thr[nn] *= corr[nn];
+        }
+        // This group's P buffer and O are free once the GEMM2 of its previous
+        // tile finished (the one before that was waited for a tile ago, so
+        // the parity names that GEMM2 alone).
+        if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 5), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+        // lazy O correction: O's TMEM lanes are head-dimension rows spanning
+        // every head's columns, so any moved maximum corrects all of them
+        // (the condition is uniform over the group: TMEM access is warp-wide)
+        if (any_moved && !first) {
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < C::kN2; c0 += 16) {
+            uint32_t r[16];
+            MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr_b[(c0 + e) % GR]);
+            MJ_TMEM_ST16(tmem_o + lane_off + c0, r);
+          }
+          ptx::tmem_st_wait();
+        }
+        // 448 p and the row sums
+#pragma unroll
+        for (int nn = 0; nn < RH; ++nn) {
+          const float mu = (m_cur[nn] == -INFINITY) ? 0.f : m_cur[nn];
+          const float p = fast_exp2(fmaf(sc[nn], c2, fmaf(-mu, c2, kLog2P448)));
+          l_thr[nn] += p;
+          sc[nn] = p;
+        }
+        {
+          uint32_t hi[RH / 4], lo[RH / 4];
+          split_p<RH>(sc, hi, lo);
+          uint8_t* prow = pbuf_wg + row * 16;
+          const int ch = h * RH, cl = GR + h * RH;  // this row's hi / lo columns
+          uint8_t* ph = prow + (ch / 16) * (kRows * 16) + (ch % 16);
+          uint8_t* pl = prow + (cl / 16) * (kRows * 16) + (cl % 16);
+          if constexpr (RH == 4) {
+            *reinterpret_cast<uint32_t*>(ph) = hi[0];
+            *reinterpret_cast<uint32_t*>(pl) = lo[0];
+          } else {
+            *reinterpret_cast<uint2*>(ph) = make_uint2(hi[0], hi[1]);
+            *reinterpret_cast<uint2*>(pl) = make_uint2(lo[0], lo[1]);
+          }
+        }
+        // rows past the sequence end: zero their V row (0 * poison must not
+        // reach O; the TMA landed whole pages)
+        if (key_begin + (i + 1) * KR > L) {
+          const int st = n % SV;
+          if (!ptx::mbar_wait_bounded(vfull(st), (n / SV) & 1, abort_flag, kWaitNs)) ok = false;
+          if (j >= L) {
+            uint4* vrow = reinterpret_cast<uint4*>(sm + C::kOffV + st * kTileBytes + row * 128);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(wgbar(wg, 4));
+        if (!ok) set_abort(abort_flag, a.status);
+      }
+      n_base += TS;
+
+      // ---- end of the unit: this group's O is final once its last GEMM2 is
+      if (t_last >= 0 && !ptx::mbar_wait_bounded(wgbar(wg, 5), t_last & 1, abort_flag, kWaitNs)) ok = false;
+      if (!ok) set_abort(abort_flag, a.status);
+      // row sums of this head: shuffles within its KR lanes
+#pragma unroll
+      for (int nn = 0; nn < RH; ++nn) {
+        float v = l_thr[nn];
+#pragma unroll
+        for (int off = KR / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        l_thr[nn] = v;
+      }
+      float* my_m = wg == 0 ? stat0 : stat1 + slot * GR;
+      float* my_l = wg == 0 ? stat0 + GR : stat1 + 2 * GR + slot * GR;
+      if (k == 0) {
+#pragma unroll
+        for (int nn = 0; nn < RH; ++nn) {
+          my_m[h * RH + nn] = m_cur[nn];
+          my_l[h * RH + nn] = l_thr[nn] * (1.f / 448.f);
+        }
+      }
+      const bool fine = !ptx::named_bar_red_or(kBarAll, 128 * kWG, *abort_flag != 0);
+      if (wg == 1) {
+        // group 1 is done with this unit: its stats stay in their slot half
+        // until group 0 has merged them
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(iempty(slot));
+        continue;
+      }
+      // ---- group 0: merge of the two groups' states and the output.  Per
+      // column: the common maximum, each group's weight, the combined sum
+      // (in place of group 0's stats; the weights in group 0's correction
+      // area).
+      float* f0_s = corr_wg;
+      float* f1_s = corr_wg + GR;
+      if (fine && st_tid < GR) {
+        const int c = st_tid, hq = c / RH;
+        const float c2c = I.cs[hq] * two_m_shift * kLog2e;
+        const float m0 = stat0[c], m1 = stat1[slot * GR + c];
+        const float mx = fmaxf(m0, m1);
+        const float f0 = (m0 == -INFINITY) ? 0.f : fast_exp2((m0 - mx) * c2c);
+        const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - mx) * c2c);
+        f0_s[c] = f0;
+        f1_s[c] = f1;
+        stat0[GR + c] = stat0[GR + c] * f0 + stat1[2 * GR + slot * GR + c] * f1;
+        stat0[c] = mx;
+      }
+      ptx::named_bar_sync(bar_wg, 128);
+      if (fine) {
+        ptx::tc_fence_after();
+        const bool final_out = I.nsp <= 1;
+        const int d = row;  // TMEM lane of O = head-dimension index
+        const uint32_t o1 = tmem + C::kWgCols + 2 * C::kN1;  // group 1's O, same lanes
+        // Sixteen columns at a time: O = f0 O_0 + f1 O_1 (hi + lo parts of
+        // each; select, not multiply: a group with no tile left its O stale)
+        // is staged column-major in this group's P buffer (idle now: its
+        // last GEMM2 is done), then written out as whole rows with 16-byte
+        // stores — one store per column and thread would take microseconds
+        // while the KV stream saturates the memory system.
+        float* stage = reinterpret_cast<float*>(pbuf_wg);
+#pragma unroll 1
+        for (int c0 = 0; c0 < GR; c0 += 16) {
+          float ov[16];
+          {
+            uint32_t rh[16], rl[16];
+            MJ_TMEM_LD16(tmem_o + lane_off + c0, rh);
+            MJ_TMEM_LD16(tmem_o + lane_off + GR + c0, rl);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float f0 = f0_s[c0 + e];
+              ov[e] = f0 > 0.f ? (__uint_as_float(rh[e]) + __uint_as_float(rl[e])) * f0 : 0.f;
+            }
+          }
+          {
+            uint32_t qh[16], ql[16];
+            MJ_TMEM_LD16(o1 + lane_off + c0, qh);
+            MJ_TMEM_LD16(o1 + lane_off + GR + c0, ql);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float f1 = f1_s[c0 + e];
+              if (f1 > 0.f) ov[e] += (__uint_as_float(qh[e]) + __uint_as_float(ql[e])) * f1;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) stage[e * kHeadDimDev + d] = ov[e];
+          ptx::named_bar_sync(bar_wg, 128);
+          // 16 rows x 32 four-float pieces
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int q = st_tid + 128 * r;
+            const int e = q >> 5, d4 = (q & 31) * 4;
+            const int c = c0 + e;
+            const int hq = c / RH, qrow = n0 + c % RH;
+            if (qrow < a.n_q) {
+              float4 v = *reinterpret_cast<const float4*>(stage + e * kHeadDimDev + d4);
+              const int g = I.g0 + hq;
+              float f = I.vd[hq] * (1.f / 448.f);
+              if (final_out) {
+                f *= a.scale_o / (stat0[GR + c] + 1e-30f);
+                const __nv_bfloat162 lo2 = __floats2bfloat162_rn(v.x * f, v.y * f);
+                const __nv_bfloat162 hi2 = __floats2bfloat162_rn(v.z * f, v.w * f);
+                uint2 packed;
+                packed.x = *reinterpret_cast<const uint32_t*>(&lo2);
+                packed.y = *reinterpret_cast<const uint32_t*>(&hi2);
+                const int64_t orow = b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + qrow) * kHeadDimDev;
+                *reinterpret_cast<uint2*>(a.o + orow + d4) = packed;
+              } else {
+                v.x *= f;
+                v.y *= f;
+                v.z *= f;
+                v.w *= f;
+                const int64_t pr = part_row(a, b, g, I.slot, qrow);
+                *reinterpret_cast<float4*>(a.o_part + pr * kHeadDimDev + d4) = v;
+              }
+            }
+          }
+          ptx::named_bar_sync(bar_wg, 128);  // the next half reuses the stage
+        }
+        // the P buffer's off-diagonal zeros again (published by the fence
+        // before this group's next P-full arrival)
+        for (int id = st_tid; id < C::kPBytes / 16; id += 128)
+          reinterpret_cast<uint4*>(pbuf_wg)[id] = make_uint4(0u, 0u, 0u, 0u);
+        if (st_tid < GR) {
+          const int c = st_tid, hq = c / RH, nn = c % RH;
+          const int qrow = n0 + nn, g = I.g0 + hq;
+          if (qrow < a.n_q) {
+            const float m_logit = stat0[c] * I.cs[hq] * two_m_shift;
+            const float l = stat0[GR + c];
+            if (final_out) {
+              a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(l);
+            } else {
+              const int64_t pr = part_row(a, b, g, I.slot, qrow);
+              a.m_part[pr] = m_logit;
+              a.l_part[pr] = l;
+            }
+          }
+        }
+      }
+      // both O accumulators and this slot are free again
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(ofree);
+        ptx::mbar_arrive(iempty(slot));
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int G, int RH, bool kQe4m3>
+cudaError_t launch_tcg(const DecodeDev& a, int n_q_tiles, int* sched, int sm_count, cudaStream_t stream) {
+  using C = GCfg<G, RH, kQe4m3>;
+  // the same box choice as the producer: all G heads at once when a page
+  // holds whole tiles
+  const int box_rows = C::KR < a.page_size ? C::KR : a.page_size;
+  const int box_heads = box_rows == C::KR ? G : 1;
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, box_rows, box_heads) ||
+      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, box_rows, box_heads))
+    return cudaErrorInvalidValue;
+  auto kern = decode_tcg_kernel<G, RH, kQe4m3>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+  if (e != cudaSuccess) return e;
+  const int num_units = a.num_work * n_q_tiles * (a.h_k / G);
+  e = cudaMemsetAsync(sched, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return e;
+  const int grid = num_units < sm_count ? num_units : sm_count;
+  kern<<<grid, kThreads, C::kBytes, stream>>>(a, mk, mv, n_q_tiles, num_units, sched);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tcg_supported(int h_k, int n_q, int* heads_per_cta, int* rows_per_head) {
+  // G heads x RH rows per head, G * RH <= 32, a head's keys within one warp
+  // (G >= 4)
+  int rh = n_q <= 4 ? 4 : (n_q <= 8 ? 8 : 0);
+  if (rh == 0) return false;
+  int g = 0;
+  if (rh == 4 && h_k % 8 == 0) {
+    g = 8;
+  } else if (h_k % 4 == 0) {
+    g = 4;
+    rh = 8;
+  }
+  if (g == 0) return false;
+  *heads_per_cta = g;
+  *rows_per_head = rh;
+  return true;
+}
+
+cudaError_t launch_decode_tcg(const DecodeDev& a, int heads_per_cta, int rows_per_head, int n_q_tiles, bool q_e4m3,
+                              int* sched, int sm_count, cudaStream_t stream) {
+  if (heads_per_cta == 8 && rows_per_head == 4)
+    return q_e4m3 ? launch_tcg<8, 4, true>(a, n_q_tiles, sched, sm_count, stream)
+                  : launch_tcg<8, 4, false>(a, n_q_tiles, sched, sm_count, stream);
+  if (heads_per_cta == 4 && rows_per_head == 8)
+    return q_e4m3 ? launch_tcg<4, 8, true>(a, n_q_tiles, sched, sm_count, stream)
+                  : launch_tcg<4, 8, false>(a, n_q_tiles, sched, sm_count, stream);
+  return cudaErrorInvalidValue;
+}
+
+int tcg_smem_bytes(int heads_per_cta, int rows_per_head, bool q_e4m3) {
+  if (heads_per_cta == 8 && rows_per_head == 4) return q_e4m3 ? GCfg<8, 4, true>::kBytes : GCfg<8, 4, false>::kBytes;
+  if (heads_per_cta == 4 && rows_per_head == 8) return q_e4m3 ? GCfg<4, 8, true>::kBytes : GCfg<4, 8, false>::kBytes;
+  return 0;
+}
+
+}  // namespace mj

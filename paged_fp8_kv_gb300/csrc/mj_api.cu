@@ -17,18 +17,38 @@ constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WorkspaceLayout {
-  size_t o_off, m_off, l_off, total;
+  size_t o_off, m_off, l_off, sched_off, total;
 };
 
+// Split partials (when the plan may split), then the persistent kernel's
+// unit counter (reset by the launch itself, in the stream).
 WorkspaceLayout workspace_layout(const mj_decode_params& p) {
-  WorkspaceLayout w{0, 0, 0, 0};
-  if (p.max_splits <= 1) return w;
-  const size_t rows = static_cast<size_t>(p.num_seqs) * p.h_k * p.max_splits * p.q_len * p.h_r;
-  w.o_off = 0;
-  w.m_off = round_up(rows * kHeadDim * sizeof(float));
-  w.l_off = w.m_off + round_up(rows * sizeof(float));
-  w.total = w.l_off + round_up(rows * sizeof(float));
+  WorkspaceLayout w{0, 0, 0, 0, 0};
+  if (p.max_splits > 1) {
+    const size_t rows = static_cast<size_t>(p.num_seqs) * p.h_k * p.max_splits * p.q_len * p.h_r;
+    w.o_off = 0;
+    w.m_off = round_up(rows * kHeadDim * sizeof(float));
+    w.l_off = w.m_off + round_up(rows * sizeof(float));
+    w.total = w.l_off + round_up(rows * sizeof(float));
+  }
+  if (choose_kernel(p).kind == KernelKind::kTensorCoreGrouped) {
+    w.sched_off = w.total;
+    w.total += kAlign;
+  }
   return w;
+}
+
+// SMs of the current device (the persistent kernel's grid), cached per
+// device; 0 when it cannot be read.
+int device_sm_count() {
+  static int cache[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 0;
+  if (dev < 64) cache[dev] = n;
+  return n;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -36,6 +56,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr int kDefaultL2Prefetch = 0;  // tiles; measured choice
 constexpr int kSmemPerSm = 233472;  // 228 KiB usable shared memory per SM
 constexpr int kSmemReservedPerCta = 1024;
+constexpr int kGroupedUnitsPerSm = 6;  // measured: GQA decode, 1 to 8 units per SM
 
 }  // namespace
 
@@ -43,7 +64,9 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
   const int n_q = p.q_len * p.h_r;
   const bool e4m3 = p.q_dtype == MJ_E4M3;
   KernelChoice k{};
+  k.heads_per_cta = 1;
   int smem;
+  int g = 0, rh = 0;
   if (p.kernel == MJ_KERNEL_CUDA_CORE) {
     k.kind = KernelKind::kCudaCore;
     k.rows_per_cta = n_q <= 4 ? 4 : (n_q <= 8 ? 8 : 16);
@@ -51,6 +74,13 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
     static const char* names[2][3] = {{"cc_n4_bf16", "cc_n8_bf16", "cc_n16_bf16"},
                                       {"cc_n4_e4m3", "cc_n8_e4m3", "cc_n16_e4m3"}};
     k.name = names[e4m3][k.rows_per_cta == 4 ? 0 : (k.rows_per_cta == 8 ? 1 : 2)];
+  } else if (p.kernel == MJ_KERNEL_TENSOR_CORE_GROUPED && tcg_supported(p.h_k, n_q, &g, &rh)) {
+    k.kind = KernelKind::kTensorCoreGrouped;
+    k.rows_per_cta = rh;
+    k.heads_per_cta = g;
+    smem = tcg_smem_bytes(g, rh, e4m3);
+    static const char* names[2][2] = {{"tcg_g8r4_bf16", "tcg_g4r8_bf16"}, {"tcg_g8r4_e4m3", "tcg_g4r8_e4m3"}};
+    k.name = names[e4m3][g == 8 ? 0 : 1];
   } else {
     k.kind = KernelKind::kTensorCore;
     k.rows_per_cta = n_q <= 8 ? 8 : (n_q <= 16 ? 16 : 32);
@@ -62,9 +92,14 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
   }
   k.n_q_tiles = (n_q + k.rows_per_cta - 1) / k.rows_per_cta;
   int per_sm = kSmemPerSm / (smem + kSmemReservedPerCta);
-  const int cap = k.kind == KernelKind::kTensorCore ? tc_min_blocks(k.rows_per_cta, e4m3) : 16;
+  int cap = 16;
+  if (k.kind == KernelKind::kTensorCore) cap = tc_min_blocks(k.rows_per_cta, e4m3);
+  if (k.kind == KernelKind::kTensorCoreGrouped) cap = 1;  // owns the SM: all of TMEM, a deep ring
   if (per_sm > cap) per_sm = cap;
-  k.ctas_per_sm = per_sm < 1 ? 1 : per_sm;
+  k.ctas_per_sm = (per_sm < 1 ? 1 : per_sm) * k.heads_per_cta;
+  // The persistent kernel takes units from a queue: the plan cuts about six
+  // units per SM, so that the greedy queue (longest first) ends balanced.
+  if (k.kind == KernelKind::kTensorCoreGrouped) k.ctas_per_sm *= kGroupedUnitsPerSm;
   return k;
 }
 
@@ -186,7 +221,14 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   const KernelChoice kc = choose_kernel(p);
   cudaError_t e = cudaSuccess;
   if (ev[0] && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return MJ_ERR_CUDA;
-  if (kc.kind == KernelKind::kTensorCore)
+  if (kc.kind == KernelKind::kTensorCoreGrouped) {
+    const int sms = device_sm_count();
+    if (sms < 1) return MJ_ERR_CUDA;
+    int* sched = reinterpret_cast<int*>(static_cast<char*>(a.workspace) + ws.sched_off);
+    e = launch_decode_tcg(d, kc.heads_per_cta, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, sched, sms,
+                          stream);
+  }
+  else if (kc.kind == KernelKind::kTensorCore)
     e = launch_decode_tc(d, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
   else
     e = launch_decode_cc(d, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);

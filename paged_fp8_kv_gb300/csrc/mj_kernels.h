@@ -1,6 +1,7 @@
 // Launchers of the device kernels (host-callable, defined in the .cu files).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "mj_device.cuh"
@@ -20,6 +21,20 @@ cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles
                              cudaStream_t stream);
 int tc_smem_bytes(int rows_per_cta, bool q_e4m3);
 int tc_min_blocks(int rows_per_cta, bool q_e4m3);  // co-resident CTAs per SM the kernel is built for
+
+// Head-grouped tensor-core decode: one CTA serves heads_per_cta kv heads
+// (rows_per_head packed query rows each); tcg_supported picks the shape.
+// Persistent: min(units, sm_count) CTAs take units from the counter at
+// `sched` (device memory, zeroed by the launch in the stream).
+cudaError_t launch_decode_tcg(const DecodeDev& a, int heads_per_cta, int rows_per_head, int n_q_tiles, bool q_e4m3,
+                              int* sched, int sm_count, cudaStream_t stream);
+int tcg_smem_bytes(int heads_per_cta, int rows_per_head, bool q_e4m3);
+
+// TMA descriptor of a paged e4m3 pool seen as (d bytes, rows in page, kv
+// heads, pages); one box is box_rows rows of box_heads heads (head-major in
+// shared memory), 128-byte swizzle.
+bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, int num_pages, int64_t s_row,
+                 int64_t s_head, int64_t s_page, int box_rows, int box_heads);
 
 // Merge of split sequences' partials into O / LSE; max_n_splits (> 1) sizes
 // the number of warps that share one row.

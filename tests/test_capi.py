@@ -33,8 +33,8 @@ def test_every_declared_symbol_is_exported():
         assert hasattr(L, n), f"{n} declared in mj.h but not exported"
 
 
-def _params(b, h_k=1, q_len=1, h_r=4, ps=16, max_blocks=1 << 16, max_splits=16, q_dtype=0):
-    return mj.make_params(b, q_len, h_k, h_r, ps, max_blocks, 100000, True, q_dtype, max_splits)
+def _params(b, h_k=1, q_len=1, h_r=4, ps=16, max_blocks=1 << 16, max_splits=16, q_dtype=0, kernel=0):
+    return mj.make_params(b, q_len, h_k, h_r, ps, max_blocks, 100000, True, q_dtype, max_splits, 128, kernel)
 
 
 @pytest.mark.parametrize("case", json.load(open(os.path.join(ROOT, "tests", "golden", "plan_examples.json")))["cases"])
@@ -187,3 +187,24 @@ def test_status_strings_and_kernel_name():
     assert mj.status_string(mj.MJ_OK) == "ok"
     assert "timed out" in mj.status_string(mj.MJ_ERR_TIMEOUT)
     assert mj.kernel_name(_params(2, h_r=4)).startswith(("cc_", "tc_"))
+
+
+def test_grouped_kernel_choice_and_plan():
+    # the head-grouped kernel: 8 heads x 4 rows or 4 heads x 8 rows per CTA
+    grouped = mj.MJ_KERNEL_TENSOR_CORE_GROUPED
+    assert mj.kernel_name(_params(2, h_k=8, h_r=4, kernel=grouped)) == "tcg_g8r4_bf16"
+    assert mj.kernel_name(_params(2, h_k=8, h_r=8, kernel=grouped)) == "tcg_g4r8_bf16"
+    assert mj.kernel_name(_params(2, h_k=12, h_r=2, kernel=grouped)) == "tcg_g4r8_bf16"
+    # no group of four heads, or more than 8 rows per head: refused
+    for h_k, h_r in [(2, 4), (6, 4), (8, 16)]:
+        p = _params(2, h_k=h_k, h_r=h_r, kernel=grouped)
+        with pytest.raises(mj.MjError):
+            mj.kernel_name(p)
+        assert _plan_status(p, [10, 10]) == mj.MJ_ERR_UNSUPPORTED
+    # its occupancy counts (CTA, kv head) pairs, so one wave covers every
+    # head of sm_count * CTAs-per-SM * 8 / h_k work items
+    p = _params(4, h_k=8, h_r=4, kernel=grouped)
+    plan = mj.decode_plan(p, [1000, 2000, 3000, 4000])
+    assert plan.opts.ctas_per_sm % 8 == 0 and plan.opts.n_q_tiles == 1
+    ref = plan_ref([1000, 2000, 3000, 4000], 8, 1, 152, plan.opts.ctas_per_sm, 16)
+    assert plan.work.tolist() == [list(w) for w in ref.work]
