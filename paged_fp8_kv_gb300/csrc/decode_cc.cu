@@ -21,6 +21,7 @@
 
 #include "mj_device.cuh"
 #include "mj_kernels.h"
+#include "sm100_ptx.cuh"
 
 namespace mj {
 namespace {
@@ -42,6 +43,9 @@ struct CcSmem {
 template <int NT, bool kQe4m3>
 __global__ void __launch_bounds__(kThreads)
 decode_cc_kernel(const DecodeDev a, int n_q_tiles) {
+  // the merge (a programmatic dependent) may launch now: its CTAs wait
+  // for this grid's completion before reading what it writes
+  ptx::griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   CcSmem<NT>& sm = *reinterpret_cast<CcSmem<NT>*>(smem_raw);
 

@@ -218,6 +218,9 @@ template <int R, bool kQe4m3>
 __global__ void __launch_bounds__((TcCfg<R, kQe4m3>::kThreads), (TcCfg<R, kQe4m3>::kMinBlocks))
 decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
+  // the merge (a programmatic dependent) may launch now: its CTAs wait
+  // for this grid's completion before reading what it writes
+  ptx::griddep_launch_dependents();
   using C = TcCfg<R, kQe4m3>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

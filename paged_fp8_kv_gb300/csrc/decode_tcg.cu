@@ -152,6 +152,9 @@ template <int G, int RH, bool kQe4m3>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles, int num_units, int* sched) {
+  // the merge (a programmatic dependent) may launch now: its CTAs wait
+  // for this grid's completion before reading what it writes
+  ptx::griddep_launch_dependents();
   using C = GCfg<G, RH, kQe4m3>;
   using It = Item<G>;
   constexpr int KR = C::KR, GR = C::GR, SK = C::kStagesK, SV = C::kStagesV;

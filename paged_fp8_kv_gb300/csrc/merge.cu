@@ -7,124 +7,146 @@
 //   LSE = max_j m_j + ln(sum_j w_j l_j),
 // and unsplit sequences are left untouched (decode wrote them).
 //
-// kWPR warps share one (packed row, kv head, sequence) and stride over its
-// splits; lane l owns d = 4l..4l+3 (16-byte loads).  Each warp keeps a
-// running (max, sum, O) and folds in kUnroll splits per step, whose loads
-// are all issued before any is used, so a long split list costs few memory
-// round trips.  The warp results are combined in a fixed order: the result
-// does not depend on timing.  kWPR follows the longest split list (1 warp
-// per row for a few splits, 16 for hundreds).
+// One (packed row, kv head, sequence) is served by kWPR warps, each taking
+// up to kPer consecutive splits: lane j of a warp loads split j's (m, l),
+// every lane loads the 16-byte piece d = 4 lane .. 4 lane + 3 of every one
+// of its splits' o, all before any is used (one memory round trip).  The
+// warp's maximum comes from the (m, l) lanes, so O is one pass of FMAs in
+// split order with no rescaling.  With kWPR > 1 the warps' (max, sum, O)
+// are combined in warp order through shared memory.  Every sum runs in a
+// fixed order: the result does not depend on timing.
+//
+// The kernel is launched as a programmatic dependent of the decode kernel:
+// its CTAs can be resident before the decode grid ends and read the split
+// counts (host inputs) meanwhile, and wait for the decode grid only before
+// reading the partials.
 
 #include <cuda_runtime.h>
 
 #include "mj_kernels.h"
+#include "sm100_ptx.cuh"
 
 namespace mj {
 namespace {
 
+constexpr int kPer = 16;      // splits per warp
 constexpr int kCtaWarps = 4;  // warps per CTA when a row needs fewer
-constexpr int kUnroll = 8;
-
-struct Running {
-  float m, l, o[4];
-};
-
-// Folds part (mj, lj, oj) into r: both rescaled to the larger maximum.
-__device__ __forceinline__ void fold(Running& r, float mj, float lj, const float4& oj) {
-  if (mj == -INFINITY) return;  // an empty part adds nothing
-  const float mn = fmaxf(r.m, mj);
-  const float a = (r.m == -INFINITY) ? 0.f : __expf(r.m - mn);
-  const float w = __expf(mj - mn);
-  r.l = fmaf(r.l, a, w * lj);
-  r.o[0] = fmaf(r.o[0], a, w * oj.x);
-  r.o[1] = fmaf(r.o[1], a, w * oj.y);
-  r.o[2] = fmaf(r.o[2], a, w * oj.z);
-  r.o[3] = fmaf(r.o[3], a, w * oj.w);
-  r.m = mn;
-}
 
 template <int kWPR>
 __global__ void __launch_bounds__((kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32) merge_kernel(const DecodeDev a) {
-  constexpr int kRows = kWPR >= kCtaWarps ? 1 : kCtaWarps / kWPR;  // rows per CTA
-  constexpr int kMergeWarps = kWPR;
+  constexpr int kRowsPerCta = kWPR >= kCtaWarps ? 1 : kCtaWarps / kWPR;
   const int lane = threadIdx.x & 31;
-  const int rsub = (threadIdx.x >> 5) / kWPR;  // row within the CTA
-  const int warp = (threadIdx.x >> 5) % kWPR;  // warp within the row
-  const int n = blockIdx.x * kRows + rsub, g = blockIdx.y, b = blockIdx.z;
+  const int wic = threadIdx.x >> 5;         // warp in the CTA
+  const int w = wic % kWPR;                 // warp within the row
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + wic / kWPR;  // (b, g, n), n fastest
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.h_k * a.n_q;
+  if (row >= rows) return;  // uniform over a row's warps (kWPR > 1: one row per CTA)
+  const int n = static_cast<int>(row % a.n_q);
+  const int g = static_cast<int>((row / a.n_q) % a.h_k);
+  const int b = static_cast<int>(row / (static_cast<int64_t>(a.n_q) * a.h_k));
   int nsp = a.n_splits[b];
-  if (nsp <= 1) return;  // uniform over the CTA
+  if (nsp <= 1) return;  // unsplit: decode wrote O; uniform over the row's warps
   nsp = nsp < a.max_splits ? nsp : a.max_splits;
-  const bool live = n < a.n_q;
+  ptx::griddep_wait();  // the decode grid's partials are complete and visible
 
-  __shared__ float s_m[kRows][kMergeWarps], s_l[kRows][kMergeWarps];
-  __shared__ __align__(16) float s_o[kRows][kMergeWarps][kHeadDimDev];
-
-  Running r{-INFINITY, 0.f, {0.f, 0.f, 0.f, 0.f}};
-  const int64_t row0 = part_row(a, b, g, 0, live ? n : 0);
+  const int j0 = w * kPer;
+  const int cnt = nsp - j0 < kPer ? nsp - j0 : kPer;  // this warp's splits (may be <= 0)
+  const int64_t pr0 = part_row(a, b, g, 0, n);
   const int64_t split_stride = a.n_q;  // rows between consecutive slots
-  for (int j0 = warp; live && j0 < nsp; j0 += kMergeWarps * kUnroll) {
-    float mj[kUnroll], lj[kUnroll];
-    float4 oj[kUnroll];
+  float m = -INFINITY, l = 0.f;
+  if (lane < cnt) {
+    const int64_t pr = pr0 + (j0 + lane) * split_stride;
+    m = a.m_part[pr];
+    l = a.l_part[pr];
+  }
+  // unconditional loads (splits past this warp's last read that one again,
+  // with weight 0), so that all of them are in flight at once
+  float4 o[kPer];
+  const int jmax = nsp - 1;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int j = j0 + u * kMergeWarps;
-      mj[u] = -INFINITY;
-      lj[u] = 0.f;
-      oj[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (j < nsp) {
-        const int64_t pr = row0 + j * split_stride;
-        mj[u] = a.m_part[pr];
-        lj[u] = a.l_part[pr];
-        oj[u] = *reinterpret_cast<const float4*>(&a.o_part[pr * kHeadDimDev + lane * 4]);
-      }
+  for (int u = 0; u < kPer; ++u) {
+    const int j = j0 + u < jmax ? j0 + u : jmax;
+    o[u] = *reinterpret_cast<const float4*>(&a.o_part[(pr0 + j * split_stride) * kHeadDimDev + lane * 4]);
+  }
+  asm volatile("" ::: "memory");  // keeps every load above ahead of the first use
+  // this warp's maximum, weights and weighted row sum
+  float mw = m;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
+  const float wt = (m == -INFINITY) ? 0.f : __expf(m - mw);
+  float lw = wt * l;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+  float4 ow = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const float wu = __shfl_sync(0xffffffffu, wt, u);  // 0 past this warp's splits
+    ow.x = fmaf(wu, o[u].x, ow.x);
+    ow.y = fmaf(wu, o[u].y, ow.y);
+    ow.z = fmaf(wu, o[u].z, ow.z);
+    ow.w = fmaf(wu, o[u].w, ow.w);
+  }
+  float mx = mw, lsum = lw;
+  if constexpr (kWPR > 1) {
+    __shared__ float s_m[kWPR], s_l[kWPR];
+    __shared__ __align__(16) float s_o[kWPR][kHeadDimDev];
+    if (lane == 0) {
+      s_m[w] = mw;
+      s_l[w] = lw;
     }
+    *reinterpret_cast<float4*>(&s_o[w][lane * 4]) = ow;
+    __syncthreads();
+    if (w != 0) return;
+    mx = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) fold(r, mj[u], lj[u], oj[u]);
-  }
-  if (lane == 0) {
-    s_m[rsub][warp] = r.m;
-    s_l[rsub][warp] = r.l;
-  }
-  *reinterpret_cast<float4*>(&s_o[rsub][warp][lane * 4]) = make_float4(r.o[0], r.o[1], r.o[2], r.o[3]);
-  __syncthreads();
-
-  // combine: 128 threads per row (kRows rows per CTA share the CTA's threads)
-  const int tpr = blockDim.x / kRows;  // threads per row, >= 32
-  const int cr = threadIdx.x / tpr;
-  const int cn = blockIdx.x * kRows + cr;
-  for (int d = threadIdx.x % tpr; cn < a.n_q && d < kHeadDimDev; d += tpr) {
-    float m_all = -INFINITY;
+    for (int v = 0; v < kWPR; ++v) mx = fmaxf(mx, s_m[v]);
+    lsum = 0.f;
+    ow = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) m_all = fmaxf(m_all, s_m[cr][w]);
-    float l_all = 0.f, o_all = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) {
-      const float ww = (s_m[cr][w] == -INFINITY) ? 0.f : __expf(s_m[cr][w] - m_all);
-      l_all = fmaf(ww, s_l[cr][w], l_all);
-      o_all = fmaf(ww, s_o[cr][w][d], o_all);
+    for (int v = 0; v < kWPR; ++v) {
+      const float f = (s_m[v] == -INFINITY) ? 0.f : __expf(s_m[v] - mx);
+      lsum = fmaf(f, s_l[v], lsum);
+      const float4 ov = *reinterpret_cast<const float4*>(&s_o[v][lane * 4]);
+      ow.x = fmaf(f, ov.x, ow.x);
+      ow.y = fmaf(f, ov.y, ow.y);
+      ow.z = fmaf(f, ov.z, ow.z);
+      ow.w = fmaf(f, ov.w, ow.w);
     }
-    const float inv = l_all > 0.f ? a.scale_o / l_all : 0.f;
-    const int64_t orow = b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + cn) * kHeadDimDev;
-    a.o[orow + d] = __float2bfloat16_rn(o_all * inv);
-    if (d == 0) a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + cn] = m_all + logf(l_all);
   }
+  const float inv = lsum > 0.f ? a.scale_o / lsum : 0.f;
+  const int64_t orow = b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + n) * kHeadDimDev;
+  const __nv_bfloat162 lo2 = __floats2bfloat162_rn(ow.x * inv, ow.y * inv);
+  const __nv_bfloat162 hi2 = __floats2bfloat162_rn(ow.z * inv, ow.w * inv);
+  uint2 packed;
+  packed.x = *reinterpret_cast<const uint32_t*>(&lo2);
+  packed.y = *reinterpret_cast<const uint32_t*>(&hi2);
+  *reinterpret_cast<uint2*>(a.o + orow + lane * 4) = packed;
+  if (lane == 0) a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + n] = mx + logf(lsum);
 }
 
 template <int kWPR>
 cudaError_t launch_merge_t(const DecodeDev& a, cudaStream_t stream) {
-  constexpr int kRows = kWPR >= kCtaWarps ? 1 : kCtaWarps / kWPR;
+  constexpr int kRowsPerCta = kWPR >= kCtaWarps ? 1 : kCtaWarps / kWPR;
   constexpr int kThreads = (kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32;
-  dim3 grid((a.n_q + kRows - 1) / kRows, a.h_k, a.num_seqs);
-  merge_kernel<kWPR><<<grid, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.h_k * a.n_q;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel<kWPR>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const DecodeDev& a, int max_n_splits, cudaStream_t stream) {
-  // about kUnroll splits per warp in one round of loads
-  if (max_n_splits <= kUnroll) return launch_merge_t<1>(a, stream);
-  if (max_n_splits <= 4 * kUnroll) return launch_merge_t<4>(a, stream);
+  if (max_n_splits <= kPer) return launch_merge_t<1>(a, stream);
+  if (max_n_splits <= 4 * kPer) return launch_merge_t<4>(a, stream);
   return launch_merge_t<16>(a, stream);
 }
 

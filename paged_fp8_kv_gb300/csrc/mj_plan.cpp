@@ -5,6 +5,7 @@
 // call, so it can run on any host thread while the GPU works.
 
 #include <algorithm>
+#include <queue>
 #include <cstring>
 #include <vector>
 
@@ -40,6 +41,18 @@ namespace {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Plan model constants (GB300, measured): K+V bytes of one 128-row tile of
+// one kv head; sustained KV bandwidth; time per tile of a CTA streaming
+// alone; the per-CTA start cost in tiles; the merge kernel; the margin a
+// finer plan must win by.
+constexpr double kTilePairBytes = 128.0 * 256.0;
+constexpr double kPlanBandwidth = 5.0e6;  // bytes per microsecond
+constexpr double kPlanTileUs = 1.2;
+constexpr int64_t kPlanCtaOverheadTiles = 1;
+constexpr double kPlanMergeUs = 8.0;
+constexpr double kPlanMargin = 0.95;
+constexpr int64_t kPlanModelMaxUnits = 1 << 16;
+
 struct Item {
   int32_t seq, begin, end, slot;
 };
@@ -62,6 +75,7 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
     return MJ_ERR_INVALID_ARG;
 
   const KernelChoice kc = choose_kernel(*params);
+  const bool default_cps = opts->ctas_per_sm == 0;
   if (opts->sm_count == 0) opts->sm_count = kDefaultSmCount;
   if (opts->ctas_per_sm == 0) opts->ctas_per_sm = kc.ctas_per_sm;
   if (opts->n_q_tiles == 0) opts->n_q_tiles = kc.n_q_tiles;
@@ -78,9 +92,6 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
     longest = std::max(longest, tiles[i]);
   }
 
-  const int64_t per_wave = static_cast<int64_t>(opts->sm_count) * opts->ctas_per_sm;
-  const int64_t slots =
-      std::max<int64_t>(1, per_wave / (static_cast<int64_t>(params->h_k) * opts->n_q_tiles));
   const int64_t floor_chunk =
       std::max<int64_t>(opts->min_chunk_tiles, ceil_div(longest, params->max_splits));
 
@@ -90,14 +101,15 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
     return s;
   };
 
-  int64_t chunk;
-  if (opts->force_splits > 0) {
-    chunk = std::max(floor_chunk, ceil_div(longest, opts->force_splits));
-  } else if (b >= slots || params->max_splits == 1) {
-    chunk = longest;
-  } else {
-    // Smallest chunk in [floor_chunk, longest] whose chunks fit one wave;
-    // total_chunks() is non-increasing in chunk.
+  // The occupancy-pinned chunk for `ctas_per_sm` (co-resident (CTA, kv
+  // head) pairs per SM): the smallest chunk whose chunks fill one wave.
+  auto chunk_for = [&](int64_t ctas_per_sm) -> int64_t {
+    const int64_t per_wave = static_cast<int64_t>(opts->sm_count) * ctas_per_sm;
+    const int64_t slots =
+        std::max<int64_t>(1, per_wave / (static_cast<int64_t>(params->h_k) * opts->n_q_tiles));
+    if (opts->force_splits > 0) return std::max(floor_chunk, ceil_div(longest, opts->force_splits));
+    if (b >= slots || params->max_splits == 1) return longest;
+    // total_chunks() is non-increasing in chunk
     int64_t lo = floor_chunk, hi = std::max(floor_chunk, longest);
     while (lo < hi) {
       const int64_t mid = lo + (hi - lo) / 2;
@@ -106,9 +118,53 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
       else
         lo = mid + 1;
     }
-    chunk = lo;
+    return lo;
+  };
+
+  // Library default for the per-head kernels: the plan for 1, 2 or 4 times
+  // the co-resident CTAs, whichever a simple model says ends first.  One
+  // wave of the occupancy-pinned plan leaves SMs idle behind the longest
+  // chunk when a few long sequences dominate; a finer plan balances (the
+  // hardware hands the next CTA to the first free slot) but may add a
+  // merge.  Model: time = max(bytes / bandwidth, longest slot of a greedy
+  // longest-first assignment x time per tile of a lone CTA) + the merge.
+  if (default_cps && opts->force_splits == 0 && params->max_splits > 1 &&
+      kc.kind != KernelKind::kTensorCoreGrouped) {
+    const int64_t units_per_item = static_cast<int64_t>(params->h_k) * opts->n_q_tiles;
+    const int64_t n_slots = static_cast<int64_t>(opts->sm_count) * kc.ctas_per_sm;
+    int64_t sum_tiles = 0;
+    for (int64_t t : tiles) sum_tiles += t;
+    const double stream_us = static_cast<double>(sum_tiles) * units_per_item * kTilePairBytes / kPlanBandwidth;
+    double best = 0;
+    int best_k = 1;
+    for (int k = 1; k <= 4; k *= 2) {
+      const int64_t chunk = chunk_for(static_cast<int64_t>(kc.ctas_per_sm) * k);
+      std::vector<int64_t> costs;
+      for (int64_t t : tiles)
+        for (int64_t beg = 0; beg < t; beg += chunk) costs.push_back(std::min(chunk, t - beg));
+      if (static_cast<int64_t>(costs.size()) * units_per_item > kPlanModelMaxUnits) break;  // keep the plan cheap
+      std::stable_sort(costs.begin(), costs.end(), [](int64_t x, int64_t y) { return x > y; });
+      std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> load;
+      for (int64_t i = 0; i < n_slots; ++i) load.push(0);
+      int64_t makespan = 0;
+      for (int64_t c : costs)
+        for (int64_t u = 0; u < units_per_item; ++u) {
+          const int64_t t = load.top() + c + kPlanCtaOverheadTiles;
+          load.pop();
+          load.push(t);
+          makespan = std::max(makespan, t);
+        }
+      const bool splits = static_cast<int64_t>(costs.size()) > b;
+      const double est = std::max(stream_us, makespan * kPlanTileUs) + (splits ? kPlanMergeUs : 0.0);
+      if (k == 1 || est < best * kPlanMargin) {
+        best = est;
+        best_k = k;
+      }
+    }
+    opts->ctas_per_sm = kc.ctas_per_sm * best_k;
   }
 
+  const int64_t chunk = chunk_for(opts->ctas_per_sm);
   std::vector<Item> items;
   items.reserve(static_cast<size_t>(total_chunks(chunk)));
   for (int i = 0; i < b; ++i) {

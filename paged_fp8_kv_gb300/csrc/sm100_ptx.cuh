@@ -244,6 +244,15 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int nthreads, bool pred
   return r != 0;
 }
 
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start once every CTA of the grid before it has called
+// griddep_launch_dependents (or exited); griddep_wait returns once that
+// grid has completed and its memory operations are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
