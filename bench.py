@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--max_splits", type=int, default=None)
     ap.add_argument("--num_seqs", type=int, default=None, help="smaller batch of the same config (profiling)")
     ap.add_argument("--kv_layout", default="nhd", choices=["nhd", "hnd", "interleaved", "flashinfer"])
-    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core, 3 head-grouped tensor-core")
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core (swap-AB), 3 head-grouped tensor-core, 4 query-rows tensor-core")
     ap.add_argument("--l2_prefetch", type=int, default=0, help="0 default, -1 off, 1..8 tiles ahead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

@@ -94,12 +94,18 @@ typedef struct {
  *                          the same arithmetic with one CTA per group of 4
  *                          or 8 kv heads, whose rows of each page it reads
  *                          together; needs h_k a multiple of 4 and
- *                          q_len*h_r <= 8 (MJ_ERR_UNSUPPORTED otherwise) */
+ *                          q_len*h_r <= 8 (MJ_ERR_UNSUPPORTED otherwise)
+ *   MJ_KERNEL_TENSOR_CORE_QROWS
+ *                          tcgen05 kernel with 128 packed query rows on the
+ *                          MMA's M and 128 keys on N: one read of the KV per
+ *                          128 rows; MJ_KERNEL_AUTO takes it for
+ *                          q_len*h_r > 64 */
 typedef enum {
   MJ_KERNEL_AUTO = 0,
   MJ_KERNEL_CUDA_CORE = 1,
   MJ_KERNEL_TENSOR_CORE = 2,
-  MJ_KERNEL_TENSOR_CORE_GROUPED = 3
+  MJ_KERNEL_TENSOR_CORE_GROUPED = 3,
+  MJ_KERNEL_TENSOR_CORE_QROWS = 4
 } mj_kernel_pref;
 
 /* Plan knobs (source: `plan_split_kv`).  A field left 0 takes the

@@ -35,6 +35,7 @@ MJ_KERNEL_AUTO = 0
 MJ_KERNEL_CUDA_CORE = 1
 MJ_KERNEL_TENSOR_CORE = 2
 MJ_KERNEL_TENSOR_CORE_GROUPED = 3
+MJ_KERNEL_TENSOR_CORE_QROWS = 4
 
 
 class MjError(RuntimeError):

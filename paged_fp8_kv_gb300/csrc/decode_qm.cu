@@ -1,0 +1,544 @@
+// Split-KV paged decode attention on the tensor cores (tcgen05,
+// kind::f8f6f4) for many packed query rows: query rows on the MMA's M.
+//
+// Sources: the "mjolnir/t5_decode.py" page — `decode` kernel (paged TMA
+// gather with out-of-range pages read as zeros, masking by select, online
+// softmax with the descales folded into the exponent and the -inf guard,
+// lazy O rescale, final-vs-partial epilogue, P stored as e4m3(p * 448)).
+// The swap-AB orientation of the pull request page (KV slots on M) pays off
+// while the live rows are few; past 32 rows it would run one CTA per 32 rows
+// and read the KV once per CTA.  Here one CTA takes 128 packed rows of one
+// kv head (a q tile) and reads each KV tile once for all of them:
+//   S[row, key] = Q[row] . K[key]         A = Q (K-major), B = K tile (K-major)
+//   O[row, d]  += P[row, key] V[key, d]    A = P (K-major), B = V tile (MN-major)
+// with 128 keys per tile.  A TMEM lane is a query row for S and for O, so
+// each softmax thread owns one row: its maximum and sum are thread-local and
+// its O rescale touches only its own TMEM lane.
+//
+// As in the swap-AB kernel, nothing is dequantised: the e4m3 K / V tiles the
+// TMA lands are the operands; bf16 Q is split into hi + lo e4m3 parts
+// (q 2^s = hi + lo) and P into hi + lo (448 p = hi + lo), each part an A
+// operand of its own MMA into the same accumulator.
+//
+// Roles (256 threads): warps 0 and 7 issue the K and V TMA tiles into two
+// rings (a K stage is freed by its GEMM1, a V stage by its GEMM2); warp 1
+// (TMEM allocator) issues GEMM1 and warp 6 GEMM2 (one thread issues a
+// tcgen05.mma only every 70-100 cycles); warps 2-5 load Q and run the
+// softmax, thread = query row.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "mj_device.cuh"
+#include "mj_kernels.h"
+#include "sm100_ptx.cuh"
+
+namespace mj {
+namespace {
+
+constexpr int kRows = 128;                   // query rows per CTA = MMA M; keys per tile = MMA N
+constexpr int kTileBytes = kRows * 128;      // one K or V tile (128 keys x d): 16 KB
+constexpr int kPartBytes = kRows * 128;      // one e4m3 operand of 128 rows x 128 bytes
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legal wait
+constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
+constexpr float kLog2P448 = 8.807354922057604f;  // log2(448)
+constexpr int kThreads = 256;
+constexpr int kMma2Warp = 6;
+constexpr int kVLoadWarp = 7;
+
+template <bool kQe4m3>
+struct QmCfg {
+  static constexpr int kStagesK = 4;
+  static constexpr int kStagesV = 5;
+  static constexpr int kQParts = kQe4m3 ? 1 : 2;
+  static constexpr int kTmemCols = 512;       // S x2 (128 each), O (128)
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kStagesK * kTileBytes;
+  static constexpr int kOffQ = (kStagesK + kStagesV) * kTileBytes;  // [hi | lo] 128 x 128 B each
+  static constexpr int kOffP = kOffQ + kQParts * kPartBytes;        // [hi | lo]
+  static constexpr int kOffBar = kOffP + 2 * kPartBytes;
+  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 2 + 2 + 1 + 1 + 1 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 64 + 1024;
+  static_assert(kBytes <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) {
+  *abort = 1;
+  if (status) atomicExch(status, kStatusTimeout);
+}
+
+__device__ __forceinline__ float round_4_sig_bits(float x) {
+  uint32_t u = __float_as_uint(x);
+  u = (u + 0x7FFFFu + ((u >> 20) & 1u)) & 0xFFF00000u;
+  return __uint_as_float(u);
+}
+
+// 128-byte-swizzled K-major row of an e4m3 operand: 16-byte chunk cc of
+// row r sits at chunk position cc ^ (r % 8).
+__device__ __forceinline__ uint8_t* swz(uint8_t* part, int r, int cc) {
+  return part + r * 128 + ((cc ^ (r & 7)) << 4);
+}
+
+template <bool kQe4m3>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
+                 const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
+  // the merge (a programmatic dependent) may launch now: its CTAs wait
+  // for this grid's completion before reading what it writes
+  ptx::griddep_launch_dependents();
+  using C = QmCfg<kQe4m3>;
+  constexpr int SK = C::kStagesK, SV = C::kStagesV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(sm);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
+  int* q_shift = reinterpret_cast<int*>(sm + C::kOffMisc + 8);
+  float* amax_red = reinterpret_cast<float*>(sm + C::kOffMisc + 16);  // [4]
+
+  // mbarriers: K ring (full, empty), V ring (full, empty), S full x2, S
+  // free x2, P full, P free, Q ready, MMA drain
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto kfull = [&](int s) { return bar0 + 8u * s; };
+  auto kempty = [&](int s) { return bar0 + 8u * (SK + s); };
+  auto vfull = [&](int s) { return bar0 + 8u * (2 * SK + s); };
+  auto vempty = [&](int s) { return bar0 + 8u * (2 * SK + SV + s); };
+  constexpr int kB = 2 * (SK + SV);
+  auto sfull = [&](int s) { return bar0 + 8u * (kB + s); };
+  auto sfree = [&](int s) { return bar0 + 8u * (kB + 2 + s); };
+  const uint32_t pfull = bar0 + 8u * (kB + 4);
+  const uint32_t pfree = bar0 + 8u * (kB + 5);
+  const uint32_t qready = bar0 + 8u * (kB + 6);
+  const uint32_t drain = bar0 + 8u * (kB + 7);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  // Linear grid, work item outermost (the plan's longest-first order holds).
+  const int g = blockIdx.x % a.h_k;
+  const int rest = blockIdx.x / a.h_k;
+  const int qt = rest % n_q_tiles;
+  const int w_idx = rest / n_q_tiles;
+  const int n0 = qt * kRows;
+
+  const int4 item = reinterpret_cast<const int4*>(a.work)[w_idx];
+  const int b = item.x, t_begin = item.y, t_end = item.z, slot = item.w;
+  if (t_end <= t_begin) return;  // padding item
+  const int L = a.seq_lens[b];
+  const int T = t_end - t_begin;  // tiles of 128 keys
+  const int key_begin = t_begin * kRows;
+
+  if (tid == 0) {
+    for (int s = 0; s < SK; ++s) {
+      ptx::mbar_init(kfull(s), 1);
+      ptx::mbar_init(kempty(s), 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      ptx::mbar_init(vfull(s), 1);
+      ptx::mbar_init(vempty(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(sfull(s), 1);
+      ptx::mbar_init(sfree(s), 4);
+    }
+    ptx::mbar_init(pfull, 4);
+    ptx::mbar_init(pfree, 1);
+    ptx::mbar_init(qready, 1);
+    ptx::mbar_init(drain, 2);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sbase + C::kOffMisc, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_s = tmem;             // S buffers at columns 0 and 128
+  const uint32_t tmem_o = tmem + 2 * kRows;  // O at columns 256..383
+
+  if (warp == 0 || warp == kVLoadWarp) {
+    // ----------------------------------------------------------- producers
+    // A tile is keys [k0, k0 + 128) of kv head g: 128 / box_rows boxes of
+    // box_rows rows (one per page when pages are shorter than a tile), box
+    // jb on lane jb.  Block-table entries come from a register window (lane
+    // l holds block wbase + l) refilled 32 blocks ahead.
+    const bool is_k = warp == 0;
+    const int NS = is_k ? SK : SV;
+    const uint32_t ring = sbase + (is_k ? C::kOffK : C::kOffV);
+    const CUtensorMap* tmap = is_k ? &tmap_k : &tmap_v;
+    auto full = [&](int st) { return is_k ? kfull(st) : vfull(st); };
+    auto empty = [&](int st) { return is_k ? kempty(st) : vempty(st); };
+    const int PS = a.page_size;
+    const int box_rows = PS < kRows ? PS : kRows;
+    const int nbox = kRows / box_rows;
+    const bool active = lane < nbox;
+    const int64_t bt_row = static_cast<int64_t>(b) * a.max_blocks;
+    int valid_pages = (L + PS - 1) / PS;
+    valid_pages = valid_pages < a.max_blocks ? valid_pages : a.max_blocks;
+    auto load_win = [&](int base) -> int {
+      const int blk = base + lane;
+      return blk < valid_pages ? a.block_table[bt_row + blk] : a.num_pages;
+    };
+    if (lane == 0) ptx::prefetch_tmap(tmap);
+    // a tile spans nbox whole blocks (or lies in one block) and the window
+    // starts at the item's first block, so a tile never straddles windows
+    int wbase = key_begin / PS;
+    int win = load_win(wbase);
+    int win_next = load_win(wbase + 32);
+    int issued = 0;
+    for (int i = 0; i < T; ++i) {
+      const int st = i % NS;
+      if (i >= NS) {
+        const bool freed = ptx::mbar_wait_bounded(empty(st), ((i / NS) - 1) & 1, abort_flag, kWaitNs);
+        if (__any_sync(0xffffffffu, !freed)) {
+          if (lane == 0) set_abort(abort_flag, a.status);
+          break;
+        }
+      }
+      const int key0 = key_begin + i * kRows;
+      if (key0 / PS >= wbase + 32) {  // uniform over the warp
+        wbase += 32;
+        win = win_next;
+        win_next = load_win(wbase + 32);
+      }
+      const int key = key0 + lane * box_rows;
+      const int pg = __shfl_sync(0xffffffffu, win, (key / PS - wbase) & 31);
+      const int page = (active && key < L) ? pg : a.num_pages;
+      const int row_off = key % PS;
+      if (lane == 0) ptx::mbar_arrive_expect_tx(full(st), kTileBytes);
+      __syncwarp();
+      if (active) ptx::tma_load_4d(ring + st * kTileBytes + lane * box_rows * 128, tmap, full(st), 0, row_off, g, page);
+      issued = i + 1;
+    }
+    if (*abort_flag && lane == 0) {
+      volatile int never = 0;
+      for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
+        ptx::mbar_wait_bounded(full(i % NS), (i / NS) & 1, &never, kWaitNs / 4);
+    }
+  } else if (warp == 1 || warp == kMma2Warp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const bool gemm1 = warp == 1;
+      bool ok = ptx::mbar_wait_bounded(qready, 0, abort_flag, kWaitNs);
+      const uint32_t idesc_s = ptx::idesc_e4m3(kRows, kRows, false, false);  // S = Q K^T
+      const uint32_t idesc_o = ptx::idesc_e4m3(kRows, kRows, false, true);   // O = P V, V MN-major
+      const uint64_t qdesc = ptx::smem_desc(sbase + C::kOffQ, 16, 1024, ptx::kSwizzle128B);
+      const uint64_t kdesc0 = ptx::smem_desc(sbase + C::kOffK, 16, 1024, ptx::kSwizzle128B);
+      const uint64_t pdesc = ptx::smem_desc(sbase + C::kOffP, 16, 1024, ptx::kSwizzle128B);
+      const uint64_t vdesc0 = ptx::smem_desc(sbase + C::kOffV, 0, 1024, ptx::kSwizzle128B);
+      constexpr uint64_t kPartStep = kPartBytes >> 4;  // descriptor step to the lo part
+      for (int i = 0; ok && i < T; ++i) {
+        const int sb = i & 1;
+        if (gemm1) {
+          const int st = i % SK;
+          if (!ptx::mbar_wait_bounded(kfull(st), (i / SK) & 1, abort_flag, kWaitNs) ||
+              (i >= 2 && !ptx::mbar_wait_bounded(sfree(sb), ((i >> 1) - 1) & 1, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t kdesc = kdesc0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // one K step = 32 bytes of d
+#pragma unroll
+            for (int part = 0; part < C::kQParts; ++part)
+              ptx::mma_e4m3(tmem_s + sb * kRows, qdesc + part * kPartStep + 2 * kk, kdesc + 2 * kk, idesc_s,
+                            (kk > 0 || part > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(sfull(sb));
+          ptx::mma_commit(kempty(st));
+        } else {
+          const int st = i % SV;
+          if (!ptx::mbar_wait_bounded(pfull, i & 1, abort_flag, kWaitNs) ||
+              !ptx::mbar_wait_bounded(vfull(st), (i / SV) & 1, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t vdesc = vdesc0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // one K step = 32 keys
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+              ptx::mma_e4m3(tmem_o, pdesc + part * kPartStep + 2 * kk, vdesc + 256 * kk, idesc_o,
+                            (i > 0 || kk > 0 || part > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(pfree);
+          ptx::mma_commit(vempty(st));
+        }
+      }
+      if (!ok) set_abort(abort_flag, a.status);
+      ptx::mma_commit(drain);
+      volatile int never = 0;
+      ptx::mbar_wait_bounded(drain, 0, &never, kWaitNs);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    // Thread = query row r (TMEM lane r of S and O); warps 2-5 cover the
+    // four lane quarters.  A wait that gives up sets the abort flag and the
+    // loop runs on (later waits return at once), so every warp takes the
+    // same path; nothing is written out after an abort.
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int st_tid = (warp - 2) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    constexpr int kBarSm = 1;
+    const int qrow = n0 + r;
+    const bool live = qrow < a.n_q;
+    const float qd = a.qd[b * a.qd_seq + g * a.qd_head];
+    const float kd = a.kd[b * a.kd_seq + g * a.kd_head];
+    const float vd = a.vd[b * a.vd_seq + g * a.vd_head];
+
+    // ---- Q row r -> two (bf16) or one (e4m3) K-major operand rows
+    {
+      uint4 raw[kQe4m3 ? 8 : 16];
+      const int64_t off = b * a.q_seq + (static_cast<int64_t>(g) * a.n_q + (live ? qrow : 0)) * kHeadDimDev;
+      if (kQe4m3) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + off);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) raw[cc] = live ? src[cc] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(swz(sm + C::kOffQ, r, cc)) = raw[cc];
+        if (st_tid == 0) *q_shift = 0;
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(kBarSm, 128);
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + off);
+#pragma unroll
+        for (int w = 0; w < 16; ++w) raw[w] = live ? src[w] : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t mbits = 0;  // bf16 |q| max: integer max of the magnitude bits
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+          const uint32_t v4[4] = {raw[w].x, raw[w].y, raw[w].z, raw[w].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) mbits = max(mbits, max(v4[e] & 0x7FFFu, (v4[e] >> 16) & 0x7FFFu));
+        }
+        float amax = __uint_as_float(mbits << 16);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) amax_red[warp - 2] = amax;
+        ptx::named_bar_sync(kBarSm, 128);
+        amax = fmaxf(fmaxf(amax_red[0], amax_red[1]), fmaxf(amax_red[2], amax_red[3]));
+        int shift = 0;
+        if (amax > 0.f) {
+          const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+          shift = 7 - e;  // max |q| 2^shift in [128, 256)
+          shift = shift > 126 ? 126 : (shift < -126 ? -126 : shift);
+        }
+        const float qscale = ldexpf(1.f, shift);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {  // 16 elements = two 16-byte words of bf16
+          uint32_t hw[4], lw[4];
+          const uint32_t w8[8] = {raw[2 * cc].x,     raw[2 * cc].y,     raw[2 * cc].z,     raw[2 * cc].w,
+                                  raw[2 * cc + 1].x, raw[2 * cc + 1].y, raw[2 * cc + 1].z, raw[2 * cc + 1].w};
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            float x[4], hf[4];
+            x[0] = __uint_as_float(w8[2 * wi] << 16) * qscale;
+            x[1] = __uint_as_float(w8[2 * wi] & 0xFFFF0000u) * qscale;
+            x[2] = __uint_as_float(w8[2 * wi + 1] << 16) * qscale;
+            x[3] = __uint_as_float(w8[2 * wi + 1] & 0xFFFF0000u) * qscale;
+            const uint16_t h01 = ptx::f32x2_to_e4m3x2(x[0], x[1]);
+            const uint16_t h23 = ptx::f32x2_to_e4m3x2(x[2], x[3]);
+            e4m3x4_to_f32(static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16), hf);
+            const uint16_t l01 = ptx::f32x2_to_e4m3x2(x[0] - hf[0], x[1] - hf[1]);
+            const uint16_t l23 = ptx::f32x2_to_e4m3x2(x[2] - hf[2], x[3] - hf[3]);
+            hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
+            lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+          }
+          *reinterpret_cast<uint4*>(swz(sm + C::kOffQ, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(swz(sm + C::kOffQ + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        if (st_tid == 0) *q_shift = shift;
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(kBarSm, 128);
+      }
+      if (st_tid == 0) ptx::mbar_arrive(qready);
+    }
+    const int shift = *q_shift;
+    // raw (computed) score -> logit and -> log2 units; 2^-shift undoes the Q scaling
+    const float scale_l = a.softmax_scale * qd * kd * ldexpf(1.f, -shift);
+    const float c2 = scale_l * kLog2e;
+    // last visible key of this row (-1: none)
+    int lim = a.causal ? L - a.q_len + qrow / a.h_r : L - 1;
+    lim = lim < L - 1 ? lim : L - 1;
+    if (!live) lim = -1;
+
+    float m_run = -INFINITY;  // running row max (raw units)
+    float l_run = 0.f;        // running row sum of 448 p
+    bool ok = true;
+    for (int i = 0; i < T; ++i) {
+      const int sb = i & 1;
+      const int key0 = key_begin + i * kRows;
+      if (!ptx::mbar_wait_bounded(sfull(sb), (i >> 1) & 1, abort_flag, kWaitNs)) ok = false;
+      ptx::tc_fence_after();
+      float s[kRows];
+#pragma unroll
+      for (int c0 = 0; c0 < kRows; c0 += 16) {
+        uint32_t rr[16];
+        MJ_TMEM_LD16(tmem_s + lane_off + sb * kRows + c0, rr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) s[c0 + e] = __uint_as_float(rr[e]);
+      }
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sfree(sb));
+      // mask by select (garbage or poison keys never leak), row max
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kRows; ++c) {
+        s[c] = (key0 + c <= lim) ? s[c] : -INFINITY;
+        mt = fmaxf(mt, s[c]);
+      }
+      const float m_new = fmaxf(m_run, mt);
+      const float mu = (m_new == -INFINITY) ? 0.f : m_new;  // the -inf guard
+      // this row's P buffer and O are free once GEMM2 of the previous tile ran
+      if (i > 0 && !ptx::mbar_wait_bounded(pfree, (i - 1) & 1, abort_flag, kWaitNs)) ok = false;
+      const bool moved = m_new != m_run;
+      const float corr = moved ? fast_exp2((m_run - mu) * c2) : 1.f;  // 0 for a fresh row
+      l_run *= corr;
+      m_run = m_new;
+      // lazy O correction: each row rescales its own TMEM lane, but TMEM
+      // access is warp-wide, so a warp corrects when any of its rows moved
+      if (i > 0 && __any_sync(0xffffffffu, moved)) {
+        {
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < kRows; c0 += 16) {
+            uint32_t rr[16];
+            MJ_TMEM_LD16(tmem_o + lane_off + c0, rr);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
+            MJ_TMEM_ST16(tmem_o + lane_off + c0, rr);
+          }
+          ptx::tmem_st_wait();
+        }
+      }
+      // 448 p, the row sum, and the hi / lo e4m3 parts of P row r
+      const float bias = fmaf(-mu, c2, kLog2P448);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          float x[4], h[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[e] = fast_exp2(fmaf(s[cc * 16 + wi * 4 + e], c2, bias));
+            l_run += x[e];
+            h[e] = round_4_sig_bits(x[e]);
+          }
+          const uint16_t h01 = ptx::f32x2_to_e4m3x2(h[0], h[1]);
+          const uint16_t h23 = ptx::f32x2_to_e4m3x2(h[2], h[3]);
+          const uint16_t l01 = ptx::f32x2_to_e4m3x2(x[0] - h[0], x[1] - h[1]);
+          const uint16_t l23 = ptx::f32x2_to_e4m3x2(x[2] - h[2], x[3] - h[3]);
+          hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
+          lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+        }
+        *reinterpret_cast<uint4*>(swz(sm + C::kOffP, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(swz(sm + C::kOffP + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      // keys past the sequence end: zero their V rows (0 * poison must not
+      // reach O; the TMA landed whole pages).  Thread r owns key row r.
+      if (key0 + kRows > L) {
+        const int st = i % SV;
+        if (!ptx::mbar_wait_bounded(vfull(st), (i / SV) & 1, abort_flag, kWaitNs)) ok = false;
+        if (key0 + r >= L) {
+          uint4* vrow = reinterpret_cast<uint4*>(sm + C::kOffV + st * kTileBytes + r * 128);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(pfull);
+      if (!ok) set_abort(abort_flag, a.status);
+    }
+
+    // ---- epilogue: `drain` fires once every MMA of both issuers is done
+    if (ok && !ptx::mbar_wait_bounded(drain, 0, abort_flag, kWaitNs)) ok = false;
+    if (!ok) set_abort(abort_flag, a.status);
+    // one decision per warp (TMEM access is warp-wide); rows past n_q load
+    // their lane but store nothing
+    if (__shfl_sync(0xffffffffu, *abort_flag == 0, 0)) {
+      ptx::tc_fence_after();
+      const bool final_out = a.n_splits[b] <= 1;
+      const float l = l_run * (1.f / 448.f);
+      const float f = vd * (1.f / 448.f) * (final_out ? a.scale_o / (l + 1e-30f) : 1.f);
+      const int64_t orow = final_out ? b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + qrow) * kHeadDimDev
+                                     : part_row(a, b, g, slot, qrow) * kHeadDimDev;
+#pragma unroll
+      for (int c0 = 0; c0 < kRows; c0 += 16) {
+        uint32_t rr[16];
+        MJ_TMEM_LD16(tmem_o + lane_off + c0, rr);
+        ptx::tmem_ld_wait();
+        if (!live) continue;
+        if (final_out) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 v2 =
+                __floats2bfloat162_rn(__uint_as_float(rr[2 * e]) * f, __uint_as_float(rr[2 * e + 1]) * f);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(a.o + orow + c0);
+          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.o_part + orow + c0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_float4(__uint_as_float(rr[4 * e]) * f, __uint_as_float(rr[4 * e + 1]) * f,
+                                 __uint_as_float(rr[4 * e + 2]) * f, __uint_as_float(rr[4 * e + 3]) * f);
+        }
+      }
+      const float m_logit = m_run * scale_l;
+      if (!live) {
+      } else if (final_out) {
+        a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(l);
+      } else {
+        const int64_t pr = part_row(a, b, g, slot, qrow);
+        a.m_part[pr] = m_logit;
+        a.l_part[pr] = l;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <bool kQe4m3>
+cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
+  using C = QmCfg<kQe4m3>;
+  const int box_rows = a.page_size < kRows ? a.page_size : kRows;
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, box_rows, 1) ||
+      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, box_rows, 1))
+    return cudaErrorInvalidValue;
+  auto kern = decode_qm_kernel<kQe4m3>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
+  kern<<<grid, kThreads, C::kBytes, stream>>>(a, mk, mv, n_q_tiles);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_qm(const DecodeDev& a, int n_q_tiles, bool q_e4m3, cudaStream_t stream) {
+  return q_e4m3 ? launch_qm<true>(a, n_q_tiles, stream) : launch_qm<false>(a, n_q_tiles, stream);
+}
+
+int qm_smem_bytes(bool q_e4m3) { return q_e4m3 ? QmCfg<true>::kBytes : QmCfg<false>::kBytes; }
+
+}  // namespace mj

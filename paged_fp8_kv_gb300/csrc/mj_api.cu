@@ -57,6 +57,9 @@ constexpr int kDefaultL2Prefetch = 0;  // tiles; measured choice
 constexpr int kSmemPerSm = 233472;  // 228 KiB usable shared memory per SM
 constexpr int kSmemReservedPerCta = 1024;
 constexpr int kGroupedUnitsPerSm = 6;  // measured: GQA decode, 1 to 8 units per SM
+// More packed rows than this go to the query-rows kernel (measured: it wins
+// from 128 rows; at 40 and 64 the swap-AB kernel is faster).
+constexpr int kQRowsFrom = 64;
 
 }  // namespace
 
@@ -74,6 +77,11 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
     static const char* names[2][3] = {{"cc_n4_bf16", "cc_n8_bf16", "cc_n16_bf16"},
                                       {"cc_n4_e4m3", "cc_n8_e4m3", "cc_n16_e4m3"}};
     k.name = names[e4m3][k.rows_per_cta == 4 ? 0 : (k.rows_per_cta == 8 ? 1 : 2)];
+  } else if (p.kernel == MJ_KERNEL_TENSOR_CORE_QROWS || (p.kernel == MJ_KERNEL_AUTO && n_q > kQRowsFrom)) {
+    k.kind = KernelKind::kTensorCoreQRows;
+    k.rows_per_cta = 128;
+    smem = qm_smem_bytes(e4m3);
+    k.name = e4m3 ? "qm_e4m3" : "qm_bf16";
   } else if (p.kernel == MJ_KERNEL_TENSOR_CORE_GROUPED && tcg_supported(p.h_k, n_q, &g, &rh)) {
     k.kind = KernelKind::kTensorCoreGrouped;
     k.rows_per_cta = rh;
@@ -94,7 +102,8 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
   int per_sm = kSmemPerSm / (smem + kSmemReservedPerCta);
   int cap = 16;
   if (k.kind == KernelKind::kTensorCore) cap = tc_min_blocks(k.rows_per_cta, e4m3);
-  if (k.kind == KernelKind::kTensorCoreGrouped) cap = 1;  // owns the SM: all of TMEM, a deep ring
+  if (k.kind == KernelKind::kTensorCoreGrouped || k.kind == KernelKind::kTensorCoreQRows)
+    cap = 1;  // owns the SM: all of TMEM, a deep ring
   if (per_sm > cap) per_sm = cap;
   k.ctas_per_sm = (per_sm < 1 ? 1 : per_sm) * k.heads_per_cta;
   // The persistent kernel takes units from a queue: the plan cuts about six
@@ -221,7 +230,9 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   const KernelChoice kc = choose_kernel(p);
   cudaError_t e = cudaSuccess;
   if (ev[0] && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return MJ_ERR_CUDA;
-  if (kc.kind == KernelKind::kTensorCoreGrouped) {
+  if (kc.kind == KernelKind::kTensorCoreQRows) {
+    e = launch_decode_qm(d, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
+  } else if (kc.kind == KernelKind::kTensorCoreGrouped) {
     const int sms = device_sm_count();
     if (sms < 1) return MJ_ERR_CUDA;
     int* sched = reinterpret_cast<int*>(static_cast<char*>(a.workspace) + ws.sched_off);

@@ -12,7 +12,7 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxSplits = 256;
 constexpr int kDefaultSmCount = 152;  // GB300
 
-enum class KernelKind { kCudaCore = 0, kTensorCore = 1, kTensorCoreGrouped = 2 };
+enum class KernelKind { kCudaCore = 0, kTensorCore = 1, kTensorCoreGrouped = 2, kTensorCoreQRows = 3 };
 
 // The decode kernel mj_decode_attn launches for a problem, and the
 // occupancy facts the plan needs about it.

@@ -30,6 +30,11 @@ cudaError_t launch_decode_tcg(const DecodeDev& a, int heads_per_cta, int rows_pe
                               int* sched, int sm_count, cudaStream_t stream);
 int tcg_smem_bytes(int heads_per_cta, int rows_per_head, bool q_e4m3);
 
+// Query-rows-on-M tensor-core decode: 128 packed rows of one kv head per
+// CTA, one CTA per SM.
+cudaError_t launch_decode_qm(const DecodeDev& a, int n_q_tiles, bool q_e4m3, cudaStream_t stream);
+int qm_smem_bytes(bool q_e4m3);
+
 // TMA descriptor of a paged e4m3 pool seen as (d bytes, rows in page, kv
 // heads, pages); one box is box_rows rows of box_heads heads (head-major in
 // shared memory), 128-byte swizzle.

@@ -208,3 +208,14 @@ def test_grouped_kernel_choice_and_plan():
     assert plan.opts.ctas_per_sm % 8 == 0 and plan.opts.n_q_tiles == 1
     ref = plan_ref([1000, 2000, 3000, 4000], 8, 1, 152, plan.opts.ctas_per_sm, 16)
     assert plan.work.tolist() == [list(w) for w in ref.work]
+
+
+def test_query_rows_kernel_choice():
+    # more than 64 packed rows: the query-rows kernel, 128 rows per q tile
+    assert mj.kernel_name(_params(2, h_k=1, q_len=4, h_r=32)) == "qm_bf16"
+    assert mj.kernel_name(_params(2, h_k=1, q_len=2, h_r=32)) == "tc_r32_bf16"
+    assert mj.kernel_name(_params(2, h_k=1, q_len=1, h_r=32)) == "tc_r32_bf16"
+    qr = mj.MJ_KERNEL_TENSOR_CORE_QROWS
+    assert mj.kernel_name(_params(2, h_k=1, h_r=16, kernel=qr, q_dtype=1)) == "qm_e4m3"
+    plan = mj.decode_plan(_params(4, h_k=1, q_len=16, h_r=32), [1000, 2000, 3000, 4000])
+    assert plan.opts.n_q_tiles == 4

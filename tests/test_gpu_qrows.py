@@ -1,0 +1,131 @@
+"""GPU parity of the query-rows tensor-core kernel
+(MJ_KERNEL_TENSOR_CORE_QROWS; the automatic choice for more than 32 packed
+rows): 128 packed query rows of one kv head on the MMA's M, 128 keys of a
+tile on N, one softmax thread per query row.
+
+Against the fp64 oracle element by element: every sweep shape of the small-
+live-head workload (packed rows 16 to 512, so one to four q tiles and a
+partly filled last tile), bf16 and e4m3 Q, causal and non-causal, every page
+size, empty and ragged lengths, forced splits with the merge, every KV
+layout, descale broadcasts, and the full-size sweep extremes on sampled
+units; plus determinism and graph replay.
+"""
+
+import copy
+
+import numpy as np
+import pytest
+import torch
+
+from paged_fp8_kv_gb300 import synthetic as syn
+from paged_fp8_kv_gb300.session import DecodeSession
+from tests.gpu_helpers import compare, sample_units
+
+pytestmark = pytest.mark.gpu
+
+QROWS = 4  # MJ_KERNEL_TENSOR_CORE_QROWS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_fp8_kv_gb300.build import build
+
+    build()
+
+
+def run(w, nan_workspace=True, kernel=QROWS, **kw):
+    s = DecodeSession(w, kernel=kernel, **kw)
+    assert s.kernel.startswith("qm_"), s.kernel
+    if nan_workspace:
+        s.fill_workspace(float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s.step(status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return s
+
+
+def check(w, units=None, **kw):
+    s = run(w, **kw)
+    return s, compare(w, s.o_host(), s.lse_host(), units=units)
+
+
+@pytest.mark.parametrize("h_r,q_len", syn.SWEEP_POINTS)
+def test_sweep_small(h_r, q_len):
+    w = syn.config(5, h_r=h_r, q_len=q_len, num_seqs=3, len_range=(0, 700))
+    check(w)
+
+
+@pytest.mark.parametrize("h_r,q_len", [(32, 2), (32, 16)])
+def test_sweep_full_sampled(h_r, q_len):
+    w = syn.config(5, h_r=h_r, q_len=q_len)
+    s = run(w, kernel=0)  # the automatic choice
+    compare(w, s.o_host(), s.lse_host(), units=[(0, 0), (77, 0), (127, 0)])
+
+
+def test_spec_verify_noncausal_small():
+    w = syn.config(4, variant="noncausal", num_seqs=5, len_range=(200, 1300))
+    s, _ = check(w)  # 40 packed rows in one q tile
+    assert s.plan.opts.n_q_tiles == 1
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+@pytest.mark.parametrize("q_is_e4m3", [False, True])
+def test_page_sizes_and_q_dtype(page_size, q_is_e4m3):
+    lens = [1, 100, 127, 128, 129, 300, 1000]
+    w = syn.make_workload("qrows", lens, 3, 2, 24, page_size, seed=91 + page_size, q_is_e4m3=q_is_e4m3,
+                          max_splits=4)
+    check(w, force_splits=2)
+
+
+@pytest.mark.parametrize("q_len,causal", [(1, True), (4, True), (3, False)])
+def test_empty_short_and_aligned_lengths(q_len, causal):
+    lens = [0, 1, 2, 3, 16, 127, 128, 129, 256, 300]
+    w = syn.make_workload("edge", lens, q_len, 2, 48, 16, seed=52, causal=causal, max_splits=4)
+    s, _ = check(w, force_splits=2)
+    assert np.all(np.isneginf(s.lse_host()[0]))  # L = 0
+    assert np.all(s.o_host()[0] == 0.0)
+
+
+def test_descale_broadcasts_and_unused_pages():
+    w = syn.config(5, h_r=32, q_len=4, num_seqs=3, len_range=(200, 900))
+    w.k_descale = np.array([1.375], dtype=np.float32)
+    w.v_descale = np.array([0.625], dtype=np.float32)
+    a, _ = check(w)
+    w2 = copy.deepcopy(w)
+    owned = set()
+    for bi, L in enumerate(w.seq_lens):
+        owned |= set(w.block_table[bi, : -(-int(L) // w.page_size)].tolist())
+    free = [p for p in range(w.num_pages) if p not in owned]
+    w2.k_cache[free] = 0x3F
+    w2.v_cache[free] = 0x40
+    b = run(w2)
+    assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
+
+
+@pytest.mark.parametrize("layout", ["hnd", "interleaved", "flashinfer"])
+def test_kv_layouts_match_nhd(layout):
+    w = syn.make_workload("qrows_layout", [200, 513, 900], 2, 4, 32, 32, seed=93)
+    a = run(w)
+    b = run(w, kv_layout=layout)
+    assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
+
+
+def test_determinism_and_graph_replay():
+    w = syn.config(5, h_r=16, q_len=8, num_seqs=4, len_range=(500, 3000))
+    s = run(w)
+    o0, l0 = s.o_vllm.clone(), s.lse.clone()
+    for _ in range(3):
+        s.step()
+    torch.cuda.synchronize()
+    assert torch.equal(o0, s.o_vllm) and torch.equal(l0, s.lse)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    s.o_vllm.zero_()
+    with torch.cuda.graph(g, stream=stream):
+        s.step(stream=stream)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o0, s.o_vllm) and torch.equal(l0, s.lse)
