@@ -1,5 +1,5 @@
 """GPU parity of the query-rows tensor-core kernel
-(MJ_KERNEL_TENSOR_CORE_QROWS; the automatic choice for more than 32 packed
+(MJ_KERNEL_TENSOR_CORE_QROWS; the automatic choice for more than 64 packed
 rows): 128 packed query rows of one kv head on the MMA's M, 128 keys of a
 tile on N, one softmax thread per query row.
 
@@ -58,7 +58,7 @@ def test_sweep_small(h_r, q_len):
     check(w)
 
 
-@pytest.mark.parametrize("h_r,q_len", [(32, 2), (32, 16)])
+@pytest.mark.parametrize("h_r,q_len", [(32, 4), (32, 16)])
 def test_sweep_full_sampled(h_r, q_len):
     w = syn.config(5, h_r=h_r, q_len=q_len)
     s = run(w, kernel=0)  # the automatic choice
