@@ -99,7 +99,7 @@ typedef struct {
  *                          tcgen05 kernel with 128 packed query rows on the
  *                          MMA's M and 128 keys on N: one read of the KV per
  *                          128 rows; MJ_KERNEL_AUTO takes it for
- *                          q_len*h_r > 64 */
+ *                          q_len*h_r > 32 */
 typedef enum {
   MJ_KERNEL_AUTO = 0,
   MJ_KERNEL_CUDA_CORE = 1,

@@ -20,11 +20,12 @@
 // (q 2^s = hi + lo) and P into hi + lo (448 p = hi + lo), each part an A
 // operand of its own MMA into the same accumulator.
 //
-// Roles (256 threads): warps 0 and 7 issue the K and V TMA tiles into two
+// Roles (384 threads): warps 0 and 11 issue the K and V TMA tiles into two
 // rings (a K stage is freed by its GEMM1, a V stage by its GEMM2); warp 1
-// (TMEM allocator) issues GEMM1 and warp 6 GEMM2 (one thread issues a
-// tcgen05.mma only every 70-100 cycles); warps 2-5 load Q and run the
-// softmax, thread = query row.
+// (TMEM allocator) issues GEMM1 and warp 10 GEMM2 (one thread issues a
+// tcgen05.mma only every 70-100 cycles); warps 2-5 and 6-9 are two softmax
+// warpgroups taking alternate tiles, thread = query row, each group with its
+// own S and O (128 TMEM columns each), merged per row at the end.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -42,22 +43,26 @@ constexpr int kPartBytes = kRows * 128;      // one e4m3 operand of 128 rows x 1
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legal wait
 constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
 constexpr float kLog2P448 = 8.807354922057604f;  // log2(448)
-constexpr int kThreads = 256;
-constexpr int kMma2Warp = 6;
-constexpr int kVLoadWarp = 7;
+constexpr int kWG = 2;                       // softmax warpgroups, alternate tiles
+constexpr int kThreads = 64 + 128 * kWG + 64;
+constexpr int kMma2Warp = 2 + 4 * kWG;       // 10
+constexpr int kVLoadWarp = kMma2Warp + 1;    // 11
+constexpr int kBarAll = 3;                   // named barrier of both warpgroups
 
 template <bool kQe4m3>
 struct QmCfg {
-  static constexpr int kStagesK = 4;
-  static constexpr int kStagesV = 5;
+  static constexpr int kStagesK = 3;
+  static constexpr int kStagesV = 4;
   static constexpr int kQParts = kQe4m3 ? 1 : 2;
-  static constexpr int kTmemCols = 512;       // S x2 (128 each), O (128)
+  static constexpr int kTmemCols = 512;  // per warpgroup: S (128), O (128)
+  static constexpr int kWgCols = 256;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kStagesK * kTileBytes;
   static constexpr int kOffQ = (kStagesK + kStagesV) * kTileBytes;  // [hi | lo] 128 x 128 B each
-  static constexpr int kOffP = kOffQ + kQParts * kPartBytes;        // [hi | lo]
-  static constexpr int kOffBar = kOffP + 2 * kPartBytes;
-  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 2 + 2 + 1 + 1 + 1 + 1;
+  static constexpr int kOffP = kOffQ + kQParts * kPartBytes;        // [wg][hi | lo]
+  static constexpr int kOffStat = kOffP + kWG * 2 * kPartBytes;     // group 1: [128] max, [128] sum
+  static constexpr int kOffBar = kOffStat + 2 * kRows * 4;
+  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 4 * kWG + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64 + 1024;
   static_assert(kBytes <= 232448, "shared memory");
@@ -68,10 +73,36 @@ __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) 
   if (status) atomicExch(status, kStatusTimeout);
 }
 
-__device__ __forceinline__ float round_4_sig_bits(float x) {
-  uint32_t u = __float_as_uint(x);
-  u = (u + 0x7FFFFu + ((u >> 20) & 1u)) & 0xFFF00000u;
-  return __uint_as_float(u);
+// Packed half-precision helpers for the exponentials and the P split.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
+}
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 // 128-byte-swizzled K-major row of an e4m3 operand: 16-byte chunk cc of
@@ -92,25 +123,24 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(sm);
+  float* stat_m = reinterpret_cast<float*>(sm + C::kOffStat);  // group 1's row max
+  float* stat_l = stat_m + kRows;                               // group 1's row sum
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
   int* q_shift = reinterpret_cast<int*>(sm + C::kOffMisc + 8);
   float* amax_red = reinterpret_cast<float*>(sm + C::kOffMisc + 16);  // [4]
 
-  // mbarriers: K ring (full, empty), V ring (full, empty), S full x2, S
-  // free x2, P full, P free, Q ready, MMA drain
+  // mbarriers: K ring (full, empty), V ring (full, empty), per warpgroup S
+  // full, S free, P full, P free; Q ready; MMA drain
   const uint32_t bar0 = sbase + C::kOffBar;
   auto kfull = [&](int s) { return bar0 + 8u * s; };
   auto kempty = [&](int s) { return bar0 + 8u * (SK + s); };
   auto vfull = [&](int s) { return bar0 + 8u * (2 * SK + s); };
   auto vempty = [&](int s) { return bar0 + 8u * (2 * SK + SV + s); };
   constexpr int kB = 2 * (SK + SV);
-  auto sfull = [&](int s) { return bar0 + 8u * (kB + s); };
-  auto sfree = [&](int s) { return bar0 + 8u * (kB + 2 + s); };
-  const uint32_t pfull = bar0 + 8u * (kB + 4);
-  const uint32_t pfree = bar0 + 8u * (kB + 5);
-  const uint32_t qready = bar0 + 8u * (kB + 6);
-  const uint32_t drain = bar0 + 8u * (kB + 7);
+  auto wgbar = [&](int wg, int k) { return bar0 + 8u * (kB + 4 * wg + k); };  // 0 S full, 1 S free, 2 P full, 3 P free
+  const uint32_t qready = bar0 + 8u * (kB + 4 * kWG);
+  const uint32_t drain = qready + 8u;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -138,12 +168,12 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::mbar_init(vfull(s), 1);
       ptx::mbar_init(vempty(s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(sfull(s), 1);
-      ptx::mbar_init(sfree(s), 4);
+    for (int wg = 0; wg < kWG; ++wg) {
+      ptx::mbar_init(wgbar(wg, 0), 1);
+      ptx::mbar_init(wgbar(wg, 1), 4);
+      ptx::mbar_init(wgbar(wg, 2), 4);
+      ptx::mbar_init(wgbar(wg, 3), 1);
     }
-    ptx::mbar_init(pfull, 4);
-    ptx::mbar_init(pfree, 1);
     ptx::mbar_init(qready, 1);
     ptx::mbar_init(drain, 2);
     *abort_flag = 0;
@@ -157,15 +187,14 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem;             // S buffers at columns 0 and 128
-  const uint32_t tmem_o = tmem + 2 * kRows;  // O at columns 256..383
 
   if (warp == 0 || warp == kVLoadWarp) {
     // ----------------------------------------------------------- producers
-    // A tile is keys [k0, k0 + 128) of kv head g: 128 / box_rows boxes of
-    // box_rows rows (one per page when pages are shorter than a tile), box
-    // jb on lane jb.  Block-table entries come from a register window (lane
-    // l holds block wbase + l) refilled 32 blocks ahead.
+    // Warp 0 loads K tiles, warp 11 V tiles.  A tile is keys [k0, k0 + 128)
+    // of kv head g: 128 / box_rows boxes of box_rows rows (one per page when
+    // pages are shorter than a tile), box jb on lane jb.  Block-table
+    // entries come from a register window (lane l holds block wbase + l)
+    // refilled 32 blocks ahead.
     const bool is_k = warp == 0;
     const int NS = is_k ? SK : SV;
     const uint32_t ring = sbase + (is_k ? C::kOffK : C::kOffV);
@@ -221,6 +250,8 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     }
   } else if (warp == 1 || warp == kMma2Warp) {
     // ----------------------------------------------------------------- MMA
+    // Tile i goes to warpgroup i & 1 as its local tile t = i >> 1: GEMM1
+    // (warp 1) into that group's S, GEMM2 (warp 10) into its O.
     if (lane == 0) {
       const bool gemm1 = warp == 1;
       bool ok = ptx::mbar_wait_bounded(qready, 0, abort_flag, kWaitNs);
@@ -228,15 +259,16 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const uint32_t idesc_o = ptx::idesc_e4m3(kRows, kRows, false, true);   // O = P V, V MN-major
       const uint64_t qdesc = ptx::smem_desc(sbase + C::kOffQ, 16, 1024, ptx::kSwizzle128B);
       const uint64_t kdesc0 = ptx::smem_desc(sbase + C::kOffK, 16, 1024, ptx::kSwizzle128B);
-      const uint64_t pdesc = ptx::smem_desc(sbase + C::kOffP, 16, 1024, ptx::kSwizzle128B);
+      const uint64_t pdesc0 = ptx::smem_desc(sbase + C::kOffP, 16, 1024, ptx::kSwizzle128B);
       const uint64_t vdesc0 = ptx::smem_desc(sbase + C::kOffV, 0, 1024, ptx::kSwizzle128B);
-      constexpr uint64_t kPartStep = kPartBytes >> 4;  // descriptor step to the lo part
+      constexpr uint64_t kPartStep = kPartBytes >> 4;  // descriptor step to the next operand part
       for (int i = 0; ok && i < T; ++i) {
-        const int sb = i & 1;
+        const int wg = i & 1, t = i >> 1;
+        const uint32_t tm = tmem + wg * C::kWgCols;
         if (gemm1) {
           const int st = i % SK;
           if (!ptx::mbar_wait_bounded(kfull(st), (i / SK) & 1, abort_flag, kWaitNs) ||
-              (i >= 2 && !ptx::mbar_wait_bounded(sfree(sb), ((i >> 1) - 1) & 1, abort_flag, kWaitNs))) {
+              (t >= 1 && !ptx::mbar_wait_bounded(wgbar(wg, 1), (t - 1) & 1, abort_flag, kWaitNs))) {
             ok = false;
             break;
           }
@@ -246,28 +278,29 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           for (int kk = 0; kk < 4; ++kk) {  // one K step = 32 bytes of d
 #pragma unroll
             for (int part = 0; part < C::kQParts; ++part)
-              ptx::mma_e4m3(tmem_s + sb * kRows, qdesc + part * kPartStep + 2 * kk, kdesc + 2 * kk, idesc_s,
+              ptx::mma_e4m3(tm, qdesc + part * kPartStep + 2 * kk, kdesc + 2 * kk, idesc_s,
                             (kk > 0 || part > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(sfull(sb));
+          ptx::mma_commit(wgbar(wg, 0));
           ptx::mma_commit(kempty(st));
         } else {
           const int st = i % SV;
-          if (!ptx::mbar_wait_bounded(pfull, i & 1, abort_flag, kWaitNs) ||
+          if (!ptx::mbar_wait_bounded(wgbar(wg, 2), t & 1, abort_flag, kWaitNs) ||
               !ptx::mbar_wait_bounded(vfull(st), (i / SV) & 1, abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           const uint64_t vdesc = vdesc0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+          const uint64_t pdesc = pdesc0 + static_cast<uint64_t>(wg) * 2 * kPartStep;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // one K step = 32 keys
 #pragma unroll
             for (int part = 0; part < 2; ++part)
-              ptx::mma_e4m3(tmem_o, pdesc + part * kPartStep + 2 * kk, vdesc + 256 * kk, idesc_o,
-                            (i > 0 || kk > 0 || part > 0) ? 1u : 0u);
+              ptx::mma_e4m3(tm + kRows, pdesc + part * kPartStep + 2 * kk, vdesc + 256 * kk, idesc_o,
+                            (t > 0 || kk > 0 || part > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(pfree);
+          ptx::mma_commit(wgbar(wg, 3));
           ptx::mma_commit(vempty(st));
         }
       }
@@ -278,23 +311,28 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     }
   } else {
     // ------------------------------------------------------------- softmax
-    // Thread = query row r (TMEM lane r of S and O); warps 2-5 cover the
-    // four lane quarters.  A wait that gives up sets the abort flag and the
-    // loop runs on (later waits return at once), so every warp takes the
-    // same path; nothing is written out after an abort.
+    // Two warpgroups take alternate tiles; in each, thread = query row r
+    // (TMEM lane r of the group's S and O), warps covering the four lane
+    // quarters.  A wait that gives up sets the abort flag and the loop runs
+    // on (later waits return at once), so every warp takes the same path;
+    // nothing is written out after an abort.
+    const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const int st_tid = (warp - 2) * 32 + lane;
+    const int st_tid = ((warp - 2) & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    constexpr int kBarSm = 1;
+    const int bar_wg = 1 + wg;
+    const uint32_t tmem_s = tmem + wg * C::kWgCols + lane_off;
+    const uint32_t tmem_o = tmem_s + kRows;
+    uint8_t* const pbuf = sm + C::kOffP + wg * 2 * kPartBytes;
     const int qrow = n0 + r;
     const bool live = qrow < a.n_q;
     const float qd = a.qd[b * a.qd_seq + g * a.qd_head];
     const float kd = a.kd[b * a.kd_seq + g * a.kd_head];
     const float vd = a.vd[b * a.vd_seq + g * a.vd_head];
 
-    // ---- Q row r -> two (bf16) or one (e4m3) K-major operand rows
-    {
+    // ---- Q row r -> two (bf16) or one (e4m3) K-major operand rows (group 0)
+    if (wg == 0) {
       uint4 raw[kQe4m3 ? 8 : 16];
       const int64_t off = b * a.q_seq + (static_cast<int64_t>(g) * a.n_q + (live ? qrow : 0)) * kHeadDimDev;
       if (kQe4m3) {
@@ -304,8 +342,6 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(swz(sm + C::kOffQ, r, cc)) = raw[cc];
         if (st_tid == 0) *q_shift = 0;
-        ptx::fence_proxy_async_smem();
-        ptx::named_bar_sync(kBarSm, 128);
       } else {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + off);
 #pragma unroll
@@ -321,7 +357,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (lane == 0) amax_red[warp - 2] = amax;
-        ptx::named_bar_sync(kBarSm, 128);
+        ptx::named_bar_sync(bar_wg, 128);
         amax = fmaxf(fmaxf(amax_red[0], amax_red[1]), fmaxf(amax_red[2], amax_red[3]));
         int shift = 0;
         if (amax > 0.f) {
@@ -354,11 +390,12 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           *reinterpret_cast<uint4*>(swz(sm + C::kOffQ + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         if (st_tid == 0) *q_shift = shift;
-        ptx::fence_proxy_async_smem();
-        ptx::named_bar_sync(kBarSm, 128);
       }
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(bar_wg, 128);
       if (st_tid == 0) ptx::mbar_arrive(qready);
     }
+    ptx::named_bar_sync(kBarAll, 128 * kWG);  // the Q shift is set
     const int shift = *q_shift;
     // raw (computed) score -> logit and -> log2 units; 2^-shift undoes the Q scaling
     const float scale_l = a.softmax_scale * qd * kd * ldexpf(1.f, -shift);
@@ -371,79 +408,110 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     float m_run = -INFINITY;  // running row max (raw units)
     float l_run = 0.f;        // running row sum of 448 p
     bool ok = true;
-    for (int i = 0; i < T; ++i) {
-      const int sb = i & 1;
+    int t_last = -1;
+    for (int i = wg; i < T; i += kWG) {
+      const int t = i >> 1;
       const int key0 = key_begin + i * kRows;
-      if (!ptx::mbar_wait_bounded(sfull(sb), (i >> 1) & 1, abort_flag, kWaitNs)) ok = false;
+      t_last = t;
+      if (!ptx::mbar_wait_bounded(wgbar(wg, 0), t & 1, abort_flag, kWaitNs)) ok = false;
       ptx::tc_fence_after();
-      float s[kRows];
-#pragma unroll
-      for (int c0 = 0; c0 < kRows; c0 += 16) {
-        uint32_t rr[16];
-        MJ_TMEM_LD16(tmem_s + lane_off + sb * kRows + c0, rr);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) s[c0 + e] = __uint_as_float(rr[e]);
-      }
-      ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sfree(sb));
-      // mask by select (garbage or poison keys never leak), row max
+      // pass 1: the row's masked maximum over the tile (select: garbage or
+      // poison keys never leak); a tile wholly below every row's limit of
+      // its warp skips the selects.  64 columns per TMEM round trip.
+      // (rows past n_q produce nothing: any value will do for them)
+      const bool unmasked = __all_sync(0xffffffffu, !live || key0 + kRows - 1 <= lim);
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kRows; ++c) {
-        s[c] = (key0 + c <= lim) ? s[c] : -INFINITY;
-        mt = fmaxf(mt, s[c]);
+      for (int h0 = 0; h0 < kRows; h0 += 64) {
+        uint32_t rr[64];
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
+        ptx::tmem_ld_wait();
+        if (unmasked) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) mt = fmaxf(mt, __uint_as_float(rr[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) mt = fmaxf(mt, (key0 + h0 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY);
+        }
       }
+      if (!live) mt = -INFINITY;  // keeps the maximum of an empty row at -inf
       const float m_new = fmaxf(m_run, mt);
       const float mu = (m_new == -INFINITY) ? 0.f : m_new;  // the -inf guard
-      // this row's P buffer and O are free once GEMM2 of the previous tile ran
-      if (i > 0 && !ptx::mbar_wait_bounded(pfree, (i - 1) & 1, abort_flag, kWaitNs)) ok = false;
       const bool moved = m_new != m_run;
       const float corr = moved ? fast_exp2((m_run - mu) * c2) : 1.f;  // 0 for a fresh row
       l_run *= corr;
       m_run = m_new;
+      // this group's P buffer and O are free once GEMM2 of its previous tile ran
+      if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
       // lazy O correction: each row rescales its own TMEM lane, but TMEM
       // access is warp-wide, so a warp corrects when any of its rows moved
-      if (i > 0 && __any_sync(0xffffffffu, moved)) {
-        {
-          ptx::tc_fence_after();
+      if (t > 0 && __any_sync(0xffffffffu, moved)) {
+        ptx::tc_fence_after();
 #pragma unroll
-          for (int c0 = 0; c0 < kRows; c0 += 16) {
-            uint32_t rr[16];
-            MJ_TMEM_LD16(tmem_o + lane_off + c0, rr);
-            ptx::tmem_ld_wait();
+        for (int h0 = 0; h0 < kRows; h0 += 64) {
+          uint32_t rr[64];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
-            MJ_TMEM_ST16(tmem_o + lane_off + c0, rr);
+          for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_o + h0 + c0, (rr + c0));
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 64; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_ST16(tmem_o + h0 + c0, (rr + c0));
+        }
+        ptx::tmem_st_wait();
+      }
+      // pass 2: x = 448 p = 256 * 2^((s - m) c + log2 448 - 8) in packed
+      // halves (ex2.approx.f16x2 of an argument <= 0.81, where half
+      // precision resolves it to 2^-11, times an exact 256; x <= 448 with
+      // about 11 significant bits), split x = hi + lo with hi = e4m3(x) and
+      // lo = e4m3(x - hi) (x - hi is exact in half precision); row sums of
+      // x in halves per 16 keys, then in fp32.  Half the exponentials and a
+      // third of the ALU work of an fp32 split.
+      const float bias = fmaf(-mu, c2, kLog2P448 - 8.f);
+      constexpr uint32_t k256x2 = 0x5C005C00u;  // (256, 256) in half precision
+#pragma unroll
+      for (int h0 = 0; h0 < kRows; h0 += 64) {
+        uint32_t rr[64];
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cc = h0 / 16 + q;  // 16-key chunk of the P row
+          uint32_t hw[4], lw[4];
+          uint32_t sum2 = 0u;
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            uint16_t h8[2], l8[2];
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+              const int e0 = q * 16 + wi * 4 + pr * 2;
+              float s0 = __uint_as_float(rr[e0]), s1 = __uint_as_float(rr[e0 + 1]);
+              if (!unmasked) {
+                const int c = h0 + e0;
+                s0 = (key0 + c <= lim) ? s0 : -INFINITY;
+                s1 = (key0 + c + 1 <= lim) ? s1 : -INFINITY;
+              }
+              const uint32_t x2 = mul_f16x2(ex2_f16x2(f32x2_to_f16x2(fmaf(s0, c2, bias), fmaf(s1, c2, bias))), k256x2);
+              const uint16_t hi8 = f16x2_to_e4m3x2(x2);
+              const uint32_t hf2 = e4m3x2_to_f16x2(hi8);
+              l8[pr] = f16x2_to_e4m3x2(sub_f16x2(x2, hf2));
+              h8[pr] = hi8;
+              sum2 = add_f16x2(sum2, x2);
+            }
+            hw[wi] = static_cast<uint32_t>(h8[0]) | (static_cast<uint32_t>(h8[1]) << 16);
+            lw[wi] = static_cast<uint32_t>(l8[0]) | (static_cast<uint32_t>(l8[1]) << 16);
           }
-          ptx::tmem_st_wait();
+          const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sum2));
+          l_run += sf.x + sf.y;
+          *reinterpret_cast<uint4*>(swz(pbuf, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(swz(pbuf + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
-      // 448 p, the row sum, and the hi / lo e4m3 parts of P row r
-      const float bias = fmaf(-mu, c2, kLog2P448);
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          float x[4], h[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[e] = fast_exp2(fmaf(s[cc * 16 + wi * 4 + e], c2, bias));
-            l_run += x[e];
-            h[e] = round_4_sig_bits(x[e]);
-          }
-          const uint16_t h01 = ptx::f32x2_to_e4m3x2(h[0], h[1]);
-          const uint16_t h23 = ptx::f32x2_to_e4m3x2(h[2], h[3]);
-          const uint16_t l01 = ptx::f32x2_to_e4m3x2(x[0] - h[0], x[1] - h[1]);
-          const uint16_t l23 = ptx::f32x2_to_e4m3x2(x[2] - h[2], x[3] - h[3]);
-          hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
-          lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
-        }
-        *reinterpret_cast<uint4*>(swz(sm + C::kOffP, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(swz(sm + C::kOffP + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));  // S read
       // keys past the sequence end: zero their V rows (0 * poison must not
       // reach O; the TMA landed whole pages).  Thread r owns key row r.
       if (key0 + kRows > L) {
@@ -458,34 +526,49 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(pfull);
+      if (lane == 0) ptx::mbar_arrive(wgbar(wg, 2));
       if (!ok) set_abort(abort_flag, a.status);
     }
 
-    // ---- epilogue: `drain` fires once every MMA of both issuers is done
-    if (ok && !ptx::mbar_wait_bounded(drain, 0, abort_flag, kWaitNs)) ok = false;
+    // ---- epilogue: this group's O is final once its last GEMM2 is done;
+    // group 0 merges both groups' rows (row r's state of group 1 through
+    // shared memory, its O from group 1's TMEM columns, same lanes)
+    if (t_last >= 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), t_last & 1, abort_flag, kWaitNs)) ok = false;
     if (!ok) set_abort(abort_flag, a.status);
-    // one decision per warp (TMEM access is warp-wide); rows past n_q load
-    // their lane but store nothing
-    if (__shfl_sync(0xffffffffu, *abort_flag == 0, 0)) {
+    if (wg == 1) {
+      stat_m[r] = m_run;
+      stat_l[r] = l_run;
+    }
+    const bool fine = !ptx::named_bar_red_or(kBarAll, 128 * kWG, *abort_flag != 0);
+    if (wg == 0 && fine) {
       ptx::tc_fence_after();
+      const float m1 = stat_m[r], l1 = stat_l[r];
+      const float mx = fmaxf(m_run, m1);
+      const float f0 = (m_run == -INFINITY) ? 0.f : fast_exp2((m_run - mx) * c2);
+      const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - mx) * c2);
+      const float l = (l_run * f0 + l1 * f1) * (1.f / 448.f);
       const bool final_out = a.n_splits[b] <= 1;
-      const float l = l_run * (1.f / 448.f);
       const float f = vd * (1.f / 448.f) * (final_out ? a.scale_o / (l + 1e-30f) : 1.f);
-      const int64_t orow = final_out ? b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + qrow) * kHeadDimDev
-                                     : part_row(a, b, g, slot, qrow) * kHeadDimDev;
-#pragma unroll
+      const int64_t orow = final_out ? b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + (live ? qrow : 0)) * kHeadDimDev
+                                     : part_row(a, b, g, slot, live ? qrow : 0) * kHeadDimDev;
+      const uint32_t o1 = tmem + C::kWgCols + kRows + lane_off;  // group 1's O, same lanes
+#pragma unroll 1
       for (int c0 = 0; c0 < kRows; c0 += 16) {
-        uint32_t rr[16];
-        MJ_TMEM_LD16(tmem_o + lane_off + c0, rr);
+        uint32_t ra[16], rb[16];
+        MJ_TMEM_LD16(tmem_o + c0, ra);
+        MJ_TMEM_LD16(o1 + c0, rb);
         ptx::tmem_ld_wait();
         if (!live) continue;
+        float v[16];
+        // select, not multiply: a group with no tile left its O stale
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          v[e] = ((f0 > 0.f ? __uint_as_float(ra[e]) * f0 : 0.f) + (f1 > 0.f ? __uint_as_float(rb[e]) * f1 : 0.f)) * f;
         if (final_out) {
           uint32_t pk[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const __nv_bfloat162 v2 =
-                __floats2bfloat162_rn(__uint_as_float(rr[2 * e]) * f, __uint_as_float(rr[2 * e + 1]) * f);
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
             pk[e] = *reinterpret_cast<const uint32_t*>(&v2);
           }
           uint4* dst = reinterpret_cast<uint4*>(a.o + orow + c0);
@@ -494,19 +577,18 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         } else {
           float4* dst = reinterpret_cast<float4*>(a.o_part + orow + c0);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_float4(__uint_as_float(rr[4 * e]) * f, __uint_as_float(rr[4 * e + 1]) * f,
-                                 __uint_as_float(rr[4 * e + 2]) * f, __uint_as_float(rr[4 * e + 3]) * f);
+          for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
       }
-      const float m_logit = m_run * scale_l;
-      if (!live) {
-      } else if (final_out) {
-        a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(l);
-      } else {
-        const int64_t pr = part_row(a, b, g, slot, qrow);
-        a.m_part[pr] = m_logit;
-        a.l_part[pr] = l;
+      if (live) {
+        const float m_logit = mx * scale_l;
+        if (final_out) {
+          a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(l);
+        } else {
+          const int64_t pr = part_row(a, b, g, slot, qrow);
+          a.m_part[pr] = m_logit;
+          a.l_part[pr] = l;
+        }
       }
     }
   }

@@ -58,8 +58,8 @@ constexpr int kSmemPerSm = 233472;  // 228 KiB usable shared memory per SM
 constexpr int kSmemReservedPerCta = 1024;
 constexpr int kGroupedUnitsPerSm = 6;  // measured: GQA decode, 1 to 8 units per SM
 // More packed rows than this go to the query-rows kernel (measured: it wins
-// from 128 rows; at 40 and 64 the swap-AB kernel is faster).
-constexpr int kQRowsFrom = 64;
+// from 40 rows on; at 32 the swap-AB kernel is faster).
+constexpr int kQRowsFrom = 32;
 
 }  // namespace
 

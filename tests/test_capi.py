@@ -211,9 +211,9 @@ def test_grouped_kernel_choice_and_plan():
 
 
 def test_query_rows_kernel_choice():
-    # more than 64 packed rows: the query-rows kernel, 128 rows per q tile
-    assert mj.kernel_name(_params(2, h_k=1, q_len=4, h_r=32)) == "qm_bf16"
-    assert mj.kernel_name(_params(2, h_k=1, q_len=2, h_r=32)) == "tc_r32_bf16"
+    # more than 32 packed rows: the query-rows kernel, 128 rows per q tile
+    assert mj.kernel_name(_params(2, h_k=1, q_len=2, h_r=32)) == "qm_bf16"
+    assert mj.kernel_name(_params(2, h_k=8, q_len=5, h_r=8)) == "qm_bf16"
     assert mj.kernel_name(_params(2, h_k=1, q_len=1, h_r=32)) == "tc_r32_bf16"
     qr = mj.MJ_KERNEL_TENSOR_CORE_QROWS
     assert mj.kernel_name(_params(2, h_k=1, h_r=16, kernel=qr, q_dtype=1)) == "qm_e4m3"

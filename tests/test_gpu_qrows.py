@@ -1,5 +1,5 @@
 """GPU parity of the query-rows tensor-core kernel
-(MJ_KERNEL_TENSOR_CORE_QROWS; the automatic choice for more than 64 packed
+(MJ_KERNEL_TENSOR_CORE_QROWS; the automatic choice for more than 32 packed
 rows): 128 packed query rows of one kv head on the MMA's M, 128 keys of a
 tile on N, one softmax thread per query row.
 
