@@ -409,104 +409,109 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     float l_run = 0.f;        // running row sum of 448 p
     bool ok = true;
     int t_last = -1;
+    // A warp whose 32 rows are all past n_q computes nothing: its P rows
+    // keep whatever they hold, which reaches only its own (unused) O rows.
+    const bool warp_live = __any_sync(0xffffffffu, live);
     for (int i = wg; i < T; i += kWG) {
       const int t = i >> 1;
       const int key0 = key_begin + i * kRows;
       t_last = t;
       if (!ptx::mbar_wait_bounded(wgbar(wg, 0), t & 1, abort_flag, kWaitNs)) ok = false;
       ptx::tc_fence_after();
-      // pass 1: the row's masked maximum over the tile (select: garbage or
-      // poison keys never leak); a tile wholly below every row's limit of
-      // its warp skips the selects.  64 columns per TMEM round trip.
-      // (rows past n_q produce nothing: any value will do for them)
-      const bool unmasked = __all_sync(0xffffffffu, !live || key0 + kRows - 1 <= lim);
-      float mt = -INFINITY;
-#pragma unroll
-      for (int h0 = 0; h0 < kRows; h0 += 64) {
-        uint32_t rr[64];
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
-        ptx::tmem_ld_wait();
-        if (unmasked) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) mt = fmaxf(mt, __uint_as_float(rr[e]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) mt = fmaxf(mt, (key0 + h0 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY);
-        }
-      }
-      if (!live) mt = -INFINITY;  // keeps the maximum of an empty row at -inf
-      const float m_new = fmaxf(m_run, mt);
-      const float mu = (m_new == -INFINITY) ? 0.f : m_new;  // the -inf guard
-      const bool moved = m_new != m_run;
-      const float corr = moved ? fast_exp2((m_run - mu) * c2) : 1.f;  // 0 for a fresh row
-      l_run *= corr;
-      m_run = m_new;
-      // this group's P buffer and O are free once GEMM2 of its previous tile ran
-      if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
-      // lazy O correction: each row rescales its own TMEM lane, but TMEM
-      // access is warp-wide, so a warp corrects when any of its rows moved
-      if (t > 0 && __any_sync(0xffffffffu, moved)) {
-        ptx::tc_fence_after();
-#pragma unroll
+      if (warp_live) {
+        // pass 1: the row's masked maximum over the tile (select: garbage or
+        // poison keys never leak); a tile wholly below every row's limit of
+        // its warp skips the selects.  64 columns per TMEM round trip.
+        // (rows past n_q produce nothing: any value will do for them)
+        const bool unmasked = __all_sync(0xffffffffu, !live || key0 + kRows - 1 <= lim);
+        float mt = -INFINITY;
+  #pragma unroll
         for (int h0 = 0; h0 < kRows; h0 += 64) {
           uint32_t rr[64];
-#pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_o + h0 + c0, (rr + c0));
+  #pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
           ptx::tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 64; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
-#pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_ST16(tmem_o + h0 + c0, (rr + c0));
-        }
-        ptx::tmem_st_wait();
-      }
-      // pass 2: x = 448 p = 256 * 2^((s - m) c + log2 448 - 8) in packed
-      // halves (ex2.approx.f16x2 of an argument <= 0.81, where half
-      // precision resolves it to 2^-11, times an exact 256; x <= 448 with
-      // about 11 significant bits), split x = hi + lo with hi = e4m3(x) and
-      // lo = e4m3(x - hi) (x - hi is exact in half precision); row sums of
-      // x in halves per 16 keys, then in fp32.  Half the exponentials and a
-      // third of the ALU work of an fp32 split.
-      const float bias = fmaf(-mu, c2, kLog2P448 - 8.f);
-      constexpr uint32_t k256x2 = 0x5C005C00u;  // (256, 256) in half precision
-#pragma unroll
-      for (int h0 = 0; h0 < kRows; h0 += 64) {
-        uint32_t rr[64];
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int cc = h0 / 16 + q;  // 16-key chunk of the P row
-          uint32_t hw[4], lw[4];
-          uint32_t sum2 = 0u;
-#pragma unroll
-          for (int wi = 0; wi < 4; ++wi) {
-            uint16_t h8[2], l8[2];
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-              const int e0 = q * 16 + wi * 4 + pr * 2;
-              float s0 = __uint_as_float(rr[e0]), s1 = __uint_as_float(rr[e0 + 1]);
-              if (!unmasked) {
-                const int c = h0 + e0;
-                s0 = (key0 + c <= lim) ? s0 : -INFINITY;
-                s1 = (key0 + c + 1 <= lim) ? s1 : -INFINITY;
-              }
-              const uint32_t x2 = mul_f16x2(ex2_f16x2(f32x2_to_f16x2(fmaf(s0, c2, bias), fmaf(s1, c2, bias))), k256x2);
-              const uint16_t hi8 = f16x2_to_e4m3x2(x2);
-              const uint32_t hf2 = e4m3x2_to_f16x2(hi8);
-              l8[pr] = f16x2_to_e4m3x2(sub_f16x2(x2, hf2));
-              h8[pr] = hi8;
-              sum2 = add_f16x2(sum2, x2);
-            }
-            hw[wi] = static_cast<uint32_t>(h8[0]) | (static_cast<uint32_t>(h8[1]) << 16);
-            lw[wi] = static_cast<uint32_t>(l8[0]) | (static_cast<uint32_t>(l8[1]) << 16);
+          if (unmasked) {
+  #pragma unroll
+            for (int e = 0; e < 64; ++e) mt = fmaxf(mt, __uint_as_float(rr[e]));
+          } else {
+  #pragma unroll
+            for (int e = 0; e < 64; ++e) mt = fmaxf(mt, (key0 + h0 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY);
           }
-          const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sum2));
-          l_run += sf.x + sf.y;
-          *reinterpret_cast<uint4*>(swz(pbuf, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(swz(pbuf + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        if (!live) mt = -INFINITY;  // keeps the maximum of an empty row at -inf
+        const float m_new = fmaxf(m_run, mt);
+        const float mu = (m_new == -INFINITY) ? 0.f : m_new;  // the -inf guard
+        const bool moved = m_new != m_run;
+        const float corr = moved ? fast_exp2((m_run - mu) * c2) : 1.f;  // 0 for a fresh row
+        l_run *= corr;
+        m_run = m_new;
+        // this group's P buffer and O are free once GEMM2 of its previous tile ran
+        if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+        // lazy O correction: each row rescales its own TMEM lane, but TMEM
+        // access is warp-wide, so a warp corrects when any of its rows moved
+        if (t > 0 && __any_sync(0xffffffffu, moved)) {
+          ptx::tc_fence_after();
+  #pragma unroll
+          for (int h0 = 0; h0 < kRows; h0 += 64) {
+            uint32_t rr[64];
+  #pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_o + h0 + c0, (rr + c0));
+            ptx::tmem_ld_wait();
+  #pragma unroll
+            for (int e = 0; e < 64; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
+  #pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_ST16(tmem_o + h0 + c0, (rr + c0));
+          }
+          ptx::tmem_st_wait();
+        }
+        // pass 2: x = 448 p = 256 * 2^((s - m) c + log2 448 - 8) in packed
+        // halves (ex2.approx.f16x2 of an argument <= 0.81, where half
+        // precision resolves it to 2^-11, times an exact 256; x <= 448 with
+        // about 11 significant bits), split x = hi + lo with hi = e4m3(x) and
+        // lo = e4m3(x - hi) (x - hi is exact in half precision); row sums of
+        // x in halves per 16 keys, then in fp32.  Half the exponentials and a
+        // third of the ALU work of an fp32 split.
+        const float bias = fmaf(-mu, c2, kLog2P448 - 8.f);
+        constexpr uint32_t k256x2 = 0x5C005C00u;  // (256, 256) in half precision
+  #pragma unroll
+        for (int h0 = 0; h0 < kRows; h0 += 64) {
+          uint32_t rr[64];
+  #pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
+          ptx::tmem_ld_wait();
+  #pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int cc = h0 / 16 + q;  // 16-key chunk of the P row
+            uint32_t hw[4], lw[4];
+            uint32_t sum2 = 0u;
+  #pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+              uint16_t h8[2], l8[2];
+  #pragma unroll
+              for (int pr = 0; pr < 2; ++pr) {
+                const int e0 = q * 16 + wi * 4 + pr * 2;
+                float s0 = __uint_as_float(rr[e0]), s1 = __uint_as_float(rr[e0 + 1]);
+                if (!unmasked) {
+                  const int c = h0 + e0;
+                  s0 = (key0 + c <= lim) ? s0 : -INFINITY;
+                  s1 = (key0 + c + 1 <= lim) ? s1 : -INFINITY;
+                }
+                const uint32_t x2 = mul_f16x2(ex2_f16x2(f32x2_to_f16x2(fmaf(s0, c2, bias), fmaf(s1, c2, bias))), k256x2);
+                const uint16_t hi8 = f16x2_to_e4m3x2(x2);
+                const uint32_t hf2 = e4m3x2_to_f16x2(hi8);
+                l8[pr] = f16x2_to_e4m3x2(sub_f16x2(x2, hf2));
+                h8[pr] = hi8;
+                sum2 = add_f16x2(sum2, x2);
+              }
+              hw[wi] = static_cast<uint32_t>(h8[0]) | (static_cast<uint32_t>(h8[1]) << 16);
+              lw[wi] = static_cast<uint32_t>(l8[0]) | (static_cast<uint32_t>(l8[1]) << 16);
+            }
+            const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sum2));
+            l_run += sf.x + sf.y;
+            *reinterpret_cast<uint4*>(swz(pbuf, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(swz(pbuf + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
         }
       }
       ptx::tc_fence_before();
