@@ -73,38 +73,6 @@ __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) 
   if (status) atomicExch(status, kStatusTimeout);
 }
 
-// Packed half-precision helpers for the exponentials and the P split.
-__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
-  uint32_t y;
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t h2) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
-  return r;
-}
-__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 // 128-byte-swizzled K-major row of an e4m3 operand: 16-byte chunk cc of
 // row r sits at chunk position cc ^ (r % 8).
 __device__ __forceinline__ uint8_t* swz(uint8_t* part, int r, int cc) {

@@ -157,54 +157,6 @@ __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) 
   if (status) atomicExch(status, kStatusTimeout);
 }
 
-// Reduces R per-lane values over the 32 lanes (max or sum), scattered by
-// recursive halving: each step keeps half of the live values and adds the
-// partner lane's copy of them.  On return v[0] holds the warp total of
-// column warp_col<R>(lane) (and, for R = 64, v[1] that of column + 32).
-template <int R, bool kMax>
-__device__ __forceinline__ void warp_reduce_scatter(float* v, int lane) {
-  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
-  if constexpr (R == 64) {
-    warp_reduce_scatter<32, kMax>(v, lane);
-    warp_reduce_scatter<32, kMax>(v + 32, lane);
-    v[1] = v[32];
-  } else {
-    int width = R;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      if (width > 1) {
-        const bool upper = (lane & off) != 0;
-        const int half = width >> 1;
-#pragma unroll
-        for (int i = 0; i < R / 2; ++i) {
-          if (i < half) {
-            const float send = upper ? v[i] : v[i + half];
-            const float keep = upper ? v[i + half] : v[i];
-            v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
-          }
-        }
-        width = half;
-      } else {
-        v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
-      }
-    }
-  }
-}
-
-// Column held by a lane after warp_reduce_scatter<R>: the lane bits that
-// chose upper halves, most significant first; lanes that agree on them hold
-// the same total (only the lowest of them stores it).
-template <int R>
-__device__ __forceinline__ int warp_col(int lane) {
-  constexpr int kShift = R >= 32 ? 0 : (R == 16 ? 1 : 2);
-  return lane >> kShift;
-}
-template <int R>
-__device__ __forceinline__ bool warp_col_writer(int lane) {
-  constexpr int kMask = R >= 32 ? 0 : (R == 16 ? 1 : 3);
-  return (lane & kMask) == 0;
-}
-
 // x rounded to 4 significant bits, ties to even: the value e4m3 gives a
 // non-negative x in its normal range [2^-6, 448] (below 2^-6 the e4m3 grid is
 // coarser; the caller's residual then carries an error below 2^-10).

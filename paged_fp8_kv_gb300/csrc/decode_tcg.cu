@@ -76,36 +76,67 @@ template <int G, int RH, bool kQe4m3>
 struct GCfg {
   static constexpr int KR = kRows / G;     // keys per head per tile
   static constexpr int GR = G * RH;        // query columns of the CTA
-  static constexpr int HPW = 32 / KR;      // heads per warp
+  // G = 2: a head's 64 keys span two warps (a pair), which exchange their
+  // column maxima and row sums through shared memory
+  static constexpr bool kPair = KR == 64;
+  static constexpr int HPW = kPair ? 1 : 32 / KR;  // heads per warp
   static constexpr int W = HPW * RH;       // S columns a warp reads
   static constexpr int kN1 = kQe4m3 ? (GR < 16 ? 16 : GR) : 2 * GR;
   static constexpr int kN2 = 2 * GR;
+  // S buffers per warpgroup: two when they fit in TMEM beside O, else one
+  // (the warpgroup's next GEMM1 then waits until its softmax has read S)
+  static constexpr int kSBufs = 2 * kN1 + kN2 <= 256 ? 2 : 1;
   // K and V rings: a K stage is free once its GEMM1 ran, a V stage only
   // after the tile's softmax and GEMM2, so V gets more stages
-  static constexpr int kStagesK = 5;
-  static constexpr int kStagesV = 7;
+  // P is produced as x = 448 p 2^-kTau: a column's reference maximum is
+  // moved only when a score passes it by kTau (log2 units); kTau = 0 is the
+  // exact running maximum
+  static constexpr int kTau = kPair ? 4 : 0;
+  static constexpr float kLog2PScale = 8.807354922057604f - kTau;  // log2(448 2^-kTau)
+  static constexpr float kPScaleInv = (1.f / 448.f) * (1 << kTau);
+  static constexpr int kStagesK = kPair ? 4 : 5;
+  static constexpr int kStagesV = kPair ? 5 : 7;
   static constexpr int kQBytes = kN1 * 128;
-  static constexpr int kPBytes = kN2 * kRows;  // [kN2/16 groups][128 rows][16 B]
-  static constexpr int kWgCols = pow2_at_least(2 * kN1 + kN2);  // TMEM per warpgroup: S x2, O
+  // P (GEMM2's B operand, MN-major, no swizzle: [16-column groups][K rows][16 B]).
+  //   G >= 4: one block-diagonal buffer per warpgroup, [kN2/16][128 rows],
+  //     the off-diagonal zeros written once.
+  //   G = 2: per head only its own columns, [2 RH/16][KR rows] (one GEMM2
+  //     MMA chain per head), and two buffers per warpgroup, so that the
+  //     softmax of a tile need not wait for the previous tile's GEMM2.
+  static constexpr int kPBufs = kPair ? 2 : 1;
+  static constexpr int kPHeadBytes = 2 * RH * KR;  // G = 2: one head's hi | lo columns
+  static constexpr int kPBufBytes = kPair ? G * kPHeadBytes : kN2 * kRows;
+  static constexpr int kPBytes = kPBufs * kPBufBytes;  // per warpgroup
+  static constexpr int kWgCols = pow2_at_least(kSBufs * kN1 + kN2);  // TMEM per warpgroup: S, O
   static constexpr int kTmemCols = kWG * kWgCols;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kStagesK * kTileBytes;
   static constexpr int kOffQ = (kStagesK + kStagesV) * kTileBytes;  // [2 unit slots]
   static constexpr int kOffP = kOffQ + 2 * kQBytes;          // [kWG] P buffers
   static constexpr int kOffCorr = kOffP + kWG * kPBytes;     // [kWG][2][GR]
-  static constexpr int kOffStat0 = kOffCorr + kWG * 2 * GR * 4;  // group 0: [GR] max, [GR] sum
-  static constexpr int kOffStat1 = kOffStat0 + 2 * GR * 4;       // group 1: [2 slots][GR] max, sum
-  static constexpr int kOffItem = kOffStat1 + 2 * 2 * GR * 4;    // [2 slots] descriptors
+  // per group and unit slot: [GR] max, [GR] sum.  Group 0's state needs no
+  // second slot for G >= 4 (its next unit cannot end before group 1 has
+  // merged this one: that unit's GEMM2s wait for both groups' O-free); the
+  // G = 2 layout has room for it.
+  static constexpr int kOffStat = kOffCorr + kWG * 2 * GR * 4;
+  static constexpr int kStatSets = kPair ? 4 : 3;
+  // pair exchange: [kWG] x ([4 warps][32] partial column values, [4][32]
+  // each warp's copy of the update thresholds, [4][32] of the exponent
+  // offsets, [4] each warp's lowest threshold)
+  static constexpr int kOffRed = kOffStat + kStatSets * 2 * GR * 4;
+  static constexpr int kRedWg = 3 * 128 + 4;  // floats per warpgroup (16-byte multiple)
+  static constexpr int kRedBytes = kPair ? kWG * kRedWg * 4 : 0;
+  static constexpr int kOffItem = kOffRed + kRedBytes;             // [2 slots] descriptors
   static constexpr int kOffBar = kOffItem + 2 * kItemBytes;
-  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 6 * kWG + 2 + 2 + 1 + 1 + 2;
+  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 9 * kWG + 2 + 2 + 1 + 1 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 32 + 1024;
-  static_assert(KR >= 16 && KR <= 32, "a head's rows must sit within one warp");
-  static_assert(W == 8 || W == 16, "TMEM load width");
+  static_assert(KR >= 16 && KR <= 64, "a head's rows sit within one warp or a warp pair");
+  static_assert(kPair ? RH == 32 : (W == 8 || W == 16), "TMEM load width / one column per lane");
   static_assert(kN1 % 16 == 0 && kN2 % 16 == 0 && kN1 <= 256 && kN2 <= 256, "MMA N");
   static_assert(kTmemCols <= 512, "TMEM");
   static_assert(kBytes <= 232448, "shared memory");
-  static_assert(40 + 8 * G <= kItemBytes, "unit descriptor");
+  static_assert(44 + 8 * G <= kItemBytes, "unit descriptor");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert(16 * 128 * 4 <= kPBytes && GR % 16 == 0, "epilogue stage: 16 columns in a P buffer");
 };
@@ -114,6 +145,7 @@ struct GCfg {
 template <int G>
 struct Item {
   int valid, b, t_begin, TS, L, g0, n0, slot, nsp, shift;
+  int u;  // unit index: its parity picks the warpgroup of the unit's first tile
   float vd[G], cs[G];  // v descale, logit scale (softmax_scale * qd * kd) per head
 };
 
@@ -162,8 +194,11 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(sm);
   float* corr_all = reinterpret_cast<float*>(sm + C::kOffCorr);
-  float* stat0 = reinterpret_cast<float*>(sm + C::kOffStat0);  // [GR] m, [GR] l
-  float* stat1 = reinterpret_cast<float*>(sm + C::kOffStat1);  // [2][GR] m, [2][GR] l
+  float* stat_all = reinterpret_cast<float*>(sm + C::kOffStat);
+  auto stat_of = [&](int w, int sl) -> float* {  // [GR] m, [GR] l of group w, unit slot sl
+    return stat_all + (C::kPair ? w * 2 + sl : (w == 0 ? 0 : 1 + sl)) * 2 * GR;
+  };
+  float* red_all = reinterpret_cast<float*>(sm + C::kOffRed);    // pair exchange (G = 2)
   auto item = [&](int slot) -> It& { return *reinterpret_cast<It*>(sm + C::kOffItem + slot * kItemBytes); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
@@ -177,11 +212,14 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   auto vfull = [&](int s) { return bar0 + 8u * (2 * SK + s); };
   auto vempty = [&](int s) { return bar0 + 8u * (2 * SK + SV + s); };
   constexpr int kB = 2 * (SK + SV);
-  // k: 0, 1 S full; 2, 3 S free; 4 P full; 5 P free
-  auto wgbar = [&](int wg, int k) { return bar0 + 8u * (kB + 6 * wg + k); };
-  auto ifull = [&](int slot) { return bar0 + 8u * (kB + 6 * kWG + slot); };
-  auto iempty = [&](int slot) { return bar0 + 8u * (kB + 6 * kWG + 2 + slot); };
-  const uint32_t ofree = bar0 + 8u * (kB + 6 * kWG + 4);
+  // k: 0, 1 S full; 2, 3 S free; 4, 5 P full (per P buffer); 6, 7 P free
+  // (the GEMM2 that read the buffer is done); 8 O done (every GEMM2)
+  auto wgbar = [&](int wg, int k) { return bar0 + 8u * (kB + 9 * wg + k); };
+  auto pfull = [&](int wg, int pb) { return wgbar(wg, 4 + pb); };
+  auto pfree = [&](int wg, int pb) { return wgbar(wg, 6 + pb); };
+  auto ifull = [&](int slot) { return bar0 + 8u * (kB + 9 * kWG + slot); };
+  auto iempty = [&](int slot) { return bar0 + 8u * (kB + 9 * kWG + 2 + slot); };
+  const uint32_t ofree = bar0 + 8u * (kB + 9 * kWG + 4);
   const uint32_t drain = ofree + 8u;
   // the descriptor alone (the producer needs no Q): before the Q conversion
   auto dfull = [&](int slot) { return drain + 8u * (1 + slot); };
@@ -205,15 +243,18 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::mbar_init(wgbar(wg, 1), 1);
       ptx::mbar_init(wgbar(wg, 2), 4);
       ptx::mbar_init(wgbar(wg, 3), 4);
-      ptx::mbar_init(wgbar(wg, 4), 4);
-      ptx::mbar_init(wgbar(wg, 5), 1);
+      ptx::mbar_init(pfull(wg, 0), 4);
+      ptx::mbar_init(pfull(wg, 1), 4);
+      ptx::mbar_init(pfree(wg, 0), 1);
+      ptx::mbar_init(pfree(wg, 1), 1);
+      ptx::mbar_init(wgbar(wg, 8), 1);
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ifull(s), 1);
       ptx::mbar_init(dfull(s), 1);
       ptx::mbar_init(iempty(s), 2 + 4 * kWG);  // both MMA issuers, every softmax warp
     }
-    ptx::mbar_init(ofree, 4);
+    ptx::mbar_init(ofree, 4 * kWG);
     ptx::mbar_init(drain, 2);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -285,6 +326,7 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           I.n0 = qt * RH;
           I.slot = wslot;
           I.nsp = a.n_splits[b];
+          I.u = u;
         }
       }
       if (lane == 0) I.valid = valid ? 1 : 0;
@@ -505,16 +547,19 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     }
   } else if (warp == 1 || warp == kMma2Warp) {
     // ----------------------------------------------------------------- MMA
-    // Tile number n counts tiles over all units; tile n goes to warpgroup
-    // n & 1 as its local tile t = n >> 1: GEMM1 (warp 1) into that group's
-    // S buffer t & 1, GEMM2 (warp 11) into its O.  Each issuer walks the
+    // Tile number n counts tiles over all units (the rings' index).  Tile i
+    // of unit u goes to warpgroup (i + u) & 1 — a function of the unit
+    // alone, so the result does not depend on which CTA ran which units —
+    // as that group's local tile t: GEMM1 (warp 1) into its S buffer
+    // t % kSBufs, GEMM2 (warp 11) into its O.  Each issuer walks the
     // units in order with blocking waits; GEMM1 runs ahead as far as the S
     // buffers allow.  Shared-memory descriptors are a base plus the
     // operand's offset >> 4 (every offset stays inside the 14-bit field).
     if (lane == 0) {
       const bool gemm1 = warp == 1;
       bool ok = true;
-      uint32_t n = 0;  // this issuer's tiles so far
+      uint32_t n = 0;                // this issuer's tiles so far
+      uint32_t tcount[2] = {0u, 0u};  // each group's tiles of the earlier units
       for (int it = 0; ok; ++it) {
         const int slot = it & 1;
         if (!ptx::mbar_wait_bounded(ifull(slot), (it >> 1) & 1, abort_flag, kWaitNs)) {
@@ -524,15 +569,18 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         const It& I = item(slot);
         if (!I.valid) break;
         const int TS = I.TS;
+        const int f = I.u & 1;
         if (gemm1) {
           const uint32_t idesc_s = ptx::idesc_e4m3(kRows, C::kN1, false, false);
           const uint64_t kdesc0 = ptx::smem_desc(sbase + C::kOffK, 16, 1024, ptx::kSwizzle128B);
           const uint64_t qdesc = ptx::smem_desc(sbase + C::kOffQ + slot * C::kQBytes, 16, 1024, ptx::kSwizzle128B);
           for (int i = 0; i < TS; ++i, ++n) {
             const int st = n % SK;
-            const int wg = n & 1, t = n >> 1, sb = t & 1;
+            const int wg = (i + f) & 1;
+            const int t = static_cast<int>(tcount[wg]) + (i >> 1), sb = t % C::kSBufs;
             if (!ptx::mbar_wait_bounded(kfull(st), (n / SK) & 1, abort_flag, kWaitNs) ||
-                (t >= 2 && !ptx::mbar_wait_bounded(wgbar(wg, 2 + sb), ((t >> 1) - 1) & 1, abort_flag, kWaitNs))) {
+                (t >= C::kSBufs &&
+                 !ptx::mbar_wait_bounded(wgbar(wg, 2 + sb), ((t / C::kSBufs) - 1) & 1, abort_flag, kWaitNs))) {
               ok = false;
               break;
             }
@@ -546,14 +594,18 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
             ptx::mma_commit(kempty(st));
           }
         } else {
-          const uint32_t idesc_o = ptx::idesc_e4m3(kRows, C::kN2, true, true);
+          const uint32_t idesc_o = C::kPair ? ptx::idesc_e4m3(kRows, 2 * RH, true, true)
+                                            : ptx::idesc_e4m3(kRows, C::kN2, true, true);
           const uint64_t vdesc0 = ptx::smem_desc(sbase + C::kOffV, 0, 1024, ptx::kSwizzle128B);
-          const uint64_t pdesc0 = ptx::smem_desc(sbase + C::kOffP, 128, 2048, ptx::kSwizzleNone);
+          const uint64_t pdesc0 = C::kPair ? ptx::smem_desc(sbase + C::kOffP, 128, KR * 16, ptx::kSwizzleNone)
+                                           : ptx::smem_desc(sbase + C::kOffP, 128, 2048, ptx::kSwizzleNone);
           for (int i = 0; i < TS; ++i, ++n) {
             const int st = n % SV;
-            const int wg = n & 1, t = n >> 1;
+            const int wg = (i + f) & 1;
+            const int t = static_cast<int>(tcount[wg]) + (i >> 1);
+            const int pb = t % C::kPBufs;
             const bool first = i < 2;  // this group's first tile of the unit: O starts over
-            if (!ptx::mbar_wait_bounded(wgbar(wg, 4), t & 1, abort_flag, kWaitNs) ||
+            if (!ptx::mbar_wait_bounded(pfull(wg, pb), (t / C::kPBufs) & 1, abort_flag, kWaitNs) ||
                 !ptx::mbar_wait_bounded(vfull(st), (n / SV) & 1, abort_flag, kWaitNs) ||
                 (first && it > 0 && !ptx::mbar_wait_bounded(ofree, (it - 1) & 1, abort_flag, kWaitNs))) {
               ok = false;
@@ -561,15 +613,30 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
             }
             ptx::tc_fence_after();
             const uint64_t vdesc = vdesc0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-            const uint64_t pdesc = pdesc0 + static_cast<uint64_t>((wg * C::kPBytes) >> 4);
-            const uint32_t d_o = tmem + wg * C::kWgCols + 2 * C::kN1;
+            const uint64_t pdesc =
+                pdesc0 + static_cast<uint64_t>((wg * C::kPBytes + pb * C::kPBufBytes) >> 4);
+            const uint32_t d_o = tmem + wg * C::kWgCols + C::kSBufs * C::kN1;
+            if constexpr (C::kPair) {
+              // per head: O[:, head h's hi | lo columns] += V_h^T P_h, K = KR keys
 #pragma unroll
-            for (int kk = 0; kk < kRows / 32; ++kk)  // one K step = 32 KV rows
-              ptx::mma_e4m3(d_o, vdesc + 256 * kk, pdesc + 32 * kk, idesc_o, (!first || kk > 0) ? 1u : 0u);
-            ptx::mma_commit(wgbar(wg, 5));
+              for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+                for (int kk = 0; kk < KR / 32; ++kk)  // one K step = 32 keys (4096 B of V, 512 B of P)
+                  ptx::mma_e4m3(d_o + hh * 2 * RH, vdesc + 256 * (hh * (KR / 32) + kk),
+                                pdesc + ((hh * C::kPHeadBytes) >> 4) + 32 * kk, idesc_o,
+                                (!first || kk > 0) ? 1u : 0u);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < kRows / 32; ++kk)  // one K step = 32 KV rows
+                ptx::mma_e4m3(d_o, vdesc + 256 * kk, pdesc + 32 * kk, idesc_o, (!first || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(pfree(wg, pb));
+            if (C::kPair) ptx::mma_commit(wgbar(wg, 8));
             ptx::mma_commit(vempty(st));
           }
         }
+        for (int w = 0; w < 2; ++w) tcount[w] += static_cast<uint32_t>(TS - ((w + f) & 1) + 1) >> 1;
         if (ok) ptx::mma_commit(iempty(slot));  // this unit's Q and slot are no longer read
       }
       if (!ok) set_abort(abort_flag, a.status);
@@ -594,11 +661,12 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     const int hw = h - h_first;           // 0 .. HPW-1
     const int bar_wg = 1 + wg;
     const uint32_t tmem_s = tmem + wg * C::kWgCols;
-    const uint32_t tmem_o = tmem_s + 2 * C::kN1;
+    const uint32_t tmem_o = tmem_s + C::kSBufs * C::kN1;
     uint8_t* const pbuf_wg = sm + C::kOffP + wg * C::kPBytes;
     float* const corr_wg = corr_all + wg * 2 * GR;
 
     uint32_t n_base = 0;  // tiles of all earlier units
+    uint32_t tb = 0;      // this group's tiles of all earlier units
     for (int it = 0;; ++it) {
       const int slot = it & 1;
       const bool got = ptx::mbar_wait_bounded(ifull(slot), (it >> 1) & 1, abort_flag, kWaitNs);
@@ -614,7 +682,206 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const int key_begin = I.t_begin * 128;
       const float two_m_shift = ldexpf(1.f, -I.shift);
       const float c2 = I.cs[h] * two_m_shift * kLog2e;  // raw score -> log2 units, this row's head
+      const int i0 = (wg + I.u) & 1;  // this group's first tile of the unit
 
+      float* my_m = stat_of(wg, slot);
+      float* my_l = my_m + GR;
+      if constexpr (C::kPair) {
+        // ---- G = 2: warps q and q ^ 1 hold one head's 64 keys.  Lane c
+        // keeps column c's reference maximum m (raw units).  A tile updates
+        // m only where its maximum passes m + kTau / c2 (kTau in log2 units),
+        // so 448 p 2^-kTau stays within e4m3's range and most tiles need
+        // neither the column reduction nor an O correction; the result does
+        // not depend on m.  Each thread keeps its key's share of every row
+        // sum, reduced once per unit.
+        const int pq = quarter ^ 1;
+        const int bar_pair = 4 + 2 * wg + h;  // named barrier of the pair's 64 threads
+        float* const red = red_all + wg * C::kRedWg;    // [4 warps][32] partial values
+        float* const thr = red + 128 + quarter * 32;   // this warp's copy: update thresholds (raw)
+        float* const bias = red + 256 + quarter * 32;  // ... and exponent offsets (log2 units)
+        float* const thr_min = red + 384 + quarter;    // ... and the lowest threshold
+        const float head_c = C::kTau / c2;  // kTau in raw units of this head
+        const int vis_all = a.causal ? L - a.q_len : L - 1;  // keys every column sees
+        float m_lane = -INFINITY;
+        float l_thr[RH];
+#pragma unroll
+        for (int nn = 0; nn < RH; ++nn) l_thr[nn] = 0.f;
+        thr[lane] = -INFINITY;  // a fresh column: its first finite score updates it
+        bias[lane] = C::kLog2PScale;
+        if (lane == 0) *thr_min = -INFINITY;
+        __syncwarp();
+        bool ok = true;
+        int t_last = -1;
+        for (int i = i0; i < TS; i += 2) {
+          const uint32_t n = n_base + i;
+          const int t = static_cast<int>(tb) + (i >> 1);
+          const int sb = t % C::kSBufs;
+          const bool first = i < 2;
+          const int j = key_begin + i * KR + k;  // this row's key
+          t_last = t;
+          if (!ptx::mbar_wait_bounded(wgbar(wg, sb), (t / C::kSBufs) & 1, abort_flag, kWaitNs)) ok = false;
+          ptx::tc_fence_after();
+          float sc[RH];
+          {
+            // this row's head's columns: hi, then lo (added)
+            uint32_t r[RH];
+            const uint32_t s_base = tmem_s + lane_off + sb * C::kN1 + h * RH;
+            MJ_TMEM_LD16(s_base, r);
+            MJ_TMEM_LD16(s_base + 16, (r + 16));
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int nn = 0; nn < RH; ++nn) sc[nn] = __uint_as_float(r[nn]);
+            if (!kQe4m3) {
+              MJ_TMEM_LD16(s_base + GR, r);
+              MJ_TMEM_LD16(s_base + GR + 16, (r + 16));
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int nn = 0; nn < RH; ++nn) sc[nn] += __uint_as_float(r[nn]);
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(wgbar(wg, 2 + sb));
+          if (j > vis_all) {  // select: keys past a column's limit, and garbage rows, never leak
+#pragma unroll
+            for (int nn = 0; nn < RH; ++nn) {
+              const int qrow = n0 + nn;
+              int lim = a.causal ? L - a.q_len + qrow / a.h_r : L - 1;
+              lim = lim < L - 1 ? lim : L - 1;
+              if (qrow >= a.n_q || j > lim) sc[nn] = -INFINITY;
+            }
+          }
+          // may any score pass its column's threshold?  A conservative test
+          // (this key's largest score against the warp's lowest threshold);
+          // one barrier answers for the group, and the update below, uniform
+          // over it, checks each column exactly.
+          float smax = sc[0];
+#pragma unroll
+          for (int nn = 1; nn < RH; ++nn) smax = fmaxf(smax, sc[nn]);
+          const bool any_ex = ptx::named_bar_red_or(bar_wg, 128, smax > *thr_min);
+          bool any_moved = false;
+          if (any_ex) {
+            // column maxima over the head's 64 keys: reduce-scatter within
+            // the warp (lane c ends with column c), then the partner's value
+            float mx[RH];
+#pragma unroll
+            for (int nn = 0; nn < RH; ++nn) mx[nn] = sc[nn];
+            warp_reduce_scatter<RH, true>(mx, lane);
+            red[quarter * 32 + lane] = mx[0];
+            ptx::named_bar_sync(bar_pair, 64);
+            const float tmax = fmaxf(mx[0], red[pq * 32 + lane]);
+            const bool moved_c = tmax > thr[lane];
+            const float mn = moved_c ? tmax : m_lane;
+            const float mu = (mn == -INFINITY) ? 0.f : mn;
+            // the -inf guard: 0 for a column that had no finite score yet
+            const float corr_c = moved_c ? fast_exp2((m_lane - mu) * c2) : 1.f;
+            m_lane = mn;
+            float* corr_b = corr_wg + (t & 1) * GR;
+            if ((quarter & 1) == 0) corr_b[h * RH + lane] = corr_c;
+            // the partner has read red; corr_b is complete
+            any_moved = ptx::named_bar_red_or(bar_wg, 128, moved_c);
+            const float tn = (mn == -INFINITY) ? -INFINITY : mn + head_c;
+            thr[lane] = tn;
+            bias[lane] = fmaf(-mu, c2, C::kLog2PScale);
+            float tlo = tn;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) tlo = fminf(tlo, __shfl_xor_sync(0xffffffffu, tlo, off));
+            if (lane == 0) *thr_min = tlo;
+            const float4* cb4 = reinterpret_cast<const float4*>(corr_b + h * RH);
+#pragma unroll
+            for (int q4 = 0; q4 < RH / 4; ++q4) {
+              const float4 f = cb4[q4];
+              l_thr[4 * q4] *= f.x;
+              l_thr[4 * q4 + 1] *= f.y;
+              l_thr[4 * q4 + 2] *= f.z;
+              l_thr[4 * q4 + 3] *= f.w;
+            }
+            __syncwarp();
+          }
+          // P buffer t & 1 is free once the GEMM2 of tile t - 2 is done
+          const int pb = t & 1;
+          if (t >= 2 && !ptx::mbar_wait_bounded(pfree(wg, pb), ((t >> 1) - 1) & 1, abort_flag, kWaitNs)) ok = false;
+          // lazy O correction (uniform over the group: TMEM access is warp-wide),
+          // after the GEMM2 of tile t - 1 (t - 2's is done: the parity names it)
+          if (any_moved && !first) {
+            if (!ptx::mbar_wait_bounded(wgbar(wg, 8), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+            const float* corr_b = corr_wg + (t & 1) * GR;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < C::kN2; c0 += 16) {
+              // O columns of head c0 / (2 RH): hi | lo halves of RH each
+              const int cb = (c0 / (2 * RH)) * RH + c0 % RH;
+              uint32_t r[16];
+              MJ_TMEM_LD16(tmem_o + lane_off + c0, r);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr_b[cb + e]);
+              MJ_TMEM_ST16(tmem_o + lane_off + c0, r);
+            }
+            ptx::tmem_st_wait();
+          }
+          // x = 448 p 2^-kTau, its row-sum shares, and the e4m3 split
+          {
+            const float4* b4 = reinterpret_cast<const float4*>(bias);
+#pragma unroll
+            for (int q4 = 0; q4 < RH / 4; ++q4) {
+              const float4 bv = b4[q4];
+              const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float x = fast_exp2(fmaf(sc[4 * q4 + e], c2, bb[e]));
+                l_thr[4 * q4 + e] += x;
+                sc[4 * q4 + e] = x;
+              }
+            }
+          }
+          {
+            uint32_t hi[RH / 4], lo[RH / 4];
+            split_e4m3_hilo<RH>(sc, hi, lo);
+            // this head's P: [hi groups 0, 1 | lo groups 2, 3][KR keys][16 B]
+            uint8_t* prow = pbuf_wg + pb * C::kPBufBytes + h * C::kPHeadBytes + k * 16;
+            constexpr int kGS = KR * 16;  // bytes between 16-column groups
+            *reinterpret_cast<uint4*>(prow) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(prow + kGS) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+            *reinterpret_cast<uint4*>(prow + 2 * kGS) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4*>(prow + 3 * kGS) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+          }
+          // rows past the sequence end: zero their V row (0 * poison must not
+          // reach O; the TMA landed whole pages)
+          if (key_begin + (i + 1) * KR > L) {
+            const int st = n % SV;
+            if (!ptx::mbar_wait_bounded(vfull(st), (n / SV) & 1, abort_flag, kWaitNs)) ok = false;
+            if (j >= L) {
+              uint4* vrow = reinterpret_cast<uint4*>(sm + C::kOffV + st * kTileBytes + row * 128);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(pfull(wg, pb));
+          if (!ok) set_abort(abort_flag, a.status);
+        }
+        n_base += TS;
+        tb += static_cast<uint32_t>(TS - i0 + 1) >> 1;
+        // ---- end of the unit: this group's O is final once its last two
+        // GEMM2s are done (each P buffer's barrier names its own)
+        if (t_last >= 1 &&
+            !ptx::mbar_wait_bounded(pfree(wg, (t_last - 1) & 1), ((t_last - 1) >> 1) & 1, abort_flag, kWaitNs))
+          ok = false;
+        if (t_last >= 0 && !ptx::mbar_wait_bounded(pfree(wg, t_last & 1), (t_last >> 1) & 1, abort_flag, kWaitNs))
+          ok = false;
+        if (!ok) set_abort(abort_flag, a.status);
+        // row sums over the pair's 64 keys; the even warp stores the head's stats
+        warp_reduce_scatter<RH, false>(l_thr, lane);
+        red[quarter * 32 + lane] = l_thr[0];
+        ptx::named_bar_sync(bar_pair, 64);
+        if ((quarter & 1) == 0) {
+          my_m[h * RH + lane] = m_lane;
+          my_l[h * RH + lane] = (l_thr[0] + red[pq * 32 + lane]) * C::kPScaleInv;
+        }
+      } else {
       float l_thr[RH], m_cur[RH];  // deferred row sums (of 448 p); running column max (raw)
       int lim[RH];                 // last visible key of column n of this row's head (-1: none)
 #pragma unroll
@@ -629,9 +896,9 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 
       bool ok = true;
       int t_last = -1;  // this group's last local tile of the unit
-      for (int i = static_cast<int>((static_cast<uint32_t>(wg) - n_base) & 1u); i < TS; i += 2) {
+      for (int i = i0; i < TS; i += 2) {
         const uint32_t n = n_base + i;
-        const int t = static_cast<int>(n >> 1);
+        const int t = static_cast<int>(tb) + (i >> 1);
         const int sb = t & 1;
         const bool first = i < 2;
         const int j = key_begin + i * KR + k;  // this row's key
@@ -694,7 +961,7 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         // This group's P buffer and O are free once the GEMM2 of its previous
         // tile finished (the one before that was waited for a tile ago, so
         // the parity names that GEMM2 alone).
-        if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 5), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+        if (t > 0 && !ptx::mbar_wait_bounded(pfree(wg, 0), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
         // lazy O correction: O's TMEM lanes are head-dimension rows spanning
         // every head's columns, so any moved maximum corrects all of them
         // (the condition is uniform over the group: TMEM access is warp-wide)
@@ -748,13 +1015,14 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(wgbar(wg, 4));
+        if (lane == 0) ptx::mbar_arrive(pfull(wg, 0));
         if (!ok) set_abort(abort_flag, a.status);
       }
       n_base += TS;
+      tb += static_cast<uint32_t>(TS - i0 + 1) >> 1;
 
       // ---- end of the unit: this group's O is final once its last GEMM2 is
-      if (t_last >= 0 && !ptx::mbar_wait_bounded(wgbar(wg, 5), t_last & 1, abort_flag, kWaitNs)) ok = false;
+      if (t_last >= 0 && !ptx::mbar_wait_bounded(pfree(wg, 0), t_last & 1, abort_flag, kWaitNs)) ok = false;
       if (!ok) set_abort(abort_flag, a.status);
       // row sums of this head: shuffles within its KR lanes
 #pragma unroll
@@ -764,8 +1032,6 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         for (int off = KR / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
         l_thr[nn] = v;
       }
-      float* my_m = wg == 0 ? stat0 : stat1 + slot * GR;
-      float* my_l = wg == 0 ? stat0 + GR : stat1 + 2 * GR + slot * GR;
       if (k == 0) {
 #pragma unroll
         for (int nn = 0; nn < RH; ++nn) {
@@ -773,39 +1039,39 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           my_l[h * RH + nn] = l_thr[nn] * (1.f / 448.f);
         }
       }
-      const bool fine = !ptx::named_bar_red_or(kBarAll, 128 * kWG, *abort_flag != 0);
-      if (wg == 1) {
-        // group 1 is done with this unit: its stats stay in their slot half
-        // until group 0 has merged them
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(iempty(slot));
-        continue;
       }
-      // ---- group 0: merge of the two groups' states and the output.  Per
-      // column: the common maximum, each group's weight, the combined sum
-      // (in place of group 0's stats; the weights in group 0's correction
-      // area).
-      float* f0_s = corr_wg;
-      float* f1_s = corr_wg + GR;
-      if (fine && st_tid < GR) {
-        const int c = st_tid, hq = c / RH;
+      const bool fine = !ptx::named_bar_red_or(kBarAll, 128 * kWG, *abort_flag != 0);
+      // ---- both groups: merge of their states and the output, group w
+      // taking the 16-column blocks 16 w, 16 w + 32, ...  Per column: the
+      // common maximum and each group's weight, folded with scale_o / l for
+      // a final output (in this group's correction area).
+      const bool final_out = I.nsp <= 1;
+      float* w0_s = corr_wg;
+      float* w1_s = corr_wg + GR;
+      const int ce = st_tid;  // the column this thread merges, if its block is this group's
+      const bool mine = ce < GR && ((ce >> 4) & 1) == wg;
+      float mx = -INFINITY, lsum = 0.f;
+      if (fine && mine) {
+        const int hq = ce / RH;
         const float c2c = I.cs[hq] * two_m_shift * kLog2e;
-        const float m0 = stat0[c], m1 = stat1[slot * GR + c];
-        const float mx = fmaxf(m0, m1);
+        const float* s0 = stat_of(0, slot);
+        const float* s1 = stat_of(1, slot);
+        const float m0 = s0[ce], m1 = s1[ce];
+        mx = fmaxf(m0, m1);
         const float f0 = (m0 == -INFINITY) ? 0.f : fast_exp2((m0 - mx) * c2c);
         const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - mx) * c2c);
-        f0_s[c] = f0;
-        f1_s[c] = f1;
-        stat0[GR + c] = stat0[GR + c] * f0 + stat1[2 * GR + slot * GR + c] * f1;
-        stat0[c] = mx;
+        lsum = s0[GR + ce] * f0 + s1[GR + ce] * f1;
+        const float sc = final_out ? a.scale_o / (lsum + 1e-30f) : 1.f;
+        w0_s[ce] = f0 * sc;
+        w1_s[ce] = f1 * sc;
       }
       ptx::named_bar_sync(bar_wg, 128);
       if (fine) {
         ptx::tc_fence_after();
-        const bool final_out = I.nsp <= 1;
         const int d = row;  // TMEM lane of O = head-dimension index
-        const uint32_t o1 = tmem + C::kWgCols + 2 * C::kN1;  // group 1's O, same lanes
-        // Sixteen columns at a time: O = f0 O_0 + f1 O_1 (hi + lo parts of
+        const uint32_t o0 = tmem + C::kSBufs * C::kN1;               // group 0's O
+        const uint32_t o1 = tmem + C::kWgCols + C::kSBufs * C::kN1;  // group 1's O, same lanes
+        // Sixteen columns at a time: O = w0 O_0 + w1 O_1 (hi + lo parts of
         // each; select, not multiply: a group with no tile left its O stale)
         // is staged column-major in this group's P buffer (idle now: its
         // last GEMM2 is done), then written out as whole rows with 16-byte
@@ -813,28 +1079,31 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         // while the KV stream saturates the memory system.
         float* stage = reinterpret_cast<float*>(pbuf_wg);
 #pragma unroll 1
-        for (int c0 = 0; c0 < GR; c0 += 16) {
+        for (int c0 = 16 * wg; c0 < GR; c0 += 32) {
+          // TMEM columns of the hi and lo parts of output columns c0 .. c0 + 15
+          const int ohi = C::kPair ? (c0 / RH) * 2 * RH + c0 % RH : c0;
+          const int olo = C::kPair ? ohi + RH : GR + c0;
           float ov[16];
           {
             uint32_t rh[16], rl[16];
-            MJ_TMEM_LD16(tmem_o + lane_off + c0, rh);
-            MJ_TMEM_LD16(tmem_o + lane_off + GR + c0, rl);
+            MJ_TMEM_LD16(o0 + lane_off + ohi, rh);
+            MJ_TMEM_LD16(o0 + lane_off + olo, rl);
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float f0 = f0_s[c0 + e];
-              ov[e] = f0 > 0.f ? (__uint_as_float(rh[e]) + __uint_as_float(rl[e])) * f0 : 0.f;
+              const float w0 = w0_s[c0 + e];
+              ov[e] = w0 > 0.f ? (__uint_as_float(rh[e]) + __uint_as_float(rl[e])) * w0 : 0.f;
             }
           }
           {
             uint32_t qh[16], ql[16];
-            MJ_TMEM_LD16(o1 + lane_off + c0, qh);
-            MJ_TMEM_LD16(o1 + lane_off + GR + c0, ql);
+            MJ_TMEM_LD16(o1 + lane_off + ohi, qh);
+            MJ_TMEM_LD16(o1 + lane_off + olo, ql);
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float f1 = f1_s[c0 + e];
-              if (f1 > 0.f) ov[e] += (__uint_as_float(qh[e]) + __uint_as_float(ql[e])) * f1;
+              const float w1 = w1_s[c0 + e];
+              if (w1 > 0.f) ov[e] += (__uint_as_float(qh[e]) + __uint_as_float(ql[e])) * w1;
             }
           }
 #pragma unroll
@@ -850,44 +1119,44 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
             if (qrow < a.n_q) {
               float4 v = *reinterpret_cast<const float4*>(stage + e * kHeadDimDev + d4);
               const int g = I.g0 + hq;
-              float f = I.vd[hq] * (1.f / 448.f);
+              const float f = I.vd[hq] * C::kPScaleInv;
+              v.x *= f;
+              v.y *= f;
+              v.z *= f;
+              v.w *= f;
               if (final_out) {
-                f *= a.scale_o / (stat0[GR + c] + 1e-30f);
-                const __nv_bfloat162 lo2 = __floats2bfloat162_rn(v.x * f, v.y * f);
-                const __nv_bfloat162 hi2 = __floats2bfloat162_rn(v.z * f, v.w * f);
+                const __nv_bfloat162 lo2 = __floats2bfloat162_rn(v.x, v.y);
+                const __nv_bfloat162 hi2 = __floats2bfloat162_rn(v.z, v.w);
                 uint2 packed;
                 packed.x = *reinterpret_cast<const uint32_t*>(&lo2);
                 packed.y = *reinterpret_cast<const uint32_t*>(&hi2);
                 const int64_t orow = b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + qrow) * kHeadDimDev;
                 *reinterpret_cast<uint2*>(a.o + orow + d4) = packed;
               } else {
-                v.x *= f;
-                v.y *= f;
-                v.z *= f;
-                v.w *= f;
                 const int64_t pr = part_row(a, b, g, I.slot, qrow);
                 *reinterpret_cast<float4*>(a.o_part + pr * kHeadDimDev + d4) = v;
               }
             }
           }
-          ptx::named_bar_sync(bar_wg, 128);  // the next half reuses the stage
+          ptx::named_bar_sync(bar_wg, 128);  // the next block reuses the stage
         }
         // the P buffer's off-diagonal zeros again (published by the fence
-        // before this group's next P-full arrival)
-        for (int id = st_tid; id < C::kPBytes / 16; id += 128)
-          reinterpret_cast<uint4*>(pbuf_wg)[id] = make_uint4(0u, 0u, 0u, 0u);
-        if (st_tid < GR) {
-          const int c = st_tid, hq = c / RH, nn = c % RH;
+        // before this group's next P-full arrival); G = 2 has none: every
+        // tile rewrites its buffer whole
+        if (!C::kPair)
+          for (int id = st_tid; id < C::kPBytes / 16; id += 128)
+            reinterpret_cast<uint4*>(pbuf_wg)[id] = make_uint4(0u, 0u, 0u, 0u);
+        if (mine) {
+          const int c = ce, hq = c / RH, nn = c % RH;
           const int qrow = n0 + nn, g = I.g0 + hq;
           if (qrow < a.n_q) {
-            const float m_logit = stat0[c] * I.cs[hq] * two_m_shift;
-            const float l = stat0[GR + c];
+            const float m_logit = mx * I.cs[hq] * two_m_shift;
             if (final_out) {
-              a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(l);
+              a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(lsum);
             } else {
               const int64_t pr = part_row(a, b, g, I.slot, qrow);
               a.m_part[pr] = m_logit;
-              a.l_part[pr] = l;
+              a.l_part[pr] = lsum;
             }
           }
         }
@@ -933,16 +1202,18 @@ cudaError_t launch_tcg(const DecodeDev& a, int n_q_tiles, int* sched, int sm_cou
 }  // namespace
 
 bool tcg_supported(int h_k, int n_q, int* heads_per_cta, int* rows_per_head) {
-  // G heads x RH rows per head, G * RH <= 32, a head's keys within one warp
-  // (G >= 4)
-  int rh = n_q <= 4 ? 4 : (n_q <= 8 ? 8 : 0);
-  if (rh == 0) return false;
-  int g = 0;
-  if (rh == 4 && h_k % 8 == 0) {
+  // G heads x RH rows per head: G = 8 x 4 and G = 4 x 8 (a head's keys
+  // within one warp), G = 2 x 32 (a head's keys in a warp pair)
+  int g = 0, rh = 0;
+  if (n_q <= 4 && h_k % 8 == 0) {
     g = 8;
-  } else if (h_k % 4 == 0) {
+    rh = 4;
+  } else if (n_q <= 8 && h_k % 4 == 0) {
     g = 4;
     rh = 8;
+  } else if (n_q <= 32 && h_k % 2 == 0) {
+    g = 2;
+    rh = 32;
   }
   if (g == 0) return false;
   *heads_per_cta = g;
@@ -958,12 +1229,17 @@ cudaError_t launch_decode_tcg(const DecodeDev& a, int heads_per_cta, int rows_pe
   if (heads_per_cta == 4 && rows_per_head == 8)
     return q_e4m3 ? launch_tcg<4, 8, true>(a, n_q_tiles, sched, sm_count, stream)
                   : launch_tcg<4, 8, false>(a, n_q_tiles, sched, sm_count, stream);
+  if (heads_per_cta == 2 && rows_per_head == 32)
+    return q_e4m3 ? launch_tcg<2, 32, true>(a, n_q_tiles, sched, sm_count, stream)
+                  : launch_tcg<2, 32, false>(a, n_q_tiles, sched, sm_count, stream);
   return cudaErrorInvalidValue;
 }
 
 int tcg_smem_bytes(int heads_per_cta, int rows_per_head, bool q_e4m3) {
   if (heads_per_cta == 8 && rows_per_head == 4) return q_e4m3 ? GCfg<8, 4, true>::kBytes : GCfg<8, 4, false>::kBytes;
   if (heads_per_cta == 4 && rows_per_head == 8) return q_e4m3 ? GCfg<4, 8, true>::kBytes : GCfg<4, 8, false>::kBytes;
+  if (heads_per_cta == 2 && rows_per_head == 32)
+    return q_e4m3 ? GCfg<2, 32, true>::kBytes : GCfg<2, 32, false>::kBytes;
   return 0;
 }
 

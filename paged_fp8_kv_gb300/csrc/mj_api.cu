@@ -56,7 +56,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr int kDefaultL2Prefetch = 0;  // tiles; measured choice
 constexpr int kSmemPerSm = 233472;  // 228 KiB usable shared memory per SM
 constexpr int kSmemReservedPerCta = 1024;
-constexpr int kGroupedUnitsPerSm = 6;  // measured: GQA decode, 1 to 8 units per SM
+// Units per SM the plan cuts for the head-grouped kernel (measured, 2 to 12
+// per SM): six for 8 heads x 4 rows (GQA decode), three for 2 heads x 32
+// rows (spec verify: each unit boundary stalls the CTA's softmax for its
+// output epilogue, a few microseconds).
+constexpr int kGroupedUnitsPerSm = 6;
+constexpr int kPairUnitsPerSm = 3;
+// More packed rows than this (up to 32) and an even number of kv heads go
+// to the 2-head x 32-row grouped kernel (measured on the spec-verify
+// workload: 32 rows 265 us vs 327 us per-head; 16 rows 307 us vs 238 us).
+constexpr int kPairFrom = 16;
 // More packed rows than this go to the query-rows kernel (measured: it wins
 // from 40 rows on; at 32 the swap-AB kernel is faster).
 constexpr int kQRowsFrom = 32;
@@ -82,13 +91,16 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
     k.rows_per_cta = 128;
     smem = qm_smem_bytes(e4m3);
     k.name = e4m3 ? "qm_e4m3" : "qm_bf16";
-  } else if (p.kernel == MJ_KERNEL_TENSOR_CORE_GROUPED && tcg_supported(p.h_k, n_q, &g, &rh)) {
+  } else if ((p.kernel == MJ_KERNEL_TENSOR_CORE_GROUPED ||
+              (p.kernel == MJ_KERNEL_AUTO && n_q > kPairFrom && n_q <= kQRowsFrom && p.h_k % 2 == 0)) &&
+             tcg_supported(p.h_k, n_q, &g, &rh)) {
     k.kind = KernelKind::kTensorCoreGrouped;
     k.rows_per_cta = rh;
     k.heads_per_cta = g;
     smem = tcg_smem_bytes(g, rh, e4m3);
-    static const char* names[2][2] = {{"tcg_g8r4_bf16", "tcg_g4r8_bf16"}, {"tcg_g8r4_e4m3", "tcg_g4r8_e4m3"}};
-    k.name = names[e4m3][g == 8 ? 0 : 1];
+    static const char* names[2][3] = {{"tcg_g8r4_bf16", "tcg_g4r8_bf16", "tcg_g2r32_bf16"},
+                                      {"tcg_g8r4_e4m3", "tcg_g4r8_e4m3", "tcg_g2r32_e4m3"}};
+    k.name = names[e4m3][g == 8 ? 0 : (g == 4 ? 1 : 2)];
   } else {
     k.kind = KernelKind::kTensorCore;
     k.rows_per_cta = n_q <= 8 ? 8 : (n_q <= 16 ? 16 : 32);
@@ -108,7 +120,7 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
   k.ctas_per_sm = (per_sm < 1 ? 1 : per_sm) * k.heads_per_cta;
   // The persistent kernel takes units from a queue: the plan cuts about six
   // units per SM, so that the greedy queue (longest first) ends balanced.
-  if (k.kind == KernelKind::kTensorCoreGrouped) k.ctas_per_sm *= kGroupedUnitsPerSm;
+  if (k.kind == KernelKind::kTensorCoreGrouped) k.ctas_per_sm *= g == 2 ? kPairUnitsPerSm : kGroupedUnitsPerSm;
   return k;
 }
 

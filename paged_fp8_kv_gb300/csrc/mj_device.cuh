@@ -87,6 +87,105 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Packed half-precision helpers for the exponentials and the P split.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
+}
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// N values 0 <= x <= 448 (N a multiple of 4) as e4m3 hi and lo parts, four
+// codes a word: x is rounded to half precision (11 significant bits), hi =
+// e4m3(x), lo = e4m3(x - hi) (the difference is exact in half precision), so
+// hi + lo carries about 8 significant bits of x.
+template <int N>
+__device__ __forceinline__ void split_e4m3_hilo(const float* x, uint32_t* hi, uint32_t* lo) {
+#pragma unroll
+  for (int w = 0; w < N / 4; ++w) {
+    const uint32_t h01 = f32x2_to_f16x2(x[4 * w], x[4 * w + 1]);
+    const uint32_t h23 = f32x2_to_f16x2(x[4 * w + 2], x[4 * w + 3]);
+    const uint16_t e01 = f16x2_to_e4m3x2(h01);
+    const uint16_t e23 = f16x2_to_e4m3x2(h23);
+    const uint16_t l01 = f16x2_to_e4m3x2(sub_f16x2(h01, e4m3x2_to_f16x2(e01)));
+    const uint16_t l23 = f16x2_to_e4m3x2(sub_f16x2(h23, e4m3x2_to_f16x2(e23)));
+    hi[w] = static_cast<uint32_t>(e01) | (static_cast<uint32_t>(e23) << 16);
+    lo[w] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+  }
+}
+
+// Reduces R per-lane values over the 32 lanes (max or sum), scattered by
+// recursive halving: each step keeps half of the live values and adds the
+// partner lane's copy of them.  On return v[0] holds the warp total of
+// column warp_col<R>(lane) (and, for R = 64, v[1] that of column + 32).
+template <int R, bool kMax>
+__device__ __forceinline__ void warp_reduce_scatter(float* v, int lane) {
+  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
+  if constexpr (R == 64) {
+    warp_reduce_scatter<32, kMax>(v, lane);
+    warp_reduce_scatter<32, kMax>(v + 32, lane);
+    v[1] = v[32];
+  } else {
+    int width = R;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      if (width > 1) {
+        const bool upper = (lane & off) != 0;
+        const int half = width >> 1;
+#pragma unroll
+        for (int i = 0; i < R / 2; ++i) {
+          if (i < half) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+          }
+        }
+        width = half;
+      } else {
+        v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
+      }
+    }
+  }
+}
+
+// Column held by a lane after warp_reduce_scatter<R>: the lane bits that
+// chose upper halves, most significant first; lanes that agree on them hold
+// the same total (only the lowest of them stores it).
+template <int R>
+__device__ __forceinline__ int warp_col(int lane) {
+  constexpr int kShift = R >= 32 ? 0 : (R == 16 ? 1 : 2);
+  return lane >> kShift;
+}
+template <int R>
+__device__ __forceinline__ bool warp_col_writer(int lane) {
+  constexpr int kMask = R >= 32 ? 0 : (R == 16 ? 1 : 3);
+  return (lane & kMask) == 0;
+}
+
 // Index helpers for the partial-result workspace.
 __device__ __forceinline__ int64_t part_row(const DecodeDev& a, int b, int g, int slot, int n) {
   return ((static_cast<int64_t>(b) * a.h_k + g) * a.max_splits + slot) * a.n_q + n;

@@ -190,13 +190,17 @@ def test_status_strings_and_kernel_name():
 
 
 def test_grouped_kernel_choice_and_plan():
-    # the head-grouped kernel: 8 heads x 4 rows or 4 heads x 8 rows per CTA
+    # the head-grouped kernel: 8 heads x 4 rows, 4 heads x 8 rows or 2 heads
+    # x 32 rows per CTA
     grouped = mj.MJ_KERNEL_TENSOR_CORE_GROUPED
     assert mj.kernel_name(_params(2, h_k=8, h_r=4, kernel=grouped)) == "tcg_g8r4_bf16"
     assert mj.kernel_name(_params(2, h_k=8, h_r=8, kernel=grouped)) == "tcg_g4r8_bf16"
     assert mj.kernel_name(_params(2, h_k=12, h_r=2, kernel=grouped)) == "tcg_g4r8_bf16"
-    # no group of four heads, or more than 8 rows per head: refused
-    for h_k, h_r in [(2, 4), (6, 4), (8, 16)]:
+    assert mj.kernel_name(_params(2, h_k=8, h_r=16, kernel=grouped)) == "tcg_g2r32_bf16"
+    assert mj.kernel_name(_params(2, h_k=6, h_r=4, kernel=grouped)) == "tcg_g2r32_bf16"
+    assert mj.kernel_name(_params(2, h_k=8, q_len=4, h_r=8, kernel=grouped, q_dtype=1)) == "tcg_g2r32_e4m3"
+    # an odd number of kv heads, or more than 32 rows per head: refused
+    for h_k, h_r in [(3, 4), (1, 16), (8, 40)]:
         p = _params(2, h_k=h_k, h_r=h_r, kernel=grouped)
         with pytest.raises(mj.MjError):
             mj.kernel_name(p)
@@ -215,6 +219,10 @@ def test_query_rows_kernel_choice():
     assert mj.kernel_name(_params(2, h_k=1, q_len=2, h_r=32)) == "qm_bf16"
     assert mj.kernel_name(_params(2, h_k=8, q_len=5, h_r=8)) == "qm_bf16"
     assert mj.kernel_name(_params(2, h_k=1, q_len=1, h_r=32)) == "tc_r32_bf16"
+    # 17 to 32 rows with an even number of kv heads: 2 heads x 32 rows per CTA
+    assert mj.kernel_name(_params(2, h_k=8, q_len=4, h_r=8)) == "tcg_g2r32_bf16"
+    assert mj.kernel_name(_params(2, h_k=8, q_len=2, h_r=8)) == "tc_r16_bf16"
+    assert mj.kernel_name(_params(2, h_k=3, q_len=4, h_r=8)) == "tc_r32_bf16"
     qr = mj.MJ_KERNEL_TENSOR_CORE_QROWS
     assert mj.kernel_name(_params(2, h_k=1, h_r=16, kernel=qr, q_dtype=1)) == "qm_e4m3"
     plan = mj.decode_plan(_params(4, h_k=1, q_len=16, h_r=32), [1000, 2000, 3000, 4000])

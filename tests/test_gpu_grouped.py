@@ -1,13 +1,14 @@
 """GPU parity of the head-grouped tensor-core kernel
-(MJ_KERNEL_TENSOR_CORE_GROUPED): one CTA serves 4 or 8 kv heads, whose
+(MJ_KERNEL_TENSOR_CORE_GROUPED): one CTA serves 2, 4 or 8 kv heads, whose
 rows of every page it fetches together.
 
 The kernel's arithmetic is the per-head tensor-core kernel's; what is new is
 the tile shape (G heads x 128/G keys on the MMA's M side, every head's query
 rows on N, P block-diagonal), the per-head masking, maxima and descales
 inside one tile, and the smaller key step.  So these cases compare it with
-the fp64 oracle element by element on: both instances (8 heads x 4 rows,
-4 heads x 8 rows), every page size (a page is 1, 2, 4 or 8 steps, or two
+the fp64 oracle element by element on: every instance (8 heads x 4 rows,
+4 heads x 8 rows, 2 heads x 32 rows with a head's keys in a warp pair),
+every page size (a page is 1, 2, 4 or 8 steps, or two
 pages one step), bf16 and e4m3 Q, causal and non-causal, empty and ragged
 lengths, forced splits with the merge, per-head descales that differ inside
 one CTA, every KV layout, determinism and graph replay.
@@ -145,3 +146,64 @@ def test_determinism_and_graph_replay():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o0, s.o_vllm) and torch.equal(l0, s.lse)
+
+
+# ---- 2 heads x 32 rows: a head's 64 keys of a step span two warps, which
+# exchange column maxima and row sums; one S buffer per warpgroup.
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+@pytest.mark.parametrize("h_k,h_r,q_len", [(8, 8, 4), (2, 8, 3), (6, 4, 4), (4, 16, 1)])
+def test_pair_instance_page_sizes(page_size, h_k, h_r, q_len):
+    lens = [1, 63, 64, 65, 100, 250, 511, 700, 1300]
+    w = syn.make_workload("grouped_pair", lens, q_len, h_k, h_r, page_size, seed=171 + page_size, max_splits=4)
+    s, _ = check(w, force_splits=2)
+    assert s.kernel == "tcg_g2r32_bf16"
+
+
+@pytest.mark.parametrize("force", [0, 3])
+def test_spec_verify_small_pair(force):
+    w = syn.config(4, num_seqs=4, len_range=(300, 3000))
+    s, _ = check(w, force_splits=force)
+    assert s.kernel == "tcg_g2r32_bf16"
+
+
+def test_spec_verify_full_sampled_pair():
+    w = syn.config(4)
+    s = run(w)
+    units = sample_units(w, 16, seed=4, include=[(int(np.argmax(w.seq_lens)), 0), (int(np.argmin(w.seq_lens)), 7)])
+    compare(w, s.o_host(), s.lse_host(), units=units)
+
+
+@pytest.mark.parametrize("q_is_e4m3", [False, True])
+@pytest.mark.parametrize("causal", [True, False])
+def test_pair_q_dtype_and_masking(q_is_e4m3, causal):
+    lens = [5, 64, 333, 1029]
+    w = syn.make_workload("grouped_pair_q", lens, 4, 4, 8, 64, seed=183, q_is_e4m3=q_is_e4m3, causal=causal,
+                          max_splits=8)
+    s, _ = check(w)
+    assert s.kernel.startswith("tcg_g2r32")
+
+
+@pytest.mark.parametrize("q_len,causal", [(4, True), (3, False)])
+def test_pair_empty_short_and_aligned_lengths(q_len, causal):
+    lens = [0, 1, 2, 3, 16, 63, 64, 65, 127, 128, 129, 256, 300]
+    w = syn.make_workload("edge_pair", lens, q_len, 2, 8, 16, seed=151, causal=causal, max_splits=4)
+    s, _ = check(w, force_splits=2)
+    assert s.kernel == "tcg_g2r32_bf16"
+    assert np.all(np.isneginf(s.lse_host()[0]))  # L = 0
+    assert np.all(s.o_host()[0] == 0.0)
+
+
+def test_pair_determinism_and_layouts():
+    # more units than CTAs: which CTA runs which unit varies between launches
+    w = syn.config(4, num_seqs=12, len_range=(500, 6000))
+    a = run(w)
+    assert a.plan.num_work * (w.h_k // 2) > torch.cuda.get_device_properties(0).multi_processor_count
+    o0, l0 = a.o_vllm.clone(), a.lse.clone()
+    for _ in range(3):
+        a.step()
+    torch.cuda.synchronize()
+    assert torch.equal(o0, a.o_vllm) and torch.equal(l0, a.lse)
+    b = run(w, kv_layout="hnd")
+    assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
