@@ -74,6 +74,7 @@ constexpr int pow2_at_least(int x) {
 
 template <int G, int RH, bool kQe4m3>
 struct GCfg {
+  static constexpr int kRH = RH;
   static constexpr int KR = kRows / G;     // keys per head per tile
   static constexpr int GR = G * RH;        // query columns of the CTA
   // G = 2: a head's 64 keys span two warps (a pair), which exchange their
@@ -128,7 +129,7 @@ struct GCfg {
   static constexpr int kRedBytes = kPair ? kWG * kRedWg * 4 : 0;
   static constexpr int kOffItem = kOffRed + kRedBytes;             // [2 slots] descriptors
   static constexpr int kOffBar = kOffItem + 2 * kItemBytes;
-  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 9 * kWG + 2 + 2 + 1 + 1 + 2;
+  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 9 * kWG + 2 + 2 + 1 + 1 + 2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 32 + 1024;
   static_assert(KR >= 16 && KR <= 64, "a head's rows sit within one warp or a warp pair");
@@ -177,6 +178,133 @@ __device__ __forceinline__ void split_p(const float* x, uint32_t* hi, uint32_t* 
   }
 }
 
+// The Q tile of a unit as e4m3 rows of `qbuf` in the 128-byte swizzled
+// K-major layout: GR rows (row c = hq * RH + n: head g0 + hq, packed row
+// n0 + n), for bf16 Q first the hi parts, then the lo parts (rows GR + c),
+// of x = q 2^shift with the power of two shift putting the tile's largest
+// |q| in [128, 256); returns shift (0 for e4m3 Q).  Run by kNT threads (ti =
+// 0 .. kNT - 1); with more than one warp, `red` holds kNT / 32 floats of
+// shared memory and `bar` names a barrier of exactly those threads.
+template <class C, bool kQe4m3, int kNT>
+__device__ __forceinline__ int convert_q_tile(const DecodeDev& a, uint8_t* qbuf, int b, int g0, int n0, int ti,
+                                              float* red, int bar) {
+  constexpr int GR = C::GR, RH = C::kRH;
+  constexpr int kChunks = GR * 8 / kNT;  // 16-element chunks per thread
+  static_assert(kChunks >= 1 && kChunks * kNT == GR * 8, "chunks");
+  // one warp loads in two halves (registers); a larger group loads at once
+  constexpr int kHalf = (kNT == 32 && kChunks >= 2) ? kChunks / 2 : kChunks;
+  constexpr int kWords = kQe4m3 ? 1 : 2;  // 16-byte words per chunk
+  const int lane = ti & 31;
+  auto q_src = [&](int kc, bool& live) -> const uint4* {
+    const int id = kc * kNT + ti;
+    const int c = id >> 3, cc = id & 7;
+    const int hq = c / RH, qrow = n0 + c % RH;
+    live = qrow < a.n_q;
+    const int64_t off =
+        b * a.q_seq + (static_cast<int64_t>(g0 + hq) * a.n_q + (live ? qrow : 0)) * kHeadDimDev + cc * 16;
+    return kQe4m3 ? reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + off)
+                  : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + off);
+  };
+  int shift = 0;
+  if (!kQe4m3) {
+    // bf16 |q| max: integer max of the magnitude bits; the loads of a half
+    // are all issued before any is used (one memory latency per half)
+    uint32_t mbits = 0;
+#pragma unroll
+    for (int k0 = 0; k0 < kChunks; k0 += kHalf) {
+      uint4 raw[kHalf][2];
+#pragma unroll
+      for (int u = 0; u < kHalf; ++u) {
+        bool live;
+        const uint4* src = q_src(k0 + u, live);
+        raw[u][0] = live ? src[0] : make_uint4(0u, 0u, 0u, 0u);
+        raw[u][1] = live ? src[1] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kHalf; ++u) {
+        const uint32_t w8[8] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
+                                raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
+#pragma unroll
+        for (int wi = 0; wi < 8; ++wi) {
+          mbits = max(mbits, w8[wi] & 0x7FFFu);
+          mbits = max(mbits, (w8[wi] >> 16) & 0x7FFFu);
+        }
+      }
+    }
+    float amax = __uint_as_float(mbits << 16);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if constexpr (kNT > 32) {
+      if (lane == 0) red[ti >> 5] = amax;
+      ptx::named_bar_sync(bar, kNT);
+#pragma unroll
+      for (int w = 0; w < kNT / 32; ++w) amax = fmaxf(amax, red[w]);
+    }
+    if (amax > 0.f) {
+      const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+      shift = 7 - e;  // max |q| 2^shift in [128, 256)
+      shift = shift > 126 ? 126 : (shift < -126 ? -126 : shift);
+    }
+  }
+  const float qscale = kQe4m3 ? 1.f : ldexpf(1.f, shift);
+  if (kQe4m3 && GR < C::kN1) {
+    for (int id = ti; id < (C::kN1 - GR) * 8; id += kNT)
+      *reinterpret_cast<uint4*>(qbuf + GR * 128 + id * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  // the conversion pass reads the chunks again (from L1)
+#pragma unroll 2
+  for (int kc = 0; kc < kChunks; ++kc) {
+    const int id = kc * kNT + ti;
+    const int c = id >> 3, cc = id & 7;
+    bool live;
+    const uint4* src = q_src(kc, live);
+    uint4 raw[kWords];
+#pragma unroll
+    for (int wd = 0; wd < kWords; ++wd) raw[wd] = live ? src[wd] : make_uint4(0u, 0u, 0u, 0u);
+    float x[16];
+    if (kQe4m3) {
+      const uint32_t w4[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) e4m3x4_to_f32(w4[wi], x + wi * 4);
+    } else {
+      const uint32_t w8[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w,
+                              raw[kWords - 1].x, raw[kWords - 1].y, raw[kWords - 1].z, raw[kWords - 1].w};
+#pragma unroll
+      for (int wi = 0; wi < 8; ++wi) {
+        x[2 * wi] = __uint_as_float(w8[wi] << 16);
+        x[2 * wi + 1] = __uint_as_float(w8[wi] & 0xFFFF0000u);
+      }
+    }
+    uint32_t hwd[4], lwd[4];
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint16_t h01, h23, l01 = 0, l23 = 0;
+      if (kQe4m3) {
+        h01 = ptx::f32x2_to_e4m3x2(x[4 * wi], x[4 * wi + 1]);
+        h23 = ptx::f32x2_to_e4m3x2(x[4 * wi + 2], x[4 * wi + 3]);
+      } else {
+        float xs[4], hf[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) xs[e] = x[4 * wi + e] * qscale;
+        h01 = ptx::f32x2_to_e4m3x2(xs[0], xs[1]);
+        h23 = ptx::f32x2_to_e4m3x2(xs[2], xs[3]);
+        e4m3x4_to_f32(static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16), hf);
+        l01 = ptx::f32x2_to_e4m3x2(xs[0] - hf[0], xs[1] - hf[1]);
+        l23 = ptx::f32x2_to_e4m3x2(xs[2] - hf[2], xs[3] - hf[3]);
+      }
+      hwd[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
+      lwd[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+    }
+    // 128-byte swizzle: chunk cc of row c at chunk position cc ^ (c % 8)
+    *reinterpret_cast<uint4*>(qbuf + c * 128 + ((cc ^ (c & 7)) << 4)) = make_uint4(hwd[0], hwd[1], hwd[2], hwd[3]);
+    if (!kQe4m3) {
+      const int cl = GR + c;
+      *reinterpret_cast<uint4*>(qbuf + cl * 128 + ((cc ^ (cl & 7)) << 4)) = make_uint4(lwd[0], lwd[1], lwd[2], lwd[3]);
+    }
+  }
+  return shift;
+}
+
 // Named barriers: 1 + wg within a softmax warpgroup, kBarAll across both.
 constexpr int kBarAll = 3;
 
@@ -223,6 +351,8 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   const uint32_t drain = ofree + 8u;
   // the descriptor alone (the producer needs no Q): before the Q conversion
   auto dfull = [&](int slot) { return drain + 8u * (1 + slot); };
+  // the first unit's Q tile converted (by the softmax warps)
+  const uint32_t qcvt = drain + 8u * 3;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -256,6 +386,7 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     }
     ptx::mbar_init(ofree, 4 * kWG);
     ptx::mbar_init(drain, 2);
+    ptx::mbar_init(qcvt, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -293,8 +424,9 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       }
       int u = 0, b = 0, t_begin = 0, t_end = 0, wslot = 0, qt = 0, grp = 0;
       bool valid = false;
-      for (;;) {  // the next unit that is not padding
-        if (lane == 0) u = atomicAdd(sched, 1);
+      for (bool first = it == 0;; first = false) {  // the next unit that is not padding
+        // the first unit of CTA x is unit x; later ones come from the counter
+        if (lane == 0) u = first ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
         u = __shfl_sync(0xffffffffu, u, 0);
         if (u >= num_units) break;
         grp = u % groups;
@@ -339,115 +471,18 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           I.vd[lane] = a.vd[b * a.vd_seq + g * a.vd_head];
           I.cs[lane] = a.softmax_scale * a.qd[b * a.qd_seq + g * a.qd_head] * a.kd[b * a.kd_seq + g * a.kd_head];
         }
-        // Q rows: column c = hq * RH + n (head g0 + hq, packed row n0 + n);
-        // chunk id = c * 8 + 16-element chunk, lane l owning ids l + 32 kc.
-        // The loads of a half are all issued before any is used (one memory
-        // latency per half); the conversion pass reads them again from L1.
-        constexpr int kChunks = GR * 8 / 32;
-        constexpr int kHalf = kChunks >= 2 ? kChunks / 2 : 1;
-        constexpr int kWords = kQe4m3 ? 1 : 2;  // 16-byte words per chunk
-        auto q_src = [&](int kc, bool& live) -> const uint4* {
-          const int id = kc * 32 + lane;
-          const int c = id >> 3, cc = id & 7;
-          const int hq = c / RH, qrow = n0 + c % RH;
-          live = qrow < a.n_q;
-          const int64_t off =
-              b * a.q_seq + (static_cast<int64_t>(g0 + hq) * a.n_q + (live ? qrow : 0)) * kHeadDimDev + cc * 16;
-          return kQe4m3 ? reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) + off)
-                        : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + off);
-        };
-        int shift = 0;
-        if (!kQe4m3) {
-          // bf16 |q| max: integer max of the magnitude bits
-          uint32_t mbits = 0;
-#pragma unroll
-          for (int k0 = 0; k0 < kChunks; k0 += kHalf) {
-            uint4 raw[kHalf][2];
-#pragma unroll
-            for (int u = 0; u < kHalf; ++u) {
-              bool live;
-              const uint4* src = q_src(k0 + u, live);
-              raw[u][0] = live ? src[0] : make_uint4(0u, 0u, 0u, 0u);
-              raw[u][1] = live ? src[1] : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int u = 0; u < kHalf; ++u) {
-              const uint32_t w8[8] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
-                                      raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
-#pragma unroll
-              for (int wi = 0; wi < 8; ++wi) {
-                mbits = max(mbits, w8[wi] & 0x7FFFu);
-                mbits = max(mbits, (w8[wi] >> 16) & 0x7FFFu);
-              }
-            }
-          }
-          float amax = __uint_as_float(mbits << 16);
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-          if (amax > 0.f) {
-            const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-            shift = 7 - e;  // max |q| 2^shift in [128, 256)
-            shift = shift > 126 ? 126 : (shift < -126 ? -126 : shift);
-          }
+        if (it == 0 && C::kPair) {
+          // G = 2: the first unit's Q tile (64 rows) is converted by the
+          // softmax warps (idle until then, and eight times as many); the
+          // 32-row instances measured slower with that code beside their
+          // softmax (more register spills)
+          const bool done = ptx::mbar_wait_bounded(qcvt, 0, abort_flag, kWaitNs);
+          if (!done && lane == 0) set_abort(abort_flag, a.status);
+        } else {
+          const int shift =
+              convert_q_tile<C, kQe4m3, 32>(a, sm + C::kOffQ + slot * C::kQBytes, b, g0, n0, lane, nullptr, 0);
+          if (lane == 0) I.shift = shift;
         }
-        const float qscale = kQe4m3 ? 1.f : ldexpf(1.f, shift);
-        uint8_t* qbuf = sm + C::kOffQ + slot * C::kQBytes;
-        if (kQe4m3 && GR < C::kN1) {
-          for (int id = lane; id < (C::kN1 - GR) * 8; id += 32)
-            *reinterpret_cast<uint4*>(qbuf + GR * 128 + id * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll 2
-        for (int kc = 0; kc < kChunks; ++kc) {
-          const int id = kc * 32 + lane;
-          const int c = id >> 3, cc = id & 7;
-          bool live;
-          const uint4* src = q_src(kc, live);
-          uint4 raw[kWords];
-#pragma unroll
-          for (int wd = 0; wd < kWords; ++wd) raw[wd] = live ? src[wd] : make_uint4(0u, 0u, 0u, 0u);
-          float x[16];
-          if (kQe4m3) {
-            const uint32_t w4[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
-#pragma unroll
-            for (int wi = 0; wi < 4; ++wi) e4m3x4_to_f32(w4[wi], x + wi * 4);
-          } else {
-            const uint32_t w8[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w,
-                                    raw[kWords - 1].x, raw[kWords - 1].y, raw[kWords - 1].z, raw[kWords - 1].w};
-#pragma unroll
-            for (int wi = 0; wi < 8; ++wi) {
-              x[2 * wi] = __uint_as_float(w8[wi] << 16);
-              x[2 * wi + 1] = __uint_as_float(w8[wi] & 0xFFFF0000u);
-            }
-          }
-          uint32_t hwd[4], lwd[4];
-#pragma unroll
-          for (int wi = 0; wi < 4; ++wi) {
-            uint16_t h01, h23, l01 = 0, l23 = 0;
-            if (kQe4m3) {
-              h01 = ptx::f32x2_to_e4m3x2(x[4 * wi], x[4 * wi + 1]);
-              h23 = ptx::f32x2_to_e4m3x2(x[4 * wi + 2], x[4 * wi + 3]);
-            } else {
-              float xs[4], hf[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) xs[e] = x[4 * wi + e] * qscale;
-              h01 = ptx::f32x2_to_e4m3x2(xs[0], xs[1]);
-              h23 = ptx::f32x2_to_e4m3x2(xs[2], xs[3]);
-              e4m3x4_to_f32(static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16), hf);
-              l01 = ptx::f32x2_to_e4m3x2(xs[0] - hf[0], xs[1] - hf[1]);
-              l23 = ptx::f32x2_to_e4m3x2(xs[2] - hf[2], xs[3] - hf[3]);
-            }
-            hwd[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
-            lwd[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
-          }
-          // 128-byte swizzle: chunk cc of row c at chunk position cc ^ (c % 8)
-          *reinterpret_cast<uint4*>(qbuf + c * 128 + ((cc ^ (c & 7)) << 4)) = make_uint4(hwd[0], hwd[1], hwd[2], hwd[3]);
-          if (!kQe4m3) {
-            const int cl = GR + c;
-            *reinterpret_cast<uint4*>(qbuf + cl * 128 + ((cc ^ (cl & 7)) << 4)) =
-                make_uint4(lwd[0], lwd[1], lwd[2], lwd[3]);
-          }
-        }
-        if (lane == 0) I.shift = shift;
       }
       ptx::fence_proxy_async_smem();
       __syncwarp();
@@ -665,6 +700,22 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     uint8_t* const pbuf_wg = sm + C::kOffP + wg * C::kPBytes;
     float* const corr_wg = corr_all + wg * 2 * GR;
 
+    // ---- the first unit's Q tile, converted by both groups together
+    if constexpr (C::kPair) {
+      const int ti = tid - 64;
+      const bool got = ptx::mbar_wait_bounded(dfull(0), 0, abort_flag, kWaitNs);
+      const bool bad = ptx::named_bar_red_or(kBarAll, 128 * kWG, !got);
+      It& I0 = item(0);
+      if (!bad && I0.valid) {
+        const int shift =
+            convert_q_tile<C, kQe4m3, 128 * kWG>(a, sm + C::kOffQ, I0.b, I0.g0, I0.n0, ti, corr_all, kBarAll);
+        if (ti == 0) I0.shift = shift;
+      }
+      if (bad && ti == 0) set_abort(abort_flag, a.status);
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(kBarAll, 128 * kWG);
+      if (ti == 0) ptx::mbar_arrive(qcvt);
+    }
     uint32_t n_base = 0;  // tiles of all earlier units
     uint32_t tb = 0;      // this group's tiles of all earlier units
     for (int it = 0;; ++it) {
