@@ -9,8 +9,10 @@
 //
 // One (packed row, kv head, sequence) is served by kWPR warps, each taking
 // up to kPer consecutive splits: lane j of a warp loads split j's (m, l),
-// every lane loads the 16-byte piece d = 4 lane .. 4 lane + 3 of every one
-// of its splits' o, all before any is used (one memory round trip).  The
+// every lane copies the 16-byte piece d = 4 lane .. 4 lane + 3 of every one
+// of its splits' o into shared memory with asynchronous copies, all issued
+// before any is waited for (one memory round trip; register loads would be
+// scheduled one latency each).  The
 // warp's maximum comes from the (m, l) lanes, so O is one pass of FMAs in
 // split order with no rescaling.  With kWPR > 1 the warps' (max, sum, O)
 // are combined in warp order through shared memory.  Every sum runs in a
@@ -59,16 +61,18 @@ __global__ void __launch_bounds__((kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32) me
     m = a.m_part[pr];
     l = a.l_part[pr];
   }
-  // unconditional loads (splits past this warp's last read that one again,
-  // with weight 0), so that all of them are in flight at once
-  float4 o[kPer];
+  // copies of this warp's splits, all in flight at once, into its kPer x
+  // 512 B of the (dynamic) staging area; slots past its last split are
+  // zero-filled without a read (their weight is 0)
+  extern __shared__ __align__(16) float4 s_stage[];
+  float4* const st = s_stage + wic * kPer * 32;
   const int jmax = nsp - 1;
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
     const int j = j0 + u < jmax ? j0 + u : jmax;
-    o[u] = *reinterpret_cast<const float4*>(&a.o_part[(pr0 + j * split_stride) * kHeadDimDev + lane * 4]);
+    cp_async16(st + u * 32 + lane, &a.o_part[(pr0 + j * split_stride) * kHeadDimDev + lane * 4], u < cnt);
   }
-  asm volatile("" ::: "memory");  // keeps every load above ahead of the first use
+  cp_async_commit();
   // this warp's maximum, weights and weighted row sum
   float mw = m;
 #pragma unroll
@@ -78,13 +82,15 @@ __global__ void __launch_bounds__((kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32) me
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
   float4 ow = make_float4(0.f, 0.f, 0.f, 0.f);
+  cp_async_wait<0>();  // this lane's copies (it reads only its own)
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
     const float wu = __shfl_sync(0xffffffffu, wt, u);  // 0 past this warp's splits
-    ow.x = fmaf(wu, o[u].x, ow.x);
-    ow.y = fmaf(wu, o[u].y, ow.y);
-    ow.z = fmaf(wu, o[u].z, ow.z);
-    ow.w = fmaf(wu, o[u].w, ow.w);
+    const float4 o = st[u * 32 + lane];
+    ow.x = fmaf(wu, o.x, ow.x);
+    ow.y = fmaf(wu, o.y, ow.y);
+    ow.z = fmaf(wu, o.z, ow.z);
+    ow.w = fmaf(wu, o.w, ow.w);
   }
   float mx = mw, lsum = lw;
   if constexpr (kWPR > 1) {
@@ -132,7 +138,12 @@ cudaError_t launch_merge_t(const DecodeDev& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kThreads / 32 * kPer * 32 * 16;  // the staging area: 8 KB a warp
+  if (cfg.dynamicSmemBytes > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(merge_kernel<kWPR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(cfg.dynamicSmemBytes));
+    if (e != cudaSuccess) return e;
+  }
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
