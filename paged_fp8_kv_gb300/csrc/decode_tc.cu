@@ -95,7 +95,13 @@ constexpr int kTileKV = 128;                 // KV rows per tile (MMA M)
 constexpr int kKVTileBytes = kTileKV * 128;  // one K or V tile: 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legal wait
 constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
-constexpr float kLog2P448 = 8.807354922057604f;  // log2(448): P is produced as 448 p
+// P is produced as x = 448 p 2^-kTau: a column's reference maximum m moves
+// only when a score passes m + kTau (log2 units), so x stays within e4m3's
+// range and most tiles need neither the column reduction nor an O
+// correction; the result does not depend on m.
+constexpr int kTau = 4;
+constexpr float kLog2PScale = 8.807354922057604f - kTau;  // log2(448 2^-kTau)
+constexpr float kPScaleInv = (1.f / 448.f) * (1 << kTau);
 
 constexpr int pow2_at_least(int x) {
   int p = 32;
@@ -155,15 +161,6 @@ struct Bars {
 __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) {
   *abort = 1;
   if (status) atomicExch(status, kStatusTimeout);
-}
-
-// x rounded to 4 significant bits, ties to even: the value e4m3 gives a
-// non-negative x in its normal range [2^-6, 448] (below 2^-6 the e4m3 grid is
-// coarser; the caller's residual then carries an error below 2^-10).
-__device__ __forceinline__ float round_4_sig_bits(float x) {
-  uint32_t u = __float_as_uint(x);
-  u = (u + 0x7FFFFu + ((u >> 20) & 1u)) & 0xFFF00000u;
-  return __uint_as_float(u);
 }
 
 template <int R, bool kQe4m3>
@@ -520,6 +517,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     // raw (computed) score -> logit and -> log2 units; 2^-shift undoes the Q scaling
     const float cta_scale = a.softmax_scale * qd * kd * ldexpf(1.f, -shift);
     const float c2 = cta_scale * kLog2e;
+    const float head_c = kTau / c2;  // kTau in raw score units
 
     float l_thr[kCols];  // deferred row sums (of 448 p) for this thread's columns
 #pragma unroll
@@ -577,17 +575,19 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       };
       load_s();
 
-      // Running maximum (shared, identical for every thread): only when some
-      // row sees a score above it (one barrier-reduction answers that for
-      // the group) are the column maxima reduced: reduce-scatter in the
-      // warp, the four warps through shared memory, then thread c updates
-      // column c.  Otherwise the tile needs no exchange at all.
+      // Reference maxima (shared, identical for every thread): only when
+      // some score passes its column's m + kTau (one barrier-reduction
+      // answers that for the group) are the column maxima reduced:
+      // reduce-scatter in the warp, the four warps through shared memory,
+      // then thread c updates column c.  Otherwise the tile needs no
+      // exchange at all.
       const float* m_now = m_s + mb * R + col0;
       bool exceed = false;
 #pragma unroll
       for (int c4 = 0; c4 < kCols; c4 += 4) {
         const float4 m4 = *reinterpret_cast<const float4*>(m_now + c4);
-        exceed |= (sc[c4] > m4.x) | (sc[c4 + 1] > m4.y) | (sc[c4 + 2] > m4.z) | (sc[c4 + 3] > m4.w);
+        exceed |= (sc[c4] > m4.x + head_c) | (sc[c4 + 1] > m4.y + head_c) | (sc[c4 + 2] > m4.z + head_c) |
+                  (sc[c4 + 3] > m4.w + head_c);
       }
       bool moved = false;
       if (ptx::named_bar_red_or(kBarSm, kSmT, exceed)) {
@@ -603,12 +603,12 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           const int c = st_tid;
           const float t = fmaxf(fmaxf(red[c], red[R + c]), fmaxf(red[2 * R + c], red[3 * R + c]));
           const float mo = m_s[mb * R + c];
-          const float mn = fmaxf(mo, t);
-          moved_c = mn != mo;
+          moved_c = t > mo + head_c;
+          const float mn = moved_c ? t : mo;
           // corr = 2^((m_old - m_use) c2); the -inf guard makes it 0 for a
           // column that had seen no key
           const float mu = (mn == -INFINITY) ? 0.f : mn;
-          corr_s[c] = fast_exp2((mo - mu) * c2);
+          corr_s[c] = moved_c ? fast_exp2((mo - mu) * c2) : 1.f;
           m_s[(mb ^ 1) * R + c] = mn;
         }
         moved = ptx::named_bar_red_or(kBarSm, kSmT, moved_c);
@@ -654,9 +654,9 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         }
         ptx::tmem_st_wait();
       }
-      // 448 p = 2^((s - m) c2 + log2 448), directly in e4m3's range; the row
-      // sums keep the same factor 448.  The -inf guard uses 0 as the
-      // reference of a column that has seen no key yet.
+      // x = 448 p 2^-kTau = 2^((s - m) c2 + log2 448 - kTau), within e4m3's
+      // range; the row sums keep the same factor.  The -inf guard uses 0 as
+      // the reference of a column that has seen no key yet.
       {
         const float* m_new = m_s + mb * R + col0;
 #pragma unroll
@@ -666,7 +666,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float m_use = (mm[e] == -INFINITY) ? 0.f : mm[e];
-            const float p = fast_exp2(fmaf(sc[c4 + e], c2, fmaf(-m_use, c2, kLog2P448)));
+            const float p = fast_exp2(fmaf(sc[c4 + e], c2, fmaf(-m_use, c2, kLog2PScale)));
             l_thr[c4 + e] += p;
             sc[c4 + e] = p;
           }
@@ -679,25 +679,11 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         ok = false;
         break;
       }
-      // split x = 448 p = hi + lo (e4m3); hi -> column c, lo -> column R + c
-      // of the P buffer [kN2/16 groups][128 rows][16 bytes]
+      // split x = hi + lo (e4m3, through half precision); hi -> column c,
+      // lo -> column R + c of the P buffer [kN2/16 groups][128 rows][16 bytes]
       {
         uint32_t hw[kCols / 4], lw[kCols / 4];
-#pragma unroll
-        for (int wi = 0; wi < kCols / 4; ++wi) {
-          float x[4], hf[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[e] = sc[wi * 4 + e];
-            hf[e] = round_4_sig_bits(x[e]);
-          }
-          const uint16_t h01 = ptx::f32x2_to_e4m3x2(hf[0], hf[1]);
-          const uint16_t h23 = ptx::f32x2_to_e4m3x2(hf[2], hf[3]);
-          hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
-          const uint16_t l01 = ptx::f32x2_to_e4m3x2(x[0] - hf[0], x[1] - hf[1]);
-          const uint16_t l23 = ptx::f32x2_to_e4m3x2(x[2] - hf[2], x[3] - hf[3]);
-          lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
-        }
+        split_e4m3_hilo<kCols>(sc, hw, lw);
         uint8_t* pbuf = sm + C::kOffP + pb * C::kPBytes + row * 16;
         if (R == 8) {
           *reinterpret_cast<uint4*>(pbuf) = make_uint4(hw[0], hw[1], lw[0], lw[1]);
@@ -755,7 +741,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::named_bar_sync(kBarSm, kSmT);
       const int nsp = a.n_splits[b];
       const bool final_out = nsp <= 1;
-      const float out_scale = vd * (1.f / 448.f);  // O and the row sums both carry 448
+      const float out_scale = vd * kPScaleInv;  // O and the row sums both carry 448 2^-kTau
       const int d = row;  // TMEM lane of O = head-dim index
       float o_row[kCols];  // O[d][c] = hi column c + lo column R + c
       if constexpr (C::kHalves == 1) {
@@ -789,7 +775,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         const int c = col0 + cl;
         const int n = n0 + c;
         if (n >= a.n_q) break;
-        const float l = (red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c]) * (1.f / 448.f);
+        const float l = (red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c]) * kPScaleInv;
         const float o = o_row[cl] * out_scale;
         if (final_out) {
           const int64_t orow = b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + n) * kHeadDimDev;
@@ -801,7 +787,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       }
       if (st_tid < R && n0 + st_tid < a.n_q) {
         const int c = st_tid, n = n0 + c;
-        const float l = (red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c]) * (1.f / 448.f);
+        const float l = (red[c] + red[R + c] + red[2 * R + c] + red[3 * R + c]) * kPScaleInv;
         const float m_logit = m_fin[c] * cta_scale;
         if (final_out) {
           a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + n] = m_logit + logf(l);
