@@ -42,7 +42,13 @@ constexpr int kTileBytes = kRows * 128;      // one K or V tile (128 keys x d): 
 constexpr int kPartBytes = kRows * 128;      // one e4m3 operand of 128 rows x 128 bytes
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legal wait
 constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
-constexpr float kLog2P448 = 8.807354922057604f;  // log2(448)
+// P is produced as x = 448 p 2^-kTau: a row's reference maximum m moves only
+// when the tile's maximum passes m + kTau (log2 units), so x stays within
+// e4m3's range and most tiles need no O correction; the result does not
+// depend on m.
+constexpr int kTau = 4;
+constexpr float kLog2PScale = 8.807354922057604f - kTau;  // log2(448 2^-kTau)
+constexpr float kPScaleInv = (1.f / 448.f) * (1 << kTau);
 constexpr int kWG = 2;                       // softmax warpgroups, alternate tiles
 constexpr int kThreads = 64 + 128 * kWG + 64;
 constexpr int kMma2Warp = 2 + 4 * kWG;       // 10
@@ -373,8 +379,9 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     lim = lim < L - 1 ? lim : L - 1;
     if (!live) lim = -1;
 
-    float m_run = -INFINITY;  // running row max (raw units)
-    float l_run = 0.f;        // running row sum of 448 p
+    float m_run = -INFINITY;  // reference row maximum (raw units)
+    float l_run = 0.f;        // running row sum of x = 448 p 2^-kTau
+    const float head_c = kTau / c2;  // kTau in raw score units
     bool ok = true;
     int t_last = -1;
     // A warp whose 32 rows are all past n_q computes nothing: its P rows
@@ -408,9 +415,9 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           }
         }
         if (!live) mt = -INFINITY;  // keeps the maximum of an empty row at -inf
-        const float m_new = fmaxf(m_run, mt);
+        const bool moved = mt > m_run + head_c;
+        const float m_new = moved ? mt : m_run;
         const float mu = (m_new == -INFINITY) ? 0.f : m_new;  // the -inf guard
-        const bool moved = m_new != m_run;
         const float corr = moved ? fast_exp2((m_run - mu) * c2) : 1.f;  // 0 for a fresh row
         l_run *= corr;
         m_run = m_new;
@@ -433,14 +440,14 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           }
           ptx::tmem_st_wait();
         }
-        // pass 2: x = 448 p = 256 * 2^((s - m) c + log2 448 - 8) in packed
-        // halves (ex2.approx.f16x2 of an argument <= 0.81, where half
-        // precision resolves it to 2^-11, times an exact 256; x <= 448 with
-        // about 11 significant bits), split x = hi + lo with hi = e4m3(x) and
+        // pass 2: x = 448 p 2^-kTau = 256 * 2^((s - m) c + log2 448 - kTau - 8)
+        // in packed halves (ex2.approx.f16x2 of an argument <= 0.81, where
+        // half precision resolves it to 2^-11, times an exact 256; x <= 448
+        // with about 11 significant bits), split x = hi + lo with hi = e4m3(x) and
         // lo = e4m3(x - hi) (x - hi is exact in half precision); row sums of
         // x in halves per 16 keys, then in fp32.  Half the exponentials and a
         // third of the ALU work of an fp32 split.
-        const float bias = fmaf(-mu, c2, kLog2P448 - 8.f);
+        const float bias = fmaf(-mu, c2, kLog2PScale - 8.f);
         constexpr uint32_t k256x2 = 0x5C005C00u;  // (256, 256) in half precision
   #pragma unroll
         for (int h0 = 0; h0 < kRows; h0 += 64) {
@@ -448,6 +455,13 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
           ptx::tmem_ld_wait();
+          if (h0 + 64 == kRows) {
+            // S is read whole: the group's next GEMM1 may overwrite it while
+            // the last half is turned into P
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
+          }
   #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int cc = h0 / 16 + q;  // 16-key chunk of the P row
@@ -482,9 +496,11 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           }
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));  // S read
+      if (!warp_live) {  // S read (a live warp released it after its last load)
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
+      }
       // keys past the sequence end: zero their V rows (0 * poison must not
       // reach O; the TMA landed whole pages).  Thread r owns key row r.
       if (key0 + kRows > L) {
@@ -519,9 +535,9 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const float mx = fmaxf(m_run, m1);
       const float f0 = (m_run == -INFINITY) ? 0.f : fast_exp2((m_run - mx) * c2);
       const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - mx) * c2);
-      const float l = (l_run * f0 + l1 * f1) * (1.f / 448.f);
+      const float l = (l_run * f0 + l1 * f1) * kPScaleInv;
       const bool final_out = a.n_splits[b] <= 1;
-      const float f = vd * (1.f / 448.f) * (final_out ? a.scale_o / (l + 1e-30f) : 1.f);
+      const float f = vd * kPScaleInv * (final_out ? a.scale_o / (l + 1e-30f) : 1.f);
       const int64_t orow = final_out ? b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + (live ? qrow : 0)) * kHeadDimDev
                                      : part_row(a, b, g, slot, live ? qrow : 0) * kHeadDimDev;
       const uint32_t o1 = tmem + C::kWgCols + kRows + lane_off;  // group 1's O, same lanes

@@ -834,6 +834,7 @@ cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles
     case 8: return launch_tc_q<8>(a, n_q_tiles, q_e4m3, stream);
     case 16: return launch_tc_q<16>(a, n_q_tiles, q_e4m3, stream);
     case 32: return launch_tc_q<32>(a, n_q_tiles, q_e4m3, stream);
+    case 64: return launch_tc_q<64>(a, n_q_tiles, q_e4m3, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -843,6 +844,7 @@ int tc_min_blocks(int rows_per_cta, bool q_e4m3) {
     case 8: return q_e4m3 ? TcCfg<8, true>::kMinBlocks : TcCfg<8, false>::kMinBlocks;
     case 16: return q_e4m3 ? TcCfg<16, true>::kMinBlocks : TcCfg<16, false>::kMinBlocks;
     case 32: return q_e4m3 ? TcCfg<32, true>::kMinBlocks : TcCfg<32, false>::kMinBlocks;
+    case 64: return q_e4m3 ? TcCfg<64, true>::kMinBlocks : TcCfg<64, false>::kMinBlocks;
     default: return 1;
   }
 }
@@ -852,6 +854,7 @@ int tc_smem_bytes(int rows_per_cta, bool q_e4m3) {
     case 8: return q_e4m3 ? TcCfg<8, true>::kBytes : TcCfg<8, false>::kBytes;
     case 16: return q_e4m3 ? TcCfg<16, true>::kBytes : TcCfg<16, false>::kBytes;
     case 32: return q_e4m3 ? TcCfg<32, true>::kBytes : TcCfg<32, false>::kBytes;
+    case 64: return q_e4m3 ? TcCfg<64, true>::kBytes : TcCfg<64, false>::kBytes;
     default: return 0;
   }
 }

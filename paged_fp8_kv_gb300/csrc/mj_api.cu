@@ -103,11 +103,11 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
     k.name = names[e4m3][g == 8 ? 0 : (g == 4 ? 1 : 2)];
   } else {
     k.kind = KernelKind::kTensorCore;
-    k.rows_per_cta = n_q <= 8 ? 8 : (n_q <= 16 ? 16 : 32);
+    k.rows_per_cta = n_q <= 8 ? 8 : (n_q <= 16 ? 16 : (n_q <= 32 ? 32 : 64));
     smem = tc_smem_bytes(k.rows_per_cta, e4m3);
-    static const char* names[2][3] = {{"tc_r8_bf16", "tc_r16_bf16", "tc_r32_bf16"},
-                                      {"tc_r8_e4m3", "tc_r16_e4m3", "tc_r32_e4m3"}};
-    const int idx = k.rows_per_cta == 8 ? 0 : (k.rows_per_cta == 16 ? 1 : 2);
+    static const char* names[2][4] = {{"tc_r8_bf16", "tc_r16_bf16", "tc_r32_bf16", "tc_r64_bf16"},
+                                      {"tc_r8_e4m3", "tc_r16_e4m3", "tc_r32_e4m3", "tc_r64_e4m3"}};
+    const int idx = k.rows_per_cta == 8 ? 0 : (k.rows_per_cta == 16 ? 1 : (k.rows_per_cta == 32 ? 2 : 3));
     k.name = names[e4m3][idx];
   }
   k.n_q_tiles = (n_q + k.rows_per_cta - 1) / k.rows_per_cta;
