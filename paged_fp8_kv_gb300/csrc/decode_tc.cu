@@ -102,6 +102,10 @@ constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
 constexpr int kTau = 4;
 constexpr float kLog2PScale = 8.807354922057604f - kTau;  // log2(448 2^-kTau)
 constexpr float kPScaleInv = (1.f / 448.f) * (1 << kTau);
+// P's lo part is stored as e4m3((x - hi) 2^kLoShift) and its products are
+// weighted back by 2^-kLoShift when the hi and lo columns of O are added
+constexpr int kLoShift = 4;
+constexpr float kLoInv = 1.f / (1 << kLoShift);
 
 constexpr int pow2_at_least(int x) {
   int p = 32;
@@ -683,7 +687,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       // lo -> column R + c of the P buffer [kN2/16 groups][128 rows][16 bytes]
       {
         uint32_t hw[kCols / 4], lw[kCols / 4];
-        split_e4m3_hilo<kCols>(sc, hw, lw);
+        split_e4m3_hilo<kCols, kLoShift>(sc, hw, lw);
         uint8_t* pbuf = sm + C::kOffP + pb * C::kPBytes + row * 16;
         if (R == 8) {
           *reinterpret_cast<uint4*>(pbuf) = make_uint4(hw[0], hw[1], lw[0], lw[1]);
@@ -756,7 +760,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
             if (c < R)
               o_row[c] = __uint_as_float(r[e]);
             else
-              o_row[c - R] += __uint_as_float(r[e]);
+              o_row[c - R] += __uint_as_float(r[e]) * kLoInv;
           }
         }
       } else {
@@ -767,7 +771,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           MJ_TMEM_LD16(tmem_o + lane_off + R + col0 + c0, rl);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o_row[c0 + e] = __uint_as_float(rh[e]) + __uint_as_float(rl[e]);
+          for (int e = 0; e < 16; ++e) o_row[c0 + e] = __uint_as_float(rh[e]) + __uint_as_float(rl[e]) * kLoInv;
         }
       }
 #pragma unroll

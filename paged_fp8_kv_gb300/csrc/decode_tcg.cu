@@ -58,7 +58,6 @@ constexpr int kRows = 128;                   // MMA M: rows of one tile
 constexpr int kTileBytes = kRows * 128;      // one K or V tile: 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far above any legal wait
 constexpr int kStatusTimeout = 5;            // MJ_ERR_TIMEOUT
-constexpr float kLog2P448 = 8.807354922057604f;  // log2(448): P is produced as 448 p
 constexpr int kWG = 2;                       // softmax warpgroups
 constexpr int kThreads = 64 + 128 * kWG + 96;
 constexpr int kSchedWarp = 2 + 4 * kWG;      // warp index of the scheduler
@@ -92,9 +91,13 @@ struct GCfg {
   // P is produced as x = 448 p 2^-kTau: a column's reference maximum is
   // moved only when a score passes it by kTau (log2 units); kTau = 0 is the
   // exact running maximum
-  static constexpr int kTau = kPair ? 4 : 0;
+  static constexpr int kTau = 4;
   static constexpr float kLog2PScale = 8.807354922057604f - kTau;  // log2(448 2^-kTau)
   static constexpr float kPScaleInv = (1.f / 448.f) * (1 << kTau);
+  // P's lo part is stored as e4m3((x - hi) 2^kLoShift); its products are
+  // weighted back by 2^-kLoShift when the hi and lo columns of O are added
+  static constexpr int kLoShift = 4;
+  static constexpr float kLoInv = 1.f / (1 << kLoShift);
   static constexpr int kStagesK = kPair ? 4 : 5;
   static constexpr int kStagesV = kPair ? 5 : 7;
   static constexpr int kQBytes = kN1 * 128;
@@ -153,29 +156,6 @@ struct Item {
 __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) {
   *abort = 1;
   if (status) atomicExch(status, kStatusTimeout);
-}
-
-__device__ __forceinline__ float round_4_sig_bits(float x) {
-  uint32_t u = __float_as_uint(x);
-  u = (u + 0x7FFFFu + ((u >> 20) & 1u)) & 0xFFF00000u;
-  return __uint_as_float(u);
-}
-
-// `N` e4m3 codes (N in {4, 8}) of the hi and lo parts of x = 448 p.
-template <int N>
-__device__ __forceinline__ void split_p(const float* x, uint32_t* hi, uint32_t* lo) {
-#pragma unroll
-  for (int w = 0; w < N / 4; ++w) {
-    float h[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) h[e] = round_4_sig_bits(x[4 * w + e]);
-    const uint16_t h01 = ptx::f32x2_to_e4m3x2(h[0], h[1]);
-    const uint16_t h23 = ptx::f32x2_to_e4m3x2(h[2], h[3]);
-    const uint16_t l01 = ptx::f32x2_to_e4m3x2(x[4 * w] - h[0], x[4 * w + 1] - h[1]);
-    const uint16_t l23 = ptx::f32x2_to_e4m3x2(x[4 * w + 2] - h[2], x[4 * w + 3] - h[3]);
-    hi[w] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
-    lo[w] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
-  }
 }
 
 // The Q tile of a unit as e4m3 rows of `qbuf` in the 128-byte swizzled
@@ -888,7 +868,7 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           }
           {
             uint32_t hi[RH / 4], lo[RH / 4];
-            split_e4m3_hilo<RH>(sc, hi, lo);
+            split_e4m3_hilo<RH, C::kLoShift>(sc, hi, lo);
             // this head's P: [hi groups 0, 1 | lo groups 2, 3][KR keys][16 B]
             uint8_t* prow = pbuf_wg + pb * C::kPBufBytes + h * C::kPHeadBytes + k * 16;
             constexpr int kGS = KR * 16;  // bytes between 16-column groups
@@ -933,12 +913,16 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           my_l[h * RH + lane] = (l_thr[0] + red[pq * 32 + lane]) * C::kPScaleInv;
         }
       } else {
-      float l_thr[RH], m_cur[RH];  // deferred row sums (of 448 p); running column max (raw)
+      // deferred row sums (of 448 p 2^-kTau); reference column maxima (raw)
+      // and the scores that would move them
+      float l_thr[RH], m_cur[RH], thr[RH];
+      const float head_c = C::kTau / c2;
       int lim[RH];                 // last visible key of column n of this row's head (-1: none)
 #pragma unroll
       for (int nn = 0; nn < RH; ++nn) {
         l_thr[nn] = 0.f;
         m_cur[nn] = -INFINITY;
+        thr[nn] = -INFINITY;  // a fresh column: its first finite score moves it
         const int qrow = n0 + nn;
         int l = a.causal ? L - a.q_len + qrow / a.h_r : L - 1;
         l = l < L - 1 ? l : L - 1;
@@ -985,29 +969,40 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(wgbar(wg, 2 + sb));
 
-        // column maxima of this head: shuffles within the head's KR lanes
-        bool moved = false;
-        float corr[RH];
+        // A column's reference maximum m moves only where a score passes
+        // m + kTau / c2 (so 448 p 2^-kTau stays within e4m3's range): one
+        // barrier tells the group whether any score does; only then are the
+        // column maxima reduced (shuffles within the head's KR lanes).
+        bool ex = false;
 #pragma unroll
-        for (int nn = 0; nn < RH; ++nn) {
-          float v = sc[nn];
+        for (int nn = 0; nn < RH; ++nn) ex |= sc[nn] > thr[nn];
+        bool any_moved = false;
+        if (ptx::named_bar_red_or(bar_wg, 128, ex)) {
+          bool moved = false;
+          float corr[RH];
 #pragma unroll
-          for (int off = KR / 2; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-          const float mn = fmaxf(m_cur[nn], v);
-          moved |= (mn != m_cur[nn]);
-          const float mu = (mn == -INFINITY) ? 0.f : mn;
-          corr[nn] = fast_exp2((m_cur[nn] - mu) * c2);  // the -inf guard: 0 for a fresh column
-          m_cur[nn] = mn;
-        }
-        float* corr_b = corr_wg + sb * GR;
-        if (k == 0) {
+          for (int nn = 0; nn < RH; ++nn) {
+            float v = sc[nn];
 #pragma unroll
-          for (int nn = 0; nn < RH; ++nn) corr_b[h * RH + nn] = moved ? corr[nn] : 1.f;
-        }
-        const bool any_moved = ptx::named_bar_red_or(bar_wg, 128, moved);
-        if (moved) {
+            for (int off = KR / 2; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+            const bool mv = v > thr[nn];
+            const float mn = mv ? v : m_cur[nn];
+            const float mu = (mn == -INFINITY) ? 0.f : mn;
+            corr[nn] = mv ? fast_exp2((m_cur[nn] - mu) * c2) : 1.f;  // the -inf guard: 0 for a fresh column
+            moved |= mv;
+            m_cur[nn] = mn;
+            thr[nn] = (mn == -INFINITY) ? -INFINITY : mn + head_c;
+          }
+          float* corr_b = corr_wg + sb * GR;
+          if (k == 0) {
 #pragma unroll
-          for (int nn = 0; nn < RH; ++nn) l_thr[nn] *= corr[nn];
+            for (int nn = 0; nn < RH; ++nn) corr_b[h * RH + nn] = corr[nn];
+          }
+          any_moved = ptx::named_bar_red_or(bar_wg, 128, moved);
+          if (moved) {
+#pragma unroll
+            for (int nn = 0; nn < RH; ++nn) l_thr[nn] *= corr[nn];
+          }
         }
         // This group's P buffer and O are free once the GEMM2 of its previous
         // tile finished (the one before that was waited for a tile ago, so
@@ -1017,6 +1012,7 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         // every head's columns, so any moved maximum corrects all of them
         // (the condition is uniform over the group: TMEM access is warp-wide)
         if (any_moved && !first) {
+          const float* corr_b = corr_wg + sb * GR;
           ptx::tc_fence_after();
 #pragma unroll
           for (int c0 = 0; c0 < C::kN2; c0 += 16) {
@@ -1029,17 +1025,17 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           }
           ptx::tmem_st_wait();
         }
-        // 448 p and the row sums
+        // x = 448 p 2^-kTau and the row sums
 #pragma unroll
         for (int nn = 0; nn < RH; ++nn) {
           const float mu = (m_cur[nn] == -INFINITY) ? 0.f : m_cur[nn];
-          const float p = fast_exp2(fmaf(sc[nn], c2, fmaf(-mu, c2, kLog2P448)));
+          const float p = fast_exp2(fmaf(sc[nn], c2, fmaf(-mu, c2, C::kLog2PScale)));
           l_thr[nn] += p;
           sc[nn] = p;
         }
         {
           uint32_t hi[RH / 4], lo[RH / 4];
-          split_p<RH>(sc, hi, lo);
+          split_e4m3_hilo<RH, C::kLoShift>(sc, hi, lo);
           uint8_t* prow = pbuf_wg + row * 16;
           const int ch = h * RH, cl = GR + h * RH;  // this row's hi / lo columns
           uint8_t* ph = prow + (ch / 16) * (kRows * 16) + (ch % 16);
@@ -1087,7 +1083,7 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
         for (int nn = 0; nn < RH; ++nn) {
           my_m[h * RH + nn] = m_cur[nn];
-          my_l[h * RH + nn] = l_thr[nn] * (1.f / 448.f);
+          my_l[h * RH + nn] = l_thr[nn] * C::kPScaleInv;
         }
       }
       }
@@ -1143,7 +1139,7 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float w0 = w0_s[c0 + e];
-              ov[e] = w0 > 0.f ? (__uint_as_float(rh[e]) + __uint_as_float(rl[e])) * w0 : 0.f;
+              ov[e] = w0 > 0.f ? (__uint_as_float(rh[e]) + __uint_as_float(rl[e]) * C::kLoInv) * w0 : 0.f;
             }
           }
           {
@@ -1154,7 +1150,7 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float w1 = w1_s[c0 + e];
-              if (w1 > 0.f) ov[e] += (__uint_as_float(qh[e]) + __uint_as_float(ql[e])) * w1;
+              if (w1 > 0.f) ov[e] += (__uint_as_float(qh[e]) + __uint_as_float(ql[e]) * C::kLoInv) * w1;
             }
           }
 #pragma unroll

@@ -121,18 +121,28 @@ __device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b) {
 
 // N values 0 <= x <= 448 (N a multiple of 4) as e4m3 hi and lo parts, four
 // codes a word: x is rounded to half precision (11 significant bits), hi =
-// e4m3(x), lo = e4m3(x - hi) (the difference is exact in half precision), so
-// hi + lo carries about 8 significant bits of x.
-template <int N>
+// e4m3(x), lo = e4m3((x - hi) 2^kLoShift) (the difference is exact in half
+// precision, and |x - hi| <= x 2^-4, so a shift up to 4 stays in range and
+// keeps the lo part clear of e4m3's subnormal floor), so hi + lo 2^-kLoShift
+// carries about 8 significant bits of x.
+template <int N, int kLoShift = 0>
 __device__ __forceinline__ void split_e4m3_hilo(const float* x, uint32_t* hi, uint32_t* lo) {
+  static_assert(kLoShift >= 0 && kLoShift <= 4, "lo shift");
+  constexpr uint32_t kScale2 = (15u + kLoShift) << 10 | (15u + kLoShift) << 26;  // (2^s, 2^s) in halves
 #pragma unroll
   for (int w = 0; w < N / 4; ++w) {
     const uint32_t h01 = f32x2_to_f16x2(x[4 * w], x[4 * w + 1]);
     const uint32_t h23 = f32x2_to_f16x2(x[4 * w + 2], x[4 * w + 3]);
     const uint16_t e01 = f16x2_to_e4m3x2(h01);
     const uint16_t e23 = f16x2_to_e4m3x2(h23);
-    const uint16_t l01 = f16x2_to_e4m3x2(sub_f16x2(h01, e4m3x2_to_f16x2(e01)));
-    const uint16_t l23 = f16x2_to_e4m3x2(sub_f16x2(h23, e4m3x2_to_f16x2(e23)));
+    uint32_t d01 = sub_f16x2(h01, e4m3x2_to_f16x2(e01));
+    uint32_t d23 = sub_f16x2(h23, e4m3x2_to_f16x2(e23));
+    if (kLoShift > 0) {
+      d01 = mul_f16x2(d01, kScale2);
+      d23 = mul_f16x2(d23, kScale2);
+    }
+    const uint16_t l01 = f16x2_to_e4m3x2(d01);
+    const uint16_t l23 = f16x2_to_e4m3x2(d23);
     hi[w] = static_cast<uint32_t>(e01) | (static_cast<uint32_t>(e23) << 16);
     lo[w] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
   }
