@@ -85,10 +85,17 @@ __device__ __forceinline__ uint8_t* swz(uint8_t* part, int r, int cc) {
   return part + r * 128 + ((cc ^ (r & 7)) << 4);
 }
 
-template <bool kQe4m3>
+// kDup > 1: a q tile has kR = 128 / kDup packed rows, each held kDup times
+// in the MMA's M rows (row r is packed row r % kR); copy s of a row takes
+// keys [s kR, (s + 1) kR) of every tile, the rest of its P row stays zero,
+// so every softmax warp has work and each covers 1 / kDup of the keys.  The
+// copies' partial states are combined at the end.
+template <bool kQe4m3, int kDup>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
+  constexpr int kR = kRows / kDup;   // packed rows per q tile; also keys per copy
+  constexpr int kCh = kR < 64 ? kR : 64;  // S columns per TMEM round trip
   // the merge (a programmatic dependent) may launch now: its CTAs wait
   // for this grid's completion before reading what it writes
   ptx::griddep_launch_dependents();
@@ -124,7 +131,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   const int rest = blockIdx.x / a.h_k;
   const int qt = rest % n_q_tiles;
   const int w_idx = rest / n_q_tiles;
-  const int n0 = qt * kRows;
+  const int n0 = qt * kR;
 
   const int4 item = reinterpret_cast<const int4*>(a.work)[w_idx];
   const int b = item.x, t_begin = item.y, t_end = item.z, slot = item.w;
@@ -152,6 +159,12 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     ptx::mbar_init(drain, 2);
     *abort_flag = 0;
     ptx::fence_mbar_init();
+  }
+  if (kDup > 1 && warp >= 2 && warp < kMma2Warp) {
+    // a copy's P row outside its key slice stays zero for the whole kernel
+    uint4* p = reinterpret_cast<uint4*>(sm + C::kOffP);
+    for (int id = tid - 64; id < kWG * 2 * kPartBytes / 16; id += 128 * kWG) p[id] = make_uint4(0u, 0u, 0u, 0u);
+    ptx::fence_proxy_async_smem();
   }
   if (warp == 1) {
     ptx::tmem_alloc(sbase + C::kOffMisc, C::kTmemCols);
@@ -299,7 +312,8 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t tmem_s = tmem + wg * C::kWgCols + lane_off;
     const uint32_t tmem_o = tmem_s + kRows;
     uint8_t* const pbuf = sm + C::kOffP + wg * 2 * kPartBytes;
-    const int qrow = n0 + r;
+    const int qrow = n0 + r % kR;
+    const int cb = (r / kR) * kR;  // first key of this row's copy (uniform over a warp)
     const bool live = qrow < a.n_q;
     const float qd = a.qd[b * a.qd_seq + g * a.qd_head];
     const float kd = a.kd[b * a.kd_seq + g * a.kd_head];
@@ -398,20 +412,21 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         // poison keys never leak); a tile wholly below every row's limit of
         // its warp skips the selects.  64 columns per TMEM round trip.
         // (rows past n_q produce nothing: any value will do for them)
-        const bool unmasked = __all_sync(0xffffffffu, !live || key0 + kRows - 1 <= lim);
+        const bool unmasked = __all_sync(0xffffffffu, !live || key0 + cb + kR - 1 <= lim);
         float mt = -INFINITY;
   #pragma unroll
-        for (int h0 = 0; h0 < kRows; h0 += 64) {
-          uint32_t rr[64];
+        for (int h0 = 0; h0 < kR; h0 += kCh) {
+          uint32_t rr[kCh];
   #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
+          for (int c0 = 0; c0 < kCh; c0 += 16) MJ_TMEM_LD16(tmem_s + cb + h0 + c0, (rr + c0));
           ptx::tmem_ld_wait();
           if (unmasked) {
   #pragma unroll
-            for (int e = 0; e < 64; ++e) mt = fmaxf(mt, __uint_as_float(rr[e]));
+            for (int e = 0; e < kCh; ++e) mt = fmaxf(mt, __uint_as_float(rr[e]));
           } else {
   #pragma unroll
-            for (int e = 0; e < 64; ++e) mt = fmaxf(mt, (key0 + h0 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY);
+            for (int e = 0; e < kCh; ++e)
+              mt = fmaxf(mt, (key0 + cb + h0 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY);
           }
         }
         if (!live) mt = -INFINITY;  // keeps the maximum of an empty row at -inf
@@ -450,12 +465,12 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         const float bias = fmaf(-mu, c2, kLog2PScale - 8.f);
         constexpr uint32_t k256x2 = 0x5C005C00u;  // (256, 256) in half precision
   #pragma unroll
-        for (int h0 = 0; h0 < kRows; h0 += 64) {
-          uint32_t rr[64];
+        for (int h0 = 0; h0 < kR; h0 += kCh) {
+          uint32_t rr[kCh];
   #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
+          for (int c0 = 0; c0 < kCh; c0 += 16) MJ_TMEM_LD16(tmem_s + cb + h0 + c0, (rr + c0));
           ptx::tmem_ld_wait();
-          if (h0 + 64 == kRows) {
+          if (h0 + kCh == kR) {
             // S is read whole: the group's next GEMM1 may overwrite it while
             // the last half is turned into P
             ptx::tc_fence_before();
@@ -463,8 +478,8 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
             if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
           }
   #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int cc = h0 / 16 + q;  // 16-key chunk of the P row
+          for (int q = 0; q < kCh / 16; ++q) {
+            const int cc = (cb + h0) / 16 + q;  // 16-key chunk of the P row
             uint32_t hw[4], lw[4];
             uint32_t sum2 = 0u;
   #pragma unroll
@@ -475,7 +490,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                 const int e0 = q * 16 + wi * 4 + pr * 2;
                 float s0 = __uint_as_float(rr[e0]), s1 = __uint_as_float(rr[e0 + 1]);
                 if (!unmasked) {
-                  const int c = h0 + e0;
+                  const int c = cb + h0 + e0;
                   s0 = (key0 + c <= lim) ? s0 : -INFINITY;
                   s1 = (key0 + c + 1 <= lim) ? s1 : -INFINITY;
                 }
@@ -535,24 +550,78 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const float mx = fmaxf(m_run, m1);
       const float f0 = (m_run == -INFINITY) ? 0.f : fast_exp2((m_run - mx) * c2);
       const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - mx) * c2);
-      const float l = (l_run * f0 + l1 * f1) * kPScaleInv;
+      const float lraw = l_run * f0 + l1 * f1;  // row sum of x, both groups
       const bool final_out = a.n_splits[b] <= 1;
-      const float f = vd * kPScaleInv * (final_out ? a.scale_o / (l + 1e-30f) : 1.f);
       const int64_t orow = final_out ? b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + (live ? qrow : 0)) * kHeadDimDev
                                      : part_row(a, b, g, slot, live ? qrow : 0) * kHeadDimDev;
       const uint32_t o1 = tmem + C::kWgCols + kRows + lane_off;  // group 1's O, same lanes
+      // the copies of row r % kR (kDup > 1): common maximum, each copy's
+      // weight, the combined sum (through shared memory: the P buffers are
+      // idle now, every GEMM2 is done)
+      const int cp = r / kR;  // this lane's copy
+      float mrow = mx, wself = 1.f, lsum = lraw;
+      float* ep_m = reinterpret_cast<float*>(sm + C::kOffP);
+      float* ep_l = ep_m + kRows;
+      float* stage = ep_l + kRows;  // [kDup - 1][kR][16]
+      if constexpr (kDup > 1) {
+        ep_m[r] = mx;
+        ep_l[r] = lraw;
+        ptx::named_bar_sync(1, 128);  // group 0's barrier
+        const int qr = r % kR;
+        mrow = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kDup; ++s2) mrow = fmaxf(mrow, ep_m[qr + s2 * kR]);
+        lsum = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < kDup; ++s2) {
+          const float ms = ep_m[qr + s2 * kR];
+          const float ws = (ms == -INFINITY) ? 0.f : fast_exp2((ms - mrow) * c2);
+          lsum = fmaf(ws, ep_l[qr + s2 * kR], lsum);
+          if (s2 == cp) wself = ws;
+        }
+      }
+      const float l = lsum * kPScaleInv;
+      const float f = vd * kPScaleInv * (final_out ? a.scale_o / (l + 1e-30f) : 1.f);
+      const bool writer = live && cp == 0;
 #pragma unroll 1
       for (int c0 = 0; c0 < kRows; c0 += 16) {
         uint32_t ra[16], rb[16];
         MJ_TMEM_LD16(tmem_o + c0, ra);
         MJ_TMEM_LD16(o1 + c0, rb);
         ptx::tmem_ld_wait();
-        if (!live) continue;
         float v[16];
-        // select, not multiply: a group with no tile left its O stale
+        // select, not multiply: a group or copy with no key left its O stale
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          v[e] = ((f0 > 0.f ? __uint_as_float(ra[e]) * f0 : 0.f) + (f1 > 0.f ? __uint_as_float(rb[e]) * f1 : 0.f)) * f;
+          v[e] = ((f0 > 0.f ? __uint_as_float(ra[e]) * f0 : 0.f) + (f1 > 0.f ? __uint_as_float(rb[e]) * f1 : 0.f));
+        if constexpr (kDup > 1) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = wself > 0.f ? v[e] * wself : 0.f;
+          if (cp > 0) {
+            float4* st4 = reinterpret_cast<float4*>(stage + ((cp - 1) * kR + r % kR) * 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          }
+          ptx::named_bar_sync(1, 128);
+          if (cp == 0) {
+#pragma unroll
+            for (int s2 = 1; s2 < kDup; ++s2) {
+              const float4* st4 = reinterpret_cast<const float4*>(stage + ((s2 - 1) * kR + r) * 16);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float4 u = st4[e];
+                v[4 * e] += u.x;
+                v[4 * e + 1] += u.y;
+                v[4 * e + 2] += u.z;
+                v[4 * e + 3] += u.w;
+              }
+            }
+          }
+          ptx::named_bar_sync(1, 128);  // the next block reuses the stage
+        }
+        if (!writer) continue;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] *= f;
         if (final_out) {
           uint32_t pk[8];
 #pragma unroll
@@ -569,8 +638,8 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
       }
-      if (live) {
-        const float m_logit = mx * scale_l;
+      if (writer) {
+        const float m_logit = mrow * scale_l;
         if (final_out) {
           a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(l);
         } else {
@@ -588,7 +657,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   if (warp == 1) ptx::tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <bool kQe4m3>
+template <bool kQe4m3, int kDup>
 cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   using C = QmCfg<kQe4m3>;
   const int box_rows = a.page_size < kRows ? a.page_size : kRows;
@@ -596,7 +665,7 @@ cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, box_rows, 1) ||
       !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, box_rows, 1))
     return cudaErrorInvalidValue;
-  auto kern = decode_qm_kernel<kQe4m3>;
+  auto kern = decode_qm_kernel<kQe4m3, kDup>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
@@ -606,8 +675,14 @@ cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_decode_qm(const DecodeDev& a, int n_q_tiles, bool q_e4m3, cudaStream_t stream) {
-  return q_e4m3 ? launch_qm<true>(a, n_q_tiles, stream) : launch_qm<false>(a, n_q_tiles, stream);
+cudaError_t launch_decode_qm(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
+                             cudaStream_t stream) {
+  switch (rows_per_cta) {
+    case 128: return q_e4m3 ? launch_qm<true, 1>(a, n_q_tiles, stream) : launch_qm<false, 1>(a, n_q_tiles, stream);
+    case 64: return q_e4m3 ? launch_qm<true, 2>(a, n_q_tiles, stream) : launch_qm<false, 2>(a, n_q_tiles, stream);
+    case 32: return q_e4m3 ? launch_qm<true, 4>(a, n_q_tiles, stream) : launch_qm<false, 4>(a, n_q_tiles, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int qm_smem_bytes(bool q_e4m3) { return q_e4m3 ? QmCfg<true>::kBytes : QmCfg<false>::kBytes; }

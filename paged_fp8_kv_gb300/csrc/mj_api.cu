@@ -88,9 +88,13 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
     k.name = names[e4m3][k.rows_per_cta == 4 ? 0 : (k.rows_per_cta == 8 ? 1 : 2)];
   } else if (p.kernel == MJ_KERNEL_TENSOR_CORE_QROWS || (p.kernel == MJ_KERNEL_AUTO && n_q > kQRowsFrom)) {
     k.kind = KernelKind::kTensorCoreQRows;
-    k.rows_per_cta = 128;
+    // up to 32 or 64 packed rows: each row held four or two times in the
+    // 128 MMA rows, every copy taking that share of a tile's keys
+    k.rows_per_cta = n_q <= 32 ? 32 : (n_q <= 64 ? 64 : 128);
     smem = qm_smem_bytes(e4m3);
-    k.name = e4m3 ? "qm_e4m3" : "qm_bf16";
+    static const char* names[2][3] = {{"qm_r32_bf16", "qm_r64_bf16", "qm_bf16"},
+                                      {"qm_r32_e4m3", "qm_r64_e4m3", "qm_e4m3"}};
+    k.name = names[e4m3][k.rows_per_cta == 32 ? 0 : (k.rows_per_cta == 64 ? 1 : 2)];
   } else if ((p.kernel == MJ_KERNEL_TENSOR_CORE_GROUPED ||
               (p.kernel == MJ_KERNEL_AUTO && n_q > kPairFrom && n_q <= kQRowsFrom && p.h_k % 2 == 0)) &&
              tcg_supported(p.h_k, n_q, &g, &rh)) {
@@ -243,7 +247,7 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   cudaError_t e = cudaSuccess;
   if (ev[0] && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return MJ_ERR_CUDA;
   if (kc.kind == KernelKind::kTensorCoreQRows) {
-    e = launch_decode_qm(d, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
+    e = launch_decode_qm(d, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
   } else if (kc.kind == KernelKind::kTensorCoreGrouped) {
     const int sms = device_sm_count();
     if (sms < 1) return MJ_ERR_CUDA;

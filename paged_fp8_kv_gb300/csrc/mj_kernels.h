@@ -32,7 +32,10 @@ int tcg_smem_bytes(int heads_per_cta, int rows_per_head, bool q_e4m3);
 
 // Query-rows-on-M tensor-core decode: 128 packed rows of one kv head per
 // CTA, one CTA per SM.
-cudaError_t launch_decode_qm(const DecodeDev& a, int n_q_tiles, bool q_e4m3, cudaStream_t stream);
+// rows_per_cta 128, 64 or 32: each packed row held 128 / rows_per_cta times,
+// every copy taking that share of a tile's keys.
+cudaError_t launch_decode_qm(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
+                             cudaStream_t stream);
 int qm_smem_bytes(bool q_e4m3);
 
 // TMA descriptor of a paged e4m3 pool seen as (d bytes, rows in page, kv

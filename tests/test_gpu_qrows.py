@@ -58,7 +58,7 @@ def test_sweep_small(h_r, q_len):
     check(w)
 
 
-@pytest.mark.parametrize("h_r,q_len", [(32, 4), (32, 16)])
+@pytest.mark.parametrize("h_r,q_len", [(16, 4), (32, 4), (32, 16)])
 def test_sweep_full_sampled(h_r, q_len):
     w = syn.config(5, h_r=h_r, q_len=q_len)
     s = run(w, kernel=0)  # the automatic choice
@@ -129,3 +129,30 @@ def test_determinism_and_graph_replay():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o0, s.o_vllm) and torch.equal(l0, s.lse)
+
+
+# ---- rows held two or four times (64 or 32 packed rows per q tile): every
+# copy takes a share of each tile's keys, the copies are combined at the end
+
+
+@pytest.mark.parametrize("q_len,h_r,causal", [(3, 8, True), (1, 24, False), (4, 16, True), (2, 5, False)])
+@pytest.mark.parametrize("page_size", [16, 128])
+def test_row_copies_lengths_and_masks(q_len, h_r, causal, page_size):
+    lens = [0, 1, 2, 5, 31, 32, 33, 127, 128, 129, 300, 1100]
+    w = syn.make_workload("copies", lens, q_len, 2, h_r, page_size, seed=61 + q_len * h_r, causal=causal, max_splits=4)
+    s, _ = check(w, force_splits=2)
+    n_q = q_len * h_r
+    assert s.kernel == ("qm_r32_bf16" if n_q <= 32 else "qm_r64_bf16")
+    assert np.all(np.isneginf(s.lse_host()[0]))  # L = 0
+    assert np.all(s.o_host()[0] == 0.0)
+
+
+def test_row_copies_e4m3_q_and_determinism():
+    w = syn.make_workload("copies_e4m3", [400, 2000, 3100], 2, 2, 16, 64, seed=67, q_is_e4m3=True)
+    a, _ = check(w)
+    assert a.kernel == "qm_r32_e4m3"
+    o0, l0 = a.o_vllm.clone(), a.lse.clone()
+    for _ in range(3):
+        a.step()
+    torch.cuda.synchronize()
+    assert torch.equal(o0, a.o_vllm) and torch.equal(l0, a.lse)
