@@ -91,15 +91,19 @@ typedef struct {
  *                          from TMA into the MMA, Q and P as hi+lo e4m3;
  *                          one CTA per kv head
  *   MJ_KERNEL_TENSOR_CORE_GROUPED
- *                          the same arithmetic with one CTA per group of 4
- *                          or 8 kv heads, whose rows of each page it reads
- *                          together; needs h_k a multiple of 4 and
- *                          q_len*h_r <= 8 (MJ_ERR_UNSUPPORTED otherwise)
+ *                          the same arithmetic, persistent, with one CTA per
+ *                          group of 8, 4 or 2 kv heads, whose rows of each
+ *                          page it reads together: 8 heads for
+ *                          q_len*h_r <= 4 (h_k a multiple of 8), 4 for <= 8
+ *                          (h_k a multiple of 4), 2 for <= 32 (h_k even);
+ *                          MJ_ERR_UNSUPPORTED otherwise
  *   MJ_KERNEL_TENSOR_CORE_QROWS
- *                          tcgen05 kernel with 128 packed query rows on the
- *                          MMA's M and 128 keys on N: one read of the KV per
- *                          128 rows; MJ_KERNEL_AUTO takes it for
- *                          q_len*h_r > 32 */
+ *                          tcgen05 kernel with 128 query rows on the MMA's M
+ *                          and 128 keys on N: one read of the KV per q tile
+ *                          of 128 packed rows, or of 64 / 32 packed rows
+ *                          each held two / four times with every copy taking
+ *                          that share of the keys; MJ_KERNEL_AUTO takes it
+ *                          for q_len*h_r > 16 */
 typedef enum {
   MJ_KERNEL_AUTO = 0,
   MJ_KERNEL_CUDA_CORE = 1,

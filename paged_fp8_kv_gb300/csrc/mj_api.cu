@@ -62,13 +62,11 @@ constexpr int kSmemReservedPerCta = 1024;
 // output epilogue, a few microseconds).
 constexpr int kGroupedUnitsPerSm = 6;
 constexpr int kPairUnitsPerSm = 3;
-// More packed rows than this (up to 32) and an even number of kv heads go
-// to the 2-head x 32-row grouped kernel (measured on the spec-verify
-// workload: 32 rows 265 us vs 327 us per-head; 16 rows 307 us vs 238 us).
-constexpr int kPairFrom = 16;
-// More packed rows than this go to the query-rows kernel (measured: it wins
-// from 40 rows on; at 32 the swap-AB kernel is faster).
-constexpr int kQRowsFrom = 32;
+// More packed rows than this go to the query-rows kernel (measured with its
+// rows held several times: 32 rows 115 us vs 121 us swap-AB on the sweep,
+// 261 us vs 260 us (2-head grouped) / 278 us on the spec-verify workload,
+// with no merge; at 16 rows the swap-AB kernel is as fast).
+constexpr int kQRowsFrom = 16;
 
 }  // namespace
 
@@ -95,9 +93,7 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
     static const char* names[2][3] = {{"qm_r32_bf16", "qm_r64_bf16", "qm_bf16"},
                                       {"qm_r32_e4m3", "qm_r64_e4m3", "qm_e4m3"}};
     k.name = names[e4m3][k.rows_per_cta == 32 ? 0 : (k.rows_per_cta == 64 ? 1 : 2)];
-  } else if ((p.kernel == MJ_KERNEL_TENSOR_CORE_GROUPED ||
-              (p.kernel == MJ_KERNEL_AUTO && n_q > kPairFrom && n_q <= kQRowsFrom && p.h_k % 2 == 0)) &&
-             tcg_supported(p.h_k, n_q, &g, &rh)) {
+  } else if (p.kernel == MJ_KERNEL_TENSOR_CORE_GROUPED && tcg_supported(p.h_k, n_q, &g, &rh)) {
     k.kind = KernelKind::kTensorCoreGrouped;
     k.rows_per_cta = rh;
     k.heads_per_cta = g;

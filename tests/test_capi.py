@@ -215,15 +215,17 @@ def test_grouped_kernel_choice_and_plan():
 
 
 def test_query_rows_kernel_choice():
-    # more than 32 packed rows: the query-rows kernel, 128 rows per q tile
+    # more than 16 packed rows: the query-rows kernel (32, 64 or 128 rows per q tile)
     assert mj.kernel_name(_params(2, h_k=1, q_len=2, h_r=32)) == "qm_r64_bf16"
     assert mj.kernel_name(_params(2, h_k=8, q_len=5, h_r=8)) == "qm_r64_bf16"
     assert mj.kernel_name(_params(2, h_k=1, q_len=4, h_r=32)) == "qm_bf16"
-    assert mj.kernel_name(_params(2, h_k=1, q_len=1, h_r=32)) == "tc_r32_bf16"
-    # 17 to 32 rows with an even number of kv heads: 2 heads x 32 rows per CTA
-    assert mj.kernel_name(_params(2, h_k=8, q_len=4, h_r=8)) == "tcg_g2r32_bf16"
+    # 17 to 32 rows: 32 rows per q tile (each held four times)
+    assert mj.kernel_name(_params(2, h_k=1, q_len=1, h_r=32)) == "qm_r32_bf16"
+    assert mj.kernel_name(_params(2, h_k=8, q_len=4, h_r=8)) == "qm_r32_bf16"
+    assert mj.kernel_name(_params(2, h_k=3, q_len=3, h_r=6)) == "qm_r32_bf16"
+    # up to 16 rows: the swap-AB kernel
     assert mj.kernel_name(_params(2, h_k=8, q_len=2, h_r=8)) == "tc_r16_bf16"
-    assert mj.kernel_name(_params(2, h_k=3, q_len=4, h_r=8)) == "tc_r32_bf16"
+    assert mj.kernel_name(_params(2, h_k=1, q_len=1, h_r=16)) == "tc_r16_bf16"
     qr = mj.MJ_KERNEL_TENSOR_CORE_QROWS
     assert mj.kernel_name(_params(2, h_k=1, h_r=16, kernel=qr, q_dtype=1)) == "qm_r32_e4m3"
     assert mj.kernel_name(_params(2, h_k=1, q_len=8, h_r=16, kernel=qr, q_dtype=1)) == "qm_e4m3"
