@@ -199,6 +199,23 @@ def traffic_record(kernel: str, workload_name: str):
 # --------------------------------------------------------------- GPU arm
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of the ranks' values: the step time reported for N
+    replicas is the slowest one's (every rank calls this)."""
+    if world <= 1:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, step_bytes: int, step_ms: float) -> float:
+    """Whole-job throughput: every replica moves step_bytes per step."""
+    return world * step_bytes / (step_ms * 1e-3) / 1e9
+
+
 def run_mj(args, rank, world, local_rank):
     import torch
 
@@ -260,10 +277,7 @@ def run_mj(args, rank, world, local_rank):
     step_ms = float(np.mean([sev[i][0].elapsed_time(sev[i][1]) for i in plain]))
     t_dec = float(np.mean(decode_ms))
 
-    if world > 1:
-        tt = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = max_over_ranks(step_ms, world, dev)
 
     launches = s.launches_per_step() * args.steps
     e2e = None if args.no_e2e else e2e_measure(args, s, w, step_bytes, dev)
@@ -427,7 +441,7 @@ def main():
             "kind": "oracle",
             "sample": f"{units} (seq, kv-head) units of the same workload ({units / (w.num_seqs * w.h_k):.1f} passes over its {w.num_seqs * w.h_k} units, random order), {secs:.1f} s of fp64 oracle work; GB/s of KV rows read",
         }
-    value = world * r["step_bytes"] / (r["step_ms"] * 1e-3) / 1e9
+    value = whole_job_gbs(world, r["step_bytes"], r["step_ms"])
     if rank == 0:
         line = {
             "metric": METRIC,
