@@ -57,7 +57,11 @@ constexpr int kBarAll = 3;                   // named barrier of both warpgroups
 
 template <bool kQe4m3>
 struct QmCfg {
-  static constexpr int kStagesK = 3;
+  // K ring: measured the bound at three stages (a stage comes back one TMA
+  // round trip after its GEMM1, and the period was that over three); the
+  // shared memory left beside Q and the P buffers takes one more (two with
+  // e4m3 Q, which has no lo part)
+  static constexpr int kStagesK = kQe4m3 ? 5 : 4;
   static constexpr int kStagesV = 4;
   static constexpr int kQParts = kQe4m3 ? 1 : 2;
   static constexpr int kTmemCols = 512;  // per warpgroup: S (128), O (128)
@@ -414,12 +418,21 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         // (rows past n_q produce nothing: any value will do for them)
         const bool unmasked = __all_sync(0xffffffffu, !live || key0 + cb + kR - 1 <= lim);
         float mt = -INFINITY;
+        // kDup > 1: the row's slice of S (kR <= 64 columns) stays in these
+        // registers for pass 2, and S goes back to GEMM1 right after this read
+        uint32_t sv[kDup > 1 ? kR : 1];
   #pragma unroll
         for (int h0 = 0; h0 < kR; h0 += kCh) {
-          uint32_t rr[kCh];
+          uint32_t rl[kDup > 1 ? 1 : kCh];
+          uint32_t* rr = kDup > 1 ? sv : rl;
   #pragma unroll
           for (int c0 = 0; c0 < kCh; c0 += 16) MJ_TMEM_LD16(tmem_s + cb + h0 + c0, (rr + c0));
           ptx::tmem_ld_wait();
+          if (kDup > 1) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
+          }
           if (unmasked) {
   #pragma unroll
             for (int e = 0; e < kCh; ++e) mt = fmaxf(mt, __uint_as_float(rr[e]));
@@ -442,16 +455,18 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         // access is warp-wide, so a warp corrects when any of its rows moved
         if (t > 0 && __any_sync(0xffffffffu, moved)) {
           ptx::tc_fence_after();
+          // (16 columns per round trip when the S slice is held in registers)
+          constexpr int kOc = kDup > 1 ? 16 : 64;
   #pragma unroll
-          for (int h0 = 0; h0 < kRows; h0 += 64) {
-            uint32_t rr[64];
+          for (int h0 = 0; h0 < kRows; h0 += kOc) {
+            uint32_t rr[kOc];
   #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_LD16(tmem_o + h0 + c0, (rr + c0));
+            for (int c0 = 0; c0 < kOc; c0 += 16) MJ_TMEM_LD16(tmem_o + h0 + c0, (rr + c0));
             ptx::tmem_ld_wait();
   #pragma unroll
-            for (int e = 0; e < 64; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
+            for (int e = 0; e < kOc; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
   #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16) MJ_TMEM_ST16(tmem_o + h0 + c0, (rr + c0));
+            for (int c0 = 0; c0 < kOc; c0 += 16) MJ_TMEM_ST16(tmem_o + h0 + c0, (rr + c0));
           }
           ptx::tmem_st_wait();
         }
@@ -466,11 +481,14 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         constexpr uint32_t k256x2 = 0x5C005C00u;  // (256, 256) in half precision
   #pragma unroll
         for (int h0 = 0; h0 < kR; h0 += kCh) {
-          uint32_t rr[kCh];
+          uint32_t rl[kDup > 1 ? 1 : kCh];
+          uint32_t* rr = kDup > 1 ? sv : rl;
+          if (kDup == 1) {
   #pragma unroll
-          for (int c0 = 0; c0 < kCh; c0 += 16) MJ_TMEM_LD16(tmem_s + cb + h0 + c0, (rr + c0));
-          ptx::tmem_ld_wait();
-          if (h0 + kCh == kR) {
+            for (int c0 = 0; c0 < kCh; c0 += 16) MJ_TMEM_LD16(tmem_s + cb + h0 + c0, (rr + c0));
+            ptx::tmem_ld_wait();
+          }
+          if (kDup == 1 && h0 + kCh == kR) {
             // S is read whole: the group's next GEMM1 may overwrite it while
             // the last half is turned into P
             ptx::tc_fence_before();
