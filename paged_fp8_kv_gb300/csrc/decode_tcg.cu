@@ -78,7 +78,8 @@ struct GCfg {
   static constexpr int GR = G * RH;        // query columns of the CTA
   // G = 2: a head's 64 keys span two warps (a pair), which exchange their
   // column maxima and row sums through shared memory
-  static constexpr bool kPair = KR == 64;
+  static constexpr bool kPair = KR >= 64;          // a head's keys span kWph warps
+  static constexpr int kWph = kPair ? KR / 32 : 1;  // warps per head (2 or 4)
   static constexpr int HPW = kPair ? 1 : 32 / KR;  // heads per warp
   static constexpr int W = HPW * RH;       // S columns a warp reads
   static constexpr int kN1 = kQe4m3 ? (GR < 16 ? 16 : GR) : 2 * GR;
@@ -99,7 +100,7 @@ struct GCfg {
   static constexpr int kLoShift = 4;
   static constexpr float kLoInv = 1.f / (1 << kLoShift);
   static constexpr int kStagesK = kPair ? 4 : 5;
-  static constexpr int kStagesV = kPair ? 5 : 7;
+  static constexpr int kStagesV = kPair ? (G == 1 ? 6 : 5) : 7;
   static constexpr int kQBytes = kN1 * 128;
   // P (GEMM2's B operand, MN-major, no swizzle: [16-column groups][K rows][16 B]).
   //   G >= 4: one block-diagonal buffer per warpgroup, [kN2/16][128 rows],
@@ -135,7 +136,7 @@ struct GCfg {
   static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 9 * kWG + 2 + 2 + 1 + 1 + 2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 32 + 1024;
-  static_assert(KR >= 16 && KR <= 64, "a head's rows sit within one warp or a warp pair");
+  static_assert(KR >= 16 && KR <= 128, "a head's rows sit within one warp, two or four");
   static_assert(kPair ? RH == 32 : (W == 8 || W == 16), "TMEM load width / one column per lane");
   static_assert(kN1 % 16 == 0 && kN2 % 16 == 0 && kN1 <= 256 && kN2 <= 256, "MMA N");
   static_assert(kTmemCols <= 512, "TMEM");
@@ -725,8 +726,12 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         // neither the column reduction nor an O correction; the result does
         // not depend on m.  Each thread keeps its key's share of every row
         // sum, reduced once per unit.
-        const int pq = quarter ^ 1;
-        const int bar_pair = 4 + 2 * wg + h;  // named barrier of the pair's 64 threads
+        // this head's warps: lane quarters wq0 .. wq0 + kWph - 1, with their
+        // own named barrier (the warpgroup's when a head fills it)
+        const int wq0 = (quarter / C::kWph) * C::kWph;
+        const bool head_lead = quarter == wq0;  // stores the head's stats
+        const int bar_head = C::kWph == 4 ? bar_wg : 4 + 2 * wg + h;
+        constexpr int kHeadThreads = 32 * C::kWph;
         float* const red = red_all + wg * C::kRedWg;    // [4 warps][32] partial values
         float* const thr = red + 128 + quarter * 32;   // this warp's copy: update thresholds (raw)
         float* const bias = red + 256 + quarter * 32;  // ... and exponent offsets (log2 units)
@@ -799,8 +804,10 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
             for (int nn = 0; nn < RH; ++nn) mx[nn] = sc[nn];
             warp_reduce_scatter<RH, true>(mx, lane);
             red[quarter * 32 + lane] = mx[0];
-            ptx::named_bar_sync(bar_pair, 64);
-            const float tmax = fmaxf(mx[0], red[pq * 32 + lane]);
+            ptx::named_bar_sync(bar_head, kHeadThreads);
+            float tmax = mx[0];
+#pragma unroll
+            for (int q2 = 0; q2 < C::kWph; ++q2) tmax = fmaxf(tmax, red[(wq0 + q2) * 32 + lane]);
             const bool moved_c = tmax > thr[lane];
             const float mn = moved_c ? tmax : m_lane;
             const float mu = (mn == -INFINITY) ? 0.f : mn;
@@ -808,7 +815,7 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
             const float corr_c = moved_c ? fast_exp2((m_lane - mu) * c2) : 1.f;
             m_lane = mn;
             float* corr_b = corr_wg + (t & 1) * GR;
-            if ((quarter & 1) == 0) corr_b[h * RH + lane] = corr_c;
+            if (head_lead) corr_b[h * RH + lane] = corr_c;
             // the partner has read red; corr_b is complete
             any_moved = ptx::named_bar_red_or(bar_wg, 128, moved_c);
             const float tn = (mn == -INFINITY) ? -INFINITY : mn + head_c;
@@ -907,10 +914,13 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         // row sums over the pair's 64 keys; the even warp stores the head's stats
         warp_reduce_scatter<RH, false>(l_thr, lane);
         red[quarter * 32 + lane] = l_thr[0];
-        ptx::named_bar_sync(bar_pair, 64);
-        if ((quarter & 1) == 0) {
+        ptx::named_bar_sync(bar_head, kHeadThreads);
+        if (head_lead) {
+          float lsum = 0.f;  // in warp order
+#pragma unroll
+          for (int q2 = 0; q2 < C::kWph; ++q2) lsum += red[(wq0 + q2) * 32 + lane];
           my_m[h * RH + lane] = m_lane;
-          my_l[h * RH + lane] = (l_thr[0] + red[pq * 32 + lane]) * C::kPScaleInv;
+          my_l[h * RH + lane] = lsum * C::kPScaleInv;
         }
       } else {
       // deferred row sums (of 448 p 2^-kTau); reference column maxima (raw)
@@ -1250,7 +1260,8 @@ cudaError_t launch_tcg(const DecodeDev& a, int n_q_tiles, int* sched, int sm_cou
 
 bool tcg_supported(int h_k, int n_q, int* heads_per_cta, int* rows_per_head) {
   // G heads x RH rows per head: G = 8 x 4 and G = 4 x 8 (a head's keys
-  // within one warp), G = 2 x 32 (a head's keys in a warp pair)
+  // within one warp), G = 2 x 32 (a head's keys in a warp pair), G = 1 x 32
+  // (one head's keys over the four warps of a group)
   int g = 0, rh = 0;
   if (n_q <= 4 && h_k % 8 == 0) {
     g = 8;
@@ -1260,6 +1271,9 @@ bool tcg_supported(int h_k, int n_q, int* heads_per_cta, int* rows_per_head) {
     rh = 8;
   } else if (n_q <= 32 && h_k % 2 == 0) {
     g = 2;
+    rh = 32;
+  } else if (n_q <= 32) {
+    g = 1;
     rh = 32;
   }
   if (g == 0) return false;
@@ -1279,6 +1293,9 @@ cudaError_t launch_decode_tcg(const DecodeDev& a, int heads_per_cta, int rows_pe
   if (heads_per_cta == 2 && rows_per_head == 32)
     return q_e4m3 ? launch_tcg<2, 32, true>(a, n_q_tiles, sched, sm_count, stream)
                   : launch_tcg<2, 32, false>(a, n_q_tiles, sched, sm_count, stream);
+  if (heads_per_cta == 1 && rows_per_head == 32)
+    return q_e4m3 ? launch_tcg<1, 32, true>(a, n_q_tiles, sched, sm_count, stream)
+                  : launch_tcg<1, 32, false>(a, n_q_tiles, sched, sm_count, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -1287,6 +1304,8 @@ int tcg_smem_bytes(int heads_per_cta, int rows_per_head, bool q_e4m3) {
   if (heads_per_cta == 4 && rows_per_head == 8) return q_e4m3 ? GCfg<4, 8, true>::kBytes : GCfg<4, 8, false>::kBytes;
   if (heads_per_cta == 2 && rows_per_head == 32)
     return q_e4m3 ? GCfg<2, 32, true>::kBytes : GCfg<2, 32, false>::kBytes;
+  if (heads_per_cta == 1 && rows_per_head == 32)
+    return q_e4m3 ? GCfg<1, 32, true>::kBytes : GCfg<1, 32, false>::kBytes;
   return 0;
 }
 

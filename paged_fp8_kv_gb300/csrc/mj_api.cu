@@ -59,9 +59,11 @@ constexpr int kSmemReservedPerCta = 1024;
 // Units per SM the plan cuts for the head-grouped kernel (measured, 2 to 12
 // per SM): six for 8 heads x 4 rows (GQA decode), three for 2 heads x 32
 // rows (spec verify: each unit boundary stalls the CTA's softmax for its
-// output epilogue, a few microseconds).
+// output epilogue, a few microseconds), two for 1 head x 32 rows (sweep with
+// h_k = 1: 118 us at two, 122 at three, 128 at four).
 constexpr int kGroupedUnitsPerSm = 6;
 constexpr int kPairUnitsPerSm = 3;
+constexpr int kOneHeadUnitsPerSm = 2;
 // More packed rows than this go to the query-rows kernel (measured with its
 // rows held several times: 32 rows 115 us vs 121 us swap-AB on the sweep,
 // 261 us vs 260 us (2-head grouped) / 278 us on the spec-verify workload,
@@ -98,9 +100,9 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
     k.rows_per_cta = rh;
     k.heads_per_cta = g;
     smem = tcg_smem_bytes(g, rh, e4m3);
-    static const char* names[2][3] = {{"tcg_g8r4_bf16", "tcg_g4r8_bf16", "tcg_g2r32_bf16"},
-                                      {"tcg_g8r4_e4m3", "tcg_g4r8_e4m3", "tcg_g2r32_e4m3"}};
-    k.name = names[e4m3][g == 8 ? 0 : (g == 4 ? 1 : 2)];
+    static const char* names[2][4] = {{"tcg_g8r4_bf16", "tcg_g4r8_bf16", "tcg_g2r32_bf16", "tcg_g1r32_bf16"},
+                                      {"tcg_g8r4_e4m3", "tcg_g4r8_e4m3", "tcg_g2r32_e4m3", "tcg_g1r32_e4m3"}};
+    k.name = names[e4m3][g == 8 ? 0 : (g == 4 ? 1 : (g == 2 ? 2 : 3))];
   } else {
     k.kind = KernelKind::kTensorCore;
     k.rows_per_cta = n_q <= 8 ? 8 : (n_q <= 16 ? 16 : (n_q <= 32 ? 32 : 64));
@@ -120,7 +122,8 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
   k.ctas_per_sm = (per_sm < 1 ? 1 : per_sm) * k.heads_per_cta;
   // The persistent kernel takes units from a queue: the plan cuts about six
   // units per SM, so that the greedy queue (longest first) ends balanced.
-  if (k.kind == KernelKind::kTensorCoreGrouped) k.ctas_per_sm *= g == 2 ? kPairUnitsPerSm : kGroupedUnitsPerSm;
+  if (k.kind == KernelKind::kTensorCoreGrouped)
+    k.ctas_per_sm *= g == 1 ? kOneHeadUnitsPerSm : (g == 2 ? kPairUnitsPerSm : kGroupedUnitsPerSm);
   return k;
 }
 

@@ -199,8 +199,10 @@ def test_grouped_kernel_choice_and_plan():
     assert mj.kernel_name(_params(2, h_k=8, h_r=16, kernel=grouped)) == "tcg_g2r32_bf16"
     assert mj.kernel_name(_params(2, h_k=6, h_r=4, kernel=grouped)) == "tcg_g2r32_bf16"
     assert mj.kernel_name(_params(2, h_k=8, q_len=4, h_r=8, kernel=grouped, q_dtype=1)) == "tcg_g2r32_e4m3"
-    # an odd number of kv heads, or more than 32 rows per head: refused
-    for h_k, h_r in [(3, 4), (1, 16), (8, 40)]:
+    assert mj.kernel_name(_params(2, h_k=3, h_r=4, kernel=grouped)) == "tcg_g1r32_bf16"
+    assert mj.kernel_name(_params(2, h_k=1, h_r=16, kernel=grouped)) == "tcg_g1r32_bf16"
+    # more than 32 rows per head: refused
+    for h_k, h_r in [(8, 40), (1, 33)]:
         p = _params(2, h_k=h_k, h_r=h_r, kernel=grouped)
         with pytest.raises(mj.MjError):
             mj.kernel_name(p)

@@ -207,3 +207,38 @@ def test_pair_determinism_and_layouts():
     assert torch.equal(o0, a.o_vllm) and torch.equal(l0, a.lse)
     b = run(w, kv_layout="hnd")
     assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
+
+
+# ---- 1 head x 32 rows: a head's 128 keys of a step over the four warps of
+# a group (an odd number of kv heads, or h_k = 1)
+
+
+@pytest.mark.parametrize("page_size", [16, 64, 128])
+@pytest.mark.parametrize("h_k,h_r,q_len", [(1, 32, 1), (1, 16, 2), (3, 8, 3)])
+def test_one_head_instance(page_size, h_k, h_r, q_len):
+    lens = [1, 63, 127, 128, 129, 250, 511, 700, 1300]
+    w = syn.make_workload("grouped_one", lens, q_len, h_k, h_r, page_size, seed=271 + page_size, max_splits=4)
+    s, _ = check(w, force_splits=2)
+    assert s.kernel == "tcg_g1r32_bf16"
+
+
+@pytest.mark.parametrize("q_is_e4m3", [False, True])
+@pytest.mark.parametrize("causal", [True, False])
+def test_one_head_q_dtype_masks_and_edges(q_is_e4m3, causal):
+    lens = [0, 1, 2, 3, 16, 127, 128, 129, 300, 2100]
+    w = syn.make_workload("edge_one", lens, 2, 1, 16, 32, seed=283, causal=causal, q_is_e4m3=q_is_e4m3, max_splits=8)
+    s, _ = check(w)
+    assert s.kernel.startswith("tcg_g1r32")
+    assert np.all(np.isneginf(s.lse_host()[0]))  # L = 0
+    assert np.all(s.o_host()[0] == 0.0)
+
+
+def test_one_head_sweep_full_sampled_and_determinism():
+    w = syn.config(5, h_r=32, q_len=1)
+    s = run(w)
+    compare(w, s.o_host(), s.lse_host(), units=[(0, 0), (64, 0), (127, 0)])
+    o0, l0 = s.o_vllm.clone(), s.lse.clone()
+    for _ in range(2):
+        s.step()
+    torch.cuda.synchronize()
+    assert torch.equal(o0, s.o_vllm) and torch.equal(l0, s.lse)
