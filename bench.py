@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--l2_prefetch", type=int, default=0, help="0 default, -1 off, 1..8 tiles ahead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time steps as plain launches, not CUDA-graph replays")
     return ap.parse_args()
 
 
@@ -245,6 +246,20 @@ def run_mj(args, rank, world, local_rank):
         flush.fill_(1)
         s.step()
     torch.cuda.synchronize()
+    # A step is timed as one replay of a CUDA graph holding (pack, decode,
+    # merge, unpack); the library makes no host sync, so it captures as is.
+    graph = None
+    if not args.eager:
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            s.step(stream=cs)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            graph.replay()
+        torch.cuda.synchronize()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
@@ -256,14 +271,16 @@ def run_mj(args, rank, world, local_rank):
     # Even steps carry events between the decode and the merge launch (the
     # per-kernel times of the roofline); an event there also serialises the
     # merge behind the decode grid, so the step time comes from the odd
-    # steps, which run exactly as a caller's would (the merge a programmatic
-    # dependent of the decode grid).
+    # steps, which run exactly as a caller's would (graph replays, the merge
+    # a programmatic dependent of the decode grid).
     with ClockSampler(local_rank) as clk:
         for i in range(args.steps):
             flush.fill_(i & 0xFF)  # L2 flush, outside the step's events
             sev[i][0].record()
             if i % 2 == 0 or args.steps == 1:
                 s.step(timing_events=evs[i])
+            elif graph is not None:
+                graph.replay()
             else:
                 s.step()
             sev[i][1].record()
@@ -471,6 +488,7 @@ def main():
                     "sm_count": s.plan.opts.sm_count,
                 },
                 "l2": "flushed before every step (512 MiB write outside the step events); KV also exceeds L2",
+                "step_timing": "eager launches" if args.eager else "CUDA-graph replay of the step (pack, decode, merge, unpack)",
                 "parallelism": f"replicas x{world}",
                 "bytes_per_step": r["step_bytes"],
                 "plan_us": round(r["plan_us"], 2),
