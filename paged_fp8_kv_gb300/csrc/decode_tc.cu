@@ -123,11 +123,15 @@ template <int R, bool kQe4m3>
 struct TcCfg {
   static constexpr int kN1 = kQe4m3 ? (R < 16 ? 16 : R) : 2 * R;
   static constexpr int kN2 = 2 * R;
-  static constexpr int kStages = R <= 32 ? 2 : 5;
-  static constexpr int kMinBlocks = R <= 16 ? 3 : (R <= 32 ? 2 : 1);
+  // 16 rows of e4m3 Q (the fully-fp8 path): three stages at two CTAs per
+  // SM instead of two at three; short split chunks then have most of their
+  // tiles in flight at once
+  static constexpr bool kDeep16 = kQe4m3 && R == 16;
+  static constexpr int kStages = kDeep16 ? 3 : (R <= 32 ? 2 : 5);
+  static constexpr int kMinBlocks = kDeep16 ? 2 : (R <= 16 ? 3 : (R <= 32 ? 2 : 1));
   // two P buffers let the softmax of tile i write while GEMM2(i-1) still
   // reads; R = 16 at 3 CTAs/SM has no room for the second one
-  static constexpr int kPBufs = R == 16 ? 1 : 2;
+  static constexpr int kPBufs = R == 16 && !kDeep16 ? 1 : 2;
   // softmax warps: four cover the 128 TMEM lanes; with R = 32 a second four
   // take the other half of the columns (two warps per lane quarter)
   static constexpr int kSmWarps = R >= 32 ? 8 : 4;
@@ -226,6 +230,15 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   const int b = item.x, t_begin = item.y, t_end = item.z, slot = item.w;
   if (t_end <= t_begin) return;  // padding item: uniform exit before any setup
   const int T = t_end - t_begin;
+  // The producer's lane j reads page j of the first tile now, alongside the
+  // sequence length (which only masks the pages past it): the first copies
+  // then wait for one memory round trip after the work item, not two.
+  const int PS = a.page_size;
+  const int ppt = kTileKV / PS;  // pages per tile: 1, 2, 4 or 8
+  const int64_t bt_row = static_cast<int64_t>(b) * a.max_blocks;
+  int first_page_raw = 0;
+  if (warp == 0 && lane < ppt && t_begin * ppt + lane < a.max_blocks)
+    first_page_raw = a.block_table[bt_row + t_begin * ppt + lane];
   const int L = a.seq_lens[b];
 
   if (tid == 0) {
@@ -264,9 +277,6 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     // Lane j handles page j of each tile: the block-table lookups of a tile
     // run in parallel, and the next tile's lookups are in flight while this
     // tile's copies are issued.
-    const int PS = a.page_size;
-    const int ppt = kTileKV / PS;  // pages per tile: 1, 2, 4 or 8
-    const int64_t bt_row = static_cast<int64_t>(b) * a.max_blocks;
     int valid_pages = (L + PS - 1) / PS;
     valid_pages = valid_pages < a.max_blocks ? valid_pages : a.max_blocks;
     auto lookup = [&](int tile) -> int {
@@ -278,7 +288,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::prefetch_tmap(&tmap_k);
       ptx::prefetch_tmap(&tmap_v);
     }
-    int next_page = lookup(t_begin);
+    int next_page = (lane < ppt && t_begin * ppt + lane < valid_pages) ? first_page_raw : a.num_pages;
     int issued = 0;
     for (int i = 0; i < T; ++i) {
       const int st = i % C::kStages;

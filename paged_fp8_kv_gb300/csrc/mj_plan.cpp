@@ -42,15 +42,22 @@ namespace {
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Plan model constants (GB300, measured): K+V bytes of one 128-row tile of
-// one kv head; sustained KV bandwidth; time per tile of a CTA streaming
-// alone; the per-CTA start cost in tiles; the merge kernel; the margin a
-// finer plan must win by.
+// one kv head; sustained KV bandwidth of the per-head kernels; time per tile
+// of one CTA while the SM's other slots stream too (one SM streams a tile
+// in about 0.65 us, shared by its co-resident CTAs; the query-rows kernel
+// owns its SM and takes 0.9 us a tile); the per-CTA start cost in tiles; the
+// merge kernel's share of a step (launched as a programmatic dependent);
+// the margin a finer plan must win by.
 constexpr double kTilePairBytes = 128.0 * 256.0;
-constexpr double kPlanBandwidth = 5.0e6;  // bytes per microsecond
-constexpr double kPlanTileUs = 1.2;
+constexpr double kPlanBandwidth = 5.45e6;  // bytes per microsecond
+constexpr double kPlanSmTileUs = 0.65;
+constexpr double kPlanQRowsTileUs = 0.9;
 constexpr int64_t kPlanCtaOverheadTiles = 1;
-constexpr double kPlanMergeUs = 8.0;
+constexpr double kPlanMergeUs = 2.5;
 constexpr double kPlanMargin = 0.95;
+// Finer plans tried: the co-resident CTAs times these thirds (3, 5, 8 and
+// 12 slots per SM for three co-resident CTAs).
+constexpr int kPlanThirds[] = {3, 5, 8, 12};
 constexpr int64_t kPlanModelMaxUnits = 1 << 16;
 
 struct Item {
@@ -121,13 +128,16 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
     return lo;
   };
 
-  // Library default for the per-head kernels: the plan for 1, 2 or 4 times
-  // the co-resident CTAs, whichever a simple model says ends first.  One
-  // wave of the occupancy-pinned plan leaves SMs idle behind the longest
-  // chunk when a few long sequences dominate; a finer plan balances (the
-  // hardware hands the next CTA to the first free slot) but may add a
+  // Library default for the per-head kernels: the plan for 1, 5/3, 8/3 or
+  // 4 times the co-resident CTAs, whichever a simple model says ends first.
+  // One wave of the occupancy-pinned plan leaves SMs idle behind the
+  // longest chunk when a few long sequences dominate; a finer plan balances
+  // (the hardware hands the next CTA to the first free slot) but may add a
   // merge.  Model: time = max(bytes / bandwidth, longest slot of a greedy
-  // longest-first assignment x time per tile of a lone CTA) + the merge.
+  // longest-first assignment x time per tile of a CTA) + the merge.
+  // (Measured on the GQA decode workload, 64 sequences of 512-8192 keys,
+  // 8 kv heads: 3, 4, 5, 6, 8, 12 slots per SM give 124.9, 122.9, 116.7,
+  // 124.9, 120.8, 120.8 us per step; the model picks 5.)
   if (default_cps && opts->force_splits == 0 && params->max_splits > 1 &&
       kc.kind != KernelKind::kTensorCoreGrouped) {
     const int64_t units_per_item = static_cast<int64_t>(params->h_k) * opts->n_q_tiles;
@@ -135,10 +145,15 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
     int64_t sum_tiles = 0;
     for (int64_t t : tiles) sum_tiles += t;
     const double stream_us = static_cast<double>(sum_tiles) * units_per_item * kTilePairBytes / kPlanBandwidth;
+    const double tile_us = kc.kind == KernelKind::kTensorCoreQRows ? kPlanQRowsTileUs
+                                                                    : kPlanSmTileUs * kc.ctas_per_sm;
     double best = 0;
-    int best_k = 1;
-    for (int k = 1; k <= 4; k *= 2) {
-      const int64_t chunk = chunk_for(static_cast<int64_t>(kc.ctas_per_sm) * k);
+    int64_t best_cps = kc.ctas_per_sm, prev_cps = 0;
+    for (int thirds : kPlanThirds) {
+      const int64_t cps = (static_cast<int64_t>(kc.ctas_per_sm) * thirds + 2) / 3;
+      if (cps == prev_cps) continue;
+      prev_cps = cps;
+      const int64_t chunk = chunk_for(cps);
       std::vector<int64_t> costs;
       for (int64_t t : tiles)
         for (int64_t beg = 0; beg < t; beg += chunk) costs.push_back(std::min(chunk, t - beg));
@@ -155,13 +170,13 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
           makespan = std::max(makespan, t);
         }
       const bool splits = static_cast<int64_t>(costs.size()) > b;
-      const double est = std::max(stream_us, makespan * kPlanTileUs) + (splits ? kPlanMergeUs : 0.0);
-      if (k == 1 || est < best * kPlanMargin) {
+      const double est = std::max(stream_us, makespan * tile_us) + (splits ? kPlanMergeUs : 0.0);
+      if (thirds == 3 || est < best * kPlanMargin) {
         best = est;
-        best_k = k;
+        best_cps = cps;
       }
     }
-    opts->ctas_per_sm = kc.ctas_per_sm * best_k;
+    opts->ctas_per_sm = static_cast<int32_t>(best_cps);
   }
 
   const int64_t chunk = chunk_for(opts->ctas_per_sm);

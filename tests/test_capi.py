@@ -233,3 +233,18 @@ def test_query_rows_kernel_choice():
     assert mj.kernel_name(_params(2, h_k=1, q_len=8, h_r=16, kernel=qr, q_dtype=1)) == "qm_e4m3"
     plan = mj.decode_plan(_params(4, h_k=1, q_len=16, h_r=32), [1000, 2000, 3000, 4000])
     assert plan.opts.n_q_tiles == 4
+
+
+def test_default_plan_splits_when_long_sequences_dominate():
+    # 64 sequences of 512-8192 keys, 8 kv heads, 4 rows: one wave of the
+    # occupancy-pinned plan leaves SMs idle behind the longest sequences, and
+    # the library's default picks a finer plan that the restated plan
+    # reproduces from the reported options
+    rng = np.random.default_rng(5)
+    lens = rng.integers(512, 8193, size=64).tolist()
+    p = mj.make_params(64, 1, 8, 4, 16, 512, 64 * 512, True, mj.MJ_BF16, 16, 128, 0, 0)
+    plan = mj.decode_plan(p, lens, sm_count=152)
+    assert plan.opts.ctas_per_sm in (5, 8, 12) and plan.max_n_splits > 1
+    ref = plan_ref(lens, 8, plan.opts.n_q_tiles, 152, plan.opts.ctas_per_sm, 16)
+    assert [tuple(x) for x in plan.work.tolist()] == [tuple(x) for x in ref.work]
+    assert plan.n_splits.tolist() == ref.n_splits
