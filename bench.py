@@ -180,6 +180,25 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def algorithmic_flops(w) -> int:
+    """QK^T and PV multiply-adds of one decode launch (2 flops each): every
+    visible (key, packed row) pair costs 2 d for S and 2 d for O."""
+    L = np.asarray(w.seq_lens, dtype=np.int64)[:, None]
+    qi = np.arange(w.q_len, dtype=np.int64)[None, :]
+    vis = np.clip(L - w.q_len + qi + 1, 0, L) if w.causal else np.repeat(L, w.q_len, axis=1)
+    return 4 * w.head_dim * w.h_k * w.h_r * int(vis.sum())
+
+
+def tensor_peak():
+    """e4m3 dense peak: the measured sustained bf16 GEMM rate x 2 (the
+    nominal fp8 : bf16 ratio of the tensor cores)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return 2.0 * float(p["bf16_tflops_sustained"]), "measured bf16 sustained x 2 (e4m3 : bf16 nominal)"
+    return 2.0 * 1700.0, "fallback bf16 sustained x 2"
+
+
 def traffic_record(kernel: str, workload_name: str):
     """dram bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source (else None)."""
@@ -512,6 +531,22 @@ def main():
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }
+        if w.q_len * w.h_r >= 128:
+            # at 128 or more packed rows the contraction nears the tensor
+            # ridge: its roof beside the HBM one (the kernels issue e4m3
+            # MMAs; with bf16 Q the hi and lo parts of Q and P double the
+            # executed MMA work over these algorithmic flops)
+            tpk, tsrc = tensor_peak()
+            tfl = algorithmic_flops(w) / (r["decode_ms"] * 1e-3) / 1e12
+            line["roofline_tensor"] = {
+                "bound": "tensor",
+                "achieved": round(tfl, 2),
+                "peak": tpk,
+                "peak_source": tsrc,
+                "unit": "TFLOP/s",
+                "frac": round(tfl / tpk, 4),
+                "flops_per_launch": algorithmic_flops(w),
+            }
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
