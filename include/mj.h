@@ -116,9 +116,13 @@ typedef enum {
  * library's value for the kernel mj_decode_attn will launch for these
  * params, and is filled in on return, so a caller can reproduce the plan:
  *   sm_count         SMs of the target GPU (0 -> 152, a GB300)
- *   ctas_per_sm      co-resident (decode CTA, kv head) pairs per SM of the
- *                    chosen kernel: CTAs per SM, times the kv heads one
- *                    CTA serves
+ *   ctas_per_sm      (decode CTA, kv head) slots per SM.  0 -> the
+ *                    library's choice: for the per-head kernels the
+ *                    co-resident pairs (CTAs per SM), or 5/3, 8/3 or 4
+ *                    times that when a model of the greedy longest-first
+ *                    schedule says the finer plan ends at least 5 % sooner;
+ *                    for the persistent head-grouped kernel its units per
+ *                    SM times the heads one unit serves
  *   n_q_tiles        CTAs per (work item, kv head) along the packed rows
  *   force_splits     > 0: cut every sequence into this many chunks
  *   min_chunk_tiles  lower bound of the chunk size in 128-row tiles (0 -> 1)
