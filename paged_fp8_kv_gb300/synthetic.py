@@ -22,9 +22,10 @@ Input recipe (numpy PCG64 streams, seed fixed per config):
   (seq, kv-head) descale and rounded to e4m3; Q is in vLLM's layout
   (num_seqs * q_len, h_q, d).
 
-The five named configs follow the workloads of the spec description
-(tiny reference, GQA decode, skewed varlen fully-fp8, speculative verify,
-small-live-head sweep); the design doc lists the recipe.
+The five named configs are the workloads the decode path is tested and
+measured on: tiny reference, GQA decode, skewed varlen fully-fp8,
+speculative verify (causal, and a non-causal block variant) and the
+small-live-head sweep.
 """
 
 from __future__ import annotations
