@@ -64,6 +64,44 @@ struct Item {
   int32_t seq, begin, end, slot;
 };
 
+// Longest-first greedy schedule of `units` copies of every cost (sorted
+// descending, plus `overhead` each) on n_slots slots, each copy to a least
+// loaded slot; returns the largest slot load.  The least load never
+// decreases along such a schedule (a least loaded slot only grows), so a
+// histogram of slot loads with a moving minimum gives the same loads as a
+// heap in time linear in the copies and the loads.
+int64_t greedy_makespan(const std::vector<int64_t>& costs, int64_t units, int64_t n_slots, int64_t overhead) {
+  if (costs.empty() || n_slots < 1) return 0;
+  int64_t total = 0;
+  for (int64_t c : costs) total += (c + overhead) * units;
+  const int64_t bound = total / n_slots + costs.front() + overhead + 1;  // > every slot load
+  int64_t makespan = 0;
+  if (bound <= (int64_t{1} << 22)) {
+    std::vector<int64_t> count(static_cast<size_t>(bound) + 1, 0);  // slots per load
+    count[0] = n_slots;
+    int64_t lo = 0;  // the least load
+    for (int64_t c : costs)
+      for (int64_t u = 0; u < units; ++u) {
+        while (count[lo] == 0) ++lo;
+        const int64_t t = lo + c + overhead;
+        --count[lo];
+        ++count[t];
+        makespan = std::max(makespan, t);
+      }
+    return makespan;
+  }
+  std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> load;
+  for (int64_t i = 0; i < n_slots; ++i) load.push(0);
+  for (int64_t c : costs)
+    for (int64_t u = 0; u < units; ++u) {
+      const int64_t t = load.top() + c + overhead;
+      load.pop();
+      load.push(t);
+      makespan = std::max(makespan, t);
+    }
+  return makespan;
+}
+
 }  // namespace
 
 }  // namespace mj
@@ -159,16 +197,7 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
         for (int64_t beg = 0; beg < t; beg += chunk) costs.push_back(std::min(chunk, t - beg));
       if (static_cast<int64_t>(costs.size()) * units_per_item > kPlanModelMaxUnits) break;  // keep the plan cheap
       std::stable_sort(costs.begin(), costs.end(), [](int64_t x, int64_t y) { return x > y; });
-      std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> load;
-      for (int64_t i = 0; i < n_slots; ++i) load.push(0);
-      int64_t makespan = 0;
-      for (int64_t c : costs)
-        for (int64_t u = 0; u < units_per_item; ++u) {
-          const int64_t t = load.top() + c + kPlanCtaOverheadTiles;
-          load.pop();
-          load.push(t);
-          makespan = std::max(makespan, t);
-        }
+      const int64_t makespan = greedy_makespan(costs, units_per_item, n_slots, kPlanCtaOverheadTiles);
       const bool splits = static_cast<int64_t>(costs.size()) > b;
       const double est = std::max(stream_us, makespan * tile_us) + (splits ? kPlanMergeUs : 0.0);
       if (thirds == 3 || est < best * kPlanMargin) {
