@@ -351,13 +351,19 @@ def e2e_measure(args, s, w, step_bytes, dev):
     seq_host = w.seq_lens
     h2d = q_h.numel() * q_h.element_size() + sl_h.numel() * 4 + bt_h.numel() * 4
     d2h = o_h.numel() * 2 + lse_h.numel() * 4
+    # pinned staging for the plan's outputs, allocated once (as a serving
+    # loop would keep it)
+    work_pin = torch.empty((max(1, w.num_seqs * s.max_splits), 4), dtype=torch.int32).pin_memory()
+    ns_pin = torch.empty((w.num_seqs,), dtype=torch.int32).pin_memory()
     times = []
     for i in range(args.warmup + args.steps):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         plan = decode_plan(s.params, seq_host, sm_count=s.sm_count)
-        work_h = torch.from_numpy(plan.work).pin_memory()
-        ns_h = torch.from_numpy(plan.n_splits).pin_memory()
+        n = plan.num_work
+        work_pin.numpy()[:n] = plan.work
+        ns_pin.numpy()[:] = plan.n_splits
+        work_h, ns_h = work_pin[:n], ns_pin
         s.q_vllm.copy_(q_h, non_blocking=True)
         s.seq_lens.copy_(sl_h, non_blocking=True)
         s.block_table.copy_(bt_h, non_blocking=True)

@@ -137,6 +137,7 @@ struct GCfg {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 32 + 1024;
   static_assert(KR >= 16 && KR <= 128, "a head's rows sit within one warp, two or four");
+  static_assert(kWph == 1 || kWph == 2 || kWph == 4, "warps per head");
   static_assert(kPair ? RH == 32 : (W == 8 || W == 16), "TMEM load width / one column per lane");
   static_assert(kN1 % 16 == 0 && kN2 % 16 == 0 && kN1 <= 256 && kN2 <= 256, "MMA N");
   static_assert(kTmemCols <= 512, "TMEM");
