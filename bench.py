@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--kv_layout", default="nhd", choices=["nhd", "hnd", "interleaved", "flashinfer"])
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core (swap-AB), 3 head-grouped tensor-core, 4 query-rows tensor-core")
     ap.add_argument("--l2_prefetch", type=int, default=0, help="0 default, -1 off, 1..8 tiles ahead")
+    ap.add_argument("--kv_evict_first", type=int, default=0, help="K/V loads with L2 EVICT_FIRST: 0 default, -1 off, 1 on")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time steps as plain launches, not CUDA-graph replays")
@@ -250,7 +251,9 @@ def run_mj(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = workload(args)
-    s = DecodeSession(w, device=str(dev), kv_layout=args.kv_layout, kernel=args.kernel, l2_prefetch=args.l2_prefetch)
+    s = DecodeSession(w, device=str(dev), kv_layout=args.kv_layout, kernel=args.kernel, l2_prefetch=args.l2_prefetch,
+        kv_evict_first=args.kv_evict_first,
+    )
     d_bytes, m_bytes, step_bytes = algorithmic_bytes(w, s.plan)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -504,6 +507,7 @@ def main():
                 "kernel": s.kernel,
                 "kv_layout": args.kv_layout,
                 "l2_prefetch": args.l2_prefetch,
+                "kv_evict_first": args.kv_evict_first,
                 "max_splits": s.max_splits,
                 "plan": {
                     "work_items": s.plan.num_work,

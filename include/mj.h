@@ -75,11 +75,17 @@ typedef enum { MJ_BF16 = 0, MJ_E4M3 = 1 } mj_dtype;
  *   l2_prefetch tensor-core kernel: KV tiles its producer pulls into L2
  *               ahead of the shared-memory loads (source: the kernel's
  *               `l2_prefetch` option on the "mjolnir/t5_decode.py" page);
- *               0 = library default, -1 = off, 1..8 = distance in tiles */
+ *               0 = library default, -1 = off, 1..8 = distance in tiles
+ *   kv_evict_first
+ *               the tensor-core kernels' K/V tile loads carry an L2
+ *               EVICT_FIRST cache policy (KV is read once; source: the
+ *               kernel's `kv_evict_first` option on the
+ *               "mjolnir/t5_decode.py" page); 0 = library default,
+ *               -1 = off, 1 = on */
 typedef struct {
   int32_t num_seqs, q_len, h_k, h_r, head_dim, page_size;
   int32_t max_blocks, num_pages, causal, q_dtype, max_splits, kernel;
-  int32_t l2_prefetch;
+  int32_t l2_prefetch, kv_evict_first;
 } mj_decode_params;
 
 /* Decode kernel families.  Both compute the same function; the choice only

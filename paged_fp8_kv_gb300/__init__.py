@@ -61,6 +61,7 @@ class DecodeParams(ctypes.Structure):
             "max_splits",
             "kernel",
             "l2_prefetch",
+            "kv_evict_first",
         )
     ]
 
@@ -170,6 +171,7 @@ def make_params(
     head_dim: int = 128,
     kernel: int = MJ_KERNEL_AUTO,
     l2_prefetch: int = 0,
+    kv_evict_first: int = 0,
 ) -> DecodeParams:
     return DecodeParams(
         num_seqs,
@@ -185,6 +187,7 @@ def make_params(
         max_splits,
         kernel,
         l2_prefetch,
+        kv_evict_first,
     )
 
 

@@ -204,6 +204,8 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       return blk < valid_pages ? a.block_table[bt_row + blk] : a.num_pages;
     };
     if (lane == 0) ptx::prefetch_tmap(tmap);
+    const bool evict_first = a.kv_evict_first != 0;
+    const uint64_t kv_policy = ptx::policy_evict_first();
     // a tile spans nbox whole blocks (or lies in one block) and the window
     // starts at the item's first block, so a tile never straddles windows
     int wbase = key_begin / PS;
@@ -231,7 +233,9 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const int row_off = key % PS;
       if (lane == 0) ptx::mbar_arrive_expect_tx(full(st), kTileBytes);
       __syncwarp();
-      if (active) ptx::tma_load_4d(ring + st * kTileBytes + lane * box_rows * 128, tmap, full(st), 0, row_off, g, page);
+      if (active)
+        ptx::tma_load_kv(ring + st * kTileBytes + lane * box_rows * 128, tmap, full(st), 0, row_off, g, page,
+                         evict_first, kv_policy);
       issued = i + 1;
     }
     if (*abort_flag && lane == 0) {

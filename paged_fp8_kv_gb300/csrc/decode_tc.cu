@@ -288,6 +288,8 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::prefetch_tmap(&tmap_k);
       ptx::prefetch_tmap(&tmap_v);
     }
+    const bool evict_first = a.kv_evict_first != 0;
+    const uint64_t kv_policy = ptx::policy_evict_first();
     int next_page = (lane < ppt && t_begin * ppt + lane < valid_pages) ? first_page_raw : a.num_pages;
     int issued = 0;
     for (int i = 0; i < T; ++i) {
@@ -322,8 +324,8 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       }
       __syncwarp();
       if (lane < ppt) {
-        ptx::tma_load_4d(dk + lane * PS * 128, &tmap_k, bar.kfull + 8 * st, 0, 0, g, page);
-        ptx::tma_load_4d(dv + lane * PS * 128, &tmap_v, bar.vfull + 8 * st, 0, 0, g, page);
+        ptx::tma_load_kv(dk + lane * PS * 128, &tmap_k, bar.kfull + 8 * st, 0, 0, g, page, evict_first, kv_policy);
+        ptx::tma_load_kv(dv + lane * PS * 128, &tmap_v, bar.vfull + 8 * st, 0, 0, g, page, evict_first, kv_policy);
       }
       issued = i + 1;
     }

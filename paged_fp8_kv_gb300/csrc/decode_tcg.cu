@@ -497,6 +497,8 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     const bool active = lane < G * bph;
     const bool one_box = bph == 1 && box_rows == KR;
     if (lane == 0) ptx::prefetch_tmap(tmap);
+    const bool evict_first = a.kv_evict_first != 0;
+    const uint64_t kv_policy = ptx::policy_evict_first();
     uint32_t n = 0;  // tiles issued, over all units
     bool alive = true;
     for (int it = 0; alive; ++it) {
@@ -547,12 +549,14 @@ decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         if (one_box) {
           if (lane == 0) {
             ptx::mbar_arrive_expect_tx(full(st), kTileBytes);
-            ptx::tma_load_4d(dst, tmap, full(st), 0, row_off, g0, page);
+            ptx::tma_load_kv(dst, tmap, full(st), 0, row_off, g0, page, evict_first, kv_policy);
           }
         } else {
           if (lane == 0) ptx::mbar_arrive_expect_tx(full(st), kTileBytes);
           __syncwarp();
-          if (active) ptx::tma_load_4d(dst + (h * KR + jb * box_rows) * 128, tmap, full(st), 0, row_off, g0 + h, page);
+          if (active)
+            ptx::tma_load_kv(dst + (h * KR + jb * box_rows) * 128, tmap, full(st), 0, row_off, g0 + h, page,
+                             evict_first, kv_policy);
         }
       }
     }

@@ -33,7 +33,8 @@ struct DecodeDev {
   int32_t* status;
   int32_t num_seqs, h_k, n_q, q_len, h_r, page_size, max_blocks, causal, max_splits, num_work;
   int32_t num_pages;
-  int32_t l2_prefetch;  // tiles the producer prefetches into L2 ahead (0 = off)
+  int32_t l2_prefetch;     // tiles the producer prefetches into L2 ahead (0 = off)
+  int32_t kv_evict_first;  // K/V tile loads with an L2 EVICT_FIRST policy (0 = off)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;

@@ -113,6 +113,32 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// The same load with an L2 cache policy (a createpolicy word).
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
+                                                 int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+      : "memory");
+}
+
+// L2 policy word: lines loaded under it are the first to be evicted.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// K/V tile load: EVICT_FIRST policy when `evict_first` (warp-uniform).
+__device__ __forceinline__ void tma_load_kv(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
+                                            int c3, bool evict_first, uint64_t policy) {
+  if (evict_first)
+    tma_load_4d_hint(dst, tmap, bar, c0, c1, c2, c3, policy);
+  else
+    tma_load_4d(dst, tmap, bar, c0, c1, c2, c3);
+}
+
 // Pulls a tensor tile into L2 only (no shared-memory destination, no
 // completion to wait for).
 __device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {

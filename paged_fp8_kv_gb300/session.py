@@ -40,6 +40,7 @@ class DecodeSession:
         kv_layout: str = "nhd",
         kernel: int = 0,
         l2_prefetch: int = 0,
+        kv_evict_first: int = 0,
     ):
         self.w = w
         self.device = torch.device(device)
@@ -63,6 +64,7 @@ class DecodeSession:
             w.head_dim,
             kernel,
             l2_prefetch,
+            kv_evict_first,
         )
         self.kernel = kernel_name(self.params)
         if sm_count is None:

@@ -275,3 +275,22 @@ def test_unpacked_output_matches_oracle_layout():
     got = s.o_vllm.float().cpu().numpy()
     ref_v = unpack_o_ref(ref_o, w.num_seqs, w.q_len, w.h_k, w.h_r)
     assert np.all(np.abs(got - ref_v) <= 2e-2 + 2e-2 * np.abs(ref_v))
+
+
+@pytest.mark.parametrize(
+    "cfg,kw,kernel",
+    [
+        (2, dict(num_seqs=4, len_range=(300, 2000)), 2),  # swap-AB
+        (2, dict(num_seqs=4, len_range=(300, 2000)), 3),  # head-grouped
+        (4, dict(num_seqs=3, len_range=(500, 1500)), 4),  # query rows
+        (3, dict(num_seqs=3, len_range=(3000, 300), max_splits=16), 2),  # fully-fp8, split
+    ],
+    ids=["swap_ab", "grouped", "query_rows", "fp8_split"],
+)
+def test_kv_evict_first_leaves_results_unchanged(cfg, kw, kernel):
+    # an L2 cache policy on the K/V loads changes no byte of the output
+    w = syn.config(cfg, **kw)
+    a = run(w, kernel=kernel, kv_evict_first=-1)
+    b = run(w, kernel=kernel, kv_evict_first=1)
+    assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
+    compare(w, b.o_host(), b.lse_host())
