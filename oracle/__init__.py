@@ -11,6 +11,9 @@ arithmetic.
   in fp64, threaded over (sequence, kv head) units (built into
   ``liboracle.so`` by :func:`build`).
 * ``plan_ref.py`` - a plain restatement of the occupancy-pinned plan.
+* ``layout_ref.py`` - the query / output row permutation.
+* ``quant_ref.py`` - the per-(sequence, kv head) fp8 query quantisation
+  fused with the pack, with its own e4m3 encoder.
 
 Every function here is pinned by ``tests/test_oracle.py`` against facts the
 source pages and mathematics fix (see that file's docstring).
