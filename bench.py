@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time steps as plain launches, not CUDA-graph replays")
+    ap.add_argument("--q_quant", action="store_true", help="also time the fused fp8 Q quantisation + pack for this shape")
     return ap.parse_args()
 
 
@@ -319,6 +320,7 @@ def run_mj(args, rank, world, local_rank):
     step_ms = max_over_ranks(step_ms, world, dev)
 
     launches = s.launches_per_step() * args.steps
+    q_quant = q_quant_measure(w, dev, flush) if (w.q_is_e4m3 or args.q_quant) and rank == 0 else None
     e2e = None if args.no_e2e else e2e_measure(args, s, w, step_bytes, dev)
     clocks = clk.summary()
     return dict(
@@ -334,7 +336,47 @@ def run_mj(args, rank, world, local_rank):
         launches=launches,
         e2e=e2e,
         clocks=clocks,
+        q_quant=q_quant,
     )
+
+
+def q_quant_measure(w, dev, flush, launches: int = 200):
+    """The upstream fp8 step for this workload's query shape: bf16 Q in
+    vLLM's layout -> e4m3 packed rows and per-(sequence, kv head)
+    descales, one fused launch (mj_quantize_pack_q), timed alone with CUDA
+    events after an L2 flush.  Bytes: bf16 Q read once, codes and descales
+    written."""
+    import torch
+
+    from paged_fp8_kv_gb300 import quantize_pack_q
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    q = torch.randn((w.num_seqs * w.q_len, w.h_q, w.head_dim), generator=gen, device=dev).to(torch.bfloat16)
+    q8 = torch.empty((w.num_seqs, w.h_k, w.n_q, w.head_dim), dtype=torch.uint8, device=dev)
+    ds = torch.empty((w.num_seqs, w.h_k), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        quantize_pack_q(q, q8, ds, w.num_seqs, w.q_len, w.h_k, w.h_r)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush.fill_(7)
+        e0.record()
+        quantize_pack_q(q, q8, ds, w.num_seqs, w.q_len, w.h_k, w.h_r)
+        e1.record()
+    torch.cuda.synchronize()
+    us = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs])) * 1e3
+    nbytes = q.numel() * 2 + q8.numel() + ds.numel() * 4
+    peak, _ = measured_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {
+        "kernel": "quantize_pack_q",
+        "shape": f"({w.num_seqs * w.q_len}, {w.h_q}, {w.head_dim}) bf16 -> ({w.num_seqs}, {w.h_k}, {w.n_q}, {w.head_dim}) e4m3",
+        "us_per_launch": round(us, 2),
+        "bytes_per_launch": int(nbytes),
+        "achieved_gbs": round(gbs, 1),
+        "frac_of_hbm": round(gbs / peak, 4),
+    }
 
 
 def e2e_measure(args, s, w, step_bytes, dev):
@@ -539,6 +581,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": r["e2e"],
             "gpu_launches": r["launches"],
+            **({"q_quant": r["q_quant"]} if r["q_quant"] else {}),
             "clocks": r["clocks"],
         }
         if w.q_len * w.h_r >= 128:

@@ -256,6 +256,27 @@ mj_status mj_decode_attn_static_ws(const mj_decode_params* params, const mj_deco
 mj_status mj_pack_q(const void* q_vllm, void* q_packed, int32_t elem_bytes, int32_t num_seqs,
                     int32_t q_len, int32_t h_k, int32_t h_r, int32_t head_dim, mj_stream_t stream);
 
+/* Fused fp8 query quantisation and pack (source: `quantize_q_fp8` and
+ * `pack_q`).  For every sequence b and kv head g the group is Q's q_len
+ * tokens x h_r heads x d values of that kv head;
+ *   q_descale[b*h_k + g] = max(amax_group |q|, 1e-6) / 448   (fp32)
+ *   q_packed[b][g][qi*h_r + hr][:] = e4m3(q / q_descale[b*h_k + g])
+ * with IEEE fp32 division and e4m3 rounding to nearest even, saturating at
+ * +-448.  The outputs feed mj_decode_attn with q_dtype MJ_E4M3 and
+ * q_descale strides (qd_seq, qd_head) = (h_k, 1).
+ *   q_vllm     device bf16 (num_seqs*q_len, h_k*h_r, head_dim), contiguous,
+ *              16-byte aligned, finite values
+ *   q_packed   device e4m3 (num_seqs, h_k, q_len*h_r, head_dim), 16-byte
+ *              aligned
+ *   q_descale  device fp32 (num_seqs, h_k)
+ *   head_dim   a multiple of 16
+ * The three buffers must not overlap.  One kernel launch on `stream`; no
+ * host sync.  Errors: MJ_ERR_INVALID_ARG (nulls, alignment, sizes,
+ * overlap), MJ_ERR_UNSUPPORTED (head_dim, a group over 2^30 values),
+ * MJ_ERR_CUDA (launch). */
+mj_status mj_quantize_pack_q(const void* q_vllm, void* q_packed, float* q_descale, int32_t num_seqs,
+                             int32_t q_len, int32_t h_k, int32_t h_r, int32_t head_dim, mj_stream_t stream);
+
 /* Inverse permutation for the bf16 output (source: `unpack_o`). */
 mj_status mj_unpack_o(const void* o_packed, void* o_vllm, int32_t num_seqs, int32_t q_len,
                       int32_t h_k, int32_t h_r, int32_t head_dim, mj_stream_t stream);

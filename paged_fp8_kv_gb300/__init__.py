@@ -138,6 +138,8 @@ def lib() -> ctypes.CDLL:
         L.mj_decode_attn.argtypes = [P(DecodeParams), P(DecodeArgs), _vp]
         L.mj_pack_q.restype = ctypes.c_int
         L.mj_pack_q.argtypes = [_vp, _vp] + [ctypes.c_int32] * 6 + [_vp]
+        L.mj_quantize_pack_q.restype = ctypes.c_int
+        L.mj_quantize_pack_q.argtypes = [_vp, _vp, _vp] + [ctypes.c_int32] * 5 + [_vp]
         L.mj_unpack_o.restype = ctypes.c_int
         L.mj_unpack_o.argtypes = [_vp, _vp] + [ctypes.c_int32] * 5 + [_vp]
         L.mj_status_string.restype = ctypes.c_char_p
@@ -360,6 +362,23 @@ def pack_q(q_vllm, q_packed, num_seqs: int, q_len: int, h_k: int, h_r: int, stre
         _stream_handle(stream),
     )
     _check(st, "mj_pack_q")
+
+
+def quantize_pack_q(q_vllm, q_packed, q_descale, num_seqs: int, q_len: int, h_k: int, h_r: int, stream=None) -> None:
+    """mj_quantize_pack_q: bf16 (b*q_len, h_k*h_r, d) -> e4m3 codes
+    (b, h_k, q_len*h_r, d) and fp32 descales (b, h_k)."""
+    st = lib().mj_quantize_pack_q(
+        _ptr(q_vllm),
+        _ptr(q_packed),
+        _ptr(q_descale),
+        num_seqs,
+        q_len,
+        h_k,
+        h_r,
+        int(q_vllm.shape[-1]),
+        _stream_handle(stream),
+    )
+    _check(st, "mj_quantize_pack_q")
 
 
 def unpack_o(o_packed, o_vllm, num_seqs: int, q_len: int, h_k: int, h_r: int, stream=None) -> None:

@@ -296,6 +296,29 @@ extern "C" mj_status mj_pack_q(const void* q_vllm, void* q_packed, int32_t elem_
   return permute(q_vllm, q_packed, elem_bytes, num_seqs, q_len, h_k, h_r, head_dim, true, stream);
 }
 
+extern "C" mj_status mj_quantize_pack_q(const void* q_vllm, void* q_packed, float* q_descale, int32_t num_seqs,
+                                        int32_t q_len, int32_t h_k, int32_t h_r, int32_t head_dim,
+                                        mj_stream_t stream) {
+  if (!q_vllm || !q_packed || !q_descale || !aligned16(q_vllm) || !aligned16(q_packed)) return MJ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_descale) & 3) != 0) return MJ_ERR_INVALID_ARG;
+  if (num_seqs < 1 || q_len < 1 || h_k < 1 || h_r < 1 || head_dim < 1) return MJ_ERR_INVALID_ARG;
+  if (head_dim % 16 != 0) return MJ_ERR_UNSUPPORTED;
+  const int64_t elems = static_cast<int64_t>(num_seqs) * q_len * h_k * h_r * head_dim;
+  if (static_cast<int64_t>(q_len) * h_r * head_dim > (int64_t{1} << 30) || elems > (int64_t{1} << 40))
+    return MJ_ERR_UNSUPPORTED;
+  const char* s = static_cast<const char*>(q_vllm);
+  const char* d = static_cast<const char*>(q_packed);
+  const char* f = reinterpret_cast<const char*>(q_descale);
+  const size_t in_bytes = static_cast<size_t>(elems) * 2, out_bytes = static_cast<size_t>(elems);
+  const size_t ds_bytes = static_cast<size_t>(num_seqs) * h_k * 4;
+  if ((s < d + out_bytes && d < s + in_bytes) || (s < f + ds_bytes && f < s + in_bytes) ||
+      (d < f + ds_bytes && f < d + out_bytes))
+    return MJ_ERR_INVALID_ARG;  // overlap
+  const cudaError_t e = launch_quantize_pack_q(q_vllm, q_packed, q_descale, num_seqs, q_len, h_k, h_r, head_dim,
+                                               reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MJ_OK : MJ_ERR_CUDA;
+}
+
 extern "C" mj_status mj_unpack_o(const void* o_packed, void* o_vllm, int32_t num_seqs, int32_t q_len,
                                  int32_t h_k, int32_t h_r, int32_t head_dim, mj_stream_t stream) {
   return permute(o_packed, o_vllm, 2, num_seqs, q_len, h_k, h_r, head_dim, false, stream);

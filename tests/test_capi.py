@@ -183,6 +183,22 @@ def test_pack_validation():
     assert L.mj_unpack_o(None, fake, 1, 2, 1, 2, 128, None) == mj.MJ_ERR_INVALID_ARG
 
 
+def test_quantize_pack_validation():
+    # every refusal happens on the host, before any launch
+    L = mj.lib()
+    src, dst, ds = 1 << 20, 1 << 26, 1 << 28
+    q = L.mj_quantize_pack_q
+    assert q(None, dst, ds, 1, 1, 1, 16, 128, None) == mj.MJ_ERR_INVALID_ARG
+    assert q(src, dst, None, 1, 1, 1, 16, 128, None) == mj.MJ_ERR_INVALID_ARG
+    assert q(src + 8, dst, ds, 1, 1, 1, 16, 128, None) == mj.MJ_ERR_INVALID_ARG  # misaligned Q
+    assert q(src, dst + 4, ds, 1, 1, 1, 16, 128, None) == mj.MJ_ERR_INVALID_ARG  # misaligned codes
+    assert q(src, dst, ds + 2, 1, 1, 1, 16, 128, None) == mj.MJ_ERR_INVALID_ARG  # misaligned descales
+    assert q(src, dst, ds, 0, 1, 1, 16, 128, None) == mj.MJ_ERR_INVALID_ARG
+    assert q(src, dst, ds, 1, 1, 1, 16, 120, None) == mj.MJ_ERR_UNSUPPORTED  # head_dim % 16
+    assert q(src, src + 2048, ds, 1, 1, 1, 16, 128, None) == mj.MJ_ERR_INVALID_ARG  # codes inside Q
+    assert q(src, dst, dst + 16, 1, 1, 1, 16, 128, None) == mj.MJ_ERR_INVALID_ARG  # descales inside codes
+
+
 def test_status_strings_and_kernel_name():
     assert mj.status_string(mj.MJ_OK) == "ok"
     assert "timed out" in mj.status_string(mj.MJ_ERR_TIMEOUT)
