@@ -256,6 +256,33 @@ mj_status mj_decode_attn_static_ws(const mj_decode_params* params, const mj_deco
 mj_status mj_pack_q(const void* q_vllm, void* q_packed, int32_t elem_bytes, int32_t num_seqs,
                     int32_t q_len, int32_t h_k, int32_t h_r, int32_t head_dim, mj_stream_t stream);
 
+/* The plan of mj_decode_plan computed on the device from device sequence
+ * lengths, so that plan, decode and merge can be captured in one CUDA graph
+ * and replayed while the lengths change (source: `plan_split_kv`; the
+ * paged-decode page's schedule kernel plans on the device for the same
+ * reason).  The rule and the item order are mj_decode_plan's, for the
+ * options given; no model picks ctas_per_sm here (0 takes the kernel's
+ * co-resident CTAs), so pass the options a host plan reported to reproduce
+ * it.  The work list always has opts->pad_to rows: items, then (0,0,0,0)
+ * padding; launch mj_decode_attn with num_work = pad_to and max_n_splits =
+ * max_splits.
+ *   opts            in/out as for mj_decode_plan; pad_to >= 1 is required
+ *   seq_lens_dev    device int32[num_seqs], 0 <= L_b <= max_blocks*page_size
+ *   work_dev        device int32[pad_to][4], 16-byte aligned
+ *   n_splits_dev    device int32[num_seqs]
+ *   chunk_tiles_dev device int32, may be NULL
+ *   status_dev      device int32, may be NULL; caller-zeroed; receives
+ *                   MJ_ERR_INVALID_ARG (a length out of range, more splits
+ *                   than max_splits) or MJ_ERR_CAPACITY (more items than
+ *                   pad_to), in which case the outputs are unspecified (every
+ *                   write stays inside the buffers)
+ * One single-CTA kernel on `stream`; no host sync.  Errors returned at once:
+ * MJ_ERR_INVALID_ARG (params, nulls, alignment, pad_to < 1),
+ * MJ_ERR_UNSUPPORTED (num_seqs > 16384), MJ_ERR_CUDA (launch). */
+mj_status mj_decode_plan_device(const mj_decode_params* params, mj_plan_opts* opts, const int32_t* seq_lens_dev,
+                                int32_t* work_dev, int32_t* n_splits_dev, int32_t* chunk_tiles_dev,
+                                int32_t* status_dev, mj_stream_t stream);
+
 /* Fused fp8 query quantisation and pack (source: `quantize_q_fp8` and
  * `pack_q`).  For every sequence b and kv head g the group is Q's q_len
  * tokens x h_r heads x d values of that kv head;

@@ -138,6 +138,8 @@ def lib() -> ctypes.CDLL:
         L.mj_decode_attn.argtypes = [P(DecodeParams), P(DecodeArgs), _vp]
         L.mj_pack_q.restype = ctypes.c_int
         L.mj_pack_q.argtypes = [_vp, _vp] + [ctypes.c_int32] * 6 + [_vp]
+        L.mj_decode_plan_device.restype = ctypes.c_int
+        L.mj_decode_plan_device.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.mj_quantize_pack_q.restype = ctypes.c_int
         L.mj_quantize_pack_q.argtypes = [_vp, _vp, _vp] + [ctypes.c_int32] * 5 + [_vp]
         L.mj_unpack_o.restype = ctypes.c_int
@@ -362,6 +364,38 @@ def pack_q(q_vllm, q_packed, num_seqs: int, q_len: int, h_k: int, h_r: int, stre
         _stream_handle(stream),
     )
     _check(st, "mj_pack_q")
+
+
+def decode_plan_device(
+    params: DecodeParams,
+    seq_lens,
+    work,
+    n_splits,
+    pad_to: int,
+    sm_count: int = 0,
+    ctas_per_sm: int = 0,
+    n_q_tiles: int = 0,
+    force_splits: int = 0,
+    min_chunk_tiles: int = 0,
+    chunk_tiles=None,
+    status=None,
+    stream=None,
+) -> PlanOpts:
+    """mj_decode_plan_device on device seq_lens (int32 (b,)) into device work
+    (int32 (pad_to, 4)) and n_splits (int32 (b,)); returns the options used."""
+    opts = PlanOpts(sm_count, ctas_per_sm, n_q_tiles, force_splits, min_chunk_tiles, pad_to)
+    st = lib().mj_decode_plan_device(
+        ctypes.byref(params),
+        ctypes.byref(opts),
+        _ptr(seq_lens),
+        _ptr(work),
+        _ptr(n_splits),
+        _ptr(chunk_tiles),
+        _ptr(status),
+        _stream_handle(stream),
+    )
+    _check(st, "mj_decode_plan_device")
+    return opts
 
 
 def quantize_pack_q(q_vllm, q_packed, q_descale, num_seqs: int, q_len: int, h_k: int, h_r: int, stream=None) -> None:

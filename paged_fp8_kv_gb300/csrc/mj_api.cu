@@ -2,6 +2,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 
@@ -294,6 +295,32 @@ extern "C" mj_status mj_pack_q(const void* q_vllm, void* q_packed, int32_t elem_
                                int32_t q_len, int32_t h_k, int32_t h_r, int32_t head_dim,
                                mj_stream_t stream) {
   return permute(q_vllm, q_packed, elem_bytes, num_seqs, q_len, h_k, h_r, head_dim, true, stream);
+}
+
+extern "C" mj_status mj_decode_plan_device(const mj_decode_params* params, mj_plan_opts* opts,
+                                           const int32_t* seq_lens_dev, int32_t* work_dev, int32_t* n_splits_dev,
+                                           int32_t* chunk_tiles_dev, int32_t* status_dev, mj_stream_t stream) {
+  const mj_status st = check_params(params);
+  if (st != MJ_OK) return st;
+  if (!opts || !seq_lens_dev || !work_dev || !n_splits_dev) return MJ_ERR_INVALID_ARG;
+  if (!aligned16(work_dev)) return MJ_ERR_INVALID_ARG;
+  if (opts->sm_count < 0 || opts->ctas_per_sm < 0 || opts->n_q_tiles < 0 || opts->force_splits < 0 ||
+      opts->min_chunk_tiles < 0 || opts->pad_to < 1)
+    return MJ_ERR_INVALID_ARG;  // the work list has a fixed length: pad_to
+  if (params->num_seqs > kMaxDevicePlanSeqs) return MJ_ERR_UNSUPPORTED;
+  const KernelChoice kc = choose_kernel(*params);
+  if (opts->sm_count == 0) opts->sm_count = kDefaultSmCount;
+  if (opts->ctas_per_sm == 0) opts->ctas_per_sm = kc.ctas_per_sm;
+  if (opts->n_q_tiles == 0) opts->n_q_tiles = kc.n_q_tiles;
+  if (opts->min_chunk_tiles == 0) opts->min_chunk_tiles = 1;
+  const int64_t slots = std::max<int64_t>(
+      1, static_cast<int64_t>(opts->sm_count) * opts->ctas_per_sm / (static_cast<int64_t>(params->h_k) * opts->n_q_tiles));
+  const int64_t max_len = static_cast<int64_t>(params->max_blocks) * params->page_size;
+  const cudaError_t e = launch_plan_device(seq_lens_dev, params->num_seqs, max_len, slots, params->max_splits,
+                                           opts->force_splits, opts->min_chunk_tiles, opts->pad_to,
+                                           reinterpret_cast<int4*>(work_dev), n_splits_dev, chunk_tiles_dev,
+                                           status_dev, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MJ_OK : MJ_ERR_CUDA;
 }
 
 extern "C" mj_status mj_quantize_pack_q(const void* q_vllm, void* q_packed, float* q_descale, int32_t num_seqs,

@@ -11,6 +11,7 @@ constexpr int kTileRows = 128;  // plan unit: KV rows per tile
 constexpr int kHeadDim = 128;
 constexpr int kMaxSplits = 256;
 constexpr int kDefaultSmCount = 152;  // GB300
+constexpr int kMaxDevicePlanSeqs = 16384;  // device plan: one CTA, keys and tiles in shared memory
 
 enum class KernelKind { kCudaCore = 0, kTensorCore = 1, kTensorCoreGrouped = 2, kTensorCoreQRows = 3 };
 

@@ -49,6 +49,9 @@ bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, in
 cudaError_t launch_merge(const DecodeDev& a, int max_n_splits, cudaStream_t stream);
 
 // Layout permutations (vLLM <-> packed rows).
+cudaError_t launch_plan_device(const int32_t* seq_lens, int num_seqs, int64_t max_len, int64_t slots,
+                               int max_splits, int force_splits, int min_chunk, int pad_to, int4* work,
+                               int32_t* n_splits, int32_t* chunk_out, int32_t* status, cudaStream_t stream);
 cudaError_t launch_quantize_pack_q(const void* q_vllm, void* q_packed, float* q_descale, int num_seqs, int q_len,
                                    int h_k, int h_r, int head_dim, cudaStream_t stream);
 cudaError_t launch_permute_rows(const void* src, void* dst, int elem_bytes, int num_seqs, int q_len,

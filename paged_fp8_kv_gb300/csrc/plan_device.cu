@@ -1,0 +1,233 @@
+// The occupancy-pinned split-KV plan computed on the device.
+//
+// Source: the "mjolnir/t5_decode.py" page, `plan_split_kv` and `SplitPlan`
+// (host helpers section); the schedule kernel of the paged-decode page
+// builds its plan on the device for the same reason: sequence lengths that
+// change from step to step inside one captured CUDA graph.  The rule is the
+// host plan's, for options the caller fixes (slots per wave, max_splits,
+// force_splits, min_chunk_tiles, a padded work-list length):
+//
+//   T_b   = max(1, ceil(L_b / 128)) tiles; T = max_b T_b
+//   floor = max(min_chunk_tiles, ceil(T / max_splits))
+//   chunk = max(floor, ceil(T / force_splits))   if force_splits > 0
+//         = T                                    if b >= slots or max_splits == 1
+//         = the least c in [floor, max(floor, T)] with sum_b ceil(T_b / c) <= slots
+//   items (b, s*chunk, min(T_b, (s+1)*chunk), s), ordered by length, longest
+//   first, equal lengths in (b, s) order; then (0, 0, 0, 0) up to pad_to.
+//
+// One CTA of 1024 threads.  The tile counts sit in shared memory; the
+// bisection's chunk totals are block reductions.  Every item of length
+// `chunk` precedes every shorter one, and those full-length items are
+// placed in (b, s) order by a prefix sum of floor(T_b / chunk).  The rest
+// (at most one item per sequence, of length T_b mod chunk) are ordered by a
+// bitonic sort of (length descending, b ascending) keys, unique per
+// sequence, so the order is the stable one.  Problems are reported in the
+// optional status word (lengths out of range, more splits than max_splits,
+// more items than pad_to); the outputs are then unspecified but every write
+// stays inside the buffers.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mj_kernels.h"
+
+namespace mj {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kTileRowsDev = 128;
+constexpr int kStatusInvalid = 1;   // MJ_ERR_INVALID_ARG
+constexpr int kStatusCapacity = 3;  // MJ_ERR_CAPACITY
+
+__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+__device__ __forceinline__ int64_t block_sum(int64_t v, int64_t* red) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  __syncthreads();  // red is free
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int64_t s = 0;
+  for (int w = 0; w < kPlanThreads / 32; ++w) s += red[w];
+  return s;
+}
+
+__device__ __forceinline__ int64_t block_max(int64_t v, int64_t* red) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v = max64(v, __shfl_xor_sync(0xffffffffu, v, off));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int64_t m = red[0];
+  for (int w = 1; w < kPlanThreads / 32; ++w) m = max64(m, red[w]);
+  return m;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+    plan_device_kernel(const int32_t* __restrict__ seq_lens, int num_seqs, int64_t max_len, int64_t slots,
+                       int max_splits, int force_splits, int min_chunk, int pad_to, int sort_n,
+                       int4* __restrict__ work, int32_t* __restrict__ n_splits, int32_t* __restrict__ chunk_out,
+                       int32_t* __restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);                // [sort_n]
+  int32_t* tiles = reinterpret_cast<int32_t*>(keys + sort_n);            // [num_seqs]
+  __shared__ int64_t red[kPlanThreads / 32];
+  __shared__ int64_t scan[kPlanThreads];
+  const int tid = threadIdx.x;
+
+  // tile counts, longest
+  int64_t bad = 0, longest = 1;
+  for (int b = tid; b < num_seqs; b += kPlanThreads) {
+    int64_t L = seq_lens[b];
+    if (L < 0 || L > max_len) {
+      bad = 1;
+      L = L < 0 ? 0 : max_len;
+    }
+    const int64_t t = L > 0 ? (L + kTileRowsDev - 1) / kTileRowsDev : 1;
+    tiles[b] = static_cast<int32_t>(t);
+    longest = max64(longest, t);
+  }
+  longest = block_max(longest, red);
+  bad = block_max(bad, red);
+
+  // chunk
+  const int64_t floor_c = max64(min_chunk, (longest + max_splits - 1) / max_splits);
+  int64_t chunk;
+  if (force_splits > 0) {
+    chunk = max64(floor_c, (longest + force_splits - 1) / force_splits);
+  } else if (num_seqs >= slots || max_splits == 1) {
+    chunk = longest;
+  } else {
+    int64_t lo = floor_c, hi = max64(floor_c, longest);
+    while (lo < hi) {  // uniform over the block: lo, hi come from block reductions
+      const int64_t mid = lo + (hi - lo) / 2;
+      int64_t part = 0;
+      for (int b = tid; b < num_seqs; b += kPlanThreads) part += (tiles[b] + mid - 1) / mid;
+      if (block_sum(part, red) <= slots)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    chunk = lo;
+  }
+
+  // per sequence: splits, full-length chunks (contiguous runs of sequences
+  // per thread, so the prefix sum keeps b order)
+  const int per = (num_seqs + kPlanThreads - 1) / kPlanThreads;
+  const int b0 = tid * per, b1 = min(num_seqs, b0 + per);
+  int64_t my_full = 0, my_rem = 0, over = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int64_t t = tiles[b];
+    const int64_t k = (t + chunk - 1) / chunk;
+    if (k > max_splits) over = 1;
+    n_splits[b] = static_cast<int32_t>(k);
+    my_full += t / chunk;
+    my_rem += (t % chunk) != 0;
+  }
+  // exclusive scans of the full-item and remainder counts over threads
+  scan[tid] = my_full;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const int64_t v = tid >= off ? scan[tid - off] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  const int64_t full_total = scan[kPlanThreads - 1];
+  int64_t off_full = scan[tid] - my_full;
+  __syncthreads();
+  scan[tid] = my_rem;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const int64_t v = tid >= off ? scan[tid - off] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  const int64_t rem_total = scan[kPlanThreads - 1];
+  int64_t off_rem = scan[tid] - my_rem;
+  __syncthreads();
+  over = block_max(over, red);
+  const int64_t n_items = full_total + rem_total;
+  const bool fits = n_items <= pad_to;
+  if (tid == 0) {
+    if (chunk_out) *chunk_out = static_cast<int32_t>(chunk);
+    if (status && (bad || over)) atomicExch(reinterpret_cast<int*>(status), kStatusInvalid);
+    else if (status && !fits) atomicExch(reinterpret_cast<int*>(status), kStatusCapacity);
+  }
+
+  // full-length items in (b, s) order; remainder keys: length descending,
+  // then b ascending (unique, so any correct sort keeps generation order)
+  for (int b = b0; b < b1; ++b) {
+    const int64_t t = tiles[b];
+    const int64_t f = t / chunk;
+    if (fits)
+      for (int64_t s = 0; s < f; ++s)
+        work[off_full + s] = make_int4(b, static_cast<int>(s * chunk), static_cast<int>((s + 1) * chunk),
+                                       static_cast<int>(s));
+    off_full += f;
+    if (t % chunk != 0) {
+      const uint64_t r = static_cast<uint64_t>(t % chunk);
+      keys[off_rem++] = ((0x7FFFFFFFull - r) << 32) | static_cast<uint64_t>(b);
+    }
+  }
+  for (int i = static_cast<int>(rem_total) + tid; i < sort_n; i += kPlanThreads) keys[i] = ~0ull;
+  __syncthreads();
+  // bitonic sort of sort_n (a power of two) keys, ascending
+  for (int k = 2; k <= sort_n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < sort_n; i += kPlanThreads) {
+        const int p = i ^ j;
+        if (p > i) {
+          const uint64_t a = keys[i], c = keys[p];
+          const bool up = (i & k) == 0;
+          if ((a > c) == up) {
+            keys[i] = c;
+            keys[p] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (fits) {
+    for (int i = tid; i < rem_total; i += kPlanThreads) {
+      const int b = static_cast<int>(keys[i] & 0xFFFFFFFFull);
+      const int64_t t = tiles[b];
+      const int64_t s = t / chunk;  // the last split slot
+      work[full_total + i] =
+          make_int4(b, static_cast<int>(s * chunk), static_cast<int>(t), static_cast<int>(s));
+    }
+    for (int64_t i = n_items + tid; i < pad_to; i += kPlanThreads) work[i] = make_int4(0, 0, 0, 0);
+  }
+}
+
+}  // namespace
+
+int plan_device_sort_n(int num_seqs) {
+  int n = 1;
+  while (n < num_seqs) n <<= 1;
+  return n;
+}
+
+size_t plan_device_smem_bytes(int num_seqs) {
+  return static_cast<size_t>(plan_device_sort_n(num_seqs)) * 8 + static_cast<size_t>(num_seqs) * 4;
+}
+
+cudaError_t launch_plan_device(const int32_t* seq_lens, int num_seqs, int64_t max_len, int64_t slots,
+                               int max_splits, int force_splits, int min_chunk, int pad_to, int4* work,
+                               int32_t* n_splits, int32_t* chunk_out, int32_t* status, cudaStream_t stream) {
+  const int sort_n = plan_device_sort_n(num_seqs);
+  const size_t smem = plan_device_smem_bytes(num_seqs);
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(plan_device_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  plan_device_kernel<<<1, kPlanThreads, smem, stream>>>(seq_lens, num_seqs, max_len, slots, max_splits, force_splits,
+                                                        min_chunk, pad_to, sort_n, work, n_splits, chunk_out, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mj

@@ -183,6 +183,21 @@ def test_pack_validation():
     assert L.mj_unpack_o(None, fake, 1, 2, 1, 2, 128, None) == mj.MJ_ERR_INVALID_ARG
 
 
+def test_plan_device_validation():
+    # refusals on the host, before any launch
+    L = mj.lib()
+    p = _params(4, h_r=4)
+    sl, work, ns = 1 << 20, 1 << 22, 1 << 24
+    f = L.mj_decode_plan_device
+    opts = lambda pad_to: mj.PlanOpts(152, 0, 0, 0, 0, pad_to)
+    assert f(ctypes.byref(p), None, sl, work, ns, None, None, None) == mj.MJ_ERR_INVALID_ARG
+    assert f(ctypes.byref(p), ctypes.byref(opts(0)), sl, work, ns, None, None, None) == mj.MJ_ERR_INVALID_ARG
+    assert f(ctypes.byref(p), ctypes.byref(opts(8)), None, work, ns, None, None, None) == mj.MJ_ERR_INVALID_ARG
+    assert f(ctypes.byref(p), ctypes.byref(opts(8)), sl, work + 4, ns, None, None, None) == mj.MJ_ERR_INVALID_ARG
+    big = _params(16385, h_r=4)
+    assert f(ctypes.byref(big), ctypes.byref(opts(8)), sl, work, ns, None, None, None) == mj.MJ_ERR_UNSUPPORTED
+
+
 def test_quantize_pack_validation():
     # every refusal happens on the host, before any launch
     L = mj.lib()
