@@ -321,6 +321,7 @@ def run_mj(args, rank, world, local_rank):
 
     launches = s.launches_per_step() * args.steps
     q_quant = q_quant_measure(w, dev, flush) if (w.q_is_e4m3 or args.q_quant) and rank == 0 else None
+    plan_dev = plan_device_measure(s, w, dev, flush) if rank == 0 else None
     e2e = None if args.no_e2e else e2e_measure(args, s, w, step_bytes, dev)
     clocks = clk.summary()
     return dict(
@@ -337,7 +338,39 @@ def run_mj(args, rank, world, local_rank):
         e2e=e2e,
         clocks=clocks,
         q_quant=q_quant,
+        plan_dev=plan_dev,
     )
+
+
+def plan_device_measure(s, w, dev, flush, launches: int = 200):
+    """The same plan built on the device (mj_decode_plan_device, the form a
+    captured graph replays), timed alone with CUDA events after an L2 flush;
+    checked equal to the host plan the steps used."""
+    import torch
+
+    import paged_fp8_kv_gb300 as mj
+
+    pad_to = max(1, w.num_seqs * s.max_splits)
+    work = torch.empty((pad_to, 4), dtype=torch.int32, device=dev)
+    ns = torch.empty((w.num_seqs,), dtype=torch.int32, device=dev)
+    o = s.plan.opts
+    kw = dict(sm_count=o.sm_count, ctas_per_sm=o.ctas_per_sm, n_q_tiles=o.n_q_tiles, min_chunk_tiles=o.min_chunk_tiles)
+    mj.decode_plan_device(s.params, s.seq_lens, work, ns, pad_to, **kw)
+    torch.cuda.synchronize()
+    same = bool(
+        np.array_equal(work[: s.plan.num_work].cpu().numpy(), s.plan.work)
+        and not work[s.plan.num_work :].any().item()
+        and np.array_equal(ns.cpu().numpy(), s.plan.n_splits)
+    )
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    for e0, e1 in evs:
+        flush.fill_(3)
+        e0.record()
+        mj.decode_plan_device(s.params, s.seq_lens, work, ns, pad_to, **kw)
+        e1.record()
+    torch.cuda.synchronize()
+    us = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs])) * 1e3
+    return {"us_per_launch": round(us, 2), "pad_to": pad_to, "equals_host_plan": same}
 
 
 def q_quant_measure(w, dev, flush, launches: int = 200):
@@ -582,6 +615,7 @@ def main():
             "e2e": r["e2e"],
             "gpu_launches": r["launches"],
             **({"q_quant": r["q_quant"]} if r["q_quant"] else {}),
+            **({"plan_device": r["plan_dev"]} if r["plan_dev"] else {}),
             "clocks": r["clocks"],
         }
         if w.q_len * w.h_r >= 128:
