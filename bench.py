@@ -344,8 +344,10 @@ def run_mj(args, rank, world, local_rank):
 
 def plan_device_measure(s, w, dev, flush, launches: int = 200):
     """The same plan built on the device (mj_decode_plan_device, the form a
-    captured graph replays), timed alone with CUDA events after an L2 flush;
-    checked equal to the host plan the steps used."""
+    captured graph replays): checked equal to the host plan the steps used,
+    timed alone with CUDA events after an L2 flush, and as the extra cost
+    in a graph step: replays of (device plan, decode, merge) against
+    (decode, merge) on the host plan's work list."""
     import torch
 
     import paged_fp8_kv_gb300 as mj
@@ -362,53 +364,61 @@ def plan_device_measure(s, w, dev, flush, launches: int = 200):
         and not work[s.plan.num_work :].any().item()
         and np.array_equal(ns.cpu().numpy(), s.plan.n_splits)
     )
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
-    for e0, e1 in evs:
-        flush.fill_(3)
-        e0.record()
-        mj.decode_plan_device(s.params, s.seq_lens, work, ns, pad_to, **kw)
-        e1.record()
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for e0, e1 in evs:
+            flush.fill_(3)
+            e0.record()
+            fn()
+            e1.record()
+        torch.cuda.synchronize()
+        return float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs])) * 1e3
+
+    us = timed(lambda: mj.decode_plan_device(s.params, s.seq_lens, work, ns, pad_to, **kw), launches)
+
+    def decode(work_t, max_n, stream):
+        mj.decode_attn(
+            s.params,
+            q=s.q_packed,
+            k_cache=s.k_cache,
+            v_cache=s.v_cache,
+            block_table=s.block_table,
+            seq_lens=s.seq_lens,
+            work=work_t,
+            n_splits=ns,
+            q_descale=s.q_descale,
+            k_descale=s.k_descale,
+            v_descale=s.v_descale,
+            o=s.o_packed,
+            lse=s.lse,
+            workspace=s.workspace,
+            softmax_scale=w.softmax_scale,
+            scale_o=w.scale_o,
+            max_n_splits=max_n,
+            stream=stream,
+        )
+
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    g_host, g_dev = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_host, stream=cs):
+        decode(s.work, s.plan.max_n_splits, cs)
+    with torch.cuda.graph(g_dev, stream=cs):
+        mj.decode_plan_device(s.params, s.seq_lens, work, ns, pad_to, stream=cs, **kw)
+        decode(work, s.max_splits, cs)
     torch.cuda.synchronize()
-    us = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs])) * 1e3
-    return {"us_per_launch": round(us, 2), "pad_to": pad_to, "equals_host_plan": same}
-
-
-def q_quant_measure(w, dev, flush, launches: int = 200):
-    """The upstream fp8 step for this workload's query shape: bf16 Q in
-    vLLM's layout -> e4m3 packed rows and per-(sequence, kv head)
-    descales, one fused launch (mj_quantize_pack_q), timed alone with CUDA
-    events after an L2 flush.  Bytes: bf16 Q read once, codes and descales
-    written."""
-    import torch
-
-    from paged_fp8_kv_gb300 import quantize_pack_q
-
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1234)
-    q = torch.randn((w.num_seqs * w.q_len, w.h_q, w.head_dim), generator=gen, device=dev).to(torch.bfloat16)
-    q8 = torch.empty((w.num_seqs, w.h_k, w.n_q, w.head_dim), dtype=torch.uint8, device=dev)
-    ds = torch.empty((w.num_seqs, w.h_k), dtype=torch.float32, device=dev)
-    for _ in range(3):
-        quantize_pack_q(q, q8, ds, w.num_seqs, w.q_len, w.h_k, w.h_r)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
-    torch.cuda.synchronize()
-    for e0, e1 in evs:
-        flush.fill_(7)
-        e0.record()
-        quantize_pack_q(q, q8, ds, w.num_seqs, w.q_len, w.h_k, w.h_r)
-        e1.record()
-    torch.cuda.synchronize()
-    us = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs])) * 1e3
-    nbytes = q.numel() * 2 + q8.numel() + ds.numel() * 4
-    peak, _ = measured_peaks()
-    gbs = nbytes / (us * 1e-6) / 1e9
+    for g in (g_host, g_dev):
+        for _ in range(3):
+            g.replay()
+    t_host = timed(g_host.replay, 100)
+    t_dev = timed(g_dev.replay, 100)
     return {
-        "kernel": "quantize_pack_q",
-        "shape": f"({w.num_seqs * w.q_len}, {w.h_q}, {w.head_dim}) bf16 -> ({w.num_seqs}, {w.h_k}, {w.n_q}, {w.head_dim}) e4m3",
         "us_per_launch": round(us, 2),
-        "bytes_per_launch": int(nbytes),
-        "achieved_gbs": round(gbs, 1),
-        "frac_of_hbm": round(gbs / peak, 4),
+        "pad_to": pad_to,
+        "equals_host_plan": same,
+        "graph_step_us_host_plan": round(t_host, 2),
+        "graph_step_us_device_plan": round(t_dev, 2),
     }
 
 

@@ -15,8 +15,8 @@
 //   items (b, s*chunk, min(T_b, (s+1)*chunk), s), ordered by length, longest
 //   first, equal lengths in (b, s) order; then (0, 0, 0, 0) up to pad_to.
 //
-// One CTA of 1024 threads.  The tile counts sit in shared memory; the
-// bisection's chunk totals are block reductions.  Every item of length
+// One CTA of 256 threads.  The tile counts sit in shared memory; the chunk
+// comes from an 8-way search (each warp sums the chunk count of one probe).  Every item of length
 // `chunk` precedes every shorter one, and those full-length items are
 // placed in (b, s) order by a prefix sum of floor(T_b / chunk).  The rest
 // (at most one item per sequence, of length T_b mod chunk) are ordered by a
@@ -35,33 +35,24 @@
 namespace mj {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
+constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kTileRowsDev = 128;
 constexpr int kStatusInvalid = 1;   // MJ_ERR_INVALID_ARG
 constexpr int kStatusCapacity = 3;  // MJ_ERR_CAPACITY
 
 __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
-__device__ __forceinline__ int64_t block_sum(int64_t v, int64_t* red) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  __syncthreads();  // red is free
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int64_t s = 0;
-  for (int w = 0; w < kPlanThreads / 32; ++w) s += red[w];
-  return s;
-}
-
-__device__ __forceinline__ int64_t block_max(int64_t v, int64_t* red) {
+__device__ __forceinline__ int64_t warp_max(int64_t v) {
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) v = max64(v, __shfl_xor_sync(0xffffffffu, v, off));
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int64_t m = red[0];
-  for (int w = 1; w < kPlanThreads / 32; ++w) m = max64(m, red[w]);
-  return m;
+  return v;
+}
+
+__device__ __forceinline__ int64_t warp_sum(int64_t v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
@@ -70,13 +61,14 @@ __global__ void __launch_bounds__(kPlanThreads)
                        int4* __restrict__ work, int32_t* __restrict__ n_splits, int32_t* __restrict__ chunk_out,
                        int32_t* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);                // [sort_n]
-  int32_t* tiles = reinterpret_cast<int32_t*>(keys + sort_n);            // [num_seqs]
-  __shared__ int64_t red[kPlanThreads / 32];
-  __shared__ int64_t scan[kPlanThreads];
-  const int tid = threadIdx.x;
+  uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);      // [sort_n]
+  int32_t* tiles = reinterpret_cast<int32_t*>(keys + sort_n);  // [num_seqs]
+  __shared__ int64_t red_a[kPlanWarps], red_b[kPlanWarps];
+  __shared__ int64_t probe[kPlanWarps];
+  __shared__ int ok[kPlanWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // tile counts, longest
+  // tile counts; the longest and whether a length was out of range
   int64_t bad = 0, longest = 1;
   for (int b = tid; b < num_seqs; b += kPlanThreads) {
     int64_t L = seq_lens[b];
@@ -88,10 +80,24 @@ __global__ void __launch_bounds__(kPlanThreads)
     tiles[b] = static_cast<int32_t>(t);
     longest = max64(longest, t);
   }
-  longest = block_max(longest, red);
-  bad = block_max(bad, red);
+  longest = warp_max(longest);
+  bad = warp_max(bad);
+  if (lane == 0) {
+    red_a[warp] = longest;
+    red_b[warp] = bad;
+  }
+  __syncthreads();  // also publishes tiles[]
+  longest = red_a[0];
+  bad = red_b[0];
+  for (int v = 1; v < kPlanWarps; ++v) {
+    longest = max64(longest, red_a[v]);
+    bad = max64(bad, red_b[v]);
+  }
 
-  // chunk
+  // chunk.  The least c in [lo, hi] with sum_b ceil(T_b / c) <= slots (a
+  // non-increasing function of c, within bound at hi) by an 8-way search:
+  // each warp evaluates one probe, the first probe within bound becomes hi
+  // and the one before it, plus one, lo.
   const int64_t floor_c = max64(min_chunk, (longest + max_splits - 1) / max_splits);
   int64_t chunk;
   if (force_splits > 0) {
@@ -100,22 +106,34 @@ __global__ void __launch_bounds__(kPlanThreads)
     chunk = longest;
   } else {
     int64_t lo = floor_c, hi = max64(floor_c, longest);
-    while (lo < hi) {  // uniform over the block: lo, hi come from block reductions
-      const int64_t mid = lo + (hi - lo) / 2;
+    while (lo < hi) {  // lo, hi uniform over the block
+      const int64_t p = lo + ((hi - lo) * (warp + 1)) / (kPlanWarps + 1);  // in [lo, hi)
       int64_t part = 0;
-      for (int b = tid; b < num_seqs; b += kPlanThreads) part += (tiles[b] + mid - 1) / mid;
-      if (block_sum(part, red) <= slots)
-        hi = mid;
-      else
-        lo = mid + 1;
+      for (int b = lane; b < num_seqs; b += 32) part += (tiles[b] + p - 1) / p;
+      part = warp_sum(part);
+      __syncthreads();  // the previous round's probes are read
+      if (lane == 0) {
+        probe[warp] = p;
+        ok[warp] = part <= slots;
+      }
+      __syncthreads();
+      int first = kPlanWarps;
+      for (int v = kPlanWarps - 1; v >= 0; --v)
+        if (ok[v]) first = v;
+      if (first < kPlanWarps) {
+        hi = probe[first];
+        if (first > 0) lo = probe[first - 1] + 1;
+      } else {
+        lo = probe[kPlanWarps - 1] + 1;
+      }
     }
     chunk = lo;
   }
 
-  // per sequence: splits, full-length chunks (contiguous runs of sequences
-  // per thread, so the prefix sum keeps b order)
+  // per sequence: splits, full-length chunks and remainders (contiguous runs
+  // of sequences per thread, so the prefix sums keep b order)
   const int per = (num_seqs + kPlanThreads - 1) / kPlanThreads;
-  const int b0 = tid * per, b1 = min(num_seqs, b0 + per);
+  const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
   int64_t my_full = 0, my_rem = 0, over = 0;
   for (int b = b0; b < b1; ++b) {
     const int64_t t = tiles[b];
@@ -125,30 +143,37 @@ __global__ void __launch_bounds__(kPlanThreads)
     my_full += t / chunk;
     my_rem += (t % chunk) != 0;
   }
-  // exclusive scans of the full-item and remainder counts over threads
-  scan[tid] = my_full;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const int64_t v = tid >= off ? scan[tid - off] : 0;
-    __syncthreads();
-    scan[tid] += v;
-    __syncthreads();
+  // exclusive scans of both counts over the threads: within warps by
+  // shuffles, then over the warps' totals
+  int64_t inc_f = my_full, inc_r = my_rem;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t f = __shfl_up_sync(0xffffffffu, inc_f, off);
+    const int64_t r = __shfl_up_sync(0xffffffffu, inc_r, off);
+    if (lane >= off) {
+      inc_f += f;
+      inc_r += r;
+    }
   }
-  const int64_t full_total = scan[kPlanThreads - 1];
-  int64_t off_full = scan[tid] - my_full;
-  __syncthreads();
-  scan[tid] = my_rem;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const int64_t v = tid >= off ? scan[tid - off] : 0;
-    __syncthreads();
-    scan[tid] += v;
-    __syncthreads();
+  over = warp_max(over);
+  __syncthreads();  // red_a / red_b are read
+  if (lane == 31) {
+    red_a[warp] = inc_f;
+    red_b[warp] = inc_r;
   }
-  const int64_t rem_total = scan[kPlanThreads - 1];
-  int64_t off_rem = scan[tid] - my_rem;
+  if (lane == 0) probe[warp] = over;
   __syncthreads();
-  over = block_max(over, red);
+  int64_t off_full = inc_f - my_full, off_rem = inc_r - my_rem;
+  int64_t full_total = 0, rem_total = 0;
+  for (int v = 0; v < kPlanWarps; ++v) {
+    if (v < warp) {
+      off_full += red_a[v];
+      off_rem += red_b[v];
+    }
+    full_total += red_a[v];
+    rem_total += red_b[v];
+    over = max64(over, probe[v]);
+  }
   const int64_t n_items = full_total + rem_total;
   const bool fits = n_items <= pad_to;
   if (tid == 0) {
@@ -178,13 +203,13 @@ __global__ void __launch_bounds__(kPlanThreads)
   for (int k = 2; k <= sort_n; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
       for (int i = tid; i < sort_n; i += kPlanThreads) {
-        const int p = i ^ j;
-        if (p > i) {
-          const uint64_t a = keys[i], c = keys[p];
+        const int q = i ^ j;
+        if (q > i) {
+          const uint64_t x = keys[i], y = keys[q];
           const bool up = (i & k) == 0;
-          if ((a > c) == up) {
-            keys[i] = c;
-            keys[p] = a;
+          if ((x > y) == up) {
+            keys[i] = y;
+            keys[q] = x;
           }
         }
       }
