@@ -352,11 +352,11 @@ def plan_device_measure(s, w, dev, flush, launches: int = 200):
 
     import paged_fp8_kv_gb300 as mj
 
-    pad_to = max(1, w.num_seqs * s.max_splits)
-    work = torch.empty((pad_to, 4), dtype=torch.int32, device=dev)
-    ns = torch.empty((w.num_seqs,), dtype=torch.int32, device=dev)
     o = s.plan.opts
     kw = dict(sm_count=o.sm_count, ctas_per_sm=o.ctas_per_sm, n_q_tiles=o.n_q_tiles, min_chunk_tiles=o.min_chunk_tiles)
+    pad_to = mj.decode_plan_max_items(s.params, **kw)  # the tightest fixed length
+    work = torch.empty((pad_to, 4), dtype=torch.int32, device=dev)
+    ns = torch.empty((w.num_seqs,), dtype=torch.int32, device=dev)
     mj.decode_plan_device(s.params, s.seq_lens, work, ns, pad_to, **kw)
     torch.cuda.synchronize()
     same = bool(
@@ -419,6 +419,45 @@ def plan_device_measure(s, w, dev, flush, launches: int = 200):
         "equals_host_plan": same,
         "graph_step_us_host_plan": round(t_host, 2),
         "graph_step_us_device_plan": round(t_dev, 2),
+    }
+
+
+def q_quant_measure(w, dev, flush, launches: int = 200):
+    """The upstream fp8 step for this workload's query shape: bf16 Q in
+    vLLM's layout -> e4m3 packed rows and per-(sequence, kv head)
+    descales, one fused launch (mj_quantize_pack_q), timed alone with CUDA
+    events after an L2 flush.  Bytes: bf16 Q read once, codes and descales
+    written."""
+    import torch
+
+    from paged_fp8_kv_gb300 import quantize_pack_q
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    q = torch.randn((w.num_seqs * w.q_len, w.h_q, w.head_dim), generator=gen, device=dev).to(torch.bfloat16)
+    q8 = torch.empty((w.num_seqs, w.h_k, w.n_q, w.head_dim), dtype=torch.uint8, device=dev)
+    ds = torch.empty((w.num_seqs, w.h_k), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        quantize_pack_q(q, q8, ds, w.num_seqs, w.q_len, w.h_k, w.h_r)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush.fill_(7)
+        e0.record()
+        quantize_pack_q(q, q8, ds, w.num_seqs, w.q_len, w.h_k, w.h_r)
+        e1.record()
+    torch.cuda.synchronize()
+    us = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs])) * 1e3
+    nbytes = q.numel() * 2 + q8.numel() + ds.numel() * 4
+    peak, _ = measured_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {
+        "kernel": "quantize_pack_q",
+        "shape": f"({w.num_seqs * w.q_len}, {w.h_q}, {w.head_dim}) bf16 -> ({w.num_seqs}, {w.h_k}, {w.n_q}, {w.head_dim}) e4m3",
+        "us_per_launch": round(us, 2),
+        "bytes_per_launch": int(nbytes),
+        "achieved_gbs": round(gbs, 1),
+        "frac_of_hbm": round(gbs / peak, 4),
     }
 
 

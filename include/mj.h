@@ -283,6 +283,15 @@ mj_status mj_decode_plan_device(const mj_decode_params* params, mj_plan_opts* op
                                 int32_t* work_dev, int32_t* n_splits_dev, int32_t* chunk_tiles_dev,
                                 int32_t* status_dev, mj_stream_t stream);
 
+/* The most work items the plan rule makes for these params and options,
+ * whatever the sequence lengths (host only): with force_splits = 0 at most
+ * max(num_seqs, slots) (the rule splits only to fill one wave of slots),
+ * else num_seqs * min(force_splits, max_splits).  The tightest pad_to for
+ * mj_decode_plan_device: padding items are launched as CTAs that exit at
+ * once, so a loose pad_to costs launch time.  Fills opts' zero fields as
+ * mj_decode_plan_device does; returns -1 for invalid params or options. */
+int32_t mj_decode_plan_max_items(const mj_decode_params* params, mj_plan_opts* opts);
+
 /* Fused fp8 query quantisation and pack (source: `quantize_q_fp8` and
  * `pack_q`).  For every sequence b and kv head g the group is Q's q_len
  * tokens x h_r heads x d values of that kv head;

@@ -138,6 +138,8 @@ def lib() -> ctypes.CDLL:
         L.mj_decode_attn.argtypes = [P(DecodeParams), P(DecodeArgs), _vp]
         L.mj_pack_q.restype = ctypes.c_int
         L.mj_pack_q.argtypes = [_vp, _vp] + [ctypes.c_int32] * 6 + [_vp]
+        L.mj_decode_plan_max_items.restype = ctypes.c_int32
+        L.mj_decode_plan_max_items.argtypes = [_vp, _vp]
         L.mj_decode_plan_device.restype = ctypes.c_int
         L.mj_decode_plan_device.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.mj_quantize_pack_q.restype = ctypes.c_int
@@ -364,6 +366,22 @@ def pack_q(q_vllm, q_packed, num_seqs: int, q_len: int, h_k: int, h_r: int, stre
         _stream_handle(stream),
     )
     _check(st, "mj_pack_q")
+
+
+def decode_plan_max_items(
+    params: DecodeParams,
+    sm_count: int = 0,
+    ctas_per_sm: int = 0,
+    n_q_tiles: int = 0,
+    force_splits: int = 0,
+    min_chunk_tiles: int = 0,
+) -> int:
+    """mj_decode_plan_max_items: the tightest pad_to for the device plan."""
+    opts = PlanOpts(sm_count, ctas_per_sm, n_q_tiles, force_splits, min_chunk_tiles, 0)
+    n = int(lib().mj_decode_plan_max_items(ctypes.byref(params), ctypes.byref(opts)))
+    if n < 0:
+        raise MjError(MJ_ERR_INVALID_ARG, "mj_decode_plan_max_items")
+    return n
 
 
 def decode_plan_device(

@@ -297,6 +297,34 @@ extern "C" mj_status mj_pack_q(const void* q_vllm, void* q_packed, int32_t elem_
   return permute(q_vllm, q_packed, elem_bytes, num_seqs, q_len, h_k, h_r, head_dim, true, stream);
 }
 
+namespace {
+
+// Options as the device plan resolves them (0 -> the kernel's values, no model).
+void resolve_device_opts(const mj_decode_params& p, mj_plan_opts* opts) {
+  const KernelChoice kc = choose_kernel(p);
+  if (opts->sm_count == 0) opts->sm_count = kDefaultSmCount;
+  if (opts->ctas_per_sm == 0) opts->ctas_per_sm = kc.ctas_per_sm;
+  if (opts->n_q_tiles == 0) opts->n_q_tiles = kc.n_q_tiles;
+  if (opts->min_chunk_tiles == 0) opts->min_chunk_tiles = 1;
+}
+
+}  // namespace
+
+extern "C" int32_t mj_decode_plan_max_items(const mj_decode_params* params, mj_plan_opts* opts) {
+  if (check_params(params) != MJ_OK || !opts) return -1;
+  if (opts->sm_count < 0 || opts->ctas_per_sm < 0 || opts->n_q_tiles < 0 || opts->force_splits < 0 ||
+      opts->min_chunk_tiles < 0)
+    return -1;
+  resolve_device_opts(*params, opts);
+  const int64_t b = params->num_seqs;
+  if (opts->force_splits > 0) return static_cast<int32_t>(b * std::min(opts->force_splits, params->max_splits));
+  const int64_t slots = std::max<int64_t>(
+      1, static_cast<int64_t>(opts->sm_count) * opts->ctas_per_sm / (static_cast<int64_t>(params->h_k) * opts->n_q_tiles));
+  // one wave's slots bound the chunks whenever the rule splits; otherwise
+  // there is one item per sequence
+  return static_cast<int32_t>(std::min<int64_t>(b * params->max_splits, std::max(b, slots)));
+}
+
 extern "C" mj_status mj_decode_plan_device(const mj_decode_params* params, mj_plan_opts* opts,
                                            const int32_t* seq_lens_dev, int32_t* work_dev, int32_t* n_splits_dev,
                                            int32_t* chunk_tiles_dev, int32_t* status_dev, mj_stream_t stream) {
@@ -308,11 +336,7 @@ extern "C" mj_status mj_decode_plan_device(const mj_decode_params* params, mj_pl
       opts->min_chunk_tiles < 0 || opts->pad_to < 1)
     return MJ_ERR_INVALID_ARG;  // the work list has a fixed length: pad_to
   if (params->num_seqs > kMaxDevicePlanSeqs) return MJ_ERR_UNSUPPORTED;
-  const KernelChoice kc = choose_kernel(*params);
-  if (opts->sm_count == 0) opts->sm_count = kDefaultSmCount;
-  if (opts->ctas_per_sm == 0) opts->ctas_per_sm = kc.ctas_per_sm;
-  if (opts->n_q_tiles == 0) opts->n_q_tiles = kc.n_q_tiles;
-  if (opts->min_chunk_tiles == 0) opts->min_chunk_tiles = 1;
+  resolve_device_opts(*params, opts);
   const int64_t slots = std::max<int64_t>(
       1, static_cast<int64_t>(opts->sm_count) * opts->ctas_per_sm / (static_cast<int64_t>(params->h_k) * opts->n_q_tiles));
   const int64_t max_len = static_cast<int64_t>(params->max_blocks) * params->page_size;

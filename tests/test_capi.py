@@ -198,6 +198,26 @@ def test_plan_device_validation():
     assert f(ctypes.byref(big), ctypes.byref(opts(8)), sl, work, ns, None, None, None) == mj.MJ_ERR_UNSUPPORTED
 
 
+def test_plan_max_items_bounds_every_plan():
+    # the bound on the work list holds for the rule's plans, whatever the
+    # lengths; it is the tightest for an even batch that fills one wave
+    rng = np.random.default_rng(17)
+    for _ in range(300):
+        b = int(rng.integers(1, 400))
+        h_k = int(rng.choice([1, 2, 8]))
+        ms = int(rng.choice([1, 16, 256]))
+        p = _params(b, h_k=h_k, h_r=int(rng.choice([4, 16, 32])), max_splits=ms, max_blocks=4096)
+        cps = int(rng.choice([1, 3, 5, 24]))
+        force = int(rng.choice([0, 0, 3])) if ms > 1 else 0
+        lens = rng.integers(0, 4096 * 16 + 1, size=b).tolist()
+        if rng.random() < 0.3:
+            lens = [4096 * 16] * b
+        bound = mj.decode_plan_max_items(p, sm_count=152, ctas_per_sm=cps, force_splits=force)
+        plan = mj.decode_plan(p, lens, sm_count=152, ctas_per_sm=cps, force_splits=force)
+        assert plan.num_work <= bound
+    assert mj.lib().mj_decode_plan_max_items(None, None) == -1
+
+
 def test_quantize_pack_validation():
     # every refusal happens on the host, before any launch
     L = mj.lib()

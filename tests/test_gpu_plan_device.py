@@ -132,7 +132,7 @@ def test_graph_of_device_plan_and_decode_follows_changing_lengths(cfg, kw, kerne
     s = DecodeSession(w, kernel=kernel)
     s.step()  # packs Q (q_len > 1) into the buffer the graph's decode reads
     torch.cuda.synchronize()
-    pad_to = w.num_seqs * w.max_splits
+    pad_to = mj.decode_plan_max_items(s.params, sm_count=s.sm_count)
     work = torch.zeros((pad_to, 4), dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
