@@ -108,8 +108,10 @@ __global__ void __launch_bounds__(kPlanThreads)
     int64_t lo = floor_c, hi = max64(floor_c, longest);
     while (lo < hi) {  // lo, hi uniform over the block
       const int64_t p = lo + ((hi - lo) * (warp + 1)) / (kPlanWarps + 1);  // in [lo, hi)
+      // tile counts and chunks fit 32 bits (at most 2^30 / 128): 32-bit divisions
+      const uint32_t p32 = static_cast<uint32_t>(p);
       int64_t part = 0;
-      for (int b = lane; b < num_seqs; b += 32) part += (tiles[b] + p - 1) / p;
+      for (int b = lane; b < num_seqs; b += 32) part += (static_cast<uint32_t>(tiles[b]) + p32 - 1) / p32;
       part = warp_sum(part);
       __syncthreads();  // the previous round's probes are read
       if (lane == 0) {
@@ -134,14 +136,15 @@ __global__ void __launch_bounds__(kPlanThreads)
   // of sequences per thread, so the prefix sums keep b order)
   const int per = (num_seqs + kPlanThreads - 1) / kPlanThreads;
   const int b0 = min(num_seqs, tid * per), b1 = min(num_seqs, b0 + per);
+  const uint32_t c32 = static_cast<uint32_t>(chunk);
   int64_t my_full = 0, my_rem = 0, over = 0;
   for (int b = b0; b < b1; ++b) {
-    const int64_t t = tiles[b];
-    const int64_t k = (t + chunk - 1) / chunk;
-    if (k > max_splits) over = 1;
+    const uint32_t t = static_cast<uint32_t>(tiles[b]);
+    const uint32_t k = (t + c32 - 1) / c32;
+    if (k > static_cast<uint32_t>(max_splits)) over = 1;
     n_splits[b] = static_cast<int32_t>(k);
-    my_full += t / chunk;
-    my_rem += (t % chunk) != 0;
+    my_full += t / c32;
+    my_rem += (t % c32) != 0;
   }
   // exclusive scans of both counts over the threads: within warps by
   // shuffles, then over the warps' totals
@@ -185,17 +188,14 @@ __global__ void __launch_bounds__(kPlanThreads)
   // full-length items in (b, s) order; remainder keys: length descending,
   // then b ascending (unique, so any correct sort keeps generation order)
   for (int b = b0; b < b1; ++b) {
-    const int64_t t = tiles[b];
-    const int64_t f = t / chunk;
+    const uint32_t t = static_cast<uint32_t>(tiles[b]);
+    const uint32_t f = t / c32, r = t % c32;
     if (fits)
-      for (int64_t s = 0; s < f; ++s)
-        work[off_full + s] = make_int4(b, static_cast<int>(s * chunk), static_cast<int>((s + 1) * chunk),
+      for (uint32_t s = 0; s < f; ++s)
+        work[off_full + s] = make_int4(b, static_cast<int>(s * c32), static_cast<int>((s + 1) * c32),
                                        static_cast<int>(s));
     off_full += f;
-    if (t % chunk != 0) {
-      const uint64_t r = static_cast<uint64_t>(t % chunk);
-      keys[off_rem++] = ((0x7FFFFFFFull - r) << 32) | static_cast<uint64_t>(b);
-    }
+    if (r != 0) keys[off_rem++] = ((0x7FFFFFFFull - r) << 32) | static_cast<uint64_t>(b);
   }
   for (int i = static_cast<int>(rem_total) + tid; i < sort_n; i += kPlanThreads) keys[i] = ~0ull;
   __syncthreads();
@@ -219,10 +219,9 @@ __global__ void __launch_bounds__(kPlanThreads)
   if (fits) {
     for (int i = tid; i < rem_total; i += kPlanThreads) {
       const int b = static_cast<int>(keys[i] & 0xFFFFFFFFull);
-      const int64_t t = tiles[b];
-      const int64_t s = t / chunk;  // the last split slot
-      work[full_total + i] =
-          make_int4(b, static_cast<int>(s * chunk), static_cast<int>(t), static_cast<int>(s));
+      const uint32_t t = static_cast<uint32_t>(tiles[b]);
+      const uint32_t s = t / c32;  // the last split slot
+      work[full_total + i] = make_int4(b, static_cast<int>(s * c32), static_cast<int>(t), static_cast<int>(s));
     }
     for (int64_t i = n_items + tid; i < pad_to; i += kPlanThreads) work[i] = make_int4(0, 0, 0, 0);
   }
