@@ -31,10 +31,11 @@
 namespace mj {
 namespace {
 
-constexpr int kPer = 16;      // splits per warp
 constexpr int kCtaWarps = 4;  // warps per CTA when a row needs fewer
 
-template <int kWPR>
+// kWPR warps per row, each staging up to kPer splits (4, 8 or 16: the
+// staging area, kPer x 512 B a warp, sets how many CTAs fit an SM)
+template <int kWPR, int kPer>
 __global__ void __launch_bounds__((kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32) merge_kernel(const DecodeDev a) {
   constexpr int kRowsPerCta = kWPR >= kCtaWarps ? 1 : kCtaWarps / kWPR;
   const int lane = threadIdx.x & 31;
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__((kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32) me
   if (lane == 0) a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + n] = mx + logf(lsum);
 }
 
-template <int kWPR>
+template <int kWPR, int kPer>
 cudaError_t launch_merge_t(const DecodeDev& a, cudaStream_t stream) {
   constexpr int kRowsPerCta = kWPR >= kCtaWarps ? 1 : kCtaWarps / kWPR;
   constexpr int kThreads = (kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32;
@@ -138,9 +139,9 @@ cudaError_t launch_merge_t(const DecodeDev& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kThreads / 32 * kPer * 32 * 16;  // the staging area: 8 KB a warp
+  cfg.dynamicSmemBytes = kThreads / 32 * kPer * 32 * 16;  // the staging area: kPer x 512 B a warp
   if (cfg.dynamicSmemBytes > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(merge_kernel<kWPR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(merge_kernel<kWPR, kPer>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(cfg.dynamicSmemBytes));
     if (e != cudaSuccess) return e;
   }
@@ -150,15 +151,17 @@ cudaError_t launch_merge_t(const DecodeDev& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<kWPR>, a);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<kWPR, kPer>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const DecodeDev& a, int max_n_splits, cudaStream_t stream) {
-  if (max_n_splits <= kPer) return launch_merge_t<1>(a, stream);
-  if (max_n_splits <= 4 * kPer) return launch_merge_t<4>(a, stream);
-  return launch_merge_t<16>(a, stream);
+  if (max_n_splits <= 4) return launch_merge_t<1, 4>(a, stream);
+  if (max_n_splits <= 8) return launch_merge_t<1, 8>(a, stream);
+  if (max_n_splits <= 16) return launch_merge_t<1, 16>(a, stream);
+  if (max_n_splits <= 64) return launch_merge_t<4, 16>(a, stream);
+  return launch_merge_t<16, 16>(a, stream);
 }
 
 }  // namespace mj
