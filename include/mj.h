@@ -80,8 +80,8 @@ typedef enum { MJ_BF16 = 0, MJ_E4M3 = 1 } mj_dtype;
  *               the tensor-core kernels' K/V tile loads carry an L2
  *               EVICT_FIRST cache policy (KV is read once; source: the
  *               kernel's `kv_evict_first` option on the
- *               "mjolnir/t5_decode.py" page); 0 = library default,
- *               -1 = off, 1 = on */
+ *               "mjolnir/t5_decode.py" page); 0 = library default (on),
+ *               -1 = off, 1 = on; results are identical either way */
 typedef struct {
   int32_t num_seqs, q_len, h_k, h_r, head_dim, page_size;
   int32_t max_blocks, num_pages, causal, q_dtype, max_splits, kernel;
