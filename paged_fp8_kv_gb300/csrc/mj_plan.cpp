@@ -175,8 +175,9 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
   // merge.  Model: time = max(bytes / bandwidth, longest slot of a greedy
   // longest-first assignment x time per tile of a CTA) + the merge.
   // (Measured on the GQA decode workload, 64 sequences of 512-8192 keys,
-  // 8 kv heads: 3, 4, 5, 6, 8, 12 slots per SM give 124.9, 122.9, 116.7,
-  // 124.9, 120.8, 120.8 us per step; the model picks 5.)
+  // 8 kv heads, with a two-stage instance at three CTAs per SM: 3, 4, 5, 6,
+  // 8, 12 slots per SM gave 124.9, 122.9, 116.7, 124.9, 120.8, 120.8 us per
+  // step and the model picked 5.)
   if (default_cps && opts->force_splits == 0 && params->max_splits > 1 &&
       kc.kind != KernelKind::kTensorCoreGrouped) {
     const int64_t units_per_item = static_cast<int64_t>(params->h_k) * opts->n_q_tiles;
