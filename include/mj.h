@@ -98,11 +98,12 @@ typedef struct {
  *                          one CTA per kv head
  *   MJ_KERNEL_TENSOR_CORE_GROUPED
  *                          the same arithmetic, persistent, with one CTA per
- *                          group of 8, 4 or 2 kv heads, whose rows of each
- *                          page it reads together: 8 heads for
+ *                          SM taking units of 8, 4, 2 or 1 kv heads, whose
+ *                          rows of each page it reads together: 8 heads for
  *                          q_len*h_r <= 4 (h_k a multiple of 8), 4 for <= 8
- *                          (h_k a multiple of 4), 2 for <= 32 (h_k even);
- *                          MJ_ERR_UNSUPPORTED otherwise
+ *                          (h_k a multiple of 4), 2 for <= 32 (h_k even),
+ *                          1 for <= 32 (any h_k); MJ_ERR_UNSUPPORTED above
+ *                          32 rows
  *   MJ_KERNEL_TENSOR_CORE_QROWS
  *                          tcgen05 kernel with 128 query rows on the MMA's M
  *                          and 128 keys on N: one read of the KV per q tile
