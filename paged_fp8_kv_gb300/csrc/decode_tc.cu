@@ -123,12 +123,12 @@ template <int R, bool kQe4m3>
 struct TcCfg {
   static constexpr int kN1 = kQe4m3 ? (R < 16 ? 16 : R) : 2 * R;
   static constexpr int kN2 = 2 * R;
-  // 16 rows of e4m3 Q (the fully-fp8 path) and 8 rows of bf16 Q: three
-  // stages at two CTAs per SM instead of two at three; a CTA then keeps a
-  // third more of its sequence in flight (GQA decode: the long sequences
-  // need no split, 109.8 -> 108.6 us a step), and short split chunks have
-  // most of their tiles in flight at once
-  static constexpr bool kDeep16 = (kQe4m3 && R == 16) || (!kQe4m3 && R == 8);
+  // 16 rows and 8 rows of bf16 Q: three stages at two CTAs per SM instead
+  // of two at three; a CTA then keeps a third more of its sequence in
+  // flight (GQA decode: the long sequences need no split, 109.8 -> 108.6
+  // us a step; sweep N = 16: 384 -> 256 work items, 101.6 -> 98.7 us), and
+  // short split chunks have most of their tiles in flight at once
+  static constexpr bool kDeep16 = R == 16 || (!kQe4m3 && R == 8);
   static constexpr int kStages = kDeep16 ? 3 : (R <= 32 ? 2 : 5);
   static constexpr int kMinBlocks = kDeep16 ? 2 : (R <= 16 ? 3 : (R <= 32 ? 2 : 1));
   // two P buffers let the softmax of tile i write while GEMM2(i-1) still
