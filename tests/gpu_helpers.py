@@ -7,7 +7,8 @@ import numpy as np
 
 import oracle
 
-# Tolerances of the spec contract: bf16 Q path and fully-fp8 path.
+# Parity tolerances, |o - ref| <= atol + rtol |ref| and |lse - ref| <= LSE_TOL:
+# bf16 Q (hi + lo e4m3 parts) and the fully-fp8 path (e4m3 Q and P).
 O_TOL_BF16 = (2e-2, 2e-2)
 O_TOL_FP8 = (5e-2, 5e-2)
 LSE_TOL = 2e-3
