@@ -1,0 +1,74 @@
+"""CPU checks of the benchmark's bookkeeping: the algorithmic bytes and flops
+of a step (worked by hand for the tiny reference workload) and the rule
+that a recorded DRAM traffic figure is reported only for the kernel source
+it was measured on."""
+
+import hashlib
+import json
+import os
+
+import pytest
+
+import bench
+import paged_fp8_kv_gb300 as mj
+from paged_fp8_kv_gb300 import synthetic as syn
+
+
+def tiny_plan(w):
+    p = mj.make_params(
+        w.num_seqs, w.q_len, w.h_k, w.h_r, w.page_size, w.max_blocks, w.num_pages, bool(w.causal),
+        mj.MJ_BF16, w.max_splits, w.head_dim, 0, 0,
+    )
+    return mj.decode_plan(p, w.seq_lens, sm_count=152)
+
+
+def test_algorithmic_bytes_by_hand():
+    # tiny reference: 2 sequences of 37 and 100 keys, 1 kv head, 8 rows,
+    # d = 128, pages of 16 rows, bf16 Q, nothing split
+    w = syn.config(1)
+    plan = tiny_plan(w)
+    decode, merge, step = bench.algorithmic_bytes(w, plan)
+    kv = (37 + 100) * 1 * 128 * 2  # K and V, one byte each
+    q = o = 2 * 1 * 8 * 128 * 2  # bf16 Q in, bf16 O out
+    lse = 2 * 1 * 8 * 4
+    block_table = (3 + 7) * 4  # ceil(37 / 16) + ceil(100 / 16) entries
+    meta = plan.num_work * 16 + 2 * 8 + 3 * 2 * 1 * 4  # work items, n_splits + seq_lens, 3 descales
+    assert plan.num_work == 2
+    assert decode == kv + q + o + lse + block_table + meta
+    assert merge == 0
+    assert step == decode
+
+
+def test_algorithmic_flops_by_hand():
+    # every visible (key, row) pair costs 2 d for S and 2 d for O
+    w = syn.config(1)
+    assert bench.algorithmic_flops(w) == 4 * 128 * 8 * (37 + 100)
+    # causal tail with 4 query tokens: token qi sees L - 4 + qi + 1 keys
+    w4 = syn.config(4, num_seqs=2, len_range=(10, 20))
+    vis = sum(sum(int(L) - 4 + qi + 1 for qi in range(4)) for L in w4.seq_lens)
+    assert bench.algorithmic_flops(w4) == 4 * 128 * w4.h_k * w4.h_r * vis
+
+
+def test_traffic_record_follows_the_source(tmp_path, monkeypatch):
+    src = "pack.cu"
+    path = os.path.join(bench.ROOT, "paged_fp8_kv_gb300", "csrc", src)
+    sha = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    rec = {
+        "k_current": {"wl": {"source": src, "source_sha": sha, "dram_bytes_per_launch": 12345}},
+        "k_stale": {"wl": {"source": src, "source_sha": "0" * 16, "dram_bytes_per_launch": 999}},
+    }
+    (tmp_path / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    assert bench.traffic_record("k_current", "wl") == 12345
+    assert bench.traffic_record("k_stale", "wl") is None
+    assert bench.traffic_record("k_current", "other") is None
+    assert bench.traffic_record("unknown", "wl") is None
+
+
+@pytest.mark.parametrize("name", ["tc_r8_bf16", "tcg_g2r32_bf16", "qm_r32_bf16", "qm_r64_bf16", "tc_r16_e4m3"])
+def test_committed_traffic_records_name_existing_sources(name):
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    for wl, e in rec[name].items():
+        assert os.path.exists(os.path.join(bench.ROOT, "paged_fp8_kv_gb300", "csrc", e["source"]))
+        assert e["dram_bytes_per_launch"] > 0 and len(e["source_sha"]) == 16
+        assert "ncu" in e["command"] and "--clock-control none" in e["command"]
