@@ -294,3 +294,12 @@ def test_kv_evict_first_leaves_results_unchanged(cfg, kw, kernel):
     b = run(w, kernel=kernel, kv_evict_first=1)
     assert torch.equal(a.o_packed, b.o_packed) and torch.equal(a.lse, b.lse)
     compare(w, b.o_host(), b.lse_host())
+
+
+@pytest.mark.parametrize("splits,lo,hi", [(3, 2, 4), (6, 5, 8), (12, 9, 16), (40, 17, 64), (100, 65, 128)])
+def test_merge_instances_by_split_count(splits, lo, hi):
+    # the merge stages 4, 8 or 16 splits a warp and spreads a row over 1, 4
+    # or 16 warps by the largest split count: each instance against the oracle
+    w = syn.config(2, num_seqs=3, len_range=(25600, 26000), max_splits=128)
+    s, _ = check(w, force_splits=splits)
+    assert lo <= s.plan.max_n_splits <= hi
