@@ -14,6 +14,9 @@ arithmetic.
 * ``layout_ref.py`` - the query / output row permutation.
 * ``quant_ref.py`` - the per-(sequence, kv head) fp8 query quantisation
   fused with the pack, with its own e4m3 encoder.
+* ``narrow_ref.py`` - the narrow KV formats (fp6 e3m2 / e2m3, fp4 e2m1):
+  value tables, the page's quantiser and bit packing, and their exact e4m3
+  view for the attention oracle.
 
 Every function here is pinned by ``tests/test_oracle.py`` against facts the
 source pages and mathematics fix (see that file's docstring).
