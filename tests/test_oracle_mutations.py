@@ -1,0 +1,101 @@
+"""Planted mistakes in copies of the oracle's Q quantisation and narrow-format
+modules: each plausible slip (a tie rule, a saturation bound, a bias, a
+subnormal step, a sign bit, a packing shift, an index order, a reduction
+axis) must make one of the pins of tests/test_quant_ref.py or
+tests/test_narrow_ref.py fail; the shipped modules pass them.  CPU only;
+the mutated copies live in a temporary directory."""
+
+import importlib.util
+import os
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ORACLE_DIR = os.path.dirname(os.path.abspath(oracle.__file__))
+
+
+def load(path, name, tmp_path, old=None, new=None):
+    src = open(path).read()
+    if old is not None:
+        assert old in src, f"mutation anchor missing: {old!r}"
+        src = src.replace(old, new, 1)
+    src = src.replace("from .layout_ref import", "from oracle.layout_ref import")
+    f = tmp_path / f"{name}.py"
+    f.write_text(src)
+    spec = importlib.util.spec_from_file_location(name, str(f))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+# ------------------------------------------------------- Q quantisation
+
+
+def pins_hold(all_pins, m) -> bool:
+    """The pin files' own checks, run against module m."""
+    try:
+        all_pins(m)
+        return True
+    except Exception:
+        return False
+
+
+def quant_pins_hold(m) -> bool:
+    from tests.test_quant_ref import all_pins
+
+    return pins_hold(all_pins, m)
+
+
+QUANT_MUTATIONS = [
+    ("ties away from zero", "(frac > 0.5 or (frac == 0.5 and int(lo) % 2 == 1))", "(frac >= 0.5)"),
+    ("saturates to NaN", "res[i] = sign | 0x7E  # saturate", "res[i] = sign | 0x7F  # saturate"),
+    ("wrong largest value", "E4M3_MAX = 448.0", "E4M3_MAX = 240.0"),
+    ("subnormal step", "step = 2.0**-9", "step = 2.0**-10"),
+    ("sign bit dropped", "res[i] = sign | _code_of_magnitude(mag)", "res[i] = _code_of_magnitude(mag)"),
+    ("amax over tokens only", "axis=(1, 3, 4)", "axis=(1, 4)"),
+    ("no amax floor", "amax = np.maximum(amax, AMAX_FLOOR)", "amax = amax"),
+    ("pack order", "return pack_q_ref(codes, num_seqs, q_len, h_k, h_r), descale", "return pack_q_ref(codes, num_seqs, q_len, h_r, h_k), descale"),
+    ("exponent off by one", "step = 2.0 ** (e - 3)", "step = 2.0 ** (e - 2)"),
+]
+
+
+def test_quant_module_passes_its_pins(tmp_path):
+    assert quant_pins_hold(load(os.path.join(ORACLE_DIR, "quant_ref.py"), "quant_ok", tmp_path))
+
+
+@pytest.mark.parametrize("label,old,new", QUANT_MUTATIONS, ids=[m[0] for m in QUANT_MUTATIONS])
+def test_quant_planted_mistake_is_caught(label, old, new, tmp_path):
+    m = load(os.path.join(ORACLE_DIR, "quant_ref.py"), "quant_mut", tmp_path, old, new)
+    assert not quant_pins_hold(m), f"no pin caught: {label}"
+
+
+# ---------------------------------------------------------- narrow formats
+
+
+def narrow_pins_hold(m) -> bool:
+    from tests.test_narrow_ref import all_pins
+
+    return pins_hold(all_pins, m)
+
+
+NARROW_MUTATIONS = [
+    ("e2m3 bias", '"e2m3": (2, 3, 1)', '"e2m3": (2, 3, 2)'),
+    ("subnormal binade", "mag = (m / (1 << mb)) * 2.0 ** (1 - bias)", "mag = (m / (1 << mb)) * 2.0 ** (-bias)"),
+    ("tie to the larger", "mag = lo if (a - pos[lo]) <= (pos[hi] - a) else hi", "mag = lo if (a - pos[lo]) < (pos[hi] - a) else hi"),
+    ("negative zero", "neg = v < 0 and pos[mag] > 0", "neg = v < 0"),
+    ("nibble order", "return (c[..., 0] | (c[..., 1] << np.uint64(4))).astype(np.uint8)", "return (c[..., 1] | (c[..., 0] << np.uint64(4))).astype(np.uint8)"),
+    ("fp6 shift", "(c[..., 1] << np.uint64(6))", "(c[..., 1] << np.uint64(5))"),
+    ("mantissa width", '"e3m2": (3, 2, 3)', '"e3m2": (2, 3, 3)'),
+]
+
+
+def test_narrow_module_passes_its_pins(tmp_path):
+    assert narrow_pins_hold(load(os.path.join(ORACLE_DIR, "narrow_ref.py"), "narrow_ok", tmp_path))
+
+
+@pytest.mark.parametrize("label,old,new", NARROW_MUTATIONS, ids=[m[0] for m in NARROW_MUTATIONS])
+def test_narrow_planted_mistake_is_caught(label, old, new, tmp_path):
+    m = load(os.path.join(ORACLE_DIR, "narrow_ref.py"), "narrow_mut", tmp_path, old, new)
+    assert not narrow_pins_hold(m), f"no pin caught: {label}"
