@@ -293,6 +293,24 @@ mj_status mj_decode_plan_device(const mj_decode_params* params, mj_plan_opts* op
  * mj_decode_plan_device does; returns -1 for invalid params or options. */
 int32_t mj_decode_plan_max_items(const mj_decode_params* params, mj_plan_opts* opts);
 
+/* Verification hooks (not needed to compute anything): the decode path's
+ * page gather and the CUDA-core kernel's e4m3 conversion as standalone
+ * launches, for byte- and bit-exact comparison with a reference.
+ *
+ * mj_check_gather_kv: for every sequence b and kv head g, K (values = 0) or
+ * V (values = 1) rows 0 .. L_b - 1 fetched exactly as the tensor-core
+ * decode kernels fetch them (the same tensor maps over the caller's
+ * strides, the same block-table lookup and TMA boxes), written densely:
+ *   out[(b*h_k + g)*out_rows + row][0..127] for row < min(L_b, out_rows)
+ * (device, 16-byte aligned; other rows are left as they were).  args'
+ * k, v, strides, block_table and seq_lens are read; the rest is ignored.
+ * mj_check_dequant_e4m3: out[c] = the fp32 value the CUDA-core kernel gives
+ * e4m3 code c, c = 0..255 (device, 16-byte aligned; NaN codes give NaN).
+ * Errors: MJ_ERR_INVALID_ARG, MJ_ERR_UNSUPPORTED (params), MJ_ERR_CUDA. */
+mj_status mj_check_gather_kv(const mj_decode_params* params, const mj_decode_args* args, int32_t values,
+                             uint8_t* out, int32_t out_rows, mj_stream_t stream);
+mj_status mj_check_dequant_e4m3(float* out, mj_stream_t stream);
+
 /* Fused fp8 query quantisation and pack (source: `quantize_q_fp8` and
  * `pack_q`).  For every sequence b and kv head g the group is Q's q_len
  * tokens x h_r heads x d values of that kv head;

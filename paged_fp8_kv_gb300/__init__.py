@@ -142,6 +142,10 @@ def lib() -> ctypes.CDLL:
         L.mj_decode_plan_max_items.argtypes = [_vp, _vp]
         L.mj_decode_plan_device.restype = ctypes.c_int
         L.mj_decode_plan_device.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.mj_check_gather_kv.restype = ctypes.c_int
+        L.mj_check_gather_kv.argtypes = [P(DecodeParams), P(DecodeArgs), ctypes.c_int32, _vp, ctypes.c_int32, _vp]
+        L.mj_check_dequant_e4m3.restype = ctypes.c_int
+        L.mj_check_dequant_e4m3.argtypes = [_vp, _vp]
         L.mj_quantize_pack_q.restype = ctypes.c_int
         L.mj_quantize_pack_q.argtypes = [_vp, _vp, _vp] + [ctypes.c_int32] * 5 + [_vp]
         L.mj_unpack_o.restype = ctypes.c_int
@@ -366,6 +370,27 @@ def pack_q(q_vllm, q_packed, num_seqs: int, q_len: int, h_k: int, h_r: int, stre
         _stream_handle(stream),
     )
     _check(st, "mj_pack_q")
+
+
+def check_gather_kv(params: DecodeParams, k_cache, v_cache, block_table, seq_lens, values: bool, out,
+                    stream=None) -> None:
+    """mj_check_gather_kv: the decode path's K (values False) or V rows of
+    every (sequence, kv head) into out (b, h_k, out_rows, 128) uint8."""
+    a = DecodeArgs()
+    a.k, a.v = _ptr(k_cache), _ptr(v_cache)
+    a.k_page, a.k_row, a.k_head = kv_strides(k_cache)
+    a.v_page, a.v_row, a.v_head = kv_strides(v_cache)
+    a.block_table, a.seq_lens = _ptr(block_table), _ptr(seq_lens)
+    st = lib().mj_check_gather_kv(
+        ctypes.byref(params), ctypes.byref(a), int(bool(values)), _ptr(out), int(out.shape[2]), _stream_handle(stream)
+    )
+    _check(st, "mj_check_gather_kv")
+
+
+def check_dequant_e4m3(out, stream=None) -> None:
+    """mj_check_dequant_e4m3: out (256,) float32 = the CUDA-core kernel's
+    value of every e4m3 code."""
+    _check(lib().mj_check_dequant_e4m3(_ptr(out), _stream_handle(stream)), "mj_check_dequant_e4m3")
 
 
 def decode_plan_max_items(

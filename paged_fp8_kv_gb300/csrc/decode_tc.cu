@@ -844,7 +844,88 @@ cudaError_t launch_tc_q(const DecodeDev& a, int n_q_tiles, bool q_e4m3, cudaStre
   return q_e4m3 ? launch_tc<R, true>(a, n_q_tiles, stream) : launch_tc<R, false>(a, n_q_tiles, stream);
 }
 
+// ---------------------------------------------------------------- checks
+// The producer's page gather and the CUDA-core kernel's dequant as
+// standalone launches, so that tests can compare them byte- and bit-exact
+// with the oracle: the same tensor maps (make_kv_map), the same page lookup
+// (lane j fetches page j of a 128-row tile through the block table; pages
+// past the sequence end are fetched out of range, as zeros), the same TMA
+// boxes, and the 128-byte swizzle the MMA descriptors assume, undone here.
+
+// grid (tiles, h_k, num_seqs), 64 threads; out rows [b][g][row][128 bytes]
+__global__ void __launch_bounds__(64) gather_kv_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap,
+                                                       uint8_t* __restrict__ out, int out_rows) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tile = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t tile_s = ptx::smem_u32(tile);
+  const uint32_t bar = tile_s + kKVTileBytes;
+  const int t = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int L = a.seq_lens[b];
+  const int T = L > 0 ? (L + kTileKV - 1) / kTileKV : 1;
+  if (t >= T) return;  // uniform over the CTA
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int PS = a.page_size;
+    const int ppt = kTileKV / PS;
+    int valid_pages = (L + PS - 1) / PS;
+    valid_pages = valid_pages < a.max_blocks ? valid_pages : a.max_blocks;
+    const int blk = t * ppt + lane;
+    const int page = (lane < ppt && blk < valid_pages)
+                         ? a.block_table[static_cast<int64_t>(b) * a.max_blocks + blk]
+                         : a.num_pages;
+    if (lane == 0) ptx::mbar_arrive_expect_tx(bar, kKVTileBytes);
+    __syncwarp();
+    if (lane < ppt) ptx::tma_load_4d(tile_s + lane * PS * 128, &tmap, bar, 0, 0, g, page);
+  }
+  volatile int never = 0;
+  if (!ptx::mbar_wait_bounded(bar, 0, &never, kWaitNs)) {  // rows stay unwritten: the test fails
+    ptx::mbar_wait_bounded(bar, 0, &never, kWaitNs / 4);     // (a bounded drain before leaving)
+    return;
+  }
+  for (int i = tid; i < kTileKV * 8; i += 64) {
+    const int r = i >> 3, cc = i & 7;
+    const int key = t * kTileKV + r;
+    if (key >= L || key >= out_rows) continue;
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + r * 128 + ((cc ^ (r & 7)) << 4));
+    *reinterpret_cast<uint4*>(out + ((static_cast<int64_t>(b) * a.h_k + g) * out_rows + key) * 128 + cc * 16) = v;
+  }
+}
+
+// 64 threads: codes 4t .. 4t + 3 through the CUDA-core kernel's conversion
+__global__ void dequant_e4m3_kernel(float* __restrict__ out) {
+  const uint32_t c0 = 4u * threadIdx.x;
+  const uint32_t w = c0 | ((c0 + 1) << 8) | ((c0 + 2) << 16) | ((c0 + 3) << 24);
+  float v[4];
+  e4m3x4_to_f32(w, v);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) out[c0 + k] = v[k];
+}
+
 }  // namespace
+
+cudaError_t launch_gather_kv(const DecodeDev& a, bool values, uint8_t* out, int out_rows, cudaStream_t stream) {
+  CUtensorMap m;
+  const bool ok = values ? make_kv_map(&m, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page,
+                                       a.page_size, 1)
+                         : make_kv_map(&m, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page,
+                                       a.page_size, 1);
+  if (!ok) return cudaErrorInvalidValue;
+  const int tiles = (out_rows + kTileKV - 1) / kTileKV;
+  const int smem = kKVTileBytes + 1024 + 64;  // tile, alignment slack, mbarrier
+  dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(a.h_k), static_cast<unsigned>(a.num_seqs));
+  gather_kv_kernel<<<grid, 64, smem, stream>>>(a, m, out, out_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_e4m3(float* out, cudaStream_t stream) {
+  dequant_e4m3_kernel<<<1, 64, 0, stream>>>(out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
                              cudaStream_t stream) {

@@ -297,6 +297,41 @@ extern "C" mj_status mj_pack_q(const void* q_vllm, void* q_packed, int32_t elem_
   return permute(q_vllm, q_packed, elem_bytes, num_seqs, q_len, h_k, h_r, head_dim, true, stream);
 }
 
+extern "C" mj_status mj_check_gather_kv(const mj_decode_params* params, const mj_decode_args* args, int32_t values,
+                                        uint8_t* out, int32_t out_rows, mj_stream_t stream) {
+  const mj_status st = check_params(params);
+  if (st != MJ_OK) return st;
+  if (!args || !out || !aligned16(out) || out_rows < 1 || values < 0 || values > 1) return MJ_ERR_INVALID_ARG;
+  const mj_decode_args& a = *args;
+  if (!a.k || !a.v || !a.block_table || !a.seq_lens || !aligned16(a.k) || !aligned16(a.v)) return MJ_ERR_INVALID_ARG;
+  const int64_t kv_strides[6] = {a.k_page, a.k_row, a.k_head, a.v_page, a.v_row, a.v_head};
+  for (int64_t s : kv_strides)
+    if (s <= 0 || (s & 15) != 0 || s >= (int64_t{1} << 40)) return MJ_ERR_INVALID_ARG;
+  DecodeDev d{};
+  d.k = a.k;
+  d.v = a.v;
+  d.k_page = a.k_page;
+  d.k_row = a.k_row;
+  d.k_head = a.k_head;
+  d.v_page = a.v_page;
+  d.v_row = a.v_row;
+  d.v_head = a.v_head;
+  d.block_table = a.block_table;
+  d.seq_lens = a.seq_lens;
+  d.num_seqs = params->num_seqs;
+  d.h_k = params->h_k;
+  d.page_size = params->page_size;
+  d.max_blocks = params->max_blocks;
+  d.num_pages = params->num_pages;
+  const cudaError_t e = launch_gather_kv(d, values != 0, out, out_rows, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MJ_OK : MJ_ERR_CUDA;
+}
+
+extern "C" mj_status mj_check_dequant_e4m3(float* out, mj_stream_t stream) {
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 15) != 0) return MJ_ERR_INVALID_ARG;
+  return launch_dequant_e4m3(out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MJ_OK : MJ_ERR_CUDA;
+}
+
 namespace {
 
 // Options as the device plan resolves them (0 -> the kernel's values, no model).

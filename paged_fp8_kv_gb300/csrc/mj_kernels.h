@@ -49,6 +49,8 @@ bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, in
 cudaError_t launch_merge(const DecodeDev& a, int max_n_splits, cudaStream_t stream);
 
 // Layout permutations (vLLM <-> packed rows).
+cudaError_t launch_gather_kv(const DecodeDev& a, bool values, uint8_t* out, int out_rows, cudaStream_t stream);
+cudaError_t launch_dequant_e4m3(float* out, cudaStream_t stream);
 cudaError_t launch_plan_device(const int32_t* seq_lens, int num_seqs, int64_t max_len, int64_t slots,
                                int max_splits, int force_splits, int min_chunk, int pad_to, int4* work,
                                int32_t* n_splits, int32_t* chunk_out, int32_t* status, cudaStream_t stream);
