@@ -218,6 +218,26 @@ def test_plan_max_items_bounds_every_plan():
     assert mj.lib().mj_decode_plan_max_items(None, None) == -1
 
 
+def test_check_hooks_validation():
+    # the verification hooks refuse bad arguments on the host, before any launch
+    L = mj.lib()
+    p = _params(2, h_r=4)
+    a = mj.DecodeArgs()
+    assert L.mj_check_gather_kv(ctypes.byref(p), None, 0, 1 << 20, 128, None) == mj.MJ_ERR_INVALID_ARG
+    assert L.mj_check_gather_kv(ctypes.byref(p), ctypes.byref(a), 0, 1 << 20, 128, None) == mj.MJ_ERR_INVALID_ARG
+    a.k, a.v, a.block_table, a.seq_lens = 1 << 20, 1 << 21, 1 << 22, 1 << 23
+    a.k_page = a.v_page = 16 * 128
+    a.k_row = a.v_row = 128
+    a.k_head = a.v_head = 128
+    assert L.mj_check_gather_kv(ctypes.byref(p), ctypes.byref(a), 2, 1 << 24, 128, None) == mj.MJ_ERR_INVALID_ARG
+    assert L.mj_check_gather_kv(ctypes.byref(p), ctypes.byref(a), 0, (1 << 24) + 8, 128, None) == mj.MJ_ERR_INVALID_ARG
+    assert L.mj_check_gather_kv(ctypes.byref(p), ctypes.byref(a), 0, 1 << 24, 0, None) == mj.MJ_ERR_INVALID_ARG
+    a.k_row = 100  # not a 16-byte multiple
+    assert L.mj_check_gather_kv(ctypes.byref(p), ctypes.byref(a), 0, 1 << 24, 128, None) == mj.MJ_ERR_INVALID_ARG
+    assert L.mj_check_dequant_e4m3(None, None) == mj.MJ_ERR_INVALID_ARG
+    assert L.mj_check_dequant_e4m3((1 << 20) + 4, None) == mj.MJ_ERR_INVALID_ARG
+
+
 def test_quantize_pack_validation():
     # every refusal happens on the host, before any launch
     L = mj.lib()
