@@ -293,6 +293,21 @@ mj_status mj_decode_plan_device(const mj_decode_params* params, mj_plan_opts* op
  * mj_decode_plan_device does; returns -1 for invalid params or options. */
 int32_t mj_decode_plan_max_items(const mj_decode_params* params, mj_plan_opts* opts);
 
+/* The preconditions mj_decode_attn cannot check cheaply (it reads device
+ * memory it does not validate), checked on host copies for debugging: for
+ * every sequence b, 0 <= L_b <= max_blocks*page_size, the block-table
+ * entries of its first ceil(L_b / page_size) pages are in [0, num_pages)
+ * (entries past them may hold anything), and q/k/v descales of every kv
+ * head are finite and positive (the kernels take the raw-score maximum
+ * before scaling).  block_table_host is [num_seqs][max_blocks]; descales
+ * are indexed [b*d_seq + g*d_head] as in mj_decode_args.  Returns MJ_OK, or
+ * MJ_ERR_INVALID_ARG with *bad_seq (optional) set to the first offending
+ * sequence (-1 when the arguments themselves are invalid).  Host only. */
+mj_status mj_check_preconditions(const mj_decode_params* params, const int32_t* block_table_host,
+                                 const int32_t* seq_lens_host, const float* q_descale, const float* k_descale,
+                                 const float* v_descale, int64_t qd_seq, int64_t qd_head, int64_t kd_seq,
+                                 int64_t kd_head, int64_t vd_seq, int64_t vd_head, int32_t* bad_seq);
+
 /* Verification hooks (not needed to compute anything): the decode path's
  * page gather and the CUDA-core kernel's e4m3 conversion as standalone
  * launches, for byte- and bit-exact comparison with a reference.

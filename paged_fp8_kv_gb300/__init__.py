@@ -142,6 +142,8 @@ def lib() -> ctypes.CDLL:
         L.mj_decode_plan_max_items.argtypes = [_vp, _vp]
         L.mj_decode_plan_device.restype = ctypes.c_int
         L.mj_decode_plan_device.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.mj_check_preconditions.restype = ctypes.c_int
+        L.mj_check_preconditions.argtypes = [P(DecodeParams), _vp, _vp, _vp, _vp, _vp] + [_i64] * 6 + [_vp]
         L.mj_check_gather_kv.restype = ctypes.c_int
         L.mj_check_gather_kv.argtypes = [P(DecodeParams), P(DecodeArgs), ctypes.c_int32, _vp, ctypes.c_int32, _vp]
         L.mj_check_dequant_e4m3.restype = ctypes.c_int
@@ -370,6 +372,40 @@ def pack_q(q_vllm, q_packed, num_seqs: int, q_len: int, h_k: int, h_r: int, stre
         _stream_handle(stream),
     )
     _check(st, "mj_pack_q")
+
+
+def check_preconditions(params: DecodeParams, block_table, seq_lens, q_descale, k_descale, v_descale):
+    """mj_check_preconditions on host (numpy) copies; returns (status, first
+    offending sequence or -1)."""
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    nb, hk = int(params.num_seqs), int(params.h_k)
+    ds = [np.ascontiguousarray(d, dtype=np.float32) for d in (q_descale, k_descale, v_descale)]
+
+    def strides(d):  # the element strides descale_strides gives a tensor
+        if d.size == 1:
+            return (0, 0)
+        if d.ndim == 1 and d.shape[0] == hk:
+            return (0, 1)
+        if d.ndim == 2 and d.shape == (nb, hk):
+            return (hk, 1)
+        raise ValueError(f"descale shape {d.shape}")
+
+    st_ = [strides(d) for d in ds]
+    bad = ctypes.c_int32(0)
+    st = lib().mj_check_preconditions(
+        ctypes.byref(params),
+        bt.ctypes.data,
+        sl.ctypes.data,
+        ds[0].ctypes.data,
+        ds[1].ctypes.data,
+        ds[2].ctypes.data,
+        *st_[0],
+        *st_[1],
+        *st_[2],
+        ctypes.addressof(bad),
+    )
+    return int(st), int(bad.value)
 
 
 def check_gather_kv(params: DecodeParams, k_cache, v_cache, block_table, seq_lens, values: bool, out,

@@ -5,6 +5,7 @@
 // call, so it can run on any host thread while the GPU works.
 
 #include <algorithm>
+#include <cmath>
 #include <queue>
 #include <cstring>
 #include <vector>
@@ -239,5 +240,46 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
   }
   *num_work = static_cast<int32_t>(n_out);
   if (chunk_tiles) *chunk_tiles = static_cast<int32_t>(chunk);
+  return MJ_OK;
+}
+
+extern "C" mj_status mj_check_preconditions(const mj_decode_params* params, const int32_t* block_table_host,
+                                            const int32_t* seq_lens_host, const float* q_descale,
+                                            const float* k_descale, const float* v_descale, int64_t qd_seq,
+                                            int64_t qd_head, int64_t kd_seq, int64_t kd_head, int64_t vd_seq,
+                                            int64_t vd_head, int32_t* bad_seq) {
+  using namespace mj;
+  if (bad_seq) *bad_seq = -1;
+  const mj_status st = check_params(params);
+  if (st != MJ_OK) return st;
+  if (!block_table_host || !seq_lens_host || !q_descale || !k_descale || !v_descale) return MJ_ERR_INVALID_ARG;
+  const int64_t strides[6] = {qd_seq, qd_head, kd_seq, kd_head, vd_seq, vd_head};
+  for (int64_t s : strides)
+    if (s < 0) return MJ_ERR_INVALID_ARG;
+  const mj_decode_params& p = *params;
+  const int64_t max_len = static_cast<int64_t>(p.max_blocks) * p.page_size;
+  for (int b = 0; b < p.num_seqs; ++b) {
+    bool ok = true;
+    const int64_t L = seq_lens_host[b];
+    if (L < 0 || L > max_len) ok = false;
+    // pages below ceil(L / page_size) are read; later entries may hold anything
+    const int64_t pages = ok ? (L + p.page_size - 1) / p.page_size : 0;
+    for (int64_t j = 0; ok && j < pages; ++j) {
+      const int32_t pg = block_table_host[static_cast<int64_t>(b) * p.max_blocks + j];
+      if (pg < 0 || pg >= p.num_pages) ok = false;
+    }
+    // the kernels take the raw-score maximum and then scale: every descale
+    // must be finite and positive
+    for (int g = 0; ok && g < p.h_k; ++g) {
+      const float d[3] = {q_descale[b * qd_seq + g * qd_head], k_descale[b * kd_seq + g * kd_head],
+                          v_descale[b * vd_seq + g * vd_head]};
+      for (float x : d)
+        if (!std::isfinite(x) || !(x > 0.f)) ok = false;
+    }
+    if (!ok) {
+      if (bad_seq) *bad_seq = b;
+      return MJ_ERR_INVALID_ARG;
+    }
+  }
   return MJ_OK;
 }

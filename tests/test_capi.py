@@ -325,3 +325,34 @@ def test_default_plan_splits_when_long_sequences_dominate():
     assert mj.lib().mj_decode_plan_max_items(ctypes.byref(p), ctypes.byref(co)) > 0
     cands = {(co.ctas_per_sm * t + 2) // 3 for t in (3, 5, 8, 12)}
     assert plan.opts.ctas_per_sm in cands
+
+
+def test_check_preconditions():
+    from paged_fp8_kv_gb300 import synthetic as syn
+
+    w = syn.make_workload("pre", [0, 1, 37, 100, 300], 1, 2, 4, 16, seed=7)
+    p = mj.make_params(w.num_seqs, 1, 2, 4, 16, w.max_blocks, w.num_pages, True, mj.MJ_BF16, 16, 128, 0, 0)
+    ok = (w.block_table, w.seq_lens, w.q_descale, w.k_descale, w.v_descale)
+    # the generator leaves -1 / INT32_MAX garbage past each sequence's pages
+    assert (w.block_table < 0).any()
+    assert mj.check_preconditions(p, *ok) == (mj.MJ_OK, -1)
+    bt = w.block_table.copy()
+    bt[3, 2] = w.num_pages  # a page the sequence reads, out of the pool
+    assert mj.check_preconditions(p, bt, *ok[1:]) == (mj.MJ_ERR_INVALID_ARG, 3)
+    bt = w.block_table.copy()
+    bt[2, 3] = -5  # page 3 of a 37-key sequence (3 pages): never read
+    assert mj.check_preconditions(p, bt, *ok[1:]) == (mj.MJ_OK, -1)
+    bt[2, 2] = -5  # its last page
+    assert mj.check_preconditions(p, bt, *ok[1:]) == (mj.MJ_ERR_INVALID_ARG, 2)
+    sl = w.seq_lens.copy()
+    sl[4] = w.max_blocks * 16 + 1
+    assert mj.check_preconditions(p, w.block_table, sl, *ok[2:]) == (mj.MJ_ERR_INVALID_ARG, 4)
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        kd = w.k_descale.copy()
+        kd[1, 1] = bad
+        assert mj.check_preconditions(p, w.block_table, w.seq_lens, w.q_descale, kd, w.v_descale) == (
+            mj.MJ_ERR_INVALID_ARG,
+            1,
+        )
+    # per-tensor and per-head descales broadcast
+    assert mj.check_preconditions(p, w.block_table, w.seq_lens, np.ones(1), np.ones(2), np.ones(2))[0] == mj.MJ_OK
