@@ -8,6 +8,7 @@ the mutated copies live in a temporary directory."""
 import importlib.util
 import os
 
+import numpy as np
 import pytest
 
 import oracle
@@ -34,9 +35,11 @@ def load(path, name, tmp_path, old=None, new=None):
 
 
 def pins_hold(all_pins, m) -> bool:
-    """The pin files' own checks, run against module m."""
+    """The pin files' own checks, run against module m (a mutant may divide
+    by zero or overflow: numpy's warnings about that are expected here)."""
     try:
-        all_pins(m)
+        with np.errstate(all="ignore"):
+            all_pins(m)
         return True
     except Exception:
         return False
