@@ -7,6 +7,7 @@ the mutated copies live in a temporary directory."""
 
 import importlib.util
 import os
+import sys
 
 import numpy as np
 import pytest
@@ -27,7 +28,11 @@ def load(path, name, tmp_path, old=None, new=None):
     f.write_text(src)
     spec = importlib.util.spec_from_file_location(name, str(f))
     mod = importlib.util.module_from_spec(spec)
-    spec.loader.exec_module(mod)
+    sys.modules[name] = mod  # dataclasses look their module up there
+    try:
+        spec.loader.exec_module(mod)
+    finally:
+        del sys.modules[name]
     return mod
 
 
@@ -86,11 +91,13 @@ def narrow_pins_hold(m) -> bool:
 NARROW_MUTATIONS = [
     ("e2m3 bias", '"e2m3": (2, 3, 1)', '"e2m3": (2, 3, 2)'),
     ("subnormal binade", "mag = (m / (1 << mb)) * 2.0 ** (1 - bias)", "mag = (m / (1 << mb)) * 2.0 ** (-bias)"),
-    ("tie to the larger", "mag = lo if (a - pos[lo]) <= (pos[hi] - a) else hi", "mag = lo if (a - pos[lo]) < (pos[hi] - a) else hi"),
-    ("negative zero", "neg = v < 0 and pos[mag] > 0", "neg = v < 0"),
-    ("nibble order", "return (c[..., 0] | (c[..., 1] << np.uint64(4))).astype(np.uint8)", "return (c[..., 1] | (c[..., 0] << np.uint64(4))).astype(np.uint8)"),
-    ("fp6 shift", "(c[..., 1] << np.uint64(6))", "(c[..., 1] << np.uint64(5))"),
+    ("tie to the larger", "if best_dist is None or dist < best_dist:", "if best_dist is None or dist <= best_dist:"),
+    ("negative zero", "(half if (v < 0 and table[best] != 0) else 0)", "(half if v < 0 else 0)"),
+    ("bit order within a byte", "out[row, j // 8] |= np.uint8(1 << (j % 8))", "out[row, j // 8] |= np.uint8(1 << (7 - j % 8))"),
+    ("bit order within a code", "j = bits * i + k\n                    out", "j = bits * i + (bits - 1 - k)\n                    out"),
+    ("element stride", "j = bits * i + k\n                    out", "j = (bits + 1) * i + k if i % 4 else bits * i + k\n                    out"),
     ("mantissa width", '"e3m2": (3, 2, 3)', '"e3m2": (2, 3, 3)'),
+    ("sign of the search", "dist = abs(abs(v) - table[c])", "dist = abs(v - table[c])"),
 ]
 
 
@@ -102,3 +109,62 @@ def test_narrow_module_passes_its_pins(tmp_path):
 def test_narrow_planted_mistake_is_caught(label, old, new, tmp_path):
     m = load(os.path.join(ORACLE_DIR, "narrow_ref.py"), "narrow_mut", tmp_path, old, new)
     assert not narrow_pins_hold(m), f"no pin caught: {label}"
+
+
+# ------------------------------------------------------------- row layout
+
+
+def layout_pins_hold(m) -> bool:
+    from tests.test_layout_ref import all_pins
+
+    return pins_hold(all_pins, m)
+
+
+LAYOUT_MUTATIONS = [
+    ("unpack: token and head axes kept", "o_packed.reshape(num_seqs, h_k, q_len, h_r, d).transpose(0, 2, 1, 3, 4)", "o_packed.reshape(num_seqs, h_k, q_len, h_r, d).transpose(0, 1, 2, 3, 4)"),
+    ("unpack: rows read head-major", "o_packed.reshape(num_seqs, h_k, q_len, h_r, d)", "o_packed.reshape(num_seqs, h_k, h_r, q_len, d)"),
+    ("unpack: kv and query heads swapped", ".reshape(num_seqs * q_len, h_k * h_r, d)", ".transpose(0, 1, 3, 2, 4).reshape(num_seqs * q_len, h_k * h_r, d)"),
+    ("pack: rows written head-major", "q_vllm.reshape(num_seqs, q_len, h_k, h_r, d).transpose(0, 2, 1, 3, 4)", "q_vllm.reshape(num_seqs, q_len, h_k, h_r, d).transpose(0, 2, 3, 1, 4)"),
+]
+
+
+def test_layout_module_passes_its_pins(tmp_path):
+    assert layout_pins_hold(load(os.path.join(ORACLE_DIR, "layout_ref.py"), "layout_ok", tmp_path))
+
+
+@pytest.mark.parametrize("label,old,new", LAYOUT_MUTATIONS, ids=[m[0] for m in LAYOUT_MUTATIONS])
+def test_layout_planted_mistake_is_caught(label, old, new, tmp_path):
+    m = load(os.path.join(ORACLE_DIR, "layout_ref.py"), "layout_mut", tmp_path, old, new)
+    assert not layout_pins_hold(m), f"no pin caught: {label}"
+
+
+# ------------------------------------------------------------------- plan
+
+
+def plan_pins_hold(m) -> bool:
+    from tests.test_plan_ref import all_pins
+
+    return pins_hold(all_pins, m)
+
+
+PLAN_MUTATIONS = [
+    ("tile of 64 rows", "TILE_ROWS = 128", "TILE_ROWS = 64"),
+    ("empty sequence owns no tile", "return max(1, whole + (1 if rest else 0))", "return whole + (1 if rest else 0)"),
+    ("slots ignore the q tiles", "slots = max(1, (sm_count * ctas_per_sm) // (h_k * n_q_tiles))", "slots = max(1, (sm_count * ctas_per_sm) // h_k)"),
+    ("no max_splits floor", "while _pieces(longest, floor_chunk) > max_splits:", "while False:"),
+    ("a full wave does not fit", "while chunk < longest and sum(_pieces(t, chunk) for t in tiles) > slots:", "while chunk < longest and sum(_pieces(t, chunk) for t in tiles) >= slots:"),
+    ("largest fitting chunk", "while chunk < longest and sum(_pieces(t, chunk) for t in tiles) > slots:", "while chunk < longest and sum(_pieces(t, chunk + 1) for t in tiles) <= slots:"),
+    ("shortest first", "items.sort(key=lambda it: (-(it[2] - it[1]), it[0], it[3]))", "items.sort(key=lambda it: (it[2] - it[1], it[0], it[3]))"),
+    ("ties by last sequence", "items.sort(key=lambda it: (-(it[2] - it[1]), it[0], it[3]))", "items.sort(key=lambda it: (-(it[2] - it[1]), -it[0], it[3]))"),
+    ("force ignores the floor", "        chunk = floor_chunk\n        while _pieces(longest, chunk) > force_splits:", "        chunk = 1\n        while _pieces(longest, chunk) > force_splits:"),
+]
+
+
+def test_plan_module_passes_its_pins(tmp_path):
+    assert plan_pins_hold(load(os.path.join(ORACLE_DIR, "plan_ref.py"), "plan_ok", tmp_path))
+
+
+@pytest.mark.parametrize("label,old,new", PLAN_MUTATIONS, ids=[m[0] for m in PLAN_MUTATIONS])
+def test_plan_planted_mistake_is_caught(label, old, new, tmp_path):
+    m = load(os.path.join(ORACLE_DIR, "plan_ref.py"), "plan_mut", tmp_path, old, new)
+    assert not plan_pins_hold(m), f"no pin caught: {label}"
