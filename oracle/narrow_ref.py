@@ -11,11 +11,11 @@ exponent 0 and no infinities or NaN:
     e2m3: 2 exponent bits, 3 mantissa bits, bias 1   (largest 7.5)
     e2m1: 2 exponent bits, 1 mantissa bit,  bias 1   (largest 6)
 
-The page's quantiser rounds |x| (clamped to the largest value) to the
-nearer of its two neighbours in the non-negative table, a tie going to the
-smaller one, and gives the code the sign bit only when the magnitude is not
-zero.  Codes are packed little-endian into a bit stream (fp4: element 2i in
-the low nibble of byte i; fp6: four elements in three bytes).
+Quantisation picks the representable magnitude nearest to |x| (the
+page's quantiser settles a tie on the smaller magnitude and saturates at
+the largest), with the sign bit only on a non-zero magnitude.  Codes are
+laid out as one little-endian bit stream per row (so fp4 puts element 2i in
+the low nibble of byte i, and fp6 fills three bytes with four elements).
 
 Every value of the three formats is also an e4m3 value, so an attention
 problem with narrow KV is the same problem with the equal e4m3 codes:
@@ -53,55 +53,59 @@ def minifloat_table(fmt: str) -> np.ndarray:
 
 
 def minifloat_encode(x: np.ndarray, fmt: str) -> np.ndarray:
-    """Codes of x: round to nearest, ties to the smaller magnitude,
-    saturating at the largest value; zero (either sign) -> code 0."""
+    """Codes of x by exhaustive nearest search: the non-negative magnitude
+    at the least distance from |x|, two equally near magnitudes resolved
+    to the smaller one (the tie rule of the page's `minifloat_quantize`);
+    anything beyond the largest magnitude is nearest to it, so the search
+    saturates by itself.  The sign bit is set for negative x whose chosen
+    magnitude is not zero (no negative-zero codes)."""
     table = minifloat_table(fmt)
     half = len(table) // 2
-    pos = table[:half]  # 0 .. largest, ascending
     xs = np.asarray(x, dtype=np.float64)
     out = np.empty(xs.shape, dtype=np.uint8)
     flat, res = xs.reshape(-1), out.reshape(-1)
     for i, v in enumerate(flat):
-        a = min(abs(v), pos[-1])
-        hi = int(np.searchsorted(pos, a, side="left"))  # first value >= a
-        if hi == 0:
-            mag = 0
-        else:
-            lo = hi - 1
-            hi = min(hi, half - 1)
-            mag = lo if (a - pos[lo]) <= (pos[hi] - a) else hi
-        neg = v < 0 and pos[mag] > 0
-        res[i] = mag + (half if neg else 0)
+        best, best_dist = 0, None
+        for c in range(half):  # non-negative codes: magnitudes ascending
+            dist = abs(abs(v) - table[c])
+            if best_dist is None or dist < best_dist:  # a tie keeps the smaller
+                best, best_dist = c, dist
+        res[i] = best + (half if (v < 0 and table[best] != 0) else 0)
     return out
 
 
 def pack_bits(codes: np.ndarray, bits: int) -> np.ndarray:
-    """Little-endian bit stream of the last axis: element i at bits
-    [bits*i, bits*(i+1)).  fp4 needs an even length, fp6 a multiple of 4."""
-    c = np.asarray(codes, dtype=np.uint64)
+    """Little-endian bit stream of the last axis: bit k of element i is
+    stream bit bits*i + k, and stream bit j is bit j % 8 of byte j // 8.
+    fp4 needs an even length, fp6 a multiple of 4 (whole bytes)."""
+    c = np.asarray(codes, dtype=np.int64)
     d = c.shape[-1]
-    if bits == 4:
-        assert d % 2 == 0
-        c = c.reshape(*c.shape[:-1], d // 2, 2)
-        return (c[..., 0] | (c[..., 1] << np.uint64(4))).astype(np.uint8)
-    assert bits == 6 and d % 4 == 0
-    c = c.reshape(*c.shape[:-1], d // 4, 4)
-    w = c[..., 0] | (c[..., 1] << np.uint64(6)) | (c[..., 2] << np.uint64(12)) | (c[..., 3] << np.uint64(18))
-    out = np.stack([w & np.uint64(0xFF), (w >> np.uint64(8)) & np.uint64(0xFF), (w >> np.uint64(16)) & np.uint64(0xFF)], axis=-1)
-    return out.reshape(*c.shape[:-2], d // 4 * 3).astype(np.uint8)
+    assert (d * bits) % 8 == 0
+    flat = c.reshape(-1, d)
+    out = np.zeros((flat.shape[0], d * bits // 8), dtype=np.uint8)
+    for row in range(flat.shape[0]):
+        for i in range(d):
+            for k in range(bits):
+                if (int(flat[row, i]) >> k) & 1:
+                    j = bits * i + k
+                    out[row, j // 8] |= np.uint8(1 << (j % 8))
+    return out.reshape(*c.shape[:-1], d * bits // 8)
 
 
 def unpack_bits(packed: np.ndarray, bits: int, d: int) -> np.ndarray:
-    """Inverse of pack_bits for a last axis of d codes."""
-    p = np.asarray(packed, dtype=np.uint64)
-    if bits == 4:
-        lo, hi = p & np.uint64(0xF), p >> np.uint64(4)
-        return np.stack([lo, hi], axis=-1).reshape(*p.shape[:-1], d).astype(np.uint8)
-    assert bits == 6
-    p = p.reshape(*p.shape[:-1], d // 4, 3)
-    w = p[..., 0] | (p[..., 1] << np.uint64(8)) | (p[..., 2] << np.uint64(16))
-    parts = [(w >> np.uint64(6 * k)) & np.uint64(0x3F) for k in range(4)]
-    return np.stack(parts, axis=-1).reshape(*p.shape[:-2], d).astype(np.uint8)
+    """Inverse of pack_bits for a last axis of d codes: code i gathers
+    stream bits bits*i .. bits*i + bits - 1, least significant first."""
+    p = np.asarray(packed, dtype=np.int64)
+    flat = p.reshape(-1, p.shape[-1])
+    out = np.zeros((flat.shape[0], d), dtype=np.uint8)
+    for row in range(flat.shape[0]):
+        for i in range(d):
+            v = 0
+            for k in range(bits):
+                j = bits * i + k
+                v |= ((int(flat[row, j // 8]) >> (j % 8)) & 1) << k
+            out[row, i] = v
+    return out.reshape(*p.shape[:-1], d)
 
 
 def to_e4m3_codes(codes: np.ndarray, fmt: str, e4m3_table: np.ndarray) -> np.ndarray:

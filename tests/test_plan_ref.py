@@ -18,9 +18,11 @@ from oracle.plan_ref import plan_ref
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "plan_examples.json")
 
 
-@pytest.mark.parametrize("case", json.load(open(GOLDEN))["cases"], ids=lambda c: c["why"][:40])
-def test_hand_derived_plans(case):
-    p = plan_ref(**case["args"])
+CASES = json.load(open(GOLDEN))["cases"]
+
+
+def pin_hand_derived(fn, case):
+    p = fn(**case["args"])
     assert p.chunk_tiles == case["chunk_tiles"]
     assert p.slots == case["slots"]
     assert p.n_splits == case["n_splits"]
@@ -28,6 +30,11 @@ def test_hand_derived_plans(case):
         assert [list(w) for w in p.work] == case["work"]
     else:
         assert len(p.work) == case["work_len"]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c["why"][:40])
+def test_hand_derived_plans(case):
+    pin_hand_derived(plan_ref, case)
 
 
 def _check_properties(p, seq_lens, h_k, n_q_tiles, sm, cps, max_splits, force, min_chunk, pad):
@@ -53,6 +60,9 @@ def _check_properties(p, seq_lens, h_k, n_q_tiles, sm, cps, max_splits, force, m
         assert len(p.work) == pad
         assert all(w == (0, 0, 0, 0) for w in p.work[len(real):])
     slots = max(1, sm * cps // (h_k * n_q_tiles))
+    if force == 0 and (len(tiles) >= slots or max_splits == 1):
+        # a batch that already fills the wave (or may not split) is not split
+        assert p.chunk_tiles == T and all(n == 1 for n in p.n_splits)
     if force == 0 and len(tiles) < slots and max_splits > 1:
         total = sum(math.ceil(t / p.chunk_tiles) for t in tiles)
         lo = max(min_chunk, math.ceil(T / max_splits))
@@ -62,9 +72,9 @@ def _check_properties(p, seq_lens, h_k, n_q_tiles, sm, cps, max_splits, force, m
             assert sum(math.ceil(t / (p.chunk_tiles - 1)) for t in tiles) > slots
 
 
-def test_random_plans_have_the_rule_properties():
+def pin_random_properties(fn, count=400):
     rng = np.random.default_rng(31)
-    for _ in range(400):
+    for _ in range(count):
         b = int(rng.integers(1, 40))
         seq_lens = rng.integers(0, 20000, size=b).tolist()
         h_k = int(rng.choice([1, 2, 8]))
@@ -74,11 +84,22 @@ def test_random_plans_have_the_rule_properties():
         max_splits = int(rng.choice([1, 16, 64, 256]))
         force = int(rng.choice([0, 0, 0, 3]))
         min_chunk = int(rng.choice([1, 1, 2]))
-        p = plan_ref(seq_lens, h_k, n_q_tiles, sm, cps, max_splits, force, min_chunk, 0)
+        p = fn(seq_lens, h_k, n_q_tiles, sm, cps, max_splits, force, min_chunk, 0)
         _check_properties(p, seq_lens, h_k, n_q_tiles, sm, cps, max_splits, force, min_chunk, 0)
         pad = len(p.work) + int(rng.integers(0, 5))
-        p2 = plan_ref(seq_lens, h_k, n_q_tiles, sm, cps, max_splits, force, min_chunk, pad)
+        p2 = fn(seq_lens, h_k, n_q_tiles, sm, cps, max_splits, force, min_chunk, pad)
         _check_properties(p2, seq_lens, h_k, n_q_tiles, sm, cps, max_splits, force, min_chunk, pad)
+
+
+def test_random_plans_have_the_rule_properties():
+    pin_random_properties(plan_ref)
+
+
+def all_pins(m):
+    """Every pin against module m (raises on the first that fails)."""
+    for case in CASES:
+        pin_hand_derived(m.plan_ref, case)
+    pin_random_properties(m.plan_ref, 150)
 
 
 def test_pad_below_item_count_is_rejected():
