@@ -169,7 +169,9 @@ size_t mj_decode_workspace_bytes(const mj_decode_params* params);
 /* Device-side arguments of mj_decode_attn.
  *   q            device, packed (b, h_k, n_q, d) rows of q_dtype; row n of
  *                kv head g of sequence b at q + b*q_seq_stride + (g*n_q+n)*d
- *                (for q_len == 1 vLLM's (b, h_q, d) is already packed)
+ *                (for q_len == 1 vLLM's (b, h_q, d) is already packed);
+ *                with num_seqs > 1, q_seq_stride and o_seq_stride are at
+ *                least h_k*n_q*d (MJ_ERR_INVALID_ARG otherwise)
  *   k, v         device e4m3 pools; element (page, r, g, i) at
  *                page*x_page + r*x_row + g*x_head + i; every stride a
  *                multiple of 16 bytes (K and V may share one buffer)
@@ -182,13 +184,19 @@ size_t mj_decode_workspace_bytes(const mj_decode_params* params);
  *   o            device bf16, packed like q with o_seq_stride
  *   lse          device fp32 (b, h_k, n_q), contiguous
  *   workspace    device, >= mj_decode_workspace_bytes; need not be
- *                initialised; may be NULL when max_splits == 1
+ *                initialised; may be NULL only when that size is 0
+ *                (max_splits == 1 and a kernel other than the head-grouped
+ *                one, which keeps its unit counter there)
  *   status       optional device int32, caller-zeroed; kernels that give up
- *                a bounded wait write MJ_ERR_TIMEOUT there; NULL = off
+ *                a bounded wait write MJ_ERR_TIMEOUT there, and the merge
+ *                writes MJ_ERR_INVALID_ARG for a sequence whose n_splits
+ *                exceeds max_n_splits or max_splits (that sequence's O and
+ *                LSE rows are then not written); NULL = off
  *   max_n_splits host hint: the plan's largest n_splits (1 = nothing was
  *                split: the merge kernel is not launched; it also sizes the
  *                merge); 0 = unknown (the merge runs, sized for max_splits).
- *                A value below the true maximum gives wrong results.
+ *                A sequence with more splits than the hint is refused by the
+ *                merge (see status), never merged in part.
  *   timing_events optional: NULL, or 3 cudaEvent_t recorded on `stream`
  *                before the decode kernel, between decode and merge, and
  *                after the merge (instrumentation only) */
@@ -325,6 +333,19 @@ mj_status mj_check_preconditions(const mj_decode_params* params, const int32_t* 
 mj_status mj_check_gather_kv(const mj_decode_params* params, const mj_decode_args* args, int32_t values,
                              uint8_t* out, int32_t out_rows, mj_stream_t stream);
 mj_status mj_check_dequant_e4m3(float* out, mj_stream_t stream);
+
+/* Verification hook of the kernels' bounded waits (every mbarrier wait in
+ * the decode kernels gives up after a time limit, sets MJ_ERR_TIMEOUT in the
+ * status word and lets the CTA drain and exit, so a lost copy or MMA cannot
+ * hang the GPU).  One warp waits on an mbarrier that nothing ever completes,
+ * with the same primitive and a limit of limit_us microseconds, then writes
+ * MJ_ERR_TIMEOUT to *status and the nanoseconds it waited to *waited_ns.
+ *   status     device int32 (caller-zeroed)
+ *   waited_ns  device int64, 8-byte aligned, or NULL
+ *   limit_us   1 .. 1000000
+ * No counterpart on the pages (their kernel's waits have no limit).
+ * Errors: MJ_ERR_INVALID_ARG, MJ_ERR_CUDA (launch). */
+mj_status mj_check_bounded_wait(int32_t* status, int64_t* waited_ns, int32_t limit_us, mj_stream_t stream);
 
 /* Fused fp8 query quantisation and pack (source: `quantize_q_fp8` and
  * `pack_q`).  For every sequence b and kv head g the group is Q's q_len

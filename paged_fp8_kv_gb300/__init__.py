@@ -148,6 +148,8 @@ def lib() -> ctypes.CDLL:
         L.mj_check_gather_kv.argtypes = [P(DecodeParams), P(DecodeArgs), ctypes.c_int32, _vp, ctypes.c_int32, _vp]
         L.mj_check_dequant_e4m3.restype = ctypes.c_int
         L.mj_check_dequant_e4m3.argtypes = [_vp, _vp]
+        L.mj_check_bounded_wait.restype = ctypes.c_int
+        L.mj_check_bounded_wait.argtypes = [_vp, _vp, ctypes.c_int32, _vp]
         L.mj_quantize_pack_q.restype = ctypes.c_int
         L.mj_quantize_pack_q.argtypes = [_vp, _vp, _vp] + [ctypes.c_int32] * 5 + [_vp]
         L.mj_unpack_o.restype = ctypes.c_int
@@ -380,6 +382,12 @@ def check_preconditions(params: DecodeParams, block_table, seq_lens, q_descale, 
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     nb, hk = int(params.num_seqs), int(params.h_k)
+    # the C checker reads num_seqs rows of max_blocks entries and num_seqs
+    # lengths: refuse arrays of another shape instead of reading past them
+    if bt.shape != (nb, int(params.max_blocks)):
+        raise ValueError(f"block_table shape {bt.shape}, expected {(nb, int(params.max_blocks))}")
+    if sl.shape != (nb,):
+        raise ValueError(f"seq_lens shape {sl.shape}, expected {(nb,)}")
     ds = [np.ascontiguousarray(d, dtype=np.float32) for d in (q_descale, k_descale, v_descale)]
 
     def strides(d):  # the element strides descale_strides gives a tensor
@@ -427,6 +435,16 @@ def check_dequant_e4m3(out, stream=None) -> None:
     """mj_check_dequant_e4m3: out (256,) float32 = the CUDA-core kernel's
     value of every e4m3 code."""
     _check(lib().mj_check_dequant_e4m3(_ptr(out), _stream_handle(stream)), "mj_check_dequant_e4m3")
+
+
+def check_bounded_wait(status, waited_ns=None, limit_us: int = 1000, stream=None) -> None:
+    """mj_check_bounded_wait: one warp waits limit_us on an mbarrier that
+    never completes, then writes MJ_ERR_TIMEOUT to status (device int32) and
+    the time waited to waited_ns (device int64, optional)."""
+    _check(
+        lib().mj_check_bounded_wait(_ptr(status), _ptr(waited_ns), int(limit_us), _stream_handle(stream)),
+        "mj_check_bounded_wait",
+    )
 
 
 def decode_plan_max_items(

@@ -906,7 +906,36 @@ __global__ void dequant_e4m3_kernel(float* __restrict__ out) {
   for (int k = 0; k < 4; ++k) out[c0 + k] = v[k];
 }
 
+// The bounded-wait primitive on its own: one warp waits on an mbarrier that
+// nothing arrives on, so the wait must give up after `limit_ns`; the warp then
+// reports MJ_ERR_TIMEOUT in the status word, as the decode kernels do, and the
+// time it waited.  No other warp and no named barrier is involved, so the
+// launch ends whatever the primitive does with its limit.
+__global__ void bounded_wait_kernel(int32_t* status, int64_t* waited_ns, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = ptx::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(b, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+  const uint64_t t0 = ptx::globaltimer_ns();
+  const bool done = ptx::mbar_wait_bounded(b, 0, &abort_flag, limit_ns);
+  const uint64_t t1 = ptx::globaltimer_ns();
+  if (threadIdx.x == 0) {
+    if (!done) atomicExch(status, 5);  // MJ_ERR_TIMEOUT
+    if (waited_ns) *waited_ns = static_cast<int64_t>(t1 - t0);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait(int32_t* status, int64_t* waited_ns, uint64_t limit_ns, cudaStream_t stream) {
+  bounded_wait_kernel<<<1, 32, 0, stream>>>(status, waited_ns, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather_kv(const DecodeDev& a, bool values, uint8_t* out, int out_rows, cudaStream_t stream) {
   CUtensorMap m;

@@ -18,6 +18,10 @@
 // are combined in warp order through shared memory.  Every sum runs in a
 // fixed order: the result does not depend on timing.
 //
+// A sequence with more splits than the launch covers (kWPR x kPer, sized
+// from the caller's max_n_splits hint) or than max_splits is not merged: its
+// rows are left as they were and MJ_ERR_INVALID_ARG goes to the status word.
+//
 // The kernel is launched as a programmatic dependent of the decode kernel:
 // its CTAs can be resident before the decode grid ends and read the split
 // counts (host inputs) meanwhile, and wait for the decode grid only before
@@ -32,6 +36,7 @@ namespace mj {
 namespace {
 
 constexpr int kCtaWarps = 4;  // warps per CTA when a row needs fewer
+constexpr int kStatusInvalidArg = 1;  // MJ_ERR_INVALID_ARG
 
 // kWPR warps per row, each staging up to kPer splits (4, 8 or 16: the
 // staging area, kPer x 512 B a warp, sets how many CTAs fit an SM)
@@ -47,9 +52,15 @@ __global__ void __launch_bounds__((kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32) me
   const int n = static_cast<int>(row % a.n_q);
   const int g = static_cast<int>((row / a.n_q) % a.h_k);
   const int b = static_cast<int>(row / (static_cast<int64_t>(a.n_q) * a.h_k));
-  int nsp = a.n_splits[b];
+  const int nsp = a.n_splits[b];
   if (nsp <= 1) return;  // unsplit: decode wrote O; uniform over the row's warps
-  nsp = nsp < a.max_splits ? nsp : a.max_splits;
+  if (nsp > kWPR * kPer || nsp > a.max_splits) {
+    // more splits than this launch was sized for (a max_n_splits hint below
+    // the plan's largest count) or than the workspace holds: refuse the row
+    // instead of merging a subset of its partials
+    if (w == 0 && lane == 0 && a.status) atomicExch(a.status, kStatusInvalidArg);
+    return;
+  }
   ptx::griddep_wait();  // the decode grid's partials are complete and visible
 
   const int j0 = w * kPer;

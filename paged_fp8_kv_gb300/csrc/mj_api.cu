@@ -1,6 +1,7 @@
 // C ABI entry points: argument validation, kernel choice and launches.
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstdio>
@@ -178,6 +179,10 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   if (!aligned16(a.q) || !aligned16(a.o)) return MJ_ERR_INVALID_ARG;
   if (a.q_seq_stride < 0 || ((a.q_seq_stride * q_bytes) & 15) != 0) return MJ_ERR_INVALID_ARG;
   if (a.o_seq_stride < 0 || ((a.o_seq_stride * 2) & 15) != 0) return MJ_ERR_INVALID_ARG;
+  // one sequence's packed rows (h_k * n_q rows of d) must fit between two
+  // sequences: a shorter O stride would make sequences overwrite each other
+  const int64_t seq_elems = static_cast<int64_t>(p.h_k) * p.q_len * p.h_r * kHeadDim;
+  if (p.num_seqs > 1 && (a.q_seq_stride < seq_elems || a.o_seq_stride < seq_elems)) return MJ_ERR_INVALID_ARG;
   const int64_t d_strides[6] = {a.qd_seq, a.qd_head, a.kd_seq, a.kd_head, a.vd_seq, a.vd_head};
   for (int64_t s : d_strides)
     if (s < 0) return MJ_ERR_INVALID_ARG;
@@ -246,6 +251,20 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
     for (int i = 0; i < 3; ++i) ev[i] = static_cast<cudaEvent_t>(a.timing_events[i]);
 
   const KernelChoice kc = choose_kernel(p);
+  const int merge_splits = a.max_n_splits == 0 ? p.max_splits : a.max_n_splits;
+  const bool merge = p.max_splits > 1 && merge_splits > 1;
+  if (verbose())
+    std::fprintf(stderr,
+                 "mj_decode_attn: kernel=%s num_seqs=%d h_k=%d n_q=%d (q_len %d x h_r %d) page_size=%d %s "
+                 "q=%s work_items=%d merge=%s (max_n_splits %d of max_splits %d) kv_evict_first=%d\n",
+                 kc.name, p.num_seqs, p.h_k, p.q_len * p.h_r, p.q_len, p.h_r, p.page_size,
+                 p.causal ? "causal" : "non-causal", p.q_dtype == MJ_E4M3 ? "e4m3" : "bf16", a.num_work,
+                 merge ? "yes" : "no", merge_splits, p.max_splits, d.kv_evict_first);
+  // an NVTX range around the launches, so a profiler's timeline names them
+  nvtxRangePushA("mj_decode_attn");
+  struct RangeEnd {
+    ~RangeEnd() { nvtxRangePop(); }
+  } range_end;
   cudaError_t e = cudaSuccess;
   if (ev[0] && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return MJ_ERR_CUDA;
   if (kc.kind == KernelKind::kTensorCoreQRows) {
@@ -263,8 +282,7 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
     e = launch_decode_cc(d, kc.rows_per_cta, kc.n_q_tiles, p.q_dtype == MJ_E4M3, stream);
   if (e != cudaSuccess) return MJ_ERR_CUDA;
   if (ev[1] && cudaEventRecord(ev[1], stream) != cudaSuccess) return MJ_ERR_CUDA;
-  const int merge_splits = a.max_n_splits == 0 ? p.max_splits : a.max_n_splits;
-  if (p.max_splits > 1 && merge_splits > 1) {
+  if (merge) {
     e = launch_merge(d, merge_splits, stream);
     if (e != cudaSuccess) return MJ_ERR_CUDA;
   }
@@ -330,6 +348,16 @@ extern "C" mj_status mj_check_gather_kv(const mj_decode_params* params, const mj
 extern "C" mj_status mj_check_dequant_e4m3(float* out, mj_stream_t stream) {
   if (!out || (reinterpret_cast<uintptr_t>(out) & 15) != 0) return MJ_ERR_INVALID_ARG;
   return launch_dequant_e4m3(out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MJ_OK : MJ_ERR_CUDA;
+}
+
+extern "C" mj_status mj_check_bounded_wait(int32_t* status, int64_t* waited_ns, int32_t limit_us,
+                                           mj_stream_t stream) {
+  if (!status || (reinterpret_cast<uintptr_t>(status) & 3) != 0) return MJ_ERR_INVALID_ARG;
+  if (waited_ns && (reinterpret_cast<uintptr_t>(waited_ns) & 7) != 0) return MJ_ERR_INVALID_ARG;
+  if (limit_us < 1 || limit_us > 1000000) return MJ_ERR_INVALID_ARG;
+  const cudaError_t e = launch_bounded_wait(status, waited_ns, static_cast<uint64_t>(limit_us) * 1000u,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MJ_OK : MJ_ERR_CUDA;
 }
 
 namespace {

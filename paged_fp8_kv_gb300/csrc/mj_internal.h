@@ -36,4 +36,8 @@ mj_status check_params(const mj_decode_params* p);
 // Kernel choice for valid params.
 KernelChoice choose_kernel(const mj_decode_params& p);
 
+// MJ_VERBOSE set to a non-empty value other than "0" in the environment
+// (read once per process): the entry points print what they chose to stderr.
+bool verbose();
+
 }  // namespace mj

@@ -51,6 +51,7 @@ cudaError_t launch_merge(const DecodeDev& a, int max_n_splits, cudaStream_t stre
 // Layout permutations (vLLM <-> packed rows).
 cudaError_t launch_gather_kv(const DecodeDev& a, bool values, uint8_t* out, int out_rows, cudaStream_t stream);
 cudaError_t launch_dequant_e4m3(float* out, cudaStream_t stream);
+cudaError_t launch_bounded_wait(int32_t* status, int64_t* waited_ns, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_plan_device(const int32_t* seq_lens, int num_seqs, int64_t max_len, int64_t slots,
                                int max_splits, int force_splits, int min_chunk, int pad_to, int4* work,
                                int32_t* n_splits, int32_t* chunk_out, int32_t* status, cudaStream_t stream);

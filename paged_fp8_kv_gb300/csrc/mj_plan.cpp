@@ -6,6 +6,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
+#include <cstdlib>
 #include <queue>
 #include <cstring>
 #include <vector>
@@ -13,6 +15,14 @@
 #include "mj_internal.h"
 
 namespace mj {
+
+bool verbose() {
+  static const bool on = [] {
+    const char* v = std::getenv("MJ_VERBOSE");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
 
 mj_status check_params(const mj_decode_params* p) {
   if (!p) return MJ_ERR_INVALID_ARG;
@@ -240,6 +250,28 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
   }
   *num_work = static_cast<int32_t>(n_out);
   if (chunk_tiles) *chunk_tiles = static_cast<int32_t>(chunk);
+  if (verbose()) {
+    // a summary in the spirit of the page's SplitPlan repr: the options the
+    // rule ran with, the chunk it chose and how the sequences were cut
+    int64_t split_seqs = 0, max_k = 0, sum_tiles = 0;
+    for (int i = 0; i < b; ++i) {
+      split_seqs += n_splits_out[i] > 1;
+      max_k = std::max<int64_t>(max_k, n_splits_out[i]);
+      sum_tiles += tiles[i];
+    }
+    const int64_t slots = std::max<int64_t>(
+        1, static_cast<int64_t>(opts->sm_count) * opts->ctas_per_sm / (static_cast<int64_t>(params->h_k) * opts->n_q_tiles));
+    std::fprintf(stderr,
+                 "mj_decode_plan: SplitPlan(kernel=%s, num_seqs=%d, h_k=%d, n_q=%d, sm_count=%d, ctas_per_sm=%d%s, "
+                 "n_q_tiles=%d, slots=%lld, max_splits=%d, force_splits=%d, chunk_tiles=%lld, tiles=%lld "
+                 "(longest %lld), work_items=%lld, padding=%lld, split_seqs=%lld, max_n_splits=%lld)\n",
+                 kc.name, b, params->h_k, params->q_len * params->h_r, opts->sm_count, opts->ctas_per_sm,
+                 default_cps ? " (library choice)" : "", opts->n_q_tiles, static_cast<long long>(slots),
+                 params->max_splits, opts->force_splits, static_cast<long long>(chunk),
+                 static_cast<long long>(sum_tiles), static_cast<long long>(longest), static_cast<long long>(n_items),
+                 static_cast<long long>(n_out - n_items), static_cast<long long>(split_seqs),
+                 static_cast<long long>(max_k));
+  }
   return MJ_OK;
 }
 

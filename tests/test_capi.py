@@ -172,6 +172,14 @@ def test_decode_attn_validation_rejects_before_launch():
     bad = _params(1, h_r=4)
     bad.head_dim = 256
     assert _attn_status(bad, _good_args()) == mj.MJ_ERR_UNSUPPORTED
+    # two sequences: a sequence stride below one sequence's h_k * n_q rows of
+    # d would make sequences overlap
+    p2 = _params(2, h_k=2, h_r=4, max_splits=1)
+    for field in ("q_seq_stride", "o_seq_stride"):
+        a = _good_args()
+        a.q_seq_stride = a.o_seq_stride = 2 * 4 * 128
+        setattr(a, field, 2 * 4 * 128 - 8)
+        assert _attn_status(p2, a) == mj.MJ_ERR_INVALID_ARG, field
 
 
 def test_pack_validation():
@@ -354,5 +362,45 @@ def test_check_preconditions():
             mj.MJ_ERR_INVALID_ARG,
             1,
         )
+    # arrays of the wrong shape are refused before the checker reads them
+    with pytest.raises(ValueError):
+        mj.check_preconditions(p, w.block_table[:, :-1], *ok[1:])
+    with pytest.raises(ValueError):
+        mj.check_preconditions(p, w.block_table[:-1], *ok[1:])
+    with pytest.raises(ValueError):
+        mj.check_preconditions(p, w.block_table, w.seq_lens[:-1], *ok[2:])
+    with pytest.raises(ValueError):
+        mj.check_preconditions(p, w.block_table, w.seq_lens, w.q_descale, np.ones(3), w.v_descale)
     # per-tensor and per-head descales broadcast
     assert mj.check_preconditions(p, w.block_table, w.seq_lens, np.ones(1), np.ones(2), np.ones(2))[0] == mj.MJ_OK
+
+
+def test_bounded_wait_hook_validation():
+    L = mj.lib()
+    fake = 1 << 20
+    assert L.mj_check_bounded_wait(None, None, 1000, None) == mj.MJ_ERR_INVALID_ARG
+    assert L.mj_check_bounded_wait(fake + 2, None, 1000, None) == mj.MJ_ERR_INVALID_ARG
+    assert L.mj_check_bounded_wait(fake, fake + 4, 1000, None) == mj.MJ_ERR_INVALID_ARG
+    for bad in (0, -5, 1000001):
+        assert L.mj_check_bounded_wait(fake, None, bad, None) == mj.MJ_ERR_INVALID_ARG
+
+
+def test_verbose_switch_prints_the_plan_and_nothing_without_it():
+    import subprocess
+    import sys
+
+    code = (
+        "import paged_fp8_kv_gb300 as mj\n"
+        "p = mj.make_params(8, 1, 1, 16, 128, 1024, 2000, True, mj.MJ_E4M3, 256)\n"
+        "mj.decode_plan(p, [131072] + [1024] * 7)\n"
+    )
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MJ_VERBOSE="1", PYTHONPATH=root)
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True)
+    line = [l for l in out.stderr.splitlines() if l.startswith("mj_decode_plan: SplitPlan(")]
+    assert len(line) == 1, out.stderr
+    for field in ("kernel=tc_r16_e4m3", "num_seqs=8", "chunk_tiles=4", "max_n_splits=256", "split_seqs=8"):
+        assert field in line[0], line[0]
+    env["MJ_VERBOSE"] = "0"
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True)
+    assert "SplitPlan" not in out.stderr

@@ -72,3 +72,22 @@ def test_dequant_is_bit_exact():
             assert np.isnan(got[c]), hex(c)
         else:
             assert got[c].view(np.uint32) == np.float32(ref[c]).view(np.uint32), hex(c)  # sign of zero too
+
+
+@pytest.mark.parametrize("limit_us", [200, 2000])
+def test_bounded_wait_gives_up_and_reports_a_timeout(limit_us):
+    # the primitive every decode-kernel wait uses, on an mbarrier that never
+    # completes: it must give up after its limit (not hang) and the status
+    # word must read MJ_ERR_TIMEOUT; the GPU stays usable afterwards
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    mj.check_bounded_wait(status, waited, limit_us)
+    torch.cuda.synchronize()
+    assert int(status.item()) == mj.MJ_ERR_TIMEOUT
+    ns = int(waited.item())
+    assert limit_us * 1000 <= ns <= limit_us * 1000 + 5_000_000, ns
+    # the context is intact: an ordinary launch still runs
+    out = torch.empty(256, dtype=torch.float32, device="cuda")
+    mj.check_dequant_e4m3(out)
+    torch.cuda.synchronize()
+    assert out[0].item() == 0.0

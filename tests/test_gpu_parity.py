@@ -303,3 +303,35 @@ def test_merge_instances_by_split_count(splits, lo, hi):
     w = syn.config(2, num_seqs=3, len_range=(25600, 26000), max_splits=128)
     s, _ = check(w, force_splits=splits)
     assert lo <= s.plan.max_n_splits <= hi
+
+
+def test_merge_refuses_a_hint_below_the_split_count():
+    # a max_n_splits hint of 2 sizes the merge for 4 splits a row; a plan
+    # with 6 splits must be refused (status word), not merged in part; with
+    # the right hint the same call merges and matches the oracle
+    import paged_fp8_kv_gb300 as mj
+
+    w = syn.config(2, num_seqs=3, len_range=(25600, 26000), max_splits=16)
+    s = DecodeSession(w, force_splits=6)
+    assert s.plan.max_n_splits == 6
+    s.fill_workspace(float("nan"))
+
+    def call(hint, status):
+        mj.decode_attn(
+            s.params, q=s.q_packed, k_cache=s.k_cache, v_cache=s.v_cache, block_table=s.block_table,
+            seq_lens=s.seq_lens, work=s.work, n_splits=s.n_splits, q_descale=s.q_descale,
+            k_descale=s.k_descale, v_descale=s.v_descale, o=s.o_packed, lse=s.lse, workspace=s.workspace,
+            softmax_scale=w.softmax_scale, scale_o=w.scale_o, status=status, max_n_splits=hint,
+        )
+        torch.cuda.synchronize()
+
+    s.o_packed.fill_(7.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    call(2, status)
+    assert int(status.item()) == 1  # MJ_ERR_INVALID_ARG
+    # every sequence had 6 splits: none was merged, O kept its old bytes
+    assert torch.all(s.o_packed.float() == 7.0)
+    status.zero_()
+    call(6, status)
+    assert int(status.item()) == 0
+    compare(w, s.o_host(), s.lse_host())

@@ -5,10 +5,11 @@ Some callers may not allocate device memory when they call into the library
 inside a framework that owns the allocator).  For them the library keeps the
 split-KV scratch in a fixed device array and this entry point uses it instead
 of a caller workspace.  This test calls it through the C ABI, twice in a row
-(the second call finds the array holding the first call's partials), and
-checks both results against the regular entry point's, within the parity
-tests' tolerance.  It also checks that a problem too large for the array is
-refused before anything runs.
+(the second call finds the array holding the first call's partials and, for
+the head-grouped kernel, its unit counter), and checks that both give the
+regular entry point's bytes exactly: the same kernels run the same plan, and
+the library's results are deterministic.  It also checks that a problem too
+large for the array is refused before anything runs.
 
 The file name sorts last so that a run stopping at the first failure has
 already run every other test.
@@ -72,29 +73,34 @@ def _static_call(s, o, lse):
     return fn(ctypes.byref(s.params), ctypes.byref(a), torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("kernel", [1, 2], ids=["cuda_core", "tensor_core"])
-def test_static_workspace_matches_regular_entry(kernel):
+CASES = [
     # a skewed fully-fp8 batch whose long sequence is split, so the merge
     # reads the static scratch
-    w = syn.config(3, num_seqs=4, len_range=(9000, 700))
+    (1, lambda: syn.config(3, num_seqs=4, len_range=(9000, 700))),
+    (2, lambda: syn.config(3, num_seqs=4, len_range=(9000, 700))),
+    # the head-grouped kernel keeps its unit counter in the scratch as well
+    (3, lambda: syn.config(2, num_seqs=8, len_range=(3000, 6000))),
+]
+
+
+@pytest.mark.parametrize("kernel,make", CASES, ids=["cuda_core", "tensor_core", "grouped"])
+def test_static_workspace_matches_regular_entry(kernel, make):
+    w = make()
     s = DecodeSession(w, kernel=kernel)
     assert s.plan.max_n_splits > 1
     assert 0 < mj.workspace_bytes(s.params) <= (32 << 20)
     s.fill_workspace(float("nan"))
     s.decode()
     torch.cuda.synchronize()
-    ref_o = s.o_packed.float().clone()
+    ref_o = s.o_packed.clone()
     ref_lse = s.lse.clone()
     for call in range(2):
         o = torch.full_like(s.o_packed, float("nan"))
         lse = torch.full_like(s.lse, float("nan"))
         assert _static_call(s, o, lse) == mj.MJ_OK
         torch.cuda.synchronize()
-        got_o, got_lse = o.float(), lse
-        assert not torch.isnan(got_o).any()
-        # the parity tests' tolerance for the fully-fp8 path
-        assert torch.all((got_o - ref_o).abs() <= 5e-2 + 5e-2 * ref_o.abs()), f"call {call}"
-        assert torch.max((got_lse - ref_lse).abs()).item() <= 2e-3, f"call {call}"
+        assert torch.equal(o, ref_o), f"O differs on call {call}"
+        assert torch.equal(lse, ref_lse), f"LSE differs on call {call}"
 
 
 def test_static_workspace_refuses_oversized_problems():
