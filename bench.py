@@ -1,7 +1,7 @@
 """Benchmark: paged fp8-KV split-KV decode attention on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mj|reference]
-                    [--config 2] [--variant ...] [--h_r ..] [--q_len ..]
+                    [--config 4] [--variant ...] [--h_r ..] [--q_len ..] [--suite 0|1]
 
 One step = one pass of the decode hot path over one batch: pack Q (q_len >
 1), the decode kernel over every work item, the merge of split sequences,
@@ -16,6 +16,11 @@ step, outside the step's CUDA events.
 
 `--impl reference` times the fp64 CPU oracle, the only reference this
 method has, on a bounded sample of the same workload.
+
+The headline workload is config 4 (speculative verify, the largest).  With
+no workload flag the line also carries `suite`: every workload of the five
+configurations (the ten sweep points included) timed the same way in the
+same run, with decode time, step time and roofline fraction each.
 
 With N > 1 (torchrun) every rank runs an independent replica: there is no
 data-path collective; barriers only bracket the timed region.
@@ -46,7 +51,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="mj", choices=["mj", "reference"])
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=4, help="headline workload: 4 = speculative verify (the largest config)")
     ap.add_argument("--variant", default=None)
     ap.add_argument("--h_r", type=int, default=None)
     ap.add_argument("--q_len", type=int, default=None)
@@ -60,6 +65,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time steps as plain launches, not CUDA-graph replays")
     ap.add_argument("--q_quant", action="store_true", help="also time the fused fp8 Q quantisation + pack for this shape")
+    ap.add_argument("--suite", type=int, default=-1, help="1: also time every workload of the five configs (default: on when no workload flag is given)")
+    ap.add_argument("--suite_steps", type=int, default=60, help="timed steps per suite workload")
     return ap.parse_args()
 
 
@@ -192,13 +199,31 @@ def algorithmic_flops(w) -> int:
 
 
 def tensor_peak():
-    """e4m3 dense peak: the measured sustained bf16 GEMM rate x 2 (the
-    nominal fp8 : bf16 ratio of the tensor cores)."""
+    """e4m3 dense peak for a kernel timed alone: the measured burst bf16 GEMM
+    rate x 2 (the nominal fp8 : bf16 ratio of the tensor cores)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         p = json.load(open(path))
-        return 2.0 * float(p["bf16_tflops_sustained"]), "measured bf16 sustained x 2 (e4m3 : bf16 nominal)"
-    return 2.0 * 1700.0, "fallback bf16 sustained x 2"
+        return 2.0 * float(p["bf16_tflops"]), "measured bf16 burst x 2 (e4m3 : bf16 nominal)"
+    return 2.0 * 1900.0, "fallback bf16 burst x 2"
+
+
+def clocks_now(index: int):
+    """One read-only nvidia-smi query of the SM clock and throttle reasons."""
+    try:
+        out = subprocess.run(
+            ["nvidia-smi", "-i", str(index), f"--query-gpu={ClockSampler.FIELDS}", "--format=csv,noheader,nounits"],
+            capture_output=True, text=True, timeout=10,
+        ).stdout.strip().splitlines()
+        parts = [p.strip() for p in out[0].split(",")]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        return {
+            "sm_mhz": float(parts[0]),
+            "sm_max_mhz": float(parts[1]),
+            "reasons": sorted(nm for nm, v in zip(names, parts[4:8]) if v.lower().startswith("active")),
+        }
+    except Exception:
+        return None
 
 
 def traffic_record(kernel: str, workload_name: str):
@@ -238,6 +263,66 @@ def whole_job_gbs(world: int, step_bytes: int, step_ms: float) -> float:
     return world * step_bytes / (step_ms * 1e-3) / 1e9
 
 
+def time_steps(s, dev, flush, steps: int, warmup: int, eager: bool = False, world: int = 1):
+    """Times `steps` decode steps of session s (L2 flushed before each, outside
+    the step's events): the step time as a CUDA-graph replay (pack, decode,
+    merge, unpack), decode and merge times from eager steps with events
+    between the kernels.  Returns (step_ms, decode_ms, merge_ms)."""
+    import torch
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        flush.fill_(1)
+        s.step()
+    torch.cuda.synchronize()
+    # A step is timed as one replay of a CUDA graph holding (pack, decode,
+    # merge, unpack); the library makes no host sync, so it captures as is.
+    graph = None
+    if not eager:
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            s.step(stream=cs)
+        torch.cuda.synchronize()
+        for _ in range(warmup):
+            flush.fill_(1)
+            graph.replay()
+        torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for e in [x for row in evs for x in row]:
+        e.record()  # torch creates the CUDA event lazily, at its first record
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    # Even steps carry events between the decode and the merge launch (the
+    # per-kernel times of the roofline); an event there also serialises the
+    # merge behind the decode grid, so the step time comes from the odd
+    # steps, which run exactly as a caller's would (graph replays, the merge
+    # a programmatic dependent of the decode grid).
+    for i in range(steps):
+        flush.fill_(i & 0xFF)  # L2 flush, outside the step's events
+        sev[i][0].record()
+        if i % 2 == 0 or steps == 1:
+            s.step(timing_events=evs[i])
+        elif graph is not None:
+            graph.replay()
+        else:
+            s.step()
+        sev[i][1].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    inner = range(0, steps, 2)
+    plain = range(1, steps, 2) if steps > 1 else range(1)
+    decode_ms = float(np.mean([evs[i][0].elapsed_time(evs[i][1]) for i in inner]))
+    merge_ms = float(np.mean([evs[i][1].elapsed_time(evs[i][2]) for i in inner]))
+    step_ms = float(np.mean([sev[i][0].elapsed_time(sev[i][1]) for i in plain]))
+    return step_ms, decode_ms, merge_ms
+
+
 def run_mj(args, rank, world, local_rank):
     import torch
 
@@ -257,7 +342,6 @@ def run_mj(args, rank, world, local_rank):
     )
     d_bytes, m_bytes, step_bytes = algorithmic_bytes(w, s.plan)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
     # host plan cost (the plan runs once per batch shape, on the host)
     t = time.perf_counter()
@@ -265,58 +349,10 @@ def run_mj(args, rank, world, local_rank):
         decode_plan(s.params, w.seq_lens, sm_count=s.sm_count)
     plan_us = (time.perf_counter() - t) / 20 * 1e6
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        s.step()
-    torch.cuda.synchronize()
-    # A step is timed as one replay of a CUDA graph holding (pack, decode,
-    # merge, unpack); the library makes no host sync, so it captures as is.
-    graph = None
-    if not args.eager:
-        cs = torch.cuda.Stream(dev)
-        cs.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cs):
-            s.step(stream=cs)
-        torch.cuda.synchronize()
-        for _ in range(args.warmup):
-            flush.fill_(1)
-            graph.replay()
-        torch.cuda.synchronize()
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for e in [x for row in evs for x in row]:
-        e.record()  # torch creates the CUDA event lazily, at its first record
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    # Even steps carry events between the decode and the merge launch (the
-    # per-kernel times of the roofline); an event there also serialises the
-    # merge behind the decode grid, so the step time comes from the odd
-    # steps, which run exactly as a caller's would (graph replays, the merge
-    # a programmatic dependent of the decode grid).
+    clk_before = clocks_now(local_rank)
     with ClockSampler(local_rank) as clk:
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)  # L2 flush, outside the step's events
-            sev[i][0].record()
-            if i % 2 == 0 or args.steps == 1:
-                s.step(timing_events=evs[i])
-            elif graph is not None:
-                graph.replay()
-            else:
-                s.step()
-            sev[i][1].record()
-        torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    inner = range(0, args.steps, 2)
-    plain = range(1, args.steps, 2) if args.steps > 1 else range(1)
-    decode_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in inner]
-    merge_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in inner]
-    step_ms = float(np.mean([sev[i][0].elapsed_time(sev[i][1]) for i in plain]))
-    t_dec = float(np.mean(decode_ms))
-
+        step_ms, t_dec, merge_ms = time_steps(s, dev, flush, args.steps, args.warmup, args.eager, world)
+    clk_after = clocks_now(local_rank)
     step_ms = max_over_ranks(step_ms, world, dev)
 
     launches = s.launches_per_step() * args.steps
@@ -324,22 +360,93 @@ def run_mj(args, rank, world, local_rank):
     plan_dev = plan_device_measure(s, w, dev, flush) if rank == 0 else None
     e2e = None if args.no_e2e else e2e_measure(args, s, w, step_bytes, dev)
     clocks = clk.summary()
+    suite = None
+    suite_clocks = None
+    if rank == 0 and args.suite == 1:
+        main_key = (args.config, args.variant, args.h_r, args.q_len)
+        with ClockSampler(local_rank) as sclk:
+            suite = run_suite(args, dev, flush, reuse={main_key: w})
+        suite_clocks = sclk.summary()
     return dict(
         w=w,
         s=s,
         step_ms=step_ms,
         decode_ms=t_dec,
-        merge_ms=float(np.mean(merge_ms)),
+        merge_ms=merge_ms,
         d_bytes=d_bytes,
         m_bytes=m_bytes,
         step_bytes=step_bytes,
         plan_us=plan_us,
         launches=launches,
         e2e=e2e,
-        clocks=clocks,
+        clocks=clock_record(clocks, clk_before, clk_after, suite_clocks),
         q_quant=q_quant,
         plan_dev=plan_dev,
+        suite=suite,
     )
+
+
+def clock_record(timed, before, after, suite):
+    """The clocks line: samples taken during the timed region (often none:
+    the region can be a few milliseconds), one query right before and right
+    after it, and the samples taken while the suite ran (seconds of load)."""
+    rec = {"during_timed": timed, "before": before, "after": after, "during_suite": suite}
+    under = [c for c in (timed, suite) if c]
+    pts = [c for c in (before, after) if c]
+    src = under[0] if under else (pts[0] if pts else None)
+    if src is None:
+        return None
+    reasons = sorted(set(r for c in under + pts for r in c.get("reasons", [])))
+    mhz = [c["sm_mhz"] for c in under] or [c["sm_mhz"] for c in pts]
+    return {
+        "sm_mhz": float(np.median(mhz)),
+        "sm_max_mhz": max(c["sm_max_mhz"] for c in under + pts),
+        "reasons": reasons,
+        "detail": rec,
+    }
+
+
+SUITE = [(1, {}), (2, {}), (3, {}), (4, {}), (4, {"variant": "noncausal"})] + [
+    (5, {"h_r": hr, "q_len": ql}) for hr in (16, 32) for ql in (1, 2, 4, 8, 16)
+]
+
+
+def run_suite(args, dev, flush, reuse=None):
+    """Every workload of the five configurations at full size, each timed like
+    the headline (graph-replayed steps with L2 flushed before each, decode and
+    merge from event-split steps), with the automatic kernel and plan."""
+    import torch
+
+    from paged_fp8_kv_gb300 import synthetic as syn
+    from paged_fp8_kv_gb300.session import DecodeSession
+
+    peak, _ = measured_peaks()
+    tpk, _ = tensor_peak()
+    out = []
+    for cfg, opts in SUITE:
+        key = (cfg, opts.get("variant"), opts.get("h_r"), opts.get("q_len"))
+        w = (reuse or {}).get(key) or syn.config(cfg, **opts)
+        s = DecodeSession(w, device=str(dev))
+        d_bytes, _, step_bytes = algorithmic_bytes(w, s.plan)
+        step_ms, dec_ms, mer_ms = time_steps(s, dev, flush, args.suite_steps, 5)
+        rec = {
+            "workload": w.name,
+            "kernel": s.kernel,
+            "n_q": w.n_q,
+            "plan": {"work_items": s.plan.num_work, "max_n_splits": s.plan.max_n_splits, "ctas_per_sm": s.plan.opts.ctas_per_sm},
+            "us_per_step": round(step_ms * 1e3, 2),
+            "decode_us": round(dec_ms * 1e3, 2),
+            "merge_us": round(mer_ms * 1e3, 2) if s.plan.max_n_splits > 1 else 0.0,
+            "step_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
+            "frac": round(d_bytes / (dec_ms * 1e-3) / 1e9 / peak, 4),
+            "frac_of_8000_gbs": round(d_bytes / (dec_ms * 1e-3) / 1e9 / 8000.0, 4),
+        }
+        if w.n_q >= 128:
+            rec["tensor_frac"] = round(algorithmic_flops(w) / (dec_ms * 1e-3) / 1e12 / tpk, 4)
+        out.append(rec)
+        del s
+        torch.cuda.empty_cache()
+    return out
 
 
 def plan_device_measure(s, w, dev, flush, launches: int = 200):
@@ -553,6 +660,11 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.suite == -1:
+        # the whole table by default; off when a single workload was asked for
+        flags = (args.variant, args.h_r, args.q_len, args.num_seqs, args.max_splits)
+        explicit = any(f is not None for f in flags) or args.kernel != 0 or "--config" in sys.argv
+        args.suite = 0 if explicit else 1
     if args.impl == "reference":
         if rank != 0:
             return
@@ -666,12 +778,14 @@ def main():
             **({"q_quant": r["q_quant"]} if r["q_quant"] else {}),
             **({"plan_device": r["plan_dev"]} if r["plan_dev"] else {}),
             "clocks": r["clocks"],
+            **({"suite": r["suite"]} if r["suite"] else {}),
         }
         if w.q_len * w.h_r >= 128:
             # at 128 or more packed rows the contraction nears the tensor
             # ridge: its roof beside the HBM one (the kernels issue e4m3
-            # MMAs; with bf16 Q the hi and lo parts of Q and P double the
-            # executed MMA work over these algorithmic flops)
+            # MMAs, timed alone: the burst peak; with bf16 Q the hi and lo
+            # parts of Q and P double the executed MMA work over these
+            # algorithmic flops)
             tpk, tsrc = tensor_peak()
             tfl = algorithmic_flops(w) / (r["decode_ms"] * 1e-3) / 1e12
             line["roofline_tensor"] = {
