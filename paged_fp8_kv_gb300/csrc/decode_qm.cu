@@ -439,11 +439,12 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           }
           if (unmasked) {
   #pragma unroll
-            for (int e = 0; e < kCh; ++e) mt = fmaxf(mt, __uint_as_float(rr[e]));
+            for (int e = 0; e < kCh; e += 2) mt = fmax3(mt, __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
           } else {
   #pragma unroll
-            for (int e = 0; e < kCh; ++e)
-              mt = fmaxf(mt, (key0 + cb + h0 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY);
+            for (int e = 0; e < kCh; e += 2)
+              mt = fmax3(mt, (key0 + cb + h0 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY,
+                         (key0 + cb + h0 + e + 1 <= lim) ? __uint_as_float(rr[e + 1]) : -INFINITY);
           }
         }
         if (!live) mt = -INFINITY;  // keeps the maximum of an empty row at -inf
@@ -474,15 +475,15 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           }
           ptx::tmem_st_wait();
         }
-        // pass 2: x = 448 p 2^-kTau = 256 * 2^((s - m) c + log2 448 - kTau - 8)
-        // in packed halves (ex2.approx.f16x2 of an argument <= 0.81, where
-        // half precision resolves it to 2^-11, times an exact 256; x <= 448
-        // with about 11 significant bits), split x = hi + lo with hi = e4m3(x) and
-        // lo = e4m3(x - hi) (x - hi is exact in half precision); row sums of
-        // x in halves per 16 keys, then in fp32.  Half the exponentials and a
-        // third of the ALU work of an fp32 split.
-        const float bias = fmaf(-mu, c2, kLog2PScale - 8.f);
-        constexpr uint32_t k256x2 = 0x5C005C00u;  // (256, 256) in half precision
+        // pass 2: x = 448 p 2^-kTau = 2^((s - m) c + log2 448 - kTau) in
+        // fp32 (ex2.approx.f32; x <= 448), the row sum of the unrounded x in
+        // fp32, and the MMA operand split x = hi + lo through half precision
+        // (x rounded to 11 significant bits, hi = e4m3(x), lo = e4m3(x - hi),
+        // the difference exact in halves): about 8 significant bits of x in P.
+        // (On GB300 the fp32 exponential issues at the same result rate as the
+        // packed-half one, so nothing is saved by narrowing it.)
+        const float bias = fmaf(-mu, c2, kLog2PScale);
+        const float2 c2x2 = make_float2(c2, c2), bias2 = make_float2(bias, bias);
   #pragma unroll
         for (int h0 = 0; h0 < kR; h0 += kCh) {
           uint32_t rl[kDup > 1 ? 1 : kCh];
@@ -503,7 +504,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           for (int q = 0; q < kCh / 16; ++q) {
             const int cc = (cb + h0) / 16 + q;  // 16-key chunk of the P row
             uint32_t hw[4], lw[4];
-            uint32_t sum2 = 0u;
+            float2 sum2 = make_float2(0.f, 0.f);
   #pragma unroll
             for (int wi = 0; wi < 4; ++wi) {
               uint16_t h8[2], l8[2];
@@ -516,18 +517,20 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                   s0 = (key0 + c <= lim) ? s0 : -INFINITY;
                   s1 = (key0 + c + 1 <= lim) ? s1 : -INFINITY;
                 }
-                const uint32_t x2 = mul_f16x2(ex2_f16x2(f32x2_to_f16x2(fmaf(s0, c2, bias), fmaf(s1, c2, bias))), k256x2);
+                const float2 y = fma2(make_float2(s0, s1), c2x2, bias2);
+                const float x0 = fast_exp2(y.x);
+                const float x1 = fast_exp2(y.y);
+                sum2 = add2(sum2, make_float2(x0, x1));
+                const uint32_t x2 = f32x2_to_f16x2(x0, x1);
                 const uint16_t hi8 = f16x2_to_e4m3x2(x2);
                 const uint32_t hf2 = e4m3x2_to_f16x2(hi8);
                 l8[pr] = f16x2_to_e4m3x2(sub_f16x2(x2, hf2));
                 h8[pr] = hi8;
-                sum2 = add_f16x2(sum2, x2);
               }
               hw[wi] = static_cast<uint32_t>(h8[0]) | (static_cast<uint32_t>(h8[1]) << 16);
               lw[wi] = static_cast<uint32_t>(l8[0]) | (static_cast<uint32_t>(l8[1]) << 16);
             }
-            const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sum2));
-            l_run += sf.x + sf.y;
+            l_run += sum2.x + sum2.y;
             *reinterpret_cast<uint4*>(swz(pbuf, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4*>(swz(pbuf + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
