@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--max_splits", type=int, default=None)
     ap.add_argument("--num_seqs", type=int, default=None, help="smaller batch of the same config (profiling)")
     ap.add_argument("--kv_layout", default="nhd", choices=["nhd", "hnd", "interleaved", "flashinfer"])
+    ap.add_argument("--kv_format", default="e4m3", choices=["e4m3", "e3m2", "e2m3", "e2m1"], help="K/V pool element format")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core (swap-AB), 3 head-grouped tensor-core, 4 query-rows tensor-core")
     ap.add_argument("--l2_prefetch", type=int, default=0, help="0 default, -1 off, 1..8 tiles ahead")
     ap.add_argument("--kv_evict_first", type=int, default=0, help="K/V loads with L2 EVICT_FIRST: 0 default, -1 off, 1 on")
@@ -83,6 +84,7 @@ def workload(args):
         q_len=args.q_len,
         max_splits=args.max_splits,
         num_seqs=args.num_seqs,
+        kv_format=args.kv_format,
     )
 
 
@@ -91,8 +93,13 @@ def describe(w) -> str:
     return (
         f"{w.name}: b={w.num_seqs}, q_len={w.q_len}, h_k={w.h_k}, h_r={w.h_r}, d={w.head_dim}, "
         f"PS={w.page_size}, L in [{int(lens.min())},{int(lens.max())}] (sum {int(lens.sum())}), "
-        f"{'causal' if w.causal else 'non-causal'}, Q {'e4m3' if w.q_is_e4m3 else 'bf16'}, KV e4m3"
+        f"{'causal' if w.causal else 'non-causal'}, Q {'e4m3' if w.q_is_e4m3 else 'bf16'}, KV {w.kv_format}"
     )
+
+
+def syn_bits(w) -> int:
+    """Bits per K/V code of the workload's pool format."""
+    return {"e4m3": 8, "e3m2": 6, "e2m3": 6, "e2m1": 4}[getattr(w, "kv_format", "e4m3")]
 
 
 def algorithmic_bytes(w, plan):
@@ -101,7 +108,7 @@ def algorithmic_bytes(w, plan):
     b, h_k, n_q, d = w.num_seqs, w.h_k, w.n_q, w.head_dim
     lens = w.seq_lens.astype(np.int64)
     qb = 1 if w.q_is_e4m3 else 2
-    kv = int(lens.sum()) * h_k * d * 2
+    kv = int(lens.sum()) * h_k * (d * syn_bits(w) // 8) * 2
     q = b * h_k * n_q * d * qb
     o = b * h_k * n_q * d * 2
     lse = b * h_k * n_q * 4
@@ -363,7 +370,7 @@ def run_mj(args, rank, world, local_rank):
     suite = None
     suite_clocks = None
     if rank == 0 and args.suite == 1:
-        main_key = (args.config, args.variant, args.h_r, args.q_len)
+        main_key = (args.config, args.variant, args.h_r, args.q_len, args.kv_format)
         with ClockSampler(local_rank) as sclk:
             suite = run_suite(args, dev, flush, reuse={main_key: w})
         suite_clocks = sclk.summary()
@@ -406,9 +413,12 @@ def clock_record(timed, before, after, suite):
     }
 
 
-SUITE = [(1, {}), (2, {}), (3, {}), (4, {}), (4, {"variant": "noncausal"})] + [
-    (5, {"h_r": hr, "q_len": ql}) for hr in (16, 32) for ql in (1, 2, 4, 8, 16)
-]
+SUITE = (
+    [(1, {}), (2, {}), (3, {}), (4, {}), (4, {"variant": "noncausal"})]
+    + [(5, {"h_r": hr, "q_len": ql}) for hr in (16, 32) for ql in (1, 2, 4, 8, 16)]
+    # narrow KV pools (fp4 / fp6 codes read by the MMA as they are)
+    + [(2, {"kv_format": "e2m1"}), (3, {"kv_format": "e2m3"}), (4, {"kv_format": "e2m1"}), (4, {"kv_format": "e3m2"})]
+)
 
 
 def run_suite(args, dev, flush, reuse=None):
@@ -424,7 +434,7 @@ def run_suite(args, dev, flush, reuse=None):
     tpk, _ = tensor_peak()
     out = []
     for cfg, opts in SUITE:
-        key = (cfg, opts.get("variant"), opts.get("h_r"), opts.get("q_len"))
+        key = (cfg, opts.get("variant"), opts.get("h_r"), opts.get("q_len"), opts.get("kv_format", "e4m3"))
         w = (reuse or {}).get(key) or syn.config(cfg, **opts)
         s = DecodeSession(w, device=str(dev))
         d_bytes, _, step_bytes = algorithmic_bytes(w, s.plan)
@@ -663,7 +673,7 @@ def main():
     if args.suite == -1:
         # the whole table by default; off when a single workload was asked for
         flags = (args.variant, args.h_r, args.q_len, args.num_seqs, args.max_splits)
-        explicit = any(f is not None for f in flags) or args.kernel != 0 or "--config" in sys.argv
+        explicit = any(f is not None for f in flags) or args.kernel != 0 or "--config" in sys.argv or args.kv_format != "e4m3"
         args.suite = 0 if explicit else 1
     if args.impl == "reference":
         if rank != 0:

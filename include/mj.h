@@ -27,8 +27,9 @@
  *     no state between calls.
  *   - "device" pointers must be valid on the current CUDA device; "host"
  *     pointers are ordinary CPU memory.
- *   - Strides are in ELEMENTS of the tensor they index (K/V elements are
- *     bytes).  The head dimension is always contiguous.
+ *   - Strides are in ELEMENTS of the tensor they index, except the K/V
+ *     strides, which are in bytes (equal to elements for e4m3 pools).  The
+ *     head dimension is always contiguous.
  *   - Every function validates its arguments first and returns an error
  *     code without launching anything when they are bad.
  *   - Launch entry points enqueue on `stream` (a cudaStream_t; NULL is the
@@ -81,12 +82,32 @@ typedef enum { MJ_BF16 = 0, MJ_E4M3 = 1 } mj_dtype;
  *               EVICT_FIRST cache policy (KV is read once; source: the
  *               kernel's `kv_evict_first` option on the
  *               "mjolnir/t5_decode.py" page); 0 = library default (on),
- *               -1 = off, 1 = on; results are identical either way */
+ *               -1 = off, 1 = on; results are identical either way
+ *   kv_format   mj_kv_format of the K/V pools (0 = e4m3) */
 typedef struct {
   int32_t num_seqs, q_len, h_k, h_r, head_dim, page_size;
   int32_t max_blocks, num_pages, causal, q_dtype, max_splits, kernel;
-  int32_t l2_prefetch, kv_evict_first;
+  int32_t l2_prefetch, kv_evict_first, kv_format;
 } mj_decode_params;
+
+/* Element format of the K and V pools (source: the KV-format constants and
+ * the narrow-format helpers of the "mjolnir/t5_decode.py" page).  Every
+ * format is sign | exponent | mantissa with a bias and a subnormal binade;
+ * the narrow ones have no infinities or NaN:
+ *   MJ_KV_E4M3  8 bits, E4M3FN (bias 7, largest 448), one code per byte
+ *   MJ_KV_E3M2  6 bits (bias 3, largest 28)
+ *   MJ_KV_E2M3  6 bits (bias 1, largest 7.5)
+ *   MJ_KV_E2M1  4 bits (bias 1, largest 6)
+ * A row of one kv head is d codes packed little-endian into d*bits/8 bytes:
+ * bit k of element i is bit (bits*i + k) % 8 of byte (bits*i + k) / 8 (fp4:
+ * element 2i in the low nibble of byte i; fp6: four elements in three
+ * bytes).  Every value of the narrow formats is an e4m3 value, so the
+ * operation is unchanged; the tensor-core kernels feed the codes to the MMA
+ * as they are (the TMA spreads each 16-element group over 16 bytes of
+ * shared memory).  Narrow formats need kernel MJ_KERNEL_AUTO,
+ * MJ_KERNEL_TENSOR_CORE or MJ_KERNEL_TENSOR_CORE_QROWS, K/V base pointers
+ * 32-byte aligned and K/V strides multiples of 32 bytes. */
+typedef enum { MJ_KV_E4M3 = 0, MJ_KV_E3M2 = 1, MJ_KV_E2M3 = 2, MJ_KV_E2M1 = 3 } mj_kv_format;
 
 /* Decode kernel families.  Both compute the same function; the choice only
  * changes speed (and last-bit rounding).
@@ -172,9 +193,11 @@ size_t mj_decode_workspace_bytes(const mj_decode_params* params);
  *                (for q_len == 1 vLLM's (b, h_q, d) is already packed);
  *                with num_seqs > 1, q_seq_stride and o_seq_stride are at
  *                least h_k*n_q*d (MJ_ERR_INVALID_ARG otherwise)
- *   k, v         device e4m3 pools; element (page, r, g, i) at
- *                page*x_page + r*x_row + g*x_head + i; every stride a
- *                multiple of 16 bytes (K and V may share one buffer)
+ *   k, v         device pools of kv_format codes; the row of (page, r, g)
+ *                starts at byte page*x_page + r*x_row + g*x_head, and holds
+ *                d codes (d*bits/8 bytes, packed as mj_kv_format says);
+ *                strides are in BYTES, each a multiple of 16 (of 32 for the
+ *                narrow formats); K and V may share one buffer
  *   block_table  device int32 (b, max_blocks); entries past ceil(L/PS) are
  *                never read; entries before must be in [0, num_pages)
  *   seq_lens     device int32[b], the same values the plan saw

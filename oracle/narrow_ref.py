@@ -77,19 +77,18 @@ def minifloat_encode(x: np.ndarray, fmt: str) -> np.ndarray:
 def pack_bits(codes: np.ndarray, bits: int) -> np.ndarray:
     """Little-endian bit stream of the last axis: bit k of element i is
     stream bit bits*i + k, and stream bit j is bit j % 8 of byte j // 8.
-    fp4 needs an even length, fp6 a multiple of 4 (whole bytes)."""
+    fp4 needs an even length, fp6 a multiple of 4 (whole bytes).  One pass
+    per (element, bit), over every row at once."""
     c = np.asarray(codes, dtype=np.int64)
     d = c.shape[-1]
     assert (d * bits) % 8 == 0
     flat = c.reshape(-1, d)
-    out = np.zeros((flat.shape[0], d * bits // 8), dtype=np.uint8)
-    for row in range(flat.shape[0]):
-        for i in range(d):
-            for k in range(bits):
-                if (int(flat[row, i]) >> k) & 1:
-                    j = bits * i + k
-                    out[row, j // 8] |= np.uint8(1 << (j % 8))
-    return out.reshape(*c.shape[:-1], d * bits // 8)
+    out = np.zeros((flat.shape[0], d * bits // 8), dtype=np.int64)
+    for i in range(d):
+        for k in range(bits):
+            j = bits * i + k
+            out[:, j // 8] |= ((flat[:, i] >> k) & 1) << (j % 8)
+    return out.astype(np.uint8).reshape(*c.shape[:-1], d * bits // 8)
 
 
 def unpack_bits(packed: np.ndarray, bits: int, d: int) -> np.ndarray:
@@ -97,15 +96,12 @@ def unpack_bits(packed: np.ndarray, bits: int, d: int) -> np.ndarray:
     stream bits bits*i .. bits*i + bits - 1, least significant first."""
     p = np.asarray(packed, dtype=np.int64)
     flat = p.reshape(-1, p.shape[-1])
-    out = np.zeros((flat.shape[0], d), dtype=np.uint8)
-    for row in range(flat.shape[0]):
-        for i in range(d):
-            v = 0
-            for k in range(bits):
-                j = bits * i + k
-                v |= ((int(flat[row, j // 8]) >> (j % 8)) & 1) << k
-            out[row, i] = v
-    return out.reshape(*p.shape[:-1], d)
+    out = np.zeros((flat.shape[0], d), dtype=np.int64)
+    for i in range(d):
+        for k in range(bits):
+            j = bits * i + k
+            out[:, i] |= ((flat[:, j // 8] >> (j % 8)) & 1) << k
+    return out.astype(np.uint8).reshape(*p.shape[:-1], d)
 
 
 def to_e4m3_codes(codes: np.ndarray, fmt: str, e4m3_table: np.ndarray) -> np.ndarray:

@@ -31,6 +31,12 @@ MJ_ERR_TIMEOUT = 5
 MJ_BF16 = 0
 MJ_E4M3 = 1
 
+MJ_KV_E4M3 = 0
+MJ_KV_E3M2 = 1
+MJ_KV_E2M3 = 2
+MJ_KV_E2M1 = 3
+KV_FORMATS = {"e4m3": MJ_KV_E4M3, "e3m2": MJ_KV_E3M2, "e2m3": MJ_KV_E2M3, "e2m1": MJ_KV_E2M1}
+
 MJ_KERNEL_AUTO = 0
 MJ_KERNEL_CUDA_CORE = 1
 MJ_KERNEL_TENSOR_CORE = 2
@@ -62,6 +68,7 @@ class DecodeParams(ctypes.Structure):
             "kernel",
             "l2_prefetch",
             "kv_evict_first",
+            "kv_format",
         )
     ]
 
@@ -186,6 +193,7 @@ def make_params(
     kernel: int = MJ_KERNEL_AUTO,
     l2_prefetch: int = 0,
     kv_evict_first: int = 0,
+    kv_format: int = MJ_KV_E4M3,
 ) -> DecodeParams:
     return DecodeParams(
         num_seqs,
@@ -202,6 +210,7 @@ def make_params(
         kernel,
         l2_prefetch,
         kv_evict_first,
+        kv_format,
     )
 
 

@@ -206,6 +206,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     if (lane == 0) ptx::prefetch_tmap(tmap);
     const bool evict_first = a.kv_evict_first != 0;
     const uint64_t kv_policy = ptx::policy_evict_first();
+    const uint32_t tile_tx = kv_box_bytes(a.kv_format, kRows);
     // a tile spans nbox whole blocks (or lies in one block) and the window
     // starts at the item's first block, so a tile never straddles windows
     int wbase = key_begin / PS;
@@ -231,7 +232,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const int pg = __shfl_sync(0xffffffffu, win, (key / PS - wbase) & 31);
       const int page = (active && key < L) ? pg : a.num_pages;
       const int row_off = key % PS;
-      if (lane == 0) ptx::mbar_arrive_expect_tx(full(st), kTileBytes);
+      if (lane == 0) ptx::mbar_arrive_expect_tx(full(st), tile_tx);  // packed bytes read
       __syncwarp();
       if (active)
         ptx::tma_load_kv(ring + st * kTileBytes + lane * box_rows * 128, tmap, full(st), 0, row_off, g, page,
@@ -250,8 +251,10 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     if (lane == 0) {
       const bool gemm1 = warp == 1;
       bool ok = ptx::mbar_wait_bounded(qready, 0, abort_flag, kWaitNs);
-      const uint32_t idesc_s = ptx::idesc_e4m3(kRows, kRows, false, false);  // S = Q K^T
-      const uint32_t idesc_o = ptx::idesc_e4m3(kRows, kRows, false, true);   // O = P V, V MN-major
+      // A = e4m3 (Q and P parts), B = the K / V tile in the pool's format
+      const uint32_t kv_fmt = kv_mma_format(a.kv_format);
+      const uint32_t idesc_s = ptx::idesc_f8f6f4(kRows, kRows, false, false, 0, kv_fmt);  // S = Q K^T
+      const uint32_t idesc_o = ptx::idesc_f8f6f4(kRows, kRows, false, true, 0, kv_fmt);   // O = P V, V MN-major
       const uint64_t qdesc = ptx::smem_desc(sbase + C::kOffQ, 16, 1024, ptx::kSwizzle128B);
       const uint64_t kdesc0 = ptx::smem_desc(sbase + C::kOffK, 16, 1024, ptx::kSwizzle128B);
       const uint64_t pdesc0 = ptx::smem_desc(sbase + C::kOffP, 16, 1024, ptx::kSwizzle128B);
@@ -687,8 +690,10 @@ cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   using C = QmCfg<kQe4m3>;
   const int box_rows = a.page_size < kRows ? a.page_size : kRows;
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, box_rows, 1) ||
-      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, box_rows, 1))
+  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, box_rows, 1,
+                   a.kv_format) ||
+      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, box_rows, 1,
+                   a.kv_format))
     return cudaErrorInvalidValue;
   auto kern = decode_qm_kernel<kQe4m3, kDup>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);

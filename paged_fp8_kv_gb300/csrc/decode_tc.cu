@@ -74,7 +74,7 @@ EncodeTiledFn encode_fn() {
 // is box_rows rows of box_heads heads: 128 bytes x box_rows x box_heads,
 // head-major in shared memory, 128-byte swizzle.
 bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, int num_pages, int64_t s_row,
-                 int64_t s_head, int64_t s_page, int box_rows, int box_heads) {
+                 int64_t s_head, int64_t s_page, int box_rows, int box_heads, int kv_format) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(h_k),
@@ -83,7 +83,10 @@ bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, in
                                  static_cast<cuuint64_t>(s_page)};
   const cuuint32_t box[4] = {128, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_heads), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(base), dims, strides, box, estr,
+  const CUtensorMapDataType type = kv_format == 0   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : kv_format == 3 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B
+                                                    : CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B;
+  const CUresult r = enc(m, type, 4, const_cast<uint8_t*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -292,6 +295,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     }
     const bool evict_first = a.kv_evict_first != 0;
     const uint64_t kv_policy = ptx::policy_evict_first();
+    const uint32_t tile_tx = kv_box_bytes(a.kv_format, kTileKV);
     int next_page = (lane < ppt && t_begin * ppt + lane < valid_pages) ? first_page_raw : a.num_pages;
     int issued = 0;
     for (int i = 0; i < T; ++i) {
@@ -320,9 +324,9 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       }
       const uint32_t dk = sbase + C::kOffK + st * kKVTileBytes;
       const uint32_t dv = sbase + C::kOffV + st * kKVTileBytes;
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar.kfull + 8 * st, kKVTileBytes);
-        ptx::mbar_arrive_expect_tx(bar.vfull + 8 * st, kKVTileBytes);
+      if (lane == 0) {  // the packed bytes the tile's boxes read (16 KB for e4m3)
+        ptx::mbar_arrive_expect_tx(bar.kfull + 8 * st, tile_tx);
+        ptx::mbar_arrive_expect_tx(bar.vfull + 8 * st, tile_tx);
       }
       __syncwarp();
       if (lane < ppt) {
@@ -344,8 +348,10 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t idesc_s = ptx::idesc_e4m3(kTileKV, C::kN1, false, false);  // S = K Q^T
-      const uint32_t idesc_o = ptx::idesc_e4m3(kTileKV, C::kN2, true, true);    // O = V^T P
+      // A = the K / V tile in the pool's format, B = e4m3 (Q and P parts)
+      const uint32_t kv_fmt = kv_mma_format(a.kv_format);
+      const uint32_t idesc_s = ptx::idesc_f8f6f4(kTileKV, C::kN1, false, false, kv_fmt, 0);  // S = K Q^T
+      const uint32_t idesc_o = ptx::idesc_f8f6f4(kTileKV, C::kN2, true, true, kv_fmt, 0);    // O = V^T P
       const uint32_t q_base = sbase + C::kOffQ;
       bool ok = ptx::mbar_wait_bounded(bar.qready, 0, abort_flag, kWaitNs);
       // Issue GEMM1 and GEMM2 as their inputs become ready, whichever comes
@@ -827,8 +833,10 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 template <int R, bool kQe4m3>
 cudaError_t launch_tc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, a.page_size, 1) ||
-      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, a.page_size, 1))
+  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, a.page_size, 1,
+                   a.kv_format) ||
+      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, a.page_size, 1,
+                   a.kv_format))
     return cudaErrorInvalidValue;
   const int smem = TcCfg<R, kQe4m3>::kBytes;
   auto kern = decode_tc_kernel<R, kQe4m3>;
@@ -878,7 +886,7 @@ __global__ void __launch_bounds__(64) gather_kv_kernel(const DecodeDev a, const 
     const int page = (lane < ppt && blk < valid_pages)
                          ? a.block_table[static_cast<int64_t>(b) * a.max_blocks + blk]
                          : a.num_pages;
-    if (lane == 0) ptx::mbar_arrive_expect_tx(bar, kKVTileBytes);
+    if (lane == 0) ptx::mbar_arrive_expect_tx(bar, kv_box_bytes(a.kv_format, kTileKV));
     __syncwarp();
     if (lane < ppt) ptx::tma_load_4d(tile_s + lane * PS * 128, &tmap, bar, 0, 0, g, page);
   }
@@ -940,9 +948,9 @@ cudaError_t launch_bounded_wait(int32_t* status, int64_t* waited_ns, uint64_t li
 cudaError_t launch_gather_kv(const DecodeDev& a, bool values, uint8_t* out, int out_rows, cudaStream_t stream) {
   CUtensorMap m;
   const bool ok = values ? make_kv_map(&m, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page,
-                                       a.page_size, 1)
+                                       a.page_size, 1, a.kv_format)
                          : make_kv_map(&m, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page,
-                                       a.page_size, 1);
+                                       a.page_size, 1, a.kv_format);
   if (!ok) return cudaErrorInvalidValue;
   const int tiles = (out_rows + kTileKV - 1) / kTileKV;
   const int smem = kKVTileBytes + 1024 + 64;  // tile, alignment slack, mbarrier

@@ -1247,8 +1247,9 @@ cudaError_t launch_tcg(const DecodeDev& a, int n_q_tiles, int* sched, int sm_cou
   const int box_rows = C::KR < a.page_size ? C::KR : a.page_size;
   const int box_heads = box_rows == C::KR ? G : 1;
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, box_rows, box_heads) ||
-      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, box_rows, box_heads))
+  if (a.kv_format != 0) return cudaErrorInvalidValue;  // e4m3 pools only (validated before)
+  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, box_rows, box_heads, 0) ||
+      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, box_rows, box_heads, 0))
     return cudaErrorInvalidValue;
   auto kern = decode_tcg_kernel<G, RH, kQe4m3>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);

@@ -54,6 +54,29 @@ int device_sm_count() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+const char* kv_format_name(int f) {
+  switch (f) {
+    case MJ_KV_E3M2: return "e3m2";
+    case MJ_KV_E2M3: return "e2m3";
+    case MJ_KV_E2M1: return "e2m1";
+    default: return "e4m3";
+  }
+}
+
+// K/V pool pointers and byte strides: 16-byte aligned (the page gathers'
+// TMA boxes), 32-byte aligned for the packed narrow formats (their TMA
+// element types require it).
+bool kv_layout_ok(const mj_decode_params& p, const void* k, const void* v, const int64_t (&strides)[6]) {
+  const bool narrow = p.kv_format != MJ_KV_E4M3;
+  if (!aligned16(k) || !aligned16(v)) return false;
+  if (narrow && (!aligned32(k) || !aligned32(v))) return false;
+  const int64_t mask = narrow ? 31 : 15;
+  for (int64_t s : strides)
+    if (s <= 0 || (s & mask) != 0 || s >= (int64_t{1} << 40)) return false;
+  return true;
+}
 
 constexpr int kDefaultL2Prefetch = 0;  // tiles; measured choice
 constexpr int kDefaultKvEvictFirst = 1;  // measured choice (faster on every workload)
@@ -155,7 +178,11 @@ extern "C" mj_status mj_kernel_name(const mj_decode_params* params, char* buf, i
   const mj_status st = check_params(params);
   if (st != MJ_OK) return st;
   if (!buf || len < 1) return MJ_ERR_INVALID_ARG;
-  std::snprintf(buf, static_cast<size_t>(len), "%s", choose_kernel(*params).name);
+  if (params->kv_format == MJ_KV_E4M3)
+    std::snprintf(buf, static_cast<size_t>(len), "%s", choose_kernel(*params).name);
+  else  // the KV format a narrow-pool launch reads, appended
+    std::snprintf(buf, static_cast<size_t>(len), "%s_kv%s", choose_kernel(*params).name,
+                  kv_format_name(params->kv_format));
   return MJ_OK;
 }
 
@@ -170,11 +197,8 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
       !a.k_descale || !a.v_descale || !a.o || !a.lse)
     return MJ_ERR_INVALID_ARG;
   if (a.num_work < 1) return MJ_ERR_INVALID_ARG;
-  // 16-byte page gathers: base pointers and every KV stride 16-byte aligned
-  if (!aligned16(a.k) || !aligned16(a.v)) return MJ_ERR_INVALID_ARG;
   const int64_t kv_strides[6] = {a.k_page, a.k_row, a.k_head, a.v_page, a.v_row, a.v_head};
-  for (int64_t s : kv_strides)
-    if (s <= 0 || (s & 15) != 0 || s >= (int64_t{1} << 40)) return MJ_ERR_INVALID_ARG;
+  if (!kv_layout_ok(p, a.k, a.v, kv_strides)) return MJ_ERR_INVALID_ARG;
   const int q_bytes = p.q_dtype == MJ_E4M3 ? 1 : 2;
   if (!aligned16(a.q) || !aligned16(a.o)) return MJ_ERR_INVALID_ARG;
   if (a.q_seq_stride < 0 || ((a.q_seq_stride * q_bytes) & 15) != 0) return MJ_ERR_INVALID_ARG;
@@ -244,6 +268,7 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   d.num_pages = p.num_pages;
   d.l2_prefetch = p.l2_prefetch == 0 ? kDefaultL2Prefetch : (p.l2_prefetch < 0 ? 0 : p.l2_prefetch);
   d.kv_evict_first = p.kv_evict_first == 0 ? kDefaultKvEvictFirst : (p.kv_evict_first > 0 ? 1 : 0);
+  d.kv_format = p.kv_format;
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
@@ -256,10 +281,11 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   if (verbose())
     std::fprintf(stderr,
                  "mj_decode_attn: kernel=%s num_seqs=%d h_k=%d n_q=%d (q_len %d x h_r %d) page_size=%d %s "
-                 "q=%s work_items=%d merge=%s (max_n_splits %d of max_splits %d) kv_evict_first=%d\n",
+                 "q=%s kv=%s work_items=%d merge=%s (max_n_splits %d of max_splits %d) kv_evict_first=%d\n",
                  kc.name, p.num_seqs, p.h_k, p.q_len * p.h_r, p.q_len, p.h_r, p.page_size,
-                 p.causal ? "causal" : "non-causal", p.q_dtype == MJ_E4M3 ? "e4m3" : "bf16", a.num_work,
-                 merge ? "yes" : "no", merge_splits, p.max_splits, d.kv_evict_first);
+                 p.causal ? "causal" : "non-causal", p.q_dtype == MJ_E4M3 ? "e4m3" : "bf16",
+                 kv_format_name(p.kv_format), a.num_work, merge ? "yes" : "no", merge_splits, p.max_splits,
+                 d.kv_evict_first);
   // an NVTX range around the launches, so a profiler's timeline names them
   nvtxRangePushA("mj_decode_attn");
   struct RangeEnd {
@@ -321,11 +347,11 @@ extern "C" mj_status mj_check_gather_kv(const mj_decode_params* params, const mj
   if (st != MJ_OK) return st;
   if (!args || !out || !aligned16(out) || out_rows < 1 || values < 0 || values > 1) return MJ_ERR_INVALID_ARG;
   const mj_decode_args& a = *args;
-  if (!a.k || !a.v || !a.block_table || !a.seq_lens || !aligned16(a.k) || !aligned16(a.v)) return MJ_ERR_INVALID_ARG;
+  if (!a.k || !a.v || !a.block_table || !a.seq_lens) return MJ_ERR_INVALID_ARG;
   const int64_t kv_strides[6] = {a.k_page, a.k_row, a.k_head, a.v_page, a.v_row, a.v_head};
-  for (int64_t s : kv_strides)
-    if (s <= 0 || (s & 15) != 0 || s >= (int64_t{1} << 40)) return MJ_ERR_INVALID_ARG;
+  if (!kv_layout_ok(*params, a.k, a.v, kv_strides)) return MJ_ERR_INVALID_ARG;
   DecodeDev d{};
+  d.kv_format = params->kv_format;
   d.k = a.k;
   d.v = a.v;
   d.k_page = a.k_page;

@@ -35,7 +35,23 @@ struct DecodeDev {
   int32_t num_pages;
   int32_t l2_prefetch;     // tiles the producer prefetches into L2 ahead (0 = off)
   int32_t kv_evict_first;  // K/V tile loads with an L2 EVICT_FIRST policy (0 = off)
+  int32_t kv_format;       // mj_kv_format of the K/V pools
 };
+
+// Bits per K/V code of a pool format (mj_kv_format: e4m3, e3m2, e2m3, e2m1).
+__host__ __device__ constexpr int kv_bits(int kv_format) { return kv_format == 0 ? 8 : (kv_format == 3 ? 4 : 6); }
+
+// The kind::f8f6f4 operand format code of a pool format.
+__host__ __device__ constexpr uint32_t kv_mma_format(int kv_format) {
+  return kv_format == 1 ? 4u : (kv_format == 2 ? 3u : (kv_format == 3 ? 5u : 0u));
+}
+
+// Bytes a TMA load of `rows` K/V rows (one head, d = 128 codes each) reads
+// from global memory and credits to its mbarrier: the packed size (the
+// shared-memory copy of a narrow row takes 128 bytes whatever the format).
+__host__ __device__ constexpr uint32_t kv_box_bytes(int kv_format, int rows) {
+  return static_cast<uint32_t>(rows) * 16u * static_cast<uint32_t>(kv_bits(kv_format));
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 

@@ -41,8 +41,12 @@ int qm_smem_bytes(bool q_e4m3);
 // TMA descriptor of a paged e4m3 pool seen as (d bytes, rows in page, kv
 // heads, pages); one box is box_rows rows of box_heads heads (head-major in
 // shared memory), 128-byte swizzle.
+// Strides are in bytes.  kv_format picks the element type: e4m3 codes are
+// bytes; the narrow formats are read packed (16 codes in 8 or 12 bytes) and
+// land 16 codes per 16 bytes of shared memory, the operand form of the
+// kind::f8f6f4 MMA.
 bool make_kv_map(CUtensorMap* m, const uint8_t* base, int page_size, int h_k, int num_pages, int64_t s_row,
-                 int64_t s_head, int64_t s_page, int box_rows, int box_heads);
+                 int64_t s_head, int64_t s_page, int box_rows, int box_heads, int kv_format);
 
 // Merge of split sequences' partials into O / LSE; max_n_splits (> 1) sizes
 // the number of warps that share one row.

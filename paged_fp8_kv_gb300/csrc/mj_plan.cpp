@@ -37,6 +37,11 @@ mj_status check_params(const mj_decode_params* p) {
   if (p->kernel < MJ_KERNEL_AUTO || p->kernel > MJ_KERNEL_TENSOR_CORE_QROWS) return MJ_ERR_INVALID_ARG;
   if (p->l2_prefetch < -1 || p->l2_prefetch > 8) return MJ_ERR_INVALID_ARG;
   if (p->kv_evict_first < -1 || p->kv_evict_first > 1) return MJ_ERR_INVALID_ARG;
+  if (p->kv_format < MJ_KV_E4M3 || p->kv_format > MJ_KV_E2M1) return MJ_ERR_INVALID_ARG;
+  // narrow pools: the tensor-core kernels only (the MMA reads the codes)
+  if (p->kv_format != MJ_KV_E4M3 && p->kernel != MJ_KERNEL_AUTO && p->kernel != MJ_KERNEL_TENSOR_CORE &&
+      p->kernel != MJ_KERNEL_TENSOR_CORE_QROWS)
+    return MJ_ERR_UNSUPPORTED;
   // int32 index ranges used by the kernels
   const int64_t n_q = static_cast<int64_t>(p->q_len) * p->h_r;
   if (n_q > 4096 || static_cast<int64_t>(p->num_seqs) * p->h_k * n_q > (int64_t{1} << 30))

@@ -229,6 +229,13 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with the A and B operand formats of kind::f8f6f4 (bits 7..9 and
+// 10..12): e4m3 0, e3m2 4, e2m3 3, e2m1 5.
+__host__ __device__ constexpr uint32_t idesc_f8f6f4(int M, int N, bool a_mn_major, bool b_mn_major, uint32_t a_fmt,
+                                                   uint32_t b_fmt) {
+  return idesc_e4m3(M, N, a_mn_major, b_mn_major) | (a_fmt << 7) | (b_fmt << 10);
+}
+
 __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(

@@ -16,6 +16,7 @@ from . import (
     decode_attn,
     decode_plan,
     kernel_name,
+    KV_FORMATS,
     make_params,
     pack_q,
     unpack_o,
@@ -65,6 +66,7 @@ class DecodeSession:
             kernel,
             l2_prefetch,
             kv_evict_first,
+            KV_FORMATS[getattr(w, "kv_format", "e4m3")],
         )
         self.kernel = kernel_name(self.params)
         if sm_count is None:
@@ -72,7 +74,8 @@ class DecodeSession:
         self.sm_count = int(sm_count)
 
         # KV cache in the requested physical layout, exposed as logical
-        # (num_pages, PS, h_k, d) byte views.
+        # (num_pages, PS, h_k, row bytes) byte views (row bytes = d for e4m3,
+        # d * bits / 8 for the packed narrow formats).
         k = torch.from_numpy(w.k_cache)
         v = torch.from_numpy(w.v_cache)
         if kv_layout == "nhd":
@@ -86,8 +89,9 @@ class DecodeSession:
         elif kv_layout == "interleaved":  # (pages, h_k, PS, 2d)
             buf = torch.cat([k.permute(0, 2, 1, 3), v.permute(0, 2, 1, 3)], dim=-1).contiguous().to(dev)
             kv = buf.transpose(1, 2)
-            self.k_cache = kv[..., : self.d]
-            self.v_cache = kv[..., self.d :]
+            rb = k.shape[-1]
+            self.k_cache = kv[..., :rb]
+            self.v_cache = kv[..., rb:]
             self._kv_buf = buf
         elif kv_layout == "flashinfer":  # (pages, 2, PS, h_k, d)
             buf = torch.stack([k, v], dim=1).contiguous().to(dev)

@@ -72,6 +72,52 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
     return code
 
 
+# Narrow KV formats: (exponent bits, mantissa bits, bias); sign bit on top,
+# a subnormal binade at exponent 0, no infinities or NaN.
+NARROW_FORMATS = {"e3m2": (3, 2, 3), "e2m3": (2, 3, 1), "e2m1": (2, 1, 1)}
+KV_FORMAT_CODE = {"e4m3": 0, "e3m2": 1, "e2m3": 2, "e2m1": 3}
+KV_FORMAT_BITS = {"e4m3": 8, "e3m2": 6, "e2m3": 6, "e2m1": 4}
+
+
+def _narrow_magnitudes(fmt: str) -> np.ndarray:
+    """The non-negative values of a narrow format, indexed by magnitude code
+    (ascending)."""
+    eb, mb, bias = NARROW_FORMATS[fmt]
+    e = np.arange(1 << (eb + mb)) >> mb
+    m = np.arange(1 << (eb + mb)) & ((1 << mb) - 1)
+    frac = m.astype(np.float64) / (1 << mb)
+    return np.where(e == 0, frac * 2.0 ** (1 - bias), (1.0 + frac) * 2.0 ** (e - bias))
+
+
+def narrow_encode(x: np.ndarray, fmt: str) -> np.ndarray:
+    """Round float values to a narrow format's codes: nearest value, a value
+    half-way between two taking the smaller magnitude (the rounding of the
+    narrow-format quantiser on the "mjolnir/t5_decode.py" page), saturating at
+    the largest; the sign bit only on a non-zero magnitude."""
+    mags = _narrow_magnitudes(fmt)
+    eb, mb, _ = NARROW_FORMATS[fmt]
+    mids = (mags[:-1] + mags[1:]) / 2.0
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    mag = np.searchsorted(mids, a, side="left").astype(np.uint8)  # ties stay below the midpoint
+    neg = (np.asarray(x) < 0) & (mag > 0)
+    return mag | np.where(neg, np.uint8(1 << (eb + mb)), np.uint8(0))
+
+
+def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
+    """Little-endian packing of the last axis (fp4: element 2i in the low
+    nibble of byte i; fp6: each four elements in three bytes, element j of the
+    group at bits 6j .. 6j + 5 of the little-endian 24-bit word)."""
+    c = np.asarray(codes, dtype=np.uint32)
+    d = c.shape[-1]
+    if bits == 4:
+        c = c.reshape(*c.shape[:-1], d // 2, 2)
+        return (c[..., 0] | (c[..., 1] << 4)).astype(np.uint8)
+    c = c.reshape(*c.shape[:-1], d // 4, 4)
+    word = c[..., 0] | (c[..., 1] << 6) | (c[..., 2] << 12) | (c[..., 3] << 18)
+    out = np.stack([word & 0xFF, (word >> 8) & 0xFF, (word >> 16) & 0xFF], axis=-1)
+    return out.reshape(*c.shape[:-2], d // 4 * 3).astype(np.uint8)
+
+
 def bf16_encode(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bf16 bit patterns (nearest, ties to even)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
@@ -114,6 +160,7 @@ class Workload:
     scale_o: float = 1.0
     max_splits: int = 16
     head_dim: int = HEAD_DIM
+    kv_format: str = "e4m3"  # e4m3, or a narrow format packed little-endian
     meta: Dict[str, object] = field(default_factory=dict)
 
     @property
@@ -173,7 +220,8 @@ class Workload:
 
     def kv_bytes(self) -> int:
         """K + V bytes of the rows the attention reads (rows < L)."""
-        return int(self.seq_lens.astype(np.int64).sum()) * self.h_k * self.head_dim * 2
+        row = self.head_dim * KV_FORMAT_BITS[self.kv_format] // 8
+        return int(self.seq_lens.astype(np.int64).sum()) * self.h_k * row * 2
 
 
 def _fill_kv(
@@ -183,13 +231,15 @@ def _fill_kv(
     block_table: np.ndarray,
     seq_lens: np.ndarray,
     descale: np.ndarray,
+    kv_format: str = "e4m3",
 ) -> None:
     """Quantised N(0,1)/descale rows for every (seq, page, row < L); the rest
     of the pool keeps the poison code it was created with.  Sequence b draws
     from its own stream, SeedSequence([seed, tag, b]), so sequences can be
     filled in parallel threads with a result that does not depend on the
-    thread count."""
-    PS, h_k, d = cache.shape[1], cache.shape[2], cache.shape[3]
+    thread count.  Narrow formats are packed (d * bits / 8 bytes a row)."""
+    PS, h_k = cache.shape[1], cache.shape[2]
+    d = HEAD_DIM
 
     def one(b: int) -> None:
         L = int(seq_lens[b])
@@ -200,9 +250,12 @@ def _fill_kv(
         pages = block_table[b, :n_pages]
         x = rng.standard_normal((n_pages * PS, h_k, d), dtype=np.float32)
         x /= descale[b].astype(np.float32)[None, :, None]
-        codes = e4m3_encode(x)
-        codes[L:] = E4M3_NAN  # rows past the sequence end
-        cache[pages] = codes.reshape(n_pages, PS, h_k, d)
+        if kv_format == "e4m3":
+            codes = e4m3_encode(x)
+        else:
+            codes = pack_codes(narrow_encode(x, kv_format), KV_FORMAT_BITS[kv_format])
+        codes[L:] = E4M3_NAN  # rows past the sequence end (poison bytes)
+        cache[pages] = codes.reshape(n_pages, PS, h_k, cache.shape[3])
 
     workers = min(len(seq_lens), os.cpu_count() or 1)
     if workers <= 1:
@@ -230,6 +283,7 @@ def make_workload(
     num_pages: Optional[int] = None,
     scale_o: float = 1.0,
     softmax_scale: Optional[float] = None,
+    kv_format: str = "e4m3",
 ) -> Workload:
     rng = np.random.Generator(np.random.PCG64(seed))
     b = len(seq_lens)
@@ -259,10 +313,11 @@ def make_workload(
     k_desc = descales()
     v_desc = descales()
     q_desc = descales() if q_is_e4m3 else np.ones((b, h_k), dtype=np.float32)
-    k_cache = np.full((num_pages, page_size, h_k, d), E4M3_NAN, dtype=np.uint8)
-    v_cache = np.full((num_pages, page_size, h_k, d), E4M3_NAN, dtype=np.uint8)
-    _fill_kv(seed, 1, k_cache, bt, seq, k_desc)
-    _fill_kv(seed, 2, v_cache, bt, seq, v_desc)
+    row_bytes = d * KV_FORMAT_BITS[kv_format] // 8
+    k_cache = np.full((num_pages, page_size, h_k, row_bytes), E4M3_NAN, dtype=np.uint8)
+    v_cache = np.full((num_pages, page_size, h_k, row_bytes), E4M3_NAN, dtype=np.uint8)
+    _fill_kv(seed, 1, k_cache, bt, seq, k_desc, kv_format)
+    _fill_kv(seed, 2, v_cache, bt, seq, v_desc, kv_format)
     h_q = h_k * h_r
     qx = rng.standard_normal((b * q_len, h_q, d), dtype=np.float32)
     if q_is_e4m3:
@@ -292,6 +347,7 @@ def make_workload(
         softmax_scale=1.0 / math.sqrt(d) if softmax_scale is None else softmax_scale,
         scale_o=scale_o,
         max_splits=max_splits,
+        kv_format=kv_format,
         meta={"seed": seed},
     )
 
@@ -319,15 +375,20 @@ def config(
     q_len: Optional[int] = None,
     max_splits: Optional[int] = None,
     seed: Optional[int] = None,
+    kv_format: str = "e4m3",
 ) -> Workload:
     """Workload of a named config (1..5).  Keyword overrides shrink it for
     parity tests (fewer sequences, shorter lengths) while keeping its
     structure; ``variant="noncausal"`` gives config 4's q_len = 5 block
     attention variant."""
+    def mk(name, *args, **kw):
+        suffix = "" if kv_format == "e4m3" else "_kv" + kv_format
+        return make_workload(name + suffix, *args, kv_format=kv_format, **kw)
+
     seed = 1111 + idx if seed is None else seed
     rng = np.random.Generator(np.random.PCG64(seed + 7919))
     if idx == 1:
-        return make_workload(
+        return mk(
             CONFIG_NAMES[1],
             [37, 100] if len_range is None else list(rng.integers(len_range[0], len_range[1] + 1, num_seqs or 2)),
             1,
@@ -343,12 +404,12 @@ def config(
         b = 64 if num_seqs is None else num_seqs
         lo, hi = (512, 8192) if len_range is None else len_range
         lens = rng.integers(lo, hi + 1, size=b)
-        return make_workload(CONFIG_NAMES[2], lens, 1, 8, 4, 16, seed=seed, max_splits=max_splits or 16)
+        return mk(CONFIG_NAMES[2], lens, 1, 8, 4, 16, seed=seed, max_splits=max_splits or 16)
     if idx == 3:
         b = 8 if num_seqs is None else num_seqs
         long_len, short = (131072, 1024) if len_range is None else len_range
         lens = [long_len] + list(short + rng.integers(-64, 65, size=b - 1))
-        return make_workload(
+        return mk(
             CONFIG_NAMES[3], lens, 1, 1, 16, 128, seed=seed, q_is_e4m3=True, max_splits=max_splits or 256
         )
     if idx == 4:
@@ -357,7 +418,7 @@ def config(
         lens = rng.integers(lo, hi + 1, size=b)
         noncausal = variant == "noncausal"
         ql = (5 if noncausal else 4) if q_len is None else q_len
-        return make_workload(
+        return mk(
             CONFIG_NAMES[4] + ("_noncausal" if noncausal else ""),
             lens,
             ql,
@@ -373,7 +434,7 @@ def config(
         L = 16384 if len_range is None else len_range[1]
         hr = 16 if h_r is None else h_r
         ql = 1 if q_len is None else q_len
-        return make_workload(
+        return mk(
             f"{CONFIG_NAMES[5]}_hr{hr}_q{ql}",
             [L] * b,
             ql,

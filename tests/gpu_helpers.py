@@ -21,7 +21,10 @@ def o_tol(w):
 def compare(w, o_gpu, lse_gpu, units=None, threads=0):
     """o_gpu (b, h_k, n_q, d) float, lse_gpu (b, h_k, n_q) float: assert
     |o - ref| <= atol + rtol |ref| and |lse - ref| <= 2e-3 on the given (b, g)
-    units (all when None).  Returns the worst errors for reporting."""
+    units (all when None).  Returns the worst errors for reporting.  A
+    narrow-KV workload is compared through its e4m3 view."""
+    if getattr(w, "kv_format", "e4m3") != "e4m3":
+        w = e4m3_view(w, None if units is None else sorted({b for b, _ in units}))
     if units is None:
         ref_o, ref_lse = oracle.attention(w, threads=threads)
         got_o, got_lse = o_gpu, lse_gpu
@@ -49,3 +52,31 @@ def sample_units(w, n, seed=0, include=()):
     while len(units) < min(n, w.num_seqs * w.h_k):
         units.add((int(rng.integers(w.num_seqs)), int(rng.integers(w.h_k))))
     return sorted(units)
+
+
+def e4m3_view(w, seqs=None):
+    """A narrow-KV workload as the same attention problem over e4m3 pools:
+    every narrow value is an e4m3 value, so the oracle's unpacking and its
+    exact code map (oracle.narrow_ref) turn the packed rows into e4m3 rows of
+    equal value.  Only the pages of `seqs` (all when None) are converted; the
+    rest of the view stays zero (the oracle never reads them)."""
+    import copy
+
+    from oracle import narrow_ref
+
+    if w.kv_format == "e4m3":
+        return w
+    bits = narrow_ref.BITS[w.kv_format]
+    e4 = oracle.e4m3_table()
+    v = copy.copy(w)
+    v.kv_format = "e4m3"
+    for name in ("k_cache", "v_cache"):
+        src = getattr(w, name)
+        dst = np.zeros(src.shape[:3] + (w.head_dim,), dtype=np.uint8)
+        bs = range(w.num_seqs) if seqs is None else seqs
+        pages = sorted({int(p) for b in bs for p in w.block_table[b, : -(-int(w.seq_lens[b]) // w.page_size)]})
+        if pages:
+            codes = narrow_ref.unpack_bits(src[pages], bits, w.head_dim)
+            dst[pages] = narrow_ref.to_e4m3_codes(codes, w.kv_format, e4)
+        setattr(v, name, dst)
+    return v

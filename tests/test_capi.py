@@ -404,3 +404,28 @@ def test_verbose_switch_prints_the_plan_and_nothing_without_it():
     env["MJ_VERBOSE"] = "0"
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True)
     assert "SplitPlan" not in out.stderr
+
+
+def test_narrow_kv_format_validation():
+    p = _params(1, h_r=4, max_splits=16)
+    p.kv_format = 4
+    assert _attn_status(p, _good_args()) == mj.MJ_ERR_INVALID_ARG
+    for kernel in (mj.MJ_KERNEL_CUDA_CORE, mj.MJ_KERNEL_TENSOR_CORE_GROUPED):
+        q = _params(1, h_k=8, h_r=4, max_splits=16, kernel=kernel)
+        q.kv_format = mj.MJ_KV_E2M1
+        buf = ctypes.create_string_buffer(64)
+        assert mj.lib().mj_kernel_name(ctypes.byref(q), buf, 64) == mj.MJ_ERR_UNSUPPORTED
+    q = _params(1, h_r=4, max_splits=16)
+    q.kv_format = mj.MJ_KV_E3M2
+    buf = ctypes.create_string_buffer(64)
+    assert mj.lib().mj_kernel_name(ctypes.byref(q), buf, 64) == mj.MJ_OK
+    assert buf.value.decode().endswith("_kve3m2")
+    # packed pools: 32-byte aligned bases and strides (16 is not enough)
+    for field, val in (("k_row", 48), ("v_page", 16 * 96 + 16), ("k", (1 << 20) + 16)):
+        a = _good_args()
+        a.k_page, a.k_row, a.k_head = 16 * 64, 64, 64
+        a.v_page, a.v_row, a.v_head = 16 * 64, 64, 64
+        a.workspace = 1 << 20
+        a.workspace_bytes = mj.workspace_bytes(q)
+        setattr(a, field, val)
+        assert _attn_status(q, a) == mj.MJ_ERR_INVALID_ARG, field

@@ -156,3 +156,28 @@ def test_row_copies_e4m3_q_and_determinism():
         a.step()
     torch.cuda.synchronize()
     assert torch.equal(o0, a.o_vllm) and torch.equal(l0, a.lse)
+
+
+@pytest.mark.parametrize("h_r,q_len", [(32, 1), (32, 4)], ids=["rows32_x4", "rows128"])
+def test_softmax_stress_identical_keys_long_rows(h_r, q_len):
+    # every key of a 16384-key row identical: all probabilities equal, the
+    # row sum is as large as it gets (L terms of the same size), and O is the
+    # plain mean of V; LSE = z + ln L within 2e-3 asks for an accurate sum
+    w = syn.config(5, h_r=h_r, q_len=q_len, num_seqs=2, len_range=(0, 16384))
+    for b in range(w.num_seqs):
+        L = int(w.seq_lens[b])
+        pages = w.block_table[b, : -(-L // w.page_size)]
+        row = w.k_cache[pages[0], 0].copy()
+        w.k_cache[pages] = row[None, None]
+        w.k_cache[pages[-1], (L % w.page_size) or w.page_size :] = 0x7F  # keep the tail poison
+    check(w)
+
+
+@pytest.mark.parametrize("h_r,q_len", [(32, 1), (32, 4)], ids=["rows32_x4", "rows128"])
+def test_softmax_stress_wide_logit_spread(h_r, q_len):
+    # queries scaled by 6: logits spread over about +-16 around their
+    # maximum, so most probabilities sit far below the largest and the
+    # reference maximum moves late in a row
+    w = syn.config(5, h_r=h_r, q_len=q_len, num_seqs=3, len_range=(0, 9000))
+    w.q = syn.bf16_encode(syn.bf16_bits_to_float(w.q) * 6.0)
+    check(w)

@@ -93,9 +93,9 @@ NARROW_MUTATIONS = [
     ("subnormal binade", "mag = (m / (1 << mb)) * 2.0 ** (1 - bias)", "mag = (m / (1 << mb)) * 2.0 ** (-bias)"),
     ("tie to the larger", "if best_dist is None or dist < best_dist:", "if best_dist is None or dist <= best_dist:"),
     ("negative zero", "(half if (v < 0 and table[best] != 0) else 0)", "(half if v < 0 else 0)"),
-    ("bit order within a byte", "out[row, j // 8] |= np.uint8(1 << (j % 8))", "out[row, j // 8] |= np.uint8(1 << (7 - j % 8))"),
-    ("bit order within a code", "j = bits * i + k\n                    out", "j = bits * i + (bits - 1 - k)\n                    out"),
-    ("element stride", "j = bits * i + k\n                    out", "j = (bits + 1) * i + k if i % 4 else bits * i + k\n                    out"),
+    ("bit order within a byte", "out[:, j // 8] |= ((flat[:, i] >> k) & 1) << (j % 8)", "out[:, j // 8] |= ((flat[:, i] >> k) & 1) << (7 - j % 8)"),
+    ("bit order within a code", "out[:, j // 8] |= ((flat[:, i] >> k) & 1) << (j % 8)", "out[:, j // 8] |= ((flat[:, i] >> (bits - 1 - k)) & 1) << (j % 8)"),
+    ("unpack reads the wrong byte", "out[:, i] |= ((flat[:, j // 8] >> (j % 8)) & 1) << k", "out[:, i] |= ((flat[:, (j // 8) ^ 1] >> (j % 8)) & 1) << k"),
     ("mantissa width", '"e3m2": (3, 2, 3)', '"e3m2": (2, 3, 3)'),
     ("sign of the search", "dist = abs(abs(v) - table[c])", "dist = abs(v - table[c])"),
 ]

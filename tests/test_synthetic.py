@@ -1,6 +1,7 @@
 """The seeded input generator: storage-format rounding and cache structure."""
 
 import numpy as np
+import pytest
 import torch
 
 from paged_fp8_kv_gb300 import synthetic as syn
@@ -61,3 +62,25 @@ def test_generation_is_deterministic():
     b = syn.config(2, num_seqs=3, len_range=(100, 400))
     for f in ("k_cache", "v_cache", "q", "block_table", "seq_lens", "k_descale"):
         np.testing.assert_array_equal(getattr(a, f), getattr(b, f))
+
+
+@pytest.mark.parametrize("fmt", ["e3m2", "e2m3", "e2m1"])
+def test_narrow_generator_agrees_with_the_oracle_encoder(fmt):
+    # two independent implementations of the same rounding (the generator's
+    # midpoint search and the oracle's exhaustive nearest search, ties to the
+    # smaller magnitude) and of the same little-endian packing
+    from oracle import narrow_ref
+
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.normal(0, 3, 5000), narrow_ref.minifloat_table(fmt), [1e6, -1e6, 0.0, -0.0]])
+    assert np.array_equal(syn.narrow_encode(x, fmt), narrow_ref.minifloat_encode(x, fmt))
+    bits = syn.KV_FORMAT_BITS[fmt]
+    codes = rng.integers(0, 1 << bits, size=(3, 4, 128)).astype(np.uint8)
+    assert np.array_equal(syn.pack_codes(codes, bits), narrow_ref.pack_bits(codes, bits))
+
+
+def test_narrow_workload_layout():
+    w = syn.config(2, num_seqs=3, len_range=(100, 400), kv_format="e2m1")
+    assert w.name.endswith("_kve2m1") and w.kv_format == "e2m1"
+    assert w.k_cache.shape[-1] == 64 and w.v_cache.shape[-1] == 64
+    assert w.kv_bytes() == int(w.seq_lens.sum()) * w.h_k * 64 * 2
