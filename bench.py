@@ -62,6 +62,7 @@ def parse():
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core (swap-AB), 3 head-grouped tensor-core, 4 query-rows tensor-core")
     ap.add_argument("--l2_prefetch", type=int, default=0, help="0 default, -1 off, 1..8 tiles ahead")
     ap.add_argument("--kv_evict_first", type=int, default=0, help="K/V loads with L2 EVICT_FIRST: 0 default, -1 off, 1 on")
+    ap.add_argument("--ctas_per_sm", type=int, default=0, help="plan slots per SM (0: the library's choice)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time steps as plain launches, not CUDA-graph replays")
@@ -345,7 +346,7 @@ def run_mj(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     w = workload(args)
     s = DecodeSession(w, device=str(dev), kv_layout=args.kv_layout, kernel=args.kernel, l2_prefetch=args.l2_prefetch,
-        kv_evict_first=args.kv_evict_first,
+        kv_evict_first=args.kv_evict_first, ctas_per_sm=args.ctas_per_sm,
     )
     d_bytes, m_bytes, step_bytes = algorithmic_bytes(w, s.plan)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -353,7 +354,7 @@ def run_mj(args, rank, world, local_rank):
     # host plan cost (the plan runs once per batch shape, on the host)
     t = time.perf_counter()
     for _ in range(20):
-        decode_plan(s.params, w.seq_lens, sm_count=s.sm_count)
+        decode_plan(s.params, w.seq_lens, sm_count=s.sm_count, ctas_per_sm=s.ctas_per_sm)
     plan_us = (time.perf_counter() - t) / 20 * 1e6
 
     clk_before = clocks_now(local_rank)
@@ -603,7 +604,7 @@ def e2e_measure(args, s, w, step_bytes, dev):
     for i in range(args.warmup + args.steps):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        plan = decode_plan(s.params, seq_host, sm_count=s.sm_count)
+        plan = decode_plan(s.params, seq_host, sm_count=s.sm_count, ctas_per_sm=s.ctas_per_sm)
         n = plan.num_work
         work_pin.numpy()[:n] = plan.work
         ns_pin.numpy()[:] = plan.n_splits
@@ -673,7 +674,13 @@ def main():
     if args.suite == -1:
         # the whole table by default; off when a single workload was asked for
         flags = (args.variant, args.h_r, args.q_len, args.num_seqs, args.max_splits)
-        explicit = any(f is not None for f in flags) or args.kernel != 0 or "--config" in sys.argv or args.kv_format != "e4m3"
+        explicit = (
+            any(f is not None for f in flags)
+            or args.kernel != 0
+            or "--config" in sys.argv
+            or args.kv_format != "e4m3"
+            or args.ctas_per_sm != 0
+        )
         args.suite = 0 if explicit else 1
     if args.impl == "reference":
         if rank != 0:

@@ -42,8 +42,10 @@ class DecodeSession:
         kernel: int = 0,
         l2_prefetch: int = 0,
         kv_evict_first: int = 0,
+        ctas_per_sm: int = 0,
     ):
         self.w = w
+        self.ctas_per_sm = int(ctas_per_sm)
         self.device = torch.device(device)
         dev = self.device
         self.num_seqs, self.q_len, self.h_k, self.h_r = w.num_seqs, w.q_len, w.h_k, w.h_r
@@ -127,7 +129,12 @@ class DecodeSession:
 
     def replan(self, seq_lens_host, force_splits: int = 0, pad_to: int = 0) -> None:
         self.plan = decode_plan(
-            self.params, seq_lens_host, sm_count=self.sm_count, force_splits=force_splits, pad_to=pad_to
+            self.params,
+            seq_lens_host,
+            sm_count=self.sm_count,
+            ctas_per_sm=self.ctas_per_sm,
+            force_splits=force_splits,
+            pad_to=pad_to,
         )
         self.work = torch.from_numpy(self.plan.work).to(self.device)
         self.n_splits = torch.from_numpy(self.plan.n_splits).to(self.device)
