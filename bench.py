@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--max_splits", type=int, default=None)
     ap.add_argument("--num_seqs", type=int, default=None, help="smaller batch of the same config (profiling)")
     ap.add_argument("--kv_layout", default="nhd", choices=["nhd", "hnd", "interleaved", "flashinfer"])
-    ap.add_argument("--kv_format", default="e4m3", choices=["e4m3", "e3m2", "e2m3", "e2m1"], help="K/V pool element format")
+    ap.add_argument("--kv_format", default="e4m3", choices=["e4m3", "e3m2", "e2m3", "e2m1", "nvfp4"], help="K/V pool element format")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core (swap-AB), 3 head-grouped tensor-core, 4 query-rows tensor-core")
     ap.add_argument("--l2_prefetch", type=int, default=0, help="0 default, -1 off, 1..8 tiles ahead")
     ap.add_argument("--kv_evict_first", type=int, default=0, help="K/V loads with L2 EVICT_FIRST: 0 default, -1 off, 1 on")
@@ -98,18 +98,13 @@ def describe(w) -> str:
     )
 
 
-def syn_bits(w) -> int:
-    """Bits per K/V code of the workload's pool format."""
-    return {"e4m3": 8, "e3m2": 6, "e2m3": 6, "e2m1": 4}[getattr(w, "kv_format", "e4m3")]
-
-
 def algorithmic_bytes(w, plan):
     """(decode kernel bytes, merge kernel bytes, step bytes): what the method
     must move, not what a kernel happens to touch."""
     b, h_k, n_q, d = w.num_seqs, w.h_k, w.n_q, w.head_dim
     lens = w.seq_lens.astype(np.int64)
     qb = 1 if w.q_is_e4m3 else 2
-    kv = int(lens.sum()) * h_k * (d * syn_bits(w) // 8) * 2
+    kv = w.kv_bytes()  # K + V rows below L in the pool's format (nvfp4: codes and scales)
     q = b * h_k * n_q * d * qb
     o = b * h_k * n_q * d * 2
     lse = b * h_k * n_q * 4
@@ -419,6 +414,8 @@ SUITE = (
     + [(5, {"h_r": hr, "q_len": ql}) for hr in (16, 32) for ql in (1, 2, 4, 8, 16)]
     # narrow KV pools (fp4 / fp6 codes read by the MMA as they are)
     + [(2, {"kv_format": "e2m1"}), (3, {"kv_format": "e2m3"}), (4, {"kv_format": "e2m1"}), (4, {"kv_format": "e3m2"})]
+    # nvfp4 (converted to e4m3 in the kernel; the fp8-Q configuration)
+    + [(3, {"kv_format": "nvfp4"})]
 )
 
 
@@ -515,6 +512,8 @@ def plan_device_measure(s, w, dev, flush, launches: int = 200):
             scale_o=w.scale_o,
             max_n_splits=max_n,
             stream=stream,
+            k_scales=s.k_scales,
+            v_scales=s.v_scales,
         )
 
     cs = torch.cuda.Stream(dev)

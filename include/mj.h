@@ -106,8 +106,19 @@ typedef struct {
  * as they are (the TMA spreads each 16-element group over 16 bytes of
  * shared memory).  Narrow formats need kernel MJ_KERNEL_AUTO,
  * MJ_KERNEL_TENSOR_CORE or MJ_KERNEL_TENSOR_CORE_QROWS, K/V base pointers
- * 32-byte aligned and K/V strides multiples of 32 bytes. */
-typedef enum { MJ_KV_E4M3 = 0, MJ_KV_E3M2 = 1, MJ_KV_E2M3 = 2, MJ_KV_E2M1 = 3 } mj_kv_format;
+ * 32-byte aligned and K/V strides multiples of 32 bytes.
+ *   MJ_KV_NVFP4 e2m1 codes packed as MJ_KV_E2M1 (64 bytes a row) plus one
+ *               e4m3 scale per 16 consecutive elements of a row, held in a
+ *               separate scale plane (mj_decode_args.k_scales / v_scales):
+ *               the 8 scales of a row are 8 consecutive bytes and the rows of
+ *               one (page, head) follow each other, page_size * 8 bytes
+ *               (layout (page, head, row, group)).  The value the operation
+ *               uses is e4m3(code * scale * 2^-3), rounded to nearest even
+ *               (the page's nvfp4 kernel value); the kernel converts each
+ *               group in shared memory before the MMA.  Needs e4m3 Q,
+ *               q_len*h_r <= 32 and MJ_KERNEL_AUTO or MJ_KERNEL_TENSOR_CORE;
+ *               code strides are 16-byte multiples. */
+typedef enum { MJ_KV_E4M3 = 0, MJ_KV_E3M2 = 1, MJ_KV_E2M3 = 2, MJ_KV_E2M1 = 3, MJ_KV_NVFP4 = 4 } mj_kv_format;
 
 /* Decode kernel families.  Both compute the same function; the choice only
  * changes speed (and last-bit rounding).
@@ -222,7 +233,12 @@ size_t mj_decode_workspace_bytes(const mj_decode_params* params);
  *                merge (see status), never merged in part.
  *   timing_events optional: NULL, or 3 cudaEvent_t recorded on `stream`
  *                before the decode kernel, between decode and merge, and
- *                after the merge (instrumentation only) */
+ *                after the merge (instrumentation only)
+ *   k_scales, v_scales
+ *                MJ_KV_NVFP4 only (ignored otherwise): device e4m3 scale
+ *                planes, 16-byte aligned; the 8 scales of row r of (page, g)
+ *                at page*x_page + g*x_head + r*8 (bytes; both strides
+ *                multiples of 16) */
 typedef struct {
   const void* q;
   int64_t q_seq_stride;
@@ -247,6 +263,9 @@ typedef struct {
   int32_t* status;
   int32_t max_n_splits;
   void* const* timing_events;
+  const uint8_t* k_scales;
+  const uint8_t* v_scales;
+  int64_t ks_page, ks_head, vs_page, vs_head;
 } mj_decode_args;
 
 /* Decode attention for one step: the decode kernel over every work item,

@@ -17,6 +17,12 @@ the largest), with the sign bit only on a non-zero magnitude.  Codes are
 laid out as one little-endian bit stream per row (so fp4 puts element 2i in
 the low nibble of byte i, and fp6 fills three bytes with four elements).
 
+nvfp4 (the same page's fourth narrow format) stores e2m1 codes with one e4m3
+scale per 16 consecutive elements of a row; the value the attention uses is
+the code's value times its scale times 2^-3, rounded to e4m3 (nearest, ties
+to even).  The product is exact (at most six significant bits), so only that
+one rounding defines the format's e4m3 view (`nvfp4_to_e4m3_codes`).
+
 Every value of the three formats is also an e4m3 value, so an attention
 problem with narrow KV is the same problem with the equal e4m3 codes:
 `to_e4m3_codes` maps them exactly, and the fp64 attention oracle then
@@ -115,3 +121,25 @@ def to_e4m3_codes(codes: np.ndarray, fmt: str, e4m3_table: np.ndarray) -> np.nda
             raise ValueError(f"{fmt} code {c} ({v}) has no unique e4m3 equal")
         lut[c] = hits[0]
     return lut[np.asarray(codes, dtype=np.int64)]
+
+
+NVFP4_GROUP = 16  # elements of a row that share one e4m3 scale
+NVFP4_SHIFT = 2.0**-3  # folded into the scale on the page; undone by the descale
+
+
+def nvfp4_to_e4m3_codes(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """e4m3 codes of an nvfp4 row block: codes (..., d) e2m1 codes (one per
+    element), scales (..., d / 16) e4m3 codes; element i takes scale
+    i // 16.  Each result is the e4m3 rounding (nearest, ties to even, via
+    the oracle's own encoder) of value(code) * value(scale) * 2^-3, computed
+    once per (code, scale) pair; a NaN scale gives the NaN code."""
+    from .quant_ref import e4m3_encode_rne
+    from . import e4m3_table
+
+    e2m1 = minifloat_table("e2m1")
+    e4 = e4m3_table()
+    products = np.array([[e2m1[c] * e4[sc] * NVFP4_SHIFT for sc in range(256)] for c in range(16)])
+    lut = e4m3_encode_rne(products.astype(np.float32))  # exact: the products fit fp32
+    c = np.asarray(codes, dtype=np.int64)
+    sc = np.repeat(np.asarray(scales, dtype=np.int64), NVFP4_GROUP, axis=-1)
+    return lut[c, sc]

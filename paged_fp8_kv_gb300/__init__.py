@@ -35,7 +35,8 @@ MJ_KV_E4M3 = 0
 MJ_KV_E3M2 = 1
 MJ_KV_E2M3 = 2
 MJ_KV_E2M1 = 3
-KV_FORMATS = {"e4m3": MJ_KV_E4M3, "e3m2": MJ_KV_E3M2, "e2m3": MJ_KV_E2M3, "e2m1": MJ_KV_E2M1}
+MJ_KV_NVFP4 = 4
+KV_FORMATS = {"e4m3": MJ_KV_E4M3, "e3m2": MJ_KV_E3M2, "e2m3": MJ_KV_E2M3, "e2m1": MJ_KV_E2M1, "nvfp4": MJ_KV_NVFP4}
 
 MJ_KERNEL_AUTO = 0
 MJ_KERNEL_CUDA_CORE = 1
@@ -120,6 +121,12 @@ class DecodeArgs(ctypes.Structure):
         ("status", _vp),
         ("max_n_splits", ctypes.c_int32),
         ("timing_events", _vp),
+        ("k_scales", _vp),
+        ("v_scales", _vp),
+        ("ks_page", _i64),
+        ("ks_head", _i64),
+        ("vs_page", _i64),
+        ("vs_head", _i64),
     ]
 
 
@@ -330,6 +337,8 @@ def decode_attn(
     max_n_splits: int = 0,
     timing_events=None,
     stream=None,
+    k_scales=None,
+    v_scales=None,
 ) -> None:
     """mj_decode_attn on device tensors.
 
@@ -365,8 +374,25 @@ def decode_attn(
             raise ValueError("timing_events: three created CUDA events (record each once first)")
         ev_arr = (ctypes.c_void_p * 3)(*handles)
         a.timing_events = ctypes.cast(ev_arr, ctypes.c_void_p)
+    _set_scales(a, k_scales, v_scales)
     st = lib().mj_decode_attn(ctypes.byref(params), ctypes.byref(a), _stream_handle(stream))
     _check(st, "mj_decode_attn")
+
+
+def scale_strides(t) -> Tuple[int, int]:
+    """(page, head) byte strides of an nvfp4 scale plane viewed as
+    (num_pages, h_k, page_size, d / 16) uint8 (rows 8 bytes apart)."""
+    if t.dim() != 4 or t.element_size() != 1 or t.stride(3) != 1 or t.stride(2) != t.shape[3]:
+        raise ValueError("scale plane: (pages, h_k, page_size, d/16) bytes with contiguous rows")
+    return int(t.stride(0)), int(t.stride(1))
+
+
+def _set_scales(a, k_scales, v_scales) -> None:
+    if k_scales is None or v_scales is None:
+        return
+    a.k_scales, a.v_scales = _ptr(k_scales), _ptr(v_scales)
+    a.ks_page, a.ks_head = scale_strides(k_scales)
+    a.vs_page, a.vs_head = scale_strides(v_scales)
 
 
 def pack_q(q_vllm, q_packed, num_seqs: int, q_len: int, h_k: int, h_r: int, stream=None) -> None:
@@ -426,14 +452,16 @@ def check_preconditions(params: DecodeParams, block_table, seq_lens, q_descale, 
 
 
 def check_gather_kv(params: DecodeParams, k_cache, v_cache, block_table, seq_lens, values: bool, out,
-                    stream=None) -> None:
+                    stream=None, k_scales=None, v_scales=None) -> None:
     """mj_check_gather_kv: the decode path's K (values False) or V rows of
-    every (sequence, kv head) into out (b, h_k, out_rows, 128) uint8."""
+    every (sequence, kv head) into out (b, h_k, out_rows, 128) uint8 (for an
+    nvfp4 pool, the e4m3 rows its conversion gives)."""
     a = DecodeArgs()
     a.k, a.v = _ptr(k_cache), _ptr(v_cache)
     a.k_page, a.k_row, a.k_head = kv_strides(k_cache)
     a.v_page, a.v_row, a.v_head = kv_strides(v_cache)
     a.block_table, a.seq_lens = _ptr(block_table), _ptr(seq_lens)
+    _set_scales(a, k_scales, v_scales)
     st = lib().mj_check_gather_kv(
         ctypes.byref(params), ctypes.byref(a), int(bool(values)), _ptr(out), int(out.shape[2]), _stream_handle(stream)
     )

@@ -122,7 +122,10 @@ constexpr int pow2_at_least(int x) {
 //   GEMM2 B operand (P): kN2 = 2R columns = [hi columns | lo columns].
 // The hi and lo parts share one MMA per K step; their products land in
 // separate accumulator columns (c and R + c) that the softmax adds.
-template <int R, bool kQe4m3>
+//   kNv: the pool is nvfp4 (e2m1 codes and an e4m3 scale per 16 elements): a
+//     fourth warpgroup converts each tile into the e4m3 ring from a ring of
+//     packed tiles the TMA fills (codes and scales of K and V, 18 KB a tile).
+template <int R, bool kQe4m3, bool kNv = false>
 struct TcCfg {
   static constexpr int kN1 = kQe4m3 ? (R < 16 ? 16 : R) : 2 * R;
   static constexpr int kN2 = 2 * R;
@@ -132,8 +135,15 @@ struct TcCfg {
   // us a step; sweep N = 16: 384 -> 256 work items, 101.6 -> 98.7 us), and
   // short split chunks have most of their tiles in flight at once
   static constexpr bool kDeep16 = R == 16 || (!kQe4m3 && R == 8);
-  static constexpr int kStages = kDeep16 ? 3 : (R <= 32 ? 2 : 5);
-  static constexpr int kMinBlocks = kDeep16 ? 2 : (R <= 16 ? 3 : (R <= 32 ? 2 : 1));
+  // nvfp4: two converted stages and six packed ones (108 KB of the pool in
+  // flight), one CTA per SM
+  static constexpr int kStages = kNv ? 2 : (kDeep16 ? 3 : (R <= 32 ? 2 : 5));
+  static constexpr int kMinBlocks = kNv ? 1 : (kDeep16 ? 2 : (R <= 16 ? 3 : (R <= 32 ? 2 : 1)));
+  static constexpr int kCvtWarps = kNv ? 4 : 0;
+  static constexpr int kPkStages = kNv ? 6 : 0;
+  static constexpr int kPkCodes = kTileKV * 64;   // 128 rows x 64 bytes of e2m1 codes
+  static constexpr int kPkScales = kTileKV * 8;   // 128 rows x 8 e4m3 scales
+  static constexpr int kPkBytes = 2 * (kPkCodes + kPkScales);  // K codes, V codes, K scales, V scales
   // two P buffers let the softmax of tile i write while GEMM2(i-1) still
   // reads; R = 16 at 3 CTAs/SM has no room for the second one
   static constexpr int kPBufs = R == 16 && !kDeep16 ? 1 : 2;
@@ -141,7 +151,7 @@ struct TcCfg {
   // take the other half of the columns (two warps per lane quarter)
   static constexpr int kSmWarps = R >= 32 ? 8 : 4;
   static constexpr int kSmThreads = 32 * kSmWarps;
-  static constexpr int kThreads = 64 + kSmThreads;
+  static constexpr int kThreads = 64 + kSmThreads + 32 * kCvtWarps;
   static constexpr int kHalves = kSmWarps / 4;
   static constexpr int kCols = R / kHalves;  // columns per softmax thread
   static constexpr int kQBytes = kN1 * 128;    // SW128 K-major rows
@@ -155,8 +165,9 @@ struct TcCfg {
   static constexpr int kOffRed = kOffP + kPBufs * kPBytes;  // [4][R] floats
   static constexpr int kOffM = kOffRed + 4 * R * 4;    // [2][R] running max
   static constexpr int kOffCorr = kOffM + 2 * R * 4;   // [R] correction
-  static constexpr int kOffBar = kOffCorr + R * 4;
-  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+  static constexpr int kOffPk = (kOffCorr + R * 4 + 1023) / 1024 * 1024;  // packed ring (nvfp4)
+  static constexpr int kOffBar = kOffPk + kPkStages * kPkBytes;
+  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 2 * kPkStages;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64 + 1024;  // + alignment slack
   static_assert(kN1 % 16 == 0 && kN1 <= 256 && kN2 % 16 == 0 && kN2 <= 256, "MMA N");
@@ -169,6 +180,7 @@ struct Bars {
   uint32_t sfull, sfree;           // + buf * 8
   uint32_t pfull, pfree;  // + buf * 8
   uint32_t odone, qready, drain;
+  uint32_t pkfull, pkempty;  // nvfp4 packed ring: + stage * 8
 };
 
 __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) {
@@ -176,14 +188,15 @@ __device__ __forceinline__ void set_abort(volatile int* abort, int32_t* status) 
   if (status) atomicExch(status, kStatusTimeout);
 }
 
-template <int R, bool kQe4m3>
-__global__ void __launch_bounds__((TcCfg<R, kQe4m3>::kThreads), (TcCfg<R, kQe4m3>::kMinBlocks))
+template <int R, bool kQe4m3, bool kNv>
+__global__ void __launch_bounds__((TcCfg<R, kQe4m3, kNv>::kThreads), (TcCfg<R, kQe4m3, kNv>::kMinBlocks))
 decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
-                 const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
+                 const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_ks,
+                 const __grid_constant__ CUtensorMap tmap_vs, int n_q_tiles) {
   // the merge (a programmatic dependent) may launch now: its CTAs wait
   // for this grid's completion before reading what it writes
   ptx::griddep_launch_dependents();
-  using C = TcCfg<R, kQe4m3>;
+  using C = TcCfg<R, kQe4m3, kNv>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(sm);
@@ -217,6 +230,10 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     bar.qready = p;
     p += 8;
     bar.drain = p;
+    p += 8;
+    bar.pkfull = p;
+    p += 8 * C::kPkStages;
+    bar.pkempty = p;
   }
 
   const int tid = threadIdx.x;
@@ -248,9 +265,15 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(bar.kfull + 8 * s, 1);
-      ptx::mbar_init(bar.vfull + 8 * s, 1);
+      // e4m3 stages: filled by the TMA (one arrival with its byte count), or
+      // by the converter warps (one arrival each)
+      ptx::mbar_init(bar.kfull + 8 * s, kNv ? C::kCvtWarps : 1);
+      ptx::mbar_init(bar.vfull + 8 * s, kNv ? C::kCvtWarps : 1);
       ptx::mbar_init(bar.kvempty + 8 * s, 1);
+    }
+    for (int s = 0; s < C::kPkStages; ++s) {
+      ptx::mbar_init(bar.pkfull + 8 * s, 1);
+      ptx::mbar_init(bar.pkempty + 8 * s, C::kCvtWarps);
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar.sfull + 8 * s, 1);
@@ -298,6 +321,47 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t tile_tx = kv_box_bytes(a.kv_format, kTileKV);
     int next_page = (lane < ppt && t_begin * ppt + lane < valid_pages) ? first_page_raw : a.num_pages;
     int issued = 0;
+    if constexpr (kNv) {
+      // nvfp4: each tile's K and V codes (PS rows of 64 bytes a page) and
+      // their scales (PS rows of 8 bytes a page, from the scale plane) into a
+      // packed stage; the converter warps turn it into e4m3 stages
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmap_ks);
+        ptx::prefetch_tmap(&tmap_vs);
+      }
+      for (int i = 0; i < T; ++i) {
+        const int ps = i % C::kPkStages;
+        if (i >= C::kPkStages) {
+          const bool got =
+              ptx::mbar_wait_bounded(bar.pkempty + 8 * ps, ((i / C::kPkStages) - 1) & 1, abort_flag, kWaitNs);
+          if (__any_sync(0xffffffffu, !got)) {
+            if (lane == 0) set_abort(abort_flag, a.status);
+            break;
+          }
+        }
+        const int page = next_page;
+        if (i + 1 < T) next_page = lookup(t_begin + i + 1);
+        const uint32_t pk = sbase + C::kOffPk + ps * C::kPkBytes;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(bar.pkfull + 8 * ps, C::kPkBytes);
+        __syncwarp();
+        if (lane < ppt) {
+          const uint32_t pb = bar.pkfull + 8 * ps;
+          ptx::tma_load_kv(pk + lane * PS * 64, &tmap_k, pb, 0, 0, g, page, evict_first, kv_policy);
+          ptx::tma_load_kv(pk + C::kPkCodes + lane * PS * 64, &tmap_v, pb, 0, 0, g, page, evict_first, kv_policy);
+          ptx::tma_load_kv(pk + 2 * C::kPkCodes + lane * PS * 8, &tmap_ks, pb, 0, 0, g, page, evict_first,
+                           kv_policy);
+          ptx::tma_load_kv(pk + 2 * C::kPkCodes + C::kPkScales + lane * PS * 8, &tmap_vs, pb, 0, 0, g, page,
+                           evict_first, kv_policy);
+        }
+        issued = i + 1;
+      }
+      if (*abort_flag && lane == 0) {
+        for (int i = (issued > C::kPkStages ? issued - C::kPkStages : 0); i < issued; ++i) {
+          volatile int never = 0;
+          ptx::mbar_wait_bounded(bar.pkfull + 8 * (i % C::kPkStages), (i / C::kPkStages) & 1, &never, kWaitNs / 4);
+        }
+      }
+    } else {
     for (int i = 0; i < T; ++i) {
       const int st = i % C::kStages;
       if (i >= C::kStages) {
@@ -345,6 +409,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         ptx::mbar_wait_bounded(bar.vfull + 8 * st, par, &never, kWaitNs / 4);
       }
     }
+    }  // e4m3 and the other narrow formats
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -427,7 +492,7 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       volatile int never = 0;
       ptx::mbar_wait_bounded(bar.drain, 0, &never, kWaitNs);
     }
-  } else {
+  } else if (warp < 2 + C::kSmWarps) {
     // ------------------------------------------------- softmax warpgroup
     constexpr int kCols = C::kCols;
     constexpr int kSmT = C::kSmThreads;
@@ -822,6 +887,50 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         }
       }
     }
+  } else if constexpr (kNv) {
+    // ---------------------------------------------- nvfp4 converter warps
+    // Tile i: its packed stage (K codes, V codes, K scales, V scales, rows of
+    // 64 and 8 bytes) -> e4m3 stage i % kStages in the layout the TMA gives
+    // e4m3 pools (128-byte rows, 16-byte chunk cc of row r at cc ^ (r % 8)),
+    // once GEMM2 of the tile that used the stage before has completed.
+    // Thread j of the group converts groups j, j + 128, ... of each tile;
+    // rows at or past the sequence end are written as zeros.
+    const int ct = tid - (64 + C::kSmThreads);  // 0 .. 127
+    bool ok = true;
+    for (int i = 0; i < T; ++i) {
+      const int ps = i % C::kPkStages;
+      const int st = i % C::kStages;
+      if (!ptx::mbar_wait_bounded(bar.pkfull + 8 * ps, (i / C::kPkStages) & 1, abort_flag, kWaitNs) ||
+          (i >= C::kStages &&
+           !ptx::mbar_wait_bounded(bar.kvempty + 8 * st, ((i / C::kStages) - 1) & 1, abort_flag, kWaitNs))) {
+        ok = false;
+        break;
+      }
+      const int key0 = (t_begin + i) * kTileKV;
+      const uint8_t* pk = sm + C::kOffPk + ps * C::kPkBytes;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const uint8_t* codes = pk + kv * C::kPkCodes;
+        const uint8_t* scales = pk + 2 * C::kPkCodes + kv * C::kPkScales;
+        uint8_t* dst = sm + (kv ? C::kOffV : C::kOffK) + st * kKVTileBytes;
+#pragma unroll 2
+        for (int j = ct; j < kTileKV * 8; j += 128) {
+          const int r = j >> 3, cc = j & 7;
+          uint4 e = make_uint4(0u, 0u, 0u, 0u);
+          if (key0 + r < L)
+            e = nvfp4_group_to_e4m3(*reinterpret_cast<const uint2*>(codes + r * 64 + cc * 8), scales[r * 8 + cc]);
+          *reinterpret_cast<uint4*>(dst + r * 128 + ((cc ^ (r & 7)) << 4)) = e;
+        }
+      }
+      ptx::fence_proxy_async_smem();  // generic-proxy writes -> the MMA's reads
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(bar.kfull + 8 * st);
+        ptx::mbar_arrive(bar.vfull + 8 * st);
+        ptx::mbar_arrive(bar.pkempty + 8 * ps);
+      }
+    }
+    if (!ok && lane == 0) set_abort(abort_flag, a.status);
   }
 
   ptx::tc_fence_before();
@@ -830,26 +939,62 @@ decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   if (warp == 1) ptx::tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int R, bool kQe4m3>
+// nvfp4 pools as byte tensors: the codes (64 bytes a row) and the scale
+// plane (a page's rows of one head, PS x 8 bytes, seen as PS / 16 rows of
+// 128 bytes); one box is one page of one head, unswizzled.
+bool make_nv_map(CUtensorMap* m, const uint8_t* base, bool scales, int page_size, int h_k, int num_pages,
+                 int64_t s_row, int64_t s_head, int64_t s_page) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t inner = scales ? 128 : 64;
+  const cuuint64_t rows = scales ? static_cast<cuuint64_t>(page_size / 16) : static_cast<cuuint64_t>(page_size);
+  const cuuint64_t dims[4] = {inner, rows, static_cast<cuuint64_t>(h_k), static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(scales ? 128 : s_row), static_cast<cuuint64_t>(s_head),
+                                 static_cast<cuuint64_t>(s_page)};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(rows), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int R, bool kQe4m3, bool kNv>
 cudaError_t launch_tc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
-  CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, a.page_size, 1,
-                   a.kv_format) ||
-      !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, a.page_size, 1,
-                   a.kv_format))
-    return cudaErrorInvalidValue;
-  const int smem = TcCfg<R, kQe4m3>::kBytes;
-  auto kern = decode_tc_kernel<R, kQe4m3>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  CUtensorMap mk, mv, mks, mvs;
+  if (kNv) {
+    if (!make_nv_map(&mk, a.k, false, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page) ||
+        !make_nv_map(&mv, a.v, false, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page) ||
+        !make_nv_map(&mks, a.ks, true, a.page_size, a.h_k, a.num_pages, 8, a.ks_head, a.ks_page) ||
+        !make_nv_map(&mvs, a.vs, true, a.page_size, a.h_k, a.num_pages, 8, a.vs_head, a.vs_page))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, a.page_size, 1,
+                     a.kv_format) ||
+        !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, a.page_size, 1,
+                     a.kv_format))
+      return cudaErrorInvalidValue;
+    mks = mk;  // unused by these instances
+    mvs = mv;
+  }
+  using C = TcCfg<R, kQe4m3, kNv>;
+  auto kern = decode_tc_kernel<R, kQe4m3, kNv>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
-  kern<<<grid, TcCfg<R, kQe4m3>::kThreads, smem, stream>>>(a, mk, mv, n_q_tiles);
+  kern<<<grid, C::kThreads, C::kBytes, stream>>>(a, mk, mv, mks, mvs, n_q_tiles);
   return cudaGetLastError();
 }
 
 template <int R>
 cudaError_t launch_tc_q(const DecodeDev& a, int n_q_tiles, bool q_e4m3, cudaStream_t stream) {
-  return q_e4m3 ? launch_tc<R, true>(a, n_q_tiles, stream) : launch_tc<R, false>(a, n_q_tiles, stream);
+  if (a.kv_format == 4) {  // nvfp4: e4m3 Q, up to 32 rows (validated before)
+    if constexpr (R <= 32) {
+      if (q_e4m3) return launch_tc<R, true, true>(a, n_q_tiles, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
+  return q_e4m3 ? launch_tc<R, true, false>(a, n_q_tiles, stream) : launch_tc<R, false, false>(a, n_q_tiles, stream);
 }
 
 // ---------------------------------------------------------------- checks
@@ -945,7 +1090,37 @@ cudaError_t launch_bounded_wait(int32_t* status, int64_t* waited_ns, uint64_t li
   return cudaGetLastError();
 }
 
+// nvfp4 pools: rows 0 .. L - 1 converted to e4m3 by the decode kernel's
+// conversion (nvfp4_group_to_e4m3), codes and scales read through the block
+// table with plain loads; grid (tiles, h_k, num_seqs), 128 threads.
+__global__ void __launch_bounds__(128) gather_nvfp4_kernel(const DecodeDev a, bool values, uint8_t* __restrict__ out,
+                                                           int out_rows) {
+  const int t = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int L = a.seq_lens[b];
+  const uint8_t* pool = values ? a.v : a.k;
+  const uint8_t* scales = values ? a.vs : a.ks;
+  const int64_t p_page = values ? a.v_page : a.k_page, p_row = values ? a.v_row : a.k_row;
+  const int64_t p_head = values ? a.v_head : a.k_head;
+  const int64_t s_page = values ? a.vs_page : a.ks_page, s_head = values ? a.vs_head : a.ks_head;
+  for (int j = threadIdx.x; j < kTileKV * 8; j += 128) {
+    const int key = t * kTileKV + (j >> 3), cc = j & 7;
+    if (key >= L || key >= out_rows) continue;
+    const int page = a.block_table[static_cast<int64_t>(b) * a.max_blocks + key / a.page_size];
+    const int row = key % a.page_size;
+    const uint2 c = *reinterpret_cast<const uint2*>(pool + page * p_page + row * p_row + g * p_head + cc * 8);
+    const uint32_t sc = scales[page * s_page + g * s_head + row * 8 + cc];
+    *reinterpret_cast<uint4*>(out + ((static_cast<int64_t>(b) * a.h_k + g) * out_rows + key) * 128 + cc * 16) =
+        nvfp4_group_to_e4m3(c, sc);
+  }
+}
+
 cudaError_t launch_gather_kv(const DecodeDev& a, bool values, uint8_t* out, int out_rows, cudaStream_t stream) {
+  if (a.kv_format == 4) {
+    const int tiles = (out_rows + kTileKV - 1) / kTileKV;
+    dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(a.h_k), static_cast<unsigned>(a.num_seqs));
+    gather_nvfp4_kernel<<<grid, 128, 0, stream>>>(a, values, out, out_rows);
+    return cudaGetLastError();
+  }
   CUtensorMap m;
   const bool ok = values ? make_kv_map(&m, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page,
                                        a.page_size, 1, a.kv_format)
@@ -975,7 +1150,8 @@ cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles
   }
 }
 
-int tc_min_blocks(int rows_per_cta, bool q_e4m3) {
+int tc_min_blocks(int rows_per_cta, bool q_e4m3, bool nvfp4) {
+  if (nvfp4) return 1;
   switch (rows_per_cta) {
     case 8: return q_e4m3 ? TcCfg<8, true>::kMinBlocks : TcCfg<8, false>::kMinBlocks;
     case 16: return q_e4m3 ? TcCfg<16, true>::kMinBlocks : TcCfg<16, false>::kMinBlocks;
@@ -985,7 +1161,15 @@ int tc_min_blocks(int rows_per_cta, bool q_e4m3) {
   }
 }
 
-int tc_smem_bytes(int rows_per_cta, bool q_e4m3) {
+int tc_smem_bytes(int rows_per_cta, bool q_e4m3, bool nvfp4) {
+  if (nvfp4) {
+    switch (rows_per_cta) {
+      case 8: return TcCfg<8, true, true>::kBytes;
+      case 16: return TcCfg<16, true, true>::kBytes;
+      case 32: return TcCfg<32, true, true>::kBytes;
+      default: return 0;
+    }
+  }
   switch (rows_per_cta) {
     case 8: return q_e4m3 ? TcCfg<8, true>::kBytes : TcCfg<8, false>::kBytes;
     case 16: return q_e4m3 ? TcCfg<16, true>::kBytes : TcCfg<16, false>::kBytes;

@@ -56,11 +56,23 @@ int device_sm_count() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
+// nvfp4 scale planes: present, 16-byte aligned, page and head strides
+// 16-byte multiples (a page's rows of one head are 8 bytes apart).
+bool scales_ok(const mj_decode_params& p, const mj_decode_args& a) {
+  if (p.kv_format != MJ_KV_NVFP4) return true;
+  if (!a.k_scales || !a.v_scales || !aligned16(a.k_scales) || !aligned16(a.v_scales)) return false;
+  const int64_t st[4] = {a.ks_page, a.ks_head, a.vs_page, a.vs_head};
+  for (int64_t s : st)
+    if (s <= 0 || (s & 15) != 0 || s >= (int64_t{1} << 40)) return false;
+  return true;
+}
+
 const char* kv_format_name(int f) {
   switch (f) {
     case MJ_KV_E3M2: return "e3m2";
     case MJ_KV_E2M3: return "e2m3";
     case MJ_KV_E2M1: return "e2m1";
+    case MJ_KV_NVFP4: return "nvfp4";
     default: return "e4m3";
   }
 }
@@ -69,7 +81,9 @@ const char* kv_format_name(int f) {
 // TMA boxes), 32-byte aligned for the packed narrow formats (their TMA
 // element types require it).
 bool kv_layout_ok(const mj_decode_params& p, const void* k, const void* v, const int64_t (&strides)[6]) {
-  const bool narrow = p.kv_format != MJ_KV_E4M3;
+  // nvfp4 codes are read as bytes (16-byte rules); the MMA-read narrow
+  // formats need 32
+  const bool narrow = p.kv_format != MJ_KV_E4M3 && p.kv_format != MJ_KV_NVFP4;
   if (!aligned16(k) || !aligned16(v)) return false;
   if (narrow && (!aligned32(k) || !aligned32(v))) return false;
   const int64_t mask = narrow ? 31 : 15;
@@ -112,7 +126,8 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
     static const char* names[2][3] = {{"cc_n4_bf16", "cc_n8_bf16", "cc_n16_bf16"},
                                       {"cc_n4_e4m3", "cc_n8_e4m3", "cc_n16_e4m3"}};
     k.name = names[e4m3][k.rows_per_cta == 4 ? 0 : (k.rows_per_cta == 8 ? 1 : 2)];
-  } else if (p.kernel == MJ_KERNEL_TENSOR_CORE_QROWS || (p.kernel == MJ_KERNEL_AUTO && n_q > kQRowsFrom)) {
+  } else if (p.kernel == MJ_KERNEL_TENSOR_CORE_QROWS ||
+             (p.kernel == MJ_KERNEL_AUTO && n_q > kQRowsFrom && p.kv_format != MJ_KV_NVFP4)) {
     k.kind = KernelKind::kTensorCoreQRows;
     // up to 32 or 64 packed rows: each row held four or two times in the
     // 128 MMA rows, every copy taking that share of a tile's keys
@@ -132,7 +147,7 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
   } else {
     k.kind = KernelKind::kTensorCore;
     k.rows_per_cta = n_q <= 8 ? 8 : (n_q <= 16 ? 16 : (n_q <= 32 ? 32 : 64));
-    smem = tc_smem_bytes(k.rows_per_cta, e4m3);
+    smem = tc_smem_bytes(k.rows_per_cta, e4m3, p.kv_format == MJ_KV_NVFP4);
     static const char* names[2][4] = {{"tc_r8_bf16", "tc_r16_bf16", "tc_r32_bf16", "tc_r64_bf16"},
                                       {"tc_r8_e4m3", "tc_r16_e4m3", "tc_r32_e4m3", "tc_r64_e4m3"}};
     const int idx = k.rows_per_cta == 8 ? 0 : (k.rows_per_cta == 16 ? 1 : (k.rows_per_cta == 32 ? 2 : 3));
@@ -141,7 +156,7 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
   k.n_q_tiles = (n_q + k.rows_per_cta - 1) / k.rows_per_cta;
   int per_sm = kSmemPerSm / (smem + kSmemReservedPerCta);
   int cap = 16;
-  if (k.kind == KernelKind::kTensorCore) cap = tc_min_blocks(k.rows_per_cta, e4m3);
+  if (k.kind == KernelKind::kTensorCore) cap = tc_min_blocks(k.rows_per_cta, e4m3, p.kv_format == MJ_KV_NVFP4);
   if (k.kind == KernelKind::kTensorCoreGrouped || k.kind == KernelKind::kTensorCoreQRows)
     cap = 1;  // owns the SM: all of TMEM, a deep ring
   if (per_sm > cap) per_sm = cap;
@@ -198,7 +213,7 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
     return MJ_ERR_INVALID_ARG;
   if (a.num_work < 1) return MJ_ERR_INVALID_ARG;
   const int64_t kv_strides[6] = {a.k_page, a.k_row, a.k_head, a.v_page, a.v_row, a.v_head};
-  if (!kv_layout_ok(p, a.k, a.v, kv_strides)) return MJ_ERR_INVALID_ARG;
+  if (!kv_layout_ok(p, a.k, a.v, kv_strides) || !scales_ok(p, a)) return MJ_ERR_INVALID_ARG;
   const int q_bytes = p.q_dtype == MJ_E4M3 ? 1 : 2;
   if (!aligned16(a.q) || !aligned16(a.o)) return MJ_ERR_INVALID_ARG;
   if (a.q_seq_stride < 0 || ((a.q_seq_stride * q_bytes) & 15) != 0) return MJ_ERR_INVALID_ARG;
@@ -269,6 +284,12 @@ extern "C" mj_status mj_decode_attn(const mj_decode_params* params, const mj_dec
   d.l2_prefetch = p.l2_prefetch == 0 ? kDefaultL2Prefetch : (p.l2_prefetch < 0 ? 0 : p.l2_prefetch);
   d.kv_evict_first = p.kv_evict_first == 0 ? kDefaultKvEvictFirst : (p.kv_evict_first > 0 ? 1 : 0);
   d.kv_format = p.kv_format;
+  d.ks = a.k_scales;
+  d.vs = a.v_scales;
+  d.ks_page = a.ks_page;
+  d.ks_head = a.ks_head;
+  d.vs_page = a.vs_page;
+  d.vs_head = a.vs_head;
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
@@ -349,9 +370,15 @@ extern "C" mj_status mj_check_gather_kv(const mj_decode_params* params, const mj
   const mj_decode_args& a = *args;
   if (!a.k || !a.v || !a.block_table || !a.seq_lens) return MJ_ERR_INVALID_ARG;
   const int64_t kv_strides[6] = {a.k_page, a.k_row, a.k_head, a.v_page, a.v_row, a.v_head};
-  if (!kv_layout_ok(*params, a.k, a.v, kv_strides)) return MJ_ERR_INVALID_ARG;
+  if (!kv_layout_ok(*params, a.k, a.v, kv_strides) || !scales_ok(*params, a)) return MJ_ERR_INVALID_ARG;
   DecodeDev d{};
   d.kv_format = params->kv_format;
+  d.ks = a.k_scales;
+  d.vs = a.v_scales;
+  d.ks_page = a.ks_page;
+  d.ks_head = a.ks_head;
+  d.vs_page = a.vs_page;
+  d.vs_head = a.vs_head;
   d.k = a.k;
   d.v = a.v;
   d.k_page = a.k_page;

@@ -36,15 +36,23 @@ struct DecodeDev {
   int32_t l2_prefetch;     // tiles the producer prefetches into L2 ahead (0 = off)
   int32_t kv_evict_first;  // K/V tile loads with an L2 EVICT_FIRST policy (0 = off)
   int32_t kv_format;       // mj_kv_format of the K/V pools
+  const uint8_t* ks;       // nvfp4 scale planes: row r of (page, g) at page*x_page + g*x_head + 8r
+  const uint8_t* vs;
+  int64_t ks_page, ks_head, vs_page, vs_head;
 };
 
-// Bits per K/V code of a pool format (mj_kv_format: e4m3, e3m2, e2m3, e2m1).
-__host__ __device__ constexpr int kv_bits(int kv_format) { return kv_format == 0 ? 8 : (kv_format == 3 ? 4 : 6); }
+// Bits per K/V code of a pool format (mj_kv_format: e4m3, e3m2, e2m3, e2m1,
+// nvfp4).
+__host__ __device__ constexpr int kv_bits(int kv_format) {
+  return kv_format == 0 ? 8 : ((kv_format == 3 || kv_format == 4) ? 4 : 6);
+}
 
-// The kind::f8f6f4 operand format code of a pool format.
+// The kind::f8f6f4 operand format code of a pool format (nvfp4 reaches the
+// MMA converted to e4m3).
 __host__ __device__ constexpr uint32_t kv_mma_format(int kv_format) {
   return kv_format == 1 ? 4u : (kv_format == 2 ? 3u : (kv_format == 3 ? 5u : 0u));
 }
+
 
 // Bytes a TMA load of `rows` K/V rows (one head, d = 128 codes each) reads
 // from global memory and credits to its mbarrier: the packed size (the
@@ -237,6 +245,43 @@ template <int R>
 __device__ __forceinline__ bool warp_col_writer(int lane) {
   constexpr int kMask = R >= 32 ? 0 : (R == 16 ? 1 : 3);
   return (lane & kMask) == 0;
+}
+
+// One nvfp4 group: 16 e2m1 codes (8 bytes, element 2i in the low nibble of
+// byte i) and their e4m3 scale -> 16 e4m3 codes of code * scale * 2^-3,
+// rounded to nearest even.  Every step before the rounding is exact in half
+// precision: an e2m1 value has two significant bits and an e4m3 scale four,
+// so the product has at most six, between 2^-13 and 336.
+__device__ __forceinline__ uint4 nvfp4_group_to_e4m3(uint2 codes, uint32_t scale_code) {
+  // the scale / 8 in both halves of a packed pair
+  const uint32_t s2 = e4m3x2_to_f16x2(static_cast<uint16_t>(scale_code & 0xFFu));
+  uint32_t sh;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(sh) : "r"(s2), "r"(0x30003000u));  // (0.125, 0.125)
+  sh = __byte_perm(sh, 0, 0x1010);  // low half in both halves
+  const uint32_t w[2] = {codes.x, codes.y};
+  uint32_t out[4];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w[k]));
+    uint16_t e[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t prod;
+      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(prod) : "r"(h[j]), "r"(sh));
+      asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e[j]) : "r"(prod));
+    }
+    out[2 * k] = static_cast<uint32_t>(e[0]) | (static_cast<uint32_t>(e[1]) << 16);
+    out[2 * k + 1] = static_cast<uint32_t>(e[2]) | (static_cast<uint32_t>(e[3]) << 16);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // Index helpers for the partial-result workspace.

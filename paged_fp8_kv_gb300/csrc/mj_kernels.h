@@ -19,8 +19,9 @@ int cc_smem_bytes(int rows_per_cta);
 // Tensor-core (tcgen05) decode (rows_per_cta in {8, 16, 32}).
 cudaError_t launch_decode_tc(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
                              cudaStream_t stream);
-int tc_smem_bytes(int rows_per_cta, bool q_e4m3);
-int tc_min_blocks(int rows_per_cta, bool q_e4m3);  // co-resident CTAs per SM the kernel is built for
+// nvfp4 pools (a.kv_format 4) run instances with a converter warpgroup.
+int tc_smem_bytes(int rows_per_cta, bool q_e4m3, bool nvfp4 = false);
+int tc_min_blocks(int rows_per_cta, bool q_e4m3, bool nvfp4 = false);  // co-resident CTAs per SM the kernel is built for
 
 // Head-grouped tensor-core decode: one CTA serves heads_per_cta kv heads
 // (rows_per_head packed query rows each); tcg_supported picks the shape.

@@ -37,7 +37,13 @@ mj_status check_params(const mj_decode_params* p) {
   if (p->kernel < MJ_KERNEL_AUTO || p->kernel > MJ_KERNEL_TENSOR_CORE_QROWS) return MJ_ERR_INVALID_ARG;
   if (p->l2_prefetch < -1 || p->l2_prefetch > 8) return MJ_ERR_INVALID_ARG;
   if (p->kv_evict_first < -1 || p->kv_evict_first > 1) return MJ_ERR_INVALID_ARG;
-  if (p->kv_format < MJ_KV_E4M3 || p->kv_format > MJ_KV_E2M1) return MJ_ERR_INVALID_ARG;
+  if (p->kv_format < MJ_KV_E4M3 || p->kv_format > MJ_KV_NVFP4) return MJ_ERR_INVALID_ARG;
+  // nvfp4: converted to e4m3 in the swap-AB kernel, for e4m3 Q (the page's
+  // fp8-Q path) and up to 32 packed rows
+  if (p->kv_format == MJ_KV_NVFP4 &&
+      (p->q_dtype != MJ_E4M3 || static_cast<int64_t>(p->q_len) * p->h_r > 32 ||
+       (p->kernel != MJ_KERNEL_AUTO && p->kernel != MJ_KERNEL_TENSOR_CORE)))
+    return MJ_ERR_UNSUPPORTED;
   // narrow pools: the tensor-core kernels only (the MMA reads the codes)
   if (p->kv_format != MJ_KV_E4M3 && p->kernel != MJ_KERNEL_AUTO && p->kernel != MJ_KERNEL_TENSOR_CORE &&
       p->kernel != MJ_KERNEL_TENSOR_CORE_QROWS)

@@ -103,6 +103,10 @@ class DecodeSession:
         else:
             raise ValueError(kv_layout)
 
+        # nvfp4: the scale planes, (num_pages, h_k, PS, d / 16) e4m3 codes
+        ks, vs = getattr(w, "k_scales", None), getattr(w, "v_scales", None)
+        self.k_scales = torch.from_numpy(ks).to(dev) if ks is not None else None
+        self.v_scales = torch.from_numpy(vs).to(dev) if vs is not None else None
         self.block_table = torch.from_numpy(w.block_table).to(dev)
         self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
         self.q_descale = torch.from_numpy(np.ascontiguousarray(w.q_descale)).to(dev)
@@ -165,6 +169,8 @@ class DecodeSession:
             max_n_splits=self.plan.max_n_splits,
             timing_events=timing_events,
             stream=stream,
+            k_scales=self.k_scales,
+            v_scales=self.v_scales,
         )
 
     def step(self, stream=None, status=None, timing_events=None) -> None:

@@ -75,8 +75,36 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
 # Narrow KV formats: (exponent bits, mantissa bits, bias); sign bit on top,
 # a subnormal binade at exponent 0, no infinities or NaN.
 NARROW_FORMATS = {"e3m2": (3, 2, 3), "e2m3": (2, 3, 1), "e2m1": (2, 1, 1)}
-KV_FORMAT_CODE = {"e4m3": 0, "e3m2": 1, "e2m3": 2, "e2m1": 3}
-KV_FORMAT_BITS = {"e4m3": 8, "e3m2": 6, "e2m3": 6, "e2m1": 4}
+KV_FORMAT_CODE = {"e4m3": 0, "e3m2": 1, "e2m3": 2, "e2m1": 3, "nvfp4": 4}
+KV_FORMAT_BITS = {"e4m3": 8, "e3m2": 6, "e2m3": 6, "e2m1": 4, "nvfp4": 4}
+NVFP4_GROUP = 16  # elements of a row sharing one e4m3 scale
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """float32 values of e4m3 (E4M3FN) codes (0x7F / 0xFF -> NaN)."""
+    c = np.asarray(codes, dtype=np.int32)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float32)
+    mag = np.where(e == 0, m * np.float32(2.0**-9), (np.float32(1.0) + m / np.float32(8.0)) * np.exp2(e - 7).astype(np.float32))
+    mag = np.where((c & 0x7F) == 0x7F, np.float32(np.nan), mag)
+    return np.where(c & 0x80, -mag, mag).astype(np.float32)
+
+
+def nvfp4_encode(v: np.ndarray):
+    """nvfp4 storage of values v (..., d): per group of 16 elements an e4m3
+    scale code = e4m3(8 * amax / 6) (so the group's largest magnitude lands on
+    e2m1's largest, 6, after the 2^-3 the format folds into its scale), and
+    e2m1 codes of v * 8 / scale (nearest, ties to the smaller magnitude).
+    Returns (codes (..., d) uint8, scale codes (..., d / 16) uint8)."""
+    v = np.asarray(v, dtype=np.float32)
+    g = v.reshape(*v.shape[:-1], v.shape[-1] // NVFP4_GROUP, NVFP4_GROUP)
+    amax = np.abs(g).max(axis=-1)
+    sc = e4m3_encode(amax * np.float32(8.0 / 6.0))
+    scv = e4m3_decode(sc)
+    denom = np.where(scv > 0, scv, np.float32(1.0))[..., None]
+    q = np.where(scv[..., None] > 0, g * np.float32(8.0) / denom, np.float32(0.0))
+    codes = narrow_encode(q, "e2m1").reshape(v.shape)
+    return codes, sc
 
 
 def _narrow_magnitudes(fmt: str) -> np.ndarray:
@@ -161,6 +189,10 @@ class Workload:
     max_splits: int = 16
     head_dim: int = HEAD_DIM
     kv_format: str = "e4m3"  # e4m3, or a narrow format packed little-endian
+    # nvfp4 only: e4m3 scale codes, (num_pages, h_k, PS, d / 16) (a page's
+    # scales of one head together, 8 bytes a row)
+    k_scales: Optional[np.ndarray] = None
+    v_scales: Optional[np.ndarray] = None
     meta: Dict[str, object] = field(default_factory=dict)
 
     @property
@@ -219,8 +251,11 @@ class Workload:
         return self._descale_strides(self.v_descale)
 
     def kv_bytes(self) -> int:
-        """K + V bytes of the rows the attention reads (rows < L)."""
+        """K + V bytes of the rows the attention reads (rows < L), nvfp4's
+        scales included."""
         row = self.head_dim * KV_FORMAT_BITS[self.kv_format] // 8
+        if self.kv_format == "nvfp4":
+            row += self.head_dim // NVFP4_GROUP
         return int(self.seq_lens.astype(np.int64).sum()) * self.h_k * row * 2
 
 
@@ -232,6 +267,7 @@ def _fill_kv(
     seq_lens: np.ndarray,
     descale: np.ndarray,
     kv_format: str = "e4m3",
+    scales: Optional[np.ndarray] = None,
 ) -> None:
     """Quantised N(0,1)/descale rows for every (seq, page, row < L); the rest
     of the pool keeps the poison code it was created with.  Sequence b draws
@@ -252,6 +288,12 @@ def _fill_kv(
         x /= descale[b].astype(np.float32)[None, :, None]
         if kv_format == "e4m3":
             codes = e4m3_encode(x)
+        elif kv_format == "nvfp4":
+            c4, sc = nvfp4_encode(x)
+            codes = pack_codes(c4, 4)
+            sc[L:] = E4M3_NAN  # rows past the sequence end: a NaN scale
+            # the scale plane is (page, head, row, group)
+            scales[pages] = sc.reshape(n_pages, PS, h_k, -1).transpose(0, 2, 1, 3)
         else:
             codes = pack_codes(narrow_encode(x, kv_format), KV_FORMAT_BITS[kv_format])
         codes[L:] = E4M3_NAN  # rows past the sequence end (poison bytes)
@@ -316,8 +358,12 @@ def make_workload(
     row_bytes = d * KV_FORMAT_BITS[kv_format] // 8
     k_cache = np.full((num_pages, page_size, h_k, row_bytes), E4M3_NAN, dtype=np.uint8)
     v_cache = np.full((num_pages, page_size, h_k, row_bytes), E4M3_NAN, dtype=np.uint8)
-    _fill_kv(seed, 1, k_cache, bt, seq, k_desc, kv_format)
-    _fill_kv(seed, 2, v_cache, bt, seq, v_desc, kv_format)
+    k_scales = v_scales = None
+    if kv_format == "nvfp4":
+        k_scales = np.full((num_pages, h_k, page_size, d // NVFP4_GROUP), E4M3_NAN, dtype=np.uint8)
+        v_scales = np.full((num_pages, h_k, page_size, d // NVFP4_GROUP), E4M3_NAN, dtype=np.uint8)
+    _fill_kv(seed, 1, k_cache, bt, seq, k_desc, kv_format, k_scales)
+    _fill_kv(seed, 2, v_cache, bt, seq, v_desc, kv_format, v_scales)
     h_q = h_k * h_r
     qx = rng.standard_normal((b * q_len, h_q, d), dtype=np.float32)
     if q_is_e4m3:
@@ -348,6 +394,8 @@ def make_workload(
         scale_o=scale_o,
         max_splits=max_splits,
         kv_format=kv_format,
+        k_scales=k_scales,
+        v_scales=v_scales,
         meta={"seed": seed},
     )
 

@@ -66,17 +66,20 @@ def e4m3_view(w, seqs=None):
 
     if w.kv_format == "e4m3":
         return w
-    bits = narrow_ref.BITS[w.kv_format]
     e4 = oracle.e4m3_table()
     v = copy.copy(w)
     v.kv_format = "e4m3"
-    for name in ("k_cache", "v_cache"):
+    for name, sname in (("k_cache", "k_scales"), ("v_cache", "v_scales")):
         src = getattr(w, name)
         dst = np.zeros(src.shape[:3] + (w.head_dim,), dtype=np.uint8)
         bs = range(w.num_seqs) if seqs is None else seqs
         pages = sorted({int(p) for b in bs for p in w.block_table[b, : -(-int(w.seq_lens[b]) // w.page_size)]})
-        if pages:
-            codes = narrow_ref.unpack_bits(src[pages], bits, w.head_dim)
+        if pages and w.kv_format == "nvfp4":
+            codes = narrow_ref.unpack_bits(src[pages], 4, w.head_dim)
+            scales = getattr(w, sname)[pages].transpose(0, 2, 1, 3)  # (page, row, head, group)
+            dst[pages] = narrow_ref.nvfp4_to_e4m3_codes(codes, scales)
+        elif pages:
+            codes = narrow_ref.unpack_bits(src[pages], narrow_ref.BITS[w.kv_format], w.head_dim)
             dst[pages] = narrow_ref.to_e4m3_codes(codes, w.kv_format, e4)
         setattr(v, name, dst)
     return v

@@ -39,6 +39,18 @@ def test_algorithmic_bytes_by_hand():
     assert step == decode
 
 
+def test_narrow_kv_bytes_by_hand():
+    # the same tiny problem with packed pools: fp4 rows of 64 bytes, fp6 rows
+    # of 96, nvfp4 rows of 64 bytes of codes and 8 of scales
+    for fmt, row in (("e2m1", 64), ("e3m2", 96), ("nvfp4", 72)):
+        w = syn.make_workload("tiny_narrow", [37, 100], 1, 1, 8, 16, seed=1112, random_descales=False,
+                              max_splits=1, num_pages=16, kv_format=fmt)
+        plan = tiny_plan(w)
+        decode, _, _ = bench.algorithmic_bytes(w, plan)
+        fixed = 2 * (2 * 1 * 8 * 128 * 2) + 2 * 1 * 8 * 4 + (3 + 7) * 4 + plan.num_work * 16 + 2 * 8 + 3 * 2 * 1 * 4
+        assert decode == (37 + 100) * 1 * row * 2 + fixed, fmt
+
+
 def test_algorithmic_flops_by_hand():
     # every visible (key, row) pair costs 2 d for S and 2 d for O
     w = syn.config(1)

@@ -408,7 +408,7 @@ def test_verbose_switch_prints_the_plan_and_nothing_without_it():
 
 def test_narrow_kv_format_validation():
     p = _params(1, h_r=4, max_splits=16)
-    p.kv_format = 4
+    p.kv_format = 5
     assert _attn_status(p, _good_args()) == mj.MJ_ERR_INVALID_ARG
     for kernel in (mj.MJ_KERNEL_CUDA_CORE, mj.MJ_KERNEL_TENSOR_CORE_GROUPED):
         q = _params(1, h_k=8, h_r=4, max_splits=16, kernel=kernel)
@@ -425,6 +425,32 @@ def test_narrow_kv_format_validation():
         a = _good_args()
         a.k_page, a.k_row, a.k_head = 16 * 64, 64, 64
         a.v_page, a.v_row, a.v_head = 16 * 64, 64, 64
+        a.workspace = 1 << 20
+        a.workspace_bytes = mj.workspace_bytes(q)
+        setattr(a, field, val)
+        assert _attn_status(q, a) == mj.MJ_ERR_INVALID_ARG, field
+
+
+def test_nvfp4_validation():
+    # e4m3 Q and at most 32 rows on the swap-AB kernel; scale planes needed
+    buf = ctypes.create_string_buffer(64)
+    for q_dtype, h_r, kernel, want in ((mj.MJ_BF16, 16, 0, mj.MJ_ERR_UNSUPPORTED), (mj.MJ_E4M3, 64, 0, mj.MJ_ERR_UNSUPPORTED),
+                                       (mj.MJ_E4M3, 16, mj.MJ_KERNEL_TENSOR_CORE_QROWS, mj.MJ_ERR_UNSUPPORTED),
+                                       (mj.MJ_E4M3, 16, 0, mj.MJ_OK), (mj.MJ_E4M3, 32, 0, mj.MJ_OK)):
+        q = _params(1, h_r=h_r, max_splits=16, q_dtype=q_dtype, kernel=kernel)
+        q.kv_format = mj.MJ_KV_NVFP4
+        assert mj.lib().mj_kernel_name(ctypes.byref(q), buf, 64) == want, (q_dtype, h_r, kernel)
+        if want == mj.MJ_OK:
+            assert buf.value.decode().startswith("tc_") and buf.value.decode().endswith("_kvnvfp4")
+    q = _params(1, h_r=16, max_splits=16, q_dtype=mj.MJ_E4M3)
+    q.kv_format = mj.MJ_KV_NVFP4
+    fake = 1 << 20
+    for field, val in (("k_scales", None), ("v_scales", fake + 8), ("ks_head", 8), ("vs_page", 0)):
+        a = _good_args()
+        a.k_page, a.k_row, a.k_head = 16 * 64, 64, 64
+        a.v_page, a.v_row, a.v_head = 16 * 64, 64, 64
+        a.k_scales, a.v_scales = fake, fake
+        a.ks_page, a.ks_head, a.vs_page, a.vs_head = 16 * 8, 16 * 8, 16 * 8, 16 * 8
         a.workspace = 1 << 20
         a.workspace_bytes = mj.workspace_bytes(q)
         setattr(a, field, val)

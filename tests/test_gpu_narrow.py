@@ -112,3 +112,56 @@ def test_full_size_sampled(cfg, opts, fmt):
     longest = int(np.argmax(w.seq_lens))
     units = sample_units(w, 6, seed=cfg, include=[(longest, w.h_k - 1), (w.num_seqs - 1, 0)])
     compare(w, s.o_host(), s.lse_host(), units=units)
+
+
+# --------------------------------------------------------------------- nvfp4
+
+
+@pytest.mark.parametrize("page_size", [16, 64, 128])
+def test_nvfp4_conversion_is_bit_exact(page_size):
+    # the kernel's conversion of each 16-code group and its scale, through the
+    # block table and the scale plane, against the oracle's definition
+    w = syn.make_workload("nv_gather", [1, 17, 130, 300], 1, 2, 4, page_size, seed=62, q_is_e4m3=True,
+                          kv_format="nvfp4")
+    s = DecodeSession(w)
+    rows = int(w.seq_lens.max())
+    for values, cache, scales in ((False, w.k_cache, w.k_scales), (True, w.v_cache, w.v_scales)):
+        out = torch.zeros((w.num_seqs, w.h_k, rows, 128), dtype=torch.uint8, device="cuda")
+        mj.check_gather_kv(s.params, s.k_cache, s.v_cache, s.block_table, s.seq_lens, values, out,
+                           k_scales=s.k_scales, v_scales=s.v_scales)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        for b in range(w.num_seqs):
+            L = int(w.seq_lens[b])
+            j = np.arange(L)
+            pg, rw = w.block_table[b, j // page_size], j % page_size
+            for g in range(w.h_k):
+                codes = narrow_ref.unpack_bits(cache[pg, rw, g], 4, 128)
+                want = narrow_ref.nvfp4_to_e4m3_codes(codes, scales[pg, g, rw])
+                assert np.array_equal(got[b, g, :L], want), f"values={values} b={b} g={g}"
+
+
+NV_SMALL = [
+    ("skewed_split", lambda: syn.config(3, num_seqs=3, len_range=(6000, 500), kv_format="nvfp4")),
+    ("gqa_rows8", lambda: syn.make_workload("nv_gqa", [1, 300, 1000, 2500, 129], 1, 8, 4, 16, seed=63,
+                                            q_is_e4m3=True, kv_format="nvfp4")),
+    ("spec_rows32", lambda: syn.make_workload("nv_spec", [500, 1800, 3], 4, 8, 8, 64, seed=64, q_is_e4m3=True,
+                                              kv_format="nvfp4")),
+]
+
+
+@pytest.mark.parametrize("name,make", NV_SMALL, ids=[c[0] for c in NV_SMALL])
+def test_nvfp4_attention_small(name, make):
+    w = make()
+    s = run(w)
+    assert s.kernel.startswith("tc_") and s.kernel.endswith("_kvnvfp4"), s.kernel
+    compare(w, s.o_host(), s.lse_host())
+    s2 = run(w, force_splits=3)
+    compare(w, s2.o_host(), s2.lse_host())
+
+
+def test_nvfp4_full_size_sampled():
+    w = syn.config(3, kv_format="nvfp4")
+    s = run(w)
+    assert s.plan.n_splits[0] > 1
+    compare(w, s.o_host(), s.lse_host(), units=[(0, 0), (3, 0), (7, 0)])

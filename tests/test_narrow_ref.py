@@ -9,12 +9,19 @@ What fixes each part, independently of the oracle's own code:
 * the encoder: every table value to its own code, midpoints to the smaller
   neighbour (the page's tie rule), saturation, no negative-zero codes;
 * the packing: hand-written bytes for a few codes, and round trips;
-* the e4m3 view: each narrow value equals the e4m3 value of its mapped code.
+* the e4m3 view: each narrow value equals the e4m3 value of its mapped code;
+* nvfp4: hand-worked (code, scale) pairs (tests/golden/nvfp4_examples.json),
+  every one of the 16 x 256 pairs within half an e4m3 step of the exact
+  product (brute force), and the scale of element i being that of group
+  i // 16.
 
 Each pin is a function of the module under test, so that
 tests/test_oracle_mutations.py can run the same pins against copies of the
 module with planted mistakes.
 """
+
+import json
+import os
 
 import numpy as np
 import pytest
@@ -84,6 +91,41 @@ def pin_e4m3_view(m, fmt):
     assert np.array_equal(e4[m.to_e4m3_codes(c, fmt, e4)], t[c] + 0.0)
 
 
+GOLDEN_NVFP4 = os.path.join(os.path.dirname(__file__), "golden", "nvfp4_examples.json")
+
+
+def pin_nvfp4_golden(m):
+    for c in json.load(open(GOLDEN_NVFP4))["cases"]:
+        got = m.nvfp4_to_e4m3_codes(np.full((1, 16), c["code"]), np.array([[c["scale"]]]))
+        assert np.all(got == c["expect"]), c["why"]
+
+
+def pin_nvfp4_rounding_bound(m):
+    e4 = oracle.e4m3_table()
+    e2 = m.minifloat_table("e2m1")
+    codes = np.repeat(np.arange(16), 16)[None, :]  # group g holds code g
+    for sc in range(256):
+        if sc in (0x7F, 0xFF):
+            continue
+        got = e4[m.nvfp4_to_e4m3_codes(codes, np.full((1, 16), sc))][0, ::16]
+        exact = e2 * e4[sc] / 8.0
+        # half a step of e4m3 at the exact value (2^-10 below the normal range)
+        mag = np.maximum(np.abs(exact), 2.0**-6)
+        half = 2.0 ** (np.floor(np.log2(mag)) - 4)
+        assert np.all(np.abs(got - exact) <= half * (1 + 1e-12)), sc
+
+
+def pin_nvfp4_groups(m):
+    codes = np.full((2, 128), 4)  # 2.0 everywhere
+    scales = np.arange(16).reshape(2, 8) * 8 + 0x38  # distinct scales per group
+    e4 = oracle.e4m3_table()
+    got = e4[m.nvfp4_to_e4m3_codes(codes, scales)]
+    for r in range(2):
+        for i in range(128):
+            assert got[r, i] == e4[m.nvfp4_to_e4m3_codes(np.full((1, 16), 4), scales[r : r + 1, i // 16 : i // 16 + 1])][0, 0]
+    assert len(set(got[0, ::16])) == 8
+
+
 def all_pins(m):
     """Every pin against module m (raises on the first that fails)."""
     pin_e2m1_values(m)
@@ -95,6 +137,9 @@ def all_pins(m):
     pin_packing_bytes(m)
     for bits in (4, 6):
         pin_packing_round_trip(m, bits)
+    pin_nvfp4_golden(m)
+    pin_nvfp4_rounding_bound(m)
+    pin_nvfp4_groups(m)
 
 
 def test_e2m1_values():
@@ -136,3 +181,15 @@ def test_packing_round_trip(bits):
 @pytest.mark.parametrize("fmt", FMTS)
 def test_e4m3_view_is_exact(fmt):
     pin_e4m3_view(narrow_ref, fmt)
+
+
+def test_nvfp4_hand_worked_examples():
+    pin_nvfp4_golden(narrow_ref)
+
+
+def test_nvfp4_rounding_bound_over_every_pair():
+    pin_nvfp4_rounding_bound(narrow_ref)
+
+
+def test_nvfp4_scale_groups():
+    pin_nvfp4_groups(narrow_ref)

@@ -24,6 +24,8 @@ def load(path, name, tmp_path, old=None, new=None):
         assert old in src, f"mutation anchor missing: {old!r}"
         src = src.replace(old, new, 1)
     src = src.replace("from .layout_ref import", "from oracle.layout_ref import")
+    src = src.replace("from .quant_ref import", "from oracle.quant_ref import")
+    src = src.replace("from . import", "from oracle import")
     f = tmp_path / f"{name}.py"
     f.write_text(src)
     spec = importlib.util.spec_from_file_location(name, str(f))
@@ -98,6 +100,9 @@ NARROW_MUTATIONS = [
     ("unpack reads the wrong byte", "out[:, i] |= ((flat[:, j // 8] >> (j % 8)) & 1) << k", "out[:, i] |= ((flat[:, (j // 8) ^ 1] >> (j % 8)) & 1) << k"),
     ("mantissa width", '"e3m2": (3, 2, 3)', '"e3m2": (2, 3, 3)'),
     ("sign of the search", "dist = abs(abs(v) - table[c])", "dist = abs(v - table[c])"),
+    ("nvfp4 shift", "NVFP4_SHIFT = 2.0**-3", "NVFP4_SHIFT = 2.0**-2"),
+    ("nvfp4 group of 8", "NVFP4_GROUP = 16  #", "NVFP4_GROUP = 8  #"),
+    ("nvfp4 scale code as value", "e2m1[c] * e4[sc] * NVFP4_SHIFT", "e2m1[c] * sc * NVFP4_SHIFT"),
 ]
 
 
