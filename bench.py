@@ -579,57 +579,41 @@ def q_quant_measure(w, dev, flush, launches: int = 200):
 
 
 def e2e_measure(args, s, w, step_bytes, dev):
-    """Same step through the public API from HOST buffers: host plan, H2D of
-    the step's inputs (Q, seq_lens, block table, work list, n_splits), the
-    step, D2H of O and LSE; host wall clock per step."""
+    """Same step through the public API from HOST buffers, as a serving loop
+    runs it (DecodeSession.stage / staged_step): per step the host plan, one
+    host-to-device copy of the step's inputs (Q, seq_lens, block table, work
+    list, n_splits, staged in one pinned buffer), the step as a CUDA graph
+    replay, one device-to-host copy of O and LSE, and a synchronisation;
+    host wall clock per step."""
     import torch
 
     from paged_fp8_kv_gb300 import decode_plan
+    from paged_fp8_kv_gb300.session import DecodeSession
 
-    pin = lambda t: t.cpu().pin_memory()
-    q_h = pin(s.q_vllm)
-    sl_h = pin(s.seq_lens)
-    bt_h = pin(s.block_table)
-    o_h = torch.empty(s.o_vllm.shape, dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty(s.lse.shape, dtype=torch.float32).pin_memory()
+    e = DecodeSession(w, device=str(dev), kv_layout=args.kv_layout, kernel=args.kernel,
+                      l2_prefetch=args.l2_prefetch, kv_evict_first=args.kv_evict_first, ctas_per_sm=args.ctas_per_sm)
+    e.stage()
     seq_host = w.seq_lens
-    h2d = q_h.numel() * q_h.element_size() + sl_h.numel() * 4 + bt_h.numel() * 4
-    d2h = o_h.numel() * 2 + lse_h.numel() * 4
-    # pinned staging for the plan's outputs, allocated once (as a serving
-    # loop would keep it)
-    work_pin = torch.empty((max(1, w.num_seqs * s.max_splits), 4), dtype=torch.int32).pin_memory()
-    ns_pin = torch.empty((w.num_seqs,), dtype=torch.int32).pin_memory()
     times = []
     for i in range(args.warmup + args.steps):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        plan = decode_plan(s.params, seq_host, sm_count=s.sm_count, ctas_per_sm=s.ctas_per_sm)
-        n = plan.num_work
-        work_pin.numpy()[:n] = plan.work
-        ns_pin.numpy()[:] = plan.n_splits
-        work_h, ns_h = work_pin[:n], ns_pin
-        s.q_vllm.copy_(q_h, non_blocking=True)
-        s.seq_lens.copy_(sl_h, non_blocking=True)
-        s.block_table.copy_(bt_h, non_blocking=True)
-        if s.work.shape == work_h.shape:
-            s.work.copy_(work_h, non_blocking=True)
-        else:
-            s.work = work_h.to(dev, non_blocking=True)
-        s.n_splits.copy_(ns_h, non_blocking=True)
-        s.step()
-        o_h.copy_(s.o_vllm, non_blocking=True)
-        lse_h.copy_(s.lse, non_blocking=True)
+        plan = decode_plan(e.params, seq_host, sm_count=e.sm_count, ctas_per_sm=e.ctas_per_sm)
+        e.staged_step(plan)
         torch.cuda.synchronize()
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-        h2d_step = h2d + work_h.numel() * 4 + ns_h.numel() * 4
+    h2d, d2h = e.staged_bytes()
     t = float(np.mean(times))
+    del e
+    torch.cuda.empty_cache()
     return {
         "value": round(step_bytes / t / 1e9, 2),
         "unit": "GB/s",
         "us_per_step": round(t * 1e6, 2),
-        "h2d_bytes_per_step": int(h2d_step),
+        "h2d_bytes_per_step": int(h2d),
         "d2h_bytes_per_step": int(d2h),
+        "how": "host plan, one pinned H2D copy of the inputs, the step as a CUDA graph replay, one D2H copy of O and LSE, sync",
     }
 
 

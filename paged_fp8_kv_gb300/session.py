@@ -191,3 +191,95 @@ class DecodeSession:
 
     def lse_host(self) -> np.ndarray:
         return self.lse.cpu().numpy()
+
+    # ------------------------------------------------ host-to-host serving step
+
+    def stage(self, work_cap: Optional[int] = None):
+        """Prepare a serving loop's step from host memory: the step's inputs
+        (Q in vLLM's layout, seq_lens, block table, work list, n_splits) become
+        views of ONE device buffer with a pinned host twin, and the outputs (O
+        in vLLM's layout, LSE) views of one more, so that a step is one
+        host-to-device copy, the decode step (replayed as a CUDA graph), and one
+        device-to-host copy.  Returns the pinned host views, keyed by name; the
+        caller fills q / seq_lens / block_table and calls staged_step()."""
+        dev = self.device
+        cap = int(work_cap or max(1, self.num_seqs * self.max_splits))
+
+        def layout(items):
+            off, out = 0, {}
+            for name, shape, dtype in items:
+                off = (off + 255) // 256 * 256
+                nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+                out[name] = (off, shape, dtype, nbytes)
+                off += nbytes
+            return out, (off + 255) // 256 * 256
+
+        ins, in_bytes = layout([
+            ("q", tuple(self.q_vllm.shape), self.q_vllm.dtype),
+            ("seq_lens", tuple(self.seq_lens.shape), torch.int32),
+            ("block_table", tuple(self.block_table.shape), torch.int32),
+            ("work", (cap, 4), torch.int32),
+            ("n_splits", (self.num_seqs,), torch.int32),
+        ])
+        outs, out_bytes = layout([
+            ("o", (self.num_seqs * self.q_len, self.h_k * self.h_r, self.d), torch.bfloat16),
+            ("lse", tuple(self.lse.shape), torch.float32),
+        ])
+        self._in_dev = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        self._in_host = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        self._out_dev = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+        self._out_host = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+
+        def view(buf, spec):
+            off, shape, dtype, nbytes = spec
+            return buf[off : off + nbytes].view(dtype).view(shape)
+
+        dv = {k: view(self._in_dev, v) for k, v in ins.items()}
+        hv = {k: view(self._in_host, v) for k, v in ins.items()}
+        hv["q"].copy_(self.q_vllm)
+        hv["seq_lens"].copy_(self.seq_lens)
+        hv["block_table"].copy_(self.block_table)
+        self.q_vllm, self.seq_lens, self.block_table = dv["q"], dv["seq_lens"], dv["block_table"]
+        if self.q_len == 1:
+            self.q_packed = self.q_vllm.view(self.num_seqs, self.h_k, self.n_q, self.d)
+        self._work_dev, self.n_splits = dv["work"], dv["n_splits"]
+        o = view(self._out_dev, outs["o"])
+        self.lse = view(self._out_dev, outs["lse"]).view(self.num_seqs, self.h_k, self.n_q)
+        if self.q_len == 1:
+            self.o_packed = o.view(self.num_seqs, self.h_k, self.n_q, self.d)
+        self.o_vllm = o
+        self._host_out = {k: view(self._out_host, v) for k, v in outs.items()}
+        self._host_in = hv
+        self._graph, self._graph_key = None, None
+        return hv
+
+    def staged_step(self, plan) -> dict:
+        """One serving step from the pinned host views stage() returned: the
+        plan's work list and split counts join the inputs there, one
+        host-to-device copy, the step as a CUDA graph (captured again only when
+        the plan's item count or largest split count changes), one
+        device-to-host copy of O and LSE.  Returns the pinned output views
+        (valid once the stream is synchronised)."""
+        n = plan.num_work
+        self._host_in["work"].numpy()[:n] = plan.work
+        self._host_in["n_splits"].numpy()[:] = plan.n_splits
+        self.plan = plan
+        self.work = self._work_dev[:n]
+        self._in_dev.copy_(self._in_host, non_blocking=True)
+        key = (n, plan.max_n_splits)
+        if self._graph is None or self._graph_key != key:
+            stream = torch.cuda.current_stream(self.device)
+            side = torch.cuda.Stream(self.device)
+            side.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                self.step(stream=side)
+            stream.wait_stream(side)
+            self._graph, self._graph_key = g, key
+        self._graph.replay()
+        self._out_host.copy_(self._out_dev, non_blocking=True)
+        return self._host_out
+
+    def staged_bytes(self):
+        """(host-to-device, device-to-host) bytes a staged step copies."""
+        return int(self._in_host.numel()), int(self._out_host.numel())

@@ -335,3 +335,30 @@ def test_merge_refuses_a_hint_below_the_split_count():
     call(6, status)
     assert int(status.item()) == 0
     compare(w, s.o_host(), s.lse_host())
+
+
+@pytest.mark.parametrize("cfg,kw", [(4, dict(num_seqs=3, len_range=(500, 1500))), (3, dict(num_seqs=3, len_range=(3000, 300)))],
+                         ids=["spec_verify_qlen4", "skewed_fp8_split"])
+def test_staged_serving_step_matches_the_step(cfg, kw):
+    # the host-to-host serving step (one pinned input copy, the step as a
+    # CUDA graph, one output copy) gives the plain step's bytes, and is
+    # captured again when the plan's shape changes
+    import paged_fp8_kv_gb300 as mj
+
+    w = syn.config(cfg, **kw)
+    s = run(w)
+    ref_o, ref_lse = s.o_vllm.cpu(), s.lse.cpu()
+    e = DecodeSession(w)
+    e.stage()
+    for force in (0, 3, 0):
+        plan = mj.decode_plan(e.params, w.seq_lens, sm_count=e.sm_count, force_splits=force)
+        out = e.staged_step(plan)
+        torch.cuda.synchronize()
+        o = out["o"].clone()
+        lse = out["lse"].view(w.num_seqs, w.h_k, w.n_q).clone()
+        if force == 0:
+            assert torch.equal(o.view(torch.int16), ref_o.view(torch.int16))
+            assert torch.equal(lse, ref_lse)
+        else:
+            packed = torch.from_numpy(pack_q_ref(o.float().numpy(), w.num_seqs, w.q_len, w.h_k, w.h_r))
+            compare(w, packed.numpy(), lse.numpy())
