@@ -43,8 +43,10 @@ struct CcSmem {
 template <int NT, bool kQe4m3>
 __global__ void __launch_bounds__(kThreads)
 decode_cc_kernel(const DecodeDev a, int n_q_tiles) {
-  // the merge (a programmatic dependent) may launch now: its CTAs wait
-  // for this grid's completion before reading what it writes
+  // Launched as a programmatic dependent: no global load or store before
+  // the grid ahead of this one has completed.  The merge (this grid's own
+  // dependent) may launch now; its CTAs wait the same way.
+  ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   CcSmem<NT>& sm = *reinterpret_cast<CcSmem<NT>*>(smem_raw);
@@ -298,8 +300,7 @@ cudaError_t launch_cc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
-  kern<<<grid, kThreads, smem, stream>>>(a, n_q_tiles);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads, 1, 1), smem, stream, a, n_q_tiles);
 }
 
 }  // namespace

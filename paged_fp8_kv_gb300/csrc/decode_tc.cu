@@ -193,8 +193,10 @@ __global__ void __launch_bounds__((TcCfg<R, kQe4m3, kNv>::kThreads), (TcCfg<R, k
 decode_tc_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_ks,
                  const __grid_constant__ CUtensorMap tmap_vs, int n_q_tiles) {
-  // the merge (a programmatic dependent) may launch now: its CTAs wait
-  // for this grid's completion before reading what it writes
+  // Launched as a programmatic dependent: no global load or store before
+  // the grid ahead of this one has completed.  The merge (this grid's own
+  // dependent) may launch now; its CTAs wait the same way.
+  ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   using C = TcCfg<R, kQe4m3, kNv>;
   extern __shared__ uint8_t smem_raw[];
@@ -982,8 +984,7 @@ cudaError_t launch_tc(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
-  kern<<<grid, C::kThreads, C::kBytes, stream>>>(a, mk, mv, mks, mvs, n_q_tiles);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(C::kThreads, 1, 1), C::kBytes, stream, a, mk, mv, mks, mvs, n_q_tiles);
 }
 
 template <int R>

@@ -294,8 +294,10 @@ template <int G, int RH, bool kQe4m3>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tcg_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles, int num_units, int* sched) {
-  // the merge (a programmatic dependent) may launch now: its CTAs wait
-  // for this grid's completion before reading what it writes
+  // Launched as a programmatic dependent: no global load or store before
+  // the grid ahead of this one has completed.  The merge (this grid's own
+  // dependent) may launch now; its CTAs wait the same way.
+  ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   using C = GCfg<G, RH, kQe4m3>;
   using It = Item<G>;
@@ -1258,8 +1260,8 @@ cudaError_t launch_tcg(const DecodeDev& a, int n_q_tiles, int* sched, int sm_cou
   e = cudaMemsetAsync(sched, 0, sizeof(int), stream);
   if (e != cudaSuccess) return e;
   const int grid = num_units < sm_count ? num_units : sm_count;
-  kern<<<grid, kThreads, C::kBytes, stream>>>(a, mk, mv, n_q_tiles, num_units, sched);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid, 1, 1), dim3(kThreads, 1, 1), C::kBytes, stream, a, mk, mv, n_q_tiles,
+                    num_units, sched);
 }
 
 }  // namespace

@@ -43,6 +43,11 @@ constexpr int kStatusInvalidArg = 1;  // MJ_ERR_INVALID_ARG
 template <int kWPR, int kPer>
 __global__ void __launch_bounds__((kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32) merge_kernel(const DecodeDev a) {
   constexpr int kRowsPerCta = kWPR >= kCtaWarps ? 1 : kCtaWarps / kWPR;
+  // a programmatic dependent of the decode grid: every CTA waits for that
+  // grid's completion (its partials complete and visible) before touching
+  // global memory, and the unpack after it may launch now
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int wic = threadIdx.x >> 5;         // warp in the CTA
   const int w = wic % kWPR;                 // warp within the row
@@ -61,8 +66,6 @@ __global__ void __launch_bounds__((kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32) me
     if (w == 0 && lane == 0 && a.status) atomicExch(a.status, kStatusInvalidArg);
     return;
   }
-  ptx::griddep_wait();  // the decode grid's partials are complete and visible
-
   const int j0 = w * kPer;
   const int cnt = nsp - j0 < kPer ? nsp - j0 : kPer;  // this warp's splits (may be <= 0)
   const int64_t pr0 = part_row(a, b, g, 0, n);
@@ -147,22 +150,14 @@ cudaError_t launch_merge_t(const DecodeDev& a, cudaStream_t stream) {
   constexpr int kRowsPerCta = kWPR >= kCtaWarps ? 1 : kCtaWarps / kWPR;
   constexpr int kThreads = (kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32;
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.h_k * a.n_q;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kThreads / 32 * kPer * 32 * 16;  // the staging area: kPer x 512 B a warp
-  if (cfg.dynamicSmemBytes > 48 * 1024) {
+  const dim3 grid(static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta), 1, 1);
+  const size_t smem = kThreads / 32 * kPer * 32 * 16;  // the staging area: kPer x 512 B a warp
+  if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(merge_kernel<kWPR, kPer>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(cfg.dynamicSmemBytes));
+                                               static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<kWPR, kPer>, a);
+  return launch_pdl(merge_kernel<kWPR, kPer>, grid, dim3(kThreads, 1, 1), smem, stream, a);
 }
 
 }  // namespace

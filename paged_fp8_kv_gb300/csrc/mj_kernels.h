@@ -4,9 +4,34 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "mj_device.cuh"
 
 namespace mj {
+
+// Launches kern as a programmatic dependent of the work before it in the
+// stream: its CTAs may become resident once every CTA of the previous grid
+// has called griddep_launch_dependents (or exited), hiding the launch under
+// that grid's tail.  Every kernel launched this way calls griddep_wait in
+// every CTA before its first global load or store and before it exits, so
+// each kernel of a chain still starts its memory work after the one before
+// it has completed, and so transitively after all earlier ones.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 constexpr int kHeadDimDev = 128;
 constexpr int kTileRowsDev = 128;

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "mj_kernels.h"
+#include "sm100_ptx.cuh"
 
 namespace mj {
 namespace {
@@ -14,6 +15,10 @@ namespace {
 __global__ void permute_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                     int64_t total_vec, int vec_per_row, int q_len, int h_k, int h_r,
                                     bool to_packed) {
+  // a programmatic dependent: no global load or store before the grid
+  // ahead of this one has completed; the next kernel may launch now
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (i >= total_vec) return;
   const int64_t row = i / vec_per_row;
@@ -52,10 +57,9 @@ cudaError_t launch_permute_rows(const void* src, void* dst, int elem_bytes, int 
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
-  permute_rows_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(src), static_cast<uint4*>(dst), total, vec_per_row, q_len, h_k, h_r,
-      to_packed);
-  return cudaGetLastError();
+  return launch_pdl(permute_rows_kernel, dim3(static_cast<unsigned>(blocks), 1, 1), dim3(threads, 1, 1), 0, stream,
+                    static_cast<const uint4*>(src), static_cast<uint4*>(dst), total, vec_per_row, q_len, h_k, h_r,
+                    to_packed);
 }
 
 }  // namespace mj

@@ -31,6 +31,7 @@
 #include <cstdint>
 
 #include "mj_kernels.h"
+#include "sm100_ptx.cuh"
 
 namespace mj {
 namespace {
@@ -60,6 +61,10 @@ __global__ void __launch_bounds__(kPlanThreads)
                        int max_splits, int force_splits, int min_chunk, int pad_to, int sort_n,
                        int4* __restrict__ work, int32_t* __restrict__ n_splits, int32_t* __restrict__ chunk_out,
                        int32_t* __restrict__ status) {
+  // a programmatic dependent: no global load or store before the grid
+  // ahead of this one has completed; the next kernel may launch now
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);      // [sort_n]
   int32_t* tiles = reinterpret_cast<int32_t*>(keys + sort_n);  // [num_seqs]
@@ -249,9 +254,9 @@ cudaError_t launch_plan_device(const int32_t* seq_lens, int num_seqs, int64_t ma
         cudaFuncSetAttribute(plan_device_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  plan_device_kernel<<<1, kPlanThreads, smem, stream>>>(seq_lens, num_seqs, max_len, slots, max_splits, force_splits,
-                                                        min_chunk, pad_to, sort_n, work, n_splits, chunk_out, status);
-  return cudaGetLastError();
+  return launch_pdl(plan_device_kernel, dim3(1, 1, 1), dim3(kPlanThreads, 1, 1), smem, stream, seq_lens, num_seqs,
+                    max_len, slots, max_splits, force_splits, min_chunk, pad_to, sort_n, work, n_splits, chunk_out,
+                    status);
 }
 
 }  // namespace mj

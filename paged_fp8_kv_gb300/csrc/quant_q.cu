@@ -45,6 +45,10 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* x) {
 __global__ void __launch_bounds__(kMaxThreads)
     quantize_pack_q_kernel(const uint4* __restrict__ q, uint4* __restrict__ q_packed, float* __restrict__ q_descale,
                            int q_len, int h_k, int h_r, int head_dim) {
+  // a programmatic dependent: no global load or store before the grid
+  // ahead of this one has completed; the next kernel may launch now
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int bg = blockIdx.x;  // b * h_k + g
   const int b = bg / h_k, g = bg % h_k;
   const int nthr = blockDim.x;
@@ -144,9 +148,9 @@ cudaError_t launch_quantize_pack_q(const void* q_vllm, void* q_packed, float* q_
   const int64_t vecs = static_cast<int64_t>(q_len) * h_r * (head_dim / 16);
   int threads = 64;
   while (threads < kMaxThreads && threads < vecs) threads *= 2;
-  quantize_pack_q_kernel<<<static_cast<unsigned>(groups), threads, 0, stream>>>(
-      static_cast<const uint4*>(q_vllm), static_cast<uint4*>(q_packed), q_descale, q_len, h_k, h_r, head_dim);
-  return cudaGetLastError();
+  return launch_pdl(quantize_pack_q_kernel, dim3(static_cast<unsigned>(groups), 1, 1), dim3(threads, 1, 1), 0, stream,
+                    static_cast<const uint4*>(q_vllm), static_cast<uint4*>(q_packed), q_descale, q_len, h_k, h_r,
+                    head_dim);
 }
 
 }  // namespace mj
