@@ -100,8 +100,10 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
   constexpr int kR = kRows / kDup;   // packed rows per q tile; also keys per copy
   constexpr int kCh = kR < 64 ? kR : 64;  // S columns per TMEM round trip
-  // the merge (a programmatic dependent) may launch now: its CTAs wait
-  // for this grid's completion before reading what it writes
+  // Launched as a programmatic dependent: no global load or store before
+  // the grid ahead of this one has completed.  The merge (this grid's own
+  // dependent) may launch now; its CTAs wait the same way.
+  ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   using C = QmCfg<kQe4m3>;
   constexpr int SK = C::kStagesK, SV = C::kStagesV;
@@ -699,8 +701,7 @@ cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
-  kern<<<grid, kThreads, C::kBytes, stream>>>(a, mk, mv, n_q_tiles);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads, 1, 1), C::kBytes, stream, a, mk, mv, n_q_tiles);
 }
 
 }  // namespace
