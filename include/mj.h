@@ -141,8 +141,10 @@ typedef enum { MJ_KV_E4M3 = 0, MJ_KV_E3M2 = 1, MJ_KV_E2M3 = 2, MJ_KV_E2M1 = 3, M
  *                          and 128 keys on N: one read of the KV per q tile
  *                          of 128 packed rows, or of 64 / 32 packed rows
  *                          each held two / four times with every copy taking
- *                          that share of the keys; MJ_KERNEL_AUTO takes it
- *                          for q_len*h_r > 16 */
+ *                          that share of the keys; above 128 rows one CTA
+ *                          takes two q tiles, so the KV is read once per
+ *                          256 rows; MJ_KERNEL_AUTO takes it for
+ *                          q_len*h_r > 16 */
 typedef enum {
   MJ_KERNEL_AUTO = 0,
   MJ_KERNEL_CUDA_CORE = 1,

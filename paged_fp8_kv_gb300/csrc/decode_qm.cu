@@ -26,6 +26,11 @@
 // tcgen05.mma only every 70-100 cycles); warps 2-5 and 6-9 are two softmax
 // warpgroups taking alternate tiles, thread = query row, each group with its
 // own S and O (128 TMEM columns each), merged per row at the end.
+//
+// Paired q tiles (more than 128 packed rows): one CTA takes two q tiles of
+// the same kv head, warpgroup w the 128 rows of q tile w, and each KV tile
+// goes to both warpgroups (a GEMM1 and a GEMM2 per group), so the KV is read
+// once for 256 rows; each group writes its own rows at the end.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -55,21 +60,24 @@ constexpr int kMma2Warp = 2 + 4 * kWG;       // 10
 constexpr int kVLoadWarp = kMma2Warp + 1;    // 11
 constexpr int kBarAll = 3;                   // named barrier of both warpgroups
 
-template <bool kQe4m3>
+template <bool kQe4m3, bool kPair = false>
 struct QmCfg {
   // K ring: measured the bound at three stages (a stage comes back one TMA
   // round trip after its GEMM1, and the period was that over three); the
   // shared memory left beside Q and the P buffers takes one more (two with
   // e4m3 Q, which has no lo part)
-  static constexpr int kStagesK = kQe4m3 ? 5 : 4;
-  static constexpr int kStagesV = 4;
+  // Paired q tiles hold two Q tiles: three K and three V stages beside a
+  // bf16 pair's 64 KB of Q parts (a stage then serves twice the work).
+  static constexpr int kStagesK = kPair ? (kQe4m3 ? 4 : 3) : (kQe4m3 ? 5 : 4);
+  static constexpr int kStagesV = kPair ? (kQe4m3 ? 4 : 3) : 4;
   static constexpr int kQParts = kQe4m3 ? 1 : 2;
+  static constexpr int kQTiles = kPair ? 2 : 1;
   static constexpr int kTmemCols = 512;  // per warpgroup: S (128), O (128)
   static constexpr int kWgCols = 256;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kStagesK * kTileBytes;
-  static constexpr int kOffQ = (kStagesK + kStagesV) * kTileBytes;  // [hi | lo] 128 x 128 B each
-  static constexpr int kOffP = kOffQ + kQParts * kPartBytes;        // [wg][hi | lo]
+  static constexpr int kOffQ = (kStagesK + kStagesV) * kTileBytes;  // [q tile][hi | lo] 128 x 128 B each
+  static constexpr int kOffP = kOffQ + kQTiles * kQParts * kPartBytes;  // [wg][hi | lo]
   static constexpr int kOffStat = kOffP + kWG * 2 * kPartBytes;     // group 1: [128] max, [128] sum
   static constexpr int kOffBar = kOffStat + 2 * kRows * 4;
   static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 4 * kWG + 2;
@@ -94,10 +102,11 @@ __device__ __forceinline__ uint8_t* swz(uint8_t* part, int r, int cc) {
 // keys [s kR, (s + 1) kR) of every tile, the rest of its P row stays zero,
 // so every softmax warp has work and each covers 1 / kDup of the keys.  The
 // copies' partial states are combined at the end.
-template <bool kQe4m3, int kDup>
+template <bool kQe4m3, int kDup, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, int n_q_tiles) {
+  static_assert(!kPair || kDup == 1, "paired q tiles: one copy of each row");
   constexpr int kR = kRows / kDup;   // packed rows per q tile; also keys per copy
   constexpr int kCh = kR < 64 ? kR : 64;  // S columns per TMEM round trip
   // Launched as a programmatic dependent: no global load or store before
@@ -105,7 +114,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   // dependent) may launch now; its CTAs wait the same way.
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
-  using C = QmCfg<kQe4m3>;
+  using C = QmCfg<kQe4m3, kPair>;
   constexpr int SK = C::kStagesK, SV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -114,8 +123,8 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   float* stat_l = stat_m + kRows;                               // group 1's row sum
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffMisc + 4);
-  int* q_shift = reinterpret_cast<int*>(sm + C::kOffMisc + 8);
-  float* amax_red = reinterpret_cast<float*>(sm + C::kOffMisc + 16);  // [4]
+  int* q_shift = reinterpret_cast<int*>(sm + C::kOffMisc + 8);        // [q tile]
+  float* amax_red = reinterpret_cast<float*>(sm + C::kOffMisc + 16);  // [q tile][4]
 
   // mbarriers: K ring (full, empty), V ring (full, empty), per warpgroup S
   // full, S free, P full, P free; Q ready; MMA drain
@@ -137,7 +146,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   const int rest = blockIdx.x / a.h_k;
   const int qt = rest % n_q_tiles;
   const int w_idx = rest / n_q_tiles;
-  const int n0 = qt * kR;
+  const int n0 = qt * kR * C::kQTiles;  // the CTA's first packed row
 
   const int4 item = reinterpret_cast<const int4*>(a.work)[w_idx];
   const int b = item.x, t_begin = item.y, t_end = item.z, slot = item.w;
@@ -161,7 +170,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::mbar_init(wgbar(wg, 2), 4);
       ptx::mbar_init(wgbar(wg, 3), 1);
     }
-    ptx::mbar_init(qready, 1);
+    ptx::mbar_init(qready, C::kQTiles);  // each q tile's group
     ptx::mbar_init(drain, 2);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -248,8 +257,10 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     }
   } else if (warp == 1 || warp == kMma2Warp) {
     // ----------------------------------------------------------------- MMA
-    // Tile i goes to warpgroup i & 1 as its local tile t = i >> 1: GEMM1
-    // (warp 1) into that group's S, GEMM2 (warp 10) into its O.
+    // Unit u is (tile i, group u & 1) with the group's local tile t = u >> 1:
+    // tile i = u alternates between the groups, or (paired q tiles) tile
+    // i = u >> 1 goes to both, whose stage is then freed after group 1's
+    // MMA.  GEMM1 (warp 1) into that group's S, GEMM2 (warp 10) into its O.
     if (lane == 0) {
       const bool gemm1 = warp == 1;
       bool ok = ptx::mbar_wait_bounded(qready, 0, abort_flag, kWaitNs);
@@ -262,8 +273,10 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const uint64_t pdesc0 = ptx::smem_desc(sbase + C::kOffP, 16, 1024, ptx::kSwizzle128B);
       const uint64_t vdesc0 = ptx::smem_desc(sbase + C::kOffV, 0, 1024, ptx::kSwizzle128B);
       constexpr uint64_t kPartStep = kPartBytes >> 4;  // descriptor step to the next operand part
-      for (int i = 0; ok && i < T; ++i) {
-        const int wg = i & 1, t = i >> 1;
+      for (int u = 0; ok && u < T * C::kQTiles; ++u) {
+        const int i = kPair ? u >> 1 : u;
+        const int wg = u & 1, t = u >> 1;
+        const bool last_use = !kPair || wg == 1;  // the tile's stage is freed after this unit
         const uint32_t tm = tmem + wg * C::kWgCols;
         if (gemm1) {
           const int st = i % SK;
@@ -274,15 +287,16 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           }
           ptx::tc_fence_after();
           const uint64_t kdesc = kdesc0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+          const uint64_t qd = qdesc + (kPair ? static_cast<uint64_t>(wg) * C::kQParts * kPartStep : 0);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // one K step = 32 bytes of d
 #pragma unroll
             for (int part = 0; part < C::kQParts; ++part)
-              ptx::mma_e4m3(tm, qdesc + part * kPartStep + 2 * kk, kdesc + 2 * kk, idesc_s,
+              ptx::mma_e4m3(tm, qd + part * kPartStep + 2 * kk, kdesc + 2 * kk, idesc_s,
                             (kk > 0 || part > 0) ? 1u : 0u);
           }
           ptx::mma_commit(wgbar(wg, 0));
-          ptx::mma_commit(kempty(st));
+          if (last_use) ptx::mma_commit(kempty(st));
         } else {
           const int st = i % SV;
           if (!ptx::mbar_wait_bounded(wgbar(wg, 2), t & 1, abort_flag, kWaitNs) ||
@@ -301,7 +315,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                             (t > 0 || kk > 0 || part > 0) ? 1u : 0u);
           }
           ptx::mma_commit(wgbar(wg, 3));
-          ptx::mma_commit(vempty(st));
+          if (last_use) ptx::mma_commit(vempty(st));
         }
       }
       if (!ok) set_abort(abort_flag, a.status);
@@ -325,15 +339,19 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t tmem_s = tmem + wg * C::kWgCols + lane_off;
     const uint32_t tmem_o = tmem_s + kRows;
     uint8_t* const pbuf = sm + C::kOffP + wg * 2 * kPartBytes;
-    const int qrow = n0 + r % kR;
+    const int qrow = n0 + (kPair ? wg * kRows : 0) + r % kR;  // paired: group w owns q tile w
     const int cb = (r / kR) * kR;  // first key of this row's copy (uniform over a warp)
     const bool live = qrow < a.n_q;
     const float qd = a.qd[b * a.qd_seq + g * a.qd_head];
     const float kd = a.kd[b * a.kd_seq + g * a.kd_head];
     const float vd = a.vd[b * a.vd_seq + g * a.vd_head];
 
-    // ---- Q row r -> two (bf16) or one (e4m3) K-major operand rows (group 0)
-    if (wg == 0) {
+    // ---- Q row r -> two (bf16) or one (e4m3) K-major operand rows (group 0;
+    // paired q tiles: each group its own tile, with its own scaling)
+    uint8_t* const qbase = sm + C::kOffQ + (kPair ? wg * C::kQParts * kPartBytes : 0);
+    int* const q_shift_g = q_shift + (kPair ? wg : 0);
+    float* const amax_g = amax_red + (kPair ? 4 * wg : 0);
+    if (kPair || wg == 0) {
       uint4 raw[kQe4m3 ? 8 : 16];
       const int64_t off = b * a.q_seq + (static_cast<int64_t>(g) * a.n_q + (live ? qrow : 0)) * kHeadDimDev;
       if (kQe4m3) {
@@ -341,8 +359,8 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) raw[cc] = live ? src[cc] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(swz(sm + C::kOffQ, r, cc)) = raw[cc];
-        if (st_tid == 0) *q_shift = 0;
+        for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(swz(qbase, r, cc)) = raw[cc];
+        if (st_tid == 0) *q_shift_g = 0;
       } else {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + off);
 #pragma unroll
@@ -357,9 +375,9 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         float amax = __uint_as_float(mbits << 16);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (lane == 0) amax_red[warp - 2] = amax;
+        if (lane == 0) amax_g[(warp - 2) & 3] = amax;
         ptx::named_bar_sync(bar_wg, 128);
-        amax = fmaxf(fmaxf(amax_red[0], amax_red[1]), fmaxf(amax_red[2], amax_red[3]));
+        amax = fmaxf(fmaxf(amax_g[0], amax_g[1]), fmaxf(amax_g[2], amax_g[3]));
         int shift = 0;
         if (amax > 0.f) {
           const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
@@ -387,17 +405,17 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
             hw[wi] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
             lw[wi] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
           }
-          *reinterpret_cast<uint4*>(swz(sm + C::kOffQ, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(swz(sm + C::kOffQ + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *reinterpret_cast<uint4*>(swz(qbase, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(swz(qbase + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-        if (st_tid == 0) *q_shift = shift;
+        if (st_tid == 0) *q_shift_g = shift;
       }
       ptx::fence_proxy_async_smem();
       ptx::named_bar_sync(bar_wg, 128);
       if (st_tid == 0) ptx::mbar_arrive(qready);
     }
     ptx::named_bar_sync(kBarAll, 128 * kWG);  // the Q shift is set
-    const int shift = *q_shift;
+    const int shift = *q_shift_g;
     // raw (computed) score -> logit and -> log2 units; 2^-shift undoes the Q scaling
     const float scale_l = a.softmax_scale * qd * kd * ldexpf(1.f, -shift);
     const float c2 = scale_l * kLog2e;
@@ -414,8 +432,9 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     // A warp whose 32 rows are all past n_q computes nothing: its P rows
     // keep whatever they hold, which reaches only its own (unused) O rows.
     const bool warp_live = __any_sync(0xffffffffu, live);
-    for (int i = wg; i < T; i += kWG) {
-      const int t = i >> 1;
+    // alternate tiles, or (paired q tiles) every tile
+    for (int i = kPair ? 0 : wg; i < T; i += kPair ? 1 : kWG) {
+      const int t = kPair ? i : i >> 1;
       const int key0 = key_begin + i * kRows;
       t_last = t;
       if (!ptx::mbar_wait_bounded(wgbar(wg, 0), t & 1, abort_flag, kWaitNs)) ok = false;
@@ -547,8 +566,9 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
       }
       // keys past the sequence end: zero their V rows (0 * poison must not
-      // reach O; the TMA landed whole pages).  Thread r owns key row r.
-      if (key0 + kRows > L) {
+      // reach O; the TMA landed whole pages).  Thread r owns key row r (of
+      // group 0 when both groups take the tile: its GEMM2 is issued first).
+      if ((!kPair || wg == 0) && key0 + kRows > L) {
         const int st = i % SV;
         if (!ptx::mbar_wait_bounded(vfull(st), (i / SV) & 1, abort_flag, kWaitNs)) ok = false;
         if (key0 + r >= L) {
@@ -566,17 +586,18 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 
     // ---- epilogue: this group's O is final once its last GEMM2 is done;
     // group 0 merges both groups' rows (row r's state of group 1 through
-    // shared memory, its O from group 1's TMEM columns, same lanes)
+    // shared memory, its O from group 1's TMEM columns, same lanes).  With
+    // paired q tiles each group writes its own rows (its state alone).
     if (t_last >= 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), t_last & 1, abort_flag, kWaitNs)) ok = false;
     if (!ok) set_abort(abort_flag, a.status);
-    if (wg == 1) {
+    if (!kPair && wg == 1) {
       stat_m[r] = m_run;
       stat_l[r] = l_run;
     }
     const bool fine = !ptx::named_bar_red_or(kBarAll, 128 * kWG, *abort_flag != 0);
-    if (wg == 0 && fine) {
+    if ((kPair || wg == 0) && fine) {
       ptx::tc_fence_after();
-      const float m1 = stat_m[r], l1 = stat_l[r];
+      const float m1 = kPair ? -INFINITY : stat_m[r], l1 = kPair ? 0.f : stat_l[r];
       const float mx = fmaxf(m_run, m1);
       const float f0 = (m_run == -INFINITY) ? 0.f : fast_exp2((m_run - mx) * c2);
       const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - mx) * c2);
@@ -617,7 +638,12 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       for (int c0 = 0; c0 < kRows; c0 += 16) {
         uint32_t ra[16], rb[16];
         MJ_TMEM_LD16(tmem_o + c0, ra);
-        MJ_TMEM_LD16(o1 + c0, rb);
+        if constexpr (kPair) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) rb[e] = 0u;  // no second group's state (f1 = 0)
+        } else {
+          MJ_TMEM_LD16(o1 + c0, rb);
+        }
         ptx::tmem_ld_wait();
         float v[16];
         // select, not multiply: a group or copy with no key left its O stale
@@ -687,9 +713,9 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   if (warp == 1) ptx::tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <bool kQe4m3, int kDup>
+template <bool kQe4m3, int kDup, bool kPair = false>
 cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
-  using C = QmCfg<kQe4m3>;
+  using C = QmCfg<kQe4m3, kPair>;
   const int box_rows = a.page_size < kRows ? a.page_size : kRows;
   CUtensorMap mk, mv;
   if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, box_rows, 1,
@@ -697,7 +723,7 @@ cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
       !make_kv_map(&mv, a.v, a.page_size, a.h_k, a.num_pages, a.v_row, a.v_head, a.v_page, box_rows, 1,
                    a.kv_format))
     return cudaErrorInvalidValue;
-  auto kern = decode_qm_kernel<kQe4m3, kDup>;
+  auto kern = decode_qm_kernel<kQe4m3, kDup, kPair>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.num_work) * n_q_tiles * a.h_k, 1, 1);
@@ -709,6 +735,8 @@ cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
 cudaError_t launch_decode_qm(const DecodeDev& a, int rows_per_cta, int n_q_tiles, bool q_e4m3,
                              cudaStream_t stream) {
   switch (rows_per_cta) {
+    case 256:  // two q tiles of 128 rows per CTA
+      return q_e4m3 ? launch_qm<true, 1, true>(a, n_q_tiles, stream) : launch_qm<false, 1, true>(a, n_q_tiles, stream);
     case 128: return q_e4m3 ? launch_qm<true, 1>(a, n_q_tiles, stream) : launch_qm<false, 1>(a, n_q_tiles, stream);
     case 64: return q_e4m3 ? launch_qm<true, 2>(a, n_q_tiles, stream) : launch_qm<false, 2>(a, n_q_tiles, stream);
     case 32: return q_e4m3 ? launch_qm<true, 4>(a, n_q_tiles, stream) : launch_qm<false, 4>(a, n_q_tiles, stream);

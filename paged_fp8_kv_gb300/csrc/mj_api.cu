@@ -130,12 +130,13 @@ KernelChoice choose_kernel(const mj_decode_params& p) {
              (p.kernel == MJ_KERNEL_AUTO && n_q > kQRowsFrom && p.kv_format != MJ_KV_NVFP4)) {
     k.kind = KernelKind::kTensorCoreQRows;
     // up to 32 or 64 packed rows: each row held four or two times in the
-    // 128 MMA rows, every copy taking that share of a tile's keys
-    k.rows_per_cta = n_q <= 32 ? 32 : (n_q <= 64 ? 64 : 128);
+    // 128 MMA rows, every copy taking that share of a tile's keys; more
+    // than 128: two q tiles per CTA sharing each KV tile
+    k.rows_per_cta = n_q <= 32 ? 32 : (n_q <= 64 ? 64 : (n_q <= 128 ? 128 : 256));
     smem = qm_smem_bytes(e4m3);
-    static const char* names[2][3] = {{"qm_r32_bf16", "qm_r64_bf16", "qm_bf16"},
-                                      {"qm_r32_e4m3", "qm_r64_e4m3", "qm_e4m3"}};
-    k.name = names[e4m3][k.rows_per_cta == 32 ? 0 : (k.rows_per_cta == 64 ? 1 : 2)];
+    static const char* names[2][4] = {{"qm_r32_bf16", "qm_r64_bf16", "qm_bf16", "qm_pair_bf16"},
+                                      {"qm_r32_e4m3", "qm_r64_e4m3", "qm_e4m3", "qm_pair_e4m3"}};
+    k.name = names[e4m3][k.rows_per_cta == 32 ? 0 : (k.rows_per_cta == 64 ? 1 : (k.rows_per_cta == 128 ? 2 : 3))];
   } else if (p.kernel == MJ_KERNEL_TENSOR_CORE_GROUPED && tcg_supported(p.h_k, n_q, &g, &rh)) {
     k.kind = KernelKind::kTensorCoreGrouped;
     k.rows_per_cta = rh;

@@ -207,8 +207,10 @@ extern "C" mj_status mj_decode_plan(const mj_decode_params* params, mj_plan_opts
     int64_t sum_tiles = 0;
     for (int64_t t : tiles) sum_tiles += t;
     const double stream_us = static_cast<double>(sum_tiles) * units_per_item * kTilePairBytes / kPlanBandwidth;
-    const double tile_us = kc.kind == KernelKind::kTensorCoreQRows ? kPlanQRowsTileUs
-                                                                    : kPlanSmTileUs * kc.ctas_per_sm;
+    // (a CTA of paired q tiles does twice the work per tile)
+    const double tile_us = kc.kind == KernelKind::kTensorCoreQRows
+                               ? kPlanQRowsTileUs * (kc.rows_per_cta > 128 ? 2 : 1)
+                               : kPlanSmTileUs * kc.ctas_per_sm;
     double best = 0;
     int64_t best_cps = kc.ctas_per_sm, prev_cps = 0;
     for (int thirds : kPlanThirds) {

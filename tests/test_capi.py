@@ -310,8 +310,12 @@ def test_query_rows_kernel_choice():
     qr = mj.MJ_KERNEL_TENSOR_CORE_QROWS
     assert mj.kernel_name(_params(2, h_k=1, h_r=16, kernel=qr, q_dtype=1)) == "qm_r32_e4m3"
     assert mj.kernel_name(_params(2, h_k=1, q_len=8, h_r=16, kernel=qr, q_dtype=1)) == "qm_e4m3"
+    # more than 128 rows: two q tiles of 128 rows per CTA
+    assert mj.kernel_name(_params(2, h_k=1, q_len=16, h_r=16)) == "qm_pair_bf16"
+    assert mj.kernel_name(_params(2, h_k=1, q_len=3, h_r=48)) == "qm_pair_bf16"
+    assert mj.kernel_name(_params(2, h_k=1, q_len=16, h_r=32, kernel=qr, q_dtype=1)) == "qm_pair_e4m3"
     plan = mj.decode_plan(_params(4, h_k=1, q_len=16, h_r=32), [1000, 2000, 3000, 4000])
-    assert plan.opts.n_q_tiles == 4
+    assert plan.opts.n_q_tiles == 2  # 512 rows: two CTAs of two q tiles
 
 
 def test_default_plan_splits_when_long_sequences_dominate():

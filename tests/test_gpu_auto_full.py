@@ -41,6 +41,8 @@ CASES = [
     (5, {"h_r": 16, "q_len": 2}, "qm_r32_bf16"),
     (5, {"h_r": 16, "q_len": 4}, "qm_r64_bf16"),
     (5, {"h_r": 32, "q_len": 4}, "qm_bf16"),
+    (5, {"h_r": 16, "q_len": 16}, "qm_pair_bf16"),
+    (5, {"h_r": 32, "q_len": 16}, "qm_pair_bf16"),
 ]
 
 

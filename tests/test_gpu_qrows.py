@@ -80,6 +80,23 @@ def test_page_sizes_and_q_dtype(page_size, q_is_e4m3):
     check(w, force_splits=2)
 
 
+@pytest.mark.parametrize("q_len,h_r", [(3, 48), (16, 16), (5, 64)], ids=["rows144", "rows256", "rows320"])
+@pytest.mark.parametrize("page_size", [16, 128])
+@pytest.mark.parametrize("q_is_e4m3", [False, True])
+def test_paired_q_tiles(q_len, h_r, page_size, q_is_e4m3):
+    """More than 128 packed rows: two q tiles per CTA, each KV tile taken by
+    both softmax groups.  144 rows leave the second group's tile mostly
+    empty; 320 rows make a second CTA whose second group has no live row."""
+    lens = [1, 100, 127, 128, 129, 300, 1000, 2500]
+    causal = q_len != 5
+    w = syn.make_workload("pair", lens, q_len, 2, h_r, page_size, seed=71 + q_len * h_r + page_size,
+                          q_is_e4m3=q_is_e4m3, causal=causal, max_splits=4)
+    s, _ = check(w, force_splits=2)
+    assert s.kernel == ("qm_pair_e4m3" if q_is_e4m3 else "qm_pair_bf16")
+    assert s.plan.opts.n_q_tiles == (q_len * h_r + 255) // 256
+    check(w)  # unsplit
+
+
 @pytest.mark.parametrize("q_len,causal", [(1, True), (4, True), (3, False)])
 def test_empty_short_and_aligned_lengths(q_len, causal):
     lens = [0, 1, 2, 3, 16, 127, 128, 129, 256, 300]
