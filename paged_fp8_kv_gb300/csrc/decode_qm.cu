@@ -564,6 +564,11 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
+        // and, like a live warp, it arrives on P full only after GEMM2 of the
+        // group's previous tile: a group with no live row (the second q tile
+        // past n_q) would otherwise complete P full a second phase before the
+        // GEMM2 thread's wait on the first
+        if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
       }
       // keys past the sequence end: zero their V rows (0 * poison must not
       // reach O; the TMA landed whole pages).  Thread r owns key row r (of
