@@ -98,10 +98,11 @@ __device__ __forceinline__ uint8_t* swz(uint8_t* part, int r, int cc) {
 }
 
 // kDup > 1: a q tile has kR = 128 / kDup packed rows, each held kDup times
-// in the MMA's M rows (row r is packed row r % kR); copy s of a row takes
-// keys [s kR, (s + 1) kR) of every tile, the rest of its P row stays zero,
-// so every softmax warp has work and each covers 1 / kDup of the keys.  The
-// copies' partial states are combined at the end.
+// in GEMM1's M rows (row r is packed row r % kR); copy s of a row takes keys
+// [s kR, (s + 1) kR) of every tile, so every softmax warp has work and each
+// covers 1 / kDup of the keys.  The copies of a row share its reference
+// maximum, write their key slices into one P row per packed row, and GEMM2
+// runs as O^T = V^T P^T with the kR packed rows on N.
 template <bool kQe4m3, int kDup, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
@@ -174,12 +175,6 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     ptx::mbar_init(drain, 2);
     *abort_flag = 0;
     ptx::fence_mbar_init();
-  }
-  if (kDup > 1 && warp >= 2 && warp < kMma2Warp) {
-    // a copy's P row outside its key slice stays zero for the whole kernel
-    uint4* p = reinterpret_cast<uint4*>(sm + C::kOffP);
-    for (int id = tid - 64; id < kWG * 2 * kPartBytes / 16; id += 128 * kWG) p[id] = make_uint4(0u, 0u, 0u, 0u);
-    ptx::fence_proxy_async_smem();
   }
   if (warp == 1) {
     ptx::tmem_alloc(sbase + C::kOffMisc, C::kTmemCols);
@@ -268,6 +263,10 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const uint32_t kv_fmt = kv_mma_format(a.kv_format);
       const uint32_t idesc_s = ptx::idesc_f8f6f4(kRows, kRows, false, false, 0, kv_fmt);  // S = Q K^T
       const uint32_t idesc_o = ptx::idesc_f8f6f4(kRows, kRows, false, true, 0, kv_fmt);   // O = P V, V MN-major
+      // row copies: O^T = V^T P^T, M = d, N = the packed rows; A = the V tile
+      // (MN-major), B = the group's P rows (K-major)
+      const uint32_t idesc_ot = ptx::idesc_f8f6f4(kRows, kR, true, false, kv_fmt, 0);
+      constexpr uint64_t kPtStep = (kR * 128) >> 4;  // descriptor step between the P rows' parts
       const uint64_t qdesc = ptx::smem_desc(sbase + C::kOffQ, 16, 1024, ptx::kSwizzle128B);
       const uint64_t kdesc0 = ptx::smem_desc(sbase + C::kOffK, 16, 1024, ptx::kSwizzle128B);
       const uint64_t pdesc0 = ptx::smem_desc(sbase + C::kOffP, 16, 1024, ptx::kSwizzle128B);
@@ -310,9 +309,14 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // one K step = 32 keys
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
-              ptx::mma_e4m3(tm + kRows, pdesc + part * kPartStep + 2 * kk, vdesc + 256 * kk, idesc_o,
-                            (t > 0 || kk > 0 || part > 0) ? 1u : 0u);
+            for (int part = 0; part < 2; ++part) {
+              if constexpr (kDup > 1)
+                ptx::mma_e4m3(tm + kRows, vdesc + 256 * kk, pdesc + part * kPtStep + 2 * kk, idesc_ot,
+                              (t > 0 || kk > 0 || part > 0) ? 1u : 0u);
+              else
+                ptx::mma_e4m3(tm + kRows, pdesc + part * kPartStep + 2 * kk, vdesc + 256 * kk, idesc_o,
+                              (t > 0 || kk > 0 || part > 0) ? 1u : 0u);
+            }
           }
           ptx::mma_commit(wgbar(wg, 3));
           if (last_use) ptx::mma_commit(vempty(st));
@@ -432,101 +436,308 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
     // A warp whose 32 rows are all past n_q computes nothing: its P rows
     // keep whatever they hold, which reaches only its own (unused) O rows.
     const bool warp_live = __any_sync(0xffffffffu, live);
-    // alternate tiles, or (paired q tiles) every tile
-    for (int i = kPair ? 0 : wg; i < T; i += kPair ? 1 : kWG) {
-      const int t = kPair ? i : i >> 1;
-      const int key0 = key_begin + i * kRows;
-      t_last = t;
-      if (!ptx::mbar_wait_bounded(wgbar(wg, 0), t & 1, abort_flag, kWaitNs)) ok = false;
-      ptx::tc_fence_after();
-      if (warp_live) {
-        // pass 1: the row's masked maximum over the tile (select: garbage or
-        // poison keys never leak); a tile wholly below every row's limit of
-        // its warp skips the selects.  64 columns per TMEM round trip.
-        // (rows past n_q produce nothing: any value will do for them)
-        const bool unmasked = __all_sync(0xffffffffu, !live || key0 + cb + kR - 1 <= lim);
-        float mt = -INFINITY;
-        // kDup > 1: the row's slice of S (kR <= 64 columns) stays in these
-        // registers for pass 2, and S goes back to GEMM1 right after this read
-        uint32_t sv[kDup > 1 ? kR : 1];
-  #pragma unroll
-        for (int h0 = 0; h0 < kR; h0 += kCh) {
-          uint32_t rl[kDup > 1 ? 1 : kCh];
-          uint32_t* rr = kDup > 1 ? sv : rl;
-  #pragma unroll
-          for (int c0 = 0; c0 < kCh; c0 += 16) MJ_TMEM_LD16(tmem_s + cb + h0 + c0, (rr + c0));
-          ptx::tmem_ld_wait();
-          if (kDup > 1) {
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
+    if constexpr (kDup == 1) {
+      // alternate tiles, or (paired q tiles) every tile
+      for (int i = kPair ? 0 : wg; i < T; i += kPair ? 1 : kWG) {
+        const int t = kPair ? i : i >> 1;
+        const int key0 = key_begin + i * kRows;
+        t_last = t;
+        if (!ptx::mbar_wait_bounded(wgbar(wg, 0), t & 1, abort_flag, kWaitNs)) ok = false;
+        ptx::tc_fence_after();
+        if (warp_live) {
+          // pass 1: the row's masked maximum over the tile (select: garbage or
+          // poison keys never leak); a tile wholly below every row's limit of
+          // its warp skips the selects.  64 columns per TMEM round trip.
+          // (rows past n_q produce nothing: any value will do for them)
+          const bool unmasked = __all_sync(0xffffffffu, !live || key0 + kRows - 1 <= lim);
+          float mt = -INFINITY;
+    #pragma unroll
+          for (int h0 = 0; h0 < kRows; h0 += kCh) {
+            uint32_t rr[kCh];
+    #pragma unroll
+            for (int c0 = 0; c0 < kCh; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
+            ptx::tmem_ld_wait();
+            if (unmasked) {
+    #pragma unroll
+              for (int e = 0; e < kCh; e += 2) mt = fmax3(mt, __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
+            } else {
+    #pragma unroll
+              for (int e = 0; e < kCh; e += 2)
+                mt = fmax3(mt, (key0 + h0 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY,
+                           (key0 + h0 + e + 1 <= lim) ? __uint_as_float(rr[e + 1]) : -INFINITY);
+            }
           }
-          if (unmasked) {
-  #pragma unroll
-            for (int e = 0; e < kCh; e += 2) mt = fmax3(mt, __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]));
-          } else {
-  #pragma unroll
-            for (int e = 0; e < kCh; e += 2)
-              mt = fmax3(mt, (key0 + cb + h0 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY,
-                         (key0 + cb + h0 + e + 1 <= lim) ? __uint_as_float(rr[e + 1]) : -INFINITY);
+          if (!live) mt = -INFINITY;  // keeps the maximum of an empty row at -inf
+          const bool moved = mt > m_run + head_c;
+          const float m_new = moved ? mt : m_run;
+          const float mu = (m_new == -INFINITY) ? 0.f : m_new;  // the -inf guard
+          const float corr = moved ? fast_exp2((m_run - mu) * c2) : 1.f;  // 0 for a fresh row
+          l_run *= corr;
+          m_run = m_new;
+          // this group's P buffer and O are free once GEMM2 of its previous tile ran
+          if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+          // lazy O correction: each row rescales its own TMEM lane, but TMEM
+          // access is warp-wide, so a warp corrects when any of its rows moved
+          if (t > 0 && __any_sync(0xffffffffu, moved)) {
+            ptx::tc_fence_after();
+            constexpr int kOc = 64;
+    #pragma unroll
+            for (int h0 = 0; h0 < kRows; h0 += kOc) {
+              uint32_t rr[kOc];
+    #pragma unroll
+              for (int c0 = 0; c0 < kOc; c0 += 16) MJ_TMEM_LD16(tmem_o + h0 + c0, (rr + c0));
+              ptx::tmem_ld_wait();
+    #pragma unroll
+              for (int e = 0; e < kOc; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
+    #pragma unroll
+              for (int c0 = 0; c0 < kOc; c0 += 16) MJ_TMEM_ST16(tmem_o + h0 + c0, (rr + c0));
+            }
+            ptx::tmem_st_wait();
+          }
+          // pass 2: x = 448 p 2^-kTau = 2^((s - m) c + log2 448 - kTau) in
+          // fp32 (ex2.approx.f32; x <= 448), the row sum of the unrounded x in
+          // fp32, and the MMA operand split x = hi + lo through half precision
+          // (x rounded to 11 significant bits, hi = e4m3(x), lo = e4m3(x - hi),
+          // the difference exact in halves): about 8 significant bits of x in P.
+          // (On GB300 the fp32 exponential issues at the same result rate as the
+          // packed-half one, so nothing is saved by narrowing it.)
+          const float bias = fmaf(-mu, c2, kLog2PScale);
+          const float2 c2x2 = make_float2(c2, c2), bias2 = make_float2(bias, bias);
+    #pragma unroll
+          for (int h0 = 0; h0 < kRows; h0 += kCh) {
+            uint32_t rr[kCh];
+    #pragma unroll
+            for (int c0 = 0; c0 < kCh; c0 += 16) MJ_TMEM_LD16(tmem_s + h0 + c0, (rr + c0));
+            ptx::tmem_ld_wait();
+            if (h0 + kCh == kRows) {
+              // S is read whole: the group's next GEMM1 may overwrite it while
+              // the last half is turned into P
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
+            }
+    #pragma unroll
+            for (int q = 0; q < kCh / 16; ++q) {
+              const int cc = h0 / 16 + q;  // 16-key chunk of the P row
+              uint32_t hw[4], lw[4];
+              float2 sum2 = make_float2(0.f, 0.f);
+    #pragma unroll
+              for (int wi = 0; wi < 4; ++wi) {
+                uint16_t h8[2], l8[2];
+    #pragma unroll
+                for (int pr = 0; pr < 2; ++pr) {
+                  const int e0 = q * 16 + wi * 4 + pr * 2;
+                  float s0 = __uint_as_float(rr[e0]), s1 = __uint_as_float(rr[e0 + 1]);
+                  if (!unmasked) {
+                    const int c = h0 + e0;
+                    s0 = (key0 + c <= lim) ? s0 : -INFINITY;
+                    s1 = (key0 + c + 1 <= lim) ? s1 : -INFINITY;
+                  }
+                  const float2 y = fma2(make_float2(s0, s1), c2x2, bias2);
+                  const float x0 = fast_exp2(y.x);
+                  const float x1 = fast_exp2(y.y);
+                  sum2 = add2(sum2, make_float2(x0, x1));
+                  const uint32_t x2 = f32x2_to_f16x2(x0, x1);
+                  const uint16_t hi8 = f16x2_to_e4m3x2(x2);
+                  const uint32_t hf2 = e4m3x2_to_f16x2(hi8);
+                  l8[pr] = f16x2_to_e4m3x2(sub_f16x2(x2, hf2));
+                  h8[pr] = hi8;
+                }
+                hw[wi] = static_cast<uint32_t>(h8[0]) | (static_cast<uint32_t>(h8[1]) << 16);
+                lw[wi] = static_cast<uint32_t>(l8[0]) | (static_cast<uint32_t>(l8[1]) << 16);
+              }
+              l_run += sum2.x + sum2.y;
+              *reinterpret_cast<uint4*>(swz(pbuf, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(swz(pbuf + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
           }
         }
-        if (!live) mt = -INFINITY;  // keeps the maximum of an empty row at -inf
-        const bool moved = mt > m_run + head_c;
-        const float m_new = moved ? mt : m_run;
+        if (!warp_live) {  // S read (a live warp released it after its last load)
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
+          // and, like a live warp, it arrives on P full only after GEMM2 of the
+          // group's previous tile: a group with no live row (the second q tile
+          // past n_q) would otherwise complete P full a second phase before the
+          // GEMM2 thread's wait on the first
+          if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+        }
+        // keys past the sequence end: zero their V rows (0 * poison must not
+        // reach O; the TMA landed whole pages).  Thread r owns key row r (of
+        // group 0 when both groups take the tile: its GEMM2 is issued first).
+        if ((!kPair || wg == 0) && key0 + kRows > L) {
+          const int st = i % SV;
+          if (!ptx::mbar_wait_bounded(vfull(st), (i / SV) & 1, abort_flag, kWaitNs)) ok = false;
+          if (key0 + r >= L) {
+            uint4* vrow = reinterpret_cast<uint4*>(sm + C::kOffV + st * kTileBytes + r * 128);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(wgbar(wg, 2));
+        if (!ok) set_abort(abort_flag, a.status);
+      }
+
+      // ---- epilogue: this group's O is final once its last GEMM2 is done;
+      // group 0 merges both groups' rows (row r's state of group 1 through
+      // shared memory, its O from group 1's TMEM columns, same lanes).  With
+      // paired q tiles each group writes its own rows (its state alone).
+      if (t_last >= 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), t_last & 1, abort_flag, kWaitNs)) ok = false;
+      if (!ok) set_abort(abort_flag, a.status);
+      if (!kPair && wg == 1) {
+        stat_m[r] = m_run;
+        stat_l[r] = l_run;
+      }
+      const bool fine = !ptx::named_bar_red_or(kBarAll, 128 * kWG, *abort_flag != 0);
+      if ((kPair || wg == 0) && fine) {
+        ptx::tc_fence_after();
+        const float m1 = kPair ? -INFINITY : stat_m[r], l1 = kPair ? 0.f : stat_l[r];
+        const float mx = fmaxf(m_run, m1);
+        const float f0 = (m_run == -INFINITY) ? 0.f : fast_exp2((m_run - mx) * c2);
+        const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - mx) * c2);
+        const float lraw = l_run * f0 + l1 * f1;  // row sum of x, both groups
+        const bool final_out = a.n_splits[b] <= 1;
+        const int64_t orow = final_out ? b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + (live ? qrow : 0)) * kHeadDimDev
+                                       : part_row(a, b, g, slot, live ? qrow : 0) * kHeadDimDev;
+        const uint32_t o1 = tmem + C::kWgCols + kRows + lane_off;  // group 1's O, same lanes
+        const float mrow = mx;
+        const float l = lraw * kPScaleInv;
+        const float f = vd * kPScaleInv * (final_out ? a.scale_o / (l + 1e-30f) : 1.f);
+        const bool writer = live;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kRows; c0 += 16) {
+          uint32_t ra[16], rb[16];
+          MJ_TMEM_LD16(tmem_o + c0, ra);
+          if constexpr (kPair) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) rb[e] = 0u;  // no second group's state (f1 = 0)
+          } else {
+            MJ_TMEM_LD16(o1 + c0, rb);
+          }
+          ptx::tmem_ld_wait();
+          float v[16];
+          // select, not multiply: a group with no key left its O stale
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            v[e] = ((f0 > 0.f ? __uint_as_float(ra[e]) * f0 : 0.f) + (f1 > 0.f ? __uint_as_float(rb[e]) * f1 : 0.f));
+          if (!writer) continue;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= f;
+          if (final_out) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const __nv_bfloat162 v2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+              pk[e] = *reinterpret_cast<const uint32_t*>(&v2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(a.o + orow + c0);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(a.o_part + orow + c0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          }
+        }
+        if (writer) {
+          const float m_logit = mrow * scale_l;
+          if (final_out) {
+            a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(l);
+          } else {
+            const int64_t pr = part_row(a, b, g, slot, qrow);
+            a.m_part[pr] = m_logit;
+            a.l_part[pr] = l;
+          }
+        }
+      }
+    } else {
+      // ---- row copies (32 or 64 packed rows, each held 4 or 2 times): copy
+      // cp of packed row qr holds keys [cp kR, (cp + 1) kR) of every tile.  The
+      // copies of a row share its reference maximum (the tile maxima of their
+      // key slices meet in shared memory), so their P entries are on one
+      // scale and GEMM2 sums them into one row: O^T[d, row] += V^T[d, key]
+      // P^T[key, row] with N = the packed rows, a quarter (half) of the MMA
+      // work of a 128-row O.  The group's O^T sits in TMEM with d on the
+      // lanes, so a correction scales every lane's column of each row.
+      const int cp = r / kR;  // this lane's copy
+      const int qr = r % kR;  // its packed row in the q tile
+      constexpr int kPtPart = kR * 128;  // one e4m3 part of the group's P rows
+      float* const mx_x = reinterpret_cast<float*>(pbuf + 2 * kPtPart);  // [kDup][kR] tile maxima of the slices
+      float* const fx = mx_x + kRows;                                      // [2][kR] per-row factors
+      const int bar_red = 4 + wg;  // the group's reduction barrier
+      for (int i = wg; i < T; i += kWG) {
+        const int t = i >> 1;
+        const int key0 = key_begin + i * kRows;
+        t_last = t;
+        if (!ptx::mbar_wait_bounded(wgbar(wg, 0), t & 1, abort_flag, kWaitNs)) ok = false;
+        ptx::tc_fence_after();
+        // the row's slice of S stays in registers, and S goes back to GEMM1
+        // right after this read
+        uint32_t sv[kR];
+        float mt = -INFINITY;
+        bool unmasked = true;
+        if (warp_live) {
+          unmasked = __all_sync(0xffffffffu, !live || key0 + cb + kR - 1 <= lim);
+  #pragma unroll
+          for (int c0 = 0; c0 < kR; c0 += 16) MJ_TMEM_LD16(tmem_s + cb + c0, (sv + c0));
+          ptx::tmem_ld_wait();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
+        if (warp_live) {
+          if (unmasked) {
+  #pragma unroll
+            for (int e = 0; e < kR; e += 2) mt = fmax3(mt, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+          } else {
+  #pragma unroll
+            for (int e = 0; e < kR; e += 2)
+              mt = fmax3(mt, (key0 + cb + e <= lim) ? __uint_as_float(sv[e]) : -INFINITY,
+                         (key0 + cb + e + 1 <= lim) ? __uint_as_float(sv[e + 1]) : -INFINITY);
+          }
+          if (!live) mt = -INFINITY;  // keeps the maximum of an empty row at -inf
+        }
+        // the row's tile maximum over its copies; every copy then takes the
+        // same decision from the same values
+        mx_x[cp * kR + qr] = mt;
+        ptx::named_bar_sync(bar_wg, 128);
+        float mrow = -INFINITY;
+  #pragma unroll
+        for (int s2 = 0; s2 < kDup; ++s2) mrow = fmaxf(mrow, mx_x[s2 * kR + qr]);
+        const bool moved = mrow > m_run + head_c;
+        const float m_new = moved ? mrow : m_run;
         const float mu = (m_new == -INFINITY) ? 0.f : m_new;  // the -inf guard
         const float corr = moved ? fast_exp2((m_run - mu) * c2) : 1.f;  // 0 for a fresh row
         l_run *= corr;
         m_run = m_new;
-        // this group's P buffer and O are free once GEMM2 of its previous tile ran
+        if (cp == 0) fx[qr] = corr;
+        const bool any_moved = ptx::named_bar_red_or(bar_red, 128, moved);  // also: fx and mx_x reads done
+        // this group's P rows and O^T are free once GEMM2 of its previous tile ran
         if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
-        // lazy O correction: each row rescales its own TMEM lane, but TMEM
-        // access is warp-wide, so a warp corrects when any of its rows moved
-        if (t > 0 && __any_sync(0xffffffffu, moved)) {
+        if (t > 0 && any_moved) {  // lazy correction: lane d scales column qr of every row by its factor
           ptx::tc_fence_after();
-          // (16 columns per round trip when the S slice is held in registers)
-          constexpr int kOc = kDup > 1 ? 16 : 64;
   #pragma unroll
-          for (int h0 = 0; h0 < kRows; h0 += kOc) {
-            uint32_t rr[kOc];
-  #pragma unroll
-            for (int c0 = 0; c0 < kOc; c0 += 16) MJ_TMEM_LD16(tmem_o + h0 + c0, (rr + c0));
+          for (int c0 = 0; c0 < kR; c0 += 16) {
+            uint32_t rr[16];
+            MJ_TMEM_LD16(tmem_o + c0, rr);
             ptx::tmem_ld_wait();
   #pragma unroll
-            for (int e = 0; e < kOc; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * corr);
-  #pragma unroll
-            for (int c0 = 0; c0 < kOc; c0 += 16) MJ_TMEM_ST16(tmem_o + h0 + c0, (rr + c0));
+            for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * fx[c0 + e]);
+            MJ_TMEM_ST16(tmem_o + c0, rr);
           }
           ptx::tmem_st_wait();
         }
-        // pass 2: x = 448 p 2^-kTau = 2^((s - m) c + log2 448 - kTau) in
-        // fp32 (ex2.approx.f32; x <= 448), the row sum of the unrounded x in
-        // fp32, and the MMA operand split x = hi + lo through half precision
-        // (x rounded to 11 significant bits, hi = e4m3(x), lo = e4m3(x - hi),
-        // the difference exact in halves): about 8 significant bits of x in P.
-        // (On GB300 the fp32 exponential issues at the same result rate as the
-        // packed-half one, so nothing is saved by narrowing it.)
-        const float bias = fmaf(-mu, c2, kLog2PScale);
-        const float2 c2x2 = make_float2(c2, c2), bias2 = make_float2(bias, bias);
+        if (warp_live) {
+          // pass 2 on the slice: x, its sum, and the hi / lo split (as for
+          // 128 rows) into row qr, keys [cb, cb + kR), of the group's P rows
+          const float bias = fmaf(-mu, c2, kLog2PScale);
+          const float2 c2x2 = make_float2(c2, c2), bias2 = make_float2(bias, bias);
   #pragma unroll
-        for (int h0 = 0; h0 < kR; h0 += kCh) {
-          uint32_t rl[kDup > 1 ? 1 : kCh];
-          uint32_t* rr = kDup > 1 ? sv : rl;
-          if (kDup == 1) {
-  #pragma unroll
-            for (int c0 = 0; c0 < kCh; c0 += 16) MJ_TMEM_LD16(tmem_s + cb + h0 + c0, (rr + c0));
-            ptx::tmem_ld_wait();
-          }
-          if (kDup == 1 && h0 + kCh == kR) {
-            // S is read whole: the group's next GEMM1 may overwrite it while
-            // the last half is turned into P
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
-          }
-  #pragma unroll
-          for (int q = 0; q < kCh / 16; ++q) {
-            const int cc = (cb + h0) / 16 + q;  // 16-key chunk of the P row
+          for (int q = 0; q < kR / 16; ++q) {
+            const int cc = cb / 16 + q;  // 16-key chunk of the P row
             uint32_t hw[4], lw[4];
             float2 sum2 = make_float2(0.f, 0.f);
   #pragma unroll
@@ -535,11 +746,10 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   #pragma unroll
               for (int pr = 0; pr < 2; ++pr) {
                 const int e0 = q * 16 + wi * 4 + pr * 2;
-                float s0 = __uint_as_float(rr[e0]), s1 = __uint_as_float(rr[e0 + 1]);
+                float s0 = __uint_as_float(sv[e0]), s1 = __uint_as_float(sv[e0 + 1]);
                 if (!unmasked) {
-                  const int c = cb + h0 + e0;
-                  s0 = (key0 + c <= lim) ? s0 : -INFINITY;
-                  s1 = (key0 + c + 1 <= lim) ? s1 : -INFINITY;
+                  s0 = (key0 + cb + e0 <= lim) ? s0 : -INFINITY;
+                  s1 = (key0 + cb + e0 + 1 <= lim) ? s1 : -INFINITY;
                 }
                 const float2 y = fma2(make_float2(s0, s1), c2x2, bias2);
                 const float x0 = fast_exp2(y.x);
@@ -555,158 +765,90 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
               lw[wi] = static_cast<uint32_t>(l8[0]) | (static_cast<uint32_t>(l8[1]) << 16);
             }
             l_run += sum2.x + sum2.y;
-            *reinterpret_cast<uint4*>(swz(pbuf, r, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(swz(pbuf + kPartBytes, r, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            *reinterpret_cast<uint4*>(swz(pbuf, qr, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(swz(pbuf + kPtPart, qr, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
-      }
-      if (!warp_live) {  // S read (a live warp released it after its last load)
+        // keys past the sequence end: zero their V rows (0 * poison must not
+        // reach O; the TMA landed whole pages).  Thread r owns key row r.
+        if (key0 + kRows > L) {
+          const int st = i % SV;
+          if (!ptx::mbar_wait_bounded(vfull(st), (i / SV) & 1, abort_flag, kWaitNs)) ok = false;
+          if (key0 + r >= L) {
+            uint4* vrow = reinterpret_cast<uint4*>(sm + C::kOffV + st * kTileBytes + r * 128);
+  #pragma unroll
+            for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(wgbar(wg, 1));
-        // and, like a live warp, it arrives on P full only after GEMM2 of the
-        // group's previous tile: a group with no live row (the second q tile
-        // past n_q) would otherwise complete P full a second phase before the
-        // GEMM2 thread's wait on the first
-        if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+        if (lane == 0) ptx::mbar_arrive(wgbar(wg, 2));
+        if (!ok) set_abort(abort_flag, a.status);
       }
-      // keys past the sequence end: zero their V rows (0 * poison must not
-      // reach O; the TMA landed whole pages).  Thread r owns key row r (of
-      // group 0 when both groups take the tile: its GEMM2 is issued first).
-      if ((!kPair || wg == 0) && key0 + kRows > L) {
-        const int st = i % SV;
-        if (!ptx::mbar_wait_bounded(vfull(st), (i / SV) & 1, abort_flag, kWaitNs)) ok = false;
-        if (key0 + r >= L) {
-          uint4* vrow = reinterpret_cast<uint4*>(sm + C::kOffV + st * kTileBytes + r * 128);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) vrow[e] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(wgbar(wg, 2));
-      if (!ok) set_abort(abort_flag, a.status);
-    }
 
-    // ---- epilogue: this group's O is final once its last GEMM2 is done;
-    // group 0 merges both groups' rows (row r's state of group 1 through
-    // shared memory, its O from group 1's TMEM columns, same lanes).  With
-    // paired q tiles each group writes its own rows (its state alone).
-    if (t_last >= 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), t_last & 1, abort_flag, kWaitNs)) ok = false;
-    if (!ok) set_abort(abort_flag, a.status);
-    if (!kPair && wg == 1) {
-      stat_m[r] = m_run;
-      stat_l[r] = l_run;
-    }
-    const bool fine = !ptx::named_bar_red_or(kBarAll, 128 * kWG, *abort_flag != 0);
-    if ((kPair || wg == 0) && fine) {
-      ptx::tc_fence_after();
-      const float m1 = kPair ? -INFINITY : stat_m[r], l1 = kPair ? 0.f : stat_l[r];
-      const float mx = fmaxf(m_run, m1);
-      const float f0 = (m_run == -INFINITY) ? 0.f : fast_exp2((m_run - mx) * c2);
-      const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - mx) * c2);
-      const float lraw = l_run * f0 + l1 * f1;  // row sum of x, both groups
-      const bool final_out = a.n_splits[b] <= 1;
-      const int64_t orow = final_out ? b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + (live ? qrow : 0)) * kHeadDimDev
-                                     : part_row(a, b, g, slot, live ? qrow : 0) * kHeadDimDev;
-      const uint32_t o1 = tmem + C::kWgCols + kRows + lane_off;  // group 1's O, same lanes
-      // the copies of row r % kR (kDup > 1): common maximum, each copy's
-      // weight, the combined sum (through shared memory: the P buffers are
-      // idle now, every GEMM2 is done)
-      const int cp = r / kR;  // this lane's copy
-      float mrow = mx, wself = 1.f, lsum = lraw;
-      float* ep_m = reinterpret_cast<float*>(sm + C::kOffP);
-      float* ep_l = ep_m + kRows;
-      float* stage = ep_l + kRows;  // [kDup - 1][kR][16]
-      if constexpr (kDup > 1) {
-        ep_m[r] = mx;
-        ep_l[r] = lraw;
-        ptx::named_bar_sync(1, 128);  // group 0's barrier
-        const int qr = r % kR;
-        mrow = -INFINITY;
-#pragma unroll
-        for (int s2 = 0; s2 < kDup; ++s2) mrow = fmaxf(mrow, ep_m[qr + s2 * kR]);
-        lsum = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < kDup; ++s2) {
-          const float ms = ep_m[qr + s2 * kR];
-          const float ws = (ms == -INFINITY) ? 0.f : fast_exp2((ms - mrow) * c2);
-          lsum = fmaf(ws, ep_l[qr + s2 * kR], lsum);
-          if (s2 == cp) wself = ws;
-        }
+      // ---- epilogue: a row's sum over its copies (one scale), then group 0
+      // merges both groups' rows (group 1's state through shared memory, its
+      // O^T from its TMEM columns) and lane d writes element d of every row
+      if (t_last >= 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), t_last & 1, abort_flag, kWaitNs)) ok = false;
+      if (!ok) set_abort(abort_flag, a.status);
+      mx_x[cp * kR + qr] = l_run;  // (every read of the maxima is done: the last tile's barrier)
+      ptx::named_bar_sync(bar_wg, 128);
+      float lrow = 0.f;
+  #pragma unroll
+      for (int s2 = 0; s2 < kDup; ++s2) lrow += mx_x[s2 * kR + qr];
+      if (wg == 1 && cp == 0) {
+        stat_m[qr] = m_run;
+        stat_l[qr] = lrow;
       }
-      const float l = lsum * kPScaleInv;
-      const float f = vd * kPScaleInv * (final_out ? a.scale_o / (l + 1e-30f) : 1.f);
-      const bool writer = live && cp == 0;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kRows; c0 += 16) {
-        uint32_t ra[16], rb[16];
-        MJ_TMEM_LD16(tmem_o + c0, ra);
-        if constexpr (kPair) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) rb[e] = 0u;  // no second group's state (f1 = 0)
-        } else {
-          MJ_TMEM_LD16(o1 + c0, rb);
-        }
-        ptx::tmem_ld_wait();
-        float v[16];
-        // select, not multiply: a group or copy with no key left its O stale
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          v[e] = ((f0 > 0.f ? __uint_as_float(ra[e]) * f0 : 0.f) + (f1 > 0.f ? __uint_as_float(rb[e]) * f1 : 0.f));
-        if constexpr (kDup > 1) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = wself > 0.f ? v[e] * wself : 0.f;
-          if (cp > 0) {
-            float4* st4 = reinterpret_cast<float4*>(stage + ((cp - 1) * kR + r % kR) * 16);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) st4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-          }
-          ptx::named_bar_sync(1, 128);
-          if (cp == 0) {
-#pragma unroll
-            for (int s2 = 1; s2 < kDup; ++s2) {
-              const float4* st4 = reinterpret_cast<const float4*>(stage + ((s2 - 1) * kR + r) * 16);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float4 u = st4[e];
-                v[4 * e] += u.x;
-                v[4 * e + 1] += u.y;
-                v[4 * e + 2] += u.z;
-                v[4 * e + 3] += u.w;
-              }
+      const bool fine = !ptx::named_bar_red_or(kBarAll, 128 * kWG, *abort_flag != 0);
+      if (wg == 0 && fine) {
+        ptx::tc_fence_after();
+        const bool final_out = a.n_splits[b] <= 1;
+        if (cp == 0) {
+          const float m1 = stat_m[qr], l1 = stat_l[qr];
+          const float mx = fmaxf(m_run, m1);
+          const float f0 = (m_run == -INFINITY) ? 0.f : fast_exp2((m_run - mx) * c2);
+          const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - mx) * c2);
+          const float l = (lrow * f0 + l1 * f1) * kPScaleInv;
+          const float f = vd * kPScaleInv * (final_out ? a.scale_o / (l + 1e-30f) : 1.f);
+          // 0 marks a group with no key for the row (its O^T column is stale)
+          fx[qr] = f0 > 0.f ? f0 * f : 0.f;
+          fx[kR + qr] = f1 > 0.f ? f1 * f : 0.f;
+          if (live) {
+            const float m_logit = mx * scale_l;
+            if (final_out) {
+              a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(l);
+            } else {
+              const int64_t pr = part_row(a, b, g, slot, qrow);
+              a.m_part[pr] = m_logit;
+              a.l_part[pr] = l;
             }
           }
-          ptx::named_bar_sync(1, 128);  // the next block reuses the stage
         }
-        if (!writer) continue;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] *= f;
-        if (final_out) {
-          uint32_t pk[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const __nv_bfloat162 v2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-            pk[e] = *reinterpret_cast<const uint32_t*>(&v2);
+        ptx::named_bar_sync(1, 128);  // group 0's barrier: the factors are written
+        const int d = r;              // this lane's element of every row
+        const uint32_t o1 = tmem + C::kWgCols + kRows + lane_off;  // group 1's O^T, same lanes
+        const int live_rows = a.n_q - n0 < kR ? a.n_q - n0 : kR;
+  #pragma unroll 1
+        for (int c0 = 0; c0 < kR; c0 += 16) {
+          uint32_t ra[16], rb[16];
+          MJ_TMEM_LD16(tmem_o + c0, ra);
+          MJ_TMEM_LD16(o1 + c0, rb);
+          ptx::tmem_ld_wait();
+  #pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = c0 + e;
+            if (c >= live_rows) break;
+            const float w0 = fx[c], w1 = fx[kR + c];
+            // select, not multiply: a group with no key left its column stale
+            const float v = (w0 > 0.f ? __uint_as_float(ra[e]) * w0 : 0.f) + (w1 > 0.f ? __uint_as_float(rb[e]) * w1 : 0.f);
+            if (final_out) {
+              a.o[b * a.o_seq + (static_cast<int64_t>(g) * a.n_q + n0 + c) * kHeadDimDev + d] = __float2bfloat16_rn(v);
+            } else {
+              a.o_part[part_row(a, b, g, slot, n0 + c) * kHeadDimDev + d] = v;
+            }
           }
-          uint4* dst = reinterpret_cast<uint4*>(a.o + orow + c0);
-          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        } else {
-          float4* dst = reinterpret_cast<float4*>(a.o_part + orow + c0);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-        }
-      }
-      if (writer) {
-        const float m_logit = mrow * scale_l;
-        if (final_out) {
-          a.lse[(static_cast<int64_t>(b) * a.h_k + g) * a.n_q + qrow] = m_logit + logf(l);
-        } else {
-          const int64_t pr = part_row(a, b, g, slot, qrow);
-          a.m_part[pr] = m_logit;
-          a.l_part[pr] = l;
         }
       }
     }
