@@ -77,7 +77,7 @@ def test_traffic_record_follows_the_source(tmp_path, monkeypatch):
     assert bench.traffic_record("unknown", "wl") is None
 
 
-@pytest.mark.parametrize("name", ["tc_r8_bf16", "tcg_g2r32_bf16", "qm_r32_bf16", "qm_r64_bf16", "tc_r16_e4m3"])
+@pytest.mark.parametrize("name", ["tc_r8_bf16", "qm_pair_bf16", "qm_r32_bf16", "qm_r64_bf16", "tc_r16_e4m3"])
 def test_committed_traffic_records_name_existing_sources(name):
     rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
     for wl, e in rec[name].items():
