@@ -20,6 +20,13 @@
 // (q 2^s = hi + lo) and P into hi + lo (448 p = hi + lo), each part an A
 // operand of its own MMA into the same accumulator.
 //
+// Row copies (17-64 packed rows): each packed row is held 4 (2) times on
+// GEMM1's M, every copy taking a quarter (half) of a tile's keys; the
+// copies share the row's reference maximum and write one P row between
+// them, and GEMM2 runs as O^T[d, row] += V^T[d, key] P^T[key, row] with the
+// packed rows on N (A = V tile MN-major, B = P rows K-major), a quarter
+// (half) of the MMA work of a 128-row O.
+//
 // Roles (384 threads): warps 0 and 11 issue the K and V TMA tiles into two
 // rings (a K stage is freed by its GEMM1, a V stage by its GEMM2); warp 1
 // (TMEM allocator) issues GEMM1 and warp 10 GEMM2 (one thread issues a
