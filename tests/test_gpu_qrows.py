@@ -149,7 +149,8 @@ def test_determinism_and_graph_replay():
 
 
 # ---- rows held two or four times (64 or 32 packed rows per q tile): every
-# copy takes a share of each tile's keys, the copies are combined at the end
+# copy takes a share of each tile's keys, the copies of a row share its
+# reference maximum and GEMM2 runs transposed on the packed rows
 
 
 @pytest.mark.parametrize("q_len,h_r,causal", [(3, 8, True), (1, 24, False), (4, 16, True), (2, 5, False)])
@@ -198,3 +199,22 @@ def test_softmax_stress_wide_logit_spread(h_r, q_len):
     w = syn.config(5, h_r=h_r, q_len=q_len, num_seqs=3, len_range=(0, 9000))
     w.q = syn.bf16_encode(syn.bf16_bits_to_float(w.q) * 6.0)
     check(w)
+
+
+@pytest.mark.parametrize("h_r,q_len", [(32, 1), (16, 4)], ids=["rows32_x4", "rows64_x2"])
+def test_row_copies_late_maximum_in_one_slice(h_r, q_len):
+    """The keys of one copy's slice (the last 32 / 64 keys of a tile) grow
+    from tile 3 on, so the row maximum moves late and from a single copy: the
+    shared maximum must rescale the O^T column that every copy has added to."""
+    w = syn.config(5, h_r=h_r, q_len=q_len, num_seqs=3, len_range=(1500, 4000))
+    kr = 128 // (128 // (h_r * q_len))  # keys per copy slice
+    for b in range(w.num_seqs):
+        L = int(w.seq_lens[b])
+        for key in range(3 * 128, L):
+            if key % 128 < 128 - kr:
+                continue
+            pg, off = w.block_table[b, key // w.page_size], key % w.page_size
+            v = syn.e4m3_decode(w.k_cache[pg, off]) * 4.0
+            w.k_cache[pg, off] = syn.e4m3_encode(v)
+    check(w)
+
