@@ -24,8 +24,8 @@
 //
 // The kernel is launched as a programmatic dependent of the decode kernel:
 // its CTAs can be resident before the decode grid ends and read the split
-// counts (host inputs) meanwhile, and wait for the decode grid only before
-// reading the partials.
+// counts (the plan's, which the decode grid does not write) meanwhile; each
+// waits for the decode grid before reading the partials or exiting.
 
 #include <cuda_runtime.h>
 
@@ -43,21 +43,24 @@ constexpr int kStatusInvalidArg = 1;  // MJ_ERR_INVALID_ARG
 template <int kWPR, int kPer>
 __global__ void __launch_bounds__((kWPR > kCtaWarps ? kWPR : kCtaWarps) * 32) merge_kernel(const DecodeDev a) {
   constexpr int kRowsPerCta = kWPR >= kCtaWarps ? 1 : kCtaWarps / kWPR;
-  // a programmatic dependent of the decode grid: every CTA waits for that
-  // grid's completion (its partials complete and visible) before touching
-  // global memory, and the unpack after it may launch now
-  ptx::griddep_wait();
-  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int wic = threadIdx.x >> 5;         // warp in the CTA
   const int w = wic % kWPR;                 // warp within the row
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + wic / kWPR;  // (b, g, n), n fastest
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.h_k * a.n_q;
-  if (row >= rows) return;  // uniform over a row's warps (kWPR > 1: one row per CTA)
   const int n = static_cast<int>(row % a.n_q);
   const int g = static_cast<int>((row / a.n_q) % a.h_k);
   const int b = static_cast<int>(row / (static_cast<int64_t>(a.n_q) * a.h_k));
-  const int nsp = a.n_splits[b];
+  // The split count comes from the plan, which the decode grid does not
+  // write and which was complete before any decode CTA passed its own wait
+  // (this grid launches only after all of them have): it is read while the
+  // decode grid drains.  Every CTA then waits for the decode grid's
+  // completion (its partials complete and visible) before any other global
+  // access or its exit, and the unpack after it may launch.
+  const int nsp = row < rows ? a.n_splits[b] : 0;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  if (row >= rows) return;  // uniform over a row's warps (kWPR > 1: one row per CTA)
   if (nsp <= 1) return;  // unsplit: decode wrote O; uniform over the row's warps
   if (nsp > kWPR * kPer || nsp > a.max_splits) {
     // more splits than this launch was sized for (a max_n_splits hint below
