@@ -11,8 +11,14 @@ paged_fp8_kv_gb300/synthetic.py) and already resident in HBM.
 
 `value` is algorithmic bytes per step (KV rows < L, Q, O, LSE, block table,
 work list, descales, split partials written and read) / device time, in
-GB/s, summed over ranks.  L2 is flushed (a 512 MiB write) before every timed
-step, outside the step's CUDA events.
+GB/s, summed over ranks.  Every timed step finds its inputs cold: the loop
+turns through enough device copies of the workload's inputs that at least
+twice the L2 of other inputs is read between two uses of one copy (a GPU
+sleep between steps, outside the step's events, keeps the host ahead);
+workloads too small for that (over 16 copies) flush L2 with a 512 MiB write
+before every step instead.  The page's own harness flushes with that write
+before every call; the headline's `l2_write_flush` record times the step
+that way too (the decode then also writes back the flush's dirty lines).
 
 `--impl reference` times the fp64 CPU oracle, the only reference this
 method has, on a bounded sample of the same workload.
@@ -66,6 +72,12 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time steps as plain launches, not CUDA-graph replays")
+    ap.add_argument(
+        "--l2",
+        default="rotate",
+        choices=["rotate", "flush"],
+        help="cold KV at every timed step: rotate device copies of the inputs (no flush), or flush L2 with a 512 MiB write",
+    )
     ap.add_argument("--q_quant", action="store_true", help="also time the fused fp8 Q quantisation + pack for this shape")
     ap.add_argument("--suite", type=int, default=-1, help="1: also time every workload of the five configs (default: on when no workload flag is given)")
     ap.add_argument("--suite_steps", type=int, default=60, help="timed steps per suite workload")
@@ -266,31 +278,70 @@ def whole_job_gbs(world: int, step_bytes: int, step_ms: float) -> float:
     return world * step_bytes / (step_ms * 1e-3) / 1e9
 
 
-def time_steps(s, dev, flush, steps: int, warmup: int, eager: bool = False, world: int = 1):
-    """Times `steps` decode steps of session s (L2 flushed before each, outside
-    the step's events): the step time as a CUDA-graph replay (pack, decode,
-    merge, unpack), decode and merge times from eager steps with events
-    between the kernels.  Returns (step_ms, decode_ms, merge_ms)."""
+COLD_MAX_COPIES = 16
+SPACER_CYCLES = 150_000  # GPU sleep between rotated steps (about 75 us)
+
+
+def cold_copies(d_bytes: int, dev) -> int:
+    """Device copies of a workload's inputs the timed loop turns through so
+    that every step finds its KV cold: at least twice the L2 of other inputs
+    is read between two uses of one copy.  1: too small to rotate (more than
+    COLD_MAX_COPIES copies), the loop flushes L2 instead."""
     import torch
 
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
+    k = 1 + -(-2 * l2 // max(int(d_bytes), 1))
+    return k if k <= COLD_MAX_COPIES else 1
+
+
+def l2_note(copies: int, d_bytes: int) -> str:
+    if copies > 1:
+        return (
+            f"KV cold: {copies} device copies of the inputs used in turn ({(copies - 1) * d_bytes / 1e6:.0f} MB "
+            "read between two uses of one, >= 2x L2), no flush in the loop; a GPU sleep between steps "
+            "(outside the step events) keeps the host ahead"
+        )
+    return "flushed before every step (512 MiB write outside the step events)"
+
+
+def time_steps(sessions, dev, flush, steps: int, warmup: int, eager: bool = False, world: int = 1):
+    """Times `steps` decode steps, turning through `sessions` (device copies
+    of one workload's inputs: cold KV at every step, a GPU sleep before each);
+    with one session L2 is flushed (a 512 MiB write) before each step instead,
+    outside the step's events.  The step time comes from CUDA-graph replays
+    (pack, decode, merge, unpack), decode and merge times from eager steps
+    with events between the kernels.  Returns (step_ms, decode_ms, merge_ms)."""
+    import torch
+
+    k = len(sessions)
+
+    def gap(i):
+        if k > 1:
+            torch.cuda._sleep(SPACER_CYCLES)
+        else:
+            flush.fill_(i & 0xFF)  # L2 flush, outside the step's events
+
     stream = torch.cuda.current_stream(dev)
-    for _ in range(warmup):
-        flush.fill_(1)
-        s.step()
+    for j in range(warmup * k):
+        gap(j)
+        sessions[j % k].step()
     torch.cuda.synchronize()
     # A step is timed as one replay of a CUDA graph holding (pack, decode,
     # merge, unpack); the library makes no host sync, so it captures as is.
-    graph = None
+    graphs = None
     if not eager:
-        cs = torch.cuda.Stream(dev)
-        cs.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cs):
-            s.step(stream=cs)
+        graphs = []
+        for s in sessions:
+            cs = torch.cuda.Stream(dev)
+            cs.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cs):
+                s.step(stream=cs)
+            graphs.append(g)
         torch.cuda.synchronize()
-        for _ in range(warmup):
-            flush.fill_(1)
-            graph.replay()
+        for j in range(warmup * k):
+            gap(j)
+            graphs[j % k].replay()
         torch.cuda.synchronize()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
@@ -306,14 +357,14 @@ def time_steps(s, dev, flush, steps: int, warmup: int, eager: bool = False, worl
     # steps, which run exactly as a caller's would (graph replays, the merge
     # a programmatic dependent of the decode grid).
     for i in range(steps):
-        flush.fill_(i & 0xFF)  # L2 flush, outside the step's events
+        gap(i)
         sev[i][0].record()
         if i % 2 == 0 or steps == 1:
-            s.step(timing_events=evs[i])
-        elif graph is not None:
-            graph.replay()
+            sessions[i % k].step(timing_events=evs[i])
+        elif graphs is not None:
+            graphs[i % k].replay()
         else:
-            s.step()
+            sessions[i % k].step()
         sev[i][1].record()
     torch.cuda.synchronize()
     if world > 1:
@@ -352,11 +403,34 @@ def run_mj(args, rank, world, local_rank):
         decode_plan(s.params, w.seq_lens, sm_count=s.sm_count, ctas_per_sm=s.ctas_per_sm)
     plan_us = (time.perf_counter() - t) / 20 * 1e6
 
+    # device copies of the inputs the timed loop turns through (cold KV at
+    # every step without an L2 flush); 1: the loop flushes L2 instead
+    copies = cold_copies(d_bytes, dev) if args.l2 == "rotate" else 1
+    sessions = [s] + [
+        DecodeSession(w, device=str(dev), kv_layout=args.kv_layout, kernel=args.kernel, l2_prefetch=args.l2_prefetch,
+            kv_evict_first=args.kv_evict_first, ctas_per_sm=args.ctas_per_sm,
+        )
+        for _ in range(copies - 1)
+    ]
     clk_before = clocks_now(local_rank)
     with ClockSampler(local_rank) as clk:
-        step_ms, t_dec, merge_ms = time_steps(s, dev, flush, args.steps, args.warmup, args.eager, world)
+        step_ms, t_dec, merge_ms = time_steps(sessions, dev, flush, args.steps, args.warmup, args.eager, world)
+        # the page's harness: a 512 MiB write before every step
+        fl_steps = min(args.steps, 200)
+        f_step, f_dec, f_mer = time_steps([s], dev, flush, fl_steps, args.warmup, args.eager, world)
     clk_after = clocks_now(local_rank)
     step_ms = max_over_ranks(step_ms, world, dev)
+    f_step = max_over_ranks(f_step, world, dev)
+    del sessions[1:]
+    torch.cuda.empty_cache()
+    write_flush = {
+        "us_per_step": round(f_step * 1e3, 2),
+        "decode_us": round(f_dec * 1e3, 2),
+        "merge_us": round(f_mer * 1e3, 2),
+        "steps": fl_steps,
+        "note": "L2 flushed by a 512 MiB write before every step (the page's harness); the decode also "
+        "writes back the flush's dirty lines",
+    }
 
     launches = s.launches_per_step() * args.steps
     q_quant = q_quant_measure(w, dev, flush) if (w.q_is_e4m3 or args.q_quant) and rank == 0 else None
@@ -376,6 +450,8 @@ def run_mj(args, rank, world, local_rank):
         step_ms=step_ms,
         decode_ms=t_dec,
         merge_ms=merge_ms,
+        copies=copies,
+        write_flush=write_flush,
         d_bytes=d_bytes,
         m_bytes=m_bytes,
         step_bytes=step_bytes,
@@ -421,8 +497,10 @@ SUITE = (
 
 def run_suite(args, dev, flush, reuse=None):
     """Every workload of the five configurations at full size, each timed like
-    the headline (graph-replayed steps with L2 flushed before each, decode and
-    merge from event-split steps), with the automatic kernel and plan."""
+    the headline (graph-replayed steps, cold KV at every step by rotated
+    input copies or an L2 flush, decode and merge from event-split steps),
+    with the automatic kernel and plan; each also timed with the page's
+    512 MiB write flush before every step."""
     import torch
 
     from paged_fp8_kv_gb300 import synthetic as syn
@@ -436,23 +514,32 @@ def run_suite(args, dev, flush, reuse=None):
         w = (reuse or {}).get(key) or syn.config(cfg, **opts)
         s = DecodeSession(w, device=str(dev))
         d_bytes, _, step_bytes = algorithmic_bytes(w, s.plan)
-        step_ms, dec_ms, mer_ms = time_steps(s, dev, flush, args.suite_steps, 5)
+        copies = cold_copies(d_bytes, dev) if args.l2 == "rotate" else 1
+        sessions = [s] + [DecodeSession(w, device=str(dev)) for _ in range(copies - 1)]
+        step_ms, dec_ms, mer_ms = time_steps(sessions, dev, flush, args.suite_steps, 5)
+        f_step, f_dec, _ = time_steps([s], dev, flush, args.suite_steps, 5)
         rec = {
             "workload": w.name,
             "kernel": s.kernel,
             "n_q": w.n_q,
             "plan": {"work_items": s.plan.num_work, "max_n_splits": s.plan.max_n_splits, "ctas_per_sm": s.plan.opts.ctas_per_sm},
+            "l2": f"rotate x{copies}" if copies > 1 else "flush",
             "us_per_step": round(step_ms * 1e3, 2),
             "decode_us": round(dec_ms * 1e3, 2),
             "merge_us": round(mer_ms * 1e3, 2) if s.plan.max_n_splits > 1 else 0.0,
             "step_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
             "frac": round(d_bytes / (dec_ms * 1e-3) / 1e9 / peak, 4),
             "frac_of_8000_gbs": round(d_bytes / (dec_ms * 1e-3) / 1e9 / 8000.0, 4),
+            "write_flush": {
+                "us_per_step": round(f_step * 1e3, 2),
+                "decode_us": round(f_dec * 1e3, 2),
+                "frac": round(d_bytes / (f_dec * 1e-3) / 1e9 / peak, 4),
+            },
         }
         if w.n_q >= 128:
             rec["tensor_frac"] = round(algorithmic_flops(w) / (dec_ms * 1e-3) / 1e12 / tpk, 4)
         out.append(rec)
-        del s
+        del s, sessions
         torch.cuda.empty_cache()
     return out
 
@@ -752,7 +839,7 @@ def main():
                     "ctas_per_sm": s.plan.opts.ctas_per_sm,
                     "sm_count": s.plan.opts.sm_count,
                 },
-                "l2": "flushed before every step (512 MiB write outside the step events); KV also exceeds L2",
+                "l2": l2_note(r["copies"], r["d_bytes"]),
                 "step_timing": "eager launches" if args.eager else "CUDA-graph replay of the step (pack, decode, merge, unpack)",
                 "parallelism": f"replicas x{world}",
                 "bytes_per_step": r["step_bytes"],
@@ -771,6 +858,10 @@ def main():
                 "algorithmic_bytes_per_launch": r["d_bytes"],
                 "decode_us": round(r["decode_ms"] * 1e3, 2),
                 "merge_us": round(r["merge_ms"] * 1e3, 2),
+            },
+            "l2_write_flush": {
+                **r["write_flush"],
+                "frac": round(r["d_bytes"] / (r["write_flush"]["decode_us"] * 1e-6) / 1e9 / peak, 4),
             },
             "cpu_baseline": cpu,
             "e2e": r["e2e"],
