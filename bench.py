@@ -282,15 +282,19 @@ COLD_MAX_COPIES = 16
 SPACER_CYCLES = 150_000  # GPU sleep between rotated steps (about 75 us)
 
 
-def cold_copies(d_bytes: int, dev) -> int:
-    """Device copies of a workload's inputs the timed loop turns through so
-    that every step finds its KV cold: at least twice the L2 of other inputs
-    is read between two uses of one copy.  1: too small to rotate (more than
-    COLD_MAX_COPIES copies), the loop flushes L2 instead."""
+def l2_bytes(dev) -> int:
     import torch
 
-    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
-    k = 1 + -(-2 * l2 // max(int(d_bytes), 1))
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
+
+
+def cold_copies(d_bytes: int, l2: int) -> int:
+    """Device copies of a workload's inputs the timed loop turns through so
+    that every step finds its KV cold: at least twice the L2 (l2 bytes) of
+    other inputs is read between two uses of one copy of d_bytes.  1: too
+    small to rotate (more than COLD_MAX_COPIES copies), the loop flushes L2
+    instead."""
+    k = 1 + -(-2 * int(l2) // max(int(d_bytes), 1))
     return k if k <= COLD_MAX_COPIES else 1
 
 
@@ -405,7 +409,7 @@ def run_mj(args, rank, world, local_rank):
 
     # device copies of the inputs the timed loop turns through (cold KV at
     # every step without an L2 flush); 1: the loop flushes L2 instead
-    copies = cold_copies(d_bytes, dev) if args.l2 == "rotate" else 1
+    copies = cold_copies(d_bytes, l2_bytes(dev)) if args.l2 == "rotate" else 1
     sessions = [s] + [
         DecodeSession(w, device=str(dev), kv_layout=args.kv_layout, kernel=args.kernel, l2_prefetch=args.l2_prefetch,
             kv_evict_first=args.kv_evict_first, ctas_per_sm=args.ctas_per_sm,
@@ -514,7 +518,7 @@ def run_suite(args, dev, flush, reuse=None):
         w = (reuse or {}).get(key) or syn.config(cfg, **opts)
         s = DecodeSession(w, device=str(dev))
         d_bytes, _, step_bytes = algorithmic_bytes(w, s.plan)
-        copies = cold_copies(d_bytes, dev) if args.l2 == "rotate" else 1
+        copies = cold_copies(d_bytes, l2_bytes(dev)) if args.l2 == "rotate" else 1
         sessions = [s] + [DecodeSession(w, device=str(dev)) for _ in range(copies - 1)]
         step_ms, dec_ms, mer_ms = time_steps(sessions, dev, flush, args.suite_steps, 5)
         f_step, f_dec, _ = time_steps([s], dev, flush, args.suite_steps, 5)

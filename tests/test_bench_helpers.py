@@ -84,3 +84,18 @@ def test_committed_traffic_records_name_existing_sources(name):
         assert os.path.exists(os.path.join(bench.ROOT, "paged_fp8_kv_gb300", "csrc", e["source"]))
         assert e["dram_bytes_per_launch"] > 0 and len(e["source_sha"]) == 16
         assert "ncu" in e["command"] and "--clock-control none" in e["command"]
+
+
+def test_cold_copies_put_twice_l2_between_reuses():
+    """The timed loop's rotation: at least 2 x L2 of other inputs between two
+    uses of one copy, else (over 16 copies) an L2 flush."""
+    import bench
+
+    l2 = 126 << 20
+    for d in (1_343_200_000, 620_000_000, 260_000_000, 44_000_000, 35_000_000, 18_000_000):
+        k = bench.cold_copies(d, l2)
+        assert 2 <= k <= bench.COLD_MAX_COPIES
+        assert (k - 1) * d >= 2 * l2
+        assert (k - 2) * d < 2 * l2  # the fewest copies that do it
+    assert bench.cold_copies(35_000, l2) == 1  # the tiny workload flushes
+    assert bench.cold_copies(2 * l2 // 16, l2) == 1
