@@ -241,6 +241,20 @@ def clocks_now(index: int):
         return None
 
 
+def traffic_applies(args) -> bool:
+    """The committed traffic figures were taken on the full workloads with
+    the default pool layout, plan and load options; a run that changes any
+    of them reports none."""
+    return (
+        args.num_seqs is None
+        and args.max_splits is None
+        and args.kv_layout == "nhd"
+        and args.l2_prefetch == 0
+        and args.kv_evict_first == 0
+        and args.ctas_per_sm == 0
+    )
+
+
 def traffic_record(kernel: str, workload_name: str):
     """dram bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source (else None)."""
@@ -858,7 +872,7 @@ def main():
                 "peak_source": peak_src,
                 "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": traffic_record(s.kernel, w.name),
+                "traffic": traffic_record(s.kernel, w.name) if traffic_applies(args) else None,
                 "algorithmic_bytes_per_launch": r["d_bytes"],
                 "decode_us": round(r["decode_ms"] * 1e3, 2),
                 "merge_us": round(r["merge_ms"] * 1e3, 2),

@@ -99,3 +99,22 @@ def test_cold_copies_put_twice_l2_between_reuses():
         assert (k - 2) * d < 2 * l2  # the fewest copies that do it
     assert bench.cold_copies(35_000, l2) == 1  # the tiny workload flushes
     assert bench.cold_copies(2 * l2 // 16, l2) == 1
+
+
+def test_traffic_only_for_the_captured_configuration():
+    """Shrunk batches or changed load options must not borrow the full
+    workload's ncu traffic figure."""
+    import bench
+
+    sys_argv = ["bench.py"]
+    import sys as _sys
+
+    old = _sys.argv
+    try:
+        _sys.argv = sys_argv
+        assert bench.traffic_applies(bench.parse())
+        for extra in (["--num_seqs", "32"], ["--kv_layout", "hnd"], ["--ctas_per_sm", "2"], ["--max_splits", "8"]):
+            _sys.argv = sys_argv + extra
+            assert not bench.traffic_applies(bench.parse())
+    finally:
+        _sys.argv = old
