@@ -43,7 +43,11 @@ class DecodeSession:
         l2_prefetch: int = 0,
         kv_evict_first: int = 0,
         ctas_per_sm: int = 0,
+        share_pool_with: Optional["DecodeSession"] = None,
     ):
+        """``share_pool_with``: another session of the same workload whose
+        device KV pool (pages, scale planes, descales) this one reads instead
+        of holding its own copy."""
         self.w = w
         self.ctas_per_sm = int(ctas_per_sm)
         self.device = torch.device(device)
@@ -80,7 +84,12 @@ class DecodeSession:
         # d * bits / 8 for the packed narrow formats).
         k = torch.from_numpy(w.k_cache)
         v = torch.from_numpy(w.v_cache)
-        if kv_layout == "nhd":
+        if share_pool_with is not None:
+            o = share_pool_with
+            self.k_cache, self.v_cache = o.k_cache, o.v_cache
+            if hasattr(o, "_kv_buf"):
+                self._kv_buf = o._kv_buf
+        elif kv_layout == "nhd":
             self.k_cache = k.to(dev)
             self.v_cache = v.to(dev)
         elif kv_layout == "hnd":  # (pages, 2, h_k, PS, d)
@@ -105,8 +114,11 @@ class DecodeSession:
 
         # nvfp4: the scale planes, (num_pages, h_k, PS, d / 16) e4m3 codes
         ks, vs = getattr(w, "k_scales", None), getattr(w, "v_scales", None)
-        self.k_scales = torch.from_numpy(ks).to(dev) if ks is not None else None
-        self.v_scales = torch.from_numpy(vs).to(dev) if vs is not None else None
+        if share_pool_with is not None:
+            self.k_scales, self.v_scales = share_pool_with.k_scales, share_pool_with.v_scales
+        else:
+            self.k_scales = torch.from_numpy(ks).to(dev) if ks is not None else None
+            self.v_scales = torch.from_numpy(vs).to(dev) if vs is not None else None
         self.block_table = torch.from_numpy(w.block_table).to(dev)
         self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
         self.q_descale = torch.from_numpy(np.ascontiguousarray(w.q_descale)).to(dev)
@@ -260,13 +272,24 @@ class DecodeSession:
         the plan's item count or largest split count changes), one
         device-to-host copy of O and LSE.  Returns the pinned output views
         (valid once the stream is synchronised)."""
+        self._stage_plan(plan)
+        self._in_dev.copy_(self._in_host, non_blocking=True)
+        self._graph_for(plan).replay()
+        self._out_host.copy_(self._out_dev, non_blocking=True)
+        return self._host_out
+
+    def _stage_plan(self, plan) -> None:
         n = plan.num_work
         self._host_in["work"].numpy()[:n] = plan.work
         self._host_in["n_splits"].numpy()[:] = plan.n_splits
         self.plan = plan
         self.work = self._work_dev[:n]
-        self._in_dev.copy_(self._in_host, non_blocking=True)
-        key = (n, plan.max_n_splits)
+
+    def _graph_for(self, plan):
+        """The step's CUDA graph for this plan shape (captured on a side
+        stream after the current stream's work, the first time a shape is
+        seen)."""
+        key = (plan.num_work, plan.max_n_splits)
         if self._graph is None or self._graph_key != key:
             stream = torch.cuda.current_stream(self.device)
             side = torch.cuda.Stream(self.device)
@@ -276,10 +299,76 @@ class DecodeSession:
                 self.step(stream=side)
             stream.wait_stream(side)
             self._graph, self._graph_key = g, key
-        self._graph.replay()
-        self._out_host.copy_(self._out_dev, non_blocking=True)
-        return self._host_out
+        return self._graph
 
     def staged_bytes(self):
         """(host-to-device, device-to-host) bytes a staged step copies."""
         return int(self._in_host.numel()), int(self._out_host.numel())
+
+
+class StagedPipeline:
+    """Serving steps from host memory with the copies off the critical path:
+    ``depth`` staged sessions over ONE device KV pool take the steps in turn.
+    Step i (slot i % depth) queues its input copy on an input-copy stream, its
+    graph replay on a compute stream once that copy is in, and the copy of its
+    O and LSE back on an output-copy stream once the replay is done (two copy
+    streams: the next step's input copy does not queue behind this step's
+    output copy, which waits for the replay); the host then
+    returns at once, plans step i + 1 and queues it, so that the copies and
+    the host's work of one step overlap the device work of its neighbours.
+
+    inputs(i) returns slot i's pinned host inputs (q, seq_lens, block_table),
+    free to fill once step i - depth's input copy has completed; submit(i,
+    plan) queues the step; outputs(i) waits for step i's output copy and
+    returns its pinned O / LSE views, valid until submit(i + depth)."""
+
+    def __init__(self, w, depth: int = 2, device: str = "cuda", **session_kw):
+        if depth < 1:
+            raise ValueError("depth >= 1")
+        first = DecodeSession(w, device=device, **session_kw)
+        self.slots = [first] + [DecodeSession(w, device=device, share_pool_with=first, **session_kw) for _ in range(depth - 1)]
+        self.host_in = [s.stage() for s in self.slots]
+        self.device = first.device
+        self.depth = depth
+        self.h2d_stream = torch.cuda.Stream(self.device)
+        self.d2h_stream = torch.cuda.Stream(self.device)
+        self.compute_stream = torch.cuda.Stream(self.device)
+        mk = lambda: [torch.cuda.Event() for _ in range(depth)]
+        self.ev_in, self.ev_done, self.ev_out = mk(), mk(), mk()
+        self.used = [False] * depth
+
+    def inputs(self, i: int) -> dict:
+        k = i % self.depth
+        if self.used[k]:
+            self.ev_in[k].synchronize()  # step i - depth has read the pinned inputs
+        return self.host_in[k]
+
+    def submit(self, i: int, plan) -> None:
+        k = i % self.depth
+        s = self.slots[k]
+        if self.used[k]:
+            self.ev_out[k].synchronize()  # step i - depth's outputs are out (and read by now)
+        s._stage_plan(plan)
+        g = s._graph_for(plan)
+        with torch.cuda.stream(self.h2d_stream):
+            if self.used[k]:
+                self.h2d_stream.wait_event(self.ev_done[k])  # its replay has read the device inputs
+            s._in_dev.copy_(s._in_host, non_blocking=True)
+            self.ev_in[k].record(self.h2d_stream)
+        with torch.cuda.stream(self.compute_stream):
+            self.compute_stream.wait_event(self.ev_in[k])
+            g.replay()
+            self.ev_done[k].record(self.compute_stream)
+        with torch.cuda.stream(self.d2h_stream):
+            self.d2h_stream.wait_event(self.ev_done[k])
+            s._out_host.copy_(s._out_dev, non_blocking=True)
+            self.ev_out[k].record(self.d2h_stream)
+        self.used[k] = True
+
+    def outputs(self, i: int) -> dict:
+        k = i % self.depth
+        self.ev_out[k].synchronize()
+        return self.slots[k]._host_out
+
+    def bytes_per_step(self):
+        return self.slots[0].staged_bytes()

@@ -362,3 +362,47 @@ def test_staged_serving_step_matches_the_step(cfg, kw):
         else:
             packed = torch.from_numpy(pack_q_ref(o.float().numpy(), w.num_seqs, w.q_len, w.h_k, w.h_r))
             compare(w, packed.numpy(), lse.numpy())
+
+
+@pytest.mark.parametrize("cfg,kw", [(4, dict(num_seqs=3, len_range=(500, 1500))), (3, dict(num_seqs=3, len_range=(3000, 300)))],
+                         ids=["spec_verify_qlen4", "skewed_fp8_split"])
+def test_pipelined_serving_steps_match_the_synchronous_step(cfg, kw):
+    # two slots over one KV pool, steps queued back to back with a different
+    # Q each: every step's O and LSE equal the synchronous staged step's on
+    # the same inputs (same kernels, same plan: the same bytes), and step 0
+    # matches the oracle
+    import paged_fp8_kv_gb300 as mj
+    from paged_fp8_kv_gb300.session import StagedPipeline
+
+    w = syn.config(cfg, **kw)
+    pipe = StagedPipeline(w, depth=2)
+    assert pipe.slots[1].k_cache.data_ptr() == pipe.slots[0].k_cache.data_ptr()  # one pool
+    e = DecodeSession(w)
+    e.stage()
+    p0 = pipe.slots[0]
+    base = torch.from_numpy(w.q.view(np.int16) if w.q.dtype == np.uint16 else w.q)
+
+    def q_of(i):
+        if base.dtype == torch.int16:  # bf16 bits: a different Q per step
+            return (base.view(torch.bfloat16).float() * (1.0 + 0.25 * i)).to(torch.bfloat16).view(torch.int16)
+        return torch.roll(base, shifts=i, dims=0)  # e4m3 codes: rows rotated
+
+    steps, got = 5, {}
+    for i in range(steps):
+        plan = mj.decode_plan(p0.params, w.seq_lens, sm_count=p0.sm_count, force_splits=3 if i == 3 else 0)
+        pipe.inputs(i)["q"].copy_(q_of(i))
+        pipe.submit(i, plan)
+        if i >= 1:
+            out = pipe.outputs(i - 1)
+            got[i - 1] = (out["o"].clone(), out["lse"].clone())
+    out = pipe.outputs(steps - 1)
+    got[steps - 1] = (out["o"].clone(), out["lse"].clone())
+    for i in range(steps):
+        plan = mj.decode_plan(e.params, w.seq_lens, sm_count=e.sm_count, force_splits=3 if i == 3 else 0)
+        e._host_in["q"].copy_(q_of(i))
+        ref = e.staged_step(plan)
+        torch.cuda.synchronize()
+        assert torch.equal(got[i][0].view(torch.int16), ref["o"].view(torch.int16)), f"step {i}"
+        assert torch.equal(got[i][1], ref["lse"]), f"step {i}"
+    o0 = got[0][0].float().numpy()
+    compare(w, pack_q_ref(o0, w.num_seqs, w.q_len, w.h_k, w.h_r), got[0][1].view(w.num_seqs, w.h_k, w.n_q).numpy())
