@@ -67,7 +67,7 @@ constexpr int kMma2Warp = 2 + 4 * kWG;       // 10
 constexpr int kVLoadWarp = kMma2Warp + 1;    // 11
 constexpr int kBarAll = 3;                   // named barrier of both warpgroups
 
-template <bool kQe4m3, bool kPair = false>
+template <bool kQe4m3, bool kPair = false, int kDup = 1>
 struct QmCfg {
   // K ring: measured the bound at three stages (a stage comes back one TMA
   // round trip after its GEMM1, and the period was that over three); the
@@ -75,7 +75,11 @@ struct QmCfg {
   // e4m3 Q, which has no lo part)
   // Paired q tiles hold two Q tiles: three K and three V stages beside a
   // bf16 pair's 64 KB of Q parts (a stage then serves twice the work).
-  static constexpr int kStagesK = kPair ? (kQe4m3 ? 4 : 3) : (kQe4m3 ? 5 : 4);
+  // Row copies keep two P buffers per group; with 64 rows (two copies) those
+  // fill the group's P region, so the copies' maxima and factors get a small
+  // region of their own and the K ring one stage fewer (a build with one K
+  // and one V stage fewer measured within 2 % on every workload).
+  static constexpr int kStagesK = kPair ? (kQe4m3 ? 4 : 3) : (kQe4m3 ? 5 : 4) - (kDup == 2 ? 1 : 0);
   static constexpr int kStagesV = kPair ? (kQe4m3 ? 4 : 3) : 4;
   static constexpr int kQParts = kQe4m3 ? 1 : 2;
   static constexpr int kQTiles = kPair ? 2 : 1;
@@ -85,9 +89,11 @@ struct QmCfg {
   static constexpr int kOffV = kStagesK * kTileBytes;
   static constexpr int kOffQ = (kStagesK + kStagesV) * kTileBytes;  // [q tile][hi | lo] 128 x 128 B each
   static constexpr int kOffP = kOffQ + kQTiles * kQParts * kPartBytes;  // [wg][hi | lo]
-  static constexpr int kOffStat = kOffP + kWG * 2 * kPartBytes;     // group 1: [128] max, [128] sum
+  static constexpr int kOffX = kOffP + kWG * 2 * kPartBytes;         // 64 rows: [wg] copies' maxima, factors
+  static constexpr int kXBytes = kDup == 2 ? kWG * 1024 : 0;
+  static constexpr int kOffStat = kOffX + kXBytes;                   // group 1: [128] max, [128] sum
   static constexpr int kOffBar = kOffStat + 2 * kRows * 4;
-  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 4 * kWG + 2;
+  static constexpr int kNumBars = 2 * (kStagesK + kStagesV) + 6 * kWG + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 64 + 1024;
   static_assert(kBytes <= 232448, "shared memory");
@@ -122,7 +128,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   // dependent) may launch now; its CTAs wait the same way.
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
-  using C = QmCfg<kQe4m3, kPair>;
+  using C = QmCfg<kQe4m3, kPair, kDup>;
   constexpr int SK = C::kStagesK, SV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -142,9 +148,20 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
   auto vfull = [&](int s) { return bar0 + 8u * (2 * SK + s); };
   auto vempty = [&](int s) { return bar0 + 8u * (2 * SK + SV + s); };
   constexpr int kB = 2 * (SK + SV);
-  auto wgbar = [&](int wg, int k) { return bar0 + 8u * (kB + 4 * wg + k); };  // 0 S full, 1 S free, 2 P full, 3 P free
-  const uint32_t qready = bar0 + 8u * (kB + 4 * kWG);
+  // per group: 0 S full, 1 S free, 2 P full, 3 GEMM2 done (P free); with two
+  // P buffers (32 rows) 2 / 3 serve even local tiles and 4 / 5 odd ones
+  auto wgbar = [&](int wg, int k) { return bar0 + 8u * (kB + 6 * wg + k); };
+  const uint32_t qready = bar0 + 8u * (kB + 6 * kWG);
   const uint32_t drain = qready + 8u;
+  // row copies (32 / 64 packed rows): two P buffers per group (local tile t
+  // writes buffer t & 1), so the softmax of tile t waits only for the GEMM2
+  // of tile t - 2; each buffer has its own P-full and GEMM2-done barriers,
+  // which then complete once every two tiles (never two phases ahead of a
+  // waiter)
+  constexpr bool kPDbl = kDup > 1;
+  auto pfull_bar = [&](int wg, int t) { return wgbar(wg, (kPDbl && (t & 1)) ? 4 : 2); };
+  auto g2done_bar = [&](int wg, int t) { return wgbar(wg, (kPDbl && (t & 1)) ? 5 : 3); };
+  auto bar_phase = [&](int t) { return static_cast<uint32_t>(kPDbl ? (t >> 1) & 1 : t & 1); };
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -177,6 +194,8 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       ptx::mbar_init(wgbar(wg, 1), 4);
       ptx::mbar_init(wgbar(wg, 2), 4);
       ptx::mbar_init(wgbar(wg, 3), 1);
+      ptx::mbar_init(wgbar(wg, 4), 4);
+      ptx::mbar_init(wgbar(wg, 5), 1);
     }
     ptx::mbar_init(qready, C::kQTiles);  // each q tile's group
     ptx::mbar_init(drain, 2);
@@ -305,14 +324,15 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
           if (last_use) ptx::mma_commit(kempty(st));
         } else {
           const int st = i % SV;
-          if (!ptx::mbar_wait_bounded(wgbar(wg, 2), t & 1, abort_flag, kWaitNs) ||
+          if (!ptx::mbar_wait_bounded(pfull_bar(wg, t), bar_phase(t), abort_flag, kWaitNs) ||
               !ptx::mbar_wait_bounded(vfull(st), (i / SV) & 1, abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           const uint64_t vdesc = vdesc0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-          const uint64_t pdesc = pdesc0 + static_cast<uint64_t>(wg) * 2 * kPartStep;
+          const uint64_t pdesc = pdesc0 + static_cast<uint64_t>(wg) * 2 * kPartStep +
+                                 (kPDbl ? static_cast<uint64_t>(t & 1) * 2 * kPtStep : 0);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {  // one K step = 32 keys
 #pragma unroll
@@ -325,7 +345,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
                               (t > 0 || kk > 0 || part > 0) ? 1u : 0u);
             }
           }
-          ptx::mma_commit(wgbar(wg, 3));
+          ptx::mma_commit(g2done_bar(wg, t));
           if (last_use) ptx::mma_commit(vempty(st));
         }
       }
@@ -672,7 +692,10 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
       const int cp = r / kR;  // this lane's copy
       const int qr = r % kR;  // its packed row in the q tile
       constexpr int kPtPart = kR * 128;  // one e4m3 part of the group's P rows
-      float* const mx_x = reinterpret_cast<float*>(pbuf + 2 * kPtPart);  // [kDup][kR] tile maxima of the slices
+      // [kDup][kR] tile maxima of the slices, then [2][kR] factors: after the
+      // two P buffers (32 rows), or in their own region (64 rows)
+      float* const mx_x = kDup == 2 ? reinterpret_cast<float*>(sm + C::kOffX + wg * 1024)
+                                    : reinterpret_cast<float*>(pbuf + 4 * kPtPart);
       float* const fx = mx_x + kRows;                                      // [2][kR] per-row factors
       const int bar_red = 4 + wg;  // the group's reduction barrier
       for (int i = wg; i < T; i += kWG) {
@@ -722,8 +745,16 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         m_run = m_new;
         if (cp == 0) fx[qr] = corr;
         const bool any_moved = ptx::named_bar_red_or(bar_red, 128, moved);  // also: fx and mx_x reads done
-        // this group's P rows and O^T are free once GEMM2 of its previous tile ran
-        if (t > 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), (t - 1) & 1, abort_flag, kWaitNs)) ok = false;
+        // this tile's P rows are free once the GEMM2 that last read them ran
+        // (the previous tile's, or with two buffers the one before it); O^T
+        // takes a correction only after the previous tile's GEMM2
+        const int t_free = kPDbl ? t - 2 : t - 1;
+        if (t_free >= 0 && !ptx::mbar_wait_bounded(g2done_bar(wg, t_free), bar_phase(t_free), abort_flag, kWaitNs))
+          ok = false;
+        if (kPDbl && t > 0 && any_moved &&
+            !ptx::mbar_wait_bounded(g2done_bar(wg, t - 1), bar_phase(t - 1), abort_flag, kWaitNs))
+          ok = false;
+        uint8_t* const pb = pbuf + (kPDbl ? (t & 1) * 2 * kPtPart : 0);  // this tile's P rows
         if (t > 0 && any_moved) {  // lazy correction: lane d scales column qr of every row by its factor
           ptx::tc_fence_after();
   #pragma unroll
@@ -772,8 +803,8 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
               lw[wi] = static_cast<uint32_t>(l8[0]) | (static_cast<uint32_t>(l8[1]) << 16);
             }
             l_run += sum2.x + sum2.y;
-            *reinterpret_cast<uint4*>(swz(pbuf, qr, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(swz(pbuf + kPtPart, qr, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            *reinterpret_cast<uint4*>(swz(pb, qr, cc)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(swz(pb + kPtPart, qr, cc)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
         // keys past the sequence end: zero their V rows (0 * poison must not
@@ -790,14 +821,15 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(wgbar(wg, 2));
+        if (lane == 0) ptx::mbar_arrive(pfull_bar(wg, t));
         if (!ok) set_abort(abort_flag, a.status);
       }
 
       // ---- epilogue: a row's sum over its copies (one scale), then group 0
       // merges both groups' rows (group 1's state through shared memory, its
       // O^T from its TMEM columns) and lane d writes element d of every row
-      if (t_last >= 0 && !ptx::mbar_wait_bounded(wgbar(wg, 3), t_last & 1, abort_flag, kWaitNs)) ok = false;
+      if (t_last >= 0 && !ptx::mbar_wait_bounded(g2done_bar(wg, t_last), bar_phase(t_last), abort_flag, kWaitNs))
+        ok = false;
       if (!ok) set_abort(abort_flag, a.status);
       mx_x[cp * kR + qr] = l_run;  // (every read of the maxima is done: the last tile's barrier)
       ptx::named_bar_sync(bar_wg, 128);
@@ -869,7 +901,7 @@ decode_qm_kernel(const DecodeDev a, const __grid_constant__ CUtensorMap tmap_k,
 
 template <bool kQe4m3, int kDup, bool kPair = false>
 cudaError_t launch_qm(const DecodeDev& a, int n_q_tiles, cudaStream_t stream) {
-  using C = QmCfg<kQe4m3, kPair>;
+  using C = QmCfg<kQe4m3, kPair, kDup>;
   const int box_rows = a.page_size < kRows ? a.page_size : kRows;
   CUtensorMap mk, mv;
   if (!make_kv_map(&mk, a.k, a.page_size, a.h_k, a.num_pages, a.k_row, a.k_head, a.k_page, box_rows, 1,
