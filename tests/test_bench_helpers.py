@@ -86,6 +86,26 @@ def test_committed_traffic_records_name_existing_sources(name):
         assert "ncu" in e["command"] and "--clock-control none" in e["command"]
 
 
+def test_committed_traffic_records_point_at_their_kernels_source():
+    """A record is invalidated by its source's hash: it must name the file
+    that holds the kernel it was taken on (the library's kernel names start
+    with the kernel family), and its capture must select that kernel."""
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    family = {"tcg": "decode_tcg.cu", "tc": "decode_tc.cu", "qm": "decode_qm.cu", "cc": "decode_cc.cu"}
+    n = 0
+    for kernel, per_wl in rec.items():
+        if not isinstance(per_wl, dict):
+            continue
+        for wl, e in per_wl.items():
+            if not (isinstance(e, dict) and "source" in e):
+                continue
+            src = family[kernel.split("_")[0]]
+            assert e["source"] == src, (kernel, wl, e["source"])
+            assert "regex:" + src[:-3] in e["command"], (kernel, wl)
+            n += 1
+    assert n >= 10
+
+
 def test_cold_copies_put_twice_l2_between_reuses():
     """The timed loop's rotation: at least 2 x L2 of other inputs between two
     uses of one copy, else (over 16 copies) an L2 flush."""
